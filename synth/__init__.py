@@ -1,0 +1,162 @@
+"""Seeded synthetic inputs for the decode-step library and its oracle.
+
+This package is an input generator only: it draws weights and token ids and
+quantises the weights into the GGUF-style Q8_0 / Q4_0 blocks that both the CUDA
+library and the fp64 oracle consume.  It holds none of the decode step's
+arithmetic (no dequantisation, norm, RoPE, attention or projection), and it
+imports neither the library nor the oracle.
+
+The generator itself is C (``csrc/synth.c``: SplitMix64 counters, Box-Muller
+normals, block quantisers), compiled on first use with the host compiler.
+"""
+from __future__ import annotations
+
+import ctypes
+import hashlib
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from .configs import CONFIGS, ModelConfig, get_config  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "csrc", "synth.c")
+_LIBDIR = os.path.join(_HERE, "_lib")
+_LIB = os.path.join(_LIBDIR, "libsynth.so")
+_lock = threading.Lock()
+_lib = None
+
+Q8_0 = 8
+Q4_0 = 4
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18}
+
+
+def build(force: bool = False) -> str:
+    """Compile the generator into ``_lib/libsynth.so`` (gcc, OpenMP)."""
+    os.makedirs(_LIBDIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+               "-std=c11", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            u64, i64, i32, dbl = ctypes.c_uint64, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
+            vp = ctypes.c_void_p
+            lib.synth_normal.argtypes = [u64, u64, i64, dbl, vp]
+            lib.synth_normal.restype = None
+            lib.synth_tokens.argtypes = [u64, i64, i32, vp]
+            lib.synth_tokens.restype = None
+            lib.synth_quant_matrix.argtypes = [u64, i64, i64, dbl, ctypes.c_int, vp]
+            lib.synth_quant_matrix.restype = ctypes.c_int
+            lib.synth_quantize.argtypes = [vp, i64, ctypes.c_int, vp]
+            lib.synth_quantize.restype = ctypes.c_int
+            lib.synth_f64_to_f16.argtypes = [dbl]
+            lib.synth_f64_to_f16.restype = ctypes.c_uint16
+            lib.synth_f16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.synth_f16_to_f64.restype = dbl
+            _lib = lib
+    return _lib
+
+
+def stream_key(*parts) -> int:
+    """64-bit stream key from a name path, e.g. stream_key("8b", 3, "wq")."""
+    s = "/".join(str(p) for p in parts).encode()
+    return int.from_bytes(hashlib.blake2b(s, digest_size=8).digest(), "little")
+
+
+def normal(key: int, n: int, sigma: float = 1.0, start: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.float64)
+    _load().synth_normal(key, start, n, sigma, out.ctypes.data)
+    return out
+
+
+def tokens(key: int, n: int, vocab: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.int32)
+    _load().synth_tokens(key, n, vocab, out.ctypes.data)
+    return out
+
+
+def quant_matrix(key: int, rows: int, cols: int, sigma: float, wtype: int) -> np.ndarray:
+    """[rows x cols] N(0, sigma) matrix quantised to blocks (uint8, flat)."""
+    nb = (cols + 31) // 32
+    out = np.empty(rows * nb * BLOCK_BYTES[wtype], dtype=np.uint8)
+    rc = _load().synth_quant_matrix(key, rows, cols, sigma, wtype, out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"bad wtype {wtype}")
+    return out
+
+
+def quantize(x: np.ndarray, wtype: int) -> np.ndarray:
+    """Quantise given values (length a multiple of 32) into blocks."""
+    x = np.ascontiguousarray(x, dtype=np.float64).ravel()
+    out = np.empty(x.size // 32 * BLOCK_BYTES[wtype], dtype=np.uint8)
+    if _load().synth_quantize(x.ctypes.data, x.size, wtype, out.ctypes.data) != 0:
+        raise ValueError("length must be a multiple of 32 and wtype 8 or 4")
+    return out
+
+
+def f64_to_f16_bits(v: float) -> int:
+    return int(_load().synth_f64_to_f16(float(v)))
+
+
+# --------------------------------------------------------------------------
+# whole-model weights
+
+
+def matrix_shapes(cfg: ModelConfig) -> dict:
+    """Logical [rows, cols] of each per-layer matrix (cols = input features)."""
+    H, hd = cfg.hidden, cfg.head_dim
+    return {
+        "wq": (cfg.n_heads * hd, H),
+        "wk": (cfg.n_kv_heads * hd, H),
+        "wv": (cfg.n_kv_heads * hd, H),
+        "wo": (H, cfg.n_heads * hd),
+        "w_gate": (cfg.ffn, H),
+        "w_up": (cfg.ffn, H),
+        "w_down": (H, cfg.ffn),
+    }
+
+
+LAYER_MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+def layer_weights(cfg: ModelConfig, layer: int) -> dict:
+    out = {}
+    for name, (rows, cols) in matrix_shapes(cfg).items():
+        out[name] = quant_matrix(stream_key(cfg.name, layer, name), rows, cols, cfg.sigma, cfg.wtype)
+    out["attn_norm"] = np.ones(cfg.hidden, dtype=np.float32)
+    out["ffn_norm"] = np.ones(cfg.hidden, dtype=np.float32)
+    return out
+
+
+def model_weights(cfg: ModelConfig, layers=None) -> dict:
+    """All weights of a config as host arrays (GGUF-style blocks).
+
+    ``layers`` restricts which layers are generated (others are None); the
+    embedding, output matrix and output norm are always generated.
+    """
+    H, V = cfg.hidden, cfg.vocab
+    w = {
+        "config": cfg,
+        "tok_embd": quant_matrix(stream_key(cfg.name, "tok_embd"), V, H, cfg.sigma, cfg.wtype),
+        "output_norm": np.ones(H, dtype=np.float32),
+    }
+    w["output"] = None if cfg.tied else quant_matrix(stream_key(cfg.name, "output"), V, H, cfg.sigma, cfg.wtype)
+    sel = range(cfg.n_layers) if layers is None else layers
+    w["layers"] = [layer_weights(cfg, l) if l in sel else None for l in range(cfg.n_layers)]
+    return w
+
+
+def prompt_tokens(cfg: ModelConfig, n: int, seed: int = 1) -> np.ndarray:
+    return tokens(stream_key(cfg.name, "prompt", seed), n, cfg.vocab)

@@ -1,0 +1,50 @@
+"""The seeded input generator: determinism, distribution, formats.  CPU only."""
+import numpy as np
+
+import synth
+from synth.configs import CONFIGS
+
+
+def test_normal_is_counter_based():
+    key = synth.stream_key("t", 1)
+    a = synth.normal(key, 1000)
+    b = synth.normal(key, 600, start=400)
+    np.testing.assert_array_equal(a[400:], b)
+    assert not np.array_equal(a, synth.normal(synth.stream_key("t", 2), 1000))
+
+
+def test_normal_moments():
+    x = synth.normal(synth.stream_key("moments"), 1 << 20, 0.02)
+    assert abs(x.mean()) < 1e-4
+    assert abs(x.std() - 0.02) < 1e-4
+    # fourth moment of a normal is 3 sigma^4
+    assert abs(np.mean(x ** 4) / 0.02 ** 4 - 3.0) < 0.05
+
+
+def test_quant_matrix_matches_quantize_of_normals():
+    key = synth.stream_key("qm")
+    rows, cols = 5, 96
+    x = synth.normal(key, rows * cols, 0.02)
+    for wt in (8, 4):
+        np.testing.assert_array_equal(synth.quant_matrix(key, rows, cols, 0.02, wt), synth.quantize(x, wt))
+
+
+def test_f16_conversion_matches_numpy():
+    v = np.concatenate([synth.normal(3, 20000, 1.0), synth.normal(4, 20000, 1e-5),
+                        synth.normal(5, 2000, 3e4), [0.0, -0.0, 65504.0, 65519.99, 2 ** -25, 3 * 2 ** -26]])
+    ours = np.array([synth.f64_to_f16_bits(x) for x in v], dtype=np.uint16)
+    ref = v.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(ours, ref)
+
+
+def test_tokens_in_range():
+    t = synth.tokens(synth.stream_key("tok"), 10000, 128256)
+    assert t.min() >= 0 and t.max() < 128256
+    assert len(np.unique(t)) > 9000
+
+
+def test_config_parameter_counts():
+    # per-layer parameter counts of the shapes
+    assert CONFIGS["8b"].layer_params() == 218_103_808
+    assert CONFIGS["70b"].layer_params() == 855_638_016
+    assert CONFIGS["1b"].layer_params() == 60_817_408
