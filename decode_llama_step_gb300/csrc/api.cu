@@ -1,0 +1,1091 @@
+// Runtime behind the C ABI: model object, device-budget ledger, paged KV
+// pool, CUDA-graph replay of the decode step, two-buffer layer streaming and
+// the KV fork.  Host logic only; the arithmetic is in the kernels.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <chrono>
+#include <string>
+#include <vector>
+
+#include "../../include/dls.h"
+#include "kernels.h"
+
+using namespace dls;
+
+namespace {
+
+thread_local std::string g_err;
+
+size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct MatOff {
+  size_t qs = 0, d = 0;
+  int rows = 0, cols = 0, nb = 0;
+  size_t qs_bytes = 0, d_bytes = 0;
+};
+
+struct LayerLayout {
+  size_t attn_norm = 0, ffn_norm = 0;
+  MatOff qkv, o, gu, down;
+  size_t bytes = 0;
+};
+
+MatOff mat_off(size_t& cur, int rows, int cols, int wtype) {
+  MatOff m;
+  m.rows = rows;
+  m.cols = cols;
+  m.nb = (cols + 31) / 32;
+  m.qs_bytes = (size_t)rows * m.nb * (wtype == 8 ? 32 : 16);
+  m.d_bytes = (size_t)rows * m.nb * 2;
+  m.qs = cur;
+  cur = a256(cur + m.qs_bytes);
+  m.d = cur;
+  cur = a256(cur + m.d_bytes);
+  return m;
+}
+
+MatDev mat_at(const uint8_t* base, const MatOff& o, int row0 = 0, int rows = -1) {
+  MatDev m;
+  const size_t rb = o.qs_bytes / (o.rows ? o.rows : 1);
+  m.qs = base + o.qs + (size_t)row0 * rb;
+  m.d = reinterpret_cast<const __half*>(base + o.d) + (size_t)row0 * o.nb;
+  m.rows = rows < 0 ? o.rows - row0 : rows;
+  m.cols = o.cols;
+  m.nb = o.nb;
+  return m;
+}
+
+struct Seq {
+  bool live = false;
+  int len = 0;
+  std::vector<int> pages;
+};
+
+struct GraphEntry {
+  int rows;
+  bool head, argmax;
+  cudaGraphExec_t exec;
+};
+
+}  // namespace
+
+struct dls_model {
+  // shapes
+  int L, H, nh, nkv, hd, F, V, wtype, pt, max_seqs, max_ctx, max_batch, max_pages;
+  float theta, eps;
+  bool tied;
+  int q_rows, kv_rows;
+  LayerLayout lay;
+  size_t emb_bytes = 0;
+  int num_sms = 0;
+  // streams, allocator, ledger
+  cudaStream_t stream = nullptr, copy_stream = nullptr;
+  bool own_stream = false;
+  dls_allocator alloc{};
+  bool have_alloc = false;
+  uint64_t used = 0, budget = 0;
+  std::vector<std::pair<void*, size_t>> allocs;
+  // weights
+  std::vector<uint8_t*> layer_dev, layer_host;
+  uint8_t* stage[2] = {nullptr, nullptr};
+  cudaEvent_t ev_filled[2] = {}, ev_free[2] = {}, ev_start = nullptr;
+  int resident = 0;
+  uint8_t* emb_block = nullptr;
+  uint8_t* out_block = nullptr;
+  MatOff emb_off, out_off;
+  float* out_norm = nullptr;
+  // KV
+  __half* k_pool = nullptr;
+  __half* v_pool = nullptr;
+  size_t page_elems = 0, kv_layer_elems = 0;
+  int n_pages = 0;
+  std::vector<int> free_pages;
+  std::vector<Seq> seqs;
+  int32_t* pt_dev = nullptr;
+  std::vector<int32_t> pt_host;
+  // workspaces
+  float *x = nullptr, *q = nullptr, *o = nullptr, *gu = nullptr, *logits = nullptr;
+  int32_t* next_tok = nullptr;
+  int32_t* tokens_dev = nullptr;
+  size_t tokens_cap = 0;
+  int32_t* argmax_buf = nullptr;
+  StepParams* sp = nullptr;
+  float2* rope = nullptr;
+  int rope_len = 0;
+  void* attn_ws = nullptr;
+  float *part_o = nullptr, *part_ml = nullptr;
+  int* counters = nullptr;
+  int attn_splits = 1;
+  int2* pairs_dev = nullptr;
+  size_t pairs_cap = 0;
+  GemvLaunch plan_qkv{}, plan_o{}, plan_gu{}, plan_down{}, plan_head{};
+  // graphs and hooks
+  std::vector<GraphEntry> graphs;
+  float* capture = nullptr;
+  int launches_per_step = 0;
+  int launch_count = 0;
+  std::string err;
+};
+
+namespace {
+
+const char* status_str(int s) {
+  switch (s) {
+    case DLS_OK: return "OK";
+    case DLS_ERR_ARG: return "ARG";
+    case DLS_ERR_BUDGET: return "BUDGET";
+    case DLS_ERR_CAPACITY: return "CAPACITY";
+    case DLS_ERR_CUDA: return "CUDA";
+    case DLS_ERR_TIMEOUT: return "TIMEOUT";
+    case DLS_ERR_STATE: return "STATE";
+    default: return "UNKNOWN";
+  }
+}
+
+int fail(dls_model* m, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  std::string s = std::string("ERR ") + status_str(code) + " " + buf;
+  if (m) m->err = s;
+  g_err = s;
+  return code;
+}
+
+#define CK(call)                                                                                      \
+  do {                                                                                                \
+    cudaError_t e_ = (call);                                                                          \
+    if (e_ != cudaSuccess) return fail(m, DLS_ERR_CUDA, "call=%s cuda=%s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+#define TRY(expr)            \
+  do {                       \
+    int r_ = (expr);         \
+    if (r_ != DLS_OK) return r_; \
+  } while (0)
+
+// ---- ledger: reserve before allocating, commit only on success --------------
+
+int dev_alloc(dls_model* m, size_t bytes, void** out, const char* what) {
+  bytes = a256(bytes ? bytes : 256);
+  if (m->budget && (bytes > m->budget || m->used > m->budget - bytes))
+    return fail(m, DLS_ERR_BUDGET, "what=%s bytes=%zu used=%llu budget=%llu", what, bytes,
+                (unsigned long long)m->used, (unsigned long long)m->budget);
+  void* p = nullptr;
+  if (m->have_alloc) {
+    p = m->alloc.alloc(m->alloc.ctx, bytes, m->stream);
+  } else if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    p = nullptr;
+  }
+  if (!p) return fail(m, DLS_ERR_CUDA, "what=%s bytes=%zu allocation failed", what, bytes);
+  m->used += bytes;
+  m->allocs.push_back({p, bytes});
+  *out = p;
+  return DLS_OK;
+}
+
+void dev_free(dls_model* m, void* p) {
+  if (!p) return;
+  for (size_t i = 0; i < m->allocs.size(); ++i)
+    if (m->allocs[i].first == p) {
+      m->used -= m->allocs[i].second;
+      m->allocs.erase(m->allocs.begin() + i);
+      if (m->have_alloc) m->alloc.free(m->alloc.ctx, p, m->stream);
+      else cudaFree(p);
+      return;
+    }
+}
+
+template <class T>
+int dev_alloc_t(dls_model* m, size_t count, T** out, const char* what) {
+  void* p = nullptr;
+  TRY(dev_alloc(m, count * sizeof(T), &p, what));
+  *out = static_cast<T*>(p);
+  return DLS_OK;
+}
+
+// Bounded host wait: poll the stream until it drains or the deadline passes.
+int sync_stream(dls_model* m, cudaStream_t s, double seconds = 900.0) {
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    cudaError_t e = cudaStreamQuery(s);
+    if (e == cudaSuccess) return DLS_OK;
+    if (e != cudaErrorNotReady) return fail(m, DLS_ERR_CUDA, "stream=%p cuda=%s", (void*)s, cudaGetErrorString(e));
+    const double dt = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+    if (dt > seconds) return fail(m, DLS_ERR_TIMEOUT, "waited_s=%.1f", dt);
+  }
+}
+
+int check_status(dls_model* m) {
+  int32_t st = 0;
+  CK(cudaMemcpyAsync(&st, &m->sp->status, sizeof st, cudaMemcpyDeviceToHost, m->stream));
+  TRY(sync_stream(m, m->stream));
+  if (st) {
+    const int32_t zero = 0;
+    CK(cudaMemcpyAsync(&m->sp->status, &zero, sizeof zero, cudaMemcpyHostToDevice, m->stream));
+    TRY(sync_stream(m, m->stream));
+    return fail(m, DLS_ERR_STATE, "device_status=0x%x (1=page 2=token 4=position)", st);
+  }
+  return DLS_OK;
+}
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// copy device results to a caller pointer (device or host); syncs for host
+int copy_out(dls_model* m, void* dst, const void* src, size_t bytes) {
+  if (!dst) return DLS_OK;
+  const bool dev = is_device_ptr(dst);
+  CK(cudaMemcpyAsync(dst, src, bytes, dev ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, m->stream));
+  if (!dev) TRY(sync_stream(m, m->stream));
+  return DLS_OK;
+}
+
+// ---- layers ------------------------------------------------------------------
+
+struct LayerPtrs {
+  const float *attn_norm, *ffn_norm;
+  MatDev qkv, o, gu, down;
+};
+
+LayerPtrs layer_ptrs(const dls_model* m, const uint8_t* base) {
+  LayerPtrs p;
+  p.attn_norm = reinterpret_cast<const float*>(base + m->lay.attn_norm);
+  p.ffn_norm = reinterpret_cast<const float*>(base + m->lay.ffn_norm);
+  p.qkv = mat_at(base, m->lay.qkv);
+  p.o = mat_at(base, m->lay.o);
+  p.gu = mat_at(base, m->lay.gu);
+  p.down = mat_at(base, m->lay.down);
+  return p;
+}
+
+MatDev head_mat(const dls_model* m) {
+  return m->tied ? mat_at(m->emb_block, m->emb_off) : mat_at(m->out_block, m->out_off);
+}
+
+// ---- the decode step -------------------------------------------------------------
+// Per batch row b (values in m->sp): embedding -> per layer [QKV+RoPE+KV
+// append, attention, O + residual, gate/up, SwiGLU->down + residual] ->
+// final norm + LM head [-> greedy pick].  With streamed layers the copy
+// stream fills buffer (l - resident) % 2 while the previous layer computes.
+
+#define LK(call)                                                                                      \
+  do {                                                                                                \
+    cudaError_t e_ = (call);                                                                          \
+    ++m->launch_count;                                                                                \
+    if (e_ != cudaSuccess) return fail(m, DLS_ERR_CUDA, "launch=%s cuda=%s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+int enqueue_copy_layer(dls_model* m, int l) {
+  const int buf = (l - m->resident) & 1;
+  CK(cudaStreamWaitEvent(m->copy_stream, m->ev_free[buf], 0));
+  CK(cudaMemcpyAsync(m->stage[buf], m->layer_host[l], m->lay.bytes, cudaMemcpyHostToDevice, m->copy_stream));
+  CK(cudaEventRecord(m->ev_filled[buf], m->copy_stream));
+  return DLS_OK;
+}
+
+int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
+  cudaStream_t s = m->stream;
+  const bool pdl = true;
+  float* x = m->x + (size_t)b * m->H;
+  float* logits = m->logits + (size_t)b * m->V;
+  LK(launch_embed(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp, b, x, m->V, s, pdl));
+  const bool streaming = m->resident < m->L;
+  if (streaming) {
+    // the copy stream joins this step after everything enqueued so far
+    CK(cudaEventRecord(m->ev_start, s));
+    CK(cudaStreamWaitEvent(m->copy_stream, m->ev_start, 0));
+    // both buffers are free at the start of a step
+    CK(cudaEventRecord(m->ev_free[0], s));
+    CK(cudaEventRecord(m->ev_free[1], s));
+    for (int l = m->resident; l < std::min(m->L, m->resident + 2); ++l) TRY(enqueue_copy_layer(m, l));
+  }
+  for (int l = 0; l < m->L; ++l) {
+    const bool streamed = l >= m->resident;
+    const int buf = (l - m->resident) & 1;
+    if (streamed) CK(cudaStreamWaitEvent(s, m->ev_filled[buf], 0));
+    const LayerPtrs P = layer_ptrs(m, streamed ? m->stage[buf] : m->layer_dev[l]);
+    KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
+              m->nkv, m->hd, m->pt, m->max_pages};
+    // (1) RMSNorm -> QKV GEMV -> RoPE -> fp16 K/V append
+    GemvArgs g{};
+    g.w = P.qkv;
+    g.unit = 2;
+    g.x = x;
+    g.g = P.attn_norm;
+    g.eps = m->eps;
+    g.y = m->q;
+    g.q_rows = m->q_rows;
+    g.kv_rows = m->kv_rows;
+    g.kv = kv;
+    g.rope_cs = m->rope;
+    g.rope_len = m->rope_len;
+    g.sp = m->sp;
+    g.brow = b;
+    LK(launch_gemv(m->wtype, PRO_RMSNORM, EPI_QKV, g, m->plan_qkv, s, pdl));
+    // (2) split-K GQA attention over the paged cache
+    AttnArgs a{};
+    a.q = m->q;
+    a.o = m->o;
+    a.k_pool = kv.k_pool;
+    a.v_pool = kv.v_pool;
+    a.page_table = m->pt_dev;
+    a.max_pages = m->max_pages;
+    a.pt_row = m->sp->seq;
+    a.len = m->sp->pos;
+    a.len_add = 1;
+    a.n_heads = m->nh;
+    a.n_kv = m->nkv;
+    a.head_dim = m->hd;
+    a.page_tokens = m->pt;
+    a.n_splits = m->attn_splits;
+    a.row0 = b;
+    a.part_o = m->part_o;
+    a.part_ml = m->part_ml;
+    a.counters = m->counters;
+    a.status = &m->sp->status;
+    a.max_len = m->max_ctx;
+    LK(launch_attention(a, 1, s, pdl));
+    // (3) O projection + residual
+    GemvArgs go{};
+    go.w = P.o;
+    go.unit = 1;
+    go.x = m->o;
+    go.y = x;
+    LK(launch_gemv(m->wtype, PRO_COPY, EPI_RESID, go, m->plan_o, s, pdl));
+    // (4) RMSNorm -> gate|up GEMV
+    GemvArgs gg{};
+    gg.w = P.gu;
+    gg.unit = 1;
+    gg.x = x;
+    gg.g = P.ffn_norm;
+    gg.eps = m->eps;
+    gg.y = m->gu;
+    LK(launch_gemv(m->wtype, PRO_RMSNORM, EPI_STORE, gg, m->plan_gu, s, pdl));
+    // (5) SwiGLU -> down GEMV + residual
+    GemvArgs gd{};
+    gd.w = P.down;
+    gd.unit = 1;
+    gd.x = m->gu;
+    gd.y = x;
+    LK(launch_gemv(m->wtype, PRO_SWIGLU, EPI_RESID, gd, m->plan_down, s, pdl));
+    if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * m->H, x, m->H * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    if (streamed) {
+      CK(cudaEventRecord(m->ev_free[buf], s));
+      if (l + 2 < m->L) TRY(enqueue_copy_layer(m, l + 2));
+    }
+  }
+  if (head || argmax) {
+    GemvArgs gh{};
+    gh.w = head_mat(m);
+    gh.unit = 1;
+    gh.x = x;
+    gh.g = m->out_norm;
+    gh.eps = m->eps;
+    gh.y = logits;
+    LK(launch_gemv(m->wtype, PRO_RMSNORM, EPI_STORE, gh, m->plan_head, s, pdl));
+  }
+  if (argmax) LK(launch_argmax(logits, m->V, 1, m->next_tok + b, s, pdl));
+  return DLS_OK;
+}
+
+int enqueue_step(dls_model* m, int rows, bool head, bool argmax, float* capture) {
+  m->launch_count = 0;
+  for (int b = 0; b < rows; ++b) TRY(enqueue_row(m, b, head, argmax, b == 0 ? capture : nullptr));
+  if (argmax) LK(launch_advance(m->sp, m->next_tok, m->tokens_dev, rows, m->stream, true));
+  m->launches_per_step = m->launch_count;
+  return DLS_OK;
+}
+
+void drop_graphs(dls_model* m) {
+  for (auto& g : m->graphs) cudaGraphExecDestroy(g.exec);
+  m->graphs.clear();
+}
+
+// Replay the step as one CUDA graph (captured on first use per shape).
+int run_step(dls_model* m, int rows, bool head, bool argmax) {
+  if (m->capture) {
+    float* cap = m->capture;
+    m->capture = nullptr;
+    return enqueue_step(m, rows, head, argmax, cap);
+  }
+  for (auto& g : m->graphs)
+    if (g.rows == rows && g.head == head && g.argmax == argmax) {
+      CK(cudaGraphLaunch(g.exec, m->stream));
+      return DLS_OK;
+    }
+  cudaGraph_t graph = nullptr;
+  CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
+  const int r = enqueue_step(m, rows, head, argmax, nullptr);
+  cudaError_t e = cudaStreamEndCapture(m->stream, &graph);
+  if (r != DLS_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return r;
+  }
+  if (e != cudaSuccess) return fail(m, DLS_ERR_CUDA, "capture cuda=%s", cudaGetErrorString(e));
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return fail(m, DLS_ERR_CUDA, "instantiate cuda=%s", cudaGetErrorString(e));
+  m->graphs.push_back({rows, head, argmax, exec});
+  CK(cudaGraphLaunch(exec, m->stream));
+  return DLS_OK;
+}
+
+// ---- paged KV ------------------------------------------------------------------
+
+int pages_needed(const dls_model* m, int len) { return (len + m->pt - 1) / m->pt; }
+
+// Give `seq` pages for positions [0, len); all-or-nothing.
+int ensure_pages(dls_model* m, int seq, int len) {
+  Seq& s = m->seqs[seq];
+  const int need = pages_needed(m, len) - (int)s.pages.size();
+  if (need <= 0) return DLS_OK;
+  if (need > (int)m->free_pages.size())
+    return fail(m, DLS_ERR_CAPACITY, "seq=%d need_pages=%d free_pages=%zu", seq, need, m->free_pages.size());
+  const int first = (int)s.pages.size();
+  for (int i = 0; i < need; ++i) {
+    const int p = m->free_pages.back();
+    m->free_pages.pop_back();
+    s.pages.push_back(p);
+    m->pt_host[(size_t)seq * m->max_pages + first + i] = p;
+  }
+  // pageable source: staged before the call returns, so the mirror may change later
+  CK(cudaMemcpyAsync(m->pt_dev + (size_t)seq * m->max_pages + first, &m->pt_host[(size_t)seq * m->max_pages + first],
+                     need * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+  return DLS_OK;
+}
+
+int release_pages(dls_model* m, int seq) {
+  Seq& s = m->seqs[seq];
+  for (int p : s.pages) m->free_pages.push_back(p);
+  const int n = (int)s.pages.size();
+  s.pages.clear();
+  s.len = 0;
+  if (n) {
+    std::fill(m->pt_host.begin() + (size_t)seq * m->max_pages, m->pt_host.begin() + (size_t)seq * m->max_pages + n, -1);
+    CK(cudaMemcpyAsync(m->pt_dev + (size_t)seq * m->max_pages, &m->pt_host[(size_t)seq * m->max_pages],
+                       n * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+  }
+  return DLS_OK;
+}
+
+int check_seq(dls_model* m, int seq) {
+  if (seq < 0 || seq >= m->max_seqs || !m->seqs[seq].live) return fail(m, DLS_ERR_ARG, "seq=%d not live", seq);
+  return DLS_OK;
+}
+
+int set_params(dls_model* m, int n, const int32_t* seqs, const int32_t* tokens, const int32_t* pos, bool reset) {
+  StepParams h{};
+  h.n = n;
+  for (int i = 0; i < n; ++i) {
+    h.seq[i] = seqs[i];
+    h.token[i] = tokens[i];
+    h.pos[i] = pos[i];
+  }
+  CK(launch_set_params(m->sp, h, reset, m->stream));
+  return DLS_OK;
+}
+
+// ---- weights: host blocks -> device layout -------------------------------------
+
+int upload_matrix(dls_model* m, const void* host_blocks, int rows, int cols, uint8_t* dst_base, const MatOff& off,
+                  int row0, uint8_t* temp) {
+  const int nb = (cols + 31) / 32;
+  const size_t bsz = m->wtype == 8 ? 34 : 18;
+  const size_t bytes = (size_t)rows * nb * bsz;
+  CK(cudaMemcpyAsync(temp, host_blocks, bytes, cudaMemcpyHostToDevice, m->stream));
+  const size_t rb = off.qs_bytes / off.rows;
+  CK(launch_repack(temp, m->wtype, rows, nb, dst_base + off.qs + (size_t)row0 * rb,
+                   reinterpret_cast<__half*>(dst_base + off.d) + (size_t)row0 * nb, m->stream));
+  return DLS_OK;
+}
+
+int upload_layer(dls_model* m, const dls_layer_desc& ld, uint8_t* dst, uint8_t* temp) {
+  CK(cudaMemcpyAsync(dst + m->lay.attn_norm, ld.attn_norm, m->H * sizeof(float), cudaMemcpyHostToDevice, m->stream));
+  CK(cudaMemcpyAsync(dst + m->lay.ffn_norm, ld.ffn_norm, m->H * sizeof(float), cudaMemcpyHostToDevice, m->stream));
+  TRY(upload_matrix(m, ld.wq, m->q_rows, m->H, dst, m->lay.qkv, 0, temp));
+  TRY(upload_matrix(m, ld.wk, m->kv_rows, m->H, dst, m->lay.qkv, m->q_rows, temp));
+  TRY(upload_matrix(m, ld.wv, m->kv_rows, m->H, dst, m->lay.qkv, m->q_rows + m->kv_rows, temp));
+  TRY(upload_matrix(m, ld.wo, m->H, m->q_rows, dst, m->lay.o, 0, temp));
+  TRY(upload_matrix(m, ld.w_gate, m->F, m->H, dst, m->lay.gu, 0, temp));
+  TRY(upload_matrix(m, ld.w_up, m->F, m->H, dst, m->lay.gu, m->F, temp));
+  TRY(upload_matrix(m, ld.w_down, m->H, m->F, dst, m->lay.down, 0, temp));
+  return DLS_OK;
+}
+
+size_t staging_bytes(const dls_model* m) { return 2 * a256(m->lay.bytes); }
+
+// Largest resident count the budget allows given what else is allocated.
+int auto_resident(const dls_model* m, uint64_t other_bytes) {
+  if (!m->budget) return m->L;
+  const uint64_t lb = a256(m->lay.bytes);
+  if (other_bytes + (uint64_t)m->L * lb <= m->budget) return m->L;
+  if (other_bytes + staging_bytes(m) > m->budget) return -1;
+  const uint64_t room = m->budget - other_bytes - staging_bytes(m);
+  return (int)std::min<uint64_t>(room / lb, (uint64_t)m->L - 1);
+}
+
+int apply_resident(dls_model* m, int n) {
+  // evict layers [n, L): keep a pinned host copy, then free the device copy
+  for (int l = n; l < m->L; ++l) {
+    if (!m->layer_dev[l]) continue;
+    if (!m->layer_host[l]) {
+      void* h = nullptr;
+      CK(cudaHostAlloc(&h, m->lay.bytes, cudaHostAllocDefault));
+      m->layer_host[l] = static_cast<uint8_t*>(h);
+      CK(cudaMemcpyAsync(h, m->layer_dev[l], m->lay.bytes, cudaMemcpyDeviceToHost, m->stream));
+      TRY(sync_stream(m, m->stream));
+    }
+    dev_free(m, m->layer_dev[l]);
+    m->layer_dev[l] = nullptr;
+  }
+  if (n >= m->L) {
+    for (auto& st : m->stage) {
+      dev_free(m, st);
+      st = nullptr;
+    }
+  }
+  if (n < m->L && !m->stage[0]) {
+    for (auto& st : m->stage) {
+      void* p = nullptr;
+      TRY(dev_alloc(m, m->lay.bytes, &p, "stream_buffer"));
+      st = static_cast<uint8_t*>(p);
+    }
+  }
+  for (int l = 0; l < n; ++l) {
+    if (m->layer_dev[l]) continue;
+    void* p = nullptr;
+    TRY(dev_alloc(m, m->lay.bytes, &p, "layer"));
+    m->layer_dev[l] = static_cast<uint8_t*>(p);
+    CK(cudaMemcpyAsync(p, m->layer_host[l], m->lay.bytes, cudaMemcpyHostToDevice, m->stream));
+  }
+  TRY(sync_stream(m, m->stream));
+  m->resident = n;
+  drop_graphs(m);
+  return DLS_OK;
+}
+
+void destroy(dls_model* m) {
+  if (!m) return;
+  if (m->stream) cudaStreamSynchronize(m->stream);
+  if (m->copy_stream) cudaStreamSynchronize(m->copy_stream);
+  drop_graphs(m);
+  while (!m->allocs.empty()) dev_free(m, m->allocs.back().first);
+  for (auto* h : m->layer_host)
+    if (h) cudaFreeHost(h);
+  for (int i = 0; i < 2; ++i) {
+    if (m->ev_filled[i]) cudaEventDestroy(m->ev_filled[i]);
+    if (m->ev_free[i]) cudaEventDestroy(m->ev_free[i]);
+  }
+  if (m->ev_start) cudaEventDestroy(m->ev_start);
+  if (m->copy_stream) cudaStreamDestroy(m->copy_stream);
+  if (m->own_stream && m->stream) cudaStreamDestroy(m->stream);
+  delete m;
+}
+
+int validate_desc(const dls_model_desc* d) {
+  dls_model* m = nullptr;
+  if (!d) return fail(m, DLS_ERR_ARG, "desc=NULL");
+  if (d->n_layers < 1 || d->hidden < 32 || d->n_heads < 1 || d->n_kv_heads < 1 || d->ffn < 1 || d->vocab < 1)
+    return fail(m, DLS_ERR_ARG, "shape n_layers=%d hidden=%d n_heads=%d n_kv_heads=%d ffn=%d vocab=%d", d->n_layers,
+                d->hidden, d->n_heads, d->n_kv_heads, d->ffn, d->vocab);
+  if (d->hidden % 32) return fail(m, DLS_ERR_ARG, "hidden=%d not a multiple of 32", d->hidden);
+  if (d->n_heads % d->n_kv_heads || d->n_heads / d->n_kv_heads > 16)
+    return fail(m, DLS_ERR_ARG, "n_heads=%d n_kv_heads=%d (groups of at most 16)", d->n_heads, d->n_kv_heads);
+  if (d->head_dim != 32 && d->head_dim != 64 && d->head_dim != 128)
+    return fail(m, DLS_ERR_ARG, "head_dim=%d (32, 64 or 128)", d->head_dim);
+  if (d->wtype != DLS_Q8_0 && d->wtype != DLS_Q4_0) return fail(m, DLS_ERR_ARG, "wtype=%d", d->wtype);
+  const int pt = d->page_tokens ? d->page_tokens : 64;
+  if (pt != 32 && pt != 64 && pt != 128 && pt != 256) return fail(m, DLS_ERR_ARG, "page_tokens=%d", d->page_tokens);
+  if (d->max_seqs < 1 || d->max_ctx < 1) return fail(m, DLS_ERR_ARG, "max_seqs=%d max_ctx=%d", d->max_seqs, d->max_ctx);
+  if (d->max_batch < 0 || d->max_batch > DLS_MAX_BATCH) return fail(m, DLS_ERR_ARG, "max_batch=%d", d->max_batch);
+  if (!(d->rope_theta > 0.f) || !(d->rms_eps >= 0.f))
+    return fail(m, DLS_ERR_ARG, "rope_theta=%g rms_eps=%g", d->rope_theta, d->rms_eps);
+  if (!d->tok_embd || !d->output_norm || !d->layers || (!d->tied_embeddings && !d->output))
+    return fail(m, DLS_ERR_ARG, "missing tensor pointer");
+  for (int l = 0; l < d->n_layers; ++l) {
+    const dls_layer_desc& L = d->layers[l];
+    if (!L.attn_norm || !L.ffn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.w_gate || !L.w_up || !L.w_down)
+      return fail(m, DLS_ERR_ARG, "layer=%d missing tensor pointer", l);
+  }
+  return DLS_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+int dls_abi_version(void) { return DLS_ABI_VERSION; }
+const char* dls_status_name(int s) { return status_str(s); }
+const char* dls_last_error(const dls_model* m) { return m ? m->err.c_str() : g_err.c_str(); }
+uint64_t dls_device_bytes(const dls_model* m) { return m ? m->used : 0; }
+uint64_t dls_device_budget(const dls_model* m) { return m ? m->budget : 0; }
+int32_t dls_resident_layers(const dls_model* m) { return m ? m->resident : -1; }
+uint64_t dls_layer_bytes(const dls_model* m) { return m ? m->lay.bytes : 0; }
+int32_t dls_debug_launches_per_step(const dls_model* m) { return m ? m->launches_per_step : -1; }
+
+int dls_check_context_budget(int32_t prefix_tokens, int32_t max_branch_tokens, int32_t headroom, int32_t n_ctx) {
+  dls_model* m = nullptr;
+  if (prefix_tokens < 0 || max_branch_tokens < 0 || headroom < 0 || n_ctx < 0)
+    return fail(m, DLS_ERR_ARG, "negative token count");
+  const long long required = (long long)prefix_tokens + max_branch_tokens + headroom;
+  if (required > n_ctx)
+    return fail(m, DLS_ERR_CAPACITY, "prefix_tokens=%d max_branch_tokens=%d headroom=%d required=%lld n_ctx=%d",
+                prefix_tokens, max_branch_tokens, headroom, required, n_ctx);
+  return DLS_OK;
+}
+
+int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator, void* cuda_stream, dls_model** out) {
+  if (!out) return fail(nullptr, DLS_ERR_ARG, "out=NULL");
+  *out = nullptr;
+  TRY(validate_desc(desc));
+  if (allocator && (!allocator->alloc || !allocator->free)) return fail(nullptr, DLS_ERR_ARG, "allocator callbacks");
+  dls_model* m = new dls_model();
+  const dls_model_desc& d = *desc;
+  m->L = d.n_layers;
+  m->H = d.hidden;
+  m->nh = d.n_heads;
+  m->nkv = d.n_kv_heads;
+  m->hd = d.head_dim;
+  m->F = d.ffn;
+  m->V = d.vocab;
+  m->wtype = d.wtype;
+  m->pt = d.page_tokens ? d.page_tokens : 64;
+  m->max_seqs = d.max_seqs;
+  m->max_ctx = d.max_ctx;
+  m->max_batch = d.max_batch ? d.max_batch : 1;
+  m->max_pages = (d.max_ctx + m->pt - 1) / m->pt;
+  m->theta = d.rope_theta;
+  m->eps = d.rms_eps;
+  m->tied = d.tied_embeddings != 0;
+  m->q_rows = d.n_heads * d.head_dim;
+  m->kv_rows = d.n_kv_heads * d.head_dim;
+  m->budget = d.device_budget_bytes;
+  if (allocator) {
+    m->alloc = *allocator;
+    m->have_alloc = true;
+  }
+  auto bail = [&](int r) {
+    std::string e = m->err;
+    destroy(m);
+    g_err = e;
+    return r;
+  };
+#define CKC(call)                                                                                           \
+  do {                                                                                                      \
+    cudaError_t e_ = (call);                                                                                \
+    if (e_ != cudaSuccess) return bail(fail(m, DLS_ERR_CUDA, "call=%s cuda=%s", #call, cudaGetErrorString(e_))); \
+  } while (0)
+#define TRYC(expr)                 \
+  do {                             \
+    int r_ = (expr);               \
+    if (r_ != DLS_OK) return bail(r_); \
+  } while (0)
+
+  int dev = 0;
+  CKC(cudaGetDevice(&dev));
+  CKC(cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev));
+  if (cuda_stream) {
+    m->stream = static_cast<cudaStream_t>(cuda_stream);
+  } else {
+    CKC(cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking));
+    m->own_stream = true;
+  }
+  CKC(cudaStreamCreateWithFlags(&m->copy_stream, cudaStreamNonBlocking));
+  for (int i = 0; i < 2; ++i) {
+    CKC(cudaEventCreateWithFlags(&m->ev_filled[i], cudaEventDisableTiming));
+    CKC(cudaEventCreateWithFlags(&m->ev_free[i], cudaEventDisableTiming));
+  }
+  CKC(cudaEventCreateWithFlags(&m->ev_start, cudaEventDisableTiming));
+  CKC(gemv_setup_attributes());
+
+  // layouts
+  size_t cur = 0;
+  m->lay.attn_norm = cur;
+  cur = a256(cur + m->H * sizeof(float));
+  m->lay.ffn_norm = cur;
+  cur = a256(cur + m->H * sizeof(float));
+  m->lay.qkv = mat_off(cur, m->q_rows + 2 * m->kv_rows, m->H, m->wtype);
+  m->lay.o = mat_off(cur, m->H, m->q_rows, m->wtype);
+  m->lay.gu = mat_off(cur, 2 * m->F, m->H, m->wtype);
+  m->lay.down = mat_off(cur, m->H, m->F, m->wtype);
+  m->lay.bytes = cur;
+  cur = 0;
+  m->emb_off = mat_off(cur, m->V, m->H, m->wtype);
+  m->emb_bytes = cur;
+  cur = 0;
+  m->out_off = mat_off(cur, m->V, m->H, m->wtype);
+
+  m->plan_qkv = gemv_plan(m->wtype, m->lay.qkv.rows, m->lay.qkv.nb, m->num_sms, 2);
+  m->plan_o = gemv_plan(m->wtype, m->lay.o.rows, m->lay.o.nb, m->num_sms, 1);
+  m->plan_gu = gemv_plan(m->wtype, m->lay.gu.rows, m->lay.gu.nb, m->num_sms, 1);
+  m->plan_down = gemv_plan(m->wtype, m->lay.down.rows, m->lay.down.nb, m->num_sms, 1);
+  m->plan_head = gemv_plan(m->wtype, m->V, m->emb_off.nb, m->num_sms, 1);
+  m->attn_splits = attn_default_splits(1, m->nkv, m->num_sms, m->max_ctx);
+
+  // fixed allocations (everything but the layers)
+  const int B = m->max_batch;
+  m->n_pages = m->max_seqs * m->max_pages;
+  m->page_elems = (size_t)m->nkv * m->pt * m->hd;
+  m->kv_layer_elems = (size_t)m->n_pages * m->page_elems;
+  m->rope_len = m->max_ctx;
+  const size_t bsz = m->wtype == 8 ? 34 : 18;
+  size_t temp_bytes = (size_t)m->V * m->emb_off.nb * bsz;
+  temp_bytes = std::max(temp_bytes, (size_t)2 * m->F * ((m->H + 31) / 32) * bsz);
+  temp_bytes = std::max(temp_bytes, (size_t)m->H * ((m->F + 31) / 32) * bsz);
+  void* p = nullptr;
+  TRYC(dev_alloc(m, m->emb_bytes, &p, "tok_embd"));
+  m->emb_block = static_cast<uint8_t*>(p);
+  if (!m->tied) {
+    TRYC(dev_alloc(m, m->emb_bytes, &p, "output"));
+    m->out_block = static_cast<uint8_t*>(p);
+  }
+  TRYC(dev_alloc_t(m, m->H, &m->out_norm, "output_norm"));
+  TRYC(dev_alloc_t(m, (size_t)m->L * m->kv_layer_elems, &m->k_pool, "k_cache"));
+  TRYC(dev_alloc_t(m, (size_t)m->L * m->kv_layer_elems, &m->v_pool, "v_cache"));
+  TRYC(dev_alloc_t(m, (size_t)m->max_seqs * m->max_pages, &m->pt_dev, "page_table"));
+  TRYC(dev_alloc_t(m, (size_t)B * m->H, &m->x, "x"));
+  TRYC(dev_alloc_t(m, (size_t)B * m->q_rows, &m->q, "q"));
+  TRYC(dev_alloc_t(m, (size_t)B * m->q_rows, &m->o, "o"));
+  TRYC(dev_alloc_t(m, (size_t)B * 2 * m->F, &m->gu, "gate_up"));
+  TRYC(dev_alloc_t(m, (size_t)B * m->V, &m->logits, "logits"));
+  TRYC(dev_alloc_t(m, (size_t)kMaxBatch, &m->next_tok, "next_token"));
+  TRYC(dev_alloc_t(m, (size_t)4096, &m->argmax_buf, "argmax"));
+  TRYC(dev_alloc_t(m, 1, &m->sp, "step_params"));
+  TRYC(dev_alloc_t(m, (size_t)m->rope_len * (m->hd / 2), &m->rope, "rope_table"));
+  const size_t ws = attn_workspace_bytes(1, m->nh, m->nkv, m->hd, m->attn_splits);
+  TRYC(dev_alloc(m, ws, &m->attn_ws, "attention_scratch"));
+  attn_workspace_carve(m->attn_ws, 1, m->nh, m->nkv, m->hd, m->attn_splits, &m->part_o, &m->part_ml, &m->counters);
+  m->pairs_cap = (size_t)m->max_pages * std::max(1, m->max_seqs - 1);
+  TRYC(dev_alloc_t(m, m->pairs_cap, &m->pairs_dev, "fork_pairs"));
+  void* temp = nullptr;
+  TRYC(dev_alloc(m, temp_bytes, &temp, "upload_temp"));
+
+  // resident layers: as many as the budget allows (first layers first)
+  m->layer_dev.assign(m->L, nullptr);
+  m->layer_host.assign(m->L, nullptr);
+  const int nres = auto_resident(m, m->used);
+  if (nres < 0) return bail(fail(m, DLS_ERR_BUDGET, "fixed_bytes=%llu budget=%llu", (unsigned long long)m->used,
+                                 (unsigned long long)m->budget));
+  if (nres < m->L) {
+    for (auto& st : m->stage) {
+      TRYC(dev_alloc(m, m->lay.bytes, &p, "stream_buffer"));
+      st = static_cast<uint8_t*>(p);
+    }
+  }
+  for (int l = 0; l < nres; ++l) {
+    TRYC(dev_alloc(m, m->lay.bytes, &p, "layer"));
+    m->layer_dev[l] = static_cast<uint8_t*>(p);
+  }
+  m->resident = nres;
+
+  // upload: norms, embeddings, layers (streamed layers go through buffer 0
+  // and then to pinned host memory)
+  CKC(cudaMemcpyAsync(m->out_norm, d.output_norm, m->H * sizeof(float), cudaMemcpyHostToDevice, m->stream));
+  TRYC(upload_matrix(m, d.tok_embd, m->V, m->H, m->emb_block, m->emb_off, 0, static_cast<uint8_t*>(temp)));
+  if (!m->tied) TRYC(upload_matrix(m, d.output, m->V, m->H, m->out_block, m->out_off, 0, static_cast<uint8_t*>(temp)));
+  for (int l = 0; l < m->L; ++l) {
+    uint8_t* dst = l < nres ? m->layer_dev[l] : m->stage[0];
+    TRYC(upload_layer(m, d.layers[l], dst, static_cast<uint8_t*>(temp)));
+    if (l >= nres) {
+      void* h = nullptr;
+      CKC(cudaHostAlloc(&h, m->lay.bytes, cudaHostAllocDefault));
+      m->layer_host[l] = static_cast<uint8_t*>(h);
+      CKC(cudaMemcpyAsync(h, dst, m->lay.bytes, cudaMemcpyDeviceToHost, m->stream));
+    }
+  }
+  CKC(launch_rope_table(m->rope, m->rope_len, m->hd, m->theta, m->stream));
+  m->pt_host.assign((size_t)m->max_seqs * m->max_pages, -1);
+  CKC(cudaMemcpyAsync(m->pt_dev, m->pt_host.data(), m->pt_host.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                      m->stream));
+  CKC(cudaMemsetAsync(m->attn_ws, 0, ws, m->stream));
+  CKC(cudaMemsetAsync(m->sp, 0, sizeof(StepParams), m->stream));
+  TRYC(sync_stream(m, m->stream));
+  dev_free(m, temp);
+  m->free_pages.clear();
+  for (int i = m->n_pages - 1; i >= 0; --i) m->free_pages.push_back(i);
+  m->seqs.assign(m->max_seqs, Seq());
+  *out = m;
+  return DLS_OK;
+#undef CKC
+#undef TRYC
+}
+
+void dls_model_destroy(dls_model* m) { destroy(m); }
+
+int dls_seq_create(dls_model* m, int32_t* seq_out) {
+  if (!m || !seq_out) return fail(m, DLS_ERR_ARG, "NULL argument");
+  for (int i = 0; i < m->max_seqs; ++i)
+    if (!m->seqs[i].live) {
+      m->seqs[i].live = true;
+      m->seqs[i].len = 0;
+      *seq_out = i;
+      return DLS_OK;
+    }
+  return fail(m, DLS_ERR_CAPACITY, "max_seqs=%d all live", m->max_seqs);
+}
+
+int dls_seq_free(dls_model* m, int32_t seq) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  TRY(check_seq(m, seq));
+  TRY(release_pages(m, seq));
+  m->seqs[seq].live = false;
+  return DLS_OK;
+}
+
+int32_t dls_seq_length(const dls_model* m, int32_t seq) {
+  if (!m || seq < 0 || seq >= m->max_seqs || !m->seqs[seq].live) return DLS_ERR_ARG;
+  return m->seqs[seq].len;
+}
+
+int dls_prefill(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  TRY(check_seq(m, seq));
+  if (n < 1 || !tokens) return fail(m, DLS_ERR_ARG, "n=%d tokens=%p", n, (const void*)tokens);
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= m->V) return fail(m, DLS_ERR_ARG, "token[%d]=%d vocab=%d", i, tokens[i], m->V);
+  Seq& s = m->seqs[seq];
+  if ((long long)s.len + n > m->max_ctx)
+    return fail(m, DLS_ERR_CAPACITY, "seq=%d length=%d n=%d max_ctx=%d", seq, s.len, n, m->max_ctx);
+  TRY(ensure_pages(m, seq, s.len + n));
+  for (int i = 0; i < n; ++i) {
+    const int32_t pos = s.len + i;
+    TRY(set_params(m, 1, &seq, &tokens[i], &pos, i == 0));
+    const bool last = i == n - 1;
+    TRY(run_step(m, 1, last && logits_out != nullptr, false));
+  }
+  TRY(copy_out(m, logits_out, m->logits, (size_t)m->V * sizeof(float)));
+  TRY(sync_stream(m, m->stream));
+  TRY(check_status(m));
+  s.len += n;
+  return DLS_OK;
+}
+
+int dls_decode_step(dls_model* m, int32_t seq, int32_t token, int32_t pos, float* logits_out) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  TRY(check_seq(m, seq));
+  if (token < 0 || token >= m->V) return fail(m, DLS_ERR_ARG, "token=%d vocab=%d", token, m->V);
+  Seq& s = m->seqs[seq];
+  if (pos != s.len) return fail(m, DLS_ERR_STATE, "seq=%d pos=%d length=%d", seq, pos, s.len);
+  if (pos >= m->max_ctx) return fail(m, DLS_ERR_CAPACITY, "seq=%d pos=%d max_ctx=%d", seq, pos, m->max_ctx);
+  TRY(ensure_pages(m, seq, pos + 1));
+  TRY(set_params(m, 1, &seq, &token, &pos, true));
+  TRY(run_step(m, 1, logits_out != nullptr, false));
+  TRY(copy_out(m, logits_out, m->logits, (size_t)m->V * sizeof(float)));
+  s.len += 1;
+  return DLS_OK;
+}
+
+int dls_decode_batch(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* tokens, const int32_t* pos,
+                     float* logits_out) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (n < 1 || n > m->max_batch || !seqs || !tokens || !pos)
+    return fail(m, DLS_ERR_ARG, "n=%d max_batch=%d", n, m->max_batch);
+  for (int i = 0; i < n; ++i) {
+    TRY(check_seq(m, seqs[i]));
+    for (int j = 0; j < i; ++j)
+      if (seqs[j] == seqs[i]) return fail(m, DLS_ERR_ARG, "seq=%d repeated", seqs[i]);
+    if (tokens[i] < 0 || tokens[i] >= m->V) return fail(m, DLS_ERR_ARG, "token[%d]=%d", i, tokens[i]);
+    if (pos[i] != m->seqs[seqs[i]].len)
+      return fail(m, DLS_ERR_STATE, "seq=%d pos=%d length=%d", seqs[i], pos[i], m->seqs[seqs[i]].len);
+    if (pos[i] >= m->max_ctx) return fail(m, DLS_ERR_CAPACITY, "seq=%d pos=%d", seqs[i], pos[i]);
+  }
+  int need = 0;
+  for (int i = 0; i < n; ++i)
+    need += std::max(0, pages_needed(m, pos[i] + 1) - (int)m->seqs[seqs[i]].pages.size());
+  if (need > (int)m->free_pages.size()) return fail(m, DLS_ERR_CAPACITY, "need_pages=%d free=%zu", need, m->free_pages.size());
+  for (int i = 0; i < n; ++i) TRY(ensure_pages(m, seqs[i], pos[i] + 1));
+  TRY(set_params(m, n, seqs, tokens, pos, true));
+  TRY(run_step(m, n, logits_out != nullptr, false));
+  TRY(copy_out(m, logits_out, m->logits, (size_t)n * m->V * sizeof(float)));
+  for (int i = 0; i < n; ++i) m->seqs[seqs[i]].len += 1;
+  return DLS_OK;
+}
+
+int dls_generate(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* tokens, int32_t n_steps,
+                 int32_t* tokens_out, float* last_logits) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (n < 1 || n > m->max_batch || !seqs || !tokens || n_steps < 1 || !tokens_out)
+    return fail(m, DLS_ERR_ARG, "n=%d n_steps=%d", n, n_steps);
+  std::vector<int32_t> pos(n);
+  int need = 0;
+  for (int i = 0; i < n; ++i) {
+    TRY(check_seq(m, seqs[i]));
+    for (int j = 0; j < i; ++j)
+      if (seqs[j] == seqs[i]) return fail(m, DLS_ERR_ARG, "seq=%d repeated", seqs[i]);
+    if (tokens[i] < 0 || tokens[i] >= m->V) return fail(m, DLS_ERR_ARG, "token[%d]=%d", i, tokens[i]);
+    pos[i] = m->seqs[seqs[i]].len;
+    if ((long long)pos[i] + n_steps > m->max_ctx)
+      return fail(m, DLS_ERR_CAPACITY, "seq=%d length=%d n_steps=%d max_ctx=%d", seqs[i], pos[i], n_steps, m->max_ctx);
+    need += std::max(0, pages_needed(m, pos[i] + n_steps) - (int)m->seqs[seqs[i]].pages.size());
+  }
+  if (need > (int)m->free_pages.size()) return fail(m, DLS_ERR_CAPACITY, "need_pages=%d free=%zu", need, m->free_pages.size());
+  const size_t ntok = (size_t)n * n_steps;
+  if (ntok > m->tokens_cap) {
+    int32_t* t = nullptr;
+    TRY(dev_alloc_t(m, std::max<size_t>(ntok, 1024), &t, "generated_tokens"));
+    dev_free(m, m->tokens_dev);
+    m->tokens_dev = t;
+    m->tokens_cap = std::max<size_t>(ntok, 1024);
+    drop_graphs(m);  // graphs bake the output pointer in
+  }
+  for (int i = 0; i < n; ++i) TRY(ensure_pages(m, seqs[i], pos[i] + n_steps));
+  TRY(set_params(m, n, seqs, tokens, pos.data(), true));
+  for (int t = 0; t < n_steps; ++t) TRY(run_step(m, n, true, true));
+  CK(cudaMemcpyAsync(tokens_out, m->tokens_dev, ntok * sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
+  TRY(copy_out(m, last_logits, m->logits, (size_t)n * m->V * sizeof(float)));
+  TRY(sync_stream(m, m->stream));
+  TRY(check_status(m));
+  for (int i = 0; i < n; ++i) m->seqs[seqs[i]].len += n_steps;
+  return DLS_OK;
+}
+
+int dls_argmax(dls_model* m, const float* logits, int32_t n_rows, int32_t* out) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (!logits || !out || n_rows < 1 || n_rows > 4096) return fail(m, DLS_ERR_ARG, "n_rows=%d", n_rows);
+  CK(launch_argmax(logits, m->V, n_rows, m->argmax_buf, m->stream, false));
+  TRY(copy_out(m, out, m->argmax_buf, (size_t)n_rows * sizeof(int32_t)));
+  return DLS_OK;
+}
+
+int dls_kv_fork(dls_model* m, int32_t src, const int32_t* dsts, int32_t n_dst) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  TRY(check_seq(m, src));
+  if (n_dst < 1 || !dsts) return fail(m, DLS_ERR_ARG, "n_dst=%d", n_dst);
+  for (int i = 0; i < n_dst; ++i) {
+    TRY(check_seq(m, dsts[i]));
+    if (dsts[i] == src) return fail(m, DLS_ERR_ARG, "dst=%d equals src", dsts[i]);
+    for (int j = 0; j < i; ++j)
+      if (dsts[j] == dsts[i]) return fail(m, DLS_ERR_ARG, "dst=%d repeated", dsts[i]);
+  }
+  const int len = m->seqs[src].len;
+  const int np = pages_needed(m, len);
+  // capacity: the destinations' own pages come back to the pool first
+  size_t avail = m->free_pages.size();
+  for (int i = 0; i < n_dst; ++i) avail += m->seqs[dsts[i]].pages.size();
+  if ((size_t)np * n_dst > avail)
+    return fail(m, DLS_ERR_CAPACITY, "src=%d length=%d pages_per_branch=%d branches=%d free_pages=%zu", src, len, np,
+                n_dst, avail);
+  if ((size_t)np * n_dst > m->pairs_cap)
+    return fail(m, DLS_ERR_CAPACITY, "copy list %zu > %zu", (size_t)np * n_dst, m->pairs_cap);
+  std::vector<int2> pairs;
+  for (int i = 0; i < n_dst; ++i) {
+    TRY(release_pages(m, dsts[i]));
+    TRY(ensure_pages(m, dsts[i], len));
+    for (int k = 0; k < np; ++k) pairs.push_back(make_int2(m->seqs[src].pages[k], m->seqs[dsts[i]].pages[k]));
+  }
+  if (!pairs.empty()) {
+    CK(cudaMemcpyAsync(m->pairs_dev, pairs.data(), pairs.size() * sizeof(int2), cudaMemcpyHostToDevice, m->stream));
+    CK(launch_kv_copy(m->k_pool, m->v_pool, m->kv_layer_elems, m->L, m->page_elems, m->pairs_dev, (int)pairs.size(),
+                      m->stream));
+    TRY(sync_stream(m, m->stream));  // pairs is a pageable host vector
+  }
+  for (int i = 0; i < n_dst; ++i) m->seqs[dsts[i]].len = len;
+  return DLS_OK;
+}
+
+int dls_set_resident_layers(dls_model* m, int32_t n) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (n < -1 || n > m->L) return fail(m, DLS_ERR_ARG, "n=%d n_layers=%d", n, m->L);
+  const uint64_t lb = a256(m->lay.bytes);
+  uint64_t cur_layers = 0;
+  for (auto* p : m->layer_dev)
+    if (p) cur_layers += lb;
+  const uint64_t cur_stage = m->stage[0] ? staging_bytes(m) : 0;
+  const uint64_t other = m->used - cur_layers - cur_stage;
+  if (n == -1) {
+    n = auto_resident(m, other);
+    if (n < 0) return fail(m, DLS_ERR_BUDGET, "no layout fits budget=%llu", (unsigned long long)m->budget);
+  }
+  const uint64_t want = other + (uint64_t)n * lb + (n < m->L ? staging_bytes(m) : 0);
+  if (m->budget && want > m->budget)
+    return fail(m, DLS_ERR_BUDGET, "resident=%d needs=%llu budget=%llu", n, (unsigned long long)want,
+                (unsigned long long)m->budget);
+  if (n == m->resident) return DLS_OK;
+  return apply_resident(m, n);
+}
+
+int dls_debug_capture(dls_model* m, float* per_layer_out) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  m->capture = per_layer_out;
+  return DLS_OK;
+}
+
+int dls_debug_read_kv(dls_model* m, int32_t seq, int32_t layer, void* k_out, void* v_out) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  TRY(check_seq(m, seq));
+  if (layer < 0 || layer >= m->L || !k_out || !v_out) return fail(m, DLS_ERR_ARG, "layer=%d", layer);
+  const Seq& s = m->seqs[seq];
+  if (s.len == 0) return DLS_OK;
+  const __half* kp = m->k_pool + (size_t)layer * m->kv_layer_elems;
+  const __half* vp = m->v_pool + (size_t)layer * m->kv_layer_elems;
+  const int32_t* pages = m->pt_dev + (size_t)seq * m->max_pages;
+  CK(launch_kv_gather(kp, pages, s.len, m->nkv, m->pt, m->hd, static_cast<__half*>(k_out), m->stream));
+  CK(launch_kv_gather(vp, pages, s.len, m->nkv, m->pt, m->hd, static_cast<__half*>(v_out), m->stream));
+  return DLS_OK;
+}
+
+static int find_matrix(dls_model* m, int32_t layer, int32_t tensor, MatDev* out) {
+  if (tensor == 7) {
+    *out = mat_at(m->emb_block, m->emb_off);
+    return DLS_OK;
+  }
+  if (tensor == 8) {
+    *out = head_mat(m);
+    return DLS_OK;
+  }
+  if (tensor < 0 || tensor > 8 || layer < 0 || layer >= m->L) return fail(m, DLS_ERR_ARG, "layer=%d tensor=%d", layer, tensor);
+  const uint8_t* base = m->layer_dev[layer];
+  if (!base) return fail(m, DLS_ERR_STATE, "layer=%d is not resident", layer);
+  switch (tensor) {
+    case 0: *out = mat_at(base, m->lay.qkv, 0, m->q_rows); break;
+    case 1: *out = mat_at(base, m->lay.qkv, m->q_rows, m->kv_rows); break;
+    case 2: *out = mat_at(base, m->lay.qkv, m->q_rows + m->kv_rows, m->kv_rows); break;
+    case 3: *out = mat_at(base, m->lay.o); break;
+    case 4: *out = mat_at(base, m->lay.gu, 0, m->F); break;
+    case 5: *out = mat_at(base, m->lay.gu, m->F, m->F); break;
+    case 6: *out = mat_at(base, m->lay.down); break;
+  }
+  return DLS_OK;
+}
+
+int dls_debug_dequant(dls_model* m, int32_t layer, int32_t tensor, float* out) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (!out) return fail(m, DLS_ERR_ARG, "out=NULL");
+  MatDev md;
+  TRY(find_matrix(m, layer, tensor, &md));
+  CK(launch_dequant(md, m->wtype, out, m->stream));
+  return DLS_OK;
+}
+
+int dls_debug_gemv(dls_model* m, int32_t layer, int32_t tensor, const float* x, float* y) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (!x || !y) return fail(m, DLS_ERR_ARG, "x/y NULL");
+  MatDev md;
+  TRY(find_matrix(m, layer, tensor, &md));
+  GemvArgs g{};
+  g.w = md;
+  g.unit = 1;
+  g.x = x;
+  g.y = y;
+  const GemvLaunch l = gemv_plan(m->wtype, md.rows, md.nb, m->num_sms, 1);
+  CK(launch_gemv(m->wtype, PRO_COPY, EPI_STORE, g, l, m->stream, false));
+  return DLS_OK;
+}
+
+}  // extern "C"

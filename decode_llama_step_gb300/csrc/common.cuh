@@ -1,0 +1,120 @@
+// Shared device helpers and launch structures of the decode-step library.
+// sm_103a only: packed fp32 (f32x2) arithmetic, programmatic dependent launch
+// (griddepcontrol), bulk L2 prefetch, non-allocating streaming loads.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dls {
+
+constexpr int kMaxBatch = 8;
+
+// Per-step inputs read by the kernels from device memory, so that one
+// captured CUDA graph serves every position.  Written by set_params_kernel
+// (decode) or advanced in place by argmax_kernel (greedy generation).
+struct StepParams {
+  int32_t n;                   // batch rows in this step
+  int32_t token[kMaxBatch];
+  int32_t pos[kMaxBatch];      // position of the new token (= KV length before the step)
+  int32_t seq[kMaxBatch];
+  int32_t step;                // generation step counter (argmax output slot)
+  int32_t status;              // nonzero: a kernel saw an invalid index (bit flags)
+};
+
+enum StatusBits : int32_t {
+  kBadPage = 1,   // page table entry missing for a position being written/read
+  kBadToken = 2,  // token id outside [0, vocab)
+  kBadPos = 4,    // position outside the rope table / context
+};
+
+// One weight matrix in the kernels' layout: codes and fp16 scales in two
+// arrays ("structure of arrays") so each lane's 16-byte load is aligned.
+//   Q8_0: qs int8 [rows][nb*32]          d fp16 [rows][nb]
+//   Q4_0: qs u8   [rows][nb][16] (GGUF nibble order kept)   d fp16 [rows][nb]
+struct MatDev {
+  const uint8_t* qs;
+  const __half* d;
+  int rows, cols, nb;
+};
+
+// ---- small PTX wrappers -----------------------------------------------------
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  // bytes: multiple of 16, address 16-byte aligned
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+typedef unsigned long long f2_t;  // two fp32 lanes in one 64-bit register pair
+
+__device__ __forceinline__ f2_t pk2(float lo, float hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 upk2(f2_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f2_t ffma2(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2_t fadd2(f2_t a, f2_t b) {
+  f2_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ---- exact int8 / int4 -> fp32 --------------------------------------------------
+// A byte b placed in the low byte of the pattern 0x4B0000bb is the float
+// 2^23 + b exactly; subtracting 2^23 + bias recovers the signed code with no
+// rounding.  One PRMT per value and one packed add per two values.
+
+__device__ __forceinline__ float mag_byte(uint32_t u, int k) {
+  return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540 | k));
+}
+
+// four int8 codes (one 32-bit word) -> two packed pairs (q0,q1), (q2,q3)
+__device__ __forceinline__ void i8x4_to_f2(uint32_t w, f2_t& p01, f2_t& p23) {
+  const uint32_t u = w ^ 0x80808080u;  // q + 128 as unsigned bytes
+  const f2_t bias = pk2(-8388736.0f, -8388736.0f);
+  p01 = fadd2(pk2(mag_byte(u, 0), mag_byte(u, 1)), bias);
+  p23 = fadd2(pk2(mag_byte(u, 2), mag_byte(u, 3)), bias);
+}
+
+// four nibble codes already isolated one per byte (values 0..15) -> (n-8)
+__device__ __forceinline__ void u4x4_to_f2(uint32_t b, f2_t& p01, f2_t& p23) {
+  const f2_t bias = pk2(-8388616.0f, -8388616.0f);  // 2^23 + 8
+  p01 = fadd2(pk2(mag_byte(b, 0), mag_byte(b, 1)), bias);
+  p23 = fadd2(pk2(mag_byte(b, 2), mag_byte(b, 3)), bias);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace dls

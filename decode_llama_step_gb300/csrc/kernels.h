@@ -1,0 +1,93 @@
+// Host-side launchers of the library's kernels (one declaration per kernel
+// family); the runtime in api.cu composes them into the decode step.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace dls {
+
+enum Pro { PRO_COPY = 0, PRO_RMSNORM = 1, PRO_SWIGLU = 2 };
+enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2 };
+
+// Where a decode row finds its KV pages (model path: row b is sequence
+// sp->seq[b] at position sp->pos[b]).
+struct KvView {
+  __half* k_pool;            // layer base, [n_pages][n_kv][page_tokens][head_dim]
+  __half* v_pool;
+  const int32_t* page_table; // [max_seqs][max_pages]
+  int n_kv, head_dim, page_tokens, max_pages;
+};
+
+struct GemvArgs {
+  MatDev w;
+  int unit;                  // rows are split across CTAs in multiples of this
+  const float* x;            // PRO_COPY/RMSNORM: [cols]; PRO_SWIGLU: gate [cols] then up [cols]
+  const float* g;            // RMSNorm gain [cols]
+  float eps;
+  float* y;                  // STORE: y[r] = acc; RESID: y[r] += acc; QKV: q rows -> y
+  // EPI_QKV
+  int q_rows, kv_rows;
+  KvView kv;
+  const float2* rope_cs;     // [rope_len][head_dim/2] cos, sin
+  int rope_len;
+  StepParams* sp;
+  int brow;                  // batch row of sp this launch serves
+};
+
+struct GemvLaunch {
+  int grid, threads, smem;
+};
+
+// Choose grid/threads/smem for a matrix and check the kernel can run it.
+GemvLaunch gemv_plan(int wtype, int rows, int nb, int num_sms, int unit);
+cudaError_t gemv_setup_attributes();   // raise dynamic smem limits once
+cudaError_t launch_gemv(int wtype, int pro, int epi, const GemvArgs& a, const GemvLaunch& l, cudaStream_t s,
+                        bool pdl);
+
+// ---- attention ------------------------------------------------------------------
+
+struct AttnArgs {
+  const float* q;            // [rows of this launch][n_heads*head_dim]
+  float* o;                  // [rows of this launch][n_heads*head_dim]
+  const __half* k_pool;
+  const __half* v_pool;
+  const int32_t* page_table; // rows of max_pages entries
+  int max_pages;
+  const int32_t* pt_row;     // page-table row per batch row (NULL: row b)
+  const int32_t* len;        // per batch row: keys attended = len[b] + len_add
+  int len_add;
+  int n_heads, n_kv, head_dim, page_tokens;
+  int n_splits;
+  int row0;                  // first batch row of this launch
+  float* part_o;             // scratch
+  float* part_ml;
+  int* counters;             // [rows][n_kv], zero between launches
+  int32_t* status;           // optional status word (may be NULL)
+  int max_len;               // upper bound on keys (guards page-table reads)
+};
+
+size_t attn_workspace_bytes(int rows, int n_heads, int n_kv, int head_dim, int n_splits);
+void attn_workspace_carve(void* ws, int rows, int n_heads, int n_kv, int head_dim, int n_splits, float** part_o,
+                          float** part_ml, int** counters);
+int attn_default_splits(int rows, int n_kv, int num_sms, int max_len);
+cudaError_t launch_attention(const AttnArgs& a, int rows, cudaStream_t s, bool pdl);
+
+// ---- small kernels --------------------------------------------------------------
+
+cudaError_t launch_embed(const MatDev& emb, int wtype, StepParams* sp, int brow, float* x, int vocab,
+                         cudaStream_t s, bool pdl);
+cudaError_t launch_argmax(const float* logits, int vocab, int rows, int32_t* out, cudaStream_t s, bool pdl);
+cudaError_t launch_advance(StepParams* sp, const int32_t* next, int32_t* tokens_out, int rows, cudaStream_t s,
+                           bool pdl);
+cudaError_t launch_set_params(StepParams* sp, const StepParams& h, bool reset_step, cudaStream_t s);
+cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, uint8_t* qs, __half* d, cudaStream_t s);
+cudaError_t launch_rope_table(float2* cs, int len, int head_dim, float theta, cudaStream_t s);
+cudaError_t launch_dequant(const MatDev& m, int wtype, float* out, cudaStream_t s);
+// copy whole KV pages: pairs[i] = (src_page, dst_page), for every layer
+cudaError_t launch_kv_copy(__half* k_pool, __half* v_pool, size_t layer_stride_elems, int n_layers,
+                           size_t page_elems, const int2* pairs, int n_pairs, cudaStream_t s);
+cudaError_t launch_kv_gather(const __half* pool, const int32_t* pages, int len, int n_kv, int page_tokens,
+                             int head_dim, __half* out, cudaStream_t s);
+
+}  // namespace dls

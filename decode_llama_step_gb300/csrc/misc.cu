@@ -1,0 +1,260 @@
+// The decode step's small kernels: embedding-row dequant, greedy pick,
+// step-parameter upkeep, weight re-layout, the RoPE sin/cos table, the KV
+// fork copy and test-only gathers.
+#include <math.h>
+
+#include "kernels.h"
+
+namespace dls {
+
+namespace {
+
+cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, cudaStream_t s, bool pdl, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// one dequantised weight: exact in fp32 (11-bit scale times a code of at most 8 bits)
+__device__ __forceinline__ float dq(const MatDev& m, int wtype, int row, int col) {
+  const int blk = col >> 5, e = col & 31;
+  const float d = __half2float(m.d[(size_t)row * m.nb + blk]);
+  if (wtype == 8) {
+    const uint32_t u = (uint32_t)m.qs[(size_t)row * m.nb * 32 + col] ^ 0x80u;
+    return d * (mag_byte(u, 0) - 8388736.0f);
+  }
+  const uint8_t byte = m.qs[((size_t)row * m.nb + blk) * 16 + (e & 15)];
+  const uint32_t nib = e < 16 ? (byte & 15u) : (byte >> 4);
+  return d * (mag_byte(nib, 0) - 8388616.0f);
+}
+
+// ---------------------------------------------------------------- embedding
+
+__global__ void embed_kernel(const MatDev emb, int wtype, StepParams* sp, int brow, float* x, int vocab) {
+  griddep_wait();
+  griddep_launch();
+  int tok = sp->token[brow];
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) atomicOr(&sp->status, kBadToken);
+    tok = 0;
+  }
+  for (int c = threadIdx.x; c < emb.cols; c += blockDim.x) x[c] = dq(emb, wtype, tok, c);
+}
+
+// ---------------------------------------------------------------- greedy pick
+
+__global__ void argmax_kernel(const float* logits, int vocab, int32_t* out) {
+  griddep_wait();
+  griddep_launch();
+  const float* row = logits + (size_t)blockIdx.x * vocab;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = threadIdx.x; i < vocab; i += blockDim.x) {
+    const float v = row[i];
+    if (v > best) {  // strided scan: the first (lowest) index wins ties per thread
+      best = v;
+      bi = i;
+    }
+  }
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) {
+      best = ov;
+      bi = oi;
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    sv[warp] = best;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+      if (sv[w] > best || (sv[w] == best && si[w] < bi)) {
+        best = sv[w];
+        bi = si[w];
+      }
+    out[blockIdx.x] = bi == 0x7fffffff ? 0 : bi;  // all-NaN row: 0
+  }
+}
+
+// next token := argmax, position += 1, record the token for the host
+__global__ void advance_kernel(StepParams* sp, const int32_t* next, int32_t* tokens_out, int rows) {
+  griddep_wait();
+  griddep_launch();
+  const int b = threadIdx.x;
+  const int step = sp->step;
+  __syncthreads();
+  if (b < rows) {
+    sp->token[b] = next[b];
+    sp->pos[b] += 1;
+    if (tokens_out) tokens_out[(size_t)step * rows + b] = next[b];
+  }
+  __syncthreads();
+  if (b == 0) sp->step = step + 1;
+}
+
+__global__ void set_params_kernel(StepParams* sp, const StepParams h, int reset_step) {
+  const int b = threadIdx.x;
+  if (b < kMaxBatch) {
+    sp->token[b] = h.token[b];
+    sp->pos[b] = h.pos[b];
+    sp->seq[b] = h.seq[b];
+  }
+  if (b == 0) {
+    sp->n = h.n;
+    if (reset_step) {
+      sp->step = 0;
+      sp->status = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- weight layout
+
+// GGUF-style blocks (2-byte scale + codes) -> scale array + code array
+__global__ void repack_kernel(const uint8_t* src, int wtype, long long n_blocks, uint8_t* qs, __half* d) {
+  const int bsz = wtype == 8 ? 34 : 18, nq = bsz - 2;
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < n_blocks;
+       b += (long long)gridDim.x * blockDim.x) {
+    const uint8_t* s = src + b * bsz;
+    d[b] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
+    uint8_t* q = qs + b * nq;
+    for (int i = 0; i < nq; ++i) q[i] = s[2 + i];
+  }
+}
+
+// RoPE table: entry (p, i) = (cos, sin) of p * theta^(-2i/hd), computed in
+// fp64 and rounded once to fp32 (the engine page, section 4.4, precomputes
+// the sin/cos table; fp64 keeps angles of up to ~1e4 radians accurate)
+__global__ void rope_table_kernel(float2* cs, int len, int hd, double theta) {
+  const int half = hd / 2;
+  for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < (long long)len * half;
+       k += (long long)gridDim.x * blockDim.x) {
+    const int p = (int)(k / half), i = (int)(k % half);
+    const double ang = (double)p * pow(theta, -2.0 * i / hd);
+    double s, c;
+    sincos(ang, &s, &c);
+    cs[k] = make_float2((float)c, (float)s);
+  }
+}
+
+__global__ void dequant_kernel(const MatDev m, int wtype, float* out) {
+  const long long total = (long long)m.rows * m.cols;
+  for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < total;
+       k += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(k / m.cols), c = (int)(k % m.cols);
+    out[k] = dq(m, wtype, r, c);
+  }
+}
+
+// ---------------------------------------------------------------- KV fork copy
+
+// Whole pages, every layer, K and V: a plain 16-byte vector copy (HBM-bound).
+// blockIdx.y = pair, blockIdx.z = layer*2 + (0: K, 1: V).
+__global__ void kv_copy_kernel(__half* k_pool, __half* v_pool, size_t layer_stride, size_t page_elems,
+                               const int2* pairs) {
+  const int2 pr = pairs[blockIdx.y];
+  const int layer = blockIdx.z >> 1;
+  __half* pool = (blockIdx.z & 1) ? v_pool : k_pool;
+  const uint4* src = reinterpret_cast<const uint4*>(pool + layer * layer_stride + (size_t)pr.x * page_elems);
+  uint4* dst = reinterpret_cast<uint4*>(pool + layer * layer_stride + (size_t)pr.y * page_elems);
+  const size_t n16 = page_elems * sizeof(__half) / 16;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = __ldcs(src + i);
+}
+
+__global__ void kv_gather_kernel(const __half* pool, const int32_t* pages, int len, int n_kv, int pt, int hd,
+                                 __half* out) {
+  const long long total = (long long)len * n_kv * hd;
+  for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < total;
+       k += (long long)gridDim.x * blockDim.x) {
+    const int dim = (int)(k % hd);
+    const int h = (int)((k / hd) % n_kv);
+    const int p = (int)(k / ((long long)hd * n_kv));
+    const int page = pages[p / pt];
+    out[k] = pool[(((size_t)page * n_kv + h) * pt + (p % pt)) * hd + dim];
+  }
+}
+
+int grid_for(long long n, int threads) {
+  long long g = (n + threads - 1) / threads;
+  if (g > 4096) g = 4096;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_embed(const MatDev& emb, int wtype, StepParams* sp, int brow, float* x, int vocab,
+                         cudaStream_t s, bool pdl) {
+  MatDev e = emb;
+  void* args[] = {&e, &wtype, &sp, &brow, &x, &vocab};
+  return launch_ex((const void*)embed_kernel, dim3(1), dim3(256), s, pdl, args);
+}
+
+cudaError_t launch_argmax(const float* logits, int vocab, int rows, int32_t* out, cudaStream_t s, bool pdl) {
+  void* args[] = {&logits, &vocab, &out};
+  return launch_ex((const void*)argmax_kernel, dim3(rows), dim3(1024), s, pdl, args);
+}
+
+cudaError_t launch_advance(StepParams* sp, const int32_t* next, int32_t* tokens_out, int rows, cudaStream_t s,
+                           bool pdl) {
+  void* args[] = {&sp, &next, &tokens_out, &rows};
+  return launch_ex((const void*)advance_kernel, dim3(1), dim3(32), s, pdl, args);
+}
+
+cudaError_t launch_set_params(StepParams* sp, const StepParams& h, bool reset_step, cudaStream_t s) {
+  set_params_kernel<<<1, 32, 0, s>>>(sp, h, reset_step ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, uint8_t* qs, __half* d, cudaStream_t s) {
+  const long long n = (long long)rows * nb;
+  repack_kernel<<<grid_for(n, 256), 256, 0, s>>>(src, wtype, n, qs, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* cs, int len, int head_dim, float theta, cudaStream_t s) {
+  rope_table_kernel<<<grid_for((long long)len * head_dim / 2, 256), 256, 0, s>>>(cs, len, head_dim, (double)theta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const MatDev& m, int wtype, float* out, cudaStream_t s) {
+  dequant_kernel<<<grid_for((long long)m.rows * m.cols, 256), 256, 0, s>>>(m, wtype, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_copy(__half* k_pool, __half* v_pool, size_t layer_stride_elems, int n_layers,
+                           size_t page_elems, const int2* pairs, int n_pairs, cudaStream_t s) {
+  if (n_pairs <= 0) return cudaSuccess;
+  const size_t n16 = page_elems * sizeof(__half) / 16;
+  int gx = (int)((n16 + 255) / 256);
+  if (gx > 64) gx = 64;
+  for (int p0 = 0; p0 < n_pairs; p0 += 65535) {  // grid.y limit
+    const int np = n_pairs - p0 < 65535 ? n_pairs - p0 : 65535;
+    kv_copy_kernel<<<dim3(gx, np, 2 * n_layers), 256, 0, s>>>(k_pool, v_pool, layer_stride_elems, page_elems,
+                                                                 pairs + p0);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_gather(const __half* pool, const int32_t* pages, int len, int n_kv, int page_tokens,
+                             int head_dim, __half* out, cudaStream_t s) {
+  kv_gather_kernel<<<grid_for((long long)len * n_kv * head_dim, 256), 256, 0, s>>>(pool, pages, len, n_kv,
+                                                                                 page_tokens, head_dim, out);
+  return cudaGetLastError();
+}
+
+}  // namespace dls

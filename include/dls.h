@@ -1,0 +1,257 @@
+/*
+ * dls.h - C ABI of the GB300 (sm_103a) decode-step library for quantised
+ * Llama-architecture models.
+ *
+ * What it computes (one token per sequence per decode step, every step on
+ * the GPU in this library's own CUDA kernels):
+ *
+ *   x = dequant(tok_embd[token])
+ *   per layer:  xn = rmsnorm(x) * g_attn
+ *               q, k, v = Wq xn, Wk xn, Wv xn            (Q8_0 / Q4_0 dequant-GEMV)
+ *               q, k = rope(q, pos), rope(k, pos)         (adjacent pairs)
+ *               K[pos], V[pos] = fp16(k), fp16(v)         (paged fp16 KV cache)
+ *               o = softmax(q K[0..pos]^T / sqrt(hd)) V   (GQA, causal)
+ *               x += Wo o
+ *               x += Wdown (silu(Wgate xn') * (Wup xn')), xn' = rmsnorm(x) * g_ffn
+ *   logits = Wout (rmsnorm(x) * g_out)                    (Wout = tok_embd if tied)
+ *
+ * Sources, by page and section: the pure C + CUDA LLM inference engine page
+ * (rskf.cn), section 1 (Llama architecture with RoPE, GQA, SwiGLU, RMSNorm and
+ * a KV cache; Q4_0 and Q8_0 weights; 8B Q8_0 resident decode) and section 4.4
+ * (single-token GEMV, fused RMSNorm, RoPE with a precomputed sin/cos table,
+ * SwiGLU fused with the projection, causal softmax with the mask inside);
+ * sections 3.3 and 4.2 (two-buffer layer streaming, SLEP) and 4.1 (the
+ * resident-layer count from the device budget); the "3 Agents. 3 LLMs. 1 Aging
+ * GPU" page (LayerStreamer: pinned host region, two device buffers, two
+ * streams, per-layer events; the admission ledger that reserves before it
+ * allocates and rolls back on failure); the SwarmKV page ("Prefill once, fan
+ * out"), sections 2-4 (prefill fills the KV cache once, the snapshot is copied
+ * per branch, branches continue RoPE at the prefix length, the context budget
+ * is checked before anything is allocated, a restore must match the snapshot
+ * size exactly).
+ *
+ * Conventions
+ *  - Every call is ordered on the model's CUDA stream.  A model handle is not
+ *    thread-safe: use it from one host thread at a time.
+ *  - Status codes: DLS_OK (0) or a negative dls_status.  A failed call leaves
+ *    the model as it was (sequences, lengths, resident layers), except
+ *    DLS_ERR_CUDA, after which the model should be destroyed.
+ *  - dls_last_error() returns "ERR <CODE> key=value ..." for the last failed
+ *    call on that model (or, for a NULL model, on the calling thread).
+ *  - Pointers marked "host" are host memory; "device" are device memory of
+ *    the model's GPU; "host or device" accepts either (detected per call).
+ *  - Nothing here traps or asserts on the device: kernels that detect a bad
+ *    index or a wait that runs out record it in a status word that the host
+ *    reads, and the call returns DLS_ERR_STATE or DLS_ERR_TIMEOUT.
+ */
+#ifndef DLS_H
+#define DLS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DLS_ABI_VERSION 1
+#define DLS_MAX_BATCH 8
+
+typedef struct dls_model dls_model;
+
+typedef enum dls_status {
+  DLS_OK = 0,
+  DLS_ERR_ARG = -1,      /* bad argument or descriptor */
+  DLS_ERR_BUDGET = -2,   /* the device budget (ledger) cannot hold the request */
+  DLS_ERR_CAPACITY = -3, /* out of sequences, KV pages or context */
+  DLS_ERR_CUDA = -4,     /* a CUDA call failed */
+  DLS_ERR_TIMEOUT = -5,  /* a bounded wait ran out */
+  DLS_ERR_STATE = -6     /* call does not fit the model's state (e.g. pos != length) */
+} dls_status;
+
+/* Weight block formats (as the workloads define them):
+ *  DLS_Q8_0: 34-byte block = little-endian fp16 d, 32 x int8 q;  w = d*q
+ *  DLS_Q4_0: 18-byte block = fp16 d, 16 bytes; byte j = element j (low
+ *            nibble) and element j+16 (high nibble); w = d*(nibble - 8)
+ * A matrix [rows x in] is row-major with ceil(in/32) blocks per row; columns
+ * past `in` in the last block must be zero weights. */
+typedef enum dls_wtype { DLS_Q4_0 = 4, DLS_Q8_0 = 8 } dls_wtype;
+
+/* Device memory source.  alloc returns device memory of at least `bytes`
+ * (256-byte aligned) or NULL; free releases it.  `stream` is the model's
+ * cudaStream_t.  Pass NULL for the allocator to use cudaMalloc/cudaFree.
+ * Every byte the library holds on the device goes through this, and is
+ * counted by the model's budget ledger. */
+typedef struct dls_allocator {
+  void* (*alloc)(void* ctx, size_t bytes, void* stream);
+  void (*free)(void* ctx, void* ptr, void* stream);
+  void* ctx;
+} dls_allocator;
+
+/* One layer's weights, all host memory, read only during dls_model_create. */
+typedef struct dls_layer_desc {
+  const float* attn_norm; /* fp32 [hidden] */
+  const float* ffn_norm;  /* fp32 [hidden] */
+  const void* wq;         /* blocks [n_heads*head_dim x hidden] */
+  const void* wk;         /* blocks [n_kv_heads*head_dim x hidden] */
+  const void* wv;         /* blocks [n_kv_heads*head_dim x hidden] */
+  const void* wo;         /* blocks [hidden x n_heads*head_dim] */
+  const void* w_gate;     /* blocks [ffn x hidden] */
+  const void* w_up;       /* blocks [ffn x hidden] */
+  const void* w_down;     /* blocks [hidden x ffn] (ffn padded to 32 with zero weights) */
+} dls_layer_desc;
+
+typedef struct dls_model_desc {
+  int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  float rope_theta; /* RoPE base; pair i of a head rotates by pos * theta^(-2i/head_dim) */
+  float rms_eps;    /* RMSNorm epsilon */
+  int32_t tied_embeddings; /* nonzero: the LM head is tok_embd, `output` is ignored */
+  int32_t wtype;           /* dls_wtype of every matrix */
+  int32_t page_tokens;     /* KV page size in tokens: 32, 64, 128 or 256; 0 = 64 */
+  int32_t max_seqs;        /* sequences the KV pool serves (>= 1) */
+  int32_t max_ctx;         /* tokens per sequence (>= 1) */
+  int32_t max_batch;       /* largest n of dls_decode_batch, 1..DLS_MAX_BATCH; 0 = 1 */
+  uint64_t device_budget_bytes; /* cap on library device memory; 0 = no cap */
+  const void* tok_embd;    /* host blocks [vocab x hidden] */
+  const void* output;      /* host blocks [vocab x hidden], or NULL when tied */
+  const float* output_norm;/* host fp32 [hidden] */
+  const dls_layer_desc* layers; /* host array [n_layers] */
+} dls_model_desc;
+
+/* ---- model ------------------------------------------------------------- */
+
+/* Validate `desc`, place the weights (re-laid-out for the kernels) and the
+ * paged KV pool on the device, and return a model in *out.
+ * Shapes: hidden, n_heads*head_dim and ffn multiples of 32 are not required
+ * except hidden % 32 == 0 and head_dim even, head_dim <= 256, n_heads a
+ * multiple of n_kv_heads.  With device_budget_bytes set, as many layers as
+ * fit stay resident (first layers first) and the rest are streamed from
+ * pinned host memory each step; DLS_ERR_BUDGET if not even that fits.
+ * `cuda_stream` (cudaStream_t) orders all work; NULL makes a private stream.
+ * The caller keeps ownership of every desc buffer (they are copied). */
+int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator, void* cuda_stream,
+                     dls_model** out);
+void dls_model_destroy(dls_model* m);
+
+/* Device bytes the ledger holds for this model, and its cap (0 = none). */
+uint64_t dls_device_bytes(const dls_model* m);
+uint64_t dls_device_budget(const dls_model* m);
+
+/* ---- sequences ---------------------------------------------------------- */
+
+/* Claim a free sequence id in [0, max_seqs).  It starts empty (length 0) and
+ * holds no KV pages until tokens are written.  DLS_ERR_CAPACITY if none free. */
+int dls_seq_create(dls_model* m, int32_t* seq_out);
+/* Release a sequence and its KV pages. */
+int dls_seq_free(dls_model* m, int32_t seq);
+/* Tokens held in the sequence's KV cache, or a negative status. */
+int32_t dls_seq_length(const dls_model* m, int32_t seq);
+
+/* ---- the hot path --------------------------------------------------------- */
+
+/* Run n prompt tokens (host int32 [n], each in [0, vocab)) through every
+ * layer at positions length..length+n-1 of `seq`, filling its KV cache.
+ * logits_out (host or device fp32 [vocab], or NULL) receives the logits of
+ * the last token.  DLS_ERR_CAPACITY if length + n > max_ctx. */
+int dls_prefill(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out);
+
+/* One decode step: `token` at position `pos`, which must equal the
+ * sequence's length (else DLS_ERR_STATE: a fork must continue at the prefix
+ * length).  Appends the token's K/V and writes logits (host or device fp32
+ * [vocab]; NULL skips the copy-out). */
+int dls_decode_step(dls_model* m, int32_t seq, int32_t token, int32_t pos, float* logits_out);
+
+/* n decode steps in one pass over the weights (1 <= n <= max_batch): row i
+ * is token tokens[i] of sequence seqs[i] at position pos[i] (host arrays;
+ * distinct sequences).  logits_out: host or device fp32 [n][vocab] or NULL. */
+int dls_decode_batch(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* tokens, const int32_t* pos,
+                     float* logits_out);
+
+/* Greedy generation kept on the device: n_steps decode steps of sequences
+ * seqs[0..n-1] starting from tokens[i] at each sequence's end; each step's
+ * argmax (lowest index on ties) is the next step's token.  tokens_out (host
+ * int32 [n_steps][n]) receives the chosen tokens; last_logits (host or
+ * device fp32 [n][vocab], or NULL) the final step's logits. */
+int dls_generate(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* tokens, int32_t n_steps,
+                 int32_t* tokens_out, float* last_logits);
+
+/* Greedy pick per row: out[i] = argmax logits[i][0..vocab) (lowest index on
+ * ties).  logits: device fp32 [n_rows][vocab]; out: host or device int32. */
+int dls_argmax(dls_model* m, const float* logits, int32_t n_rows, int32_t* out);
+
+/* KV fork: copy the first length(src) positions of every layer's K and V of
+ * `src_seq` into each destination sequence (bit-exact device-to-device copy)
+ * and set each destination's length to length(src).  Destinations must be
+ * distinct live sequences other than src; their previous contents are
+ * dropped.  DLS_ERR_CAPACITY if the KV pool cannot hold the copies. */
+int dls_kv_fork(dls_model* m, int32_t src_seq, const int32_t* dst_seqs, int32_t n_dst);
+
+/* Context-budget check done before any allocation (SwarmKV page, section 4,
+ * step 0): DLS_OK if prefix_tokens + max_branch_tokens + headroom <= n_ctx,
+ * else DLS_ERR_CAPACITY with the numbers in dls_last_error(NULL). */
+int dls_check_context_budget(int32_t prefix_tokens, int32_t max_branch_tokens, int32_t headroom, int32_t n_ctx);
+
+/* ---- layer residency and streaming ----------------------------------------- */
+
+/* Keep layers [0, n) resident on the device and stream layers [n, n_layers)
+ * from pinned host memory through two device buffers on a copy stream,
+ * overlapped with compute.  n = -1 picks the largest n the budget allows.
+ * DLS_ERR_BUDGET (model unchanged) if the layout does not fit the budget. */
+int dls_set_resident_layers(dls_model* m, int32_t n);
+int32_t dls_resident_layers(const dls_model* m);
+/* Bytes of one layer's weights as the kernels read them (the per-layer H2D
+ * transfer of a streamed layer). */
+uint64_t dls_layer_bytes(const dls_model* m);
+
+/* ---- standalone op ----------------------------------------------------------- */
+
+/* Split-K (flash-decoding) GQA attention of one query position over an fp16
+ * paged KV cache, for `n_batch` independent rows.  All pointers device:
+ *   q         fp32 [n_batch][n_heads][head_dim] (already rotated)
+ *   k_pages,  fp16 pools [n_pages][n_kv_heads][page_tokens][head_dim]
+ *   v_pages
+ *   page_table int32 [n_batch][max_pages]: logical page -> physical page
+ *   lengths   int32 [n_batch]: keys 0..lengths[b]-1 are attended (>= 1)
+ *   o         fp32 [n_batch][n_heads][head_dim]
+ *   workspace scratch of dls_attention_workspace_bytes(...) bytes; its
+ *             counter words must be zero before the first call (the call
+ *             leaves them zero again).
+ * `n_splits` = how many CTAs share one (row, kv head); 0 = choose.  Returns
+ * DLS_ERR_ARG on a bad shape.  cuda_stream orders the work. */
+int dls_attention_decode(const float* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                         const int32_t* lengths, float* o, void* workspace, size_t workspace_bytes,
+                         int32_t n_batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                         int32_t page_tokens, int32_t max_pages, int32_t n_splits, void* cuda_stream);
+size_t dls_attention_workspace_bytes(int32_t n_batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                     int32_t n_splits);
+
+/* ---- test and profiling hooks ------------------------------------------------ */
+
+/* Arm a capture of the residual stream after every layer for the next
+ * decode call (batch row 0): per_layer_out device fp32 [n_layers][hidden].
+ * NULL disarms.  The captured call runs without CUDA-graph replay. */
+int dls_debug_capture(dls_model* m, float* per_layer_out);
+/* Copy positions [0, length) of one layer's K and V of `seq` into device
+ * fp16 [length][n_kv_heads][head_dim] buffers. */
+int dls_debug_read_kv(dls_model* m, int32_t seq, int32_t layer, void* k_out, void* v_out);
+/* Dequantise one weight matrix as the kernels see it into device fp32
+ * [rows][cols].  tensor: 0 wq, 1 wk, 2 wv, 3 wo, 4 w_gate, 5 w_up, 6 w_down,
+ * 7 tok_embd, 8 output (layer ignored for 7 and 8). */
+int dls_debug_dequant(dls_model* m, int32_t layer, int32_t tensor, float* out);
+/* y = W x with the decode GEMV kernel for one matrix (ids as above);
+ * x device fp32 [cols], y device fp32 [rows]. */
+int dls_debug_gemv(dls_model* m, int32_t layer, int32_t tensor, const float* x, float* y);
+/* Kernel launches issued by the last decode / generate step (all of this
+ * library's kernels, per step). */
+int32_t dls_debug_launches_per_step(const dls_model* m);
+
+/* ---- errors -------------------------------------------------------------------- */
+
+const char* dls_last_error(const dls_model* m);
+const char* dls_status_name(int status);
+int dls_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DLS_H */

@@ -1,0 +1,294 @@
+"""GPU parity on the tiny configuration (2 layers, hidden 256, 4/2 heads,
+head_dim 64, FFN 688, vocab 1024, Q8_0) and a Q4_0 twin, through the C ABI.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import OracleModel, ops, quant
+from synth.configs import ModelConfig
+
+from parity import assert_close, check_greedy
+
+pytestmark = pytest.mark.gpu
+
+TINY = synth.get_config("tiny")
+TINY_Q4 = ModelConfig("tinyq4", 2, 256, 4, 2, 64, 688, 1024, 10000.0, 4, 0.02)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+@pytest.fixture(scope="module", params=[TINY, TINY_Q4], ids=["q8_0", "q4_0"])
+def setup(request, gpu_lib):
+    torch = _torch()
+    from decode_llama_step_gb300 import dls
+    cfg = request.param
+    w = synth.model_weights(cfg)
+    stream = torch.cuda.Stream()
+    m = dls.Model(cfg, w, max_seqs=6, max_ctx=160, max_batch=4, page_tokens=32, stream=stream)
+    orc = OracleModel(cfg, w)
+    yield cfg, w, m, orc, stream
+    m.close()
+
+
+def test_dequant_bit_exact(setup):
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    shapes = synth.matrix_shapes(cfg)
+    for l in range(cfg.n_layers):
+        for name in synth.LAYER_MATRICES:
+            rows, cols = shapes[name]
+            out = torch.empty(rows, cols, device="cuda")
+            m.debug_dequant(l, name, out)
+            stream.synchronize()
+            ref = quant.matrix(w["layers"][l][name], rows, cols, cfg.wtype)
+            got = out.cpu().numpy().astype(np.float64)
+            assert np.array_equal(got, ref), f"layer {l} {name}"
+    for name in ("tok_embd", "output"):
+        out = torch.empty(cfg.vocab, cfg.hidden, device="cuda")
+        m.debug_dequant(0, name, out)
+        stream.synchronize()
+        ref = quant.matrix(w[name], cfg.vocab, cfg.hidden, cfg.wtype)
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), ref), name
+
+
+def test_gemv_every_matrix(setup):
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    shapes = synth.matrix_shapes(cfg)
+    shapes["output"] = (cfg.vocab, cfg.hidden)
+    for name, (rows, cols) in shapes.items():
+        x = synth.normal(synth.stream_key("gemv-x", name), cols, 1.0).astype(np.float32)
+        xd = torch.from_numpy(x).cuda()
+        y = torch.empty(rows, device="cuda")
+        m.debug_gemv(1, name, xd, y)
+        stream.synchronize()
+        ref = orc.matmul(1 if name != "output" else None, name, x.astype(np.float64))
+        # fp32 accumulation over <= 704 terms: far inside the layer tolerance
+        assert_close(y.cpu().numpy(), ref, f"gemv {name}", tol=1e-5)
+
+
+def _run_against_oracle(cfg, m, orc, n_prompt, n_decode, seed=1):
+    torch = _torch()
+    prompt = synth.prompt_tokens(cfg, n_prompt, seed=seed)
+    seq = m.seq_create()
+    try:
+        logits = torch.empty(cfg.vocab, device="cuda")
+        cap = torch.empty(cfg.n_layers, cfg.hidden, device="cuda")
+        m.prefill(seq, prompt, logits)
+        oseq = orc.new_seq()
+        ref = orc.prefill(oseq, prompt)
+        assert_close(logits.cpu().numpy(), ref, "prefill logits")
+        tok = check_greedy(logits.cpu().numpy(), ref, "prefill")
+        for i in range(n_decode):
+            pos = n_prompt + i
+            m.debug_capture(cap)
+            m.decode_step(seq, tok, pos, logits)
+            ocap = []
+            ref = orc.decode_step(oseq, tok, pos, capture=ocap)
+            got_cap = cap.cpu().numpy()
+            for l in range(cfg.n_layers):
+                assert_close(got_cap[l], ocap[l], f"step {i} layer {l} residual")
+            assert_close(logits.cpu().numpy(), ref, f"step {i} logits")
+            tok = check_greedy(logits.cpu().numpy(), ref, f"step {i}")
+        assert m.seq_length(seq) == n_prompt + n_decode
+    finally:
+        m.seq_free(seq)
+
+
+def test_prefill_and_greedy_decode_parity(setup):
+    cfg, w, m, orc, stream = setup
+    _run_against_oracle(cfg, m, orc, 16, 32)
+
+
+def test_decode_across_page_boundaries(setup):
+    # 32-token pages: positions 31/32/33 and 63/64/65 cross pages
+    cfg, w, m, orc, stream = setup
+    _run_against_oracle(cfg, m, orc, 30, 37, seed=5)
+
+
+def test_graph_replay_matches_eager(setup):
+    # decode without capture runs the captured CUDA graph; with capture armed
+    # it runs eagerly: both must give identical bits
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    prompt = synth.prompt_tokens(cfg, 9, seed=3)
+    a, b = m.seq_create(), m.seq_create()
+    try:
+        la = torch.empty(cfg.vocab, device="cuda")
+        lb = torch.empty(cfg.vocab, device="cuda")
+        m.prefill(a, prompt)
+        m.prefill(b, prompt)
+        cap = torch.empty(cfg.n_layers, cfg.hidden, device="cuda")
+        m.decode_step(a, 7, 9, la)
+        m.debug_capture(cap)
+        m.decode_step(b, 7, 9, lb)
+        stream.synchronize()
+        assert torch.equal(la, lb)
+    finally:
+        m.seq_free(a)
+        m.seq_free(b)
+
+
+def test_generate_matches_oracle_greedy(setup):
+    cfg, w, m, orc, stream = setup
+    prompt = synth.prompt_tokens(cfg, 16)
+    seq = m.seq_create()
+    try:
+        m.prefill(seq, prompt)
+        oseq = orc.new_seq()
+        ref = orc.prefill(oseq, prompt)
+        tok0 = int(np.argmax(ref))
+        toks = m.generate([seq], [tok0], 12)[:, 0]
+        otoks, ologits = orc.greedy_decode(oseq, tok0, 12)
+        for i in range(12):
+            gap = ops.top2_gap(ologits[i])
+            if gap <= 1e-2:
+                break  # beyond here the runs may legitimately diverge
+            assert toks[i] == otoks[i], f"step {i}"
+        assert m.seq_length(seq) == 16 + 12
+    finally:
+        m.seq_free(seq)
+
+
+def test_decode_batch_equals_single_steps(setup):
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    seqs = [m.seq_create() for _ in range(3)]
+    try:
+        for i, s in enumerate(seqs):
+            m.prefill(s, synth.prompt_tokens(cfg, 5 + 3 * i, seed=10 + i))
+        pos = [m.seq_length(s) for s in seqs]
+        toks = [3, 500, 1023]
+        out = torch.empty(3, cfg.vocab, device="cuda")
+        m.decode_batch(seqs, toks, pos, out)
+        ref_logits = []
+        for i, s in enumerate(seqs):
+            oseq = orc.new_seq()
+            orc.prefill(oseq, synth.prompt_tokens(cfg, 5 + 3 * i, seed=10 + i))
+            ref_logits.append(orc.decode_step(oseq, toks[i], pos[i]))
+        for i in range(3):
+            assert_close(out[i].cpu().numpy(), ref_logits[i], f"batch row {i}")
+    finally:
+        for s in seqs:
+            m.seq_free(s)
+
+
+def test_kv_fork_bit_exact_and_continues(setup):
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    prefix = synth.prompt_tokens(cfg, 45, seed=7)   # partial last page (45 = 32 + 13)
+    src = m.seq_create()
+    dsts = [m.seq_create(), m.seq_create()]
+    indep = m.seq_create()
+    try:
+        m.prefill(src, prefix)
+        m.prefill(dsts[0], synth.prompt_tokens(cfg, 70, seed=8))  # old contents dropped by the fork
+        m.kv_fork(src, dsts)
+        n, kvd = 45, cfg.n_kv_heads * cfg.head_dim
+        for l in range(cfg.n_layers):
+            ks = torch.empty(n, kvd, dtype=torch.float16, device="cuda")
+            vs = torch.empty_like(ks)
+            m.debug_read_kv(src, l, ks, vs)
+            for d in dsts:
+                assert m.seq_length(d) == n
+                kd = torch.empty_like(ks)
+                vd = torch.empty_like(ks)
+                m.debug_read_kv(d, l, kd, vd)
+                stream.synchronize()
+                assert torch.equal(kd.view(torch.int16), ks.view(torch.int16))
+                assert torch.equal(vd.view(torch.int16), vs.view(torch.int16))
+        # a branch continues RoPE at the prefix length and matches an independent prefill
+        m.prefill(indep, prefix)
+        lf = torch.empty(cfg.vocab, device="cuda")
+        li = torch.empty(cfg.vocab, device="cuda")
+        m.decode_step(dsts[1], 11, n, lf)
+        m.decode_step(indep, 11, n, li)
+        stream.synchronize()
+        assert torch.equal(lf, li)
+        from decode_llama_step_gb300 import dls
+        with pytest.raises(dls.DlsError) as e:
+            m.decode_step(dsts[0], 11, 0, lf)   # restarting at position 0 is refused
+        assert e.value.code == dls.DLS_ERR_STATE
+    finally:
+        for s in [src, *dsts, indep]:
+            m.seq_free(s)
+
+
+def test_streamed_layers_match_resident(setup):
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    prompt = synth.prompt_tokens(cfg, 12, seed=9)
+    outs = []
+    for n_res in (cfg.n_layers, 0, 1):
+        m.set_resident_layers(n_res)
+        assert m.resident_layers() == n_res
+        s = m.seq_create()
+        lg = torch.empty(cfg.vocab, device="cuda")
+        m.prefill(s, prompt)
+        m.decode_step(s, 5, 12, lg)
+        stream.synchronize()
+        outs.append(lg.clone())
+        m.seq_free(s)
+    m.set_resident_layers(cfg.n_layers)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_error_paths(setup):
+    torch = _torch()
+    from decode_llama_step_gb300 import dls
+    cfg, w, m, orc, stream = setup
+    s = m.seq_create()
+    try:
+        with pytest.raises(dls.DlsError) as e:
+            m.decode_step(s, cfg.vocab, 0)
+        assert e.value.code == dls.DLS_ERR_ARG
+        with pytest.raises(dls.DlsError) as e:
+            m.decode_step(s, 1, 3)
+        assert e.value.code == dls.DLS_ERR_STATE
+        with pytest.raises(dls.DlsError) as e:
+            m.prefill(s, np.zeros(161, dtype=np.int32))
+        assert e.value.code == dls.DLS_ERR_CAPACITY
+        assert m.seq_length(s) == 0
+        with pytest.raises(dls.DlsError):
+            m.kv_fork(s, [s])
+    finally:
+        m.seq_free(s)
+
+
+def test_attention_op_against_oracle(gpu_lib):
+    torch = _torch()
+    from decode_llama_step_gb300 import dls
+    rng = np.random.default_rng(3)
+    for nh, nkv, hd in [(4, 2, 64), (32, 8, 128), (8, 8, 32), (64, 8, 128)]:
+        pt, maxp = 32, 12
+        lengths = np.array([1, 2, 31, 32, 33, 65, 200, 384][: 4 if nh == 64 else 8], dtype=np.int32)
+        nb = len(lengths)
+        npages = nb * maxp
+        kp = rng.standard_normal((npages, nkv, pt, hd)).astype(np.float16)
+        vp = rng.standard_normal((npages, nkv, pt, hd)).astype(np.float16)
+        table = rng.permutation(npages).astype(np.int32).reshape(nb, maxp)
+        q = rng.standard_normal((nb, nh, hd)).astype(np.float32) * 2
+        tk, tv = torch.from_numpy(kp).cuda(), torch.from_numpy(vp).cuda()
+        tt, tl = torch.from_numpy(table).cuda(), torch.from_numpy(lengths).cuda()
+        tq = torch.from_numpy(q).cuda()
+        for splits in (1, 3, 7, 0):
+            ns = splits or 16
+            wsb = dls.attention_workspace_bytes(nb, nh, nkv, hd, ns)
+            ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+            o = torch.empty(nb, nh, hd, device="cuda")
+            dls.attention_decode(tq, tk, tv, tt, tl, o, ws, wsb, nb, nh, nkv, hd, pt, maxp, ns)
+            got = o.cpu().numpy()
+            for b in range(nb):
+                n = lengths[b]
+                pos = np.arange(n)
+                pages = table[b][pos // pt]
+                K = kp[pages, :, pos % pt, :].astype(np.float64)   # [n, nkv, hd]
+                V = vp[pages, :, pos % pt, :].astype(np.float64)
+                ref = ops.attention(q[b].astype(np.float64), K, V)
+                assert_close(got[b], ref, f"attn nh={nh} nkv={nkv} hd={hd} n={n} splits={splits}", tol=1e-5)
+            # the call leaves its arrival counters at zero for the next call
+            assert int(ws[: nb * nkv * 4].view(torch.int32).abs().sum()) == 0
