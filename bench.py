@@ -1,0 +1,337 @@
+#!/usr/bin/env python
+"""Decode-step benchmark: batch-1 greedy decode of the Llama-3.1-8B-shaped
+Q8_0 model (32 layers, hidden 4096, 32/8 heads, head_dim 128, FFN 14336,
+vocab 128256, seeded N(0, 0.02) weights) at KV context 2048 (``--ctx 8192``
+for the long-context case), through the library's C ABI.
+
+One "step" = one decode token: embedding, 32 layers (RMSNorm + QKV GEMV +
+RoPE + KV append, split-K attention, O GEMV, gate/up GEMV, SwiGLU + down
+GEMV), final norm, LM head GEMV and the greedy pick, all on the GPU.  The
+weights (8.2 GB per token) are larger than L2, so no flush is needed between
+steps.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on the
+same workload instead (bounded sample).  Under torchrun each rank runs an
+independent replica (decode does not shard); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "decode tok/s, 8B-shape Q8_0 batch 1; achieved HBM GB/s as % of peak"
+
+# ncu DRAM traffic per launch of the dominant kernel (the decode GEMV),
+# from the capture summarised in profiles/gemv_q8_0_8b_decode.md, valid only
+# for the kernel source it was taken on (sha256 prefix of csrc/gemv.cu).
+NCU_TRAFFIC = {"gemv_sha": None, "bytes_per_launch": None}
+
+KIND_NAMES = {1: "embed", 2: "gemv_qkv", 3: "attention", 4: "gemv_o", 5: "gemv_gate_up", 6: "gemv_down",
+              7: "gemv_head", 8: "argmax", 9: "advance"}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=256)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="8b")
+    p.add_argument("--ctx", type=int, default=2048)
+    p.add_argument("--e2e-steps", type=int, default=32)
+    p.add_argument("--profile-steps", type=int, default=4)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def gemv_bytes(rows, cols, wtype):
+    nb = (cols + 31) // 32
+    per_block = 34 if wtype == 8 else 18
+    return rows * nb * per_block + cols * 4 + rows * 4
+
+
+def step_bytes(cfg, ctx_len):
+    """Algorithmic HBM bytes of one decode token at KV length ctx_len."""
+    H, F, V = cfg.hidden, cfg.ffn, cfg.vocab
+    qd, kvd = cfg.q_dim, cfg.kv_dim
+    per_layer = (gemv_bytes(qd + 2 * kvd, H, cfg.wtype) + gemv_bytes(H, qd, cfg.wtype)
+                 + gemv_bytes(2 * F, H, cfg.wtype) + gemv_bytes(H, F, cfg.wtype)
+                 + 2 * ctx_len * kvd * 2)            # K and V read (fp16)
+    head = gemv_bytes(V, H, cfg.wtype)
+    return cfg.n_layers * per_layer + head
+
+
+def kind_bytes(cfg, kind, ctx_len):
+    H, F, V = cfg.hidden, cfg.ffn, cfg.vocab
+    qd, kvd = cfg.q_dim, cfg.kv_dim
+    return {2: gemv_bytes(qd + 2 * kvd, H, cfg.wtype) + 2 * kvd * 2,
+            3: 2 * ctx_len * kvd * 2 + 2 * qd * 4,
+            4: gemv_bytes(H, qd, cfg.wtype),
+            5: gemv_bytes(2 * F, H, cfg.wtype),
+            6: gemv_bytes(H, F, cfg.wtype) + F * 4,
+            7: gemv_bytes(V, H, cfg.wtype)}.get(kind, 0)
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.tmp,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        self.tmp.flush()
+        self.tmp.seek(0)
+        sm, mx, reasons = [], None, set()
+        for line in self.tmp.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(cfg, ctx, n_layer_samples=2):
+    """Time the fp64 oracle's decode step on a bounded sample: n layers of the
+    model at KV length ctx (seeded fp16-valued cache) plus the LM head, scaled
+    to the whole model.  Returns (tok/s, seconds, description, cores)."""
+    import synth
+    from oracle import OracleModel, ops
+
+    layers = list(range(n_layer_samples))
+    w = synth.model_weights(cfg, layers=layers)
+    orc = OracleModel(cfg, w, cache_bytes=0)
+    seq = orc.new_seq(capacity=ctx + 1)
+    for l in layers:
+        k = ops.round_f16(synth.normal(synth.stream_key("bench-kv", l, "k"), ctx * cfg.kv_dim, 1.0))
+        v = ops.round_f16(synth.normal(synth.stream_key("bench-kv", l, "v"), ctx * cfg.kv_dim, 1.0))
+        seq.set_layer(l, k.reshape(ctx, cfg.n_kv_heads, cfg.head_dim), v.reshape(ctx, cfg.n_kv_heads, cfg.head_dim))
+    x = orc.embed(1)
+    t0 = time.perf_counter()
+    for l in layers:
+        x = orc.layer_forward(l, x, ctx, seq)
+    t_layers = (time.perf_counter() - t0) / len(layers)
+    t1 = time.perf_counter()
+    orc.final_logits(x)
+    t_head = time.perf_counter() - t1
+    per_tok = t_layers * cfg.n_layers + t_head
+    cores = len(os.sched_getaffinity(0))
+    desc = (f"fp64 oracle decode of layers 0-{len(layers) - 1} of {cfg.n_layers} at KV length {ctx} plus the "
+            f"LM head, scaled to {cfg.n_layers} layers ({t_layers:.2f} s/layer, head {t_head:.2f} s)")
+    return 1.0 / per_tok, t_layers * len(layers) + t_head, desc, cores
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import synth
+    cfg = synth.get_config(args.config)
+    n = max(1, min(args.steps, 3))
+    tps, secs, desc, cores = cpu_oracle_sample(cfg, args.ctx, n_layer_samples=n)
+    line = {"metric": METRIC, "impl": "reference", "value": round(tps, 6), "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": n, "warmup": 0, "ms_per_step": round(1000.0 / tps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{cfg.name} Q8_0 batch-1 greedy decode, KV ctx {args.ctx}", "ctx": args.ctx,
+                       "batch": 1},
+            "cpu_baseline": {"value": round(tps, 6), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(tps, 6), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    import synth
+    from decode_llama_step_gb300 import dls
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    cfg = synth.get_config(args.config)
+    t0 = time.time()
+    w = synth.model_weights(cfg)
+    gen_s = time.time() - t0
+    stream = torch.cuda.Stream()
+    extra = args.warmup + args.steps + args.e2e_steps + args.profile_steps + 8
+    t0 = time.time()
+    m = dls.Model(cfg, w, max_seqs=1, max_ctx=args.ctx + extra, stream=stream)
+    create_s = time.time() - t0
+    del w
+    seq = m.seq_create()
+    prompt = synth.prompt_tokens(cfg, args.ctx, seed=1)
+    logits = torch.empty(cfg.vocab, device="cuda")
+    t0 = time.time()
+    m.prefill(seq, prompt, logits)
+    prefill_s = time.time() - t0
+    tok = int(torch.argmax(logits).item())
+
+    # warm-up (also captures the generation graph)
+    toks = m.generate([seq], [tok], args.warmup)
+    tok = int(toks[-1, 0])
+    ctx0 = m.seq_length(seq)
+
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        toks = m.generate([seq], [tok], args.steps)
+        end.record(stream)
+        end.synchronize()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * args.steps / (ms / 1000.0)
+    tok = int(toks[-1, 0])
+    launches = m.launches_per_step()
+
+    # roofline: per-kernel device times from event-instrumented steps
+    kinds_ms = {}
+    pos = m.seq_length(seq)
+    for _ in range(args.profile_steps):
+        kms, kk = m.profile_step(seq, tok, pos)
+        pos += 1
+        for d, k in zip(kms, kk):
+            kinds_ms.setdefault(int(k), []).append(float(d))
+    ctx_mid = ctx0 + args.steps // 2
+    gemv_kinds = (2, 4, 5, 6, 7)
+    gemv_bytes_total = sum(kind_bytes(cfg, k, ctx_mid) * len(kinds_ms.get(k, [])) for k in gemv_kinds)
+    gemv_ms_total = sum(sum(kinds_ms.get(k, [])) for k in gemv_kinds)
+    gemv_launches = sum(len(kinds_ms.get(k, [])) for k in gemv_kinds)
+    peak, peak_src = peaks()
+    achieved = gemv_bytes_total / (gemv_ms_total / 1000.0) / 1e9 if gemv_ms_total else 0.0
+    src_sha = hashlib.sha256(open(os.path.join(ROOT, "decode_llama_step_gb300", "csrc", "gemv.cu"), "rb").read()).hexdigest()[:16]
+    traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["gemv_sha"] == src_sha else None
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": "dequant-GEMV (QKV, O, gate/up, down, LM head launches of one step)",
+                "bytes_per_launch": round(gemv_bytes_total / max(gemv_launches, 1)),
+                "avg_launch_us": round(1000.0 * gemv_ms_total / max(gemv_launches, 1), 2),
+                "peak_source": f"{peak_src} (MEMORY copy, hbm_gbs)"}
+    step_b = step_bytes(cfg, ctx_mid)
+    whole = step_b / (ms_per_step / 1000.0) / 1e9
+    per_kind = {KIND_NAMES.get(k, str(k)): {"launches_per_step": len(v) // max(args.profile_steps, 1),
+                                            "ms_per_step": round(sum(v) / max(args.profile_steps, 1), 4)}
+                for k, v in sorted(kinds_ms.items())}
+
+    # end to end: host token in, host logits out (pinned), host argmax, per step
+    host_logits = torch.empty(cfg.vocab, dtype=torch.float32, pin_memory=True)
+    hl = host_logits.numpy()
+    e2e_n = args.e2e_steps
+    pos = m.seq_length(seq)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_n):
+        m.decode_step(seq, tok, pos + i, host_logits)
+        tok = int(np.argmax(hl))
+    e2e_s = time.perf_counter() - t0
+    e2e_val = world * e2e_n / e2e_s
+
+    line = {"metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"Llama-3.1-8B-shape Q8_0 batch-1 greedy decode, KV ctx {ctx0}..{ctx0 + args.steps}",
+                       "ctx": args.ctx, "batch": 1, "weights": "seeded N(0,0.02), quantised Q8_0",
+                       "l2": "no flush: 8.2 GB of weights per step > 126 MB L2",
+                       "parallelism": f"replicas x{world}"},
+            "hbm": {"algorithmic_bytes_per_step": step_b, "achieved_gbs": round(whole, 1),
+                    "frac_of_peak": round(whole / peak, 4), "peak_gbs": peak},
+            "roofline": roofline,
+            "kernels": per_kind,
+            "e2e": {"value": round(e2e_val, 3), "unit": "tok/s", "h2d_bytes_per_step": 8,
+                    "d2h_bytes_per_step": cfg.vocab * 4,
+                    "how": "dls_decode_step with host token, pinned host logits, host argmax"},
+            "gpu_launches": launches * args.steps,
+            "clocks": clk.summary(),
+            "setup_s": {"weights": round(gen_s, 1), "create": round(create_s, 1), "prefill": round(prefill_s, 2),
+                        "prefill_tok_s": round(args.ctx / prefill_s, 1)}}
+    if rank == 0 and not args.no_cpu_baseline:
+        tps, secs, desc, cores = cpu_oracle_sample(cfg, args.ctx)
+        line["cpu_baseline"] = {"value": round(tps, 6), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    m.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

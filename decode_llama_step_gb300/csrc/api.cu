@@ -23,7 +23,7 @@ size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct MatOff {
   size_t qs = 0, d = 0;
-  int rows = 0, cols = 0, nb = 0;
+  int rows = 0, cols = 0, nb = 0, ds = 0;
   size_t qs_bytes = 0, d_bytes = 0;
 };
 
@@ -38,8 +38,9 @@ MatOff mat_off(size_t& cur, int rows, int cols, int wtype) {
   m.rows = rows;
   m.cols = cols;
   m.nb = (cols + 31) / 32;
+  m.ds = (m.nb + 7) & ~7;  // 16-byte scale rows
   m.qs_bytes = (size_t)rows * m.nb * (wtype == 8 ? 32 : 16);
-  m.d_bytes = (size_t)rows * m.nb * 2;
+  m.d_bytes = (size_t)rows * m.ds * 2;
   m.qs = cur;
   cur = a256(cur + m.qs_bytes);
   m.d = cur;
@@ -51,10 +52,11 @@ MatDev mat_at(const uint8_t* base, const MatOff& o, int row0 = 0, int rows = -1)
   MatDev m;
   const size_t rb = o.qs_bytes / (o.rows ? o.rows : 1);
   m.qs = base + o.qs + (size_t)row0 * rb;
-  m.d = reinterpret_cast<const __half*>(base + o.d) + (size_t)row0 * o.nb;
+  m.d = reinterpret_cast<const __half*>(base + o.d) + (size_t)row0 * o.ds;
   m.rows = rows < 0 ? o.rows - row0 : rows;
   m.cols = o.cols;
   m.nb = o.nb;
+  m.ds = o.ds;
   return m;
 }
 
@@ -127,6 +129,10 @@ struct dls_model {
   float* capture = nullptr;
   int launches_per_step = 0;
   int launch_count = 0;
+  // per-kernel timing (dls_debug_profile_step): an event after every launch
+  bool profiling = false;
+  std::vector<cudaEvent_t> prof_events;
+  std::vector<int> prof_kinds;
   std::string err;
 };
 
@@ -281,11 +287,27 @@ MatDev head_mat(const dls_model* m) {
 // final norm + LM head [-> greedy pick].  With streamed layers the copy
 // stream fills buffer (l - resident) % 2 while the previous layer computes.
 
-#define LK(call)                                                                                      \
+enum KernelKind { K_EMBED = 1, K_QKV = 2, K_ATTN = 3, K_O = 4, K_GATE_UP = 5, K_DOWN = 6, K_HEAD = 7, K_ARGMAX = 8,
+                  K_ADVANCE = 9 };
+
+int prof_mark(dls_model* m, int kind) {
+  const size_t i = m->prof_kinds.size();
+  if (i >= m->prof_events.size()) {
+    cudaEvent_t e;
+    CK(cudaEventCreate(&e));
+    m->prof_events.push_back(e);
+  }
+  CK(cudaEventRecord(m->prof_events[i], m->stream));
+  m->prof_kinds.push_back(kind);
+  return DLS_OK;
+}
+
+#define LK(kind, call)                                                                                 \
   do {                                                                                                \
     cudaError_t e_ = (call);                                                                          \
     ++m->launch_count;                                                                                \
     if (e_ != cudaSuccess) return fail(m, DLS_ERR_CUDA, "launch=%s cuda=%s", #call, cudaGetErrorString(e_)); \
+    if (m->profiling) TRY(prof_mark(m, kind));                                                        \
   } while (0)
 
 int enqueue_copy_layer(dls_model* m, int l) {
@@ -298,10 +320,10 @@ int enqueue_copy_layer(dls_model* m, int l) {
 
 int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
   cudaStream_t s = m->stream;
-  const bool pdl = true;
+  const bool pdl = !m->profiling;  // profiled kernels run strictly one after another
   float* x = m->x + (size_t)b * m->H;
   float* logits = m->logits + (size_t)b * m->V;
-  LK(launch_embed(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp, b, x, m->V, s, pdl));
+  LK(K_EMBED, launch_embed(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp, b, x, m->V, s, pdl));
   const bool streaming = m->resident < m->L;
   if (streaming) {
     // the copy stream joins this step after everything enqueued so far
@@ -334,7 +356,7 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
     g.rope_len = m->rope_len;
     g.sp = m->sp;
     g.brow = b;
-    LK(launch_gemv(m->wtype, PRO_RMSNORM, EPI_QKV, g, m->plan_qkv, s, pdl));
+    LK(K_QKV, launch_gemv(m->wtype, PRO_RMSNORM, EPI_QKV, g, m->plan_qkv, s, pdl));
     // (2) split-K GQA attention over the paged cache
     AttnArgs a{};
     a.q = m->q;
@@ -357,14 +379,14 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
     a.counters = m->counters;
     a.status = &m->sp->status;
     a.max_len = m->max_ctx;
-    LK(launch_attention(a, 1, s, pdl));
+    LK(K_ATTN, launch_attention(a, 1, s, pdl));
     // (3) O projection + residual
     GemvArgs go{};
     go.w = P.o;
     go.unit = 1;
     go.x = m->o;
     go.y = x;
-    LK(launch_gemv(m->wtype, PRO_COPY, EPI_RESID, go, m->plan_o, s, pdl));
+    LK(K_O, launch_gemv(m->wtype, PRO_COPY, EPI_RESID, go, m->plan_o, s, pdl));
     // (4) RMSNorm -> gate|up GEMV
     GemvArgs gg{};
     gg.w = P.gu;
@@ -373,14 +395,14 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
     gg.g = P.ffn_norm;
     gg.eps = m->eps;
     gg.y = m->gu;
-    LK(launch_gemv(m->wtype, PRO_RMSNORM, EPI_STORE, gg, m->plan_gu, s, pdl));
+    LK(K_GATE_UP, launch_gemv(m->wtype, PRO_RMSNORM, EPI_STORE, gg, m->plan_gu, s, pdl));
     // (5) SwiGLU -> down GEMV + residual
     GemvArgs gd{};
     gd.w = P.down;
     gd.unit = 1;
     gd.x = m->gu;
     gd.y = x;
-    LK(launch_gemv(m->wtype, PRO_SWIGLU, EPI_RESID, gd, m->plan_down, s, pdl));
+    LK(K_DOWN, launch_gemv(m->wtype, PRO_SWIGLU, EPI_RESID, gd, m->plan_down, s, pdl));
     if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * m->H, x, m->H * sizeof(float), cudaMemcpyDeviceToDevice, s));
     if (streamed) {
       CK(cudaEventRecord(m->ev_free[buf], s));
@@ -395,16 +417,16 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
     gh.g = m->out_norm;
     gh.eps = m->eps;
     gh.y = logits;
-    LK(launch_gemv(m->wtype, PRO_RMSNORM, EPI_STORE, gh, m->plan_head, s, pdl));
+    LK(K_HEAD, launch_gemv(m->wtype, PRO_RMSNORM, EPI_STORE, gh, m->plan_head, s, pdl));
   }
-  if (argmax) LK(launch_argmax(logits, m->V, 1, m->next_tok + b, s, pdl));
+  if (argmax) LK(K_ARGMAX, launch_argmax(logits, m->V, 1, m->next_tok + b, s, pdl));
   return DLS_OK;
 }
 
 int enqueue_step(dls_model* m, int rows, bool head, bool argmax, float* capture) {
   m->launch_count = 0;
   for (int b = 0; b < rows; ++b) TRY(enqueue_row(m, b, head, argmax, b == 0 ? capture : nullptr));
-  if (argmax) LK(launch_advance(m->sp, m->next_tok, m->tokens_dev, rows, m->stream, true));
+  if (argmax) LK(K_ADVANCE, launch_advance(m->sp, m->next_tok, m->tokens_dev, rows, m->stream, true));
   m->launches_per_step = m->launch_count;
   return DLS_OK;
 }
@@ -508,8 +530,8 @@ int upload_matrix(dls_model* m, const void* host_blocks, int rows, int cols, uin
   const size_t bytes = (size_t)rows * nb * bsz;
   CK(cudaMemcpyAsync(temp, host_blocks, bytes, cudaMemcpyHostToDevice, m->stream));
   const size_t rb = off.qs_bytes / off.rows;
-  CK(launch_repack(temp, m->wtype, rows, nb, dst_base + off.qs + (size_t)row0 * rb,
-                   reinterpret_cast<__half*>(dst_base + off.d) + (size_t)row0 * nb, m->stream));
+  CK(launch_repack(temp, m->wtype, rows, nb, off.ds, dst_base + off.qs + (size_t)row0 * rb,
+                   reinterpret_cast<__half*>(dst_base + off.d) + (size_t)row0 * off.ds, m->stream));
   return DLS_OK;
 }
 
@@ -591,6 +613,7 @@ void destroy(dls_model* m) {
     if (m->ev_free[i]) cudaEventDestroy(m->ev_free[i]);
   }
   if (m->ev_start) cudaEventDestroy(m->ev_start);
+  for (auto e : m->prof_events) cudaEventDestroy(e);
   if (m->copy_stream) cudaStreamDestroy(m->copy_stream);
   if (m->own_stream && m->stream) cudaStreamDestroy(m->stream);
   delete m;
@@ -1018,6 +1041,40 @@ int dls_set_resident_layers(dls_model* m, int32_t n) {
                 (unsigned long long)m->budget);
   if (n == m->resident) return DLS_OK;
   return apply_resident(m, n);
+}
+
+int dls_debug_profile_step(dls_model* m, int32_t seq, int32_t token, int32_t pos, int32_t max_kernels,
+                           float* kernel_ms, int32_t* kernel_kind, int32_t* n_kernels) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (!kernel_ms || !kernel_kind || !n_kernels || max_kernels < 1) return fail(m, DLS_ERR_ARG, "output arrays");
+  TRY(check_seq(m, seq));
+  if (token < 0 || token >= m->V) return fail(m, DLS_ERR_ARG, "token=%d vocab=%d", token, m->V);
+  Seq& s = m->seqs[seq];
+  if (pos != s.len) return fail(m, DLS_ERR_STATE, "seq=%d pos=%d length=%d", seq, pos, s.len);
+  if (pos >= m->max_ctx) return fail(m, DLS_ERR_CAPACITY, "seq=%d pos=%d max_ctx=%d", seq, pos, m->max_ctx);
+  TRY(ensure_pages(m, seq, pos + 1));
+  TRY(set_params(m, 1, &seq, &token, &pos, true));
+  // hold the GPU for a few ms so the whole step is queued before it starts:
+  // the event deltas then measure kernels, not host launch gaps
+  CK(launch_delay(2000000, m->stream));
+  m->prof_kinds.clear();
+  m->profiling = true;
+  TRY(prof_mark(m, 0));
+  const int r = enqueue_step(m, 1, true, false, nullptr);
+  m->profiling = false;
+  TRY(r);
+  TRY(sync_stream(m, m->stream));
+  const int n = (int)m->prof_kinds.size() - 1;
+  if (n > max_kernels) return fail(m, DLS_ERR_ARG, "max_kernels=%d < %d launches", max_kernels, n);
+  for (int i = 0; i < n; ++i) {
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, m->prof_events[i], m->prof_events[i + 1]));
+    kernel_ms[i] = ms;
+    kernel_kind[i] = m->prof_kinds[i + 1];
+  }
+  *n_kernels = n;
+  s.len += 1;
+  return DLS_OK;
 }
 
 int dls_debug_capture(dls_model* m, float* per_layer_out) {

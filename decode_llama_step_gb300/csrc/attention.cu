@@ -30,14 +30,23 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+constexpr int NSTAGE = 4;   // K/V tile ring depth
+
 template <int HD>
 __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   constexpr int DPL = HD / 32;            // dims per lane when scoring
   constexpr int HPT = NT / HD;            // head slots per pass (threads share d)
   constexpr int OPT = (kMaxG + HPT - 1) / HPT;
+  constexpr int TILE_B = TILE * HD * 2;   // bytes of one K (or V) tile
+  constexpr int kMaxSplits = 128;
+  extern __shared__ __align__(128) uint8_t s_dyn[];
+  // K/V tile ring in dynamic shared memory: [NSTAGE][K|V][TILE*HD] halves
+  auto kv_tile = [&](int st, int which) { return reinterpret_cast<__half*>(s_dyn) + ((size_t)st * 2 + which) * TILE * HD; };
   __shared__ __align__(16) float s_q[kMaxG * HD];
   __shared__ float s_s[kMaxG][TILE];
   __shared__ float s_alpha[kMaxG], s_m[kMaxG], s_l[kMaxG];
+  __shared__ __align__(8) uint64_t s_full[NSTAGE];
+  __shared__ float s_w[kMaxG][kMaxSplits];
   __shared__ int s_last;
 
   const int g = a.n_heads / a.n_kv;
@@ -48,6 +57,10 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   const int d = tid % HD, hslot = tid / HD;
   const int pt = a.page_tokens;
 
+  if (tid == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(smem_u32(&s_full[i]), 1);
+    mbar_fence_init();
+  }
   griddep_wait();
   griddep_launch();
 
@@ -61,6 +74,31 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   int per = (n + S - 1) / S;
   per = (per + TILE - 1) / TILE * TILE;
   const int t0 = sp * per, t1 = min(n, t0 + per);
+  const int ntiles = t1 > t0 ? (t1 - t0 + TILE - 1) / TILE : 0;
+
+  // thread 0 issues the K and V copies of a tile (a tile never crosses a page)
+  auto issue = [&](int i) -> bool {
+    const int t = t0 + i * TILE;
+    const int nt = min(TILE, t1 - t);
+    const int page = ptab[t / pt];
+    const uint32_t bar = smem_u32(&s_full[i % NSTAGE]);
+    if (page < 0) {
+      mbar_arrive(bar);  // complete the phase with nothing copied
+      return false;
+    }
+    const size_t base = (((size_t)page * a.n_kv + kvh) * pt + (t % pt)) * HD;
+    const uint32_t bytes = (uint32_t)nt * HD * 2;
+    mbar_expect_tx(bar, 2 * bytes);
+    bulk_g2s(smem_u32(kv_tile(i % NSTAGE, 0)), a.k_pool + base, bytes, bar);
+    bulk_g2s(smem_u32(kv_tile(i % NSTAGE, 1)), a.v_pool + base, bytes, bar);
+    return true;
+  };
+  __syncthreads();  // barriers initialised
+  if (tid == 0) {
+    bool ok = true;
+    for (int i = 0; i < min(NSTAGE, ntiles); ++i) ok &= issue(i);
+    if (!ok && a.status) atomicOr(a.status, kBadPage);
+  }
 
   const float scale = 1.0f / sqrtf((float)HD);
   const float* qrow = a.q + ((size_t)brel * a.n_heads + (size_t)kvh * g) * HD;
@@ -74,41 +112,24 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   for (int k = 0; k < OPT; ++k) oacc[k] = 0.f;
   __syncthreads();
 
-  for (int t = t0; t < t1; t += TILE) {
+  bool failed = false;
+  for (int i = 0; i < ntiles; ++i) {
+    const int t = t0 + i * TILE;
     const int nt = min(TILE, t1 - t);
-    const int page = ptab[t / pt];
-    if (page < 0) {
-      if (a.status && tid == 0) atomicOr(a.status, kBadPage);
-      break;
-    }
-    const size_t base = (((size_t)page * a.n_kv + kvh) * pt + (t % pt)) * HD;
-    const __half* kb = a.k_pool + base;
-    const __half* vb = a.v_pool + base;
-    // V of the tile: one column d per thread, issued before the scores
-    __half vreg[TILE];
-#pragma unroll
-    for (int j = 0; j < TILE; ++j) vreg[j] = j < nt ? vb[(size_t)j * HD + d] : __float2half(0.f);
-    // K of this warp's tokens (j = warp, warp + 4, ...)
-    constexpr int TPW = TILE / (NT / 32);
-    __half kreg[TPW][DPL];
-#pragma unroll
-    for (int u = 0; u < TPW; ++u) {
-      const int j = warp + u * (NT / 32);
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) kreg[u][e] = j < nt ? kb[(size_t)j * HD + lane * DPL + e] : __float2half(0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < TPW; ++u) {
-      const int j = warp + u * (NT / 32);
+    if (!mbar_wait(smem_u32(&s_full[i % NSTAGE]), (i / NSTAGE) & 1)) failed = true;
+    const __half* kt = kv_tile(i % NSTAGE, 0);
+    const __half* vt = kv_tile(i % NSTAGE, 1);
+    // scores: warp w scores tokens w, w+4, ...; lanes split the head dim
+    for (int j = warp; j < nt; j += NT / 32) {
       float kf[DPL];
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) kf[e] = __half2float(kreg[u][e]);
+      for (int e = 0; e < DPL; ++e) kf[e] = __half2float(kt[j * HD + lane * DPL + e]);
       for (int h = 0; h < g; ++h) {
         float p = 0.f;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) p = fmaf(s_q[h * HD + lane * DPL + e], kf[e], p);
         p = warp_sum(p);
-        if (lane == 0 && j < nt) s_s[h][j] = p;
+        if (lane == 0) s_s[h][j] = p;
       }
     }
     __syncthreads();
@@ -129,21 +150,19 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
       }
     }
     __syncthreads();
-    float vf[TILE];
-#pragma unroll
-    for (int j = 0; j < TILE; ++j) vf[j] = __half2float(vreg[j]);
 #pragma unroll
     for (int k = 0; k < OPT; ++k) {
       const int h = hslot + k * HPT;
       if (h < g) {
         float o = oacc[k] * s_alpha[h];
-#pragma unroll
-        for (int j = 0; j < TILE; ++j) o = fmaf(s_s[h][j], vf[j], o);  // p = 0 beyond nt
+        for (int j = 0; j < nt; ++j) o = fmaf(s_s[h][j], __half2float(vt[j * HD + d]), o);
         oacc[k] = o;
       }
     }
-    __syncthreads();
+    __syncthreads();  // slot i % NSTAGE is free again
+    if (tid == 0 && i + NSTAGE < ntiles && !issue(i + NSTAGE) && a.status) atomicOr(a.status, kBadPage);
   }
+  if (failed && a.status && tid == 0) atomicOr(a.status, kTimeout);
 
   // ---- partials to scratch
   const size_t slot = ((size_t)brel * a.n_kv + kvh) * S + sp;
@@ -163,24 +182,34 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  // ---- last CTA of this (row, kv head): combine the S splits in order
+  // ---- last CTA of this (row, kv head): combine the S splits
+  // weights w_s = exp(m_s - M) / sum_s l_s exp(m_s - M), one warp per head
   const size_t slot0 = ((size_t)brel * a.n_kv + kvh) * S;
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+  for (int h = warp; h < g; h += NT / 32) {
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(&ml[(slot0 + s) * g + h]).x);
+    M = warp_max(M);
+    float den = 0.f;
+    for (int s = lane; s < S; s += 32) {
+      const float2 v = __ldcg(&ml[(slot0 + s) * g + h]);
+      const float e = v.y > 0.f ? expf(v.x - M) : 0.f;  // empty split: weight 0
+      s_w[h][s] = e;
+      den = fmaf(v.y, e, den);
+    }
+    den = warp_sum(den);
+    for (int s = lane; s < S; s += 32) s_w[h][s] /= den;
+  }
+  __syncthreads();
 #pragma unroll
   for (int k = 0; k < OPT; ++k) {
     const int h = hslot + k * HPT;
     if (h >= g) continue;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(&ml[(slot0 + s) * g + h]).x);
-    float num = 0.f, den = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float2 v = __ldcg(&ml[(slot0 + s) * g + h]);
-      if (v.y == 0.f) continue;  // empty split
-      const float e = expf(v.x - M);
-      den = fmaf(v.y, e, den);
-      num = fmaf(__ldcg(&a.part_o[((slot0 + s) * g + h) * HD + d]), e, num);
-    }
-    a.o[((size_t)brel * a.n_heads + (size_t)kvh * g + h) * HD + d] = num / den;
+    float acc = 0.f;
+    const float* po = a.part_o + (slot0 * g + h) * HD + d;
+#pragma unroll 8
+    for (int s = 0; s < S; ++s) acc = fmaf(s_w[h][s], __ldcg(po + (size_t)s * g * HD), acc);
+    a.o[((size_t)brel * a.n_heads + (size_t)kvh * g + h) * HD + d] = acc;
   }
   if (tid == 0) a.counters[(size_t)brel * a.n_kv + kvh] = 0;
 }
@@ -212,15 +241,29 @@ int attn_default_splits(int rows, int n_kv, int num_sms, int max_len) {
   int s = (2 * num_sms + rows * n_kv - 1) / (rows * n_kv);
   const int cap = (max_len + TILE - 1) / TILE;
   if (s > cap) s = cap;
+  if (s > 128) s = 128;  // combine weights live in shared memory
   if (s < 1) s = 1;
   return s;
 }
 
+template <int HD>
+cudaError_t attn_attr() {
+  static bool done = false;  // one process-wide attribute per instantiation
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       NSTAGE * 2 * TILE * HD * 2);
+  done = e == cudaSuccess;
+  return e;
+}
+
 cudaError_t launch_attention(const AttnArgs& a, int rows, cudaStream_t s, bool pdl) {
+  if (a.n_splits > 128 || a.n_splits < 1) return cudaErrorInvalidValue;
+  cudaError_t e = a.head_dim == 32 ? attn_attr<32>() : a.head_dim == 64 ? attn_attr<64>() : attn_attr<128>();
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_kv * a.n_splits, rows);
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = NSTAGE * 2 * TILE * a.head_dim * 2;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -251,6 +294,7 @@ extern "C" int dls_attention_decode(const float* q, const void* k_pages, const v
                                     int32_t head_dim, int32_t page_tokens, int32_t max_pages, int32_t n_splits,
                                     void* cuda_stream) {
   if (!q || !k_pages || !v_pages || !page_table || !lengths || !o || !workspace) return DLS_ERR_ARG;
+  if (n_splits > 128) return DLS_ERR_ARG;
   if (n_batch < 1 || n_kv_heads < 1 || n_heads < 1 || n_heads % n_kv_heads || n_heads / n_kv_heads > dls::kMaxG ||
       (head_dim != 32 && head_dim != 64 && head_dim != 128) || page_tokens < 32 || page_tokens % 32 ||
       max_pages < 1)

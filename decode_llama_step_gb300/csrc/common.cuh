@@ -26,16 +26,19 @@ enum StatusBits : int32_t {
   kBadPage = 1,   // page table entry missing for a position being written/read
   kBadToken = 2,  // token id outside [0, vocab)
   kBadPos = 4,    // position outside the rope table / context
+  kTimeout = 8,   // a bounded wait on an mbarrier ran out
 };
 
 // One weight matrix in the kernels' layout: codes and fp16 scales in two
-// arrays ("structure of arrays") so each lane's 16-byte load is aligned.
-//   Q8_0: qs int8 [rows][nb*32]          d fp16 [rows][nb]
-//   Q4_0: qs u8   [rows][nb][16] (GGUF nibble order kept)   d fp16 [rows][nb]
+// arrays ("structure of arrays"), so rows of codes are contiguous, 16-byte
+// aligned and can be moved by bulk copies.
+//   Q8_0: qs int8 [rows][nb*32]                             d fp16 [rows][ds]
+//   Q4_0: qs u8   [rows][nb][16] (GGUF nibble order kept)   d fp16 [rows][ds]
 struct MatDev {
   const uint8_t* qs;
   const __half* d;
   int rows, cols, nb;
+  int ds;  // scale row stride in elements: nb rounded up to 8 (16-byte rows)
 };
 
 // ---- small PTX wrappers -----------------------------------------------------
@@ -107,6 +110,60 @@ __device__ __forceinline__ void u4x4_to_f2(uint32_t b, f2_t& p01, f2_t& p23) {
   const f2_t bias = pk2(-8388616.0f, -8388616.0f);  // 2^23 + 8
   p01 = fadd2(pk2(mag_byte(b, 0), mag_byte(b, 1)), bias);
   p23 = fadd2(pk2(mag_byte(b, 2), mag_byte(b, 3)), bias);
+}
+
+// ---- mbarrier + bulk async copy (TMA, non-tensor form) ---------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for phase `parity` of an mbarrier; gives up after `limit_ns` of
+// global time and returns false (the caller records an error and stops).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 0 && global_ns() - t0 > limit_ns) return false;
+  }
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes and
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -1,348 +1,333 @@
-// Batch-1 dequant-GEMV y = W x for Q8_0 / Q4_0 weights, the decode step's
+// Batch-1 dequant-GEMV y = W x for Q8_0 / Q4_0 weights: the decode step's
 // projections (engine page, section 4.4: a GEMV specialised for the
-// single-token vector-matrix product; RMSNorm fused into it; SwiGLU fused
+// single-token vector-matrix product, RMSNorm fused into it, SwiGLU fused
 // with the projection).
 //
-// Design (HBM-bound, ~2.4 ALU ops per weight):
-//  * Each CTA owns a contiguous, balanced range of rows, so it streams one
-//    contiguous slice of the code array and of the scale array.
-//  * A warp owns K-chunks of 512 (Q8_0) / 1024 (Q4_0) columns: per row each
-//    lane issues one 16-byte non-allocating load, R = 8 rows at a time,
-//    double-buffered, so 128-256 bytes per lane are in flight.
-//  * Codes become exact fp32 through the 0x4B0000bb magic pattern (one byte
-//    permute per value); products accumulate with packed f32x2 FMAs.
-//  * Per row the R partial sums reduce across lanes with a halving
-//    butterfly (9 shuffles for 8 rows), then across warps in shared memory
-//    in a fixed order: the result is deterministic.
-//  * Prologue: the activation vector goes to shared memory, optionally as
-//    rmsnorm(x) * g or as silu(gate) * up.  Before waiting on the previous
-//    kernel (programmatic dependent launch) the CTA asks L2 to prefetch the
-//    head of its weight slice: weights never depend on the previous kernel.
-//  * Epilogues: store, residual add, or RoPE on (q, k) pairs plus the fp16
-//    K/V append into the paged cache.
+// HBM-bound design for sm_103a:
+//  * One CTA per SM owns a contiguous, balanced range of rows; its slice of
+//    the code array and of the scale array is contiguous.
+//  * A producer warp streams that slice through a shared-memory ring with
+//    1-D bulk async copies (TMA, cp.async.bulk) and mbarriers: stages of RS
+//    whole rows (~16 KB of codes plus their scales), ~96 KB in flight per SM.
+//    The first stages are issued before waiting on the previous kernel
+//    (programmatic dependent launch): weights never depend on it.
+//  * Consumer warps own K-chunks (512 columns for Q8_0, 1024 for Q4_0); each
+//    lane holds its activation slice in registers for the whole kernel and
+//    reads 16 bytes of codes per row per chunk from shared memory.
+//  * Codes become exact fp32 through the 0x4B0000bb pattern (one byte permute
+//    per value); products accumulate in packed f32x2 FMAs; per-row partials
+//    reduce across lanes with a halving butterfly and across warps in a fixed
+//    order (deterministic results).
+//  * Prologues: copy, rmsnorm(x) * g, or silu(gate) * up, computed while the
+//    activation is loaded into registers.  Epilogues: store, residual add, or
+//    RoPE on adjacent (q, k) pairs plus the fp16 K/V append into the cache.
 #include "kernels.h"
 
 namespace dls {
 
 namespace {
 
-constexpr int R = 8;             // rows in flight per warp
-constexpr int kMaxThreads = 256;   // at most 8 warps (gemv_plan)
-constexpr int kPrefetchBytes = 48 * 1024;
+constexpr int kMaxConsumers = 14;
+constexpr int kRB = 64;              // rows per epilogue block
+constexpr int kStageCodes = 16384;   // target code bytes per ring stage
+constexpr int kRingBytes = 96 * 1024;
 
 template <int WT>
 struct Geo {
-  static constexpr int CH = WT == 8 ? 512 : 1024;  // columns per warp chunk
+  static constexpr int CH = WT == 8 ? 512 : 1024;   // columns per chunk
+  static constexpr int XV = WT == 8 ? 8 : 16;       // packed x pairs per lane per chunk
+  static constexpr int MC = WT == 8 ? 4 : 2;        // max chunks per warp (register budget)
 };
 
-template <int WT>
-__device__ __forceinline__ size_t row_bytes(int nb) {
-  return WT == 8 ? (size_t)nb * 32 : (size_t)nb * 16;
-}
-
-struct Item {
-  uint4 v[R];
-  uint32_t d[R];   // fp16 bits of the scale (0 when the slot is empty)
-};
-
-template <int WT>
-__device__ __forceinline__ void load_item(Item& it, const MatDev& w, int row0, int nrows, int chunk, int lane) {
-  const int nb = w.nb;
-  const int kpad = nb * 32;
-  bool ok;
-  size_t qoff;
-  int blk;
-  if (WT == 8) {
-    const int col = chunk * 512 + lane * 16;
-    ok = col < kpad;
-    qoff = (size_t)col;
-    blk = col >> 5;
-  } else {
-    blk = chunk * 32 + lane;
-    ok = blk < nb;
-    qoff = (size_t)blk * 16;
-  }
-  const size_t rb = row_bytes<WT>(nb);
+template <int RS>
+__device__ __forceinline__ float butterfly(float (&acc)[RS], int lane) {
+  // After this, lane holds the warp total of row (lane >> (5 - log2 RS)).
+  if (RS == 1) return warp_sum(acc[0]);
+  float v[RS];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    if (ok && r < nrows) {
-      const int row = row0 + r;
-      it.v[r] = ld_stream(w.qs + (size_t)row * rb + qoff);
-      it.d[r] = ld_stream_u16(w.d + (size_t)row * nb + blk);
-    } else {
-      it.v[r] = make_uint4(0, 0, 0, 0);
-      it.d[r] = 0;
+  for (int i = 0; i < RS; ++i) v[i] = acc[i];
+  int n = RS, off = 16;
+#pragma unroll
+  for (; n > 1; n >>= 1, off >>= 1) {
+    const bool hi = lane & off;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float send = hi ? v[j] : v[n / 2 + j];
+      const float keep = hi ? v[n / 2 + j] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
     }
   }
-}
-
-template <int WT>
-__device__ __forceinline__ void compute_item(const Item& it, float (&acc)[R], const float* s_x, int nb, int chunk,
-                                             int lane) {
-  const int kpad = nb * 32;
-  if (WT == 8) {
-    const int col = chunk * 512 + lane * 16;
-    if (col >= kpad) return;
-    const float4* xv = reinterpret_cast<const float4*>(s_x + col);
-    f2_t x2[8];
+  float t = v[0];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const float4 t = xv[m];
-      x2[2 * m] = pk2(t.x, t.y);
-      x2[2 * m + 1] = pk2(t.z, t.w);
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      f2_t s = pk2(0.f, 0.f);
-      const uint32_t wv[4] = {it.v[r].x, it.v[r].y, it.v[r].z, it.v[r].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        f2_t p01, p23;
-        i8x4_to_f2(wv[k], p01, p23);
-        s = ffma2(p01, x2[2 * k], s);
-        s = ffma2(p23, x2[2 * k + 1], s);
-      }
-      const float2 sf = upk2(s);
-      acc[r] = fmaf(__half2float(__ushort_as_half((unsigned short)it.d[r])), sf.x + sf.y, acc[r]);
-    }
-  } else {
-    const int blk = chunk * 32 + lane;
-    if (blk >= nb) return;
-    const float4* xv = reinterpret_cast<const float4*>(s_x + blk * 32);
-    f2_t x2[16];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float4 t = xv[m];
-      x2[2 * m] = pk2(t.x, t.y);
-      x2[2 * m + 1] = pk2(t.z, t.w);
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      f2_t s = pk2(0.f, 0.f);
-      const uint32_t wv[4] = {it.v[r].x, it.v[r].y, it.v[r].z, it.v[r].w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        // bytes 4k..4k+3: low nibbles = elements 4k.., high nibbles = 16+4k..
-        const uint32_t lo = wv[k] & 0x0F0F0F0Fu;
-        const uint32_t hi = (wv[k] >> 4) & 0x0F0F0F0Fu;
-        f2_t a01, a23, b01, b23;
-        u4x4_to_f2(lo, a01, a23);
-        u4x4_to_f2(hi, b01, b23);
-        s = ffma2(a01, x2[2 * k], s);
-        s = ffma2(a23, x2[2 * k + 1], s);
-        s = ffma2(b01, x2[8 + 2 * k], s);
-        s = ffma2(b23, x2[8 + 2 * k + 1], s);
-      }
-      const float2 sf = upk2(s);
-      acc[r] = fmaf(__half2float(__ushort_as_half((unsigned short)it.d[r])), sf.x + sf.y, acc[r]);
-    }
-  }
-}
-
-// Sum acc[0..7] over the warp; the total of row (lane >> 2) & 7 ends in
-// every lane of that quad.
-__device__ __forceinline__ float butterfly8(const float (&acc)[R], int lane) {
-  float t4[4], t2[2];
-  const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float send = b16 ? acc[j] : acc[4 + j];
-    const float keep = b16 ? acc[4 + j] : acc[j];
-    t4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const float send = b8 ? t4[j] : t4[2 + j];
-    const float keep = b8 ? t4[2 + j] : t4[j];
-    t2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-  float t1 = (b4 ? t2[1] : t2[0]) + __shfl_xor_sync(0xffffffffu, b4 ? t2[0] : t2[1], 4);
-  t1 += __shfl_xor_sync(0xffffffffu, t1, 2);
-  t1 += __shfl_xor_sync(0xffffffffu, t1, 1);
-  return t1;
-}
-
-__device__ __forceinline__ float block_sum(float v, float* s_red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = warp_sum(v);
-  __syncthreads();
-  if (lane == 0) s_red[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-  for (int w = 0; w < nw; ++w) t += s_red[w];  // fixed order: deterministic
+  for (; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
   return t;
 }
 
-template <int WT, int PRO, int EPI>
-__global__ void __launch_bounds__(kMaxThreads) gemv_kernel(const GemvArgs a, const int rb_cap) {
-  extern __shared__ __align__(16) float smem[];
+// dot of 16 code bytes (one lane's slice of one row) with its activations
+template <int WT>
+__device__ __forceinline__ float dot16(uint4 q, const f2_t* xr) {
+  f2_t s = pk2(0.f, 0.f);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  if (WT == 8) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f2_t p01, p23;
+      i8x4_to_f2(w[k], p01, p23);
+      s = ffma2(p01, xr[2 * k], s);
+      s = ffma2(p23, xr[2 * k + 1], s);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // bytes 4k..: low nibbles = elements 4k.., high = 16+4k..
+      f2_t a01, a23, b01, b23;
+      u4x4_to_f2(w[k] & 0x0F0F0F0Fu, a01, a23);
+      u4x4_to_f2((w[k] >> 4) & 0x0F0F0F0Fu, b01, b23);
+      s = ffma2(a01, xr[2 * k], s);
+      s = ffma2(a23, xr[2 * k + 1], s);
+      s = ffma2(b01, xr[8 + 2 * k], s);
+      s = ffma2(b23, xr[8 + 2 * k + 1], s);
+    }
+  }
+  const float2 f = upk2(s);
+  return f.x + f.y;
+}
+
+struct Shared {
+  uint64_t full[16];
+  uint64_t empty[16];
+  float red[32];
+  float rs;
+  int abort;
+};
+
+template <int WT, int PRO, int EPI, int RS>
+__global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const GemvArgs a, const GemvLaunch L) {
+  using G = Geo<WT>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  float* s_part = reinterpret_cast<float*>(smem_raw + sizeof(Shared));   // [nwc][kRB]
+  uint8_t* ring = smem_raw + ((sizeof(Shared) + L.nwc * kRB * 4 + 127) & ~127);
   const MatDev& w = a.w;
   const int nb = w.nb, kpad = nb * 32, cols = w.cols;
-  const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* s_x = smem;                  // [kpad]
-  float* s_part = smem + kpad;        // [nw][rb_cap]
-  __shared__ float s_red[32];
+  const int nwc = L.nwc, NS = L.ns;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t row_bytes = WT == 8 ? (size_t)nb * 32 : (size_t)nb * 16;
+  const size_t drow_bytes = (size_t)w.ds * 2;
+  const uint32_t stage_q = RS * (uint32_t)row_bytes;
+  const uint32_t stage_bytes = stage_q + RS * (uint32_t)drow_bytes;
 
   const int units = (w.rows + a.unit - 1) / a.unit;
   const int u0 = (int)((long long)units * blockIdx.x / gridDim.x);
   const int u1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x);
   const int r0 = u0 * a.unit, r1 = min(w.rows, u1 * a.unit);
+  const int nrows = max(r1 - r0, 0);
+  const int nst = (nrows + RS - 1) / RS;
 
-  // Weights do not depend on the previous kernel: start pulling this CTA's
-  // slice into L2 before waiting for it.
-  if (threadIdx.x == 0 && r1 > r0) {
-    const size_t rbytes = row_bytes<WT>(nb);
-    const uint8_t* qa = w.qs + (size_t)r0 * rbytes;
-    const size_t qn = min((size_t)(r1 - r0) * rbytes, (size_t)kPrefetchBytes) & ~(size_t)15;
-    if (qn) prefetch_l2(qa, (uint32_t)qn);
-    const uintptr_t da = reinterpret_cast<uintptr_t>(w.d + (size_t)r0 * nb);
-    const uintptr_t da16 = da & ~(uintptr_t)15;
-    const size_t dn = (min((size_t)(r1 - r0) * nb * 2, (size_t)kPrefetchBytes / 16) + (da - da16)) & ~(size_t)15;
-    if (dn) prefetch_l2(reinterpret_cast<const void*>(da16), (uint32_t)dn);
-  }
-
-  griddep_wait();
-
-  // ---- prologue: activation vector -> shared memory
-  if (PRO == PRO_RMSNORM) {
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < cols; i += blockDim.x) {
-      const float v = a.x[i];
-      ss = fmaf(v, v, ss);
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&sh.full[s]), 1);
+      mbar_init(smem_u32(&sh.empty[s]), nwc);
     }
-    ss = block_sum(ss, s_red);
-    const float rs = 1.0f / sqrtf(ss / (float)cols + a.eps);
-    for (int i = threadIdx.x; i < kpad; i += blockDim.x) s_x[i] = i < cols ? a.x[i] * rs * a.g[i] : 0.f;
-  } else if (PRO == PRO_SWIGLU) {
-    for (int i = threadIdx.x; i < kpad; i += blockDim.x) s_x[i] = i < cols ? silu(a.x[i]) * a.x[cols + i] : 0.f;
-  } else {
-    for (int i = threadIdx.x; i < kpad; i += blockDim.x) s_x[i] = i < cols ? a.x[i] : 0.f;
+    sh.abort = 0;
+    mbar_fence_init();
   }
   __syncthreads();
-  griddep_launch();
 
-  constexpr int CH = Geo<WT>::CH;
-  const int nchunk = (kpad + CH - 1) / CH;
-  const int mc = warp < nchunk ? (nchunk - warp + nw - 1) / nw : 0;
-  const int nwa = min(nw, nchunk);
-
-  int32_t pos = 0, seq = 0;
-  if (EPI == EPI_QKV) {
-    pos = a.sp->pos[a.brow];
-    seq = a.sp->seq[a.brow];
-  }
-
-  for (int rb0 = r0; rb0 < r1; rb0 += rb_cap) {
-    const int rbn = min(rb_cap, r1 - rb0);
-    const int ngroups = (rbn + R - 1) / R;
-    const int nitems = ngroups * mc;
-    float acc[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = 0.f;
-    Item A, B;
-    auto item_rows = [&](int i, int& row0, int& nrows, int& chunk) {
-      const int g = i / mc, j = i - g * mc;
-      row0 = rb0 + g * R;
-      nrows = min(R, rb0 + rbn - row0);
-      chunk = warp + j * nw;
-    };
-    auto finish_group = [&](int i) {
-      const int g = i / mc;
-      const float t = butterfly8(acc, lane);
-      const int rr = g * R + ((lane >> 2) & 7);
-      if ((lane & 3) == 0 && rr < rbn) s_part[warp * rb_cap + rr] = t;
-#pragma unroll
-      for (int r = 0; r < R; ++r) acc[r] = 0.f;
-    };
-    if (nitems > 0) {
-      int row0, nrows, chunk;
-      item_rows(0, row0, nrows, chunk);
-      load_item<WT>(A, w, row0, nrows, chunk, lane);
-    }
-    for (int i = 0; i < nitems; i += 2) {
-      int row0, nrows, chunk;
-      if (i + 1 < nitems) {
-        item_rows(i + 1, row0, nrows, chunk);
-        load_item<WT>(B, w, row0, nrows, chunk, lane);
-      }
-      item_rows(i, row0, nrows, chunk);
-      compute_item<WT>(A, acc, s_x, nb, chunk, lane);
-      if ((i % mc) == mc - 1) finish_group(i);
-      if (i + 1 < nitems) {
-        if (i + 2 < nitems) {
-          item_rows(i + 2, row0, nrows, chunk);
-          load_item<WT>(A, w, row0, nrows, chunk, lane);
+  if (warp == nwc) {
+    // ---------------- producer: stream this CTA's rows through the ring
+    if (lane == 0) {
+      int issued = 0;
+      for (int s = 0; s < nst; ++s) {
+        const int slot = s % NS;
+        if (s >= NS && !mbar_wait(smem_u32(&sh.empty[slot]), ((s / NS) - 1) & 1)) {
+          atomicOr(&a.sp->status, kTimeout);
+          sh.abort = 1;
+          break;
         }
-        item_rows(i + 1, row0, nrows, chunk);
-        compute_item<WT>(B, acc, s_x, nb, chunk, lane);
-        if (((i + 1) % mc) == mc - 1) finish_group(i + 1);
+        const int rows_s = min(RS, nrows - s * RS);
+        const int row = r0 + s * RS;
+        uint8_t* dst = ring + (size_t)slot * stage_bytes;
+        const uint32_t qb = rows_s * (uint32_t)row_bytes, db = rows_s * (uint32_t)drow_bytes;
+        const uint32_t bar = smem_u32(&sh.full[slot]);
+        mbar_expect_tx(bar, qb + db);
+        bulk_g2s(smem_u32(dst), w.qs + (size_t)row * row_bytes, qb, bar);
+        bulk_g2s(smem_u32(dst + stage_q), reinterpret_cast<const uint8_t*>(w.d) + (size_t)row * drow_bytes, db, bar);
+        ++issued;
       }
+      // never leave with copies in flight: wait for every issued stage
+      for (int s = max(0, issued - NS); s < issued; ++s)
+        mbar_wait(smem_u32(&sh.full[s % NS]), (s / NS) & 1);
     }
-    __syncthreads();
-
-    // ---- cross-warp reduction (fixed order) and epilogue
-    if (EPI == EPI_QKV) {
-      const int hd = a.kv.head_dim;
-      for (int pi = threadIdx.x; pi < (rbn >> 1); pi += blockDim.x) {
-        const int rr = pi * 2, r = rb0 + rr;
+  } else {
+    // ---------------- consumers
+    griddep_wait();
+    // prologue: this lane's activation slice, in registers
+    if (PRO == PRO_RMSNORM) {
+      float ss = 0.f;
+      const int n4 = cols >> 2;
+      const float4* x4 = reinterpret_cast<const float4*>(a.x);
+      for (int i = tid; i < n4; i += nwc * 32) {
+        const float4 v = x4[i];
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+      }
+      for (int i = (n4 << 2) + tid; i < cols; i += nwc * 32) ss = fmaf(a.x[i], a.x[i], ss);
+      ss = warp_sum(ss);
+      if (lane == 0) sh.red[warp] = ss;
+      named_bar(1, nwc * 32);
+      if (tid == 0) {
+        float t = 0.f;
+        for (int i = 0; i < nwc; ++i) t += sh.red[i];  // fixed order
+        sh.rs = 1.0f / sqrtf(t / (float)cols + a.eps);
+      }
+      named_bar(1, nwc * 32);
+    }
+    const int nchunk = (kpad + G::CH - 1) / G::CH;
+    const int mc = warp < nchunk ? min(G::MC, (nchunk - warp + nwc - 1) / nwc) : 0;
+    f2_t xr[G::MC][G::XV];
+    bool valid[G::MC];
+#pragma unroll
+    for (int k = 0; k < G::MC; ++k) {
+      const int c = warp + k * nwc;
+      const int col0 = WT == 8 ? c * 512 + lane * 16 : (c * 32 + lane) * 32;
+      valid[k] = k < mc && col0 < kpad;
+#pragma unroll
+      for (int e = 0; e < G::XV; ++e) {
         float v0 = 0.f, v1 = 0.f;
-        for (int ww = 0; ww < nwa; ++ww) {
-          v0 += s_part[ww * rb_cap + rr];
-          v1 += s_part[ww * rb_cap + rr + 1];
-        }
-        if (r < a.q_rows + a.kv_rows) {  // q or k: rotate the adjacent pair
-          if (pos < 0 || pos >= a.rope_len) {
-            atomicOr(&a.sp->status, kBadPos);
-            continue;
+        const int i0 = col0 + 2 * e;
+        if (valid[k]) {
+          if (i0 < cols) {
+            if (PRO == PRO_SWIGLU) v0 = silu(a.x[i0]) * a.x[cols + i0];
+            else v0 = a.x[i0];
+            if (PRO == PRO_RMSNORM) v0 *= sh.rs * a.g[i0];
           }
-          const int i = (r % hd) >> 1;
-          const float2 cs = a.rope_cs[(size_t)pos * (hd >> 1) + i];
-          const float t0 = v0 * cs.x - v1 * cs.y;
-          const float t1 = v0 * cs.y + v1 * cs.x;
-          v0 = t0;
-          v1 = t1;
-        }
-        if (r < a.q_rows) {
-          a.y[r] = v0;
-          a.y[r + 1] = v1;
-        } else {
-          const bool is_k = r < a.q_rows + a.kv_rows;
-          const int rk = r - a.q_rows - (is_k ? 0 : a.kv_rows);
-          const int kvh = rk / hd, dim = rk % hd;
-          const int pt = a.kv.page_tokens;
-          const int lp = pos / pt;
-          const int page = (pos >= 0 && lp < a.kv.max_pages) ? a.kv.page_table[(size_t)seq * a.kv.max_pages + lp] : -1;
-          if (page < 0) {
-            atomicOr(&a.sp->status, kBadPage);
-            continue;
+          if (i0 + 1 < cols) {
+            if (PRO == PRO_SWIGLU) v1 = silu(a.x[i0 + 1]) * a.x[cols + i0 + 1];
+            else v1 = a.x[i0 + 1];
+            if (PRO == PRO_RMSNORM) v1 *= sh.rs * a.g[i0 + 1];
           }
-          const size_t off = (((size_t)page * a.kv.n_kv + kvh) * pt + (pos % pt)) * hd + dim;
-          __half* dst = (is_k ? a.kv.k_pool : a.kv.v_pool) + off;
-          *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(v0, v1);
         }
-      }
-    } else {
-      for (int rr = threadIdx.x; rr < rbn; rr += blockDim.x) {
-        float v = 0.f;
-        for (int ww = 0; ww < nwa; ++ww) v += s_part[ww * rb_cap + rr];
-        if (EPI == EPI_RESID) a.y[rb0 + rr] += v;
-        else a.y[rb0 + rr] = v;
+        xr[k][e] = pk2(v0, v1);
       }
     }
-    __syncthreads();
+    griddep_launch();
+
+    int32_t pos = 0, seq = 0;
+    if (EPI == EPI_QKV) {
+      pos = a.sp->pos[a.brow];
+      seq = a.sp->seq[a.brow];
+    }
+    const int stages_per_block = kRB / RS;
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % NS;
+      if (!sh.abort && !mbar_wait(smem_u32(&sh.full[slot]), (s / NS) & 1)) {
+        atomicOr(&a.sp->status, kTimeout);
+        sh.abort = 1;
+      }
+      const int rows_s = min(RS, nrows - s * RS);
+      const uint8_t* st = ring + (size_t)slot * stage_bytes;
+      float acc[RS];
+#pragma unroll
+      for (int rr = 0; rr < RS; ++rr) acc[rr] = 0.f;
+      if (!sh.abort) {
+#pragma unroll
+        for (int k = 0; k < G::MC; ++k) {
+          if (!valid[k]) continue;
+          const int c = warp + k * nwc;
+          const int qoff = WT == 8 ? c * 512 + lane * 16 : (c * 32 + lane) * 16;
+          const int blk = WT == 8 ? (c * 512 + lane * 16) >> 5 : c * 32 + lane;
+#pragma unroll
+          for (int rr = 0; rr < RS; ++rr) {
+            if (rr < rows_s) {
+              const uint4 q = *reinterpret_cast<const uint4*>(st + rr * row_bytes + qoff);
+              const __half d = *reinterpret_cast<const __half*>(st + stage_q + rr * drow_bytes + blk * 2);
+              acc[rr] = fmaf(__half2float(d), dot16<WT>(q, xr[k]), acc[rr]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.empty[slot]));
+      const float t = butterfly<RS>(acc, lane);
+      const int rr = RS == 1 ? 0 : (lane >> (5 - (RS == 2 ? 1 : RS == 4 ? 2 : 3)));
+      const int lrow = s * RS + rr - (s / stages_per_block) * kRB;
+      if ((lane & ((32 / RS) - 1)) == 0 && rr < rows_s) s_part[warp * kRB + lrow] = t;
+
+      // ---- end of an epilogue block (or the last stage): reduce + epilogue
+      if ((s + 1) % stages_per_block == 0 || s == nst - 1) {
+        named_bar(1, nwc * 32);
+        const int b0 = r0 + (s / stages_per_block) * kRB;
+        const int bn = min(kRB, r1 - b0);
+        const int nwa = min(nwc, nchunk);
+        if (EPI == EPI_QKV) {
+          const int hd = a.kv.head_dim;
+          for (int pi = tid; pi < (bn >> 1); pi += nwc * 32) {
+            const int lr = pi * 2, r = b0 + lr;
+            float v0 = 0.f, v1 = 0.f;
+            for (int ww = 0; ww < nwa; ++ww) {
+              v0 += s_part[ww * kRB + lr];
+              v1 += s_part[ww * kRB + lr + 1];
+            }
+            if (r < a.q_rows + a.kv_rows) {  // q or k: rotate the adjacent pair
+              if (pos < 0 || pos >= a.rope_len) {
+                atomicOr(&a.sp->status, kBadPos);
+                continue;
+              }
+              const float2 cs = a.rope_cs[(size_t)pos * (hd >> 1) + ((r % hd) >> 1)];
+              const float t0 = v0 * cs.x - v1 * cs.y;
+              v1 = v0 * cs.y + v1 * cs.x;
+              v0 = t0;
+            }
+            if (r < a.q_rows) {
+              a.y[r] = v0;
+              a.y[r + 1] = v1;
+            } else {
+              const bool is_k = r < a.q_rows + a.kv_rows;
+              const int rk = r - a.q_rows - (is_k ? 0 : a.kv_rows);
+              const int kvh = rk / hd, dim = rk % hd;
+              const int pt = a.kv.page_tokens;
+              const int lp = pos / pt;
+              const int page =
+                  (pos >= 0 && lp < a.kv.max_pages) ? a.kv.page_table[(size_t)seq * a.kv.max_pages + lp] : -1;
+              if (page < 0) {
+                atomicOr(&a.sp->status, kBadPage);
+                continue;
+              }
+              const size_t off = (((size_t)page * a.kv.n_kv + kvh) * pt + (pos % pt)) * hd + dim;
+              __half* dst = (is_k ? a.kv.k_pool : a.kv.v_pool) + off;
+              *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(v0, v1);
+            }
+          }
+        } else {
+          for (int lr = tid; lr < bn; lr += nwc * 32) {
+            float v = 0.f;
+            for (int ww = 0; ww < nwa; ++ww) v += s_part[ww * kRB + lr];
+            if (EPI == EPI_RESID) a.y[b0 + lr] += v;
+            else a.y[b0 + lr] = v;
+          }
+        }
+        named_bar(1, nwc * 32);
+      }
+    }
   }
+  __syncthreads();
 }
 
-template <int WT, int PRO, int EPI>
-constexpr auto kernel_ptr() {
-  return &gemv_kernel<WT, PRO, EPI>;
+using KernelFn = void (*)(const GemvArgs, const GemvLaunch);
+
+template <int WT, int P, int E>
+KernelFn pick_rs(int rs) {
+  switch (rs) {
+    case 1: return &gemv_kernel<WT, P, E, 1>;
+    case 2: return &gemv_kernel<WT, P, E, 2>;
+    case 4: return &gemv_kernel<WT, P, E, 4>;
+    case 8: return &gemv_kernel<WT, P, E, 8>;
+  }
+  return nullptr;
 }
 
-using KernelFn = void (*)(const GemvArgs, const int);
-
-KernelFn pick(int wtype, int pro, int epi) {
+KernelFn pick(int wtype, int pro, int epi, int rs) {
 #define DLS_PICK(WT, P, E) \
-  if (wtype == WT && pro == P && epi == E) return kernel_ptr<WT, P, E>();
+  if (wtype == WT && pro == P && epi == E) return pick_rs<WT, P, E>(rs);
   DLS_PICK(8, PRO_RMSNORM, EPI_QKV)
   DLS_PICK(8, PRO_COPY, EPI_RESID)
   DLS_PICK(8, PRO_RMSNORM, EPI_STORE)
@@ -357,32 +342,42 @@ KernelFn pick(int wtype, int pro, int epi) {
   return nullptr;
 }
 
-constexpr int kRbCapRows = 2048;
-
 }  // namespace
 
 GemvLaunch gemv_plan(int wtype, int rows, int nb, int num_sms, int unit) {
   const int kpad = nb * 32;
   const int CH = wtype == 8 ? 512 : 1024;
+  const int MC = wtype == 8 ? 4 : 2;
   const int nchunk = (kpad + CH - 1) / CH;
-  // warps per CTA: the largest divisor of the chunk count that is <= 8, so
-  // every warp owns the same number of chunks
-  int nw = 1;
+  // consumer warps: the largest divisor of the chunk count <= 8 that keeps
+  // chunks per warp within the register budget; else a divisor up to 14;
+  // else an uneven split
+  int nwc = 0;
   for (int d = 1; d <= 8; ++d)
-    if (nchunk % d == 0) nw = d;
-  if (nchunk > 8 && nw < 4) nw = 8;  // awkward counts: accept a short last round
-  const int ctas_per_sm = nw >= 8 ? 1 : (nw >= 4 ? 2 : 4);
+    if (nchunk % d == 0 && nchunk / d <= MC) nwc = d;
+  if (!nwc)
+    for (int d = 9; d <= kMaxConsumers && !nwc; ++d)
+      if (nchunk % d == 0 && nchunk / d <= MC) nwc = d;
+  if (!nwc) nwc = std::min(kMaxConsumers, (nchunk + MC - 1) / MC);
+  const int row_bytes = wtype == 8 ? nb * 32 : nb * 16;
+  const int ds = (nb + 7) & ~7;
+  int rs = 1;
+  while (rs < 8 && (rs * 2) * row_bytes <= kStageCodes) rs *= 2;
+  const int stage = rs * row_bytes + rs * ds * 2;
+  int ns = kRingBytes / stage;
+  ns = std::max(2, std::min(16, ns));
   const int units = (rows + unit - 1) / unit;
-  int grid = num_sms * ctas_per_sm;
-  if (grid > units) grid = units;
+  int grid = std::min(num_sms, units);
   if (grid < 1) grid = 1;
-  const int rows_cta = ((units + grid - 1) / grid) * unit;
-  int rb = rows_cta < kRbCapRows ? rows_cta : kRbCapRows;
-  rb = (rb + 1) & ~1;
   GemvLaunch l;
   l.grid = grid;
-  l.threads = nw * 32;
-  l.smem = (kpad + nw * rb) * 4;
+  l.threads = (nwc + 1) * 32;
+  l.nwc = nwc;
+  l.rs = rs;
+  l.ns = ns;
+  l.mc = (nchunk + nwc - 1) / nwc;
+  const int head = (int)((sizeof(Shared) + nwc * kRB * 4 + 127) & ~127);
+  l.smem = head + ns * stage;
   return l;
 }
 
@@ -391,21 +386,20 @@ cudaError_t gemv_setup_attributes() {
   const int epis[3] = {EPI_STORE, EPI_RESID, EPI_QKV};
   for (int wt : {8, 4})
     for (int p : pros)
-      for (int e : epis) {
-        KernelFn f = pick(wt, p, e);
-        if (!f) continue;
-        cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (err != cudaSuccess) return err;
-      }
+      for (int e : epis)
+        for (int rs : {1, 2, 4, 8}) {
+          KernelFn f = pick(wt, p, e, rs);
+          if (!f) continue;
+          cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+          if (err != cudaSuccess) return err;
+        }
   return cudaSuccess;
 }
 
 cudaError_t launch_gemv(int wtype, int pro, int epi, const GemvArgs& a, const GemvLaunch& l, cudaStream_t s,
                         bool pdl) {
-  KernelFn f = pick(wtype, pro, epi);
-  if (!f) return cudaErrorInvalidValue;
-  const int nw = l.threads / 32;
-  const int rb = (l.smem / 4 - a.w.nb * 32) / nw;
+  KernelFn f = pick(wtype, pro, epi, l.rs);
+  if (!f || l.ns > 16 || l.nwc > kMaxConsumers || a.w.ds % 8) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(l.grid);
   cfg.blockDim = dim3(l.threads);
@@ -416,7 +410,7 @@ cudaError_t launch_gemv(int wtype, int pro, int epi, const GemvArgs& a, const Ge
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, f, a, rb);
+  return cudaLaunchKernelEx(&cfg, f, a, l);
 }
 
 }  // namespace dls

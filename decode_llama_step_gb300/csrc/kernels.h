@@ -3,6 +3,8 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dls {
@@ -37,6 +39,10 @@ struct GemvArgs {
 
 struct GemvLaunch {
   int grid, threads, smem;
+  int nwc;  // consumer warps (plus one producer warp)
+  int rs;   // rows per ring stage
+  int ns;   // ring stages
+  int mc;   // K-chunks per consumer warp
 };
 
 // Choose grid/threads/smem for a matrix and check the kernel can run it.
@@ -81,12 +87,15 @@ cudaError_t launch_argmax(const float* logits, int vocab, int rows, int32_t* out
 cudaError_t launch_advance(StepParams* sp, const int32_t* next, int32_t* tokens_out, int rows, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_set_params(StepParams* sp, const StepParams& h, bool reset_step, cudaStream_t s);
-cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, uint8_t* qs, __half* d, cudaStream_t s);
+cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, int ds, uint8_t* qs, __half* d,
+                          cudaStream_t s);
 cudaError_t launch_rope_table(float2* cs, int len, int head_dim, float theta, cudaStream_t s);
 cudaError_t launch_dequant(const MatDev& m, int wtype, float* out, cudaStream_t s);
 // copy whole KV pages: pairs[i] = (src_page, dst_page), for every layer
 cudaError_t launch_kv_copy(__half* k_pool, __half* v_pool, size_t layer_stride_elems, int n_layers,
                            size_t page_elems, const int2* pairs, int n_pairs, cudaStream_t s);
+// spin (bounded by the global timer) for `ns` nanoseconds on the stream
+cudaError_t launch_delay(long long ns, cudaStream_t s);
 cudaError_t launch_kv_gather(const __half* pool, const int32_t* pages, int len, int n_kv, int page_tokens,
                              int head_dim, __half* out, cudaStream_t s);
 

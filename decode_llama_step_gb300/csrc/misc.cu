@@ -25,7 +25,7 @@ cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, cudaStream_t s, boo
 // one dequantised weight: exact in fp32 (11-bit scale times a code of at most 8 bits)
 __device__ __forceinline__ float dq(const MatDev& m, int wtype, int row, int col) {
   const int blk = col >> 5, e = col & 31;
-  const float d = __half2float(m.d[(size_t)row * m.nb + blk]);
+  const float d = __half2float(m.d[(size_t)row * m.ds + blk]);
   if (wtype == 8) {
     const uint32_t u = (uint32_t)m.qs[(size_t)row * m.nb * 32 + col] ^ 0x80u;
     return d * (mag_byte(u, 0) - 8388736.0f);
@@ -124,12 +124,13 @@ __global__ void set_params_kernel(StepParams* sp, const StepParams h, int reset_
 // ---------------------------------------------------------------- weight layout
 
 // GGUF-style blocks (2-byte scale + codes) -> scale array + code array
-__global__ void repack_kernel(const uint8_t* src, int wtype, long long n_blocks, uint8_t* qs, __half* d) {
+__global__ void repack_kernel(const uint8_t* src, int wtype, long long n_blocks, int nb, int ds, uint8_t* qs,
+                              __half* d) {
   const int bsz = wtype == 8 ? 34 : 18, nq = bsz - 2;
   for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < n_blocks;
        b += (long long)gridDim.x * blockDim.x) {
     const uint8_t* s = src + b * bsz;
-    d[b] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
+    d[(b / nb) * ds + (b % nb)] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
     uint8_t* q = qs + b * nq;
     for (int i = 0; i < nq; ++i) q[i] = s[2 + i];
   }
@@ -188,6 +189,16 @@ __global__ void kv_gather_kernel(const __half* pool, const int32_t* pages, int l
   }
 }
 
+__global__ void delay_kernel(long long ns) {
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (int i = 0; i < (1 << 24); ++i) {  // bounded: at most ~16M polls
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if ((long long)(t - t0) >= ns) break;
+    __nanosleep(1000);
+  }
+}
+
 int grid_for(long long n, int threads) {
   long long g = (n + threads - 1) / threads;
   if (g > 4096) g = 4096;
@@ -220,9 +231,10 @@ cudaError_t launch_set_params(StepParams* sp, const StepParams& h, bool reset_st
   return cudaGetLastError();
 }
 
-cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, uint8_t* qs, __half* d, cudaStream_t s) {
+cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, int ds, uint8_t* qs, __half* d,
+                          cudaStream_t s) {
   const long long n = (long long)rows * nb;
-  repack_kernel<<<grid_for(n, 256), 256, 0, s>>>(src, wtype, n, qs, d);
+  repack_kernel<<<grid_for(n, 256), 256, 0, s>>>(src, wtype, n, nb, ds, qs, d);
   return cudaGetLastError();
 }
 
@@ -247,6 +259,11 @@ cudaError_t launch_kv_copy(__half* k_pool, __half* v_pool, size_t layer_stride_e
     kv_copy_kernel<<<dim3(gx, np, 2 * n_layers), 256, 0, s>>>(k_pool, v_pool, layer_stride_elems, page_elems,
                                                                  pairs + p0);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_delay(long long ns, cudaStream_t s) {
+  delay_kernel<<<1, 1, 0, s>>>(ns);
   return cudaGetLastError();
 }
 

@@ -78,6 +78,7 @@ _SIGS = {
     "dls_debug_dequant": (ctypes.c_int, [vp, i32, i32, vp]),
     "dls_debug_gemv": (ctypes.c_int, [vp, i32, i32, vp, vp]),
     "dls_debug_launches_per_step": (i32, [vp]),
+    "dls_debug_profile_step": (ctypes.c_int, [vp, i32, i32, i32, i32, vp, vp, vp]),
 }
 
 
@@ -322,6 +323,15 @@ class Model:
 
     def debug_gemv(self, layer: int, tensor: str, x, y):
         self._c(self.lib.dls_debug_gemv(self.handle, layer, TENSOR_IDS[tensor], _ptr(x), _ptr(y)))
+
+    def profile_step(self, seq: int, token: int, pos: int, max_kernels: int = 4096):
+        """(durations_ms, kinds) of every kernel of one decode step."""
+        ms = np.zeros(max_kernels, dtype=np.float32)
+        kinds = np.zeros(max_kernels, dtype=np.int32)
+        n = i32()
+        self._c(self.lib.dls_debug_profile_step(self.handle, seq, int(token), int(pos), max_kernels, ms.ctypes.data,
+                                                kinds.ctypes.data, ctypes.byref(n)))
+        return ms[: n.value].copy(), kinds[: n.value].copy()
 
     def launches_per_step(self) -> int:
         return int(self.lib.dls_debug_launches_per_step(self.handle))

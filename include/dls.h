@@ -122,9 +122,9 @@ typedef struct dls_model_desc {
 
 /* Validate `desc`, place the weights (re-laid-out for the kernels) and the
  * paged KV pool on the device, and return a model in *out.
- * Shapes: hidden, n_heads*head_dim and ffn multiples of 32 are not required
- * except hidden % 32 == 0 and head_dim even, head_dim <= 256, n_heads a
- * multiple of n_kv_heads.  With device_budget_bytes set, as many layers as
+ * Shape rules (else DLS_ERR_ARG): hidden a multiple of 32; head_dim 32, 64
+ * or 128; n_heads a multiple of n_kv_heads with at most 16 query heads per
+ * KV head; ffn and vocab any positive size.  With device_budget_bytes set, as many layers as
  * fit stay resident (first layers first) and the rest are streamed from
  * pinned host memory each step; DLS_ERR_BUDGET if not even that fits.
  * `cuda_stream` (cudaStream_t) orders all work; NULL makes a private stream.
@@ -241,6 +241,14 @@ int dls_debug_dequant(dls_model* m, int32_t layer, int32_t tensor, float* out);
 /* y = W x with the decode GEMV kernel for one matrix (ids as above);
  * x device fp32 [cols], y device fp32 [rows]. */
 int dls_debug_gemv(dls_model* m, int32_t layer, int32_t tensor, const float* x, float* y);
+/* One decode step (same contract as dls_decode_step, logits left in the
+ * model's buffer) run with a CUDA event after every kernel and without
+ * programmatic dependent launch, so each kernel's device time is measured
+ * alone.  Writes up to max_kernels durations (host float ms) and kernel
+ * kinds (host int32: 1 embedding, 2 QKV GEMV, 3 attention, 4 O GEMV, 5
+ * gate/up GEMV, 6 down GEMV, 7 LM head GEMV) and the count to *n_kernels. */
+int dls_debug_profile_step(dls_model* m, int32_t seq, int32_t token, int32_t pos, int32_t max_kernels,
+                           float* kernel_ms, int32_t* kernel_kind, int32_t* n_kernels);
 /* Kernel launches issued by the last decode / generate step (all of this
  * library's kernels, per step). */
 int32_t dls_debug_launches_per_step(const dls_model* m);
