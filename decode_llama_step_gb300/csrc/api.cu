@@ -2,6 +2,7 @@
 // pool, CUDA-graph replay of the decode step, two-buffer layer streaming and
 // the KV fork.  Host logic only; the arithmetic is in the kernels.
 #include <stdarg.h>
+#include <stdlib.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -131,6 +132,9 @@ struct dls_model {
   int launch_count = 0;
   // per-kernel timing (dls_debug_profile_step): an event after every launch
   bool profiling = false;
+  // programmatic dependent launch between the step's kernels; off by default
+  // (measured slower on this path), DLS_PDL=1 turns it on
+  bool pdl = false;
   std::vector<cudaEvent_t> prof_events;
   std::vector<int> prof_kinds;
   std::string err;
@@ -320,7 +324,7 @@ int enqueue_copy_layer(dls_model* m, int l) {
 
 int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
   cudaStream_t s = m->stream;
-  const bool pdl = !m->profiling;  // profiled kernels run strictly one after another
+  const bool pdl = m->pdl && !m->profiling;  // profiled kernels run strictly one after another
   float* x = m->x + (size_t)b * m->H;
   float* logits = m->logits + (size_t)b * m->V;
   LK(K_EMBED, launch_embed(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp, b, x, m->V, s, pdl));
@@ -426,7 +430,7 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
 int enqueue_step(dls_model* m, int rows, bool head, bool argmax, float* capture) {
   m->launch_count = 0;
   for (int b = 0; b < rows; ++b) TRY(enqueue_row(m, b, head, argmax, b == 0 ? capture : nullptr));
-  if (argmax) LK(K_ADVANCE, launch_advance(m->sp, m->next_tok, m->tokens_dev, rows, m->stream, true));
+  if (argmax) LK(K_ADVANCE, launch_advance(m->sp, m->next_tok, m->tokens_dev, rows, m->stream, m->pdl));
   m->launches_per_step = m->launch_count;
   return DLS_OK;
 }
@@ -703,6 +707,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
     m->alloc = *allocator;
     m->have_alloc = true;
   }
+  if (const char* e = getenv("DLS_PDL")) m->pdl = atoi(e) != 0;
   auto bail = [&](int r) {
     std::string e = m->err;
     destroy(m);
@@ -754,11 +759,11 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   cur = 0;
   m->out_off = mat_off(cur, m->V, m->H, m->wtype);
 
-  m->plan_qkv = gemv_plan(m->wtype, m->lay.qkv.rows, m->lay.qkv.nb, m->num_sms, 2);
-  m->plan_o = gemv_plan(m->wtype, m->lay.o.rows, m->lay.o.nb, m->num_sms, 1);
-  m->plan_gu = gemv_plan(m->wtype, m->lay.gu.rows, m->lay.gu.nb, m->num_sms, 1);
-  m->plan_down = gemv_plan(m->wtype, m->lay.down.rows, m->lay.down.nb, m->num_sms, 1);
-  m->plan_head = gemv_plan(m->wtype, m->V, m->emb_off.nb, m->num_sms, 1);
+  m->plan_qkv = gemv_plan(m->wtype, PRO_RMSNORM, EPI_QKV, m->lay.qkv.rows, m->lay.qkv.nb, m->num_sms, 2);
+  m->plan_o = gemv_plan(m->wtype, PRO_COPY, EPI_RESID, m->lay.o.rows, m->lay.o.nb, m->num_sms, 1);
+  m->plan_gu = gemv_plan(m->wtype, PRO_RMSNORM, EPI_STORE, m->lay.gu.rows, m->lay.gu.nb, m->num_sms, 1);
+  m->plan_down = gemv_plan(m->wtype, PRO_SWIGLU, EPI_RESID, m->lay.down.rows, m->lay.down.nb, m->num_sms, 1);
+  m->plan_head = gemv_plan(m->wtype, PRO_RMSNORM, EPI_STORE, m->V, m->emb_off.nb, m->num_sms, 1);
   m->attn_splits = attn_default_splits(1, m->nkv, m->num_sms, m->max_ctx);
 
   // fixed allocations (everything but the layers)
@@ -1140,7 +1145,7 @@ int dls_debug_gemv(dls_model* m, int32_t layer, int32_t tensor, const float* x, 
   g.unit = 1;
   g.x = x;
   g.y = y;
-  const GemvLaunch l = gemv_plan(m->wtype, md.rows, md.nb, m->num_sms, 1);
+  const GemvLaunch l = gemv_plan(m->wtype, PRO_COPY, EPI_STORE, md.rows, md.nb, m->num_sms, 1);
   CK(launch_gemv(m->wtype, PRO_COPY, EPI_STORE, g, l, m->stream, false));
   return DLS_OK;
 }

@@ -20,9 +20,11 @@ namespace dls {
 
 namespace {
 
-constexpr int TILE = 32;
-constexpr int NT = 128;
+constexpr int TILE = 32;   // tokens per tile: one lane per token when scoring
+constexpr int NW = 4;      // warps per CTA
+constexpr int NT = 32 * NW;
 constexpr int kMaxG = 16;
+constexpr int kMaxSplits = 128;
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -30,39 +32,37 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-constexpr int NSTAGE = 4;   // K/V tile ring depth
-
-template <int HD>
+// CTA (kv head, split sp) covers a contiguous run of 32-token tiles of one
+// sequence; warp w takes tiles w, w + 4, ... of that run.  Per tile a warp
+// bulk-copies K and V into its own shared-memory stage, scores the tile with
+// one lane per token (the head dimension walked from a lane-dependent start
+// so the 32 lanes read 32 different banks), updates its online softmax for
+// the G query heads of the group in registers, and accumulates P V with each
+// lane owning HD/32 output dimensions.  The 4 warps then merge in shared
+// memory into one (m, l, o) partial per CTA; the last CTA of a (row, kv
+// head) merges the S partials in split order.
+template <int HD, int G>
 __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
-  constexpr int DPL = HD / 32;            // dims per lane when scoring
-  constexpr int HPT = NT / HD;            // head slots per pass (threads share d)
-  constexpr int OPT = (kMaxG + HPT - 1) / HPT;
-  constexpr int TILE_B = TILE * HD * 2;   // bytes of one K (or V) tile
-  constexpr int kMaxSplits = 128;
+  constexpr int DPL = HD / 32;              // output dims per lane
+  constexpr int W2 = HD / 2;                // 2-element words per row
+  constexpr int STAGE = 2 * TILE * HD;      // halves per warp stage (K then V)
   extern __shared__ __align__(128) uint8_t s_dyn[];
-  // K/V tile ring in dynamic shared memory: [NSTAGE][K|V][TILE*HD] halves
-  auto kv_tile = [&](int st, int which) { return reinterpret_cast<__half*>(s_dyn) + ((size_t)st * 2 + which) * TILE * HD; };
-  __shared__ __align__(16) float s_q[kMaxG * HD];
-  __shared__ float s_s[kMaxG][TILE];
-  __shared__ float s_alpha[kMaxG], s_m[kMaxG], s_l[kMaxG];
-  __shared__ __align__(8) uint64_t s_full[NSTAGE];
-  __shared__ float s_w[kMaxG][kMaxSplits];
+  __half* s_stage = reinterpret_cast<__half*>(s_dyn);          // [NW][STAGE]
+  __shared__ __align__(16) float s_q[G * HD];
+  __shared__ float s_wm[NW][G], s_wl[NW][G];
+  __shared__ __align__(8) uint64_t s_full[NW];
+  __shared__ float s_w[G][kMaxSplits];
   __shared__ int s_last;
 
-  const int g = a.n_heads / a.n_kv;
   const int S = a.n_splits;
   const int kvh = blockIdx.x / S, sp = blockIdx.x - kvh * S;
   const int brel = blockIdx.y, b = a.row0 + brel;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int d = tid % HD, hslot = tid / HD;
   const int pt = a.page_tokens;
 
-  if (tid == 0) {
-    for (int i = 0; i < NSTAGE; ++i) mbar_init(smem_u32(&s_full[i]), 1);
-    mbar_fence_init();
-  }
+  if (lane == 0) mbar_init(smem_u32(&s_full[warp]), 1);
+  mbar_fence_init();
   griddep_wait();
-  griddep_launch();
 
   int n = a.len[b] + a.len_add;
   if (n < 1 || n > a.max_len) {
@@ -71,17 +71,17 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   }
   const int ptrow = a.pt_row ? a.pt_row[b] : b;
   const int32_t* ptab = a.page_table + (size_t)ptrow * a.max_pages;
-  int per = (n + S - 1) / S;
-  per = (per + TILE - 1) / TILE * TILE;
-  const int t0 = sp * per, t1 = min(n, t0 + per);
-  const int ntiles = t1 > t0 ? (t1 - t0 + TILE - 1) / TILE : 0;
+  const int n_tiles = (n + TILE - 1) / TILE;
+  const int per = (n_tiles + S - 1) / S;
+  const int tb = sp * per, te = min(n_tiles, tb + per);
 
-  // thread 0 issues the K and V copies of a tile (a tile never crosses a page)
+  // lane 0 of a warp copies tile i (K then V) into the warp's stage
+  __half* st = s_stage + (size_t)warp * STAGE;
+  const uint32_t bar = smem_u32(&s_full[warp]);
   auto issue = [&](int i) -> bool {
-    const int t = t0 + i * TILE;
-    const int nt = min(TILE, t1 - t);
+    const int t = i * TILE;
+    const int nt = min(TILE, n - t);
     const int page = ptab[t / pt];
-    const uint32_t bar = smem_u32(&s_full[i % NSTAGE]);
     if (page < 0) {
       mbar_arrive(bar);  // complete the phase with nothing copied
       return false;
@@ -89,89 +89,123 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
     const size_t base = (((size_t)page * a.n_kv + kvh) * pt + (t % pt)) * HD;
     const uint32_t bytes = (uint32_t)nt * HD * 2;
     mbar_expect_tx(bar, 2 * bytes);
-    bulk_g2s(smem_u32(kv_tile(i % NSTAGE, 0)), a.k_pool + base, bytes, bar);
-    bulk_g2s(smem_u32(kv_tile(i % NSTAGE, 1)), a.v_pool + base, bytes, bar);
+    bulk_g2s(smem_u32(st), a.k_pool + base, bytes, bar);
+    bulk_g2s(smem_u32(st + TILE * HD), a.v_pool + base, bytes, bar);
     return true;
   };
-  __syncthreads();  // barriers initialised
-  if (tid == 0) {
-    bool ok = true;
-    for (int i = 0; i < min(NSTAGE, ntiles); ++i) ok &= issue(i);
-    if (!ok && a.status) atomicOr(a.status, kBadPage);
-  }
+  __syncwarp();
+  if (lane == 0 && tb + warp < te && !issue(tb + warp) && a.status) atomicOr(a.status, kBadPage);
 
   const float scale = 1.0f / sqrtf((float)HD);
-  const float* qrow = a.q + ((size_t)brel * a.n_heads + (size_t)kvh * g) * HD;
-  for (int i = tid; i < g * HD; i += NT) s_q[i] = qrow[i] * scale;
-  if (tid < g) {
-    s_m[tid] = -INFINITY;
-    s_l[tid] = 0.f;
-  }
-  float oacc[OPT];
-#pragma unroll
-  for (int k = 0; k < OPT; ++k) oacc[k] = 0.f;
+  const float* qrow = a.q + ((size_t)brel * a.n_heads + (size_t)kvh * G) * HD;
+  for (int i = tid; i < G * HD; i += NT) s_q[i] = qrow[i] * scale;
   __syncthreads();
+  griddep_launch();
 
+  float m_run[G], l_run[G], o[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
+  }
   bool failed = false;
-  for (int i = 0; i < ntiles; ++i) {
-    const int t = t0 + i * TILE;
-    const int nt = min(TILE, t1 - t);
-    if (!mbar_wait(smem_u32(&s_full[i % NSTAGE]), (i / NSTAGE) & 1)) failed = true;
-    const __half* kt = kv_tile(i % NSTAGE, 0);
-    const __half* vt = kv_tile(i % NSTAGE, 1);
-    // scores: warp w scores tokens w, w+4, ...; lanes split the head dim
-    for (int j = warp; j < nt; j += NT / 32) {
-      float kf[DPL];
+  int use = 0;
+  for (int i = tb + warp; i < te; i += NW, ++use) {
+    const int nt = min(TILE, n - i * TILE);
+    if (!mbar_wait(bar, use & 1)) failed = true;
+    // ---- scores, lane = token
+    float sc[G];
+    {
+      float2 acc[G];
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) kf[e] = __half2float(kt[j * HD + lane * DPL + e]);
-      for (int h = 0; h < g; ++h) {
-        float p = 0.f;
+      for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+      const __half2* krow = reinterpret_cast<const __half2*>(st + lane * HD);
+      const float2* q2 = reinterpret_cast<const float2*>(s_q);
+#pragma unroll 4
+      for (int w2 = 0; w2 < W2; ++w2) {
+        const int wi = (w2 + lane) & (W2 - 1);
+        const float2 kf = __half22float2(krow[wi]);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) p = fmaf(s_q[h * HD + lane * DPL + e], kf[e], p);
-        p = warp_sum(p);
-        if (lane == 0) s_s[h][j] = p;
+        for (int h = 0; h < G; ++h) acc[h] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h]);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) sc[h] = lane < nt ? acc[h].x + acc[h].y : -INFINITY;
+    }
+    // ---- online softmax (per head, in registers)
+    float p[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float m_new = fmaxf(m_run[h], warp_max(sc[h]));
+      p[h] = lane < nt ? expf(sc[h] - m_new) : 0.f;
+      const float al = expf(m_run[h] - m_new);  // 0 on the warp's first tile
+      l_run[h] = l_run[h] * al + warp_sum(p[h]);
+      m_run[h] = m_new;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[h][e] *= al;
+    }
+    // ---- o += P V, lane = DPL dims
+    const __half* vt = st + TILE * HD + lane * DPL;
+    for (int j = 0; j < nt; ++j) {
+      float vf[DPL];
+      if (DPL == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(vt + j * HD);
+        const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        vf[0] = v01.x;
+        vf[1] = v01.y;
+        vf[2 % DPL] = v23.x;
+        vf[3 % DPL] = v23.y;
+      } else {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) vf[e] = __half2float(vt[j * HD + e]);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pj = __shfl_sync(0xffffffffu, p[h], j);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pj, vf[e], o[h][e]);
       }
     }
-    __syncthreads();
-    // online softmax update, one warp per head
-    for (int h = warp; h < g; h += NT / 32) {
-      const float sv = lane < nt ? s_s[h][lane] : -INFINITY;
-      const float mx = warp_max(sv);
-      const float m_old = s_m[h];
-      const float m_new = fmaxf(m_old, mx);
-      const float p = lane < nt ? expf(sv - m_new) : 0.f;
-      const float ps = warp_sum(p);
-      s_s[h][lane] = p;
-      if (lane == 0) {
-        const float al = expf(m_old - m_new);  // 0 on the first tile (m_old = -inf)
-        s_alpha[h] = al;
-        s_l[h] = s_l[h] * al + ps;
-        s_m[h] = m_new;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < OPT; ++k) {
-      const int h = hslot + k * HPT;
-      if (h < g) {
-        float o = oacc[k] * s_alpha[h];
-        for (int j = 0; j < nt; ++j) o = fmaf(s_s[h][j], __half2float(vt[j * HD + d]), o);
-        oacc[k] = o;
-      }
-    }
-    __syncthreads();  // slot i % NSTAGE is free again
-    if (tid == 0 && i + NSTAGE < ntiles && !issue(i + NSTAGE) && a.status) atomicOr(a.status, kBadPage);
+    __syncwarp();  // the stage is free again
+    if (lane == 0 && i + NW < te && !issue(i + NW) && a.status) atomicOr(a.status, kBadPage);
   }
-  if (failed && a.status && tid == 0) atomicOr(a.status, kTimeout);
+  if (failed && a.status) atomicOr(a.status, kTimeout);
 
-  // ---- partials to scratch
-  const size_t slot = ((size_t)brel * a.n_kv + kvh) * S + sp;
+  // ---- merge the 4 warps of this CTA; the per-warp outputs reuse the
+  // (now idle) K/V stage memory: NW*G*HD floats <= NW*2*TILE*HD halves
+  __syncthreads();
+  float(*s_wo)[G * HD] = reinterpret_cast<float(*)[G * HD]>(s_dyn);
+  static_assert(NW * G * HD * 4 <= NW * 2 * TILE * HD * 2, "merge buffer must fit the stages");
+  if (lane == 0) {
 #pragma unroll
-  for (int k = 0; k < OPT; ++k) {
-    const int h = hslot + k * HPT;
-    if (h < g) a.part_o[(slot * g + h) * HD + d] = oacc[k];
+    for (int h = 0; h < G; ++h) {
+      s_wm[warp][h] = m_run[h];
+      s_wl[warp][h] = l_run[h];
+    }
   }
-  if (tid < g) reinterpret_cast<float2*>(a.part_ml)[slot * g + tid] = make_float2(s_m[tid], s_l[tid]);
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) s_wo[warp][h * HD + lane * DPL + e] = o[h][e];
+  __syncthreads();
+  const size_t slot = ((size_t)brel * a.n_kv + kvh) * S + sp;
+  for (int idx = tid; idx < G * HD; idx += NT) {
+    const int h = idx / HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_wm[w][h]);
+    float acc = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float e = s_wl[w][h] > 0.f ? expf(s_wm[w][h] - M) : 0.f;
+      acc = fmaf(e, s_wo[w][idx], acc);
+      L = fmaf(e, s_wl[w][h], L);
+    }
+    a.part_o[slot * G * HD + idx] = acc;
+    if ((idx % HD) == 0) reinterpret_cast<float2*>(a.part_ml)[slot * G + h] = make_float2(M, L);
+  }
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -182,17 +216,16 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  // ---- last CTA of this (row, kv head): combine the S splits
-  // weights w_s = exp(m_s - M) / sum_s l_s exp(m_s - M), one warp per head
+  // ---- last CTA of this (row, kv head): merge the S splits
   const size_t slot0 = ((size_t)brel * a.n_kv + kvh) * S;
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
-  for (int h = warp; h < g; h += NT / 32) {
+  for (int h = warp; h < G; h += NW) {
     float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(&ml[(slot0 + s) * g + h]).x);
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(&ml[(slot0 + s) * G + h]).x);
     M = warp_max(M);
     float den = 0.f;
     for (int s = lane; s < S; s += 32) {
-      const float2 v = __ldcg(&ml[(slot0 + s) * g + h]);
+      const float2 v = __ldcg(&ml[(slot0 + s) * G + h]);
       const float e = v.y > 0.f ? expf(v.x - M) : 0.f;  // empty split: weight 0
       s_w[h][s] = e;
       den = fmaf(v.y, e, den);
@@ -201,15 +234,13 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
     for (int s = lane; s < S; s += 32) s_w[h][s] /= den;
   }
   __syncthreads();
-#pragma unroll
-  for (int k = 0; k < OPT; ++k) {
-    const int h = hslot + k * HPT;
-    if (h >= g) continue;
+  for (int idx = tid; idx < G * HD; idx += NT) {
+    const int h = idx / HD;
+    const float* po = a.part_o + slot0 * G * HD + idx;
     float acc = 0.f;
-    const float* po = a.part_o + (slot0 * g + h) * HD + d;
 #pragma unroll 8
-    for (int s = 0; s < S; ++s) acc = fmaf(s_w[h][s], __ldcg(po + (size_t)s * g * HD), acc);
-    a.o[((size_t)brel * a.n_heads + (size_t)kvh * g + h) * HD + d] = acc;
+    for (int s = 0; s < S; ++s) acc = fmaf(s_w[h][s], __ldcg(po + (size_t)s * G * HD), acc);
+    a.o[((size_t)brel * a.n_heads + (size_t)kvh * G) * HD + idx] = acc;
   }
   if (tid == 0) a.counters[(size_t)brel * a.n_kv + kvh] = 0;
 }
@@ -237,45 +268,61 @@ void attn_workspace_carve(void* ws, int rows, int n_heads, int n_kv, int head_di
   *part_ml = reinterpret_cast<float*>(p);
 }
 
+// Splits per (row, kv head): about one tile per warp at the longest context,
+// but no more than two CTAs per SM over the grid.
 int attn_default_splits(int rows, int n_kv, int num_sms, int max_len) {
-  int s = (2 * num_sms + rows * n_kv - 1) / (rows * n_kv);
-  const int cap = (max_len + TILE - 1) / TILE;
+  const int tiles = (max_len + TILE - 1) / TILE;
+  int s = (tiles + NW - 1) / NW;
+  const int cap = (2 * num_sms + rows * n_kv - 1) / (rows * n_kv);
   if (s > cap) s = cap;
-  if (s > 128) s = 128;  // combine weights live in shared memory
+  if (s > kMaxSplits) s = kMaxSplits;  // merge weights live in shared memory
   if (s < 1) s = 1;
   return s;
 }
 
+using AttnFn = void (*)(const AttnArgs);
+
+template <int HD, int G>
+AttnFn attn_fn() {
+  static bool done = false;  // raise the dynamic shared memory limit once
+  if (!done) {
+    if (cudaFuncSetAttribute(attn_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             NW * 2 * TILE * HD * 2) != cudaSuccess)
+      return nullptr;
+    done = true;
+  }
+  return attn_kernel<HD, G>;
+}
+
 template <int HD>
-cudaError_t attn_attr() {
-  static bool done = false;  // one process-wide attribute per instantiation
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       NSTAGE * 2 * TILE * HD * 2);
-  done = e == cudaSuccess;
-  return e;
+AttnFn attn_fn_g(int g) {
+  switch (g) {
+    case 1: return attn_fn<HD, 1>();
+    case 2: return attn_fn<HD, 2>();
+    case 4: return attn_fn<HD, 4>();
+    case 8: return attn_fn<HD, 8>();
+    case 16: return attn_fn<HD, 16>();
+  }
+  return nullptr;
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int rows, cudaStream_t s, bool pdl) {
-  if (a.n_splits > 128 || a.n_splits < 1) return cudaErrorInvalidValue;
-  cudaError_t e = a.head_dim == 32 ? attn_attr<32>() : a.head_dim == 64 ? attn_attr<64>() : attn_attr<128>();
-  if (e != cudaSuccess) return e;
+  if (a.n_splits > kMaxSplits || a.n_splits < 1 || a.n_kv < 1 || a.n_heads % a.n_kv) return cudaErrorInvalidValue;
+  const int g = a.n_heads / a.n_kv;
+  AttnFn f = a.head_dim == 32 ? attn_fn_g<32>(g) : a.head_dim == 64 ? attn_fn_g<64>(g)
+           : a.head_dim == 128 ? attn_fn_g<128>(g) : nullptr;
+  if (!f) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_kv * a.n_splits, rows);
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = NSTAGE * 2 * TILE * a.head_dim * 2;
+  cfg.dynamicSmemBytes = NW * 2 * TILE * a.head_dim * 2;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  switch (a.head_dim) {
-    case 32: return cudaLaunchKernelEx(&cfg, attn_kernel<32>, a);
-    case 64: return cudaLaunchKernelEx(&cfg, attn_kernel<64>, a);
-    case 128: return cudaLaunchKernelEx(&cfg, attn_kernel<128>, a);
-    default: return cudaErrorInvalidValue;
-  }
+  return cudaLaunchKernelEx(&cfg, f, a);
 }
 
 }  // namespace dls

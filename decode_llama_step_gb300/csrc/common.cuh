@@ -97,19 +97,19 @@ __device__ __forceinline__ float mag_byte(uint32_t u, int k) {
   return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540 | k));
 }
 
-// four int8 codes (one 32-bit word) -> two packed pairs (q0,q1), (q2,q3)
-__device__ __forceinline__ void i8x4_to_f2(uint32_t w, f2_t& p01, f2_t& p23) {
+// four int8 codes (one 32-bit word) -> two pairs (q0,q1), (q2,q3)
+__device__ __forceinline__ void i8x4_to_f2(uint32_t w, float2& p01, float2& p23) {
   const uint32_t u = w ^ 0x80808080u;  // q + 128 as unsigned bytes
-  const f2_t bias = pk2(-8388736.0f, -8388736.0f);
-  p01 = fadd2(pk2(mag_byte(u, 0), mag_byte(u, 1)), bias);
-  p23 = fadd2(pk2(mag_byte(u, 2), mag_byte(u, 3)), bias);
+  const float2 bias = make_float2(-8388736.0f, -8388736.0f);
+  p01 = __fadd2_rn(make_float2(mag_byte(u, 0), mag_byte(u, 1)), bias);
+  p23 = __fadd2_rn(make_float2(mag_byte(u, 2), mag_byte(u, 3)), bias);
 }
 
 // four nibble codes already isolated one per byte (values 0..15) -> (n-8)
-__device__ __forceinline__ void u4x4_to_f2(uint32_t b, f2_t& p01, f2_t& p23) {
-  const f2_t bias = pk2(-8388616.0f, -8388616.0f);  // 2^23 + 8
-  p01 = fadd2(pk2(mag_byte(b, 0), mag_byte(b, 1)), bias);
-  p23 = fadd2(pk2(mag_byte(b, 2), mag_byte(b, 3)), bias);
+__device__ __forceinline__ void u4x4_to_f2(uint32_t b, float2& p01, float2& p23) {
+  const float2 bias = make_float2(-8388616.0f, -8388616.0f);  // 2^23 + 8
+  p01 = __fadd2_rn(make_float2(mag_byte(b, 0), mag_byte(b, 1)), bias);
+  p23 = __fadd2_rn(make_float2(mag_byte(b, 2), mag_byte(b, 3)), bias);
 }
 
 // ---- mbarrier + bulk async copy (TMA, non-tensor form) ---------------------------

@@ -8,7 +8,8 @@
 //    the code array and of the scale array is contiguous.
 //  * A producer warp streams that slice through a shared-memory ring with
 //    1-D bulk async copies (TMA, cp.async.bulk) and mbarriers: stages of RS
-//    whole rows (~16 KB of codes plus their scales), ~96 KB in flight per SM.
+//    whole rows (~16 KB of codes plus their scales), 64 KB in flight per CTA,
+//    two CTAs per SM where registers allow.
 //    The first stages are issued before waiting on the previous kernel
 //    (programmatic dependent launch): weights never depend on it.
 //  * Consumer warps own K-chunks (512 columns for Q8_0, 1024 for Q4_0); each
@@ -30,13 +31,13 @@ namespace {
 constexpr int kMaxConsumers = 14;
 constexpr int kRB = 64;              // rows per epilogue block
 constexpr int kStageCodes = 16384;   // target code bytes per ring stage
-constexpr int kRingBytes = 96 * 1024;
+constexpr int kRingBytes = 64 * 1024;
 
 template <int WT>
 struct Geo {
   static constexpr int CH = WT == 8 ? 512 : 1024;   // columns per chunk
-  static constexpr int XV = WT == 8 ? 8 : 16;       // packed x pairs per lane per chunk
-  static constexpr int MC = WT == 8 ? 4 : 2;        // max chunks per warp (register budget)
+  static constexpr int XV = WT == 8 ? 8 : 16;       // x pairs per lane per chunk
+  static constexpr int MCMAX = WT == 8 ? 4 : 2;     // max chunks per warp (register budget)
 };
 
 template <int RS>
@@ -65,31 +66,30 @@ __device__ __forceinline__ float butterfly(float (&acc)[RS], int lane) {
 
 // dot of 16 code bytes (one lane's slice of one row) with its activations
 template <int WT>
-__device__ __forceinline__ float dot16(uint4 q, const f2_t* xr) {
-  f2_t s = pk2(0.f, 0.f);
+__device__ __forceinline__ float dot16(uint4 q, const float2* xr) {
+  float2 s = make_float2(0.f, 0.f);
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
   if (WT == 8) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      f2_t p01, p23;
+      float2 p01, p23;
       i8x4_to_f2(w[k], p01, p23);
-      s = ffma2(p01, xr[2 * k], s);
-      s = ffma2(p23, xr[2 * k + 1], s);
+      s = __ffma2_rn(p01, xr[2 * k], s);
+      s = __ffma2_rn(p23, xr[2 * k + 1], s);
     }
   } else {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {  // bytes 4k..: low nibbles = elements 4k.., high = 16+4k..
-      f2_t a01, a23, b01, b23;
+      float2 a01, a23, b01, b23;
       u4x4_to_f2(w[k] & 0x0F0F0F0Fu, a01, a23);
       u4x4_to_f2((w[k] >> 4) & 0x0F0F0F0Fu, b01, b23);
-      s = ffma2(a01, xr[2 * k], s);
-      s = ffma2(a23, xr[2 * k + 1], s);
-      s = ffma2(b01, xr[8 + 2 * k], s);
-      s = ffma2(b23, xr[8 + 2 * k + 1], s);
+      s = __ffma2_rn(a01, xr[2 * k], s);
+      s = __ffma2_rn(a23, xr[2 * k + 1], s);
+      s = __ffma2_rn(b01, xr[8 + 2 * k], s);
+      s = __ffma2_rn(b23, xr[8 + 2 * k + 1], s);
     }
   }
-  const float2 f = upk2(s);
-  return f.x + f.y;
+  return s.x + s.y;
 }
 
 struct Shared {
@@ -100,7 +100,7 @@ struct Shared {
   int abort;
 };
 
-template <int WT, int PRO, int EPI, int RS>
+template <int WT, int PRO, int EPI, int RS, int MC>
 __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const GemvArgs a, const GemvLaunch L) {
   using G = Geo<WT>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
         bulk_g2s(smem_u32(dst + stage_q), reinterpret_cast<const uint8_t*>(w.d) + (size_t)row * drow_bytes, db, bar);
         ++issued;
       }
+      griddep_launch();  // all of this CTA's weights are in flight
       // never leave with copies in flight: wait for every issued stage
       for (int s = max(0, issued - NS); s < issued; ++s)
         mbar_wait(smem_u32(&sh.full[s % NS]), (s / NS) & 1);
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
   } else {
     // ---------------- consumers
     griddep_wait();
+    if (nst == 0) griddep_launch();
     // prologue: this lane's activation slice, in registers
     if (PRO == PRO_RMSNORM) {
       float ss = 0.f;
@@ -182,11 +184,11 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
       named_bar(1, nwc * 32);
     }
     const int nchunk = (kpad + G::CH - 1) / G::CH;
-    const int mc = warp < nchunk ? min(G::MC, (nchunk - warp + nwc - 1) / nwc) : 0;
-    f2_t xr[G::MC][G::XV];
-    bool valid[G::MC];
+    const int mc = warp < nchunk ? min(MC, (nchunk - warp + nwc - 1) / nwc) : 0;
+    float2 xr[MC][G::XV];
+    bool valid[MC];
 #pragma unroll
-    for (int k = 0; k < G::MC; ++k) {
+    for (int k = 0; k < MC; ++k) {
       const int c = warp + k * nwc;
       const int col0 = WT == 8 ? c * 512 + lane * 16 : (c * 32 + lane) * 32;
       valid[k] = k < mc && col0 < kpad;
@@ -206,10 +208,9 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
             if (PRO == PRO_RMSNORM) v1 *= sh.rs * a.g[i0 + 1];
           }
         }
-        xr[k][e] = pk2(v0, v1);
+        xr[k][e] = make_float2(v0, v1);
       }
     }
-    griddep_launch();
 
     int32_t pos = 0, seq = 0;
     if (EPI == EPI_QKV) {
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
         atomicOr(&a.sp->status, kTimeout);
         sh.abort = 1;
       }
+      if (s == nst - 1) griddep_launch();  // last stage arrived: let the next kernel start
       const int rows_s = min(RS, nrows - s * RS);
       const uint8_t* st = ring + (size_t)slot * stage_bytes;
       float acc[RS];
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
       for (int rr = 0; rr < RS; ++rr) acc[rr] = 0.f;
       if (!sh.abort) {
 #pragma unroll
-        for (int k = 0; k < G::MC; ++k) {
+        for (int k = 0; k < MC; ++k) {
           if (!valid[k]) continue;
           const int c = warp + k * nwc;
           const int qoff = WT == 8 ? c * 512 + lane * 16 : (c * 32 + lane) * 16;
@@ -314,20 +316,28 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
 
 using KernelFn = void (*)(const GemvArgs, const GemvLaunch);
 
-template <int WT, int P, int E>
+template <int WT, int P, int E, int MC>
 KernelFn pick_rs(int rs) {
   switch (rs) {
-    case 1: return &gemv_kernel<WT, P, E, 1>;
-    case 2: return &gemv_kernel<WT, P, E, 2>;
-    case 4: return &gemv_kernel<WT, P, E, 4>;
-    case 8: return &gemv_kernel<WT, P, E, 8>;
+    case 1: return &gemv_kernel<WT, P, E, 1, MC>;
+    case 2: return &gemv_kernel<WT, P, E, 2, MC>;
+    case 4: return &gemv_kernel<WT, P, E, 4, MC>;
+    case 8: return &gemv_kernel<WT, P, E, 8, MC>;
   }
   return nullptr;
 }
 
-KernelFn pick(int wtype, int pro, int epi, int rs) {
+template <int WT, int P, int E>
+KernelFn pick_mc(int rs, int mc) {
+  if (mc <= 1) return pick_rs<WT, P, E, 1>(rs);
+  if (mc <= 2) return pick_rs<WT, P, E, 2>(rs);
+  if (WT == 8 && mc <= 4) return pick_rs<WT, P, E, (WT == 8 ? 4 : 2)>(rs);
+  return nullptr;
+}
+
+KernelFn pick(int wtype, int pro, int epi, int rs, int mc) {
 #define DLS_PICK(WT, P, E) \
-  if (wtype == WT && pro == P && epi == E) return pick_rs<WT, P, E>(rs);
+  if (wtype == WT && pro == P && epi == E) return pick_mc<WT, P, E>(rs, mc);
   DLS_PICK(8, PRO_RMSNORM, EPI_QKV)
   DLS_PICK(8, PRO_COPY, EPI_RESID)
   DLS_PICK(8, PRO_RMSNORM, EPI_STORE)
@@ -344,10 +354,10 @@ KernelFn pick(int wtype, int pro, int epi, int rs) {
 
 }  // namespace
 
-GemvLaunch gemv_plan(int wtype, int rows, int nb, int num_sms, int unit) {
+GemvLaunch gemv_plan(int wtype, int pro, int epi, int rows, int nb, int num_sms, int unit) {
   const int kpad = nb * 32;
   const int CH = wtype == 8 ? 512 : 1024;
-  const int MC = wtype == 8 ? 4 : 2;
+  const int MC = wtype == 8 ? 4 : 2;  // Geo<WT>::MCMAX
   const int nchunk = (kpad + CH - 1) / CH;
   // consumer warps: the largest divisor of the chunk count <= 8 that keeps
   // chunks per warp within the register budget; else a divisor up to 14;
@@ -366,11 +376,7 @@ GemvLaunch gemv_plan(int wtype, int rows, int nb, int num_sms, int unit) {
   const int stage = rs * row_bytes + rs * ds * 2;
   int ns = kRingBytes / stage;
   ns = std::max(2, std::min(16, ns));
-  const int units = (rows + unit - 1) / unit;
-  int grid = std::min(num_sms, units);
-  if (grid < 1) grid = 1;
   GemvLaunch l;
-  l.grid = grid;
   l.threads = (nwc + 1) * 32;
   l.nwc = nwc;
   l.rs = rs;
@@ -378,6 +384,19 @@ GemvLaunch gemv_plan(int wtype, int rows, int nb, int num_sms, int unit) {
   l.mc = (nchunk + nwc - 1) / nwc;
   const int head = (int)((sizeof(Shared) + nwc * kRB * 4 + 127) & ~127);
   l.smem = head + ns * stage;
+  // CTAs per SM from the occupancy the kernel actually achieves (registers,
+  // shared memory), at most 2
+  int occ = 1;
+  KernelFn f = pick(wtype, pro, epi, rs, l.mc);
+  if (f && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, l.threads, l.smem) != cudaSuccess) {
+    cudaGetLastError();
+    occ = 1;
+  }
+  occ = std::max(1, std::min(2, occ));
+  const int units = (rows + unit - 1) / unit;
+  int grid = std::min(num_sms * occ, units);
+  if (grid < 1) grid = 1;
+  l.grid = grid;
   return l;
 }
 
@@ -387,18 +406,19 @@ cudaError_t gemv_setup_attributes() {
   for (int wt : {8, 4})
     for (int p : pros)
       for (int e : epis)
-        for (int rs : {1, 2, 4, 8}) {
-          KernelFn f = pick(wt, p, e, rs);
-          if (!f) continue;
-          cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-          if (err != cudaSuccess) return err;
-        }
+        for (int rs : {1, 2, 4, 8})
+          for (int mc : {1, 2, 4}) {
+            KernelFn f = pick(wt, p, e, rs, mc);
+            if (!f) continue;
+            cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+            if (err != cudaSuccess) return err;
+          }
   return cudaSuccess;
 }
 
 cudaError_t launch_gemv(int wtype, int pro, int epi, const GemvArgs& a, const GemvLaunch& l, cudaStream_t s,
                         bool pdl) {
-  KernelFn f = pick(wtype, pro, epi, l.rs);
+  KernelFn f = pick(wtype, pro, epi, l.rs, l.mc);
   if (!f || l.ns > 16 || l.nwc > kMaxConsumers || a.w.ds % 8) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(l.grid);

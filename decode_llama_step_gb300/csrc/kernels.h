@@ -46,7 +46,7 @@ struct GemvLaunch {
 };
 
 // Choose grid/threads/smem for a matrix and check the kernel can run it.
-GemvLaunch gemv_plan(int wtype, int rows, int nb, int num_sms, int unit);
+GemvLaunch gemv_plan(int wtype, int pro, int epi, int rows, int nb, int num_sms, int unit);
 cudaError_t gemv_setup_attributes();   // raise dynamic smem limits once
 cudaError_t launch_gemv(int wtype, int pro, int epi, const GemvArgs& a, const GemvLaunch& l, cudaStream_t s,
                         bool pdl);

@@ -37,6 +37,7 @@ __device__ __forceinline__ float dq(const MatDev& m, int wtype, int row, int col
 
 // ---------------------------------------------------------------- embedding
 
+// one 32-element block per thread iteration, all loads issued up front
 __global__ void embed_kernel(const MatDev emb, int wtype, StepParams* sp, int brow, float* x, int vocab) {
   griddep_wait();
   griddep_launch();
@@ -45,7 +46,38 @@ __global__ void embed_kernel(const MatDev emb, int wtype, StepParams* sp, int br
     if (threadIdx.x == 0) atomicOr(&sp->status, kBadToken);
     tok = 0;
   }
-  for (int c = threadIdx.x; c < emb.cols; c += blockDim.x) x[c] = dq(emb, wtype, tok, c);
+  for (int blk = threadIdx.x; blk < emb.nb; blk += blockDim.x) {
+    const float d = __half2float(emb.d[(size_t)tok * emb.ds + blk]);
+    float v[32];
+    if (wtype == 8) {
+      const uint4* q = reinterpret_cast<const uint4*>(emb.qs + ((size_t)tok * emb.nb + blk) * 32);
+      const uint4 q0 = q[0], q1 = q[1];
+      const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t u = w[k] ^ 0x80808080u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[4 * k + e] = mag_byte(u, e) - 8388736.0f;
+      }
+    } else {
+      const uint4 q = *reinterpret_cast<const uint4*>(emb.qs + ((size_t)tok * emb.nb + blk) * 16);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t lo = w[k] & 0x0F0F0F0Fu, hi = (w[k] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[4 * k + e] = mag_byte(lo, e) - 8388616.0f;
+          v[16 + 4 * k + e] = mag_byte(hi, e) - 8388616.0f;
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int c = blk * 32 + e;
+      if (c < emb.cols) x[c] = d * v[e];
+    }
+  }
 }
 
 // ---------------------------------------------------------------- greedy pick
