@@ -653,6 +653,16 @@ int validate_desc(const dls_model_desc* d) {
 
 }  // namespace
 
+int dls::report_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = std::string("ERR ") + status_str(code) + " " + buf;
+  return code;
+}
+
 // =================================================================== C ABI
 
 extern "C" {

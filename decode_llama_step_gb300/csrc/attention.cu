@@ -13,6 +13,8 @@
 // the arrival counter to zero for the next launch.
 #include <math.h>
 
+#include <mutex>
+
 #include "../../include/dls.h"
 #include "kernels.h"
 
@@ -375,4 +377,96 @@ extern "C" int dls_attention_decode(const float* q, const void* k_pages, const v
                             &a.counters);
   cudaError_t e = dls::launch_attention(a, n_batch, static_cast<cudaStream_t>(cuda_stream), false);
   return e == cudaSuccess ? DLS_OK : DLS_ERR_CUDA;
+}
+
+// ---- allocation-free variant -------------------------------------------------------
+//
+// Some callers cannot call cudaMalloc or any allocating routine: a serving
+// process that carves all device memory into fixed pools at start-up and
+// forbids allocations afterwards (an allocation could fail or fragment the
+// plan mid-request), or code on a latency-critical path where an allocator
+// call may take a lock or synchronise the device.  For them this entry point
+// takes the split-K scratch from a file-scope device array instead of a
+// caller-provided workspace.
+
+namespace {
+
+// Scratch of dls_attention_decode_noalloc.  Every GPU that loads this library
+// holds these bytes until the process exits.
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[DLS_ATTENTION_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[256] = {};  // device address of the scratch, per device id
+
+// Device address of the scratch on the current device, looked up once per
+// device (host code sees only a host-side stand-in under the symbol's name).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return DLS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_noalloc_scratch) != cudaSuccess || !p) return DLS_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DLS_OK;
+}
+
+}  // namespace
+
+extern "C" int dls_attention_decode_noalloc(const float* q, const void* k_pages, const void* v_pages,
+                                            const int32_t* page_table, const int32_t* lengths, float* o,
+                                            int32_t n_batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                            int32_t page_tokens, int32_t max_pages, int32_t n_splits,
+                                            void* cuda_stream) {
+  if (!q || !k_pages || !v_pages || !page_table || !lengths || !o)
+    return dls::report_error(DLS_ERR_ARG, "noalloc attention: NULL pointer argument");
+  if (n_splits > 128 || n_batch < 1 || n_kv_heads < 1 || n_heads < 1 || n_heads % n_kv_heads ||
+      n_heads / n_kv_heads > dls::kMaxG || (head_dim != 32 && head_dim != 64 && head_dim != 128) ||
+      page_tokens < 32 || page_tokens % 32 || max_pages < 1)
+    return dls::report_error(DLS_ERR_ARG, "noalloc attention: bad shape n_batch=%d n_heads=%d n_kv_heads=%d "
+                             "head_dim=%d page_tokens=%d max_pages=%d n_splits=%d", n_batch, n_heads, n_kv_heads,
+                             head_dim, page_tokens, max_pages, n_splits);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
+    return dls::report_error(DLS_ERR_CUDA, "noalloc attention: no current device");
+  const int max_len = page_tokens * max_pages;
+  if (n_splits <= 0) n_splits = dls::attn_default_splits(n_batch, n_kv_heads, sms, max_len);
+  const size_t need = dls::attn_workspace_bytes(n_batch, n_heads, n_kv_heads, head_dim, n_splits);
+  if (need > DLS_ATTENTION_NOALLOC_SCRATCH_BYTES)
+    return dls::report_error(DLS_ERR_CAPACITY, "noalloc attention: needs %zu bytes of scratch, the built-in "
+                             "array holds %zu (fewer rows or splits fit)", need,
+                             (size_t)DLS_ATTENTION_NOALLOC_SCRATCH_BYTES);
+  void* ws = nullptr;
+  if (noalloc_scratch(&ws) != DLS_OK)
+    return dls::report_error(DLS_ERR_CUDA, "noalloc attention: cudaGetSymbolAddress failed");
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // the arrival counters at the head of the scratch must start at zero
+  const size_t counter_bytes = ((size_t)n_batch * n_kv_heads * sizeof(int) + 255) & ~(size_t)255;
+  if (cudaMemsetAsync(ws, 0, counter_bytes, st) != cudaSuccess)
+    return dls::report_error(DLS_ERR_CUDA, "noalloc attention: clearing the counters failed");
+  dls::AttnArgs a = {};
+  a.q = q;
+  a.o = o;
+  a.k_pool = static_cast<const __half*>(k_pages);
+  a.v_pool = static_cast<const __half*>(v_pages);
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.pt_row = nullptr;
+  a.len = lengths;
+  a.len_add = 0;
+  a.n_heads = n_heads;
+  a.n_kv = n_kv_heads;
+  a.head_dim = head_dim;
+  a.page_tokens = page_tokens;
+  a.n_splits = n_splits;
+  a.row0 = 0;
+  a.status = nullptr;
+  a.max_len = max_len;
+  dls::attn_workspace_carve(ws, n_batch, n_heads, n_kv_heads, head_dim, n_splits, &a.part_o, &a.part_ml,
+                            &a.counters);
+  if (dls::launch_attention(a, n_batch, st, false) != cudaSuccess)
+    return dls::report_error(DLS_ERR_CUDA, "noalloc attention: launch failed");
+  return DLS_OK;
 }

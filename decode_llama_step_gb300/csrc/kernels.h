@@ -99,4 +99,8 @@ cudaError_t launch_delay(long long ns, cudaStream_t s);
 cudaError_t launch_kv_gather(const __half* pool, const int32_t* pages, int len, int n_kv, int page_tokens,
                              int head_dim, __half* out, cudaStream_t s);
 
+// Record a failure for dls_last_error(NULL) (calls without a model) and
+// return `code`.
+int report_error(int code, const char* fmt, ...);
+
 }  // namespace dls

@@ -73,6 +73,7 @@ _SIGS = {
     "dls_layer_bytes": (u64, [vp]),
     "dls_attention_decode": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, sz, i32, i32, i32, i32, i32, i32, i32, vp]),
     "dls_attention_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
+    "dls_attention_decode_noalloc": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]),
     "dls_debug_capture": (ctypes.c_int, [vp, vp]),
     "dls_debug_read_kv": (ctypes.c_int, [vp, i32, i32, vp, vp]),
     "dls_debug_dequant": (ctypes.c_int, [vp, i32, i32, vp]),
@@ -150,6 +151,18 @@ def attention_decode(q, k_pages, v_pages, page_table, lengths, o, workspace, wor
     _check(load().dls_attention_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(lengths),
                                        _ptr(o), _ptr(workspace), workspace_bytes, n_batch, n_heads, n_kv_heads,
                                        head_dim, page_tokens, max_pages, n_splits, _stream_handle(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20  # DLS_ATTENTION_NOALLOC_SCRATCH_BYTES
+
+
+def attention_decode_noalloc(q, k_pages, v_pages, page_table, lengths, o, n_batch, n_heads, n_kv_heads, head_dim,
+                             page_tokens, max_pages, n_splits=0, stream=None):
+    """dls_attention_decode without a workspace: for callers that may not
+    allocate device memory; the scratch is a fixed array in the library."""
+    _check(load().dls_attention_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                               _ptr(lengths), _ptr(o), n_batch, n_heads, n_kv_heads, head_dim,
+                                               page_tokens, max_pages, n_splits, _stream_handle(stream)))
 
 
 def _stream_handle(stream):

@@ -225,6 +225,29 @@ int dls_attention_decode(const float* q, const void* k_pages, const void* v_page
 size_t dls_attention_workspace_bytes(int32_t n_batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                      int32_t n_splits);
 
+/* Allocation-free dls_attention_decode.  The pages have no counterpart of
+ * this call: it serves callers that may not allocate device memory at all
+ * (a process that fixes its device memory plan at start-up, or code where
+ * an allocator call could block or synchronise).  Same arguments and result
+ * as dls_attention_decode minus the workspace: the split-K scratch is a
+ * fixed array of DLS_ATTENTION_NOALLOC_SCRATCH_BYTES inside the library,
+ * present on every GPU that loads the library until the process exits.
+ * Nothing is allocated (no cudaMalloc, no allocating library call).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture on that device.
+ *  - Every call shares the one array; the call zeroes the arrival counters
+ *    it needs on `cuda_stream`, but calls that overlap on the GPU (other
+ *    streams, concurrent threads) race on the scratch and must not be issued.
+ *  - DLS_ERR_CAPACITY if the shape needs more scratch than the array holds
+ *    (dls_attention_workspace_bytes tells the need), DLS_ERR_ARG on a bad
+ *    shape; the message is in dls_last_error(NULL). */
+#define DLS_ATTENTION_NOALLOC_SCRATCH_BYTES (4u << 20)
+int dls_attention_decode_noalloc(const float* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* page_table, const int32_t* lengths, float* o, int32_t n_batch,
+                                 int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t page_tokens,
+                                 int32_t max_pages, int32_t n_splits, void* cuda_stream);
+
 /* ---- test and profiling hooks ------------------------------------------------ */
 
 /* Arm a capture of the residual stream after every layer for the next
