@@ -58,6 +58,7 @@ MatDev mat_at(const uint8_t* base, const MatOff& o, int row0 = 0, int rows = -1)
   m.cols = o.cols;
   m.nb = o.nb;
   m.ds = o.ds;
+  m.rstep = 1;
   return m;
 }
 
@@ -115,6 +116,8 @@ struct dls_model {
   int32_t* tokens_dev = nullptr;
   size_t tokens_cap = 0;
   int32_t* argmax_buf = nullptr;
+  int2* argmax_part = nullptr;
+  int* argmax_cnt = nullptr;
   StepParams* sp = nullptr;
   float2* rope = nullptr;
   int rope_len = 0;
@@ -391,22 +394,22 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
     go.x = m->o;
     go.y = x;
     LK(K_O, launch_gemv(m->wtype, PRO_COPY, EPI_RESID, go, m->plan_o, s, pdl));
-    // (4) RMSNorm -> gate|up GEMV
+    // (4) RMSNorm -> interleaved gate|up GEMV -> SwiGLU: h = silu(gate) * up
     GemvArgs gg{};
     gg.w = P.gu;
-    gg.unit = 1;
+    gg.unit = 2;
     gg.x = x;
     gg.g = P.ffn_norm;
     gg.eps = m->eps;
     gg.y = m->gu;
-    LK(K_GATE_UP, launch_gemv(m->wtype, PRO_RMSNORM, EPI_STORE, gg, m->plan_gu, s, pdl));
-    // (5) SwiGLU -> down GEMV + residual
+    LK(K_GATE_UP, launch_gemv(m->wtype, PRO_RMSNORM, EPI_SWIGLU, gg, m->plan_gu, s, pdl));
+    // (5) down GEMV on h + residual
     GemvArgs gd{};
     gd.w = P.down;
     gd.unit = 1;
     gd.x = m->gu;
     gd.y = x;
-    LK(K_DOWN, launch_gemv(m->wtype, PRO_SWIGLU, EPI_RESID, gd, m->plan_down, s, pdl));
+    LK(K_DOWN, launch_gemv(m->wtype, PRO_COPY, EPI_RESID, gd, m->plan_down, s, pdl));
     if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * m->H, x, m->H * sizeof(float), cudaMemcpyDeviceToDevice, s));
     if (streamed) {
       CK(cudaEventRecord(m->ev_free[buf], s));
@@ -423,7 +426,9 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
     gh.y = logits;
     LK(K_HEAD, launch_gemv(m->wtype, PRO_RMSNORM, EPI_STORE, gh, m->plan_head, s, pdl));
   }
-  if (argmax) LK(K_ARGMAX, launch_argmax(logits, m->V, 1, m->next_tok + b, s, pdl));
+  if (argmax)
+    LK(K_ARGMAX, launch_argmax(logits, m->V, 1, m->next_tok + b, m->argmax_part, m->argmax_cnt,
+                               argmax_blocks(1, m->num_sms), s, pdl));
   return DLS_OK;
 }
 
@@ -528,13 +533,13 @@ int set_params(dls_model* m, int n, const int32_t* seqs, const int32_t* tokens, 
 // ---- weights: host blocks -> device layout -------------------------------------
 
 int upload_matrix(dls_model* m, const void* host_blocks, int rows, int cols, uint8_t* dst_base, const MatOff& off,
-                  int row0, uint8_t* temp) {
+                  int row0, uint8_t* temp, int row_step = 1) {
   const int nb = (cols + 31) / 32;
   const size_t bsz = m->wtype == 8 ? 34 : 18;
   const size_t bytes = (size_t)rows * nb * bsz;
   CK(cudaMemcpyAsync(temp, host_blocks, bytes, cudaMemcpyHostToDevice, m->stream));
   const size_t rb = off.qs_bytes / off.rows;
-  CK(launch_repack(temp, m->wtype, rows, nb, off.ds, dst_base + off.qs + (size_t)row0 * rb,
+  CK(launch_repack(temp, m->wtype, rows, nb, off.ds, row_step, dst_base + off.qs + (size_t)row0 * rb,
                    reinterpret_cast<__half*>(dst_base + off.d) + (size_t)row0 * off.ds, m->stream));
   return DLS_OK;
 }
@@ -546,8 +551,9 @@ int upload_layer(dls_model* m, const dls_layer_desc& ld, uint8_t* dst, uint8_t* 
   TRY(upload_matrix(m, ld.wk, m->kv_rows, m->H, dst, m->lay.qkv, m->q_rows, temp));
   TRY(upload_matrix(m, ld.wv, m->kv_rows, m->H, dst, m->lay.qkv, m->q_rows + m->kv_rows, temp));
   TRY(upload_matrix(m, ld.wo, m->H, m->q_rows, dst, m->lay.o, 0, temp));
-  TRY(upload_matrix(m, ld.w_gate, m->F, m->H, dst, m->lay.gu, 0, temp));
-  TRY(upload_matrix(m, ld.w_up, m->F, m->H, dst, m->lay.gu, m->F, temp));
+  // gate and up rows interleaved: row 2i = gate_i, row 2i+1 = up_i
+  TRY(upload_matrix(m, ld.w_gate, m->F, m->H, dst, m->lay.gu, 0, temp, 2));
+  TRY(upload_matrix(m, ld.w_up, m->F, m->H, dst, m->lay.gu, 1, temp, 2));
   TRY(upload_matrix(m, ld.w_down, m->H, m->F, dst, m->lay.down, 0, temp));
   return DLS_OK;
 }
@@ -771,8 +777,8 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
 
   m->plan_qkv = gemv_plan(m->wtype, PRO_RMSNORM, EPI_QKV, m->lay.qkv.rows, m->lay.qkv.nb, m->num_sms, 2);
   m->plan_o = gemv_plan(m->wtype, PRO_COPY, EPI_RESID, m->lay.o.rows, m->lay.o.nb, m->num_sms, 1);
-  m->plan_gu = gemv_plan(m->wtype, PRO_RMSNORM, EPI_STORE, m->lay.gu.rows, m->lay.gu.nb, m->num_sms, 1);
-  m->plan_down = gemv_plan(m->wtype, PRO_SWIGLU, EPI_RESID, m->lay.down.rows, m->lay.down.nb, m->num_sms, 1);
+  m->plan_gu = gemv_plan(m->wtype, PRO_RMSNORM, EPI_SWIGLU, m->lay.gu.rows, m->lay.gu.nb, m->num_sms, 2);
+  m->plan_down = gemv_plan(m->wtype, PRO_COPY, EPI_RESID, m->lay.down.rows, m->lay.down.nb, m->num_sms, 1);
   m->plan_head = gemv_plan(m->wtype, PRO_RMSNORM, EPI_STORE, m->V, m->emb_off.nb, m->num_sms, 1);
   m->attn_splits = attn_default_splits(1, m->nkv, m->num_sms, m->max_ctx);
 
@@ -804,6 +810,8 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   TRYC(dev_alloc_t(m, (size_t)B * m->V, &m->logits, "logits"));
   TRYC(dev_alloc_t(m, (size_t)kMaxBatch, &m->next_tok, "next_token"));
   TRYC(dev_alloc_t(m, (size_t)4096, &m->argmax_buf, "argmax"));
+  TRYC(dev_alloc_t(m, (size_t)4096 + 2 * m->num_sms, &m->argmax_part, "argmax_partials"));
+  TRYC(dev_alloc_t(m, (size_t)4096, &m->argmax_cnt, "argmax_counters"));
   TRYC(dev_alloc_t(m, 1, &m->sp, "step_params"));
   TRYC(dev_alloc_t(m, (size_t)m->rope_len * (m->hd / 2), &m->rope, "rope_table"));
   const size_t ws = attn_workspace_bytes(1, m->nh, m->nkv, m->hd, m->attn_splits);
@@ -852,6 +860,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   CKC(cudaMemcpyAsync(m->pt_dev, m->pt_host.data(), m->pt_host.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
                       m->stream));
   CKC(cudaMemsetAsync(m->attn_ws, 0, ws, m->stream));
+  CKC(cudaMemsetAsync(m->argmax_cnt, 0, 4096 * sizeof(int), m->stream));
   CKC(cudaMemsetAsync(m->sp, 0, sizeof(StepParams), m->stream));
   TRYC(sync_stream(m, m->stream));
   dev_free(m, temp);
@@ -996,7 +1005,8 @@ int dls_generate(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* to
 int dls_argmax(dls_model* m, const float* logits, int32_t n_rows, int32_t* out) {
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
   if (!logits || !out || n_rows < 1 || n_rows > 4096) return fail(m, DLS_ERR_ARG, "n_rows=%d", n_rows);
-  CK(launch_argmax(logits, m->V, n_rows, m->argmax_buf, m->stream, false));
+  CK(launch_argmax(logits, m->V, n_rows, m->argmax_buf, m->argmax_part, m->argmax_cnt,
+                   argmax_blocks(n_rows, m->num_sms), m->stream, false));
   TRY(copy_out(m, out, m->argmax_buf, (size_t)n_rows * sizeof(int32_t)));
   return DLS_OK;
 }
@@ -1129,8 +1139,11 @@ static int find_matrix(dls_model* m, int32_t layer, int32_t tensor, MatDev* out)
     case 1: *out = mat_at(base, m->lay.qkv, m->q_rows, m->kv_rows); break;
     case 2: *out = mat_at(base, m->lay.qkv, m->q_rows + m->kv_rows, m->kv_rows); break;
     case 3: *out = mat_at(base, m->lay.o); break;
-    case 4: *out = mat_at(base, m->lay.gu, 0, m->F); break;
-    case 5: *out = mat_at(base, m->lay.gu, m->F, m->F); break;
+    case 4:  // gate rows are the even rows of the interleaved gate|up matrix
+    case 5:  // up rows are the odd rows
+      *out = mat_at(base, m->lay.gu, tensor - 4, m->F);
+      out->rstep = 2;
+      break;
     case 6: *out = mat_at(base, m->lay.down); break;
   }
   return DLS_OK;
@@ -1151,9 +1164,19 @@ int dls_debug_gemv(dls_model* m, int32_t layer, int32_t tensor, const float* x, 
   MatDev md;
   TRY(find_matrix(m, layer, tensor, &md));
   GemvArgs g{};
-  g.w = md;
   g.unit = 1;
   g.x = x;
+  if (md.rstep == 2) {
+    // gate or up: run the whole interleaved matrix, then pick every other row
+    g.w = mat_at(m->layer_dev[layer], m->lay.gu);
+    g.y = m->gu;
+    const GemvLaunch l = gemv_plan(m->wtype, PRO_COPY, EPI_STORE, g.w.rows, g.w.nb, m->num_sms, 1);
+    CK(launch_gemv(m->wtype, PRO_COPY, EPI_STORE, g, l, m->stream, false));
+    CK(cudaMemcpy2DAsync(y, sizeof(float), m->gu + (tensor - 4), 2 * sizeof(float), sizeof(float), m->F,
+                         cudaMemcpyDeviceToDevice, m->stream));
+    return DLS_OK;
+  }
+  g.w = md;
   g.y = y;
   const GemvLaunch l = gemv_plan(m->wtype, PRO_COPY, EPI_STORE, md.rows, md.nb, m->num_sms, 1);
   CK(launch_gemv(m->wtype, PRO_COPY, EPI_STORE, g, l, m->stream, false));

@@ -38,7 +38,8 @@ struct MatDev {
   const uint8_t* qs;
   const __half* d;
   int rows, cols, nb;
-  int ds;  // scale row stride in elements: nb rounded up to 8 (16-byte rows)
+  int ds;     // scale row stride in elements: nb rounded up to 8 (16-byte rows)
+  int rstep;  // storage rows per logical row (2 for one half of an interleaved pair); GEMVs need 1
 };
 
 // ---- small PTX wrappers -----------------------------------------------------
@@ -145,14 +146,18 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for phase `parity` of an mbarrier; gives up after `limit_ns` of
-// global time and returns false (the caller records an error and stops).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+// Wait for phase `parity` of an mbarrier, backing off with `sleep_ns` naps
+// after a few polls so a waiting warp does not take issue slots from working
+// ones; gives up after `limit_ns` of global time and returns false (the
+// caller records an error and stops).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t sleep_ns = 20,
+                                          uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 0 && global_ns() - t0 > limit_ns) return false;
+    if (i > 4) __nanosleep(sleep_ns);
+    if ((i & 63) == 0 && global_ns() - t0 > limit_ns) return false;
   }
 }
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes and

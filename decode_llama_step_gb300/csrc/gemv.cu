@@ -19,9 +19,11 @@
 //    per value); products accumulate in packed f32x2 FMAs; per-row partials
 //    reduce across lanes with a halving butterfly and across warps in a fixed
 //    order (deterministic results).
-//  * Prologues: copy, rmsnorm(x) * g, or silu(gate) * up, computed while the
-//    activation is loaded into registers.  Epilogues: store, residual add, or
-//    RoPE on adjacent (q, k) pairs plus the fp16 K/V append into the cache.
+//  * Prologues: copy or rmsnorm(x) * g, computed while the activation is
+//    loaded into registers.  Epilogues: store, residual add, RoPE on adjacent
+//    (q, k) pairs plus the fp16 K/V append into the cache, or SwiGLU on
+//    interleaved (gate, up) row pairs (engine page, section 4.4: SwiGLU
+//    fused with the projection), which feeds the down projection directly.
 #include "kernels.h"
 
 namespace dls {
@@ -163,29 +165,13 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
     // ---------------- consumers
     griddep_wait();
     if (nst == 0) griddep_launch();
-    // prologue: this lane's activation slice, in registers
-    if (PRO == PRO_RMSNORM) {
-      float ss = 0.f;
-      const int n4 = cols >> 2;
-      const float4* x4 = reinterpret_cast<const float4*>(a.x);
-      for (int i = tid; i < n4; i += nwc * 32) {
-        const float4 v = x4[i];
-        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-      }
-      for (int i = (n4 << 2) + tid; i < cols; i += nwc * 32) ss = fmaf(a.x[i], a.x[i], ss);
-      ss = warp_sum(ss);
-      if (lane == 0) sh.red[warp] = ss;
-      named_bar(1, nwc * 32);
-      if (tid == 0) {
-        float t = 0.f;
-        for (int i = 0; i < nwc; ++i) t += sh.red[i];  // fixed order
-        sh.rs = 1.0f / sqrtf(t / (float)cols + a.eps);
-      }
-      named_bar(1, nwc * 32);
-    }
+    // prologue: this lane's activation slice in registers, loaded with one
+    // round of float4 loads.  The consumer lanes' slices partition [0, kpad),
+    // so their squares also give the RMSNorm sum of squares.
     const int nchunk = (kpad + G::CH - 1) / G::CH;
     const int mc = warp < nchunk ? min(MC, (nchunk - warp + nwc - 1) / nwc) : 0;
-    float2 xr[MC][G::XV];
+    constexpr int V4 = G::XV / 2;  // float4 per lane per chunk
+    float4 raw[MC][V4];
     bool valid[MC];
 #pragma unroll
     for (int k = 0; k < MC; ++k) {
@@ -193,24 +179,68 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
       const int col0 = WT == 8 ? c * 512 + lane * 16 : (c * 32 + lane) * 32;
       valid[k] = k < mc && col0 < kpad;
 #pragma unroll
-      for (int e = 0; e < G::XV; ++e) {
-        float v0 = 0.f, v1 = 0.f;
-        const int i0 = col0 + 2 * e;
+      for (int m4 = 0; m4 < V4; ++m4) {
+        const int i0 = col0 + 4 * m4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (valid[k]) {
-          if (i0 < cols) {
-            if (PRO == PRO_SWIGLU) v0 = silu(a.x[i0]) * a.x[cols + i0];
-            else v0 = a.x[i0];
-            if (PRO == PRO_RMSNORM) v0 *= sh.rs * a.g[i0];
-          }
-          if (i0 + 1 < cols) {
-            if (PRO == PRO_SWIGLU) v1 = silu(a.x[i0 + 1]) * a.x[cols + i0 + 1];
-            else v1 = a.x[i0 + 1];
-            if (PRO == PRO_RMSNORM) v1 *= sh.rs * a.g[i0 + 1];
+          if (i0 + 3 < cols && (cols & 3) == 0) {
+            v = *reinterpret_cast<const float4*>(a.x + i0);
+          } else {
+            if (i0 < cols) v.x = a.x[i0];
+            if (i0 + 1 < cols) v.y = a.x[i0 + 1];
+            if (i0 + 2 < cols) v.z = a.x[i0 + 2];
+            if (i0 + 3 < cols) v.w = a.x[i0 + 3];
           }
         }
-        xr[k][e] = make_float2(v0, v1);
+        raw[k][m4] = v;
       }
     }
+    if (PRO == PRO_RMSNORM) {
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < MC; ++k)
+#pragma unroll
+        for (int m4 = 0; m4 < V4; ++m4) {
+          const float4 v = raw[k][m4];
+          ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+        }
+      ss = warp_sum(ss);
+      if (lane == 0) sh.red[warp] = ss;
+      named_bar(1, nwc * 32);
+      float t = 0.f;
+      for (int i = 0; i < nwc; ++i) t += sh.red[i];  // fixed order, same in every thread
+      const float rs = 1.0f / sqrtf(t / (float)cols + a.eps);
+#pragma unroll
+      for (int k = 0; k < MC; ++k) {
+        const int c = warp + k * nwc;
+        const int col0 = WT == 8 ? c * 512 + lane * 16 : (c * 32 + lane) * 32;
+#pragma unroll
+        for (int m4 = 0; m4 < V4; ++m4) {
+          const int i0 = col0 + 4 * m4;
+          float4 gg = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (valid[k]) {
+            if (i0 + 3 < cols && (cols & 3) == 0) {
+              gg = *reinterpret_cast<const float4*>(a.g + i0);
+            } else {
+              if (i0 < cols) gg.x = a.g[i0];
+              if (i0 + 1 < cols) gg.y = a.g[i0 + 1];
+              if (i0 + 2 < cols) gg.z = a.g[i0 + 2];
+              if (i0 + 3 < cols) gg.w = a.g[i0 + 3];
+            }
+          }
+          raw[k][m4] = make_float4(raw[k][m4].x * rs * gg.x, raw[k][m4].y * rs * gg.y, raw[k][m4].z * rs * gg.z,
+                                   raw[k][m4].w * rs * gg.w);
+        }
+      }
+    }
+    float2 xr[MC][G::XV];
+#pragma unroll
+    for (int k = 0; k < MC; ++k)
+#pragma unroll
+      for (int m4 = 0; m4 < V4; ++m4) {
+        xr[k][2 * m4] = make_float2(raw[k][m4].x, raw[k][m4].y);
+        xr[k][2 * m4 + 1] = make_float2(raw[k][m4].z, raw[k][m4].w);
+      }
 
     int32_t pos = 0, seq = 0;
     if (EPI == EPI_QKV) {
@@ -299,6 +329,17 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
               *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(v0, v1);
             }
           }
+        } else if (EPI == EPI_SWIGLU) {
+          // rows (2i, 2i+1) are (gate_i, up_i): h_i = silu(gate_i) * up_i
+          for (int pi = tid; pi < (bn >> 1); pi += nwc * 32) {
+            const int lr = pi * 2;
+            float g0 = 0.f, u0 = 0.f;
+            for (int ww = 0; ww < nwa; ++ww) {
+              g0 += s_part[ww * kRB + lr];
+              u0 += s_part[ww * kRB + lr + 1];
+            }
+            a.y[(b0 + lr) >> 1] = silu(g0) * u0;
+          }
         } else {
           for (int lr = tid; lr < bn; lr += nwc * 32) {
             float v = 0.f;
@@ -341,12 +382,12 @@ KernelFn pick(int wtype, int pro, int epi, int rs, int mc) {
   DLS_PICK(8, PRO_RMSNORM, EPI_QKV)
   DLS_PICK(8, PRO_COPY, EPI_RESID)
   DLS_PICK(8, PRO_RMSNORM, EPI_STORE)
-  DLS_PICK(8, PRO_SWIGLU, EPI_RESID)
+  DLS_PICK(8, PRO_RMSNORM, EPI_SWIGLU)
   DLS_PICK(8, PRO_COPY, EPI_STORE)
   DLS_PICK(4, PRO_RMSNORM, EPI_QKV)
   DLS_PICK(4, PRO_COPY, EPI_RESID)
   DLS_PICK(4, PRO_RMSNORM, EPI_STORE)
-  DLS_PICK(4, PRO_SWIGLU, EPI_RESID)
+  DLS_PICK(4, PRO_RMSNORM, EPI_SWIGLU)
   DLS_PICK(4, PRO_COPY, EPI_STORE)
 #undef DLS_PICK
   return nullptr;
@@ -401,8 +442,8 @@ GemvLaunch gemv_plan(int wtype, int pro, int epi, int rows, int nb, int num_sms,
 }
 
 cudaError_t gemv_setup_attributes() {
-  const int pros[3] = {PRO_COPY, PRO_RMSNORM, PRO_SWIGLU};
-  const int epis[3] = {EPI_STORE, EPI_RESID, EPI_QKV};
+  const int pros[2] = {PRO_COPY, PRO_RMSNORM};
+  const int epis[4] = {EPI_STORE, EPI_RESID, EPI_QKV, EPI_SWIGLU};
   for (int wt : {8, 4})
     for (int p : pros)
       for (int e : epis)

@@ -9,8 +9,9 @@
 
 namespace dls {
 
-enum Pro { PRO_COPY = 0, PRO_RMSNORM = 1, PRO_SWIGLU = 2 };
-enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2 };
+enum Pro { PRO_COPY = 0, PRO_RMSNORM = 1 };
+// EPI_SWIGLU: rows come in (gate, up) pairs; y[r/2] = silu(gate) * up
+enum Epi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
 
 // Where a decode row finds its KV pages (model path: row b is sequence
 // sp->seq[b] at position sp->pos[b]).
@@ -24,10 +25,10 @@ struct KvView {
 struct GemvArgs {
   MatDev w;
   int unit;                  // rows are split across CTAs in multiples of this
-  const float* x;            // PRO_COPY/RMSNORM: [cols]; PRO_SWIGLU: gate [cols] then up [cols]
+  const float* x;            // activation [cols]
   const float* g;            // RMSNorm gain [cols]
   float eps;
-  float* y;                  // STORE: y[r] = acc; RESID: y[r] += acc; QKV: q rows -> y
+  float* y;                  // STORE: y[r] = acc; RESID: y[r] += acc; QKV: q rows -> y; SWIGLU: y[r/2]
   // EPI_QKV
   int q_rows, kv_rows;
   KvView kv;
@@ -83,12 +84,17 @@ cudaError_t launch_attention(const AttnArgs& a, int rows, cudaStream_t s, bool p
 
 cudaError_t launch_embed(const MatDev& emb, int wtype, StepParams* sp, int brow, float* x, int vocab,
                          cudaStream_t s, bool pdl);
-cudaError_t launch_argmax(const float* logits, int vocab, int rows, int32_t* out, cudaStream_t s, bool pdl);
+// greedy pick per row over [rows][vocab]; part/counters: scratch of
+// argmax_scratch_entries(rows, num_sms) int2 and `rows` ints (zero between calls)
+int argmax_blocks(int rows, int num_sms);
+cudaError_t launch_argmax(const float* logits, int vocab, int rows, int32_t* out, int2* part, int* counters,
+                          int nblk, cudaStream_t s, bool pdl);
 cudaError_t launch_advance(StepParams* sp, const int32_t* next, int32_t* tokens_out, int rows, cudaStream_t s,
                            bool pdl);
 cudaError_t launch_set_params(StepParams* sp, const StepParams& h, bool reset_step, cudaStream_t s);
-cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, int ds, uint8_t* qs, __half* d,
-                          cudaStream_t s);
+// source row r goes to destination row r * row_step (qs, d point at the first destination row)
+cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, int ds, int row_step, uint8_t* qs,
+                          __half* d, cudaStream_t s);
 cudaError_t launch_rope_table(float2* cs, int len, int head_dim, float theta, cudaStream_t s);
 cudaError_t launch_dequant(const MatDev& m, int wtype, float* out, cudaStream_t s);
 // copy whole KV pages: pairs[i] = (src_page, dst_page), for every layer

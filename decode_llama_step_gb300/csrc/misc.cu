@@ -25,6 +25,7 @@ cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, cudaStream_t s, boo
 // one dequantised weight: exact in fp32 (11-bit scale times a code of at most 8 bits)
 __device__ __forceinline__ float dq(const MatDev& m, int wtype, int row, int col) {
   const int blk = col >> 5, e = col & 31;
+  row *= m.rstep;
   const float d = __half2float(m.d[(size_t)row * m.ds + blk]);
   if (wtype == 8) {
     const uint32_t u = (uint32_t)m.qs[(size_t)row * m.nb * 32 + col] ^ 0x80u;
@@ -82,29 +83,40 @@ __global__ void embed_kernel(const MatDev emb, int wtype, StepParams* sp, int br
 
 // ---------------------------------------------------------------- greedy pick
 
-__global__ void argmax_kernel(const float* logits, int vocab, int32_t* out) {
+// CTA (blk, row) reduces a contiguous slice of one row to (value, index);
+// the last CTA of the row to finish reduces the slices in order.  Ties go
+// to the lowest index; NaN never wins.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+__global__ void argmax_kernel(const float* logits, int vocab, int32_t* out, int2* part, int* counters) {
   griddep_wait();
   griddep_launch();
-  const float* row = logits + (size_t)blockIdx.x * vocab;
+  const int row = blockIdx.y, nblk = gridDim.x;
+  const int per = (vocab + nblk - 1) / nblk;
+  const int lo = blockIdx.x * per, hi = min(vocab, lo + per);
+  const float* r = logits + (size_t)row * vocab;
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  for (int i = threadIdx.x; i < vocab; i += blockDim.x) {
-    const float v = row[i];
-    if (v > best) {  // strided scan: the first (lowest) index wins ties per thread
+  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    const float v = r[i];
+    if (better(v, i, best, bi)) {
       best = v;
       bi = i;
     }
   }
-  __shared__ float sv[32];
-  __shared__ int si[32];
   for (int o = 16; o > 0; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, best, o);
     const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ov > best || (ov == best && oi < bi)) {
+    if (better(ov, oi, best, bi)) {
       best = ov;
       bi = oi;
     }
   }
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
     sv[warp] = best;
@@ -113,12 +125,28 @@ __global__ void argmax_kernel(const float* logits, int vocab, int32_t* out) {
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
-      if (sv[w] > best || (sv[w] == best && si[w] < bi)) {
+      if (better(sv[w], si[w], best, bi)) {
         best = sv[w];
         bi = si[w];
       }
-    out[blockIdx.x] = bi == 0x7fffffff ? 0 : bi;  // all-NaN row: 0
+    part[(size_t)row * nblk + blockIdx.x] = make_int2(__float_as_int(best), bi);
+    __threadfence();
+    s_last = atomicAdd(&counters[row], 1) == nblk - 1;
   }
+  __syncthreads();
+  if (!s_last || threadIdx.x != 0) return;
+  __threadfence();
+  best = -INFINITY;
+  bi = 0x7fffffff;
+  for (int b = 0; b < nblk; ++b) {
+    const int2 p = __ldcg(&part[(size_t)row * nblk + b]);
+    if (better(__int_as_float(p.x), p.y, best, bi)) {
+      best = __int_as_float(p.x);
+      bi = p.y;
+    }
+  }
+  out[row] = bi == 0x7fffffff ? 0 : bi;  // all-NaN row: 0
+  counters[row] = 0;
 }
 
 // next token := argmax, position += 1, record the token for the host
@@ -156,14 +184,15 @@ __global__ void set_params_kernel(StepParams* sp, const StepParams h, int reset_
 // ---------------------------------------------------------------- weight layout
 
 // GGUF-style blocks (2-byte scale + codes) -> scale array + code array
-__global__ void repack_kernel(const uint8_t* src, int wtype, long long n_blocks, int nb, int ds, uint8_t* qs,
-                              __half* d) {
+__global__ void repack_kernel(const uint8_t* src, int wtype, long long n_blocks, int nb, int ds, int row_step,
+                              uint8_t* qs, __half* d) {
   const int bsz = wtype == 8 ? 34 : 18, nq = bsz - 2;
   for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < n_blocks;
        b += (long long)gridDim.x * blockDim.x) {
     const uint8_t* s = src + b * bsz;
-    d[(b / nb) * ds + (b % nb)] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
-    uint8_t* q = qs + b * nq;
+    const long long r = (b / nb) * row_step, j = b % nb;
+    d[r * ds + j] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
+    uint8_t* q = qs + (r * nb + j) * nq;
     for (int i = 0; i < nq; ++i) q[i] = s[2 + i];
   }
 }
@@ -247,9 +276,15 @@ cudaError_t launch_embed(const MatDev& emb, int wtype, StepParams* sp, int brow,
   return launch_ex((const void*)embed_kernel, dim3(1), dim3(256), s, pdl, args);
 }
 
-cudaError_t launch_argmax(const float* logits, int vocab, int rows, int32_t* out, cudaStream_t s, bool pdl) {
-  void* args[] = {&logits, &vocab, &out};
-  return launch_ex((const void*)argmax_kernel, dim3(rows), dim3(1024), s, pdl, args);
+int argmax_blocks(int rows, int num_sms) {
+  int n = (2 * num_sms) / (rows > 0 ? rows : 1);
+  return n < 1 ? 1 : (n > num_sms ? num_sms : n);
+}
+
+cudaError_t launch_argmax(const float* logits, int vocab, int rows, int32_t* out, int2* part, int* counters,
+                          int nblk, cudaStream_t s, bool pdl) {
+  void* args[] = {&logits, &vocab, &out, &part, &counters};
+  return launch_ex((const void*)argmax_kernel, dim3(nblk, rows), dim3(256), s, pdl, args);
 }
 
 cudaError_t launch_advance(StepParams* sp, const int32_t* next, int32_t* tokens_out, int rows, cudaStream_t s,
@@ -263,10 +298,10 @@ cudaError_t launch_set_params(StepParams* sp, const StepParams& h, bool reset_st
   return cudaGetLastError();
 }
 
-cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, int ds, uint8_t* qs, __half* d,
-                          cudaStream_t s) {
+cudaError_t launch_repack(const uint8_t* src, int wtype, int rows, int nb, int ds, int row_step, uint8_t* qs,
+                          __half* d, cudaStream_t s) {
   const long long n = (long long)rows * nb;
-  repack_kernel<<<grid_for(n, 256), 256, 0, s>>>(src, wtype, n, nb, ds, qs, d);
+  repack_kernel<<<grid_for(n, 256), 256, 0, s>>>(src, wtype, n, nb, ds, row_step, qs, d);
   return cudaGetLastError();
 }
 
