@@ -133,6 +133,16 @@ struct dls_model {
   float* capture = nullptr;
   int launches_per_step = 0;
   int launch_count = 0;
+  // persistent decode-step kernel (all layers resident, one row, no capture)
+  StepPlan step{};
+  bool use_step = false;
+  bool step_graph_ok = true;  // false: the cooperative launch could not be captured; run it eagerly
+  StepLayer* step_layers = nullptr;
+  float *step_part_o = nullptr, *step_part_ml = nullptr;
+  int* step_att_cnt = nullptr;
+  int2* step_am = nullptr;
+  unsigned* step_bar = nullptr;  // [0] barrier counter, [1] abort flag
+  unsigned long long* step_trace = nullptr;  // phase timestamps when profiling
   // per-kernel timing (dls_debug_profile_step): an event after every launch
   bool profiling = false;
   // programmatic dependent launch between the step's kernels; off by default
@@ -295,7 +305,7 @@ MatDev head_mat(const dls_model* m) {
 // stream fills buffer (l - resident) % 2 while the previous layer computes.
 
 enum KernelKind { K_EMBED = 1, K_QKV = 2, K_ATTN = 3, K_O = 4, K_GATE_UP = 5, K_DOWN = 6, K_HEAD = 7, K_ARGMAX = 8,
-                  K_ADVANCE = 9 };
+                  K_ADVANCE = 9, K_STEP = 10 };
 
 int prof_mark(dls_model* m, int kind) {
   const size_t i = m->prof_kinds.size();
@@ -432,8 +442,59 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
   return DLS_OK;
 }
 
+int enqueue_persistent(dls_model* m, bool head, bool argmax) {
+  StepArgs a{};
+  a.layers = m->step_layers;
+  a.n_layers = m->L;
+  a.emb = mat_at(m->emb_block, m->emb_off);
+  a.head = head_mat(m);
+  a.out_norm = m->out_norm;
+  a.H = m->H;
+  a.q_rows = m->q_rows;
+  a.kv_rows = m->kv_rows;
+  a.n_heads = m->nh;
+  a.n_kv = m->nkv;
+  a.hd = m->hd;
+  a.F = m->F;
+  a.vocab = m->V;
+  a.eps = m->eps;
+  a.page_table = m->pt_dev;
+  a.max_pages = m->max_pages;
+  a.page_tokens = m->pt;
+  a.max_len = m->max_ctx;
+  a.rope_cs = m->rope;
+  a.rope_len = m->rope_len;
+  a.sp = m->sp;
+  a.x = m->x;
+  a.q = m->q;
+  a.o = m->o;
+  a.h = m->gu;
+  a.logits = m->logits;
+  a.part_o = m->step_part_o;
+  a.part_ml = m->step_part_ml;
+  a.att_counters = m->step_att_cnt;
+  a.am_part = m->step_am;
+  a.tokens_out = argmax ? m->tokens_dev : nullptr;
+  a.greedy = argmax ? 1 : 0;
+  a.head_rows = (head || argmax) ? m->V : 0;
+  a.bar = m->step_bar;
+  a.abort = reinterpret_cast<int*>(m->step_bar + 1);
+  a.S = m->step.splits;
+  a.trace = m->profiling ? m->step_trace : nullptr;
+  a.ns = m->step.ns;
+  a.stage_bytes = m->step.stage_bytes;
+  CK(cudaMemsetAsync(m->step_bar, 0, 2 * sizeof(unsigned), m->stream));
+  LK(K_STEP, launch_step(m->step, a, m->stream));
+  return DLS_OK;
+}
+
 int enqueue_step(dls_model* m, int rows, bool head, bool argmax, float* capture) {
   m->launch_count = 0;
+  if (m->use_step && rows == 1 && !capture) {
+    TRY(enqueue_persistent(m, head, argmax));
+    m->launches_per_step = m->launch_count;
+    return DLS_OK;
+  }
   for (int b = 0; b < rows; ++b) TRY(enqueue_row(m, b, head, argmax, b == 0 ? capture : nullptr));
   if (argmax) LK(K_ADVANCE, launch_advance(m->sp, m->next_tok, m->tokens_dev, rows, m->stream, m->pdl));
   m->launches_per_step = m->launch_count;
@@ -452,6 +513,8 @@ int run_step(dls_model* m, int rows, bool head, bool argmax) {
     m->capture = nullptr;
     return enqueue_step(m, rows, head, argmax, cap);
   }
+  const bool persistent = m->use_step && rows == 1;
+  if (persistent && !m->step_graph_ok) return enqueue_step(m, rows, head, argmax, nullptr);
   for (auto& g : m->graphs)
     if (g.rows == rows && g.head == head && g.argmax == argmax) {
       CK(cudaGraphLaunch(g.exec, m->stream));
@@ -461,15 +524,17 @@ int run_step(dls_model* m, int rows, bool head, bool argmax) {
   CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
   const int r = enqueue_step(m, rows, head, argmax, nullptr);
   cudaError_t e = cudaStreamEndCapture(m->stream, &graph);
-  if (r != DLS_OK) {
-    if (graph) cudaGraphDestroy(graph);
-    return r;
-  }
-  if (e != cudaSuccess) return fail(m, DLS_ERR_CUDA, "capture cuda=%s", cudaGetErrorString(e));
   cudaGraphExec_t exec = nullptr;
-  e = cudaGraphInstantiate(&exec, graph, 0);
-  cudaGraphDestroy(graph);
-  if (e != cudaSuccess) return fail(m, DLS_ERR_CUDA, "instantiate cuda=%s", cudaGetErrorString(e));
+  if (r == DLS_OK && e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+  if (graph) cudaGraphDestroy(graph);
+  if (persistent && (r != DLS_OK || e != cudaSuccess)) {
+    // a cooperative launch that cannot live in a graph: launch it directly
+    cudaGetLastError();
+    m->step_graph_ok = false;
+    return enqueue_step(m, rows, head, argmax, nullptr);
+  }
+  if (r != DLS_OK) return r;
+  if (e != cudaSuccess) return fail(m, DLS_ERR_CUDA, "capture cuda=%s", cudaGetErrorString(e));
   m->graphs.push_back({rows, head, argmax, exec});
   CK(cudaGraphLaunch(exec, m->stream));
   return DLS_OK;
@@ -570,6 +635,8 @@ int auto_resident(const dls_model* m, uint64_t other_bytes) {
   return (int)std::min<uint64_t>(room / lb, (uint64_t)m->L - 1);
 }
 
+int setup_persistent(dls_model* m);
+
 int apply_resident(dls_model* m, int n) {
   // evict layers [n, L): keep a pinned host copy, then free the device copy
   for (int l = n; l < m->L; ++l) {
@@ -607,6 +674,45 @@ int apply_resident(dls_model* m, int n) {
   TRY(sync_stream(m, m->stream));
   m->resident = n;
   drop_graphs(m);
+  return setup_persistent(m);
+}
+
+// Plan the persistent step kernel when every layer is resident; allocate its
+// scratch once.  Without a plan the step runs as separate kernels.
+int setup_persistent(dls_model* m) {
+  m->use_step = false;
+  // opt-in (DLS_STEP_KERNEL=1) until it is faster than the separate kernels
+  const char* e = getenv("DLS_STEP_KERNEL");
+  if (!e || atoi(e) == 0) return DLS_OK;
+  if (m->resident < m->L) return DLS_OK;
+  if (!m->step.fn) m->step = step_plan(m->wtype, m->H, m->q_rows, m->F, m->nh, m->nkv, m->hd, m->num_sms);
+  if (!m->step.fn) return DLS_OK;
+  const int g = m->nh / m->nkv, S = m->step.splits;
+  if (!m->step_layers) {
+    TRY(dev_alloc_t(m, (size_t)m->L, &m->step_layers, "step_layers"));
+    TRY(dev_alloc_t(m, (size_t)m->nkv * S * g * m->hd, &m->step_part_o, "step_attention_partials"));
+    TRY(dev_alloc_t(m, (size_t)m->nkv * S * g * 2, &m->step_part_ml, "step_attention_ml"));
+    TRY(dev_alloc_t(m, (size_t)m->nkv, &m->step_att_cnt, "step_attention_counters"));
+    TRY(dev_alloc_t(m, (size_t)m->step.grid, &m->step_am, "step_argmax"));
+    TRY(dev_alloc_t(m, (size_t)2, &m->step_bar, "step_barrier"));
+    TRY(dev_alloc_t(m, (size_t)(5 * m->L + 8), &m->step_trace, "step_trace"));
+    CK(cudaMemsetAsync(m->step_att_cnt, 0, m->nkv * sizeof(int), m->stream));
+  }
+  std::vector<StepLayer> hl(m->L);
+  for (int l = 0; l < m->L; ++l) {
+    const LayerPtrs P = layer_ptrs(m, m->layer_dev[l]);
+    hl[l].attn_norm = P.attn_norm;
+    hl[l].ffn_norm = P.ffn_norm;
+    hl[l].qkv = P.qkv;
+    hl[l].o = P.o;
+    hl[l].gu = P.gu;
+    hl[l].down = P.down;
+    hl[l].k_pool = m->k_pool + (size_t)l * m->kv_layer_elems;
+    hl[l].v_pool = m->v_pool + (size_t)l * m->kv_layer_elems;
+  }
+  CK(cudaMemcpyAsync(m->step_layers, hl.data(), hl.size() * sizeof(StepLayer), cudaMemcpyHostToDevice, m->stream));
+  TRY(sync_stream(m, m->stream));
+  m->use_step = true;
   return DLS_OK;
 }
 
@@ -867,6 +973,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   m->free_pages.clear();
   for (int i = m->n_pages - 1; i >= 0; --i) m->free_pages.push_back(i);
   m->seqs.assign(m->max_seqs, Seq());
+  TRYC(setup_persistent(m));
   *out = m;
   return DLS_OK;
 #undef CKC
@@ -1089,6 +1196,21 @@ int dls_debug_profile_step(dls_model* m, int32_t seq, int32_t token, int32_t pos
   m->profiling = false;
   TRY(r);
   TRY(sync_stream(m, m->stream));
+  if (m->use_step) {
+    // one persistent launch: per-phase durations from its timestamps
+    const int nph = 5 * m->L + 2;  // embed, 5 per layer, head
+    std::vector<unsigned long long> ts(nph + 1);
+    CK(cudaMemcpy(ts.data(), m->step_trace, ts.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+    const int kinds[5] = {K_QKV, K_ATTN, K_O, K_GATE_UP, K_DOWN};
+    if (nph > max_kernels) return fail(m, DLS_ERR_ARG, "max_kernels=%d < %d phases", max_kernels, nph);
+    for (int i = 0; i < nph; ++i) {
+      kernel_ms[i] = (float)((ts[i + 1] - ts[i]) * 1e-6);
+      kernel_kind[i] = i == 0 ? K_EMBED : (i == nph - 1 ? K_HEAD : kinds[(i - 1) % 5]);
+    }
+    *n_kernels = nph;
+    s.len += 1;
+    return DLS_OK;
+  }
   const int n = (int)m->prof_kinds.size() - 1;
   if (n > max_kernels) return fail(m, DLS_ERR_ARG, "max_kernels=%d < %d launches", max_kernels, n);
   for (int i = 0; i < n; ++i) {

@@ -105,6 +105,52 @@ cudaError_t launch_delay(long long ns, cudaStream_t s);
 cudaError_t launch_kv_gather(const __half* pool, const int32_t* pages, int len, int n_kv, int page_tokens,
                              int head_dim, __half* out, cudaStream_t s);
 
+// ---- persistent decode step ------------------------------------------------------
+
+struct StepLayer {
+  const float* attn_norm;
+  const float* ffn_norm;
+  MatDev qkv, o, gu, down;  // gu: interleaved (gate, up) rows
+  __half* k_pool;           // this layer's KV pools
+  __half* v_pool;
+};
+
+struct StepArgs {
+  const StepLayer* layers;  // device array [n_layers]
+  int n_layers;
+  MatDev emb, head;
+  const float* out_norm;
+  int H, q_rows, kv_rows, n_heads, n_kv, hd, F, vocab;
+  float eps;
+  const int32_t* page_table;  // [max_seqs][max_pages]; the step serves row 0 of sp
+  int max_pages, page_tokens, max_len;
+  const float2* rope_cs;
+  int rope_len;
+  StepParams* sp;
+  float *x, *q, *o, *h, *logits;
+  float *part_o, *part_ml;  // attention partials [n_kv * S]
+  int* att_counters;        // [n_kv], zero between launches
+  int2* am_part;            // [grid]
+  int32_t* tokens_out;      // greedy: token of step sp->step goes to tokens_out[step]
+  int greedy;               // pick argmax and advance sp at the end
+  int head_rows;            // 0: skip the LM head (prefill tokens before the last)
+  unsigned* bar;            // grid barrier counter, zero at launch
+  int* abort;               // set when a bounded wait gives up, zero at launch
+  int S;                    // attention splits per KV head (one per CTA)
+  unsigned long long* trace;  // optional: CTA 0 writes the global timer after each phase
+  int ns;                   // ring stages
+  uint32_t stage_bytes;     // ring slot size
+};
+
+struct StepPlan {
+  const void* fn;  // NULL: no persistent kernel for this shape
+  int grid, threads, smem, ns, splits;
+  uint32_t stage_bytes;
+};
+
+StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, int hd, int num_sms);
+cudaError_t launch_step(const StepPlan& p, const StepArgs& a, cudaStream_t s);
+
 // Record a failure for dls_last_error(NULL) (calls without a model) and
 // return `code`.
 int report_error(int code, const char* fmt, ...);

@@ -1,0 +1,814 @@
+// Persistent decode-step kernel: the whole single-token decode step of a
+// resident model (embedding, every layer's QKV GEMV + RoPE + KV append,
+// attention, O GEMV, gate/up GEMV + SwiGLU, down GEMV, final norm + LM head,
+// and optionally the greedy pick) in one cooperative launch with one CTA per
+// SM.
+//
+// Why: the step is HBM-bound on weights, but run as ~160 separate kernels
+// every boundary costs a launch, a pipeline ramp and a latency-bound
+// prologue while HBM idles.  Here one producer warp per CTA streams this
+// CTA's slice of every phase's weights -- and the K/V tiles of its
+// attention task -- through one shared-memory ring in program order, never
+// waiting on the phase boundaries (weights and past K/V do not depend on
+// them).  Eight consumer warps run the phases in order, separated by grid
+// barriers; while they wait at a barrier the ring keeps filling.
+//
+// Phases per token (pages: the engine page, sections 1 and 4.4):
+//   embed -> for each layer: QKV | attention | O | gate/up | down -> head [-> argmax]
+// with a grid barrier after each.  Row slices, chunk ownership, reduction
+// orders and epilogues follow the standalone decode GEMV (gemv.cu), and the
+// attention task follows attention.cu's split-K scheme with the splits
+// mapped one per CTA.
+//
+// Every wait is bounded: an mbarrier or grid-barrier wait that runs out
+// sets a global abort flag that ends all other waits, and a status bit the
+// host reads.  The producer never leaves with copies in flight.
+#include <math.h>
+
+#include "gemv_core.cuh"
+#include "kernels.h"
+
+namespace dls {
+
+namespace {
+
+constexpr int NWC = 8;               // consumer warps
+constexpr int NTHR = 32 * (NWC + 1);
+constexpr int kRB = 64;              // rows per epilogue block
+constexpr int kTile = 32;            // attention tokens per ring stage
+constexpr int kMaxStages = 16;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct Sh {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  float red[32];
+  int last;
+};
+
+struct Ctx {
+  const StepArgs* A;
+  Sh* sh;
+  uint8_t* ring;
+  float* s_part;   // [NWC][kRB]
+  float* s_q;      // [G*HD]
+  float* s_wm;     // [NWC][G]
+  float* s_wl;     // [NWC][G]
+  float* s_wo;     // [NWC][G*HD]
+  int sidx;        // ring stages consumed / produced so far
+  unsigned epoch;  // grid barriers passed (thread 0)
+  int pos, seq;
+};
+
+__device__ __forceinline__ bool aborted(const StepArgs& A) { return *(volatile int*)A.abort != 0; }
+
+__device__ __forceinline__ void set_abort(const StepArgs& A) {
+  atomicExch(A.abort, 1);
+  atomicOr(&A.sp->status, kTimeout);
+}
+
+// mbarrier wait that also gives up when another CTA aborted
+__device__ __forceinline__ bool wait_bar(const StepArgs& A, uint32_t bar, uint32_t parity, uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i > 4) __nanosleep(sleep_ns);
+    if ((i & 63) == 0) {
+      if (aborted(A)) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        set_abort(A);
+        return false;
+      }
+    }
+  }
+}
+
+// All consumer warps of all CTAs; the producer warp never takes part.
+__device__ __forceinline__ void grid_sync(Ctx& c) {
+  const StepArgs& A = *c.A;
+  named_bar(1, NWC * 32);
+  if (A.trace && blockIdx.x == 0 && threadIdx.x == 0) A.trace[c.epoch + 1] = global_ns();  // phase end
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned target = (++c.epoch) * gridDim.x;
+    atomicAdd(A.bar, 1u);
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(A.bar) : "memory");
+      if (v >= target) break;
+      if ((i & 15) == 15) {
+        if (aborted(A)) break;
+        if (global_ns() - t0 > kWaitNs) {
+          set_abort(A);
+          break;
+        }
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+  }
+  named_bar(1, NWC * 32);
+}
+
+__device__ __forceinline__ void row_split(int rows, int unit, int& r0, int& r1) {
+  const int units = (rows + unit - 1) / unit;
+  const int u0 = (int)((long long)units * blockIdx.x / gridDim.x);
+  const int u1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x);
+  r0 = u0 * unit;
+  r1 = min(rows, u1 * unit);
+}
+
+template <int WT>
+__device__ __forceinline__ size_t row_bytes_of(const MatDev& w) {
+  return WT == 8 ? (size_t)w.nb * 32 : (size_t)w.nb * 16;
+}
+
+// ------------------------------------------------------------------ producer
+
+template <int WT, int RS>
+__device__ void produce_gemv(Ctx& c, const MatDev& w, int unit, int& issued) {
+  const StepArgs& A = *c.A;
+  int r0, r1;
+  row_split(w.rows, unit, r0, r1);
+  const size_t rb = row_bytes_of<WT>(w), db = (size_t)w.ds * 2;
+  for (int row = r0; row < r1; row += RS) {
+    const int slot = c.sidx % A.ns;
+    if (c.sidx >= A.ns && !wait_bar(A, smem_u32(&c.sh->empty[slot]), ((c.sidx / A.ns) - 1) & 1, 200)) return;
+    const int n = min(RS, r1 - row);
+    uint8_t* dst = c.ring + (size_t)slot * A.stage_bytes;
+    const uint32_t bar = smem_u32(&c.sh->full[slot]);
+    mbar_expect_tx(bar, (uint32_t)(n * (rb + db)));
+    bulk_g2s(smem_u32(dst), w.qs + (size_t)row * rb, (uint32_t)(n * rb), bar);
+    bulk_g2s(smem_u32(dst + RS * rb), reinterpret_cast<const uint8_t*>(w.d) + (size_t)row * db, (uint32_t)(n * db),
+             bar);
+    ++c.sidx;
+    ++issued;
+  }
+}
+
+__device__ __forceinline__ void attn_task(const StepArgs& A, int n, int& kvh, int& tb, int& te) {
+  const int ntask = A.n_kv * A.S;
+  kvh = blockIdx.x / A.S;
+  const int sp = blockIdx.x % A.S;
+  const int n_tiles = (n + kTile - 1) / kTile;
+  const int per = (n_tiles + A.S - 1) / A.S;
+  tb = sp * per;
+  te = min(n_tiles, tb + per);
+  if ((int)blockIdx.x >= ntask) te = tb;  // no task for this CTA
+}
+
+template <int HD>
+__device__ void produce_attention(Ctx& c, const __half* k_pool, const __half* v_pool, int& issued) {
+  const StepArgs& A = *c.A;
+  const int n = c.pos + 1;
+  int kvh, tb, te;
+  attn_task(A, n, kvh, tb, te);
+  const int32_t* ptab = A.page_table + (size_t)c.seq * A.max_pages;
+  for (int t = tb; t < te; ++t) {
+    const int slot = c.sidx % A.ns;
+    if (c.sidx >= A.ns && !wait_bar(A, smem_u32(&c.sh->empty[slot]), ((c.sidx / A.ns) - 1) & 1, 200)) return;
+    const uint32_t bar = smem_u32(&c.sh->full[slot]);
+    // positions before pos are final; pos itself is written by this step
+    const int n_old = max(0, min(kTile, c.pos - t * kTile));
+    const int page = ptab[(t * kTile) / A.page_tokens];
+    if (n_old > 0 && page >= 0) {
+      const size_t base = (((size_t)page * A.n_kv + kvh) * A.page_tokens + (t * kTile) % A.page_tokens) * HD;
+      uint8_t* dst = c.ring + (size_t)slot * A.stage_bytes;
+      const uint32_t bytes = (uint32_t)n_old * HD * 2;
+      mbar_expect_tx(bar, 2 * bytes);
+      bulk_g2s(smem_u32(dst), k_pool + base, bytes, bar);
+      bulk_g2s(smem_u32(dst + kTile * HD * 2), v_pool + base, bytes, bar);
+    } else {
+      if (page < 0) atomicOr(&A.sp->status, kBadPage);
+      mbar_arrive(bar);
+    }
+    ++c.sidx;
+    ++issued;
+  }
+}
+
+// ------------------------------------------------------------------ consumers
+
+// The lane's activation slice (chunks warp, warp+NWC, ...), from L2.
+template <int WT, int PRO, int MC>
+__device__ __forceinline__ void load_x(Ctx& c, const MatDev& w, const float* x, const float* gain,
+                                       float2 (&xr)[MC][Geo<WT>::XV], bool (&valid)[MC]) {
+  using Gm = Geo<WT>;
+  constexpr int V4 = Gm::XV / 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kpad = w.nb * 32, cols = w.cols;
+  const int nchunk = (kpad + Gm::CH - 1) / Gm::CH;
+  const int mc = warp < nchunk ? min(MC, (nchunk - warp + NWC - 1) / NWC) : 0;
+  float4 raw[MC][V4];
+#pragma unroll
+  for (int k = 0; k < MC; ++k) {
+    const int ch = warp + k * NWC;
+    const int col0 = WT == 8 ? ch * 512 + lane * 16 : (ch * 32 + lane) * 32;
+    valid[k] = k < mc && col0 < kpad;
+#pragma unroll
+    for (int m4 = 0; m4 < V4; ++m4) {
+      const int i0 = col0 + 4 * m4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (valid[k]) {
+        if (i0 + 3 < cols && (cols & 3) == 0) {
+          v = __ldcg(reinterpret_cast<const float4*>(x + i0));
+        } else {
+          if (i0 < cols) v.x = __ldcg(x + i0);
+          if (i0 + 1 < cols) v.y = __ldcg(x + i0 + 1);
+          if (i0 + 2 < cols) v.z = __ldcg(x + i0 + 2);
+          if (i0 + 3 < cols) v.w = __ldcg(x + i0 + 3);
+        }
+      }
+      raw[k][m4] = v;
+    }
+  }
+  if (PRO == PRO_RMSNORM) {
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < MC; ++k)
+#pragma unroll
+      for (int m4 = 0; m4 < V4; ++m4) {
+        const float4 v = raw[k][m4];
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+      }
+    ss = warp_sum(ss);
+    named_bar(1, NWC * 32);  // previous readers of red[] are done
+    if (lane == 0) c.sh->red[warp] = ss;
+    named_bar(1, NWC * 32);
+    float t = 0.f;
+    for (int i = 0; i < NWC; ++i) t += c.sh->red[i];  // fixed order
+    const float rs = 1.0f / sqrtf(t / (float)cols + c.A->eps);
+#pragma unroll
+    for (int k = 0; k < MC; ++k) {
+      const int ch = warp + k * NWC;
+      const int col0 = WT == 8 ? ch * 512 + lane * 16 : (ch * 32 + lane) * 32;
+#pragma unroll
+      for (int m4 = 0; m4 < V4; ++m4) {
+        const int i0 = col0 + 4 * m4;
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid[k]) {
+          if (i0 + 3 < cols && (cols & 3) == 0) {
+            g = *reinterpret_cast<const float4*>(gain + i0);
+          } else {
+            if (i0 < cols) g.x = gain[i0];
+            if (i0 + 1 < cols) g.y = gain[i0 + 1];
+            if (i0 + 2 < cols) g.z = gain[i0 + 2];
+            if (i0 + 3 < cols) g.w = gain[i0 + 3];
+          }
+        }
+        raw[k][m4] = make_float4(raw[k][m4].x * rs * g.x, raw[k][m4].y * rs * g.y, raw[k][m4].z * rs * g.z,
+                                 raw[k][m4].w * rs * g.w);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < MC; ++k)
+#pragma unroll
+    for (int m4 = 0; m4 < V4; ++m4) {
+      xr[k][2 * m4] = make_float2(raw[k][m4].x, raw[k][m4].y);
+      xr[k][2 * m4 + 1] = make_float2(raw[k][m4].z, raw[k][m4].w);
+    }
+}
+
+struct EpiArgs {
+  float* y;
+  // EPI_QKV
+  __half* k_pool;
+  __half* v_pool;
+};
+
+template <int WT, int PRO, int EPI, int RS, int MC>
+__device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, const float* gain, const EpiArgs& e) {
+  using Gm = Geo<WT>;
+  const StepArgs& A = *c.A;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float2 xr[MC][Gm::XV];
+  bool valid[MC];
+  load_x<WT, PRO, MC>(c, w, x, gain, xr, valid);
+  int r0, r1;
+  row_split(w.rows, unit, r0, r1);
+  const int nrows = max(r1 - r0, 0);
+  const int nst = (nrows + RS - 1) / RS;
+  const size_t rb = row_bytes_of<WT>(w), db = (size_t)w.ds * 2;
+  const int kpad = w.nb * 32;
+  const int nchunk = (kpad + Gm::CH - 1) / Gm::CH;
+  const int nwa = min(NWC, nchunk);
+  constexpr int spb = kRB / RS;  // stages per epilogue block
+  for (int s = 0; s < nst; ++s) {
+    const int slot = c.sidx % A.ns;
+    const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), (c.sidx / A.ns) & 1, 20);
+    const int rows_s = min(RS, nrows - s * RS);
+    const uint8_t* st = c.ring + (size_t)slot * A.stage_bytes;
+    float acc[RS];
+#pragma unroll
+    for (int rr = 0; rr < RS; ++rr) acc[rr] = 0.f;
+    if (ok) {
+#pragma unroll
+      for (int k = 0; k < MC; ++k) {
+        if (!valid[k]) continue;
+        const int ch = warp + k * NWC;
+        const int qoff = WT == 8 ? ch * 512 + lane * 16 : (ch * 32 + lane) * 16;
+        const int blk = WT == 8 ? (ch * 512 + lane * 16) >> 5 : ch * 32 + lane;
+#pragma unroll
+        for (int rr = 0; rr < RS; ++rr) {
+          if (rr < rows_s) {
+            const uint4 q = *reinterpret_cast<const uint4*>(st + rr * rb + qoff);
+            const __half d = *reinterpret_cast<const __half*>(st + RS * rb + rr * db + blk * 2);
+            acc[rr] = fmaf(__half2float(d), dot16<WT>(q, xr[k]), acc[rr]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&c.sh->empty[slot]));
+    ++c.sidx;
+    const float t = butterfly<RS>(acc, lane);
+    const int rr = RS == 1 ? 0 : (lane >> (5 - (RS == 2 ? 1 : RS == 4 ? 2 : 3)));
+    const int lrow = s * RS + rr - (s / spb) * kRB;
+    if ((lane & ((32 / RS) - 1)) == 0 && rr < rows_s) c.s_part[warp * kRB + lrow] = t;
+
+    if ((s + 1) % spb == 0 || s == nst - 1) {
+      named_bar(1, NWC * 32);
+      const int b0 = r0 + (s / spb) * kRB;
+      const int bn = min(kRB, r1 - b0);
+      if (EPI == EPI_QKV || EPI == EPI_SWIGLU) {
+        for (int pi = tid; pi < (bn >> 1); pi += NWC * 32) {
+          const int lr = pi * 2, r = b0 + lr;
+          float v0 = 0.f, v1 = 0.f;
+          for (int ww = 0; ww < nwa; ++ww) {
+            v0 += c.s_part[ww * kRB + lr];
+            v1 += c.s_part[ww * kRB + lr + 1];
+          }
+          if (EPI == EPI_SWIGLU) {
+            e.y[r >> 1] = silu(v0) * v1;
+            continue;
+          }
+          const int hd = A.hd;
+          if (r < A.q_rows + A.kv_rows) {
+            if (c.pos < 0 || c.pos >= A.rope_len) {
+              atomicOr(&A.sp->status, kBadPos);
+              continue;
+            }
+            const float2 cs = A.rope_cs[(size_t)c.pos * (hd >> 1) + ((r % hd) >> 1)];
+            const float t0 = v0 * cs.x - v1 * cs.y;
+            v1 = v0 * cs.y + v1 * cs.x;
+            v0 = t0;
+          }
+          if (r < A.q_rows) {
+            e.y[r] = v0;
+            e.y[r + 1] = v1;
+          } else {
+            const bool is_k = r < A.q_rows + A.kv_rows;
+            const int rk = r - A.q_rows - (is_k ? 0 : A.kv_rows);
+            const int kvh = rk / hd, dim = rk % hd;
+            const int pt = A.page_tokens;
+            const int lp = c.pos / pt;
+            const int page = (c.pos >= 0 && lp < A.max_pages) ? A.page_table[(size_t)c.seq * A.max_pages + lp] : -1;
+            if (page < 0) {
+              atomicOr(&A.sp->status, kBadPage);
+              continue;
+            }
+            const size_t off = (((size_t)page * A.n_kv + kvh) * pt + (c.pos % pt)) * hd + dim;
+            *reinterpret_cast<__half2*>((is_k ? e.k_pool : e.v_pool) + off) = __floats2half2_rn(v0, v1);
+          }
+        }
+      } else {
+        for (int lr = tid; lr < bn; lr += NWC * 32) {
+          float v = 0.f;
+          for (int ww = 0; ww < nwa; ++ww) v += c.s_part[ww * kRB + lr];
+          if (EPI == EPI_RESID) e.y[b0 + lr] = __ldcg(e.y + b0 + lr) + v;
+          else e.y[b0 + lr] = v;
+        }
+      }
+      named_bar(1, NWC * 32);
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// One CTA's attention task: split sp of KV head kvh.  Warp j % NWC owns the
+// task's j-th tile (one ring stage); position pos (written this step) is
+// copied from global into its tile before scoring.
+template <int HD, int G>
+__device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_pool) {
+  constexpr int DPL = HD / 32, W2 = HD / 2;
+  const StepArgs& A = *c.A;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n = c.pos + 1;
+  int kvh, tb, te;
+  attn_task(A, n, kvh, tb, te);
+  const bool has_task = (int)blockIdx.x < A.n_kv * A.S;
+  const int sp = blockIdx.x % A.S;
+  const float scale = 1.0f / sqrtf((float)HD);
+  if (has_task) {
+    const float* qrow = A.q + (size_t)kvh * G * HD;
+    for (int i = tid; i < G * HD; i += NWC * 32) c.s_q[i] = __ldcg(qrow + i) * scale;
+  }
+  named_bar(1, NWC * 32);
+  float m_run[G], l_run[G], o[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
+  }
+  const int pg = c.pos / A.page_tokens;
+  const int pos_page = A.page_table[(size_t)c.seq * A.max_pages + pg];
+  for (int j = 0; j < te - tb; ++j) {
+    const int slot = c.sidx % A.ns;
+    if ((j % NWC) == warp) {
+      const int t = tb + j;
+      const int nt = min(kTile, n - t * kTile);
+      const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), (c.sidx / A.ns) & 1, 20);
+      __half* kt = reinterpret_cast<__half*>(c.ring + (size_t)slot * A.stage_bytes);
+      __half* vt = kt + kTile * HD;
+      const int jp = c.pos - t * kTile;  // the new position inside this tile, if any
+      if (jp >= 0 && jp < kTile && pos_page >= 0) {
+        const size_t off = (((size_t)pos_page * A.n_kv + kvh) * A.page_tokens + (c.pos % A.page_tokens)) * HD;
+        for (int i = lane; i < HD / 2; i += 32) {
+          reinterpret_cast<__half2*>(kt + jp * HD)[i] = __ldcg(reinterpret_cast<const __half2*>(k_pool + off) + i);
+          reinterpret_cast<__half2*>(vt + jp * HD)[i] = __ldcg(reinterpret_cast<const __half2*>(v_pool + off) + i);
+        }
+        __syncwarp();
+      }
+      if (ok) {
+        float sc[G];
+        {
+          float2 acc[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+          const __half2* krow = reinterpret_cast<const __half2*>(kt + lane * HD);
+          const float2* q2 = reinterpret_cast<const float2*>(c.s_q);
+#pragma unroll 4
+          for (int w2 = 0; w2 < W2; ++w2) {
+            const int wi = (w2 + lane) & (W2 - 1);
+            const float2 kf = __half22float2(krow[wi]);
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h]);
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) sc[h] = lane < nt ? acc[h].x + acc[h].y : -INFINITY;
+        }
+        float p[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float m_new = fmaxf(m_run[h], warp_max_f(sc[h]));
+          p[h] = lane < nt ? expf(sc[h] - m_new) : 0.f;
+          const float al = expf(m_run[h] - m_new);
+          l_run[h] = l_run[h] * al + warp_sum(p[h]);
+          m_run[h] = m_new;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) o[h][e] *= al;
+        }
+        const __half* vl = vt + lane * DPL;
+        for (int jj = 0; jj < nt; ++jj) {
+          float vf[DPL];
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) vf[e] = __half2float(vl[jj * HD + e]);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float pj = __shfl_sync(0xffffffffu, p[h], jj);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pj, vf[e], o[h][e]);
+          }
+        }
+      }
+      // generic writes into the slot above must be ordered before the next
+      // bulk copy into it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+    if (lane == 0) mbar_arrive(smem_u32(&c.sh->empty[slot]));
+    ++c.sidx;
+  }
+  // merge the warps of this CTA
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      c.s_wm[warp * G + h] = m_run[h];
+      c.s_wl[warp * G + h] = l_run[h];
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) c.s_wo[(warp * G + h) * HD + lane * DPL + e] = o[h][e];
+  named_bar(1, NWC * 32);
+  if (has_task) {
+    const size_t slot = (size_t)kvh * A.S + sp;
+    for (int idx = tid; idx < G * HD; idx += NWC * 32) {
+      const int h = idx / HD;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NWC; ++w) M = fmaxf(M, c.s_wm[w * G + h]);
+      float acc = 0.f, L = 0.f;
+#pragma unroll
+      for (int w = 0; w < NWC; ++w) {
+        const float ew = c.s_wl[w * G + h] > 0.f ? expf(c.s_wm[w * G + h] - M) : 0.f;
+        acc = fmaf(ew, c.s_wo[(w * G) * HD + idx], acc);
+        L = fmaf(ew, c.s_wl[w * G + h], L);
+      }
+      A.part_o[slot * G * HD + idx] = acc;
+      if ((idx % HD) == 0) reinterpret_cast<float2*>(A.part_ml)[slot * G + h] = make_float2(M, L);
+    }
+    __threadfence();
+  }
+  named_bar(1, NWC * 32);
+  if (tid == 0) c.sh->last = has_task ? (atomicAdd(&A.att_counters[kvh], 1) == A.S - 1) : 0;
+  named_bar(1, NWC * 32);
+  if (c.sh->last) {
+    __threadfence();
+    // merge the S splits of this KV head, in split order
+    const size_t slot0 = (size_t)kvh * A.S;
+    const float2* ml = reinterpret_cast<const float2*>(A.part_ml);
+    for (int idx = tid; idx < G * HD; idx += NWC * 32) {
+      const int h = idx / HD;
+      float M = -INFINITY;
+      for (int s = 0; s < A.S; ++s) M = fmaxf(M, __ldcg(&ml[(slot0 + s) * G + h]).x);
+      float num = 0.f, den = 0.f;
+      for (int s = 0; s < A.S; ++s) {
+        const float2 v = __ldcg(&ml[(slot0 + s) * G + h]);
+        if (v.y == 0.f) continue;
+        const float ew = expf(v.x - M);
+        den = fmaf(v.y, ew, den);
+        num = fmaf(__ldcg(&A.part_o[(slot0 + s) * G * HD + idx]), ew, num);
+      }
+      A.o[(size_t)kvh * G * HD + idx] = num / den;
+    }
+    if (tid == 0) A.att_counters[kvh] = 0;
+  }
+}
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+template <int WT, int HD, int G, int RSA, int MCA, int RSB, int MCB>
+__global__ void __launch_bounds__(NTHR, 1) step_kernel(const StepArgs A) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  Ctx c;
+  c.A = &A;
+  c.sh = reinterpret_cast<Sh*>(smem);
+  size_t off = (sizeof(Sh) + 127) & ~(size_t)127;
+  c.s_part = reinterpret_cast<float*>(smem + off);
+  off += NWC * kRB * 4;
+  c.s_q = reinterpret_cast<float*>(smem + off);
+  off += G * HD * 4;
+  c.s_wm = reinterpret_cast<float*>(smem + off);
+  off += NWC * G * 4;
+  c.s_wl = reinterpret_cast<float*>(smem + off);
+  off += NWC * G * 4;
+  c.s_wo = reinterpret_cast<float*>(smem + off);
+  off += NWC * G * HD * 4;
+  c.ring = smem + ((off + 127) & ~(size_t)127);
+  c.sidx = 0;
+  c.epoch = 0;
+  c.pos = A.sp->pos[0];
+  c.seq = A.sp->seq[0];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < A.ns; ++s) {
+      mbar_init(smem_u32(&c.sh->full[s]), 1);
+      mbar_init(smem_u32(&c.sh->empty[s]), NWC);
+    }
+    mbar_fence_init();
+    if (A.trace && blockIdx.x == 0) A.trace[0] = global_ns();
+  }
+  __syncthreads();
+
+  if (warp == NWC) {
+    // ---------------- producer: every phase's stages, in consumer order
+    if (lane == 0) {
+      int issued = 0;
+      for (int l = 0; l < A.n_layers && !aborted(A); ++l) {
+        const StepLayer& L = A.layers[l];
+        produce_gemv<WT, RSA>(c, L.qkv, 2, issued);
+        produce_attention<HD>(c, L.k_pool, L.v_pool, issued);
+        produce_gemv<WT, RSA>(c, L.o, 1, issued);
+        produce_gemv<WT, RSA>(c, L.gu, 2, issued);
+        produce_gemv<WT, RSB>(c, L.down, 1, issued);
+      }
+      if (!aborted(A) && A.head_rows) produce_gemv<WT, RSA>(c, A.head, 1, issued);
+      // never leave with copies in flight
+      for (int s = max(0, c.sidx - A.ns); s < c.sidx; ++s) {
+        const uint32_t bar = smem_u32(&c.sh->full[s % A.ns]);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(bar, (s / A.ns) & 1) && global_ns() - t0 < kWaitNs) __nanosleep(100);
+      }
+    }
+  } else {
+    // ---------------- consumers
+    // embedding row -> x (rows split like the residual epilogues)
+    {
+      int tok = A.sp->token[0];
+      if (tok < 0 || tok >= A.vocab) {
+        if (tid == 0) atomicOr(&A.sp->status, kBadToken);
+        tok = 0;
+      }
+      int r0, r1;
+      row_split(A.H, 1, r0, r1);
+      const MatDev& E = A.emb;
+      for (int col = r0 + tid; col < r1; col += NWC * 32) {
+        const int blk = col >> 5, e = col & 31;
+        const float d = __half2float(E.d[(size_t)tok * E.ds + blk]);
+        float q;
+        if (WT == 8) {
+          q = mag_byte((uint32_t)E.qs[(size_t)tok * E.nb * 32 + col] ^ 0x80u, 0) - 8388736.0f;
+        } else {
+          const uint8_t byte = E.qs[((size_t)tok * E.nb + blk) * 16 + (e & 15)];
+          q = mag_byte(e < 16 ? (byte & 15u) : (byte >> 4), 0) - 8388616.0f;
+        }
+        A.x[col] = d * q;
+      }
+    }
+    grid_sync(c);
+    for (int l = 0; l < A.n_layers; ++l) {
+      const StepLayer& L = A.layers[l];
+      EpiArgs e{};
+      e.y = A.q;
+      e.k_pool = L.k_pool;
+      e.v_pool = L.v_pool;
+      consume_gemv<WT, PRO_RMSNORM, EPI_QKV, RSA, MCA>(c, L.qkv, 2, A.x, L.attn_norm, e);
+      grid_sync(c);
+      consume_attention<HD, G>(c, L.k_pool, L.v_pool);
+      grid_sync(c);
+      e.y = A.x;
+      consume_gemv<WT, PRO_COPY, EPI_RESID, RSA, MCA>(c, L.o, 1, A.o, nullptr, e);
+      grid_sync(c);
+      e.y = A.h;
+      consume_gemv<WT, PRO_RMSNORM, EPI_SWIGLU, RSA, MCA>(c, L.gu, 2, A.x, L.ffn_norm, e);
+      grid_sync(c);
+      e.y = A.x;
+      consume_gemv<WT, PRO_COPY, EPI_RESID, RSB, MCB>(c, L.down, 1, A.h, nullptr, e);
+      grid_sync(c);
+    }
+    EpiArgs e{};
+    e.y = A.logits;
+    if (A.head_rows) consume_gemv<WT, PRO_RMSNORM, EPI_STORE, RSA, MCA>(c, A.head, 1, A.x, A.out_norm, e);
+    if (A.head_rows && A.greedy) {
+      grid_sync(c);
+      // greedy pick: each CTA reduces a slice of the logits, CTA 0 the slices
+      int r0, r1;
+      row_split(A.vocab, 1, r0, r1);
+      float best = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int i = r0 + tid; i < r1; i += NWC * 32) {
+        const float v = __ldcg(A.logits + i);
+        if (better(v, i, best, bi)) {
+          best = v;
+          bi = i;
+        }
+      }
+      for (int o2 = 16; o2 > 0; o2 >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o2);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o2);
+        if (better(ov, oi, best, bi)) {
+          best = ov;
+          bi = oi;
+        }
+      }
+      if (lane == 0) {
+        c.s_wm[warp] = best;
+        reinterpret_cast<int*>(c.s_wl)[warp] = bi;
+      }
+      named_bar(1, NWC * 32);
+      if (tid == 0) {
+        for (int w = 1; w < NWC; ++w)
+          if (better(c.s_wm[w], reinterpret_cast<int*>(c.s_wl)[w], best, bi)) {
+            best = c.s_wm[w];
+            bi = reinterpret_cast<int*>(c.s_wl)[w];
+          }
+        A.am_part[blockIdx.x] = make_int2(__float_as_int(best), bi);
+      }
+      grid_sync(c);
+      if (blockIdx.x == 0 && tid == 0) {
+        best = -INFINITY;
+        bi = 0x7fffffff;
+        for (int b = 0; b < (int)gridDim.x; ++b) {
+          const int2 p2 = __ldcg(&A.am_part[b]);
+          if (better(__int_as_float(p2.x), p2.y, best, bi)) {
+            best = __int_as_float(p2.x);
+            bi = p2.y;
+          }
+        }
+        const int tok = bi == 0x7fffffff ? 0 : bi;
+        const int step = A.sp->step;
+        if (A.tokens_out) A.tokens_out[step] = tok;
+        A.sp->token[0] = tok;
+        A.sp->pos[0] = c.pos + 1;
+        A.sp->step = step + 1;
+      }
+    }
+    if (A.trace && blockIdx.x == 0 && tid == 0) A.trace[c.epoch + 1] = global_ns();
+  }
+  __syncthreads();
+}
+
+template <int WT, int HD, int G, int RSA, int MCA, int RSB, int MCB>
+const void* step_fn() {
+  return reinterpret_cast<const void*>(&step_kernel<WT, HD, G, RSA, MCA, RSB, MCB>);
+}
+
+struct Variant {
+  int wt, hd, g, rsa, mca, rsb, mcb;
+  const void* (*fn)();
+};
+
+// The shapes with a persistent-kernel instantiation (others use the
+// multi-kernel step).
+const Variant kVariants[] = {
+    {8, 128, 4, 4, 1, 1, 4, &step_fn<8, 128, 4, 4, 1, 1, 4>},  // 8B-shape Q8_0
+    {4, 128, 4, 8, 1, 2, 2, &step_fn<4, 128, 4, 8, 1, 2, 2>},  // 8B-shape Q4_0
+    {8, 64, 4, 8, 1, 2, 2, &step_fn<8, 64, 4, 8, 1, 2, 2>},    // 1B-shape Q8_0
+    {8, 64, 2, 8, 1, 8, 1, &step_fn<8, 64, 2, 8, 1, 8, 1>},    // tiny Q8_0
+    {4, 64, 2, 8, 1, 8, 1, &step_fn<4, 64, 2, 8, 1, 8, 1>},    // tiny Q4_0
+    {4, 128, 8, 4, 1, 1, 4, &step_fn<4, 128, 8, 4, 1, 1, 4>},  // 70B-shape Q4_0
+};
+
+int pow2_rows(int row_bytes) {
+  int rs = 1;
+  while (rs < 8 && (rs * 2) * row_bytes <= 16384) rs *= 2;
+  return rs;
+}
+
+}  // namespace
+
+StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, int hd, int num_sms) {
+  StepPlan p{};
+  p.fn = nullptr;
+  if (q_rows != H) return p;  // O projection must share the hidden-size geometry
+  const int G = n_heads / n_kv;
+  const int nb_h = (H + 31) / 32, nb_f = (F + 31) / 32;
+  const int rb_h = wtype == 8 ? nb_h * 32 : nb_h * 16, rb_f = wtype == 8 ? nb_f * 32 : nb_f * 16;
+  const int CH = wtype == 8 ? 512 : 1024;
+  const int rsa = pow2_rows(rb_h), rsb = pow2_rows(rb_f);
+  const int mca = ((nb_h * 32 + CH - 1) / CH + NWC - 1) / NWC;
+  const int mcb = ((nb_f * 32 + CH - 1) / CH + NWC - 1) / NWC;
+  for (const Variant& v : kVariants)
+    if (v.wt == wtype && v.hd == hd && v.g == G && v.rsa == rsa && v.mca == mca && v.rsb == rsb && v.mcb == mcb) {
+      p.fn = v.fn();
+      break;
+    }
+  if (!p.fn) return p;
+  const int ds_h = (nb_h + 7) & ~7, ds_f = (nb_f + 7) & ~7;
+  size_t stage = std::max((size_t)rsa * (rb_h + ds_h * 2), (size_t)rsb * (rb_f + ds_f * 2));
+  stage = std::max(stage, (size_t)2 * kTile * hd * 2);
+  stage = (stage + 127) & ~(size_t)127;
+  size_t head = ((sizeof(Sh) + 127) & ~(size_t)127) + NWC * kRB * 4 + G * hd * 4 + 2 * NWC * G * 4 + NWC * G * hd * 4;
+  head = (head + 127) & ~(size_t)127;
+  const size_t budget = 220 * 1024;
+  int ns = (int)((budget - head) / stage);
+  ns = std::min(ns, kMaxStages);
+  if (ns < 2) {
+    p.fn = nullptr;
+    return p;
+  }
+  p.ns = ns;
+  p.stage_bytes = (uint32_t)stage;
+  p.smem = (int)(head + ns * stage);
+  p.grid = num_sms;
+  p.threads = NTHR;
+  p.splits = num_sms / n_kv;
+  if (p.splits < 1) {
+    p.fn = nullptr;
+    return p;
+  }
+  if (cudaFuncSetAttribute(p.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem) != cudaSuccess) {
+    cudaGetLastError();
+    p.fn = nullptr;
+    return p;
+  }
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p.fn, p.threads, p.smem) != cudaSuccess || occ < 1) {
+    cudaGetLastError();
+    p.fn = nullptr;
+  }
+  return p;
+}
+
+cudaError_t launch_step(const StepPlan& p, const StepArgs& a, cudaStream_t s) {
+  if (!p.fn) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident: the grid barriers rely on it
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {const_cast<StepArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, p.fn, args);
+}
+
+}  // namespace dls
