@@ -32,7 +32,7 @@ enum StatusBits : int32_t {
 // One weight matrix in the kernels' layout: codes and fp16 scales in two
 // arrays ("structure of arrays"), so rows of codes are contiguous, 16-byte
 // aligned and can be moved by bulk copies.
-//   Q8_0: qs int8 [rows][nb*32]                             d fp16 [rows][ds]
+//   Q8_0: qs u8 [rows][nb*32] holding q + 128                d fp16 [rows][ds]
 //   Q4_0: qs u8   [rows][nb][16] (GGUF nibble order kept)   d fp16 [rows][ds]
 struct MatDev {
   const uint8_t* qs;
@@ -98,12 +98,24 @@ __device__ __forceinline__ float mag_byte(uint32_t u, int k) {
   return __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540 | k));
 }
 
-// four int8 codes (one 32-bit word) -> two pairs (q0,q1), (q2,q3)
-__device__ __forceinline__ void i8x4_to_f2(uint32_t w, float2& p01, float2& p23) {
-  const uint32_t u = w ^ 0x80808080u;  // q + 128 as unsigned bytes
+// four biased Q8_0 codes (q + 128 per byte, one 32-bit word) -> (q0,q1), (q2,q3)
+__device__ __forceinline__ void i8x4_to_f2(uint32_t u, float2& p01, float2& p23) {
   const float2 bias = make_float2(-8388736.0f, -8388736.0f);
   p01 = __fadd2_rn(make_float2(mag_byte(u, 0), mag_byte(u, 1)), bias);
   p23 = __fadd2_rn(make_float2(mag_byte(u, 2), mag_byte(u, 3)), bias);
+}
+
+// two-way integer dot: c + a.lo16*b.byte(0|2) + a.hi16*b.byte(1|3), a signed
+// 16-bit pair, b unsigned bytes; exact in int32
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
 // four nibble codes already isolated one per byte (values 0..15) -> (n-8)
@@ -167,6 +179,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// shared-memory loads by 32-bit shared address
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_half_as_float(uint32_t a) {
+  uint16_t h;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+  return __half2float(__ushort_as_half(h));
+}
+
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

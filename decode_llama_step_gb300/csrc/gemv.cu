@@ -24,6 +24,8 @@
 //    (q, k) pairs plus the fp16 K/V append into the cache, or SwiGLU on
 //    interleaved (gate, up) row pairs (engine page, section 4.4: SwiGLU
 //    fused with the projection), which feeds the down projection directly.
+#include <stdlib.h>
+
 #include "gemv_core.cuh"
 #include "kernels.h"
 
@@ -35,6 +37,7 @@ constexpr int kMaxConsumers = 14;
 constexpr int kRB = 64;              // rows per epilogue block
 constexpr int kStageCodes = 16384;   // target code bytes per ring stage
 constexpr int kRingBytes = 64 * 1024;
+constexpr int kRingBytesSmall = 44 * 1024;  // ring when more than two CTAs share an SM
 
 struct Shared {
   uint64_t full[16];
@@ -175,14 +178,9 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
         }
       }
     }
-    float2 xr[MC][G::XV];
+    XQ<WT> xq[MC];
 #pragma unroll
-    for (int k = 0; k < MC; ++k)
-#pragma unroll
-      for (int m4 = 0; m4 < V4; ++m4) {
-        xr[k][2 * m4] = make_float2(raw[k][m4].x, raw[k][m4].y);
-        xr[k][2 * m4 + 1] = make_float2(raw[k][m4].z, raw[k][m4].w);
-      }
+    for (int k = 0; k < MC; ++k) quantize_slice<WT>(reinterpret_cast<const float*>(raw[k]), xq[k]);
 
     int32_t pos = 0, seq = 0;
     if (EPI == EPI_QKV) {
@@ -198,24 +196,26 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
       }
       if (s == nst - 1) griddep_launch();  // last stage arrived: let the next kernel start
       const int rows_s = min(RS, nrows - s * RS);
-      const uint8_t* st = ring + (size_t)slot * stage_bytes;
+      const uint32_t st = smem_u32(ring) + (uint32_t)slot * stage_bytes;
       float acc[RS];
 #pragma unroll
       for (int rr = 0; rr < RS; ++rr) acc[rr] = 0.f;
       if (!sh.abort) {
+        // branch-free: every row slot is computed (rows past rows_s read
+        // stale stage bytes and are discarded), invalid lanes read offset 0
+        // and contribute exactly 0 through a select
 #pragma unroll
         for (int k = 0; k < MC; ++k) {
-          if (!valid[k]) continue;
           const int c = warp + k * nwc;
-          const int qoff = WT == 8 ? c * 512 + lane * 16 : (c * 32 + lane) * 16;
-          const int blk = WT == 8 ? (c * 512 + lane * 16) >> 5 : c * 32 + lane;
+          const int qoff = valid[k] ? (WT == 8 ? c * 512 + lane * 16 : (c * 32 + lane) * 16) : 0;
+          const int blk = valid[k] ? (WT == 8 ? (c * 512 + lane * 16) >> 5 : c * 32 + lane) : 0;
+          const uint32_t qa = st + (uint32_t)qoff, da = st + stage_q + (uint32_t)blk * 2;
 #pragma unroll
           for (int rr = 0; rr < RS; ++rr) {
-            if (rr < rows_s) {
-              const uint4 q = *reinterpret_cast<const uint4*>(st + rr * row_bytes + qoff);
-              const __half d = *reinterpret_cast<const __half*>(st + stage_q + rr * drow_bytes + blk * 2);
-              acc[rr] = fmaf(__half2float(d), dot16<WT>(q, xr[k]), acc[rr]);
-            }
+            const uint4 q = lds128(qa + rr * (uint32_t)row_bytes);
+            const float d = lds_half_as_float(da + rr * (uint32_t)drow_bytes);
+            const float t = (float)idot16<WT>(q, xq[k]);
+            acc[rr] = valid[k] ? fmaf(d * xq[k].s, t, acc[rr]) : acc[rr];
           }
         }
       }
@@ -357,7 +357,9 @@ GemvLaunch gemv_plan(int wtype, int pro, int epi, int rows, int nb, int num_sms,
   int rs = 1;
   while (rs < 8 && (rs * 2) * row_bytes <= kStageCodes) rs *= 2;
   const int stage = rs * row_bytes + rs * ds * 2;
-  int ns = kRingBytes / stage;
+  const char* cps_env = getenv("DLS_GEMV_CTAS");
+  const int cps_max = cps_env ? std::max(1, std::min(4, atoi(cps_env))) : 2;
+  int ns = (cps_max > 2 ? kRingBytesSmall : kRingBytes) / stage;
   ns = std::max(2, std::min(16, ns));
   GemvLaunch l;
   l.threads = (nwc + 1) * 32;
@@ -375,7 +377,7 @@ GemvLaunch gemv_plan(int wtype, int pro, int epi, int rows, int nb, int num_sms,
     cudaGetLastError();
     occ = 1;
   }
-  occ = std::max(1, std::min(2, occ));
+  occ = std::max(1, std::min(cps_max, occ));
   const int units = (rows + unit - 1) / unit;
   int grid = std::min(num_sms * occ, units);
   if (grid < 1) grid = 1;

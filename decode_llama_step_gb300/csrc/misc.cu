@@ -28,7 +28,7 @@ __device__ __forceinline__ float dq(const MatDev& m, int wtype, int row, int col
   row *= m.rstep;
   const float d = __half2float(m.d[(size_t)row * m.ds + blk]);
   if (wtype == 8) {
-    const uint32_t u = (uint32_t)m.qs[(size_t)row * m.nb * 32 + col] ^ 0x80u;
+    const uint32_t u = (uint32_t)m.qs[(size_t)row * m.nb * 32 + col];  // stored biased: q + 128
     return d * (mag_byte(u, 0) - 8388736.0f);
   }
   const uint8_t byte = m.qs[((size_t)row * m.nb + blk) * 16 + (e & 15)];
@@ -56,7 +56,7 @@ __global__ void embed_kernel(const MatDev emb, int wtype, StepParams* sp, int br
       const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint32_t u = w[k] ^ 0x80808080u;
+        const uint32_t u = w[k];  // stored biased: q + 128
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[4 * k + e] = mag_byte(u, e) - 8388736.0f;
       }
@@ -193,7 +193,10 @@ __global__ void repack_kernel(const uint8_t* src, int wtype, long long n_blocks,
     const long long r = (b / nb) * row_step, j = b % nb;
     d[r * ds + j] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
     uint8_t* q = qs + (r * nb + j) * nq;
-    for (int i = 0; i < nq; ++i) q[i] = s[2 + i];
+    // Q8_0 codes are stored biased (q + 128, as unsigned bytes) so the
+    // kernels' exact byte -> float conversion needs no per-word XOR
+    const uint8_t bias = wtype == 8 ? 0x80 : 0x00;
+    for (int i = 0; i < nq; ++i) q[i] = s[2 + i] ^ bias;
   }
 }
 

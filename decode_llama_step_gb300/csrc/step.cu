@@ -194,7 +194,7 @@ __device__ void produce_attention(Ctx& c, const __half* k_pool, const __half* v_
 // The lane's activation slice (chunks warp, warp+NWC, ...), from L2.
 template <int WT, int PRO, int MC>
 __device__ __forceinline__ void load_x(Ctx& c, const MatDev& w, const float* x, const float* gain,
-                                       float2 (&xr)[MC][Geo<WT>::XV], bool (&valid)[MC]) {
+                                       XQ<WT> (&xq)[MC], bool (&valid)[MC]) {
   using Gm = Geo<WT>;
   constexpr int V4 = Gm::XV / 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -264,12 +264,7 @@ __device__ __forceinline__ void load_x(Ctx& c, const MatDev& w, const float* x, 
     }
   }
 #pragma unroll
-  for (int k = 0; k < MC; ++k)
-#pragma unroll
-    for (int m4 = 0; m4 < V4; ++m4) {
-      xr[k][2 * m4] = make_float2(raw[k][m4].x, raw[k][m4].y);
-      xr[k][2 * m4 + 1] = make_float2(raw[k][m4].z, raw[k][m4].w);
-    }
+  for (int k = 0; k < MC; ++k) quantize_slice<WT>(reinterpret_cast<const float*>(raw[k]), xq[k]);
 }
 
 struct EpiArgs {
@@ -284,9 +279,9 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
   using Gm = Geo<WT>;
   const StepArgs& A = *c.A;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float2 xr[MC][Gm::XV];
+  XQ<WT> xq[MC];
   bool valid[MC];
-  load_x<WT, PRO, MC>(c, w, x, gain, xr, valid);
+  load_x<WT, PRO, MC>(c, w, x, gain, xq, valid);
   int r0, r1;
   row_split(w.rows, unit, r0, r1);
   const int nrows = max(r1 - r0, 0);
@@ -300,24 +295,24 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
     const int slot = c.sidx % A.ns;
     const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), (c.sidx / A.ns) & 1, 20);
     const int rows_s = min(RS, nrows - s * RS);
-    const uint8_t* st = c.ring + (size_t)slot * A.stage_bytes;
+    const uint32_t st = smem_u32(c.ring) + (uint32_t)slot * A.stage_bytes;
     float acc[RS];
 #pragma unroll
     for (int rr = 0; rr < RS; ++rr) acc[rr] = 0.f;
     if (ok) {
+      // branch-free: see the standalone GEMV
 #pragma unroll
       for (int k = 0; k < MC; ++k) {
-        if (!valid[k]) continue;
         const int ch = warp + k * NWC;
-        const int qoff = WT == 8 ? ch * 512 + lane * 16 : (ch * 32 + lane) * 16;
-        const int blk = WT == 8 ? (ch * 512 + lane * 16) >> 5 : ch * 32 + lane;
+        const int qoff = valid[k] ? (WT == 8 ? ch * 512 + lane * 16 : (ch * 32 + lane) * 16) : 0;
+        const int blk = valid[k] ? (WT == 8 ? (ch * 512 + lane * 16) >> 5 : ch * 32 + lane) : 0;
+        const uint32_t qa = st + (uint32_t)qoff, da = st + (uint32_t)(RS * rb) + (uint32_t)blk * 2;
 #pragma unroll
         for (int rr = 0; rr < RS; ++rr) {
-          if (rr < rows_s) {
-            const uint4 q = *reinterpret_cast<const uint4*>(st + rr * rb + qoff);
-            const __half d = *reinterpret_cast<const __half*>(st + RS * rb + rr * db + blk * 2);
-            acc[rr] = fmaf(__half2float(d), dot16<WT>(q, xr[k]), acc[rr]);
-          }
+          const uint4 q = lds128(qa + rr * (uint32_t)rb);
+          const float d = lds_half_as_float(da + rr * (uint32_t)db);
+          const float t = (float)idot16<WT>(q, xq[k]);
+          acc[rr] = valid[k] ? fmaf(d * xq[k].s, t, acc[rr]) : acc[rr];
         }
       }
     }
@@ -622,7 +617,7 @@ __global__ void __launch_bounds__(NTHR, 1) step_kernel(const StepArgs A) {
         const float d = __half2float(E.d[(size_t)tok * E.ds + blk]);
         float q;
         if (WT == 8) {
-          q = mag_byte((uint32_t)E.qs[(size_t)tok * E.nb * 32 + col] ^ 0x80u, 0) - 8388736.0f;
+          q = mag_byte((uint32_t)E.qs[(size_t)tok * E.nb * 32 + col], 0) - 8388736.0f;  // stored q + 128
         } else {
           const uint8_t byte = E.qs[((size_t)tok * E.nb + blk) * 16 + (e & 15)];
           q = mag_byte(e < 16 ? (byte & 15u) : (byte >> 4), 0) - 8388616.0f;
