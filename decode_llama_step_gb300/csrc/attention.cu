@@ -23,7 +23,7 @@ namespace dls {
 namespace {
 
 constexpr int TILE = 32;   // tokens per tile: one lane per token when scoring
-constexpr int NW = 4;      // warps per CTA
+constexpr int NW = 8;      // warps per CTA
 constexpr int NT = 32 * NW;
 constexpr int kMaxG = 16;
 constexpr int kMaxSplits = 128;
@@ -35,24 +35,29 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // CTA (kv head, split sp) covers a contiguous run of 32-token tiles of one
-// sequence; warp w takes tiles w, w + 4, ... of that run.  Per tile a warp
-// bulk-copies K and V into its own shared-memory stage, scores the tile with
-// one lane per token (the head dimension walked from a lane-dependent start
-// so the 32 lanes read 32 different banks), updates its online softmax for
-// the G query heads of the group in registers, and accumulates P V with each
-// lane owning HD/32 output dimensions.  The 4 warps then merge in shared
-// memory into one (m, l, o) partial per CTA; the last CTA of a (row, kv
-// head) merges the S partials in split order.
+// sequence.  Its 8 warps form TS tile slots x HG head groups: warp w works
+// on tiles slot, slot + TS, ... (slot = w % TS) for the query heads of group
+// w / TS, so two warps share each tile when the group has 2+ heads.  Per
+// tile: one bulk copy brings K and V into the slot's shared-memory stage;
+// each warp scores the tile with one lane per token (the head dimension
+// walked from a lane-dependent start so the 32 lanes read 32 different
+// banks), keeps its heads' online softmax in registers, and accumulates P V
+// with each lane owning HD/32 output dimensions.  The warps then merge in
+// shared memory into one (m, l, o) partial per CTA; the last CTA of a
+// (row, kv head) merges the S partials in split order.
 template <int HD, int G>
 __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
+  constexpr int HG = G >= 2 ? 2 : 1;        // head groups
+  constexpr int TS = NW / HG;               // tile slots
+  constexpr int HPW = G / HG;               // heads per warp
   constexpr int DPL = HD / 32;              // output dims per lane
   constexpr int W2 = HD / 2;                // 2-element words per row
-  constexpr int STAGE = 2 * TILE * HD;      // halves per warp stage (K then V)
+  constexpr int STAGE = 2 * TILE * HD;      // halves per slot stage (K then V)
   extern __shared__ __align__(128) uint8_t s_dyn[];
-  __half* s_stage = reinterpret_cast<__half*>(s_dyn);          // [NW][STAGE]
+  __half* s_stage = reinterpret_cast<__half*>(s_dyn);          // [TS][STAGE]
   __shared__ __align__(16) float s_q[G * HD];
-  __shared__ float s_wm[NW][G], s_wl[NW][G];
-  __shared__ __align__(8) uint64_t s_full[NW];
+  __shared__ float s_wm[NW][HPW], s_wl[NW][HPW];
+  __shared__ __align__(8) uint64_t s_full[TS];
   __shared__ float s_w[G][kMaxSplits];
   __shared__ int s_last;
 
@@ -60,9 +65,10 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   const int kvh = blockIdx.x / S, sp = blockIdx.x - kvh * S;
   const int brel = blockIdx.y, b = a.row0 + brel;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slot = warp % TS, hg = warp / TS;
   const int pt = a.page_tokens;
 
-  if (lane == 0) mbar_init(smem_u32(&s_full[warp]), 1);
+  if (tid < TS) mbar_init(smem_u32(&s_full[tid]), 1);
   mbar_fence_init();
   griddep_wait();
 
@@ -77,9 +83,9 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   const int per = (n_tiles + S - 1) / S;
   const int tb = sp * per, te = min(n_tiles, tb + per);
 
-  // lane 0 of a warp copies tile i (K then V) into the warp's stage
-  __half* st = s_stage + (size_t)warp * STAGE;
-  const uint32_t bar = smem_u32(&s_full[warp]);
+  // the first warp of a slot copies tile i (K then V) into the slot's stage
+  __half* st = s_stage + (size_t)slot * STAGE;
+  const uint32_t bar = smem_u32(&s_full[slot]);
   auto issue = [&](int i) -> bool {
     const int t = i * TILE;
     const int nt = min(TILE, n - t);
@@ -95,8 +101,8 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
     bulk_g2s(smem_u32(st + TILE * HD), a.v_pool + base, bytes, bar);
     return true;
   };
-  __syncwarp();
-  if (lane == 0 && tb + warp < te && !issue(tb + warp) && a.status) atomicOr(a.status, kBadPage);
+  __syncthreads();  // barriers initialised
+  if (hg == 0 && lane == 0 && tb + slot < te && !issue(tb + slot) && a.status) atomicOr(a.status, kBadPage);
 
   const float scale = 1.0f / sqrtf((float)HD);
   const float* qrow = a.q + ((size_t)brel * a.n_heads + (size_t)kvh * G) * HD;
@@ -104,41 +110,41 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   __syncthreads();
   griddep_launch();
 
-  float m_run[G], l_run[G], o[G][DPL];
+  float m_run[HPW], l_run[HPW], o[HPW][DPL];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+  for (int h = 0; h < HPW; ++h) {
     m_run[h] = -INFINITY;
     l_run[h] = 0.f;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
   }
+  const float2* q2 = reinterpret_cast<const float2*>(s_q) + (size_t)hg * HPW * W2;
   bool failed = false;
   int use = 0;
-  for (int i = tb + warp; i < te; i += NW, ++use) {
+  for (int i = tb + slot; i < te; i += TS, ++use) {
     const int nt = min(TILE, n - i * TILE);
     if (!mbar_wait(bar, use & 1)) failed = true;
     // ---- scores, lane = token
-    float sc[G];
+    float sc[HPW];
     {
-      float2 acc[G];
+      float2 acc[HPW];
 #pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+      for (int h = 0; h < HPW; ++h) acc[h] = make_float2(0.f, 0.f);
       const __half2* krow = reinterpret_cast<const __half2*>(st + lane * HD);
-      const float2* q2 = reinterpret_cast<const float2*>(s_q);
 #pragma unroll 4
       for (int w2 = 0; w2 < W2; ++w2) {
         const int wi = (w2 + lane) & (W2 - 1);
         const float2 kf = __half22float2(krow[wi]);
 #pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h]);
+        for (int h = 0; h < HPW; ++h) acc[h] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h]);
       }
 #pragma unroll
-      for (int h = 0; h < G; ++h) sc[h] = lane < nt ? acc[h].x + acc[h].y : -INFINITY;
+      for (int h = 0; h < HPW; ++h) sc[h] = lane < nt ? acc[h].x + acc[h].y : -INFINITY;
     }
     // ---- online softmax (per head, in registers)
-    float p[G];
+    float p[HPW];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < HPW; ++h) {
       const float m_new = fmaxf(m_run[h], warp_max(sc[h]));
       p[h] = lane < nt ? expf(sc[h] - m_new) : 0.f;
       const float al = expf(m_run[h] - m_new);  // 0 on the warp's first tile
@@ -164,49 +170,51 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
         for (int e = 0; e < DPL; ++e) vf[e] = __half2float(vt[j * HD + e]);
       }
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
+      for (int h = 0; h < HPW; ++h) {
         const float pj = __shfl_sync(0xffffffffu, p[h], j);
 #pragma unroll
         for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pj, vf[e], o[h][e]);
       }
     }
-    __syncwarp();  // the stage is free again
-    if (lane == 0 && i + NW < te && !issue(i + NW) && a.status) atomicOr(a.status, kBadPage);
+    // both warps of the slot are done with the stage before it is refilled
+    if (HG > 1) named_bar(1 + slot, 32 * HG);
+    else __syncwarp();
+    if (hg == 0 && lane == 0 && i + TS < te && !issue(i + TS) && a.status) atomicOr(a.status, kBadPage);
   }
   if (failed && a.status) atomicOr(a.status, kTimeout);
 
-  // ---- merge the 4 warps of this CTA; the per-warp outputs reuse the
-  // (now idle) K/V stage memory: NW*G*HD floats <= NW*2*TILE*HD halves
+  // ---- merge the warps of this CTA; per-warp outputs reuse the (now idle)
+  // stage memory: NW*HPW*HD floats <= TS*2*TILE*HD halves
   __syncthreads();
-  float(*s_wo)[G * HD] = reinterpret_cast<float(*)[G * HD]>(s_dyn);
-  static_assert(NW * G * HD * 4 <= NW * 2 * TILE * HD * 2, "merge buffer must fit the stages");
+  float(*s_wo)[HPW * HD] = reinterpret_cast<float(*)[HPW * HD]>(s_dyn);
+  static_assert(NW * HPW * HD * 4 <= TS * 2 * TILE * HD * 2, "merge buffer must fit the stages");
   if (lane == 0) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < HPW; ++h) {
       s_wm[warp][h] = m_run[h];
       s_wl[warp][h] = l_run[h];
     }
   }
 #pragma unroll
-  for (int h = 0; h < G; ++h)
+  for (int h = 0; h < HPW; ++h)
 #pragma unroll
     for (int e = 0; e < DPL; ++e) s_wo[warp][h * HD + lane * DPL + e] = o[h][e];
   __syncthreads();
-  const size_t slot = ((size_t)brel * a.n_kv + kvh) * S + sp;
+  const size_t slot0 = ((size_t)brel * a.n_kv + kvh) * S;
   for (int idx = tid; idx < G * HD; idx += NT) {
-    const int h = idx / HD;
+    const int h = idx / HD, hl = h % HPW, g0 = (h / HPW) * TS;  // warps g0 .. g0+TS-1 hold head h
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_wm[w][h]);
+    for (int t = 0; t < TS; ++t) M = fmaxf(M, s_wm[g0 + t][hl]);
     float acc = 0.f, L = 0.f;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float e = s_wl[w][h] > 0.f ? expf(s_wm[w][h] - M) : 0.f;
-      acc = fmaf(e, s_wo[w][idx], acc);
-      L = fmaf(e, s_wl[w][h], L);
+    for (int t = 0; t < TS; ++t) {
+      const float e = s_wl[g0 + t][hl] > 0.f ? expf(s_wm[g0 + t][hl] - M) : 0.f;
+      acc = fmaf(e, s_wo[g0 + t][hl * HD + (idx % HD)], acc);
+      L = fmaf(e, s_wl[g0 + t][hl], L);
     }
-    a.part_o[slot * G * HD + idx] = acc;
-    if ((idx % HD) == 0) reinterpret_cast<float2*>(a.part_ml)[slot * G + h] = make_float2(M, L);
+    a.part_o[(slot0 + sp) * G * HD + idx] = acc;
+    if ((idx % HD) == 0) reinterpret_cast<float2*>(a.part_ml)[(slot0 + sp) * G + h] = make_float2(M, L);
   }
   __threadfence();
   __syncthreads();
@@ -218,8 +226,7 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  // ---- last CTA of this (row, kv head): merge the S splits
-  const size_t slot0 = ((size_t)brel * a.n_kv + kvh) * S;
+  // ---- last CTA of this (row, kv head): merge the S splits, all loads in flight
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
   for (int h = warp; h < G; h += NW) {
     float M = -INFINITY;
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
     const int h = idx / HD;
     const float* po = a.part_o + slot0 * G * HD + idx;
     float acc = 0.f;
-#pragma unroll 8
+#pragma unroll 16
     for (int s = 0; s < S; ++s) acc = fmaf(s_w[h][s], __ldcg(po + (size_t)s * G * HD), acc);
     a.o[((size_t)brel * a.n_heads + (size_t)kvh * G) * HD + idx] = acc;
   }
@@ -274,7 +281,7 @@ void attn_workspace_carve(void* ws, int rows, int n_heads, int n_kv, int head_di
 // but no more than two CTAs per SM over the grid.
 int attn_default_splits(int rows, int n_kv, int num_sms, int max_len) {
   const int tiles = (max_len + TILE - 1) / TILE;
-  int s = (tiles + NW - 1) / NW;
+  int s = (tiles + 3) / 4;  // about one tile per slot
   const int cap = (2 * num_sms + rows * n_kv - 1) / (rows * n_kv);
   if (s > cap) s = cap;
   if (s > kMaxSplits) s = kMaxSplits;  // merge weights live in shared memory
@@ -284,12 +291,17 @@ int attn_default_splits(int rows, int n_kv, int num_sms, int max_len) {
 
 using AttnFn = void (*)(const AttnArgs);
 
+int attn_smem(int hd, int g) {
+  const int ts = g >= 2 ? NW / 2 : NW;
+  return ts * 2 * TILE * hd * 2;
+}
+
 template <int HD, int G>
 AttnFn attn_fn() {
   static bool done = false;  // raise the dynamic shared memory limit once
   if (!done) {
     if (cudaFuncSetAttribute(attn_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             NW * 2 * TILE * HD * 2) != cudaSuccess)
+                             attn_smem(HD, G)) != cudaSuccess)
       return nullptr;
     done = true;
   }
@@ -317,7 +329,7 @@ cudaError_t launch_attention(const AttnArgs& a, int rows, cudaStream_t s, bool p
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_kv * a.n_splits, rows);
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = NW * 2 * TILE * a.head_dim * 2;
+  cfg.dynamicSmemBytes = attn_smem(a.head_dim, a.n_heads / a.n_kv);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
