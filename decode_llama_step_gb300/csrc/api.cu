@@ -22,6 +22,9 @@ thread_local std::string g_err;
 
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// prompt tokens per prefill pass (bounded scratch; longer prompts run in chunks)
+constexpr int kPrefillChunk = 1024;
+
 struct MatOff {
   size_t qs = 0, d = 0;
   int rows = 0, cols = 0, nb = 0, ds = 0;
@@ -127,6 +130,11 @@ struct dls_model {
   int attn_splits = 1;
   int2* pairs_dev = nullptr;
   size_t pairs_cap = 0;
+  // prefill scratch for chunks of up to pf_cap tokens (tensor-core path)
+  int pf_cap = 0, pf_ldh = 0;
+  float *pf_x = nullptr, *pf_qkv = nullptr, *pf_q = nullptr;
+  __half *pf_a = nullptr, *pf_h = nullptr;
+  int32_t* pf_tok = nullptr;
   GemvLaunch plan_qkv{}, plan_o{}, plan_gu{}, plan_down{}, plan_head{};
   // graphs and hooks
   std::vector<GraphEntry> graphs;
@@ -335,27 +343,46 @@ int enqueue_copy_layer(dls_model* m, int l) {
   return DLS_OK;
 }
 
+// Start a pass over the layers: with streamed layers, the copy stream joins
+// the compute stream here and fills both buffers with the first two.
+int stream_begin(dls_model* m) {
+  if (m->resident >= m->L) return DLS_OK;
+  CK(cudaEventRecord(m->ev_start, m->stream));
+  CK(cudaStreamWaitEvent(m->copy_stream, m->ev_start, 0));
+  // both buffers are free at the start of a pass
+  CK(cudaEventRecord(m->ev_free[0], m->stream));
+  CK(cudaEventRecord(m->ev_free[1], m->stream));
+  for (int l = m->resident; l < std::min(m->L, m->resident + 2); ++l) TRY(enqueue_copy_layer(m, l));
+  return DLS_OK;
+}
+
+// Weights of layer l for the compute stream (waits for its buffer if streamed).
+int layer_begin(dls_model* m, int l, LayerPtrs* P) {
+  const bool streamed = l >= m->resident;
+  const int buf = (l - m->resident) & 1;
+  if (streamed) CK(cudaStreamWaitEvent(m->stream, m->ev_filled[buf], 0));
+  *P = layer_ptrs(m, streamed ? m->stage[buf] : m->layer_dev[l]);
+  return DLS_OK;
+}
+
+// Layer l's last kernel is enqueued: release its buffer, refill it with l + 2.
+int layer_end(dls_model* m, int l) {
+  if (l < m->resident) return DLS_OK;
+  CK(cudaEventRecord(m->ev_free[(l - m->resident) & 1], m->stream));
+  if (l + 2 < m->L) TRY(enqueue_copy_layer(m, l + 2));
+  return DLS_OK;
+}
+
 int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
   cudaStream_t s = m->stream;
   const bool pdl = m->pdl && !m->profiling;  // profiled kernels run strictly one after another
   float* x = m->x + (size_t)b * m->H;
   float* logits = m->logits + (size_t)b * m->V;
   LK(K_EMBED, launch_embed(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp, b, x, m->V, s, pdl));
-  const bool streaming = m->resident < m->L;
-  if (streaming) {
-    // the copy stream joins this step after everything enqueued so far
-    CK(cudaEventRecord(m->ev_start, s));
-    CK(cudaStreamWaitEvent(m->copy_stream, m->ev_start, 0));
-    // both buffers are free at the start of a step
-    CK(cudaEventRecord(m->ev_free[0], s));
-    CK(cudaEventRecord(m->ev_free[1], s));
-    for (int l = m->resident; l < std::min(m->L, m->resident + 2); ++l) TRY(enqueue_copy_layer(m, l));
-  }
+  TRY(stream_begin(m));
   for (int l = 0; l < m->L; ++l) {
-    const bool streamed = l >= m->resident;
-    const int buf = (l - m->resident) & 1;
-    if (streamed) CK(cudaStreamWaitEvent(s, m->ev_filled[buf], 0));
-    const LayerPtrs P = layer_ptrs(m, streamed ? m->stage[buf] : m->layer_dev[l]);
+    LayerPtrs P;
+    TRY(layer_begin(m, l, &P));
     KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
               m->nkv, m->hd, m->pt, m->max_pages};
     // (1) RMSNorm -> QKV GEMV -> RoPE -> fp16 K/V append
@@ -421,10 +448,7 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
     gd.y = x;
     LK(K_DOWN, launch_gemv(m->wtype, PRO_COPY, EPI_RESID, gd, m->plan_down, s, pdl));
     if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * m->H, x, m->H * sizeof(float), cudaMemcpyDeviceToDevice, s));
-    if (streamed) {
-      CK(cudaEventRecord(m->ev_free[buf], s));
-      if (l + 2 < m->L) TRY(enqueue_copy_layer(m, l + 2));
-    }
+    TRY(layer_end(m, l));
   }
   if (head || argmax) {
     GemvArgs gh{};
@@ -439,6 +463,81 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
   if (argmax)
     LK(K_ARGMAX, launch_argmax(logits, m->V, 1, m->next_tok + b, m->argmax_part, m->argmax_cnt,
                                argmax_blocks(1, m->num_sms), s, pdl));
+  return DLS_OK;
+}
+
+// ---- prefill ---------------------------------------------------------------------
+// T prompt tokens at positions pos0 .. pos0+T-1 of `seq`, all at once: the
+// projections run as tensor-core GEMMs over the T tokens (fp16 operands,
+// fp32 accumulation), attention as a causal flash pass over the paged cache
+// (which already holds positions < pos0 and receives the chunk's K/V here).
+int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos0, bool head, float* capture) {
+  cudaStream_t s = m->stream;
+  const int H = m->H, qkv_ld = m->q_rows + 2 * m->kv_rows;
+  CK(cudaMemcpyAsync(m->pf_tok, tokens, (size_t)T * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  LK(K_EMBED, launch_embed_rows(mat_at(m->emb_block, m->emb_off), m->wtype, m->pf_tok, T, m->V, m->pf_x, H,
+                                &m->sp->status, s));
+  TRY(stream_begin(m));
+  for (int l = 0; l < m->L; ++l) {
+    LayerPtrs P;
+    TRY(layer_begin(m, l, &P));
+    KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
+              m->nkv, m->hd, m->pt, m->max_pages};
+    // (1) RMSNorm -> fp16 -> QKV GEMM -> RoPE, fp16 K/V into the pages
+    LK(K_QKV, launch_rmsnorm_rows(m->pf_x, T, H, H, P.attn_norm, m->eps, m->pf_a, H, s));
+    PgArgs g{};
+    g.w = P.qkv;
+    g.x = m->pf_a;
+    g.kx = H;
+    g.T = T;
+    g.y = m->pf_qkv;
+    g.ldy = qkv_ld;
+    g.status = &m->sp->status;
+    LK(K_QKV, launch_pgemm(m->wtype, EPI_STORE, g, s));
+    LK(K_QKV, launch_rope_kv_rows(m->pf_qkv, T, qkv_ld, m->q_rows, m->kv_rows, kv, seq, pos0, m->rope, m->rope_len,
+                                  m->pf_q, &m->sp->status, s));
+    // (2) causal attention; the output reuses the qkv buffer
+    float* o = m->pf_qkv;
+    LK(K_ATTN, launch_pattn(m->pf_q, o, kv, m->pt_dev + (size_t)seq * m->max_pages, m->nh, T, pos0, s));
+    // (3) O projection + residual
+    LK(K_O, launch_to_f16_rows(o, T, m->q_rows, m->q_rows, m->pf_a, m->q_rows, s));
+    PgArgs go = g;
+    go.w = P.o;
+    go.kx = m->q_rows;
+    go.y = m->pf_x;
+    go.ldy = H;
+    LK(K_O, launch_pgemm(m->wtype, EPI_RESID, go, s));
+    // (4) RMSNorm -> fp16 -> gate/up GEMM with SwiGLU -> fp16 h
+    LK(K_GATE_UP, launch_rmsnorm_rows(m->pf_x, T, H, H, P.ffn_norm, m->eps, m->pf_a, H, s));
+    PgArgs gg = g;
+    gg.w = P.gu;
+    gg.y = nullptr;
+    gg.h = m->pf_h;
+    gg.ldh = m->pf_ldh;
+    LK(K_GATE_UP, launch_pgemm(m->wtype, EPI_SWIGLU, gg, s));
+    // (5) down GEMM + residual
+    PgArgs gd = g;
+    gd.w = P.down;
+    gd.x = m->pf_h;
+    gd.kx = m->pf_ldh;
+    gd.y = m->pf_x;
+    gd.ldy = H;
+    LK(K_DOWN, launch_pgemm(m->wtype, EPI_RESID, gd, s));
+    if (capture)
+      CK(cudaMemcpyAsync(capture + (size_t)l * H, m->pf_x + (size_t)(T - 1) * H, H * sizeof(float),
+                         cudaMemcpyDeviceToDevice, s));
+    TRY(layer_end(m, l));
+  }
+  if (head) {
+    GemvArgs gh{};
+    gh.w = head_mat(m);
+    gh.unit = 1;
+    gh.x = m->pf_x + (size_t)(T - 1) * H;
+    gh.g = m->out_norm;
+    gh.eps = m->eps;
+    gh.y = m->logits;
+    LK(K_HEAD, launch_gemv(m->wtype, PRO_RMSNORM, EPI_STORE, gh, m->plan_head, s, false));
+  }
   return DLS_OK;
 }
 
@@ -863,6 +962,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   }
   CKC(cudaEventCreateWithFlags(&m->ev_start, cudaEventDisableTiming));
   CKC(gemv_setup_attributes());
+  CKC(pgemm_setup_attributes());
 
   // layouts
   size_t cur = 0;
@@ -925,6 +1025,17 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   attn_workspace_carve(m->attn_ws, 1, m->nh, m->nkv, m->hd, m->attn_splits, &m->part_o, &m->part_ml, &m->counters);
   m->pairs_cap = (size_t)m->max_pages * std::max(1, m->max_seqs - 1);
   TRYC(dev_alloc_t(m, m->pairs_cap, &m->pairs_dev, "fork_pairs"));
+  m->pf_cap = std::min(m->max_ctx, kPrefillChunk);
+  if (const char* e = getenv("DLS_PREFILL_CHUNK")) m->pf_cap = std::max(1, std::min(m->max_ctx, atoi(e)));
+  m->pf_ldh = (m->F + 31) & ~31;
+  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * m->H, &m->pf_x, "prefill_x"));
+  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * std::max(m->H, m->q_rows), &m->pf_a, "prefill_a16"));
+  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * (m->q_rows + 2 * m->kv_rows), &m->pf_qkv, "prefill_qkv"));
+  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * m->q_rows, &m->pf_q, "prefill_q"));
+  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * m->pf_ldh, &m->pf_h, "prefill_h16"));
+  TRYC(dev_alloc_t(m, (size_t)m->pf_cap, &m->pf_tok, "prefill_tokens"));
+  // columns F .. pf_ldh of h are read by the down GEMM and never written
+  CKC(cudaMemsetAsync(m->pf_h, 0, (size_t)m->pf_cap * m->pf_ldh * sizeof(__half), m->stream));
   void* temp = nullptr;
   TRYC(dev_alloc(m, temp_bytes, &temp, "upload_temp"));
 
@@ -1017,11 +1128,14 @@ int dls_prefill(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, flo
   if ((long long)s.len + n > m->max_ctx)
     return fail(m, DLS_ERR_CAPACITY, "seq=%d length=%d n=%d max_ctx=%d", seq, s.len, n, m->max_ctx);
   TRY(ensure_pages(m, seq, s.len + n));
-  for (int i = 0; i < n; ++i) {
-    const int32_t pos = s.len + i;
-    TRY(set_params(m, 1, &seq, &tokens[i], &pos, i == 0));
-    const bool last = i == n - 1;
-    TRY(run_step(m, 1, last && logits_out != nullptr, false));
+  const int32_t pos0 = s.len;
+  TRY(set_params(m, 1, &seq, &tokens[0], &pos0, true));  // clears the device status word
+  float* cap = m->capture;
+  m->capture = nullptr;
+  for (int c0 = 0; c0 < n; c0 += m->pf_cap) {
+    const int T = std::min(m->pf_cap, n - c0);
+    const bool last = c0 + T == n;
+    TRY(enqueue_prefill(m, seq, tokens + c0, T, pos0 + c0, last && logits_out != nullptr, last ? cap : nullptr));
   }
   TRY(copy_out(m, logits_out, m->logits, (size_t)m->V * sizeof(float)));
   TRY(sync_stream(m, m->stream));
@@ -1303,6 +1417,42 @@ int dls_debug_gemv(dls_model* m, int32_t layer, int32_t tensor, const float* x, 
   const GemvLaunch l = gemv_plan(m->wtype, PRO_COPY, EPI_STORE, md.rows, md.nb, m->num_sms, 1);
   CK(launch_gemv(m->wtype, PRO_COPY, EPI_STORE, g, l, m->stream, false));
   return DLS_OK;
+}
+
+int dls_debug_gemm(dls_model* m, int32_t layer, int32_t tensor, int32_t n_tokens, const float* x, float* y) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (!x || !y || n_tokens < 1) return fail(m, DLS_ERR_ARG, "x/y NULL or n_tokens=%d", n_tokens);
+  MatDev md;
+  TRY(find_matrix(m, layer, tensor, &md));
+  const bool pair = md.rstep == 2;  // gate or up: run the interleaved matrix, keep every other column
+  const MatDev w = pair ? mat_at(m->layer_dev[layer], m->lay.gu) : md;
+  const int kx = w.nb * 32;
+  void *xh = nullptr, *yt = nullptr;
+  TRY(dev_alloc(m, (size_t)n_tokens * kx * sizeof(__half), &xh, "debug_gemm_x"));
+  int r = pair ? dev_alloc(m, (size_t)n_tokens * w.rows * sizeof(float), &yt, "debug_gemm_y") : DLS_OK;
+  if (r == DLS_OK) {
+    cudaError_t e = launch_to_f16_rows(x, n_tokens, w.cols, w.cols, static_cast<__half*>(xh), kx, m->stream);
+    PgArgs g{};
+    g.w = w;
+    g.x = static_cast<const __half*>(xh);
+    g.kx = kx;
+    g.T = n_tokens;
+    g.y = pair ? static_cast<float*>(yt) : y;
+    g.ldy = w.rows;
+    g.status = &m->sp->status;
+    if (e == cudaSuccess) e = launch_pgemm(m->wtype, EPI_STORE, g, m->stream);
+    if (e == cudaSuccess && pair)
+      e = cudaMemcpy2DAsync(y, sizeof(float), static_cast<float*>(yt) + (tensor - 4), 2 * sizeof(float), sizeof(float),
+                            (size_t)n_tokens * m->F, cudaMemcpyDeviceToDevice, m->stream);
+    if (e != cudaSuccess) r = fail(m, DLS_ERR_CUDA, "debug_gemm cuda=%s", cudaGetErrorString(e));
+    if (r == DLS_OK) r = sync_stream(m, m->stream);
+  }
+  const int rs = sync_stream(m, m->stream);
+  dev_free(m, xh);
+  dev_free(m, yt);
+  TRY(r);
+  TRY(rs);
+  return check_status(m);
 }
 
 }  // extern "C"

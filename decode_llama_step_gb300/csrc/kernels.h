@@ -151,6 +151,36 @@ struct StepPlan {
 StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, int hd, int num_sms);
 cudaError_t launch_step(const StepPlan& p, const StepArgs& a, cudaStream_t s);
 
+// ---- prefill (T tokens at once) --------------------------------------------------
+
+struct PgArgs {
+  MatDev w;            // weight rows = GEMM M
+  const __half* x;     // activations [T][kx] fp16, kx >= w.nb * 32, zero beyond the true width
+  int kx;              // row stride of x in elements (multiple of 8)
+  int T;               // tokens = GEMM N
+  float* y;            // STORE / RESID: y[t * ldy + m]
+  int ldy;
+  __half* h;           // SWIGLU: h[t * ldh + m / 2] = silu(gate) * up (rows interleaved gate, up)
+  int ldh;
+  int32_t* status;     // kTimeout on a wait that gave up
+};
+
+int pgemm_smem_bytes();
+cudaError_t pgemm_setup_attributes();
+cudaError_t launch_pgemm(int wtype, int epi, const PgArgs& a, cudaStream_t s);
+cudaError_t launch_embed_rows(const MatDev& emb, int wtype, const int32_t* tokens, int T, int vocab, float* x, int ldx,
+                              int32_t* status, cudaStream_t s);
+cudaError_t launch_rmsnorm_rows(const float* x, int T, int H, int ldx, const float* g, float eps, __half* out, int ldo,
+                                cudaStream_t s);
+cudaError_t launch_to_f16_rows(const float* x, int T, int cols, int ldx, __half* out, int ldo, cudaStream_t s);
+cudaError_t launch_rope_kv_rows(const float* qkv, int T, int ld, int q_rows, int kv_rows, const KvView& kv, int seq,
+                                int pos0, const float2* rope_cs, int rope_len, float* q_out, int32_t* status,
+                                cudaStream_t s);
+// causal attention of T query tokens at positions pos0 .. pos0+T-1 over one
+// sequence (ptab_row = its page-table row); q, o: [T][n_heads][head_dim]
+cudaError_t launch_pattn(const float* q, float* o, const KvView& kv, const int32_t* ptab_row, int n_heads, int T,
+                         int pos0, cudaStream_t s);
+
 // Record a failure for dls_last_error(NULL) (calls without a model) and
 // return `code`.
 int report_error(int code, const char* fmt, ...);

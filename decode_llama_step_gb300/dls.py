@@ -78,6 +78,7 @@ _SIGS = {
     "dls_debug_read_kv": (ctypes.c_int, [vp, i32, i32, vp, vp]),
     "dls_debug_dequant": (ctypes.c_int, [vp, i32, i32, vp]),
     "dls_debug_gemv": (ctypes.c_int, [vp, i32, i32, vp, vp]),
+    "dls_debug_gemm": (ctypes.c_int, [vp, i32, i32, i32, vp, vp]),
     "dls_debug_launches_per_step": (i32, [vp]),
     "dls_debug_profile_step": (ctypes.c_int, [vp, i32, i32, i32, i32, vp, vp, vp]),
 }
@@ -336,6 +337,10 @@ class Model:
 
     def debug_gemv(self, layer: int, tensor: str, x, y):
         self._c(self.lib.dls_debug_gemv(self.handle, layer, TENSOR_IDS[tensor], _ptr(x), _ptr(y)))
+
+    def debug_gemm(self, layer: int, tensor: str, x, y):
+        """y[t] = W x[t] with the prefill GEMM; x device fp32 [T][cols], y [T][rows]."""
+        self._c(self.lib.dls_debug_gemm(self.handle, layer, TENSOR_IDS[tensor], int(x.shape[0]), _ptr(x), _ptr(y)))
 
     def profile_step(self, seq: int, token: int, pos: int, max_kernels: int = 4096):
         """(durations_ms, kinds) of every kernel of one decode step."""

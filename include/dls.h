@@ -150,9 +150,16 @@ int32_t dls_seq_length(const dls_model* m, int32_t seq);
 /* ---- the hot path --------------------------------------------------------- */
 
 /* Run n prompt tokens (host int32 [n], each in [0, vocab)) through every
- * layer at positions length..length+n-1 of `seq`, filling its KV cache.
- * logits_out (host or device fp32 [vocab], or NULL) receives the logits of
- * the last token.  DLS_ERR_CAPACITY if length + n > max_ctx. */
+ * layer at positions length..length+n-1 of `seq`, filling its KV cache
+ * (SwarmKV, section 2: prefill computes and stores the K/V of every prompt
+ * token once).  The tokens go through in chunks of up to 1024 (the
+ * environment variable DLS_PREFILL_CHUNK, read at model creation, sets
+ * another size): each projection of a chunk is one tensor-core GEMM with
+ * fp16 operands (weights dequantised to fp16(d*q), activations rounded to
+ * fp16) and fp32 accumulation; attention is causal over the cache.  Results
+ * per token do not depend on the chunking.  logits_out (host or device fp32
+ * [vocab], or NULL) receives the logits of the last token.  DLS_ERR_CAPACITY
+ * if length + n > max_ctx. */
 int dls_prefill(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out);
 
 /* One decode step: `token` at position `pos`, which must equal the
@@ -251,8 +258,9 @@ int dls_attention_decode_noalloc(const float* q, const void* k_pages, const void
 /* ---- test and profiling hooks ------------------------------------------------ */
 
 /* Arm a capture of the residual stream after every layer for the next
- * decode call (batch row 0): per_layer_out device fp32 [n_layers][hidden].
- * NULL disarms.  The captured call runs without CUDA-graph replay. */
+ * decode call (batch row 0) or prefill call (its last prompt token):
+ * per_layer_out device fp32 [n_layers][hidden].  NULL disarms.  A captured
+ * decode call runs without CUDA-graph replay. */
 int dls_debug_capture(dls_model* m, float* per_layer_out);
 /* Copy positions [0, length) of one layer's K and V of `seq` into device
  * fp16 [length][n_kv_heads][head_dim] buffers. */
@@ -264,6 +272,10 @@ int dls_debug_dequant(dls_model* m, int32_t layer, int32_t tensor, float* out);
 /* y = W x with the decode GEMV kernel for one matrix (ids as above);
  * x device fp32 [cols], y device fp32 [rows]. */
 int dls_debug_gemv(dls_model* m, int32_t layer, int32_t tensor, const float* x, float* y);
+/* Y = X W^T with the prefill GEMM for one matrix (ids as above): X device
+ * fp32 [n_tokens][cols], rounded to fp16 on the device; Y device fp32
+ * [n_tokens][rows].  Synchronises the model's stream. */
+int dls_debug_gemm(dls_model* m, int32_t layer, int32_t tensor, int32_t n_tokens, const float* x, float* y);
 /* One decode step (same contract as dls_decode_step, logits left in the
  * model's buffer) run with a CUDA event after every kernel and without
  * programmatic dependent launch, so each kernel's device time is measured

@@ -1,0 +1,178 @@
+"""Prefill on the tensor cores, through the C ABI, against the oracle:
+the GEMM on every matrix (one to three 128-token tiles, ragged tails), the
+per-layer residual of the last prompt token, the fp16 K/V it writes, the
+logits, a prefill that continues a sequence, and chunk-size independence.
+
+The GEMM rounds each dequantised weight d*q and each activation to fp16 once
+and accumulates the exact products in fp32.  Against an fp64 product of the
+same fp16-rounded operands it must agree to fp32 accumulation error; against
+the exact fp64 product it must meet the layer tolerance (2e-3 of L-inf).
+"""
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import OracleModel, quant
+from synth.configs import ModelConfig
+
+from parity import assert_close, check_greedy, rel_err
+
+pytestmark = pytest.mark.gpu
+
+TINY = synth.get_config("tiny")
+# hidden 224 and ffn 720 end in half a 64-column K tile; ffn, vocab and q
+# rows end in partial 128-row tiles; hidden != n_heads * head_dim
+RAGGED = ModelConfig("ragged", 2, 224, 4, 2, 64, 720, 1000, 10000.0, 8, 0.02)
+# Q4_0, head_dim 32, 4 query heads per KV head
+RAGGED_Q4 = ModelConfig("raggedq4", 2, 224, 8, 2, 32, 720, 1000, 10000.0, 4, 0.02)
+CFGS = [TINY, RAGGED, RAGGED_Q4]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _make(cfg, w, chunk=None, **kw):
+    from decode_llama_step_gb300 import dls
+    torch = _torch()
+    old = os.environ.get("DLS_PREFILL_CHUNK")
+    if chunk is not None:
+        os.environ["DLS_PREFILL_CHUNK"] = str(chunk)
+    try:
+        stream = torch.cuda.Stream()
+        m = dls.Model(cfg, w, max_seqs=4, max_ctx=kw.get("max_ctx", 200), max_batch=1, page_tokens=32,
+                      stream=stream)
+    finally:
+        if old is None:
+            os.environ.pop("DLS_PREFILL_CHUNK", None)
+        else:
+            os.environ["DLS_PREFILL_CHUNK"] = old
+    return m, stream
+
+
+@pytest.fixture(scope="module", params=CFGS, ids=[c.name for c in CFGS])
+def setup(request, gpu_lib):
+    cfg = request.param
+    w = synth.model_weights(cfg)
+    m, stream = _make(cfg, w, chunk=48)   # several chunks per prompt below
+    orc = OracleModel(cfg, w)
+    yield cfg, w, m, orc, stream
+    m.close()
+
+
+def _f16(a):
+    return np.asarray(a, dtype=np.float32).astype(np.float16).astype(np.float64)
+
+
+@pytest.mark.parametrize("T", [1, 37, 300])
+def test_gemm_every_matrix(setup, T):
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    shapes = synth.matrix_shapes(cfg)
+    shapes["output"] = (cfg.vocab, cfg.hidden)
+    shapes["tok_embd"] = (cfg.vocab, cfg.hidden)
+    for name, (rows, cols) in shapes.items():
+        x = synth.normal(synth.stream_key("gemm-x", name, T), T * cols, 1.0).astype(np.float32).reshape(T, cols)
+        y = torch.empty(T, rows, device="cuda")
+        m.debug_gemm(1, name, torch.from_numpy(x).cuda(), y)
+        got = y.cpu().numpy()
+        if name in ("output", "tok_embd"):
+            W = quant.matrix(w[name], cfg.vocab, cfg.hidden, cfg.wtype)
+        else:
+            W = quant.matrix(w["layers"][1][name], rows, cols, cfg.wtype)
+        ref16 = _f16(x) @ _f16(W).T
+        e16 = rel_err(got, ref16)
+        assert e16 <= 2e-5, f"{name} T={T}: vs fp16-operand product {e16:.3e}"
+        assert_close(got, x.astype(np.float64) @ W.T, f"gemm {name} T={T}")
+
+
+def _read_kv(m, cfg, seq, n, layer):
+    torch = _torch()
+    kvd = cfg.n_kv_heads * cfg.head_dim
+    k = torch.empty(n, kvd, dtype=torch.float16, device="cuda")
+    v = torch.empty_like(k)
+    m.debug_read_kv(seq, layer, k, v)
+    return k, v
+
+
+def test_prefill_layers_kv_logits(setup):
+    """A 100-token prompt (three 48-token chunks), then 41 more tokens
+    continuing the same sequence: per-layer residual of the last token, all
+    K/V, logits and greedy token against the oracle after each call."""
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    seq = m.seq_create()
+    oseq = orc.new_seq()
+    try:
+        n0 = 0
+        for n, seed in ((100, 3), (41, 4)):
+            prompt = synth.prompt_tokens(cfg, n, seed=seed)
+            cap = torch.empty(cfg.n_layers, cfg.hidden, device="cuda")
+            logits = torch.empty(cfg.vocab, device="cuda")
+            m.debug_capture(cap)
+            m.prefill(seq, prompt, logits)
+            ocap = []
+            ref = orc.prefill(oseq, prompt, capture=ocap)
+            n0 += n
+            assert m.seq_length(seq) == n0
+            got_cap = cap.cpu().numpy()
+            for l in range(cfg.n_layers):
+                assert_close(got_cap[l], ocap[l], f"n={n} layer {l} residual")
+                k, v = _read_kv(m, cfg, seq, n0, l)
+                shape = (n0, cfg.n_kv_heads, cfg.head_dim)
+                assert_close(k.cpu().numpy().astype(np.float64).reshape(shape), oseq.keys(l), f"layer {l} K")
+                assert_close(v.cpu().numpy().astype(np.float64).reshape(shape), oseq.values(l), f"layer {l} V")
+            assert_close(logits.cpu().numpy(), ref, f"n={n} logits")
+            check_greedy(logits.cpu().numpy(), ref, f"n={n}")
+    finally:
+        m.seq_free(seq)
+
+
+def test_prefill_then_decode(setup):
+    """Decode steps attend over the K/V the prefill wrote."""
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    prompt = synth.prompt_tokens(cfg, 77, seed=6)
+    seq = m.seq_create()
+    oseq = orc.new_seq()
+    try:
+        logits = torch.empty(cfg.vocab, device="cuda")
+        m.prefill(seq, prompt, logits)
+        ref = orc.prefill(oseq, prompt)
+        tok = check_greedy(logits.cpu().numpy(), ref, "prefill")
+        for i in range(6):
+            m.decode_step(seq, tok, 77 + i, logits)
+            ref = orc.decode_step(oseq, tok, 77 + i)
+            assert_close(logits.cpu().numpy(), ref, f"step {i} logits")
+            tok = check_greedy(logits.cpu().numpy(), ref, f"step {i}")
+    finally:
+        m.seq_free(seq)
+
+
+def test_chunk_size_does_not_change_results(gpu_lib):
+    """Every token's arithmetic is independent of which chunk carries it:
+    chunks of 48, 7 and one chunk of 150 give bit-identical K/V and logits."""
+    torch = _torch()
+    cfg = TINY
+    w = synth.model_weights(cfg)
+    prompt = synth.prompt_tokens(cfg, 150, seed=12)
+    outs = []
+    for chunk in (None, 48, 7):
+        m, stream = _make(cfg, w, chunk=chunk)
+        try:
+            s = m.seq_create()
+            lg = torch.empty(cfg.vocab, device="cuda")
+            m.prefill(s, prompt, lg)
+            kv = [_read_kv(m, cfg, s, 150, l) for l in range(cfg.n_layers)]
+            stream.synchronize()
+            outs.append((lg.clone(), [(k.clone(), v.clone()) for k, v in kv]))
+        finally:
+            m.close()
+    for lg, kv in outs[1:]:
+        assert torch.equal(lg, outs[0][0])
+        for (k, v), (k0, v0) in zip(kv, outs[0][1]):
+            assert torch.equal(k.view(torch.int16), k0.view(torch.int16))
+            assert torch.equal(v.view(torch.int16), v0.view(torch.int16))
