@@ -23,7 +23,10 @@ thread_local std::string g_err;
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // prompt tokens per prefill pass (bounded scratch; longer prompts run in chunks)
-constexpr int kPrefillChunk = 1024;
+constexpr int kPrefillChunk = 2048;
+// split-K limits of the tensor-core GEMM at batch sizes <= 16
+constexpr int kTgMaxSplit = 8;
+constexpr int kTgCounters = 4096;
 
 struct MatOff {
   size_t qs = 0, d = 0;
@@ -135,6 +138,10 @@ struct dls_model {
   float *pf_x = nullptr, *pf_qkv = nullptr, *pf_q = nullptr;
   __half *pf_a = nullptr, *pf_h = nullptr;
   int32_t* pf_tok = nullptr;
+  // tensor-core GEMM split-K workspace: partial sums and per-tile counters
+  float* tg_part = nullptr;
+  int* tg_cnt = nullptr;
+  size_t tg_part_elems = 0;
   GemvLaunch plan_qkv{}, plan_o{}, plan_gu{}, plan_down{}, plan_head{};
   // graphs and hooks
   std::vector<GraphEntry> graphs;
@@ -466,6 +473,20 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
   return DLS_OK;
 }
 
+// ---- tensor-core GEMM -----------------------------------------------------------
+
+int run_tgemm(dls_model* m, int kind, int epi, PgArgs g) {
+  const TgPlan p = tgemm_plan(g.w.rows, g.w.nb * 32, g.T, m->num_sms, kTgMaxSplit);
+  if (p.split > 1) {
+    if ((size_t)p.split * g.T * g.w.rows > m->tg_part_elems || (size_t)((g.w.rows + 127) / 128) > (size_t)kTgCounters)
+      return fail(m, DLS_ERR_CAPACITY, "gemm split workspace rows=%d T=%d split=%d", g.w.rows, g.T, p.split);
+    g.part = m->tg_part;
+    g.counters = m->tg_cnt;
+  }
+  LK(kind, launch_tgemm(m->wtype, epi, g, p, m->stream));
+  return DLS_OK;
+}
+
 // ---- prefill ---------------------------------------------------------------------
 // T prompt tokens at positions pos0 .. pos0+T-1 of `seq`, all at once: the
 // projections run as tensor-core GEMMs over the T tokens (fp16 operands,
@@ -493,7 +514,7 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
     g.y = m->pf_qkv;
     g.ldy = qkv_ld;
     g.status = &m->sp->status;
-    LK(K_QKV, launch_pgemm(m->wtype, EPI_STORE, g, s));
+    TRY(run_tgemm(m, K_QKV, EPI_STORE, g));
     LK(K_QKV, launch_rope_kv_rows(m->pf_qkv, T, qkv_ld, m->q_rows, m->kv_rows, kv, seq, pos0, m->rope, m->rope_len,
                                   m->pf_q, &m->sp->status, s));
     // (2) causal attention; the output reuses the qkv buffer
@@ -506,7 +527,7 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
     go.kx = m->q_rows;
     go.y = m->pf_x;
     go.ldy = H;
-    LK(K_O, launch_pgemm(m->wtype, EPI_RESID, go, s));
+    TRY(run_tgemm(m, K_O, EPI_RESID, go));
     // (4) RMSNorm -> fp16 -> gate/up GEMM with SwiGLU -> fp16 h
     LK(K_GATE_UP, launch_rmsnorm_rows(m->pf_x, T, H, H, P.ffn_norm, m->eps, m->pf_a, H, s));
     PgArgs gg = g;
@@ -514,7 +535,7 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
     gg.y = nullptr;
     gg.h = m->pf_h;
     gg.ldh = m->pf_ldh;
-    LK(K_GATE_UP, launch_pgemm(m->wtype, EPI_SWIGLU, gg, s));
+    TRY(run_tgemm(m, K_GATE_UP, EPI_SWIGLU, gg));
     // (5) down GEMM + residual
     PgArgs gd = g;
     gd.w = P.down;
@@ -522,7 +543,7 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
     gd.kx = m->pf_ldh;
     gd.y = m->pf_x;
     gd.ldy = H;
-    LK(K_DOWN, launch_pgemm(m->wtype, EPI_RESID, gd, s));
+    TRY(run_tgemm(m, K_DOWN, EPI_RESID, gd));
     if (capture)
       CK(cudaMemcpyAsync(capture + (size_t)l * H, m->pf_x + (size_t)(T - 1) * H, H * sizeof(float),
                          cudaMemcpyDeviceToDevice, s));
@@ -962,7 +983,8 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   }
   CKC(cudaEventCreateWithFlags(&m->ev_start, cudaEventDisableTiming));
   CKC(gemv_setup_attributes());
-  CKC(pgemm_setup_attributes());
+  CKC(tgemm_setup_attributes());
+  CKC(prefill_setup_attributes());
 
   // layouts
   size_t cur = 0;
@@ -1034,6 +1056,14 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   TRYC(dev_alloc_t(m, (size_t)m->pf_cap * m->q_rows, &m->pf_q, "prefill_q"));
   TRYC(dev_alloc_t(m, (size_t)m->pf_cap * m->pf_ldh, &m->pf_h, "prefill_h16"));
   TRYC(dev_alloc_t(m, (size_t)m->pf_cap, &m->pf_tok, "prefill_tokens"));
+  {
+    // split-K partials for batches of up to 16 rows: [split][16][rows]
+    const int max_rows = std::max(std::max(m->q_rows + 2 * m->kv_rows, 2 * m->F), m->H);
+    m->tg_part_elems = (size_t)kTgMaxSplit * 16 * max_rows;
+    TRYC(dev_alloc_t(m, m->tg_part_elems, &m->tg_part, "gemm_split_partials"));
+    TRYC(dev_alloc_t(m, (size_t)kTgCounters, &m->tg_cnt, "gemm_split_counters"));
+    CKC(cudaMemsetAsync(m->tg_cnt, 0, (size_t)kTgCounters * sizeof(int), m->stream));
+  }
   // columns F .. pf_ldh of h are read by the down GEMM and never written
   CKC(cudaMemsetAsync(m->pf_h, 0, (size_t)m->pf_cap * m->pf_ldh * sizeof(__half), m->stream));
   void* temp = nullptr;
@@ -1440,7 +1470,13 @@ int dls_debug_gemm(dls_model* m, int32_t layer, int32_t tensor, int32_t n_tokens
     g.y = pair ? static_cast<float*>(yt) : y;
     g.ldy = w.rows;
     g.status = &m->sp->status;
-    if (e == cudaSuccess) e = launch_pgemm(m->wtype, EPI_STORE, g, m->stream);
+    const TgPlan p = tgemm_plan(w.rows, kx, n_tokens, m->num_sms, kTgMaxSplit);
+    if (p.split > 1) {
+      if ((size_t)p.split * n_tokens * w.rows > m->tg_part_elems) e = cudaErrorInvalidValue;
+      g.part = m->tg_part;
+      g.counters = m->tg_cnt;
+    }
+    if (e == cudaSuccess) e = launch_tgemm(m->wtype, EPI_STORE, g, p, m->stream);
     if (e == cudaSuccess && pair)
       e = cudaMemcpy2DAsync(y, sizeof(float), static_cast<float*>(yt) + (tensor - 4), 2 * sizeof(float), sizeof(float),
                             (size_t)n_tokens * m->F, cudaMemcpyDeviceToDevice, m->stream);

@@ -163,11 +163,18 @@ struct PgArgs {
   __half* h;           // SWIGLU: h[t * ldh + m / 2] = silu(gate) * up (rows interleaved gate, up)
   int ldh;
   int32_t* status;     // kTimeout on a wait that gave up
+  float* part;         // split-K partial sums [split][T][rows] (split > 1)
+  int* counters;       // one per output tile, zero between launches (split > 1)
 };
 
-int pgemm_smem_bytes();
-cudaError_t pgemm_setup_attributes();
-cudaError_t launch_pgemm(int wtype, int epi, const PgArgs& a, cudaStream_t s);
+// tile width (tokens per CTA: 16, 128 or 256) and K splits of one GEMM
+struct TgPlan {
+  int bn, split;
+};
+TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split);
+cudaError_t tgemm_setup_attributes();  // smem limits; fails if tensor maps cannot be made
+cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, cudaStream_t s);
+cudaError_t prefill_setup_attributes();
 cudaError_t launch_embed_rows(const MatDev& emb, int wtype, const int32_t* tokens, int T, int vocab, float* x, int ldx,
                               int32_t* status, cudaStream_t s);
 cudaError_t launch_rmsnorm_rows(const float* x, int T, int H, int ldx, const float* g, float eps, __half* out, int ldo,

@@ -1,243 +1,22 @@
-// Prefill: the same layer math for T prompt tokens at once (SwarmKV page,
+// Prefill kernels besides the projections (those are the tensor-core GEMM
+// in gemm.cu): the layer math for T prompt tokens at once (SwarmKV page,
 // section 2: prefill runs every prompt token through every layer once and
-// fills the KV cache; its cost grows with the prompt length, so it is where
-// the dense tensor-core work is).
+// fills the KV cache).
 //
-//  * pgemm_kernel: D[m, t] = sum_k W[m, k] X[t, k] on tcgen05 (kind::f16,
-//    M = 128 weight rows, N = 128 tokens, K = 16 per instruction, fp32
-//    accumulators in tensor memory).  Loader warps dequantise the Q8_0/Q4_0
-//    weight tile (fp16(d * q), one rounding) and copy the fp16 token tile
-//    into 128-byte-swizzled shared memory; one thread issues the MMAs and
-//    commits them to the stage's "empty" barrier; four epilogue warps read the
-//    accumulators back (tcgen05.ld) and store, add to the residual, or apply
-//    SwiGLU to interleaved (gate, up) row pairs.
 //  * pattn_kernel: causal attention of T query tokens over the sequence's
 //    paged fp16 cache, flash style on CUDA cores (64 query-head rows per CTA,
 //    32-key tiles, online softmax in registers).
-//  * row kernels: RMSNorm -> fp16, RoPE + fp16 K/V append, fp32 -> fp16.
+//  * row kernels: embedding rows, RMSNorm -> fp16, RoPE + fp16 K/V append,
+//    fp32 -> fp16.
 #include <math.h>
 
 #include <utility>
 
 #include "kernels.h"
-#include "tc.cuh"
 
 namespace dls {
 
 namespace {
-
-constexpr int PBM = 128, PBN = 128, PBK = 64, PNST = 4;
-constexpr int PTHREADS = 256;               // warp 0: MMA issue; warps 1-7: loaders; 4-7: epilogue
-constexpr int NLOAD = PTHREADS - 32;        // loader threads
-constexpr int kTileA = PBM * PBK * 2;       // 16 KB
-constexpr int kTileB = PBN * PBK * 2;       // 16 KB
-constexpr int kStageP = kTileA + kTileB;
-constexpr int kChunks = PBM * PBK / 8;      // 16-byte chunks per tile (1024)
-constexpr int kCPT = (kChunks + NLOAD - 1) / NLOAD;  // chunks per loader thread
-constexpr uint64_t kWaitNsP = 2000000000ull;
-
-struct PgShared {
-  uint64_t full[PNST];
-  uint64_t empty[PNST];
-  uint64_t done;
-  uint32_t tmem;
-  int abort;
-};
-
-__device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i > 4) __nanosleep(32);
-    if ((i & 63) == 0) {
-      if (*(volatile int*)abort_flag) return false;
-      if (global_ns() - t0 > kWaitNsP) {
-        *(volatile int*)abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-// 8 weights (row, cols col..col+7) dequantised to fp16(d * q), packed
-template <int WT>
-__device__ __forceinline__ uint4 dequant8(uint2 u, float d, int e) {
-  float v[8];
-  if (WT == 8) {  // bytes hold q + 128
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[i] = d * (mag_byte(u.x, i) - 8388736.0f);
-      v[4 + i] = d * (mag_byte(u.y, i) - 8388736.0f);
-    }
-  } else {  // 8 bytes of the block; low nibbles for elements 0-15, high for 16-31
-    const uint32_t lo = e < 16 ? (u.x & 0x0F0F0F0Fu) : ((u.x >> 4) & 0x0F0F0F0Fu);
-    const uint32_t hi = e < 16 ? (u.y & 0x0F0F0F0Fu) : ((u.y >> 4) & 0x0F0F0F0Fu);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[i] = d * (mag_byte(lo, i) - 8388616.0f);
-      v[4 + i] = d * (mag_byte(hi, i) - 8388616.0f);
-    }
-  }
-  uint4 r;
-  __half2 h;
-  h = __floats2half2_rn(v[0], v[1]);
-  r.x = *reinterpret_cast<uint32_t*>(&h);
-  h = __floats2half2_rn(v[2], v[3]);
-  r.y = *reinterpret_cast<uint32_t*>(&h);
-  h = __floats2half2_rn(v[4], v[5]);
-  r.z = *reinterpret_cast<uint32_t*>(&h);
-  h = __floats2half2_rn(v[6], v[7]);
-  r.w = *reinterpret_cast<uint32_t*>(&h);
-  return r;
-}
-
-// shared offset of 16-byte chunk j of row r in a 128-byte-swizzled tile
-__device__ __forceinline__ uint32_t swz(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
-
-template <int WT, int EPI>
-__global__ void __launch_bounds__(PTHREADS, 1) pgemm_kernel(const PgArgs a) {
-  extern __shared__ uint8_t psmem[];
-  const uint32_t raw = smem_u32(psmem);
-  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  const uint32_t sbase = raw + pad;                       // 1024-aligned stage area
-  PgShared& sh = *reinterpret_cast<PgShared*>(psmem + pad + PNST * kStageP);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const MatDev& w = a.w;
-  const int m0 = blockIdx.x * PBM, n0 = blockIdx.y * PBN;
-  const int kpad = w.nb * 32;
-  const int nk = (kpad + PBK - 1) / PBK;
-  const size_t rb = WT == 8 ? (size_t)w.nb * 32 : (size_t)w.nb * 16;
-
-  if (warp == 0) {
-    tmem_alloc(smem_u32(&sh.tmem), PBN);
-    tmem_relinquish();
-  }
-  if (tid == 0) {
-    for (int s = 0; s < PNST; ++s) {
-      mbar_init(smem_u32(&sh.full[s]), PTHREADS / 32 - 1);
-      mbar_init(smem_u32(&sh.empty[s]), 1);
-    }
-    mbar_init(smem_u32(&sh.done), 1);
-    sh.abort = 0;
-    mbar_fence_init();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sh.tmem;
-  constexpr uint32_t idesc = umma_idesc_f16(PBM, PBN);
-
-  if (warp == 0) {
-    // ---------------- MMA issue (one thread)
-    if (lane == 0) {
-      for (int kt = 0; kt < nk; ++kt) {
-        const int s = kt % PNST;
-        if (!pwait(smem_u32(&sh.full[s]), (kt / PNST) & 1, &sh.abort)) break;
-        tc_fence_after();
-        const uint32_t sa = sbase + s * kStageP, sb = sa + kTileA;
-#pragma unroll
-        for (int ks = 0; ks < PBK / 16; ++ks)
-          umma_f16(tmem, umma_desc_k128(sa + ks * 32), umma_desc_k128(sb + ks * 32), idesc, (kt | ks) != 0);
-        umma_commit(smem_u32(&sh.empty[s]));
-      }
-      umma_commit(smem_u32(&sh.done));
-    }
-    __syncwarp();
-  } else {
-    // ---------------- loaders: weight tile (dequantised) and token tile
-    const int lt = tid - 32;
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % PNST;
-      const int k0 = kt * PBK;
-      const uint32_t sa = sbase + s * kStageP, sb = sa + kTileA;
-      // global loads first (registers), then wait for the slot
-      uint2 cu[kCPT];
-      float cd[kCPT];
-      uint4 xv[kCPT];
-#pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
-        const int c = lt + i * NLOAD;
-        const int r = c >> 3, j = c & 7;
-        const int col = k0 + 8 * j;
-        cu[i] = make_uint2(0, 0);
-        cd[i] = 0.f;
-        xv[i] = make_uint4(0, 0, 0, 0);
-        if (c < kChunks) {
-          const int row = m0 + r;
-          if (row < w.rows && col < kpad) {
-            cd[i] = __half2float(w.d[(size_t)row * w.ds + (col >> 5)]);
-            const size_t off = WT == 8 ? (size_t)row * rb + col : (size_t)row * rb + (col >> 5) * 16 + (col & 15);
-            cu[i] = *reinterpret_cast<const uint2*>(w.qs + off);
-          }
-          const int tok = n0 + r;
-          if (tok < a.T && col < kpad) xv[i] = *reinterpret_cast<const uint4*>(a.x + (size_t)tok * a.kx + col);
-        }
-      }
-      if (kt >= PNST && !pwait(smem_u32(&sh.empty[s]), ((kt / PNST) - 1) & 1, &sh.abort)) break;
-#pragma unroll
-      for (int i = 0; i < kCPT; ++i) {
-        const int c = lt + i * NLOAD;
-        if (c < kChunks) {
-          const int r = c >> 3, j = c & 7;
-          sts128(sa + swz(r, j), dequant8<WT>(cu[i], cd[i], (k0 + 8 * j) & 31));
-          sts128(sb + swz(r, j), xv[i]);
-        }
-      }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.full[s]));
-    }
-  }
-
-  // ---------------- epilogue: warps 4-7 read TMEM lanes 32*(warp-4) ..
-  if (warp >= 4) {
-    const bool waited = pwait(smem_u32(&sh.done), 0, &sh.abort);
-    const bool ok = __all_sync(0xffffffffu, waited && !*(volatile int*)&sh.abort);
-    tc_fence_after();
-    const int m = m0 + (warp - 4) * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
-    for (int c0 = 0; c0 < PBN; c0 += 16) {
-      uint32_t r[16];
-      tmem_ld16(taddr + c0, r);
-      tmem_wait_ld();
-      if (!ok) continue;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int t = n0 + c0 + j;
-        const float v = __uint_as_float(r[j]);
-        if (EPI == EPI_SWIGLU) {
-          const float up = __shfl_down_sync(0xffffffffu, v, 1);
-          if ((lane & 1) == 0 && t < a.T && m + 1 < w.rows)
-            a.h[(size_t)t * a.ldh + (m >> 1)] = __float2half_rn(silu(v) * up);
-        } else if (t < a.T && m < w.rows) {
-          float* dst = a.y + (size_t)t * a.ldy + m;
-          if (EPI == EPI_RESID) *dst += v;
-          else *dst = v;
-        }
-      }
-    }
-    if (!ok && a.status && lane == 0) atomicOr(a.status, kTimeout);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, PBN);
-  }
-}
-
-using PgFn = void (*)(const PgArgs);
-
-template <int WT>
-PgFn pg_pick(int epi) {
-  switch (epi) {
-    case EPI_STORE: return pgemm_kernel<WT, EPI_STORE>;
-    case EPI_RESID: return pgemm_kernel<WT, EPI_RESID>;
-    case EPI_SWIGLU: return pgemm_kernel<WT, EPI_SWIGLU>;
-  }
-  return nullptr;
-}
 
 // ---------------------------------------------------------------- row kernels
 
@@ -465,15 +244,7 @@ __global__ void embed_rows_kernel(const MatDev emb, int wtype, const int32_t* to
 
 }  // namespace
 
-int pgemm_smem_bytes() { return PNST * kStageP + (int)sizeof(PgShared) + 1024; }
-
-cudaError_t pgemm_setup_attributes() {
-  for (int e : {EPI_STORE, EPI_RESID, EPI_SWIGLU}) {
-    for (PgFn f : {pg_pick<8>(e), pg_pick<4>(e)}) {
-      cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pgemm_smem_bytes());
-      if (err != cudaSuccess) return err;
-    }
-  }
+cudaError_t prefill_setup_attributes() {
   for (int g : {1, 2, 4, 8, 16}) {
     const std::pair<PaFn, int> fs[] = {{pa_pick<32>(g), pa_smem_bytes<32>()},
                                        {pa_pick<64>(g), pa_smem_bytes<64>()},
@@ -490,15 +261,6 @@ cudaError_t launch_embed_rows(const MatDev& emb, int wtype, const int32_t* token
                               int32_t* status, cudaStream_t s) {
   if (emb.cols % 4) return cudaErrorInvalidValue;
   embed_rows_kernel<<<T, 256, 0, s>>>(emb, wtype, tokens, vocab, x, ldx, status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_pgemm(int wtype, int epi, const PgArgs& a, cudaStream_t s) {
-  if (a.kx % 8 || a.kx < a.w.nb * 32 || a.T < 1) return cudaErrorInvalidValue;
-  PgFn f = wtype == 8 ? pg_pick<8>(epi) : pg_pick<4>(epi);
-  if (!f) return cudaErrorInvalidValue;
-  dim3 grid((a.w.rows + PBM - 1) / PBM, (a.T + PBN - 1) / PBN);
-  f<<<grid, PTHREADS, pgemm_smem_bytes(), s>>>(a);
   return cudaGetLastError();
 }
 

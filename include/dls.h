@@ -156,8 +156,9 @@ int32_t dls_seq_length(const dls_model* m, int32_t seq);
  * environment variable DLS_PREFILL_CHUNK, read at model creation, sets
  * another size): each projection of a chunk is one tensor-core GEMM with
  * fp16 operands (weights dequantised to fp16(d*q), activations rounded to
- * fp16) and fp32 accumulation; attention is causal over the cache.  Results
- * per token do not depend on the chunking.  logits_out (host or device fp32
+ * fp16) and fp32 accumulation; attention is causal over the cache.  The
+ * chunking changes a token's results at most by the fp32 summation order of
+ * the GEMM tiling (chunks of up to 16 tokens split K across CTAs).  logits_out (host or device fp32
  * [vocab], or NULL) receives the logits of the last token.  DLS_ERR_CAPACITY
  * if length + n > max_ctx. */
 int dls_prefill(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out);

@@ -67,7 +67,7 @@ def _f16(a):
     return np.asarray(a, dtype=np.float32).astype(np.float16).astype(np.float64)
 
 
-@pytest.mark.parametrize("T", [1, 37, 300])
+@pytest.mark.parametrize("T", [1, 8, 16, 17, 300])
 def test_gemm_every_matrix(setup, T):
     torch = _torch()
     cfg, w, m, orc, stream = setup
@@ -153,14 +153,18 @@ def test_prefill_then_decode(setup):
 
 
 def test_chunk_size_does_not_change_results(gpu_lib):
-    """Every token's arithmetic is independent of which chunk carries it:
-    chunks of 48, 7 and one chunk of 150 give bit-identical K/V and logits."""
+    """A token's arithmetic does not depend on which chunk carries it as long
+    as the chunks run the same GEMM tiling: one chunk of 150 and three chunks
+    of 50 (128-token tiles) give bit-identical K/V and logits.  Chunks of 7 run the
+    16-token tiles with K split across CTAs: the fp32 summation order
+    changes, and where that moves an activation or a K/V entry across an
+    fp16 rounding boundary the difference is one fp16 step there."""
     torch = _torch()
     cfg = TINY
     w = synth.model_weights(cfg)
     prompt = synth.prompt_tokens(cfg, 150, seed=12)
     outs = []
-    for chunk in (None, 48, 7):
+    for chunk in (None, 50, 7):
         m, stream = _make(cfg, w, chunk=chunk)
         try:
             s = m.seq_create()
@@ -171,8 +175,13 @@ def test_chunk_size_does_not_change_results(gpu_lib):
             outs.append((lg.clone(), [(k.clone(), v.clone()) for k, v in kv]))
         finally:
             m.close()
-    for lg, kv in outs[1:]:
-        assert torch.equal(lg, outs[0][0])
-        for (k, v), (k0, v0) in zip(kv, outs[0][1]):
-            assert torch.equal(k.view(torch.int16), k0.view(torch.int16))
-            assert torch.equal(v.view(torch.int16), v0.view(torch.int16))
+    lg, kv = outs[1]
+    assert torch.equal(lg, outs[0][0])
+    for (k, v), (k0, v0) in zip(kv, outs[0][1]):
+        assert torch.equal(k.view(torch.int16), k0.view(torch.int16))
+        assert torch.equal(v.view(torch.int16), v0.view(torch.int16))
+    lg, kv = outs[2]
+    assert_close(lg.cpu().numpy(), outs[0][0].cpu().numpy(), "chunks of 7 vs one chunk", tol=1e-3)
+    for (k, v), (k0, v0) in zip(kv, outs[0][1]):
+        assert_close(k.float().cpu().numpy(), k0.float().cpu().numpy(), "K, chunks of 7", tol=1e-3)
+        assert_close(v.float().cpu().numpy(), v0.float().cpu().numpy(), "V, chunks of 7", tol=1e-3)
