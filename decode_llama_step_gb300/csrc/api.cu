@@ -138,6 +138,11 @@ struct dls_model {
   float *pf_x = nullptr, *pf_qkv = nullptr, *pf_q = nullptr;
   __half *pf_a = nullptr, *pf_h = nullptr;
   int32_t* pf_tok = nullptr;
+  // batched decode (2..max_batch rows): attention scratch for that many rows
+  void* attn_ws_b = nullptr;
+  float *part_o_b = nullptr, *part_ml_b = nullptr;
+  int* counters_b = nullptr;
+  int attn_splits_b = 1;
   // tensor-core GEMM split-K workspace: partial sums and per-tile counters
   float* tg_part = nullptr;
   int* tg_cnt = nullptr;
@@ -562,6 +567,103 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
   return DLS_OK;
 }
 
+// ---- batched decode ------------------------------------------------------------
+// n = 2..max_batch rows (row b: sequence sp->seq[b], token sp->token[b] at
+// position sp->pos[b]) in one pass over the weights: each projection is one
+// tensor-core GEMM over the n rows (fp16 operands, fp32 accumulation), so a
+// weight byte is read once per step for the whole batch.
+int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
+  cudaStream_t s = m->stream;
+  const int H = m->H, qkv_ld = m->q_rows + 2 * m->kv_rows;
+  float* x = m->x;  // [n][H]
+  LK(K_EMBED, launch_embed_rows(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp->token, n, m->V, x, H,
+                                &m->sp->status, s));
+  TRY(stream_begin(m));
+  for (int l = 0; l < m->L; ++l) {
+    LayerPtrs P;
+    TRY(layer_begin(m, l, &P));
+    KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
+              m->nkv, m->hd, m->pt, m->max_pages};
+    // (1) RMSNorm -> fp16 -> QKV GEMM -> RoPE + fp16 K/V append per row
+    LK(K_QKV, launch_rmsnorm_rows(x, n, H, H, P.attn_norm, m->eps, m->pf_a, H, s));
+    PgArgs g{};
+    g.w = P.qkv;
+    g.x = m->pf_a;
+    g.kx = H;
+    g.T = n;
+    g.y = m->pf_qkv;
+    g.ldy = qkv_ld;
+    g.status = &m->sp->status;
+    TRY(run_tgemm(m, K_QKV, EPI_STORE, g));
+    LK(K_QKV, launch_rope_kv_batch(m->pf_qkv, n, qkv_ld, m->q_rows, m->kv_rows, kv, m->sp->seq, m->sp->pos, m->rope,
+                                   m->rope_len, m->pf_q, &m->sp->status, s));
+    // (2) split-K attention, one row per sequence
+    AttnArgs a{};
+    a.q = m->pf_q;
+    a.o = m->o;
+    a.k_pool = kv.k_pool;
+    a.v_pool = kv.v_pool;
+    a.page_table = m->pt_dev;
+    a.max_pages = m->max_pages;
+    a.pt_row = m->sp->seq;
+    a.len = m->sp->pos;
+    a.len_add = 1;
+    a.n_heads = m->nh;
+    a.n_kv = m->nkv;
+    a.head_dim = m->hd;
+    a.page_tokens = m->pt;
+    a.n_splits = m->attn_splits_b;
+    a.row0 = 0;
+    a.part_o = m->part_o_b;
+    a.part_ml = m->part_ml_b;
+    a.counters = m->counters_b;
+    a.status = &m->sp->status;
+    a.max_len = m->max_ctx;
+    LK(K_ATTN, launch_attention(a, n, s, false));
+    // (3) O GEMM + residual
+    LK(K_O, launch_to_f16_rows(m->o, n, m->q_rows, m->q_rows, m->pf_a, m->q_rows, s));
+    PgArgs go = g;
+    go.w = P.o;
+    go.kx = m->q_rows;
+    go.y = x;
+    go.ldy = H;
+    TRY(run_tgemm(m, K_O, EPI_RESID, go));
+    // (4) RMSNorm -> gate/up GEMM with SwiGLU -> (5) down GEMM + residual
+    LK(K_GATE_UP, launch_rmsnorm_rows(x, n, H, H, P.ffn_norm, m->eps, m->pf_a, H, s));
+    PgArgs gg = g;
+    gg.w = P.gu;
+    gg.y = nullptr;
+    gg.h = m->pf_h;
+    gg.ldh = m->pf_ldh;
+    TRY(run_tgemm(m, K_GATE_UP, EPI_SWIGLU, gg));
+    PgArgs gd = g;
+    gd.w = P.down;
+    gd.x = m->pf_h;
+    gd.kx = m->pf_ldh;
+    gd.y = x;
+    gd.ldy = H;
+    TRY(run_tgemm(m, K_DOWN, EPI_RESID, gd));
+    if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * H, x, H * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    TRY(layer_end(m, l));
+  }
+  if (head || argmax) {
+    LK(K_HEAD, launch_rmsnorm_rows(x, n, H, H, m->out_norm, m->eps, m->pf_a, H, s));
+    PgArgs gh{};
+    gh.w = head_mat(m);
+    gh.x = m->pf_a;
+    gh.kx = H;
+    gh.T = n;
+    gh.y = m->logits;
+    gh.ldy = m->V;
+    gh.status = &m->sp->status;
+    TRY(run_tgemm(m, K_HEAD, EPI_STORE, gh));
+  }
+  if (argmax)
+    LK(K_ARGMAX, launch_argmax(m->logits, m->V, n, m->next_tok, m->argmax_part, m->argmax_cnt,
+                               argmax_blocks(n, m->num_sms), s, false));
+  return DLS_OK;
+}
+
 int enqueue_persistent(dls_model* m, bool head, bool argmax) {
   StepArgs a{};
   a.layers = m->step_layers;
@@ -615,7 +717,8 @@ int enqueue_step(dls_model* m, int rows, bool head, bool argmax, float* capture)
     m->launches_per_step = m->launch_count;
     return DLS_OK;
   }
-  for (int b = 0; b < rows; ++b) TRY(enqueue_row(m, b, head, argmax, b == 0 ? capture : nullptr));
+  if (rows >= 2) TRY(enqueue_batch(m, rows, head, argmax, capture));
+  else TRY(enqueue_row(m, 0, head, argmax, capture));
   if (argmax) LK(K_ADVANCE, launch_advance(m->sp, m->next_tok, m->tokens_dev, rows, m->stream, m->pdl));
   m->launches_per_step = m->launch_count;
   return DLS_OK;
@@ -1050,12 +1153,22 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   m->pf_cap = std::min(m->max_ctx, kPrefillChunk);
   if (const char* e = getenv("DLS_PREFILL_CHUNK")) m->pf_cap = std::max(1, std::min(m->max_ctx, atoi(e)));
   m->pf_ldh = (m->F + 31) & ~31;
-  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * m->H, &m->pf_x, "prefill_x"));
-  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * std::max(m->H, m->q_rows), &m->pf_a, "prefill_a16"));
-  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * (m->q_rows + 2 * m->kv_rows), &m->pf_qkv, "prefill_qkv"));
-  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * m->q_rows, &m->pf_q, "prefill_q"));
-  TRYC(dev_alloc_t(m, (size_t)m->pf_cap * m->pf_ldh, &m->pf_h, "prefill_h16"));
+  // token-major scratch shared by prefill chunks and batched decode rows
+  const size_t pf_rows = (size_t)std::max(m->pf_cap, B);
+  TRYC(dev_alloc_t(m, pf_rows * m->H, &m->pf_x, "prefill_x"));
+  TRYC(dev_alloc_t(m, pf_rows * std::max(m->H, m->q_rows), &m->pf_a, "prefill_a16"));
+  TRYC(dev_alloc_t(m, pf_rows * (m->q_rows + 2 * m->kv_rows), &m->pf_qkv, "prefill_qkv"));
+  TRYC(dev_alloc_t(m, pf_rows * m->q_rows, &m->pf_q, "prefill_q"));
+  TRYC(dev_alloc_t(m, pf_rows * m->pf_ldh, &m->pf_h, "prefill_h16"));
   TRYC(dev_alloc_t(m, (size_t)m->pf_cap, &m->pf_tok, "prefill_tokens"));
+  if (B > 1) {
+    m->attn_splits_b = attn_default_splits(B, m->nkv, m->num_sms, m->max_ctx);
+    const size_t wsb = attn_workspace_bytes(B, m->nh, m->nkv, m->hd, m->attn_splits_b);
+    TRYC(dev_alloc(m, wsb, &m->attn_ws_b, "attention_scratch_batch"));
+    attn_workspace_carve(m->attn_ws_b, B, m->nh, m->nkv, m->hd, m->attn_splits_b, &m->part_o_b, &m->part_ml_b,
+                         &m->counters_b);
+    CKC(cudaMemsetAsync(m->counters_b, 0, (size_t)B * m->nkv * sizeof(int), m->stream));
+  }
   {
     // split-K partials for batches of up to 16 rows: [split][16][rows]
     const int max_rows = std::max(std::max(m->q_rows + 2 * m->kv_rows, 2 * m->F), m->H);
@@ -1065,7 +1178,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
     CKC(cudaMemsetAsync(m->tg_cnt, 0, (size_t)kTgCounters * sizeof(int), m->stream));
   }
   // columns F .. pf_ldh of h are read by the down GEMM and never written
-  CKC(cudaMemsetAsync(m->pf_h, 0, (size_t)m->pf_cap * m->pf_ldh * sizeof(__half), m->stream));
+  CKC(cudaMemsetAsync(m->pf_h, 0, pf_rows * m->pf_ldh * sizeof(__half), m->stream));
   void* temp = nullptr;
   TRYC(dev_alloc(m, temp_bytes, &temp, "upload_temp"));
 

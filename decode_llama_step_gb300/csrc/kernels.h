@@ -183,6 +183,10 @@ cudaError_t launch_to_f16_rows(const float* x, int T, int cols, int ldx, __half*
 cudaError_t launch_rope_kv_rows(const float* qkv, int T, int ld, int q_rows, int kv_rows, const KvView& kv, int seq,
                                 int pos0, const float2* rope_cs, int rope_len, float* q_out, int32_t* status,
                                 cudaStream_t s);
+// the same for n batch rows, row t being sequence seqs[t] at position poss[t]
+cudaError_t launch_rope_kv_batch(const float* qkv, int n, int ld, int q_rows, int kv_rows, const KvView& kv,
+                                 const int32_t* seqs, const int32_t* poss, const float2* rope_cs, int rope_len,
+                                 float* q_out, int32_t* status, cudaStream_t s);
 // causal attention of T query tokens at positions pos0 .. pos0+T-1 over one
 // sequence (ptab_row = its page-table row); q, o: [T][n_heads][head_dim]
 cudaError_t launch_pattn(const float* q, float* o, const KvView& kv, const int32_t* ptab_row, int n_heads, int T,

@@ -45,8 +45,11 @@ __global__ void to_f16_rows_kernel(const float* x, int cols, int ldx, __half* ou
 // RoPE on the q and k rows of token t at position pos0 + t; q -> q_out
 // (fp32), k and v -> the sequence's pages (fp16)
 __global__ void rope_kv_rows_kernel(const float* qkv, int ld, int q_rows, int kv_rows, KvView kv, int seq, int pos0,
-                                    const float2* rope_cs, int rope_len, float* q_out, int32_t* status) {
-  const int t = blockIdx.x, pos = pos0 + t;
+                                    const int32_t* seqs, const int32_t* poss, const float2* rope_cs, int rope_len,
+                                    float* q_out, int32_t* status) {
+  const int t = blockIdx.x;
+  const int pos = poss ? poss[t] : pos0 + t;
+  if (seqs) seq = seqs[t];
   const float* row = qkv + (size_t)t * ld;
   const int hd = kv.head_dim;
   const int lp = pos / kv.page_tokens;
@@ -278,7 +281,16 @@ cudaError_t launch_to_f16_rows(const float* x, int T, int cols, int ldx, __half*
 cudaError_t launch_rope_kv_rows(const float* qkv, int T, int ld, int q_rows, int kv_rows, const KvView& kv, int seq,
                                 int pos0, const float2* rope_cs, int rope_len, float* q_out, int32_t* status,
                                 cudaStream_t s) {
-  rope_kv_rows_kernel<<<T, 256, 0, s>>>(qkv, ld, q_rows, kv_rows, kv, seq, pos0, rope_cs, rope_len, q_out, status);
+  rope_kv_rows_kernel<<<T, 256, 0, s>>>(qkv, ld, q_rows, kv_rows, kv, seq, pos0, nullptr, nullptr, rope_cs, rope_len,
+                                        q_out, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_kv_batch(const float* qkv, int n, int ld, int q_rows, int kv_rows, const KvView& kv,
+                                 const int32_t* seqs, const int32_t* poss, const float2* rope_cs, int rope_len,
+                                 float* q_out, int32_t* status, cudaStream_t s) {
+  rope_kv_rows_kernel<<<n, 256, 0, s>>>(qkv, ld, q_rows, kv_rows, kv, 0, 0, seqs, poss, rope_cs, rope_len, q_out,
+                                        status);
   return cudaGetLastError();
 }
 

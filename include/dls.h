@@ -171,7 +171,11 @@ int dls_decode_step(dls_model* m, int32_t seq, int32_t token, int32_t pos, float
 
 /* n decode steps in one pass over the weights (1 <= n <= max_batch): row i
  * is token tokens[i] of sequence seqs[i] at position pos[i] (host arrays;
- * distinct sequences).  logits_out: host or device fp32 [n][vocab] or NULL. */
+ * distinct sequences).  logits_out: host or device fp32 [n][vocab] or NULL.
+ * With n >= 2 every projection is one tensor-core GEMM over the n rows
+ * (fp16 operands as in dls_prefill, fp32 accumulation), so each weight byte
+ * is read once per step for the whole batch (SwarmKV, section 4: the
+ * branches of a fork decode together); n = 1 is dls_decode_step. */
 int dls_decode_batch(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* tokens, const int32_t* pos,
                      float* logits_out);
 

@@ -230,6 +230,39 @@ def test_decode_batch_equals_single_steps(setup):
             m.seq_free(s)
 
 
+def test_generate_batch_matches_oracle(setup):
+    # three sequences of different lengths decode together on the tensor-core
+    # path; every step's token is the oracle's greedy token while the
+    # oracle's top-2 gap exceeds 1e-2
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    lens = (9, 33, 20)
+    seqs = [m.seq_create() for _ in lens]
+    try:
+        oseqs, toks0 = [], []
+        for i, (s, n) in enumerate(zip(seqs, lens)):
+            prompt = synth.prompt_tokens(cfg, n, seed=40 + i)
+            m.prefill(s, prompt)
+            oseq = orc.new_seq()
+            toks0.append(int(np.argmax(orc.prefill(oseq, prompt))))
+            oseqs.append(oseq)
+        last = torch.empty(len(lens), cfg.vocab, device="cuda")
+        toks = m.generate(seqs, toks0, 10, last)
+        for i, oseq in enumerate(oseqs):
+            otoks, ologits = orc.greedy_decode(oseq, toks0[i], 10)
+            for t in range(10):
+                if ops.top2_gap(ologits[t]) <= 1e-2:
+                    break
+                assert toks[t, i] == otoks[t], f"row {i} step {t}"
+            else:
+                assert_close(last[i].cpu().numpy(), ologits[-1], f"row {i} final logits")
+        for s, n in zip(seqs, lens):
+            assert m.seq_length(s) == n + 10
+    finally:
+        for s in seqs:
+            m.seq_free(s)
+
+
 def test_kv_fork_bit_exact_and_continues(setup):
     torch = _torch()
     cfg, w, m, orc, stream = setup
