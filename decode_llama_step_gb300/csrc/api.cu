@@ -25,7 +25,7 @@ size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 // prompt tokens per prefill pass (bounded scratch; longer prompts run in chunks)
 constexpr int kPrefillChunk = 2048;
 // split-K limits of the tensor-core GEMM at batch sizes <= 16
-constexpr int kTgMaxSplit = 8;
+constexpr int kTgMaxSplit = 16;
 constexpr int kTgCounters = 4096;
 
 struct MatOff {

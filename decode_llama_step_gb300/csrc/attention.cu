@@ -282,7 +282,7 @@ void attn_workspace_carve(void* ws, int rows, int n_heads, int n_kv, int head_di
 int attn_default_splits(int rows, int n_kv, int num_sms, int max_len) {
   const int tiles = (max_len + TILE - 1) / TILE;
   int s = (tiles + 3) / 4;  // about one tile per slot
-  const int cap = (2 * num_sms + rows * n_kv - 1) / (rows * n_kv);
+  const int cap = (4 * num_sms + rows * n_kv - 1) / (rows * n_kv);
   if (s > cap) s = cap;
   if (s > kMaxSplits) s = kMaxSplits;  // merge weights live in shared memory
   if (s < 1) s = 1;

@@ -15,11 +15,13 @@
 //             the dequantising reads bank-conflict free) and their scales.
 //   warp 1    owns the tensor memory; one thread issues 4 MMAs (K = 16) per
 //             step and commits them to the barriers that free the stage.
-//   warps 2-5 dequantise: thread r turns row r's 64 codes into fp16(d * q)
-//             (packed half2 arithmetic, one rounding, bit-identical to
-//             rounding the exact fp32 product) and writes them swizzled as
-//             the MMA's A operand; afterwards they read the accumulators
-//             (tcgen05.ld) and run the epilogue.
+//   warps 2-9 dequantise: two threads per weight row, each turning 32 of
+//             the row's 64 codes into fp16(d * q) (packed half2 arithmetic,
+//             one rounding, bit-identical to rounding the exact fp32
+//             product) and writing them swizzled as the MMA's A operand;
+//             afterwards they read the accumulators (tcgen05.ld; two warps
+//             per 32-lane quarter of tensor memory, each half the columns)
+//             and run the epilogue.
 // Every wait is bounded (2 s); a wait that gives up sets an abort flag that
 // all roles see, the kernel stores nothing and reports kTimeout.
 #include <cuda.h>
@@ -34,7 +36,9 @@ namespace dls {
 namespace {
 
 constexpr int GBM = 128, GBK = 64;
-constexpr int GTHREADS = 192;
+constexpr int GTHREADS = 320;
+constexpr int NDQ = 8;  // dequantising / epilogue warps
+constexpr int kSplitMax = 16;  // K splits of one tile (the partial sums are added in registers)
 constexpr int kATile = GBM * GBK * 2;  // 16 KB fp16 A operand per stage
 constexpr int kScaleBox = GBM * 16;    // 8 fp16 scales per row
 constexpr uint64_t kWaitNsG = 2000000000ull;
@@ -44,8 +48,10 @@ struct GCfg {
   static constexpr int kCodes = WT == 8 ? GBM * 64 : GBM * 32;
   static constexpr int kB = BN * 128;
   static constexpr int kStage = kB + kCodes + kScaleBox;  // bytes the TMA lands per stage
-  static constexpr int NR = BN >= 256 ? 4 : BN >= 128 ? 5 : 6;
-  static constexpr int NA = 2;
+  // small batches: two CTAs per SM (<= 113 KB each), one streaming while
+  // the other starts up or finishes
+  static constexpr int NR = BN >= 256 ? 4 : BN >= 128 ? 5 : (WT == 8 ? 4 : 6);
+  static constexpr int NA = 3;
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
   static constexpr int kBarOff = NA * kATile + NR * kStage;
   static constexpr int kSmem = kBarOff + 256 + 1024;
@@ -95,48 +101,49 @@ __device__ __forceinline__ void dq4(uint32_t u, __half2 bias, __half2 d, uint32_
   hi = dq2(u, 0x4342u, bias, d);
 }
 
-// Row r of one K step: codes at `qrow` (swizzled by the TMA), scales of the
-// step's two blocks in `dsc`, fp16 output at `arow` (128-byte swizzle).
-// `half_valid`: only the first 32 columns lie inside the matrix.
+// Half hf (columns 32hf .. 32hf+31) of row r of one K step: codes at `qrow`
+// (swizzled by the TMA), scales of the step's two blocks in `dsc`, fp16
+// output at `arow` (128-byte swizzle).  `zero`: these columns lie outside
+// the matrix (the second half of a K step past the last block).
 template <int WT>
-__device__ __forceinline__ void dequant_row(uint32_t qrow, uint32_t dsc, uint32_t arow, int r, bool half_valid) {
+__device__ __forceinline__ void dequant_half(uint32_t qrow, uint32_t dsc, uint32_t arow, int r, int hf, bool zero) {
   const __half2 dh = *reinterpret_cast<const __half2*>(&dsc);
-  const __half2 d0 = __low2half2(dh), d1 = __high2half2(dh);
+  const __half2 d = hf ? __high2half2(dh) : __low2half2(dh);
   const int sw = r & 7;
+  if (zero) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sts128(arow + (((4 * hf + j) ^ sw) << 4), make_uint4(0, 0, 0, 0));
+    return;
+  }
   if (WT == 8) {
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1024 + 128
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {  // 16 codes: columns 16c .. 16c+15
+    for (int cc = 0; cc < 2; ++cc) {  // 16 codes: columns 16c .. 16c+15
+      const int c = 2 * hf + cc;
       const uint4 u = lds128(qrow + ((c ^ ((r >> 1) & 3)) << 4));
-      const __half2 d = c < 2 ? d0 : d1;
       uint4 o0, o1;
       dq4(u.x, bias, d, o0.x, o0.y);
       dq4(u.y, bias, d, o0.z, o0.w);
       dq4(u.z, bias, d, o1.x, o1.y);
       dq4(u.w, bias, d, o1.z, o1.w);
-      if (half_valid && c >= 2) o0 = o1 = make_uint4(0, 0, 0, 0);
       sts128(arow + (((2 * c) ^ sw) << 4), o0);
       sts128(arow + (((2 * c + 1) ^ sw) << 4), o1);
     }
   } else {
     const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1024 + 8
+    // one 16-byte block: low nibbles = columns 0-15, high nibbles = 16-31
+    const uint4 u = lds128(qrow + ((hf ^ ((r >> 2) & 1)) << 4));
+    uint4 o[4];
+    dq4(u.x & 0x0F0F0F0Fu, bias, d, o[0].x, o[0].y);
+    dq4(u.y & 0x0F0F0F0Fu, bias, d, o[0].z, o[0].w);
+    dq4(u.z & 0x0F0F0F0Fu, bias, d, o[1].x, o[1].y);
+    dq4(u.w & 0x0F0F0F0Fu, bias, d, o[1].z, o[1].w);
+    dq4((u.x >> 4) & 0x0F0F0F0Fu, bias, d, o[2].x, o[2].y);
+    dq4((u.y >> 4) & 0x0F0F0F0Fu, bias, d, o[2].z, o[2].w);
+    dq4((u.z >> 4) & 0x0F0F0F0Fu, bias, d, o[3].x, o[3].y);
+    dq4((u.w >> 4) & 0x0F0F0F0Fu, bias, d, o[3].z, o[3].w);
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {  // one 16-byte block: low nibbles = columns 0-15, high = 16-31
-      const uint4 u = lds128(qrow + ((c ^ ((r >> 2) & 1)) << 4));
-      const __half2 d = c == 0 ? d0 : d1;
-      uint4 o[4];  // columns 0-7, 8-15 (low nibbles of bytes 0-15), 16-23, 24-31 (high nibbles)
-      dq4(u.x & 0x0F0F0F0Fu, bias, d, o[0].x, o[0].y);
-      dq4(u.y & 0x0F0F0F0Fu, bias, d, o[0].z, o[0].w);
-      dq4(u.z & 0x0F0F0F0Fu, bias, d, o[1].x, o[1].y);
-      dq4(u.w & 0x0F0F0F0Fu, bias, d, o[1].z, o[1].w);
-      dq4((u.x >> 4) & 0x0F0F0F0Fu, bias, d, o[2].x, o[2].y);
-      dq4((u.y >> 4) & 0x0F0F0F0Fu, bias, d, o[2].z, o[2].w);
-      dq4((u.z >> 4) & 0x0F0F0F0Fu, bias, d, o[3].x, o[3].y);
-      dq4((u.w >> 4) & 0x0F0F0F0Fu, bias, d, o[3].z, o[3].w);
-      const bool zero = half_valid && c == 1;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sts128(arow + (((4 * c + j) ^ sw) << 4), zero ? make_uint4(0, 0, 0, 0) : o[j]);
-    }
+    for (int j = 0; j < 4; ++j) sts128(arow + (((4 * hf + j) ^ sw) << 4), o[j]);
   }
 }
 
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(GTHREADS) tgemm_kernel(const __grid_constant__
       mbar_init(smem_u32(&sh.rempty[i]), 1);
     }
     for (int i = 0; i < C::NA; ++i) {
-      mbar_init(smem_u32(&sh.afull[i]), 4);
+      mbar_init(smem_u32(&sh.afull[i]), NDQ);
       mbar_init(smem_u32(&sh.aempty[i]), 1);
     }
     mbar_init(smem_u32(&sh.done), 1);
@@ -239,8 +246,8 @@ __global__ void __launch_bounds__(GTHREADS) tgemm_kernel(const __grid_constant__
     }
     __syncwarp();
   } else {
-    // ---------------- dequantise (thread = weight row r of the tile)
-    const int r = tid - 64;
+    // ---------------- dequantise (thread pair per weight row)
+    const int dt = tid - 64, r = dt & (GBM - 1), hf = dt >> 7;
     for (int i = 0; i < nk; ++i) {
       const int s = i % C::NR, ai = i % C::NA;
       if (!gwait(smem_u32(&sh.rfull[s]), (i / C::NR) & 1, &sh.abort)) break;
@@ -249,61 +256,77 @@ __global__ void __launch_bounds__(GTHREADS) tgemm_kernel(const __grid_constant__
       const uint32_t st = rbase + s * C::kStage;
       const uint32_t qrow = st + C::kB + r * (WT == 8 ? 64 : 32);
       const uint32_t dsc = lds32(st + C::kB + C::kCodes + r * 16 + (((kt * 2) & 7) << 1));
-      dequant_row<WT>(qrow, dsc, abase + ai * kATile + r * 128, r, kpad - kt * GBK < GBK);
+      dequant_half<WT>(qrow, dsc, abase + ai * kATile + r * 128, r, hf, hf && kpad - kt * GBK < GBK);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.afull[ai]));
     }
 
-    // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) ..
+    // ---------------- epilogue: warp w reads TMEM lanes 32 * (w % 4) .., half the columns
     const bool waited = gwait(smem_u32(&sh.done), 0, &sh.abort, false);
     const bool ok = __all_sync(0xffffffffu, waited && !*(volatile int*)&sh.abort);
     tc_fence_after();
     const int q = warp & 3;
+    constexpr int CW = BN / 2;                  // columns per warp
+    const int cb = ((warp - 2) >> 2) * CW;       // this warp's first column
     const int m = m0 + q * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + cb;
     if (S == 1) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(taddr + c0, v);
+      for (int c0 = 0; c0 < CW; c0 += 8) {
+        uint32_t v[8];
+        tmem_ld8(taddr + c0, v);
         tmem_wait_ld();
-        if (!ok || n0 + c0 >= a.T) continue;
+        if (!ok || n0 + cb + c0 >= a.T) continue;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) epi_store<EPI>(a, n0 + c0 + j, m, w.rows, __uint_as_float(v[j]));
+        for (int j = 0; j < 8; ++j) epi_store<EPI>(a, n0 + cb + c0 + j, m, w.rows, __uint_as_float(v[j]));
       }
     } else {
       // partial tile -> workspace [S][T][rows]; the last CTA of the tile adds the S parts in order
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(taddr + c0, v);
+      for (int c0 = 0; c0 < CW; c0 += 8) {
+        uint32_t v[8];
+        tmem_ld8(taddr + c0, v);
         tmem_wait_ld();
         if (!ok) continue;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = n0 + c0 + j;
+        for (int j = 0; j < 8; ++j) {
+          const int t = n0 + cb + c0 + j;
           if (t < a.T && m < w.rows) a.part[((size_t)z * a.T + t) * w.rows + m] = __uint_as_float(v[j]);
         }
       }
       __threadfence();
-      named_bar(1, 128);
+      named_bar(1, 32 * NDQ);
       const int tile = blockIdx.y * gridDim.x + blockIdx.x;
       if (tid == 64) {
         const int prev = atomicAdd(&a.counters[tile], 1);
         sh.last = prev == S - 1;
         if (sh.last) a.counters[tile] = 0;  // ready for the next launch
       }
-      named_bar(1, 128);
+      named_bar(1, 32 * NDQ);
       if (sh.last && ok) {
+        // add the S partials in split order; all of a column pair's loads are
+        // issued before the first add (the split count is at most kSplitMax)
         __threadfence();
-        const int tmax = min(BN, a.T - n0);
-        for (int j = 0; j < tmax; ++j) {
-          const int t = n0 + j;
-          float acc = 0.f;
-          if (m < w.rows)
-            for (int zz = 0; zz < S; ++zz) acc += __ldcg(&a.part[((size_t)zz * a.T + t) * w.rows + m]);
-          epi_store<EPI>(a, t, m, w.rows, acc);
+        const int tmax = min(CW, a.T - n0 - cb);
+        for (int j = 0; j < tmax; j += 2) {
+          const int t0 = n0 + cb + j, t1 = t0 + 1;
+          const bool r_ok = m < w.rows, ok1 = j + 1 < tmax;
+          float v0[kSplitMax], v1[kSplitMax];
+#pragma unroll
+          for (int zz = 0; zz < kSplitMax; ++zz) {
+            const bool in = zz < S && r_ok;
+            v0[zz] = in ? __ldcg(&a.part[((size_t)zz * a.T + t0) * w.rows + m]) : 0.f;
+            v1[zz] = in && ok1 ? __ldcg(&a.part[((size_t)zz * a.T + t1) * w.rows + m]) : 0.f;
+          }
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int zz = 0; zz < kSplitMax; ++zz) {
+            acc0 += v0[zz];
+            acc1 += v1[zz];
+          }
+          epi_store<EPI>(a, t0, m, w.rows, acc0);
+          if (ok1) epi_store<EPI>(a, t1, m, w.rows, acc1);
         }
       }
     }
@@ -400,11 +423,21 @@ TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split) {
   const int mt = (rows + GBM - 1) / GBM;
   const int nk = (kpad + GBK - 1) / GBK;
   if (T <= 16) {
-    // decode batch: two CTAs per SM; split K until the grid covers them
+    // decode batch (two CTAs per SM): split K so that the CTAs fill whole
+    // waves; the fewest splits among the best fills, at least 8 K steps each
     p.bn = 16;
-    int s = (2 * num_sms) / mt;
-    s = std::min(s, std::min(max_split, nk / 4));
-    p.split = std::max(1, s);
+    num_sms *= 2;
+    const int smax = std::max(1, std::min(std::min(max_split, kSplitMax), nk / 8));
+    double best = -1.0;
+    p.split = 1;
+    for (int s = 1; s <= smax; ++s) {
+      const int ctas = mt * s;
+      const double fill = (double)ctas / ((double)((ctas + num_sms - 1) / num_sms) * num_sms);
+      if (fill > best + 0.02) {
+        best = fill;
+        p.split = s;
+      }
+    }
   } else {
     // prompt chunk: fewer, wider tiles unless that leaves SMs idle for a wave
     const int t128 = mt * ((T + 127) / 128), t256 = mt * ((T + 255) / 256);

@@ -20,11 +20,16 @@ namespace {
 
 // ---------------------------------------------------------------- row kernels
 
-// out[t] = fp16(rmsnorm(x[t]) * g), zero-padded to ldo columns
+// out[t] = fp16(rmsnorm(x[t]) * g), zero-padded to ldo columns (H % 4 == 0)
 __global__ void rmsnorm_rows_kernel(const float* x, int H, int ldx, const float* g, float eps, __half* out, int ldo) {
-  const float* xr = x + (size_t)blockIdx.x * ldx;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * ldx);
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  const int n4 = H >> 2;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = xr[i];
+    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+  }
   __shared__ float red[32];
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
@@ -33,13 +38,36 @@ __global__ void rmsnorm_rows_kernel(const float* x, int H, int ldx, const float*
   for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
   const float rs = 1.0f / sqrtf(t / (float)H + eps);
   __half* o = out + (size_t)blockIdx.x * ldo;
-  for (int i = threadIdx.x; i < ldo; i += blockDim.x) o[i] = __float2half_rn(i < H ? xr[i] * rs * g[i] : 0.f);
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = xr[i], gg = g4[i];
+    const __half2 a = __floats2half2_rn(v.x * rs * gg.x, v.y * rs * gg.y);
+    const __half2 b = __floats2half2_rn(v.z * rs * gg.z, v.w * rs * gg.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&a);
+    pk.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(o + 4 * i) = pk;
+  }
+  for (int i = H + threadIdx.x; i < ldo; i += blockDim.x) o[i] = __float2half_rn(0.f);
 }
 
+// out[t][0..cols) = fp16(x[t]), zero up to ldo (cols % 4 == 0)
 __global__ void to_f16_rows_kernel(const float* x, int cols, int ldx, __half* out, int ldo) {
-  const float* xr = x + (size_t)blockIdx.x * ldx;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * ldx);
   __half* o = out + (size_t)blockIdx.x * ldo;
-  for (int i = threadIdx.x; i < ldo; i += blockDim.x) o[i] = __float2half_rn(i < cols ? xr[i] : 0.f);
+  for (int i = threadIdx.x; i < (cols >> 2); i += blockDim.x) {
+    const float4 v = xr[i];
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&a);
+    pk.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(o + 4 * i) = pk;
+  }
+  for (int i = cols + threadIdx.x; i < ldo; i += blockDim.x) o[i] = __float2half_rn(0.f);
+}
+
+int row_threads(int elems) {
+  int t = (elems + 31) / 32 * 32;
+  return t < 64 ? 64 : t > 1024 ? 1024 : t;
 }
 
 // RoPE on the q and k rows of token t at position pos0 + t; q -> q_out
@@ -269,28 +297,30 @@ cudaError_t launch_embed_rows(const MatDev& emb, int wtype, const int32_t* token
 
 cudaError_t launch_rmsnorm_rows(const float* x, int T, int H, int ldx, const float* g, float eps, __half* out, int ldo,
                                 cudaStream_t s) {
-  rmsnorm_rows_kernel<<<T, 256, 0, s>>>(x, H, ldx, g, eps, out, ldo);
+  if (H % 4 || ldx % 4 || ldo % 4) return cudaErrorInvalidValue;
+  rmsnorm_rows_kernel<<<T, row_threads(H / 4), 0, s>>>(x, H, ldx, g, eps, out, ldo);
   return cudaGetLastError();
 }
 
 cudaError_t launch_to_f16_rows(const float* x, int T, int cols, int ldx, __half* out, int ldo, cudaStream_t s) {
-  to_f16_rows_kernel<<<T, 256, 0, s>>>(x, cols, ldx, out, ldo);
+  if (cols % 4 || ldx % 4 || ldo % 4) return cudaErrorInvalidValue;
+  to_f16_rows_kernel<<<T, row_threads(cols / 4), 0, s>>>(x, cols, ldx, out, ldo);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rope_kv_rows(const float* qkv, int T, int ld, int q_rows, int kv_rows, const KvView& kv, int seq,
                                 int pos0, const float2* rope_cs, int rope_len, float* q_out, int32_t* status,
                                 cudaStream_t s) {
-  rope_kv_rows_kernel<<<T, 256, 0, s>>>(qkv, ld, q_rows, kv_rows, kv, seq, pos0, nullptr, nullptr, rope_cs, rope_len,
-                                        q_out, status);
+  rope_kv_rows_kernel<<<T, row_threads((q_rows + 2 * kv_rows) / 2), 0, s>>>(
+      qkv, ld, q_rows, kv_rows, kv, seq, pos0, nullptr, nullptr, rope_cs, rope_len, q_out, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rope_kv_batch(const float* qkv, int n, int ld, int q_rows, int kv_rows, const KvView& kv,
                                  const int32_t* seqs, const int32_t* poss, const float2* rope_cs, int rope_len,
                                  float* q_out, int32_t* status, cudaStream_t s) {
-  rope_kv_rows_kernel<<<n, 256, 0, s>>>(qkv, ld, q_rows, kv_rows, kv, 0, 0, seqs, poss, rope_cs, rope_len, q_out,
-                                        status);
+  rope_kv_rows_kernel<<<n, row_threads((q_rows + 2 * kv_rows) / 2), 0, s>>>(qkv, ld, q_rows, kv_rows, kv, 0, 0, seqs,
+                                                                              poss, rope_cs, rope_len, q_out, status);
   return cudaGetLastError();
 }
 
