@@ -33,10 +33,12 @@ import numpy as np  # noqa: E402
 
 METRIC = "decode tok/s, 8B-shape Q8_0 batch 1; achieved HBM GB/s as % of peak"
 
-# ncu DRAM traffic per launch of the dominant kernel (the decode GEMV),
-# from the capture summarised in profiles/gemv_q8_0_8b_decode.md, valid only
-# for the kernel source it was taken on (sha256 prefix of csrc/gemv.cu).
-NCU_TRAFFIC = {"gemv_sha": None, "bytes_per_launch": None}
+# ncu DRAM traffic (read + write) per launch of the dominant kernel (the
+# decode GEMV, averaged over one step's 129 GEMV launches of the 32-layer
+# model), from the capture summarised in profiles/gemv_q8_0_8b_decode.md;
+# valid only for the kernel source it was taken on (sha256 prefix of
+# csrc/gemv.cu).
+NCU_TRAFFIC = {"gemv_sha": "7b7462b1ed7b26b0", "bytes_per_launch": 61900000}
 
 KIND_NAMES = {1: "embed", 2: "gemv_qkv", 3: "attention", 4: "gemv_o", 5: "gemv_gate_up", 6: "gemv_down",
               7: "gemv_head", 8: "argmax", 9: "advance"}
@@ -53,16 +55,203 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=32)
     p.add_argument("--profile-steps", type=int, default=4)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layers", type=int, default=0,
+                   help="keep only the first N layers (small cases for ncu captures; not a bench result)")
+    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream"], default="decode",
+                   help="decode (default, the headline line); the others are secondary measurements: "
+                        "prefill (prompt of --ctx tokens), fork (shared prefix -> 8 branches), "
+                        "stream (70B Q4_0 resident vs a 24 GB device budget)")
     return p.parse_args()
 
 
-def peaks():
+def peaks(key="hbm_gbs"):
+    fallback = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return fallback[key], "fallback"
+
+
+def load_config(name, layers):
+    import dataclasses
+    import synth
+    cfg = synth.get_config(name)
+    if layers:
+        cfg = dataclasses.replace(cfg, n_layers=min(layers, cfg.n_layers))
+    return cfg
+
+
+def prefill_flops(cfg, T, pos0=0):
+    """Algorithmic FLOPs of prefilling T tokens after pos0 cached ones: the
+    projections, causal attention (scores and P V over keys 0..pos), and the
+    LM head of the last token."""
+    pairs = T * pos0 + T * (T + 1) // 2          # (query, key) pairs
+    att = 2 * 2 * cfg.n_heads * cfg.head_dim * pairs
+    return cfg.n_layers * (2 * cfg.layer_params() * T + att) + 2 * cfg.vocab * cfg.hidden
+
+
+def _events(torch, stream, fn):
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1000.0
+
+
+def base_line(metric, value, unit, steps, warmup, ms, workload, extra):
+    line = {"metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": 1, "steps": steps,
+            "warmup": warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": {"workload": workload}}
+    line.update(extra)
+    return line
+
+
+def run_prefill(args):
+    """Prompt processing: --steps prefills of --ctx tokens, each on a fresh sequence."""
+    import torch
+    import synth
+    from decode_llama_step_gb300 import dls
+    cfg = load_config(args.config, args.layers)
+    w = synth.model_weights(cfg)
+    stream = torch.cuda.Stream()
+    m = dls.Model(cfg, w, max_seqs=2, max_ctx=args.ctx + 8, stream=stream)
+    del w
+    prompt = synth.prompt_tokens(cfg, args.ctx, seed=1)
+    for _ in range(max(args.warmup, 1)):
+        s = m.seq_create()
+        m.prefill(s, prompt)
+        m.seq_free(s)
+    times = []
+    with ClockSampler(0) as clk:
+        for _ in range(args.steps):
+            s = m.seq_create()
+            times.append(_events(torch, stream, lambda: m.prefill(s, prompt)))
+            m.seq_free(s)
+    t = sum(times) / len(times)
+    fl = prefill_flops(cfg, args.ctx)
+    peak, src = peaks("bf16_tflops")
+    m.close()
+    return base_line(f"prefill tok/s, {cfg.name}-shape {'Q8_0' if cfg.wtype == 8 else 'Q4_0'}", args.ctx / t,
+                     "tok/s", args.steps, args.warmup, 1000 * t,
+                     f"{cfg.name} prefill of a {args.ctx}-token prompt (seeded ids) on an empty sequence",
+                     {"tensor": {"flops_per_prefill": fl, "achieved_tflops": round(fl / t / 1e12, 1),
+                                 "peak_tflops": peak, "frac": round(fl / t / 1e12 / peak, 4),
+                                 "peak_source": f"{src} bf16_tflops (fp16 operands run at the bf16 rate)"},
+                      "clocks": clk.summary()})
+
+
+def run_fork(args):
+    """Shared-prefix fork: one prefill of the prefix, a KV fork into 8
+    branches and batch-8 greedy decode, against 8 independent prefills of
+    the prefix followed by the same decode."""
+    import torch
+    import synth
+    from decode_llama_step_gb300 import dls
+    cfg = load_config("fork8b", args.layers)
+    P, B, D = cfg.workload["prefix"], cfg.workload["branches"], cfg.workload["decode"]
+    w = synth.model_weights(cfg)
+    stream = torch.cuda.Stream()
+    m = dls.Model(cfg, w, max_seqs=B + 1, max_ctx=P + D + 8, max_batch=B, page_tokens=64, stream=stream)
+    del w
+    prefix = synth.prompt_tokens(cfg, P, seed=1)
+    start = [100 + b for b in range(B)]
+    s = m.seq_create()
+    m.prefill(s, prefix[:256])
+    m.generate([s], [1], 2)
+    m.seq_free(s)
+    with ClockSampler(0) as clk:
+        src = m.seq_create()
+        t_pre = _events(torch, stream, lambda: m.prefill(src, prefix))
+        dsts = [m.seq_create() for _ in range(B)]
+        t_fork = _events(torch, stream, lambda: m.kv_fork(src, dsts))
+        m.generate(dsts, start, 2)  # capture the batch-8 graph outside the timing
+        for d in dsts:
+            m.seq_free(d)
+        dsts = [m.seq_create() for _ in range(B)]
+        m.kv_fork(src, dsts)
+        t_dec = _events(torch, stream, lambda: m.generate(dsts, start, D))
+        for d in dsts:
+            m.seq_free(d)
+        m.seq_free(src)
+        # the same branches from 8 independent prefills
+        t_ind = 0.0
+        seqs = []
+        for b in range(B):
+            q = m.seq_create()
+            t_ind += _events(torch, stream, lambda: m.prefill(q, prefix))
+            seqs.append(q)
+    kv_bytes = cfg.n_layers * 2 * P * cfg.kv_dim * 2
+    fork_path = t_pre + t_fork + t_dec
+    indep_path = t_ind + t_dec
+    m.close()
+    return base_line("shared-prefix fork: branch tokens/s of prefill + fork + batch-8 decode, 8B-shape Q4_0",
+                     B * D / fork_path, "tok/s", D, 2, 1000 * t_dec / D,
+                     f"fork8b: prefix {P} -> {B} branches x {D} greedy tokens, batch {B}",
+                     {"fork": {"prefill_ms": round(1000 * t_pre, 2), "prefill_tok_s": round(P / t_pre, 1),
+                               "fork_ms": round(1000 * t_fork, 3),
+                               "fork_copy_gbs": round(2 * B * kv_bytes / t_fork / 1e9, 1),
+                               "decode_ms": round(1000 * t_dec, 2), "decode_tok_s": round(B * D / t_dec, 1),
+                               "fork_path_s": round(fork_path, 4), "independent_prefills_path_s": round(indep_path, 4),
+                               "speedup_vs_independent": round(indep_path / fork_path, 3)},
+                      "clocks": clk.summary()})
+
+
+def h2d_peak(torch, chunk=256 << 20, inflight=4, reps=10):
+    """Best pinned host -> device copy rate: 256 MB chunks, several in flight."""
+    host = torch.empty(chunk * inflight, dtype=torch.uint8, pin_memory=True)
+    dev = torch.empty(chunk * inflight, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    best = 0.0
+    for _ in range(reps):
+        def go():
+            with torch.cuda.stream(s):
+                for i in range(inflight):
+                    dev[i * chunk:(i + 1) * chunk].copy_(host[i * chunk:(i + 1) * chunk], non_blocking=True)
+        t = _events(torch, s, go)
+        best = max(best, chunk * inflight / t / 1e9)
+    return best
+
+
+def run_stream(args):
+    """70B Q4_0 decode at KV length --ctx (default 4096): all layers resident
+    vs a 24 GB device budget (the layers that do not fit stream from pinned
+    host memory through two device buffers)."""
+    import torch
+    import synth
+    from decode_llama_step_gb300 import dls
+    cfg = synth.get_config("70b")
+    ctx = args.ctx if args.ctx != 2048 else cfg.workload["ctx"]
+    D = min(args.steps, cfg.workload["decode"])
+    w = synth.model_weights(cfg)
+    stream = torch.cuda.Stream()
+    peak_h2d = h2d_peak(torch)
+    prompt = synth.prompt_tokens(cfg, ctx, seed=1)
+    out = {}
+    for label, budget in (("resident", 0), ("budget_24GB", cfg.workload["budget_bytes"])):
+        m = dls.Model(cfg, w, max_seqs=1, max_ctx=ctx + D + 16, stream=stream, device_budget_bytes=budget)
+        s = m.seq_create()
+        t_pre = _events(torch, stream, lambda: m.prefill(s, prompt))
+        m.generate([s], [1], 2)
+        with ClockSampler(0) as clk:
+            t = _events(torch, stream, lambda: m.generate([s], [1], D))
+        res = m.resident_layers()
+        streamed_bytes = (cfg.n_layers - res) * m.layer_bytes()
+        out[label] = {"resident_layers": res, "decode_tok_s": round(D / t, 3), "ms_per_token": round(1000 * t / D, 2),
+                      "prefill_s": round(t_pre, 2), "h2d_bytes_per_token": streamed_bytes,
+                      "h2d_gbs": round(streamed_bytes / (t / D) / 1e9, 1) if streamed_bytes else None,
+                      "h2d_frac_of_peak": round(streamed_bytes / (t / D) / 1e9 / peak_h2d, 4) if streamed_bytes else None,
+                      "clocks": clk.summary()}
+        m.close()
+    del w
+    b = out["budget_24GB"]
+    return base_line("70B-shape Q4_0 decode tok/s with a 24 GB device budget (layer streaming)", b["decode_tok_s"],
+                     "tok/s", D, 2, b["ms_per_token"], f"70b Q4_0, KV ctx {ctx}, {D} greedy tokens",
+                     {"stream": out, "h2d_peak_gbs": round(peak_h2d, 1),
+                      "h2d_peak_how": "pinned cudaMemcpyAsync, 4 x 256 MB in flight, best of 10"})
 
 
 def gemv_bytes(rows, cols, wtype):
@@ -199,6 +388,12 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "decode":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        fn = {"prefill": run_prefill, "fork": run_fork, "stream": run_stream}[args.workload]
+        print(json.dumps(fn(args)), flush=True)
+        return 0
 
     import torch
 
@@ -214,7 +409,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    cfg = synth.get_config(args.config)
+    cfg = load_config(args.config, args.layers)
     t0 = time.time()
     w = synth.model_weights(cfg)
     gen_s = time.time() - t0
@@ -305,7 +500,8 @@ def main():
     line = {"metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": f"Llama-3.1-8B-shape Q8_0 batch-1 greedy decode, KV ctx {ctx0}..{ctx0 + args.steps}",
+            "config": {"workload": f"{cfg.name}-shape {'Q8_0' if cfg.wtype == 8 else 'Q4_0'} batch-1 greedy decode, "
+                                   f"{cfg.n_layers} layers, KV ctx {ctx0}..{ctx0 + args.steps}",
                        "ctx": args.ctx, "batch": 1, "weights": "seeded N(0,0.02), quantised Q8_0",
                        "l2": "no flush: 8.2 GB of weights per step > 126 MB L2",
                        "parallelism": f"replicas x{world}"},

@@ -522,11 +522,30 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
     TRY(run_tgemm(m, K_QKV, EPI_STORE, g));
     LK(K_QKV, launch_rope_kv_rows(m->pf_qkv, T, qkv_ld, m->q_rows, m->kv_rows, kv, seq, pos0, m->rope, m->rope_len,
                                   m->pf_q, &m->sp->status, s));
-    // (2) causal attention; the output reuses the qkv buffer
-    float* o = m->pf_qkv;
-    LK(K_ATTN, launch_pattn(m->pf_q, o, kv, m->pt_dev + (size_t)seq * m->max_pages, m->nh, T, pos0, s));
+    // (2) causal attention -> fp16 operand of the O projection (tensor cores
+    // for head_dim 64/128; CUDA cores otherwise, through the qkv buffer)
+    if (fattn_supported(m->hd, m->nh / m->nkv, m->pt)) {
+      FattnArgs fa{};
+      fa.q = m->pf_q;
+      fa.n_heads = m->nh;
+      fa.n_kv = m->nkv;
+      fa.head_dim = m->hd;
+      fa.T = T;
+      fa.pos0 = pos0;
+      fa.ptab = m->pt_dev + (size_t)seq * m->max_pages;
+      fa.max_pages = m->max_pages;
+      fa.page_tokens = m->pt;
+      fa.pool_rows = m->n_pages * m->nkv * m->pt;
+      fa.out = m->pf_a;
+      fa.ld_out = m->q_rows;
+      fa.status = &m->sp->status;
+      LK(K_ATTN, launch_fattn(fa, kv.k_pool, kv.v_pool, s));
+    } else {
+      float* o = m->pf_qkv;
+      LK(K_ATTN, launch_pattn(m->pf_q, o, kv, m->pt_dev + (size_t)seq * m->max_pages, m->nh, T, pos0, s));
+      LK(K_O, launch_to_f16_rows(o, T, m->q_rows, m->q_rows, m->pf_a, m->q_rows, s));
+    }
     // (3) O projection + residual
-    LK(K_O, launch_to_f16_rows(o, T, m->q_rows, m->q_rows, m->pf_a, m->q_rows, s));
     PgArgs go = g;
     go.w = P.o;
     go.kx = m->q_rows;
@@ -1088,6 +1107,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   CKC(gemv_setup_attributes());
   CKC(tgemm_setup_attributes());
   CKC(prefill_setup_attributes());
+  CKC(fattn_setup_attributes());
 
   // layouts
   size_t cur = 0;
@@ -1133,6 +1153,10 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   TRYC(dev_alloc_t(m, m->H, &m->out_norm, "output_norm"));
   TRYC(dev_alloc_t(m, (size_t)m->L * m->kv_layer_elems, &m->k_pool, "k_cache"));
   TRYC(dev_alloc_t(m, (size_t)m->L * m->kv_layer_elems, &m->v_pool, "v_cache"));
+  // positions past a sequence's length inside its last page are read (and
+  // given zero weight) by the prefill attention: keep them finite
+  CKC(cudaMemsetAsync(m->k_pool, 0, (size_t)m->L * m->kv_layer_elems * sizeof(__half), m->stream));
+  CKC(cudaMemsetAsync(m->v_pool, 0, (size_t)m->L * m->kv_layer_elems * sizeof(__half), m->stream));
   TRYC(dev_alloc_t(m, (size_t)m->max_seqs * m->max_pages, &m->pt_dev, "page_table"));
   TRYC(dev_alloc_t(m, (size_t)B * m->H, &m->x, "x"));
   TRYC(dev_alloc_t(m, (size_t)B * m->q_rows, &m->q, "q"));

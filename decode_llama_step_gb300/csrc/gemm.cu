@@ -361,8 +361,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1, uint64_t stride1,
-            uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+}  // namespace
+
+bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+                  uint64_t stride1, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {dim0, dim1};
@@ -372,6 +374,8 @@ bool map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 using TgFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const PgArgs);
 
@@ -460,11 +464,11 @@ cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, c
   if (!f) return cudaErrorInvalidValue;
   CUtensorMap tx, tq, td;
   const uint64_t rb = wtype == 8 ? (uint64_t)w.nb * 32 : (uint64_t)w.nb * 16;
-  if (!map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, (uint64_t)a.kx, (uint64_t)a.T, (uint64_t)a.kx * 2, GBK,
+  if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, (uint64_t)a.kx, (uint64_t)a.T, (uint64_t)a.kx * 2, GBK,
               (uint32_t)p.bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.qs, rb, (uint64_t)w.rows, rb, wtype == 8 ? 64 : 32, GBM,
+      !make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.qs, rb, (uint64_t)w.rows, rb, wtype == 8 ? 64 : 32, GBM,
               wtype == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B) ||
-      !map_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w.d, (uint64_t)w.ds, (uint64_t)w.rows, (uint64_t)w.ds * 2, 8, GBM,
+      !make_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w.d, (uint64_t)w.ds, (uint64_t)w.rows, (uint64_t)w.ds * 2, 8, GBM,
               CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   dim3 grid((a.T + p.bn - 1) / p.bn, (w.rows + GBM - 1) / GBM, p.split);

@@ -1,6 +1,7 @@
 // Host-side launchers of the library's kernels (one declaration per kernel
 // family); the runtime in api.cu composes them into the decode step.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -191,6 +192,28 @@ cudaError_t launch_rope_kv_batch(const float* qkv, int n, int ld, int q_rows, in
 // sequence (ptab_row = its page-table row); q, o: [T][n_heads][head_dim]
 cudaError_t launch_pattn(const float* q, float* o, const KvView& kv, const int32_t* ptab_row, int n_heads, int T,
                          int pos0, cudaStream_t s);
+
+// 2-D tiled tensor map (row-major, dim0 contiguous; strides in bytes)
+bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+                  uint64_t stride1, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw);
+
+// ---- prefill attention on the tensor cores ---------------------------------------
+
+struct FattnArgs {
+  const float* q;            // [T][n_heads][head_dim] fp32 (RoPE applied)
+  int n_heads, n_kv, head_dim;
+  int T, pos0;               // query tokens at positions pos0 .. pos0+T-1
+  const int32_t* ptab;       // the sequence's page-table row
+  int max_pages, page_tokens;
+  int pool_rows;             // rows of head_dim in one layer's K (or V) pool: n_pages * n_kv * page_tokens
+  __half* out;               // [T][ld_out] fp16, head h at columns h * head_dim
+  int ld_out;
+  int32_t* status;
+};
+
+bool fattn_supported(int head_dim, int g, int page_tokens);
+cudaError_t fattn_setup_attributes();
+cudaError_t launch_fattn(const FattnArgs& a, const __half* k_pool, const __half* v_pool, cudaStream_t s);
 
 // Record a failure for dls_last_error(NULL) (calls without a model) and
 // return `code`.

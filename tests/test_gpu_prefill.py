@@ -25,9 +25,11 @@ TINY = synth.get_config("tiny")
 # hidden 224 and ffn 720 end in half a 64-column K tile; ffn, vocab and q
 # rows end in partial 128-row tiles; hidden != n_heads * head_dim
 RAGGED = ModelConfig("ragged", 2, 224, 4, 2, 64, 720, 1000, 10000.0, 8, 0.02)
-# Q4_0, head_dim 32, 4 query heads per KV head
+# Q4_0, head_dim 32 (CUDA-core prefill attention), 4 query heads per KV head
 RAGGED_Q4 = ModelConfig("raggedq4", 2, 224, 8, 2, 32, 720, 1000, 10000.0, 4, 0.02)
-CFGS = [TINY, RAGGED, RAGGED_Q4]
+# head_dim 128 with 4 query heads per KV head (the 8B attention shape), 256-token pages
+WIDE = ModelConfig("wide", 2, 256, 8, 2, 128, 512, 512, 500000.0, 8, 0.02)
+CFGS = [(TINY, 32), (RAGGED, 32), (RAGGED_Q4, 32), (WIDE, 256)]
 
 
 def _torch():
@@ -35,7 +37,7 @@ def _torch():
     return torch
 
 
-def _make(cfg, w, chunk=None, **kw):
+def _make(cfg, w, chunk=None, page_tokens=32, **kw):
     from decode_llama_step_gb300 import dls
     torch = _torch()
     old = os.environ.get("DLS_PREFILL_CHUNK")
@@ -43,7 +45,7 @@ def _make(cfg, w, chunk=None, **kw):
         os.environ["DLS_PREFILL_CHUNK"] = str(chunk)
     try:
         stream = torch.cuda.Stream()
-        m = dls.Model(cfg, w, max_seqs=4, max_ctx=kw.get("max_ctx", 200), max_batch=1, page_tokens=32,
+        m = dls.Model(cfg, w, max_seqs=4, max_ctx=kw.get("max_ctx", 200), max_batch=1, page_tokens=page_tokens,
                       stream=stream)
     finally:
         if old is None:
@@ -53,11 +55,11 @@ def _make(cfg, w, chunk=None, **kw):
     return m, stream
 
 
-@pytest.fixture(scope="module", params=CFGS, ids=[c.name for c in CFGS])
+@pytest.fixture(scope="module", params=CFGS, ids=[f"{c.name}-pt{pt}" for c, pt in CFGS])
 def setup(request, gpu_lib):
-    cfg = request.param
+    cfg, pt = request.param
     w = synth.model_weights(cfg)
-    m, stream = _make(cfg, w, chunk=48)   # several chunks per prompt below
+    m, stream = _make(cfg, w, chunk=48, page_tokens=pt)   # several chunks per prompt below
     orc = OracleModel(cfg, w)
     yield cfg, w, m, orc, stream
     m.close()
