@@ -55,6 +55,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=32)
     p.add_argument("--profile-steps", type=int, default=4)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-region", action="store_true",
+                   help="bracket the timed decode region with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     p.add_argument("--layers", type=int, default=0,
                    help="keep only the first N layers (small cases for ncu captures; not a bench result)")
     p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream"], default="decode",
@@ -438,10 +440,14 @@ def main():
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        if args.profile_region:
+            torch.cuda.profiler.start()
         start.record(stream)
         toks = m.generate([seq], [tok], args.steps)
         end.record(stream)
         end.synchronize()
+        if args.profile_region:
+            torch.cuda.profiler.stop()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
