@@ -33,12 +33,11 @@ import numpy as np  # noqa: E402
 
 METRIC = "decode tok/s, 8B-shape Q8_0 batch 1; achieved HBM GB/s as % of peak"
 
-# ncu DRAM traffic (read + write) per launch of the dominant kernel (the
-# decode GEMV, averaged over one step's 129 GEMV launches of the 32-layer
-# model), from the capture summarised in profiles/gemv_q8_0_8b_decode.md;
-# valid only for the kernel source it was taken on (sha256 prefix of
-# csrc/gemv.cu).
-NCU_TRAFFIC = {"gemv_sha": "7b7462b1ed7b26b0", "bytes_per_launch": 61900000}
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch
+# of the dominant kernel, keyed by the sha256 prefix of the source file it
+# was captured on (a changed kernel has no traffic figure until it is
+# captured again); the captures are summarised under profiles/.
+NCU_TRAFFIC = {}
 
 KIND_NAMES = {1: "embed", 2: "gemv_qkv", 3: "attention", 4: "gemv_o", 5: "gemv_gate_up", 6: "gemv_down",
               7: "gemv_head", 8: "argmax", 9: "advance"}
@@ -470,19 +469,32 @@ def main():
         for d, k in zip(kms, kk):
             kinds_ms.setdefault(int(k), []).append(float(d))
     ctx_mid = ctx0 + args.steps // 2
+    ctx_prof = pos - args.profile_steps // 2  # mean KV length of the profiled steps
     gemv_kinds = (2, 4, 5, 6, 7)
     gemv_bytes_total = sum(kind_bytes(cfg, k, ctx_mid) * len(kinds_ms.get(k, [])) for k in gemv_kinds)
     gemv_ms_total = sum(sum(kinds_ms.get(k, [])) for k in gemv_kinds)
     gemv_launches = sum(len(kinds_ms.get(k, [])) for k in gemv_kinds)
     peak, peak_src = peaks()
     achieved = gemv_bytes_total / (gemv_ms_total / 1000.0) / 1e9 if gemv_ms_total else 0.0
-    src_sha = hashlib.sha256(open(os.path.join(ROOT, "decode_llama_step_gb300", "csrc", "gemv.cu"), "rb").read()).hexdigest()[:16]
-    traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["gemv_sha"] == src_sha else None
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": "dequant-GEMV (QKV, O, gate/up, down, LM head launches of one step)",
+    persistent = launches == 1
+    if persistent:
+        # one cooperative launch per token: the step kernel is the whole
+        # step; its duration is the span of its phase timestamps
+        kern_ms = sum(sum(v) for v in kinds_ms.values()) / max(args.profile_steps, 1)
+        kern_b = step_bytes(cfg, ctx_prof)
+        src = "step.cu"
+        achieved = kern_b / (kern_ms / 1000.0) / 1e9 if kern_ms else 0.0
+        kern = {"kernel": "persistent decode-step kernel (embedding, 32 layers, LM head, greedy pick in one launch)",
+                "bytes_per_launch": kern_b, "avg_launch_us": round(1000.0 * kern_ms, 2)}
+    else:
+        src = "gemv.cu"
+        kern = {"kernel": "dequant-GEMV (QKV, O, gate/up, down, LM head launches of one step)",
                 "bytes_per_launch": round(gemv_bytes_total / max(gemv_launches, 1)),
-                "avg_launch_us": round(1000.0 * gemv_ms_total / max(gemv_launches, 1), 2),
+                "avg_launch_us": round(1000.0 * gemv_ms_total / max(gemv_launches, 1), 2)}
+    src_sha = hashlib.sha256(open(os.path.join(ROOT, "decode_llama_step_gb300", "csrc", src), "rb").read()).hexdigest()[:16]
+    traffic = NCU_TRAFFIC.get(src_sha)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic, **kern,
                 "peak_source": f"{peak_src} (MEMORY copy, hbm_gbs)"}
     step_b = step_bytes(cfg, ctx_mid)
     whole = step_b / (ms_per_step / 1000.0) / 1e9

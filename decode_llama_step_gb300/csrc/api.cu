@@ -136,7 +136,8 @@ struct dls_model {
   // prefill scratch for chunks of up to pf_cap tokens (tensor-core path)
   int pf_cap = 0, pf_ldh = 0;
   float *pf_x = nullptr, *pf_qkv = nullptr, *pf_q = nullptr;
-  __half *pf_a = nullptr, *pf_h = nullptr;
+  __half *pf_a = nullptr, *pf_h = nullptr;        // fp16 GEMM operands (hi planes)
+  __half *pf_a_lo = nullptr, *pf_h_lo = nullptr;  // their lo planes (fp16 of the rounding residual)
   int32_t* pf_tok = nullptr;
   // batched decode (2..max_batch rows): attention scratch for that many rows
   void* attn_ws_b = nullptr;
@@ -163,6 +164,7 @@ struct dls_model {
   int2* step_am = nullptr;
   unsigned* step_bar = nullptr;  // [0] barrier counter, [1] abort flag
   unsigned long long* step_trace = nullptr;  // phase timestamps when profiling
+  unsigned long long* step_ctrace = nullptr; // per-CTA phase timestamps when profiling
   // per-kernel timing (dls_debug_profile_step): an event after every launch
   bool profiling = false;
   // programmatic dependent launch between the step's kernels; off by default
@@ -510,10 +512,11 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
     KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
               m->nkv, m->hd, m->pt, m->max_pages};
     // (1) RMSNorm -> fp16 -> QKV GEMM -> RoPE, fp16 K/V into the pages
-    LK(K_QKV, launch_rmsnorm_rows(m->pf_x, T, H, H, P.attn_norm, m->eps, m->pf_a, H, s));
+    LK(K_QKV, launch_rmsnorm_rows(m->pf_x, T, H, H, P.attn_norm, m->eps, m->pf_a, m->pf_a_lo, H, s));
     PgArgs g{};
     g.w = P.qkv;
     g.x = m->pf_a;
+    g.xlo = m->pf_a_lo;
     g.kx = H;
     g.T = T;
     g.y = m->pf_qkv;
@@ -537,13 +540,14 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
       fa.page_tokens = m->pt;
       fa.pool_rows = m->n_pages * m->nkv * m->pt;
       fa.out = m->pf_a;
+      fa.out_lo = m->pf_a_lo;
       fa.ld_out = m->q_rows;
       fa.status = &m->sp->status;
       LK(K_ATTN, launch_fattn(fa, kv.k_pool, kv.v_pool, s));
     } else {
       float* o = m->pf_qkv;
       LK(K_ATTN, launch_pattn(m->pf_q, o, kv, m->pt_dev + (size_t)seq * m->max_pages, m->nh, T, pos0, s));
-      LK(K_O, launch_to_f16_rows(o, T, m->q_rows, m->q_rows, m->pf_a, m->q_rows, s));
+      LK(K_O, launch_to_f16_rows(o, T, m->q_rows, m->q_rows, m->pf_a, m->pf_a_lo, m->q_rows, s));
     }
     // (3) O projection + residual
     PgArgs go = g;
@@ -553,17 +557,19 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
     go.ldy = H;
     TRY(run_tgemm(m, K_O, EPI_RESID, go));
     // (4) RMSNorm -> fp16 -> gate/up GEMM with SwiGLU -> fp16 h
-    LK(K_GATE_UP, launch_rmsnorm_rows(m->pf_x, T, H, H, P.ffn_norm, m->eps, m->pf_a, H, s));
+    LK(K_GATE_UP, launch_rmsnorm_rows(m->pf_x, T, H, H, P.ffn_norm, m->eps, m->pf_a, m->pf_a_lo, H, s));
     PgArgs gg = g;
     gg.w = P.gu;
     gg.y = nullptr;
     gg.h = m->pf_h;
+    gg.hlo = m->pf_h_lo;
     gg.ldh = m->pf_ldh;
     TRY(run_tgemm(m, K_GATE_UP, EPI_SWIGLU, gg));
     // (5) down GEMM + residual
     PgArgs gd = g;
     gd.w = P.down;
     gd.x = m->pf_h;
+    gd.xlo = m->pf_h_lo;
     gd.kx = m->pf_ldh;
     gd.y = m->pf_x;
     gd.ldy = H;
@@ -604,10 +610,11 @@ int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
     KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
               m->nkv, m->hd, m->pt, m->max_pages};
     // (1) RMSNorm -> fp16 -> QKV GEMM -> RoPE + fp16 K/V append per row
-    LK(K_QKV, launch_rmsnorm_rows(x, n, H, H, P.attn_norm, m->eps, m->pf_a, H, s));
+    LK(K_QKV, launch_rmsnorm_rows(x, n, H, H, P.attn_norm, m->eps, m->pf_a, m->pf_a_lo, H, s));
     PgArgs g{};
     g.w = P.qkv;
     g.x = m->pf_a;
+    g.xlo = m->pf_a_lo;
     g.kx = H;
     g.T = n;
     g.y = m->pf_qkv;
@@ -640,7 +647,7 @@ int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
     a.max_len = m->max_ctx;
     LK(K_ATTN, launch_attention(a, n, s, false));
     // (3) O GEMM + residual
-    LK(K_O, launch_to_f16_rows(m->o, n, m->q_rows, m->q_rows, m->pf_a, m->q_rows, s));
+    LK(K_O, launch_to_f16_rows(m->o, n, m->q_rows, m->q_rows, m->pf_a, m->pf_a_lo, m->q_rows, s));
     PgArgs go = g;
     go.w = P.o;
     go.kx = m->q_rows;
@@ -648,16 +655,18 @@ int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
     go.ldy = H;
     TRY(run_tgemm(m, K_O, EPI_RESID, go));
     // (4) RMSNorm -> gate/up GEMM with SwiGLU -> (5) down GEMM + residual
-    LK(K_GATE_UP, launch_rmsnorm_rows(x, n, H, H, P.ffn_norm, m->eps, m->pf_a, H, s));
+    LK(K_GATE_UP, launch_rmsnorm_rows(x, n, H, H, P.ffn_norm, m->eps, m->pf_a, m->pf_a_lo, H, s));
     PgArgs gg = g;
     gg.w = P.gu;
     gg.y = nullptr;
     gg.h = m->pf_h;
+    gg.hlo = m->pf_h_lo;
     gg.ldh = m->pf_ldh;
     TRY(run_tgemm(m, K_GATE_UP, EPI_SWIGLU, gg));
     PgArgs gd = g;
     gd.w = P.down;
     gd.x = m->pf_h;
+    gd.xlo = m->pf_h_lo;
     gd.kx = m->pf_ldh;
     gd.y = x;
     gd.ldy = H;
@@ -666,10 +675,11 @@ int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
     TRY(layer_end(m, l));
   }
   if (head || argmax) {
-    LK(K_HEAD, launch_rmsnorm_rows(x, n, H, H, m->out_norm, m->eps, m->pf_a, H, s));
+    LK(K_HEAD, launch_rmsnorm_rows(x, n, H, H, m->out_norm, m->eps, m->pf_a, m->pf_a_lo, H, s));
     PgArgs gh{};
     gh.w = head_mat(m);
     gh.x = m->pf_a;
+    gh.xlo = m->pf_a_lo;
     gh.kx = H;
     gh.T = n;
     gh.y = m->logits;
@@ -722,6 +732,7 @@ int enqueue_persistent(dls_model* m, bool head, bool argmax) {
   a.abort = reinterpret_cast<int*>(m->step_bar + 1);
   a.S = m->step.splits;
   a.trace = m->profiling ? m->step_trace : nullptr;
+  a.ctrace = m->profiling ? m->step_ctrace : nullptr;
   a.ns = m->step.ns;
   a.stage_bytes = m->step.stage_bytes;
   CK(cudaMemsetAsync(m->step_bar, 0, 2 * sizeof(unsigned), m->stream));
@@ -938,6 +949,7 @@ int setup_persistent(dls_model* m) {
     TRY(dev_alloc_t(m, (size_t)m->step.grid, &m->step_am, "step_argmax"));
     TRY(dev_alloc_t(m, (size_t)2, &m->step_bar, "step_barrier"));
     TRY(dev_alloc_t(m, (size_t)(5 * m->L + 8), &m->step_trace, "step_trace"));
+    TRY(dev_alloc_t(m, (size_t)(5 * m->L + 8) * m->step.grid * 4, &m->step_ctrace, "step_cta_trace"));
     CK(cudaMemsetAsync(m->step_att_cnt, 0, m->nkv * sizeof(int), m->stream));
   }
   std::vector<StepLayer> hl(m->L);
@@ -1180,10 +1192,12 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   // token-major scratch shared by prefill chunks and batched decode rows
   const size_t pf_rows = (size_t)std::max(m->pf_cap, B);
   TRYC(dev_alloc_t(m, pf_rows * m->H, &m->pf_x, "prefill_x"));
-  TRYC(dev_alloc_t(m, pf_rows * std::max(m->H, m->q_rows), &m->pf_a, "prefill_a16"));
+  TRYC(dev_alloc_t(m, 2 * pf_rows * std::max(m->H, m->q_rows), &m->pf_a, "prefill_a16"));
+  m->pf_a_lo = m->pf_a + pf_rows * std::max(m->H, m->q_rows);
   TRYC(dev_alloc_t(m, pf_rows * (m->q_rows + 2 * m->kv_rows), &m->pf_qkv, "prefill_qkv"));
   TRYC(dev_alloc_t(m, pf_rows * m->q_rows, &m->pf_q, "prefill_q"));
-  TRYC(dev_alloc_t(m, pf_rows * m->pf_ldh, &m->pf_h, "prefill_h16"));
+  TRYC(dev_alloc_t(m, 2 * pf_rows * m->pf_ldh, &m->pf_h, "prefill_h16"));
+  m->pf_h_lo = m->pf_h + pf_rows * m->pf_ldh;
   TRYC(dev_alloc_t(m, (size_t)m->pf_cap, &m->pf_tok, "prefill_tokens"));
   if (B > 1) {
     m->attn_splits_b = attn_default_splits(B, m->nkv, m->num_sms, m->max_ctx);
@@ -1202,7 +1216,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
     CKC(cudaMemsetAsync(m->tg_cnt, 0, (size_t)kTgCounters * sizeof(int), m->stream));
   }
   // columns F .. pf_ldh of h are read by the down GEMM and never written
-  CKC(cudaMemsetAsync(m->pf_h, 0, pf_rows * m->pf_ldh * sizeof(__half), m->stream));
+  CKC(cudaMemsetAsync(m->pf_h, 0, 2 * pf_rows * m->pf_ldh * sizeof(__half), m->stream));
   void* temp = nullptr;
   TRYC(dev_alloc(m, temp_bytes, &temp, "upload_temp"));
 
@@ -1505,6 +1519,18 @@ int dls_debug_profile_step(dls_model* m, int32_t seq, int32_t token, int32_t pos
   return DLS_OK;
 }
 
+int dls_debug_step_trace(dls_model* m, uint64_t* out, int32_t max_entries, int32_t* n_entries) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (!out || !n_entries || max_entries < 0) return fail(m, DLS_ERR_ARG, "output arrays");
+  if (!m->use_step || !m->step_ctrace) return fail(m, DLS_ERR_STATE, "no persistent step kernel in use");
+  const size_t n = (size_t)(5 * m->L + 8) * m->step.grid * 4;
+  if ((size_t)max_entries < n) return fail(m, DLS_ERR_ARG, "max_entries=%d < %zu", max_entries, n);
+  TRY(sync_stream(m, m->stream));
+  CK(cudaMemcpy(out, m->step_ctrace, n * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+  *n_entries = (int32_t)n;
+  return DLS_OK;
+}
+
 int dls_debug_capture(dls_model* m, float* per_layer_out) {
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
   m->capture = per_layer_out;
@@ -1595,13 +1621,16 @@ int dls_debug_gemm(dls_model* m, int32_t layer, int32_t tensor, int32_t n_tokens
   const MatDev w = pair ? mat_at(m->layer_dev[layer], m->lay.gu) : md;
   const int kx = w.nb * 32;
   void *xh = nullptr, *yt = nullptr;
-  TRY(dev_alloc(m, (size_t)n_tokens * kx * sizeof(__half), &xh, "debug_gemm_x"));
+  TRY(dev_alloc(m, 2 * (size_t)n_tokens * kx * sizeof(__half), &xh, "debug_gemm_x"));
   int r = pair ? dev_alloc(m, (size_t)n_tokens * w.rows * sizeof(float), &yt, "debug_gemm_y") : DLS_OK;
   if (r == DLS_OK) {
-    cudaError_t e = launch_to_f16_rows(x, n_tokens, w.cols, w.cols, static_cast<__half*>(xh), kx, m->stream);
+    __half* xhi = static_cast<__half*>(xh);
+    __half* xlo = xhi + (size_t)n_tokens * kx;
+    cudaError_t e = launch_to_f16_rows(x, n_tokens, w.cols, w.cols, xhi, xlo, kx, m->stream);
     PgArgs g{};
     g.w = w;
-    g.x = static_cast<const __half*>(xh);
+    g.x = xhi;
+    g.xlo = xlo;
     g.kx = kx;
     g.T = n_tokens;
     g.y = pair ? static_cast<float*>(yt) : y;

@@ -307,15 +307,26 @@ __global__ void __launch_bounds__(FTHREADS, 1) fattn_kernel(const __grid_constan
     ok = __all_sync(0xffffffffu, ok && !*(volatile int*)&sh.abort);
     if (ok && row_ok) {
       const float inv = 1.0f / l_run;
-      __half* orow = a.out + (size_t)t * a.ld_out + ((size_t)kvh * G + h) * HD;
+      const size_t off = (size_t)t * a.ld_out + ((size_t)kvh * G + h) * HD;
+      __half* orow = a.out + off;
+      __half* lrow = a.out_lo + off;
 #pragma unroll
       for (int c = 0; c < HD / 8; ++c) {
-        uint4 pk;
+        uint4 pk, pl;
         pk.x = pack_h2(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
         pk.y = pack_h2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
         pk.z = pack_h2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
         pk.w = pack_h2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+        // lo plane: what fp16 rounding dropped
+        const uint32_t* hw = &pk.x;
+        uint32_t* lw = &pl.x;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
+          lw[j] = pack_h2(o[8 * c + 2 * j] * inv - f.x, o[8 * c + 2 * j + 1] * inv - f.y);
+        }
         *reinterpret_cast<uint4*>(orow + 8 * c) = pk;
+        *reinterpret_cast<uint4*>(lrow + 8 * c) = pl;
       }
     }
     if (!ok && a.status && lane == 0) atomicOr(a.status, kTimeout);
@@ -377,7 +388,8 @@ cudaError_t launch_fattn(const FattnArgs& a, const __half* k_pool, const __half*
   const int g = a.n_heads / a.n_kv;
   int smem = 0;
   FaFn f = fa_select(a.head_dim, g, &smem);
-  if (!f || !fattn_supported(a.head_dim, g, a.page_tokens) || a.T < 1 || a.ld_out % 8) return cudaErrorInvalidValue;
+  if (!f || !fattn_supported(a.head_dim, g, a.page_tokens) || a.T < 1 || a.ld_out % 8 || !a.out_lo)
+    return cudaErrorInvalidValue;
   CUtensorMap tk, tv;
   const int pr = a.page_tokens < FBK ? a.page_tokens : FBK;
   if (!make_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k_pool, a.head_dim, a.pool_rows, a.head_dim * 2, 64, pr,

@@ -46,15 +46,17 @@ constexpr uint64_t kWaitNsG = 2000000000ull;
 template <int WT, int BN>
 struct GCfg {
   static constexpr int kCodes = WT == 8 ? GBM * 64 : GBM * 32;
-  static constexpr int kB = BN * 128;
-  static constexpr int kStage = kB + kCodes + kScaleBox;  // bytes the TMA lands per stage
+  static constexpr int kB = BN * 128;                          // one activation plane
+  static constexpr int kStage = 2 * kB + kCodes + kScaleBox;  // bytes the TMA lands per stage: x hi | x lo | codes | scales
   // small batches: two CTAs per SM (<= 113 KB each), one streaming while
   // the other starts up or finishes
-  static constexpr int NR = BN >= 256 ? 4 : BN >= 128 ? 5 : (WT == 8 ? 4 : 6);
-  static constexpr int NA = 3;
+  static constexpr int NR = BN >= 128 ? 3 : (WT == 8 ? 3 : 4);
+  static constexpr int NA = BN >= 128 ? 3 : 2;                // fp16 weight tiles (hi and lo planes)
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
-  static constexpr int kBarOff = NA * kATile + NR * kStage;
+  static constexpr int kBarOff = NA * 2 * kATile + NR * kStage;
   static constexpr int kSmem = kBarOff + 256 + 1024;
+  static_assert(BN >= 128 || kSmem <= 113 * 1024, "two CTAs per SM");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 template <int NR, int NA>
@@ -87,32 +89,42 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   return v;
 }
 
-// two codes (bytes k0, k1 of u as selected) -> fp16(d * q) pair
-__device__ __forceinline__ uint32_t dq2(uint32_t u, uint32_t sel, __half2 bias, __half2 d) {
+// two codes (bytes k0, k1 of u as selected) -> hi = fp16(d * q) and
+// lo = fp16(d * q - hi) pairs.  d * q has at most 19 significant bits, so
+// the fused multiply-add gives the exact residual (lo is representable).
+__device__ __forceinline__ void dq2(uint32_t u, uint32_t sel, __half2 bias, __half2 d, uint32_t& hi, uint32_t& lo) {
   const uint32_t p = __byte_perm(u, 0x64646464u, sel);  // fp16 1024 + byte in each half
   const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&p), bias);
   const __half2 v = __hmul2(q, d);
-  return *reinterpret_cast<const uint32_t*>(&v);
+  const __half2 r = __hfma2(q, d, __hneg2(v));
+  hi = *reinterpret_cast<const uint32_t*>(&v);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// 4 codes of one 32-bit word -> 4 fp16 (two words)
-__device__ __forceinline__ void dq4(uint32_t u, __half2 bias, __half2 d, uint32_t& lo, uint32_t& hi) {
-  lo = dq2(u, 0x4140u, bias, d);
-  hi = dq2(u, 0x4342u, bias, d);
+// 4 codes of one 32-bit word -> 4 fp16 of each plane (two words each)
+__device__ __forceinline__ void dq4(uint32_t u, __half2 bias, __half2 d, uint32_t& h0, uint32_t& h1, uint32_t& l0,
+                                    uint32_t& l1) {
+  dq2(u, 0x4140u, bias, d, h0, l0);
+  dq2(u, 0x4342u, bias, d, h1, l1);
 }
 
 // Half hf (columns 32hf .. 32hf+31) of row r of one K step: codes at `qrow`
 // (swizzled by the TMA), scales of the step's two blocks in `dsc`, fp16
-// output at `arow` (128-byte swizzle).  `zero`: these columns lie outside
-// the matrix (the second half of a K step past the last block).
+// output planes at `arow` (hi) and `arow + kATile` (lo), 128-byte swizzle.
+// `zero`: these columns lie outside the matrix (the second half of a K
+// step past the last block).
 template <int WT>
 __device__ __forceinline__ void dequant_half(uint32_t qrow, uint32_t dsc, uint32_t arow, int r, int hf, bool zero) {
   const __half2 dh = *reinterpret_cast<const __half2*>(&dsc);
   const __half2 d = hf ? __high2half2(dh) : __low2half2(dh);
   const int sw = r & 7;
+  const uint32_t lrow = arow + kATile;
   if (zero) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) sts128(arow + (((4 * hf + j) ^ sw) << 4), make_uint4(0, 0, 0, 0));
+    for (int j = 0; j < 4; ++j) {
+      sts128(arow + (((4 * hf + j) ^ sw) << 4), make_uint4(0, 0, 0, 0));
+      sts128(lrow + (((4 * hf + j) ^ sw) << 4), make_uint4(0, 0, 0, 0));
+    }
     return;
   }
   if (WT == 8) {
@@ -121,29 +133,32 @@ __device__ __forceinline__ void dequant_half(uint32_t qrow, uint32_t dsc, uint32
     for (int cc = 0; cc < 2; ++cc) {  // 16 codes: columns 16c .. 16c+15
       const int c = 2 * hf + cc;
       const uint4 u = lds128(qrow + ((c ^ ((r >> 1) & 3)) << 4));
-      uint4 o0, o1;
-      dq4(u.x, bias, d, o0.x, o0.y);
-      dq4(u.y, bias, d, o0.z, o0.w);
-      dq4(u.z, bias, d, o1.x, o1.y);
-      dq4(u.w, bias, d, o1.z, o1.w);
-      sts128(arow + (((2 * c) ^ sw) << 4), o0);
-      sts128(arow + (((2 * c + 1) ^ sw) << 4), o1);
+      uint4 h0, h1, l0, l1;
+      dq4(u.x, bias, d, h0.x, h0.y, l0.x, l0.y);
+      dq4(u.y, bias, d, h0.z, h0.w, l0.z, l0.w);
+      dq4(u.z, bias, d, h1.x, h1.y, l1.x, l1.y);
+      dq4(u.w, bias, d, h1.z, h1.w, l1.z, l1.w);
+      sts128(arow + (((2 * c) ^ sw) << 4), h0);
+      sts128(arow + (((2 * c + 1) ^ sw) << 4), h1);
+      sts128(lrow + (((2 * c) ^ sw) << 4), l0);
+      sts128(lrow + (((2 * c + 1) ^ sw) << 4), l1);
     }
   } else {
     const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1024 + 8
     // one 16-byte block: low nibbles = columns 0-15, high nibbles = 16-31
     const uint4 u = lds128(qrow + ((hf ^ ((r >> 2) & 1)) << 4));
-    uint4 o[4];
-    dq4(u.x & 0x0F0F0F0Fu, bias, d, o[0].x, o[0].y);
-    dq4(u.y & 0x0F0F0F0Fu, bias, d, o[0].z, o[0].w);
-    dq4(u.z & 0x0F0F0F0Fu, bias, d, o[1].x, o[1].y);
-    dq4(u.w & 0x0F0F0F0Fu, bias, d, o[1].z, o[1].w);
-    dq4((u.x >> 4) & 0x0F0F0F0Fu, bias, d, o[2].x, o[2].y);
-    dq4((u.y >> 4) & 0x0F0F0F0Fu, bias, d, o[2].z, o[2].w);
-    dq4((u.z >> 4) & 0x0F0F0F0Fu, bias, d, o[3].x, o[3].y);
-    dq4((u.w >> 4) & 0x0F0F0F0Fu, bias, d, o[3].z, o[3].w);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) sts128(arow + (((4 * hf + j) ^ sw) << 4), o[j]);
+    for (int j = 0; j < 4; ++j) {  // output chunk j: columns 8j .. 8j+7
+      const uint32_t a = w[(2 * j) & 3], b = w[(2 * j + 1) & 3];
+      const uint32_t sa = j < 2 ? a & 0x0F0F0F0Fu : (a >> 4) & 0x0F0F0F0Fu;
+      const uint32_t sb = j < 2 ? b & 0x0F0F0F0Fu : (b >> 4) & 0x0F0F0F0Fu;
+      uint4 h, l;
+      dq4(sa, bias, d, h.x, h.y, l.x, l.y);
+      dq4(sb, bias, d, h.z, h.w, l.z, l.w);
+      sts128(arow + (((4 * hf + j) ^ sw) << 4), h);
+      sts128(lrow + (((4 * hf + j) ^ sw) << 4), l);
+    }
   }
 }
 
@@ -151,7 +166,12 @@ template <int EPI>
 __device__ __forceinline__ void epi_store(const PgArgs& a, int t, int m, int rows, float v) {
   if (EPI == EPI_SWIGLU) {
     const float up = __shfl_down_sync(0xffffffffu, v, 1);
-    if ((threadIdx.x & 1) == 0 && t < a.T && m + 1 < rows) a.h[(size_t)t * a.ldh + (m >> 1)] = __float2half_rn(silu(v) * up);
+    if ((threadIdx.x & 1) == 0 && t < a.T && m + 1 < rows) {
+      const float hv = silu(v) * up;
+      const __half hh = __float2half_rn(hv);
+      a.h[(size_t)t * a.ldh + (m >> 1)] = hh;
+      a.hlo[(size_t)t * a.ldh + (m >> 1)] = __float2half_rn(hv - __half2float(hh));
+    }
   } else if (t < a.T && m < rows) {
     float* dst = a.y + (size_t)t * a.ldy + m;
     if (EPI == EPI_RESID) *dst += v;
@@ -161,6 +181,7 @@ __device__ __forceinline__ void epi_store(const PgArgs& a, int t, int m, int row
 
 template <int WT, int EPI, int BN>
 __global__ void __launch_bounds__(GTHREADS) tgemm_kernel(const __grid_constant__ CUtensorMap tm_x,
+                                                         const __grid_constant__ CUtensorMap tm_xl,
                                                          const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_d, const PgArgs a) {
   using C = GCfg<WT, BN>;
@@ -168,8 +189,8 @@ __global__ void __launch_bounds__(GTHREADS) tgemm_kernel(const __grid_constant__
   extern __shared__ uint8_t gsm[];
   const uint32_t raw = smem_u32(gsm);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  const uint32_t abase = raw + pad;               // NA fp16 A tiles
-  const uint32_t rbase = abase + C::NA * kATile;  // NR stages: B tile | codes | scales
+  const uint32_t abase = raw + pad;                   // NA fp16 A tiles, each hi plane | lo plane
+  const uint32_t rbase = abase + C::NA * 2 * kATile;  // NR stages: B hi | B lo | codes | scales
   Bars& sh = *reinterpret_cast<Bars*>(gsm + pad + C::kBarOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const MatDev& w = a.w;
@@ -197,6 +218,7 @@ __global__ void __launch_bounds__(GTHREADS) tgemm_kernel(const __grid_constant__
     sh.abort = 0;
     mbar_fence_init();
     prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_xl);
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_d);
   }
@@ -217,8 +239,9 @@ __global__ void __launch_bounds__(GTHREADS) tgemm_kernel(const __grid_constant__
         const int kt = kt0 + i;
         mbar_expect_tx(bar, C::kStage);
         tma_load_2d(st, &tm_x, kt * GBK, n0, bar);
-        tma_load_2d(st + C::kB, &tm_q, kt * (WT == 8 ? 64 : 32), m0, bar);
-        tma_load_2d(st + C::kB + C::kCodes, &tm_d, (kt * 2) & ~7, m0, bar);
+        tma_load_2d(st + C::kB, &tm_xl, kt * GBK, n0, bar);
+        tma_load_2d(st + 2 * C::kB, &tm_q, kt * (WT == 8 ? 64 : 32), m0, bar);
+        tma_load_2d(st + 2 * C::kB + C::kCodes, &tm_d, (kt * 2) & ~7, m0, bar);
         issued = i + 1;
       }
       // copies still in flight (after an abort) land before the CTA exits
@@ -235,10 +258,14 @@ __global__ void __launch_bounds__(GTHREADS) tgemm_kernel(const __grid_constant__
         if (!gwait(smem_u32(&sh.afull[ai]), (i / C::NA) & 1, &sh.abort)) break;
         if (!gwait(smem_u32(&sh.rfull[s]), (i / C::NR) & 1, &sh.abort)) break;
         tc_fence_after();
-        const uint32_t sa = abase + ai * kATile, sb = rbase + s * C::kStage;
+        const uint32_t sa = abase + ai * 2 * kATile, sb = rbase + s * C::kStage;
+        // w x = w_hi x_hi + w_hi x_lo + w_lo x_hi (w_lo x_lo is below fp32 rounding)
 #pragma unroll
-        for (int ks = 0; ks < GBK / 16; ++ks)
+        for (int ks = 0; ks < GBK / 16; ++ks) {
           umma_f16(tmem, umma_desc_k128(sa + ks * 32), umma_desc_k128(sb + ks * 32), idesc, (i | ks) != 0);
+          umma_f16(tmem, umma_desc_k128(sa + ks * 32), umma_desc_k128(sb + C::kB + ks * 32), idesc, true);
+          umma_f16(tmem, umma_desc_k128(sa + kATile + ks * 32), umma_desc_k128(sb + ks * 32), idesc, true);
+        }
         umma_commit(smem_u32(&sh.rempty[s]));
         umma_commit(smem_u32(&sh.aempty[ai]));
       }
@@ -254,9 +281,9 @@ __global__ void __launch_bounds__(GTHREADS) tgemm_kernel(const __grid_constant__
       if (i >= C::NA && !gwait(smem_u32(&sh.aempty[ai]), ((i / C::NA) - 1) & 1, &sh.abort)) break;
       const int kt = kt0 + i;
       const uint32_t st = rbase + s * C::kStage;
-      const uint32_t qrow = st + C::kB + r * (WT == 8 ? 64 : 32);
-      const uint32_t dsc = lds32(st + C::kB + C::kCodes + r * 16 + (((kt * 2) & 7) << 1));
-      dequant_half<WT>(qrow, dsc, abase + ai * kATile + r * 128, r, hf, hf && kpad - kt * GBK < GBK);
+      const uint32_t qrow = st + 2 * C::kB + r * (WT == 8 ? 64 : 32);
+      const uint32_t dsc = lds32(st + 2 * C::kB + C::kCodes + r * 16 + (((kt * 2) & 7) << 1));
+      dequant_half<WT>(qrow, dsc, abase + ai * 2 * kATile + r * 128, r, hf, hf && kpad - kt * GBK < GBK);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.afull[ai]));
@@ -377,7 +404,7 @@ bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint
 
 namespace {
 
-using TgFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const PgArgs);
+using TgFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const PgArgs);
 
 template <int WT, int BN>
 TgFn tg_pick(int epi) {
@@ -403,7 +430,6 @@ TgFn tg_select(int wtype, int epi, int bn, int* smem) {
   switch (bn) {
     case 16: return tg_pick<16>(wtype, epi, smem);
     case 128: return tg_pick<128>(wtype, epi, smem);
-    case 256: return tg_pick<256>(wtype, epi, smem);
   }
   return nullptr;
 }
@@ -413,7 +439,7 @@ TgFn tg_select(int wtype, int epi, int bn, int* smem) {
 cudaError_t tgemm_setup_attributes() {
   for (int wt : {8, 4})
     for (int e : {EPI_STORE, EPI_RESID, EPI_SWIGLU})
-      for (int bn : {16, 128, 256}) {
+      for (int bn : {16, 128}) {
         int smem = 0;
         TgFn f = tg_select(wt, e, bn, &smem);
         cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -443,11 +469,9 @@ TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split) {
       }
     }
   } else {
-    // prompt chunk: fewer, wider tiles unless that leaves SMs idle for a wave
-    const int t128 = mt * ((T + 127) / 128), t256 = mt * ((T + 255) / 256);
-    const double c128 = (double)((t128 + num_sms - 1) / num_sms);
-    const double c256 = 1.8 * (double)((t256 + num_sms - 1) / num_sms);
-    p.bn = c256 <= c128 ? 256 : 128;
+    // prompt chunk: 128-token tiles (two activation planes and two weight
+    // planes leave no room for wider ones)
+    p.bn = 128;
     p.split = 1;
   }
   return p;
@@ -457,14 +481,18 @@ cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, c
   const MatDev& w = a.w;
   const int kpad = w.nb * 32;
   const int nk = (kpad + GBK - 1) / GBK;
-  if (a.kx % 8 || a.kx < kpad || a.T < 1 || w.rstep != 1 || p.split < 1 || p.split > nk) return cudaErrorInvalidValue;
+  if (a.kx % 8 || a.kx < kpad || a.T < 1 || w.rstep != 1 || p.split < 1 || p.split > nk || !a.xlo)
+    return cudaErrorInvalidValue;
+  if (epi == EPI_SWIGLU && !a.hlo) return cudaErrorInvalidValue;
   if (p.split > 1 && (!a.part || !a.counters)) return cudaErrorInvalidValue;
   int smem = 0;
   TgFn f = tg_select(wtype, epi, p.bn, &smem);
   if (!f) return cudaErrorInvalidValue;
-  CUtensorMap tx, tq, td;
+  CUtensorMap tx, txl, tq, td;
   const uint64_t rb = wtype == 8 ? (uint64_t)w.nb * 32 : (uint64_t)w.nb * 16;
   if (!make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, (uint64_t)a.kx, (uint64_t)a.T, (uint64_t)a.kx * 2, GBK,
+              (uint32_t)p.bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&txl, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.xlo, (uint64_t)a.kx, (uint64_t)a.T, (uint64_t)a.kx * 2, GBK,
               (uint32_t)p.bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.qs, rb, (uint64_t)w.rows, rb, wtype == 8 ? 64 : 32, GBM,
               wtype == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B) ||
@@ -472,7 +500,7 @@ cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, c
               CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   dim3 grid((a.T + p.bn - 1) / p.bn, (w.rows + GBM - 1) / GBM, p.split);
-  f<<<grid, GTHREADS, smem, s>>>(tx, tq, td, a);
+  f<<<grid, GTHREADS, smem, s>>>(tx, txl, tq, td, a);
   return cudaGetLastError();
 }
 

@@ -139,6 +139,8 @@ struct StepArgs {
   int* abort;               // set when a bounded wait gives up, zero at launch
   int S;                    // attention splits per KV head (one per CTA)
   unsigned long long* trace;  // optional: CTA 0 writes the global timer after each phase
+  unsigned long long* ctrace; // optional: per phase and CTA {consumer arrival, release, producer first issue,
+                              // producer last issue}: [phase][grid][4]
   int ns;                   // ring stages
   uint32_t stage_bytes;     // ring slot size
 };
@@ -154,21 +156,28 @@ cudaError_t launch_step(const StepPlan& p, const StepArgs& a, cudaStream_t s);
 
 // ---- prefill (T tokens at once) --------------------------------------------------
 
+// Activations enter the tensor cores as two fp16 planes, x = x_hi + x_lo
+// with x_hi = fp16(x) and x_lo = fp16(x - x_hi), and the dequantised weights
+// likewise (w_hi = fp16(d*q), w_lo = fp16(d*q - w_hi)); the GEMM accumulates
+// w_hi x_hi + w_hi x_lo + w_lo x_hi in fp32, which carries both operands to
+// about 22 bits instead of fp16's 11.
 struct PgArgs {
   MatDev w;            // weight rows = GEMM M
-  const __half* x;     // activations [T][kx] fp16, kx >= w.nb * 32, zero beyond the true width
+  const __half* x;     // activations [T][kx] fp16 (hi plane), kx >= w.nb * 32, zero beyond the true width
+  const __half* xlo;   // lo plane, same layout
   int kx;              // row stride of x in elements (multiple of 8)
   int T;               // tokens = GEMM N
   float* y;            // STORE / RESID: y[t * ldy + m]
   int ldy;
-  __half* h;           // SWIGLU: h[t * ldh + m / 2] = silu(gate) * up (rows interleaved gate, up)
+  __half* h;           // SWIGLU: h[t * ldh + m / 2] = silu(gate) * up (rows interleaved gate, up), hi plane
+  __half* hlo;         // SWIGLU: lo plane of h
   int ldh;
   int32_t* status;     // kTimeout on a wait that gave up
   float* part;         // split-K partial sums [split][T][rows] (split > 1)
   int* counters;       // one per output tile, zero between launches (split > 1)
 };
 
-// tile width (tokens per CTA: 16, 128 or 256) and K splits of one GEMM
+// tile width (tokens per CTA: 16 or 128) and K splits of one GEMM
 struct TgPlan {
   int bn, split;
 };
@@ -178,9 +187,11 @@ cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, c
 cudaError_t prefill_setup_attributes();
 cudaError_t launch_embed_rows(const MatDev& emb, int wtype, const int32_t* tokens, int T, int vocab, float* x, int ldx,
                               int32_t* status, cudaStream_t s);
-cudaError_t launch_rmsnorm_rows(const float* x, int T, int H, int ldx, const float* g, float eps, __half* out, int ldo,
+cudaError_t launch_rmsnorm_rows(const float* x, int T, int H, int ldx, const float* g, float eps, __half* out,
+                                __half* out_lo, int ldo,
                                 cudaStream_t s);
-cudaError_t launch_to_f16_rows(const float* x, int T, int cols, int ldx, __half* out, int ldo, cudaStream_t s);
+cudaError_t launch_to_f16_rows(const float* x, int T, int cols, int ldx, __half* out, __half* out_lo, int ldo,
+                               cudaStream_t s);
 cudaError_t launch_rope_kv_rows(const float* qkv, int T, int ld, int q_rows, int kv_rows, const KvView& kv, int seq,
                                 int pos0, const float2* rope_cs, int rope_len, float* q_out, int32_t* status,
                                 cudaStream_t s);
@@ -206,7 +217,8 @@ struct FattnArgs {
   const int32_t* ptab;       // the sequence's page-table row
   int max_pages, page_tokens;
   int pool_rows;             // rows of head_dim in one layer's K (or V) pool: n_pages * n_kv * page_tokens
-  __half* out;               // [T][ld_out] fp16, head h at columns h * head_dim
+  __half* out;               // [T][ld_out] fp16 hi plane, head h at columns h * head_dim
+  __half* out_lo;            // lo plane (fp16 of the rounding residual), same layout
   int ld_out;
   int32_t* status;
 };

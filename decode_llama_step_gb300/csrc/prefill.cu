@@ -20,8 +20,20 @@ namespace {
 
 // ---------------------------------------------------------------- row kernels
 
-// out[t] = fp16(rmsnorm(x[t]) * g), zero-padded to ldo columns (H % 4 == 0)
-__global__ void rmsnorm_rows_kernel(const float* x, int H, int ldx, const float* g, float eps, __half* out, int ldo) {
+// hi and lo fp16 planes of four fp32 values: hi = fp16(v), lo = fp16(v - hi)
+__device__ __forceinline__ void split4(float a, float b, float c, float d, uint2& hi, uint2& lo) {
+  const __half2 h0 = __floats2half2_rn(a, b), h1 = __floats2half2_rn(c, d);
+  const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+  const __half2 l0 = __floats2half2_rn(a - f0.x, b - f0.y), l1 = __floats2half2_rn(c - f1.x, d - f1.y);
+  hi.x = *reinterpret_cast<const uint32_t*>(&h0);
+  hi.y = *reinterpret_cast<const uint32_t*>(&h1);
+  lo.x = *reinterpret_cast<const uint32_t*>(&l0);
+  lo.y = *reinterpret_cast<const uint32_t*>(&l1);
+}
+
+// out[t] = fp16 planes of rmsnorm(x[t]) * g, zero-padded to ldo columns (H % 4 == 0)
+__global__ void rmsnorm_rows_kernel(const float* x, int H, int ldx, const float* g, float eps, __half* out,
+                                    __half* out_lo, int ldo) {
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * ldx);
   const float4* g4 = reinterpret_cast<const float4*>(g);
   const int n4 = H >> 2;
@@ -38,31 +50,30 @@ __global__ void rmsnorm_rows_kernel(const float* x, int H, int ldx, const float*
   for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += red[i];
   const float rs = 1.0f / sqrtf(t / (float)H + eps);
   __half* o = out + (size_t)blockIdx.x * ldo;
+  __half* ol = out_lo + (size_t)blockIdx.x * ldo;
   for (int i = threadIdx.x; i < n4; i += blockDim.x) {
     const float4 v = xr[i], gg = g4[i];
-    const __half2 a = __floats2half2_rn(v.x * rs * gg.x, v.y * rs * gg.y);
-    const __half2 b = __floats2half2_rn(v.z * rs * gg.z, v.w * rs * gg.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<const uint32_t*>(&a);
-    pk.y = *reinterpret_cast<const uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(o + 4 * i) = pk;
+    uint2 hi, lo;
+    split4(v.x * rs * gg.x, v.y * rs * gg.y, v.z * rs * gg.z, v.w * rs * gg.w, hi, lo);
+    *reinterpret_cast<uint2*>(o + 4 * i) = hi;
+    *reinterpret_cast<uint2*>(ol + 4 * i) = lo;
   }
-  for (int i = H + threadIdx.x; i < ldo; i += blockDim.x) o[i] = __float2half_rn(0.f);
+  for (int i = H + threadIdx.x; i < ldo; i += blockDim.x) o[i] = ol[i] = __float2half_rn(0.f);
 }
 
-// out[t][0..cols) = fp16(x[t]), zero up to ldo (cols % 4 == 0)
-__global__ void to_f16_rows_kernel(const float* x, int cols, int ldx, __half* out, int ldo) {
+// out[t][0..cols) = fp16 planes of x[t], zero up to ldo (cols % 4 == 0)
+__global__ void to_f16_rows_kernel(const float* x, int cols, int ldx, __half* out, __half* out_lo, int ldo) {
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * ldx);
   __half* o = out + (size_t)blockIdx.x * ldo;
+  __half* ol = out_lo + (size_t)blockIdx.x * ldo;
   for (int i = threadIdx.x; i < (cols >> 2); i += blockDim.x) {
     const float4 v = xr[i];
-    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
-    uint2 pk;
-    pk.x = *reinterpret_cast<const uint32_t*>(&a);
-    pk.y = *reinterpret_cast<const uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(o + 4 * i) = pk;
+    uint2 hi, lo;
+    split4(v.x, v.y, v.z, v.w, hi, lo);
+    *reinterpret_cast<uint2*>(o + 4 * i) = hi;
+    *reinterpret_cast<uint2*>(ol + 4 * i) = lo;
   }
-  for (int i = cols + threadIdx.x; i < ldo; i += blockDim.x) o[i] = __float2half_rn(0.f);
+  for (int i = cols + threadIdx.x; i < ldo; i += blockDim.x) o[i] = ol[i] = __float2half_rn(0.f);
 }
 
 int row_threads(int elems) {
@@ -295,16 +306,17 @@ cudaError_t launch_embed_rows(const MatDev& emb, int wtype, const int32_t* token
   return cudaGetLastError();
 }
 
-cudaError_t launch_rmsnorm_rows(const float* x, int T, int H, int ldx, const float* g, float eps, __half* out, int ldo,
-                                cudaStream_t s) {
-  if (H % 4 || ldx % 4 || ldo % 4) return cudaErrorInvalidValue;
-  rmsnorm_rows_kernel<<<T, row_threads(H / 4), 0, s>>>(x, H, ldx, g, eps, out, ldo);
+cudaError_t launch_rmsnorm_rows(const float* x, int T, int H, int ldx, const float* g, float eps, __half* out,
+                                __half* out_lo, int ldo, cudaStream_t s) {
+  if (H % 4 || ldx % 4 || ldo % 4 || !out_lo) return cudaErrorInvalidValue;
+  rmsnorm_rows_kernel<<<T, row_threads(H / 4), 0, s>>>(x, H, ldx, g, eps, out, out_lo, ldo);
   return cudaGetLastError();
 }
 
-cudaError_t launch_to_f16_rows(const float* x, int T, int cols, int ldx, __half* out, int ldo, cudaStream_t s) {
-  if (cols % 4 || ldx % 4 || ldo % 4) return cudaErrorInvalidValue;
-  to_f16_rows_kernel<<<T, row_threads(cols / 4), 0, s>>>(x, cols, ldx, out, ldo);
+cudaError_t launch_to_f16_rows(const float* x, int T, int cols, int ldx, __half* out, __half* out_lo, int ldo,
+                               cudaStream_t s) {
+  if (cols % 4 || ldx % 4 || ldo % 4 || !out_lo) return cudaErrorInvalidValue;
+  to_f16_rows_kernel<<<T, row_threads(cols / 4), 0, s>>>(x, cols, ldx, out, out_lo, ldo);
   return cudaGetLastError();
 }
 

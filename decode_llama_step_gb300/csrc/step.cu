@@ -58,6 +58,7 @@ struct Ctx {
   int sidx;        // ring stages consumed / produced so far
   unsigned epoch;  // grid barriers passed (thread 0)
   int pos, seq;
+  int pos_page;    // page holding position pos, -1 if none
 };
 
 __device__ __forceinline__ bool aborted(const StepArgs& A) { return *(volatile int*)A.abort != 0; }
@@ -85,29 +86,34 @@ __device__ __forceinline__ bool wait_bar(const StepArgs& A, uint32_t bar, uint32
 }
 
 // All consumer warps of all CTAs; the producer warp never takes part.
+// Thread 0 publishes the CTA's writes with a release add on the counter and
+// waits for the whole grid with acquire loads (the CTA barriers on either
+// side order the other threads' accesses around it).
 __device__ __forceinline__ void grid_sync(Ctx& c) {
   const StepArgs& A = *c.A;
   named_bar(1, NWC * 32);
   if (A.trace && blockIdx.x == 0 && threadIdx.x == 0) A.trace[c.epoch + 1] = global_ns();  // phase end
   if (threadIdx.x == 0) {
-    __threadfence();
+    if (A.ctrace) A.ctrace[((size_t)c.epoch * gridDim.x + blockIdx.x) * 4 + 0] = global_ns();
     const unsigned target = (++c.epoch) * gridDim.x;
-    atomicAdd(A.bar, 1u);
-    const uint64_t t0 = global_ns();
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(A.bar) : "memory");
+    uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
       unsigned v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(A.bar) : "memory");
       if (v >= target) break;
       if ((i & 15) == 15) {
         if (aborted(A)) break;
-        if (global_ns() - t0 > kWaitNs) {
+        const uint64_t now = global_ns();
+        if (!t0) t0 = now;
+        if (now - t0 > kWaitNs) {
           set_abort(A);
           break;
         }
       }
-      __nanosleep(32);
+      if (i >= 64) __nanosleep(32);
     }
-    __threadfence();
+    if (A.ctrace) A.ctrace[((size_t)(c.epoch - 1) * gridDim.x + blockIdx.x) * 4 + 1] = global_ns();
   }
   named_bar(1, NWC * 32);
 }
@@ -126,27 +132,42 @@ __device__ __forceinline__ size_t row_bytes_of(const MatDev& w) {
 }
 
 // ------------------------------------------------------------------ producer
+//
+// This CTA's copy stream in program order: per layer its QKV rows, its
+// attention tiles, its O rows, gate/up rows and down rows; then its LM head
+// rows.  One chunk fills one ring stage: RS whole rows (codes, then their
+// scales at offset RS * row bytes) or one 32-token K/V tile (K, then V at
+// offset kTile * HD * 2).
 
-template <int WT, int RS>
-__device__ void produce_gemv(Ctx& c, const MatDev& w, int unit, int& issued) {
-  const StepArgs& A = *c.A;
-  int r0, r1;
-  row_split(w.rows, unit, r0, r1);
-  const size_t rb = row_bytes_of<WT>(w), db = (size_t)w.ds * 2;
-  for (int row = r0; row < r1; row += RS) {
-    const int slot = c.sidx % A.ns;
-    if (c.sidx >= A.ns && !wait_bar(A, smem_u32(&c.sh->empty[slot]), ((c.sidx / A.ns) - 1) & 1, 200)) return;
-    const int n = min(RS, r1 - row);
-    uint8_t* dst = c.ring + (size_t)slot * A.stage_bytes;
-    const uint32_t bar = smem_u32(&c.sh->full[slot]);
-    mbar_expect_tx(bar, (uint32_t)(n * (rb + db)));
-    bulk_g2s(smem_u32(dst), w.qs + (size_t)row * rb, (uint32_t)(n * rb), bar);
-    bulk_g2s(smem_u32(dst + RS * rb), reinterpret_cast<const uint8_t*>(w.d) + (size_t)row * db, (uint32_t)(n * db),
-             bar);
-    ++c.sidx;
-    ++issued;
-  }
-}
+// Row ranges of this CTA in each GEMV phase (the same for every layer).
+struct Rows {
+  int qkv0, qkv1, o0, o1, gu0, gu1, dn0, dn1, hd0, hd1;
+};
+
+// A cursor over the stream.  Entering a phase sets up its base pointers
+// and counts once, so a chunk costs a few adds.
+struct PCur {
+  int l = 0;    // layer; n_layers = the LM head
+  int ph = -1;  // 0 QKV, 1 attention, 2 O, 3 gate/up, 4 down; -1 = not started
+  int i = 0, n = 0;  // chunk index and count in the phase
+  // GEMV phase: rows [row, row_end) remain; codes and scales of `row`
+  const uint8_t* q;
+  const uint8_t* d;
+  uint32_t rb, db;
+  int rs, row, row_end;
+  // attention phase
+  int tb;
+  const __half* kp;
+  const __half* vp;
+};
+
+struct Chunk {
+  const uint8_t* a;
+  const uint8_t* b;
+  uint32_t na, nb;   // bytes of each range (both 0: an empty stage)
+  uint32_t off_b;    // stage offset of the second range
+  bool bad_page;
+};
 
 __device__ __forceinline__ void attn_task(const StepArgs& A, int n, int& kvh, int& tb, int& te) {
   const int ntask = A.n_kv * A.S;
@@ -159,33 +180,163 @@ __device__ __forceinline__ void attn_task(const StepArgs& A, int n, int& kvh, in
   if ((int)blockIdx.x >= ntask) te = tb;  // no task for this CTA
 }
 
-template <int HD>
-__device__ void produce_attention(Ctx& c, const __half* k_pool, const __half* v_pool, int& issued) {
+template <int WT>
+__device__ __forceinline__ void gemv_phase(PCur& u, const MatDev& w, int r0, int r1, int rs) {
+  u.rb = (uint32_t)row_bytes_of<WT>(w);
+  u.db = (uint32_t)w.ds * 2;
+  u.rs = rs;
+  u.row = r0;
+  u.row_end = r1;
+  u.q = w.qs + (size_t)r0 * u.rb;
+  u.d = reinterpret_cast<const uint8_t*>(w.d) + (size_t)r0 * u.db;
+  u.n = r1 > r0 ? (r1 - r0 + rs - 1) / rs : 0;
+}
+
+// Set up phase (u.l, u.ph).
+template <int WT, int HD, int RSA, int RSB>
+__device__ void begin_phase(const Ctx& c, const Rows& R, PCur& u) {
   const StepArgs& A = *c.A;
-  const int n = c.pos + 1;
-  int kvh, tb, te;
-  attn_task(A, n, kvh, tb, te);
-  const int32_t* ptab = A.page_table + (size_t)c.seq * A.max_pages;
-  for (int t = tb; t < te; ++t) {
-    const int slot = c.sidx % A.ns;
-    if (c.sidx >= A.ns && !wait_bar(A, smem_u32(&c.sh->empty[slot]), ((c.sidx / A.ns) - 1) & 1, 200)) return;
-    const uint32_t bar = smem_u32(&c.sh->full[slot]);
+  u.i = 0;
+  if (u.l >= A.n_layers) {
+    gemv_phase<WT>(u, A.head, R.hd0, R.hd1, RSA);
+    if (!A.head_rows) u.n = 0;
+    return;
+  }
+  const StepLayer& L = A.layers[u.l];
+  switch (u.ph) {
+    case 0: gemv_phase<WT>(u, L.qkv, R.qkv0, R.qkv1, RSA); break;
+    case 1: {
+      int kvh, te;
+      attn_task(A, c.pos + 1, kvh, u.tb, te);
+      u.n = max(0, te - u.tb);
+      const size_t head_off = (size_t)kvh * A.page_tokens * HD;
+      u.kp = L.k_pool + head_off;
+      u.vp = L.v_pool + head_off;
+      break;
+    }
+    case 2: gemv_phase<WT>(u, L.o, R.o0, R.o1, RSA); break;
+    case 3: gemv_phase<WT>(u, L.gu, R.gu0, R.gu1, RSA); break;
+    default: gemv_phase<WT>(u, L.down, R.dn0, R.dn1, RSB); break;
+  }
+}
+
+// The next chunk of the stream at cursor u (advancing it); false at the end.
+template <int WT, int HD, int RSA, int RSB>
+__device__ bool next_chunk(const Ctx& c, const Rows& R, PCur& u, Chunk& ch) {
+  const StepArgs& A = *c.A;
+  while (u.ph < 0 || u.i >= u.n) {
+    if (u.ph >= 0) {  // leave the finished phase
+      if (u.l >= A.n_layers) return false;  // the LM head was the last phase
+      if (++u.ph == 5) {
+        u.ph = 0;
+        ++u.l;
+      }
+    } else {
+      u.ph = 0;
+    }
+    if (u.l > A.n_layers) return false;
+    begin_phase<WT, HD, RSA, RSB>(c, R, u);
+  }
+  ch.bad_page = false;
+  if (u.l < A.n_layers && u.ph == 1) {
+    const int t = u.tb + u.i;
     // positions before pos are final; pos itself is written by this step
     const int n_old = max(0, min(kTile, c.pos - t * kTile));
-    const int page = ptab[(t * kTile) / A.page_tokens];
+    const int page = A.page_table[(size_t)c.seq * A.max_pages + (t * kTile) / A.page_tokens];
+    ch.na = ch.nb = 0;
+    ch.off_b = kTile * HD * 2;
+    ch.bad_page = page < 0;
     if (n_old > 0 && page >= 0) {
-      const size_t base = (((size_t)page * A.n_kv + kvh) * A.page_tokens + (t * kTile) % A.page_tokens) * HD;
-      uint8_t* dst = c.ring + (size_t)slot * A.stage_bytes;
-      const uint32_t bytes = (uint32_t)n_old * HD * 2;
-      mbar_expect_tx(bar, 2 * bytes);
-      bulk_g2s(smem_u32(dst), k_pool + base, bytes, bar);
-      bulk_g2s(smem_u32(dst + kTile * HD * 2), v_pool + base, bytes, bar);
-    } else {
-      if (page < 0) atomicOr(&A.sp->status, kBadPage);
+      const size_t base = ((size_t)page * A.n_kv * A.page_tokens + (t * kTile) % A.page_tokens) * HD;
+      ch.a = reinterpret_cast<const uint8_t*>(u.kp + base);
+      ch.b = reinterpret_cast<const uint8_t*>(u.vp + base);
+      ch.na = ch.nb = (uint32_t)n_old * HD * 2;
+    }
+  } else {
+    const int n = min(u.rs, u.row_end - u.row);
+    ch.a = u.q;
+    ch.na = (uint32_t)n * u.rb;
+    ch.b = u.d;
+    ch.nb = (uint32_t)n * u.db;
+    ch.off_b = (uint32_t)u.rs * u.rb;
+    u.q += ch.na;
+    u.d += ch.nb;
+    u.row += n;
+  }
+  ++u.i;
+  return true;
+}
+
+// The producer warp's lane 0: fill the ring in stream order.
+template <int WT, int HD, int RSA, int RSB>
+__device__ void produce(Ctx& c) {
+  const StepArgs& A = *c.A;
+  Rows R;
+  {
+    const StepLayer& L0 = A.layers[0];  // every layer has the same shapes
+    row_split(L0.qkv.rows, 2, R.qkv0, R.qkv1);
+    row_split(L0.o.rows, 1, R.o0, R.o1);
+    row_split(L0.gu.rows, 2, R.gu0, R.gu1);
+    row_split(L0.down.rows, 1, R.dn0, R.dn1);
+  }
+  row_split(A.head.rows, 1, R.hd0, R.hd1);
+  PCur rc;
+  Chunk ch;
+  int last_phase = -1;
+  // the abort flag is checked inside waits only: a global load per chunk
+  // would serialise an L2 round trip into every stage issue
+  for (;;) {
+    if (!next_chunk<WT, HD, RSA, RSB>(c, R, rc, ch)) break;
+    const int phase = 1 + 5 * rc.l + (rc.l < A.n_layers ? rc.ph : 0);
+    if (A.ctrace) {
+      unsigned long long* t = A.ctrace + ((size_t)phase * gridDim.x + blockIdx.x) * 4;
+      const unsigned long long now = global_ns();
+      if (phase != last_phase) t[2] = now;
+      t[3] = now;
+      last_phase = phase;
+    }
+    const int slot = c.sidx % A.ns;
+    if (c.sidx >= A.ns) {
+      const uint32_t bar = smem_u32(&c.sh->empty[slot]);
+      const uint32_t parity = ((c.sidx / A.ns) - 1) & 1;
+      if (!mbar_try_wait(bar, parity)) {
+        const uint64_t t0 = global_ns();
+        bool ok = true;
+        for (uint32_t it = 1;; ++it) {
+          if (mbar_try_wait(bar, parity)) break;
+          if (it > 4) __nanosleep(200);
+          if ((it & 63) == 0) {
+            if (aborted(A)) {
+              ok = false;
+              break;
+            }
+            if (global_ns() - t0 > kWaitNs) {
+              set_abort(A);
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (!ok) break;
+      }
+    }
+    const uint32_t bar = smem_u32(&c.sh->full[slot]);
+    uint8_t* dst = c.ring + (size_t)slot * A.stage_bytes;
+    if (ch.bad_page) atomicOr(&A.sp->status, kBadPage);
+    if (ch.na + ch.nb == 0) {
       mbar_arrive(bar);
+    } else {
+      mbar_expect_tx(bar, ch.na + ch.nb);
+      bulk_g2s(smem_u32(dst), ch.a, ch.na, bar);
+      if (ch.nb) bulk_g2s(smem_u32(dst + ch.off_b), ch.b, ch.nb, bar);
     }
     ++c.sidx;
-    ++issued;
+  }
+  // never leave with copies in flight
+  for (int s = max(0, c.sidx - A.ns); s < c.sidx; ++s) {
+    const uint32_t bar = smem_u32(&c.sh->full[s % A.ns]);
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, (s / A.ns) & 1) && global_ns() - t0 < kWaitNs) __nanosleep(100);
   }
 }
 
@@ -202,6 +353,32 @@ __device__ __forceinline__ void load_x(Ctx& c, const MatDev& w, const float* x, 
   const int nchunk = (kpad + Gm::CH - 1) / Gm::CH;
   const int mc = warp < nchunk ? min(MC, (nchunk - warp + NWC - 1) / NWC) : 0;
   float4 raw[MC][V4];
+  float4 gg[PRO == PRO_RMSNORM ? MC : 1][V4];
+  if (PRO == PRO_RMSNORM) {
+    // the gains are weights: their loads go out together with x's
+#pragma unroll
+    for (int k = 0; k < MC; ++k) {
+      const int ch = warp + k * NWC;
+      const int col0 = WT == 8 ? ch * 512 + lane * 16 : (ch * 32 + lane) * 32;
+      const bool vk = k < mc && col0 < kpad;
+#pragma unroll
+      for (int m4 = 0; m4 < V4; ++m4) {
+        const int i0 = col0 + 4 * m4;
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (vk) {
+          if (i0 + 3 < cols && (cols & 3) == 0) {
+            g = *reinterpret_cast<const float4*>(gain + i0);
+          } else {
+            if (i0 < cols) g.x = gain[i0];
+            if (i0 + 1 < cols) g.y = gain[i0 + 1];
+            if (i0 + 2 < cols) g.z = gain[i0 + 2];
+            if (i0 + 3 < cols) g.w = gain[i0 + 3];
+          }
+        }
+        gg[PRO == PRO_RMSNORM ? k : 0][m4] = g;
+      }
+    }
+  }
 #pragma unroll
   for (int k = 0; k < MC; ++k) {
     const int ch = warp + k * NWC;
@@ -241,27 +418,13 @@ __device__ __forceinline__ void load_x(Ctx& c, const MatDev& w, const float* x, 
     for (int i = 0; i < NWC; ++i) t += c.sh->red[i];  // fixed order
     const float rs = 1.0f / sqrtf(t / (float)cols + c.A->eps);
 #pragma unroll
-    for (int k = 0; k < MC; ++k) {
-      const int ch = warp + k * NWC;
-      const int col0 = WT == 8 ? ch * 512 + lane * 16 : (ch * 32 + lane) * 32;
+    for (int k = 0; k < MC; ++k)
 #pragma unroll
       for (int m4 = 0; m4 < V4; ++m4) {
-        const int i0 = col0 + 4 * m4;
-        float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (valid[k]) {
-          if (i0 + 3 < cols && (cols & 3) == 0) {
-            g = *reinterpret_cast<const float4*>(gain + i0);
-          } else {
-            if (i0 < cols) g.x = gain[i0];
-            if (i0 + 1 < cols) g.y = gain[i0 + 1];
-            if (i0 + 2 < cols) g.z = gain[i0 + 2];
-            if (i0 + 3 < cols) g.w = gain[i0 + 3];
-          }
-        }
+        const float4 g = gg[PRO == PRO_RMSNORM ? k : 0][m4];
         raw[k][m4] = make_float4(raw[k][m4].x * rs * g.x, raw[k][m4].y * rs * g.y, raw[k][m4].z * rs * g.z,
                                  raw[k][m4].w * rs * g.w);
       }
-    }
   }
 #pragma unroll
   for (int k = 0; k < MC; ++k) quantize_slice<WT>(reinterpret_cast<const float*>(raw[k]), xq[k]);
@@ -291,6 +454,16 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
   const int nchunk = (kpad + Gm::CH - 1) / Gm::CH;
   const int nwa = min(NWC, nchunk);
   constexpr int spb = kRB / RS;  // stages per epilogue block
+  // RoPE factors of this thread's pair in the first two epilogue blocks,
+  // loaded before the stages arrive (the position is fixed for the step)
+  float2 cs_pre[2] = {make_float2(1.f, 0.f), make_float2(1.f, 0.f)};
+  if (EPI == EPI_QKV && c.pos >= 0 && c.pos < A.rope_len && tid < kRB / 2) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const int r = r0 + b * kRB + 2 * tid;
+      if (r < r1 && r < A.q_rows + A.kv_rows) cs_pre[b] = A.rope_cs[(size_t)c.pos * (A.hd >> 1) + ((r % A.hd) >> 1)];
+    }
+  }
   for (int s = 0; s < nst; ++s) {
     const int slot = c.sidx % A.ns;
     const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), (c.sidx / A.ns) & 1, 20);
@@ -346,7 +519,9 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
               atomicOr(&A.sp->status, kBadPos);
               continue;
             }
-            const float2 cs = A.rope_cs[(size_t)c.pos * (hd >> 1) + ((r % hd) >> 1)];
+            const int blk = s / spb;
+            const float2 cs = (pi == tid && blk < 2) ? (blk == 0 ? cs_pre[0] : cs_pre[1])
+                                                     : A.rope_cs[(size_t)c.pos * (hd >> 1) + ((r % hd) >> 1)];
             const float t0 = v0 * cs.x - v1 * cs.y;
             v1 = v0 * cs.y + v1 * cs.x;
             v0 = t0;
@@ -359,8 +534,7 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
             const int rk = r - A.q_rows - (is_k ? 0 : A.kv_rows);
             const int kvh = rk / hd, dim = rk % hd;
             const int pt = A.page_tokens;
-            const int lp = c.pos / pt;
-            const int page = (c.pos >= 0 && lp < A.max_pages) ? A.page_table[(size_t)c.seq * A.max_pages + lp] : -1;
+            const int page = c.pos_page;
             if (page < 0) {
               atomicOr(&A.sp->status, kBadPage);
               continue;
@@ -388,14 +562,23 @@ __device__ __forceinline__ float warp_max_f(float v) {
   return v;
 }
 
-// One CTA's attention task: split sp of KV head kvh.  Warp j % NWC owns the
-// task's j-th tile (one ring stage); position pos (written this step) is
-// copied from global into its tile before scoring.
+// One CTA's attention task: split sp of KV head kvh, tiles tb .. te-1 (one
+// ring stage each).  The consumer warps form TS tile slots x HG head groups:
+// warp w scores the tiles j with j % TS == w % TS for the HPW query heads of
+// group w / TS, so every warp has work when the task holds TS tiles or more.
+// Position pos (written by this step's QKV phase) is copied from global
+// into its tile before scoring.  The TS warps of a head group merge in
+// shared memory into one (m, l, o) partial per CTA; the last CTA of a KV
+// head merges the S partials in split order with all loads in flight.
 template <int HD, int G>
 __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_pool) {
+  constexpr int HG = G >= 2 ? 2 : 1;  // head groups
+  constexpr int TS = NWC / HG;        // tile slots
+  constexpr int HPW = G / HG;         // heads per warp
   constexpr int DPL = HD / 32, W2 = HD / 2;
   const StepArgs& A = *c.A;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tslot = warp % TS, hg = warp / TS;
   const int n = c.pos + 1;
   int kvh, tb, te;
   attn_task(A, n, kvh, tb, te);
@@ -407,27 +590,27 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
     for (int i = tid; i < G * HD; i += NWC * 32) c.s_q[i] = __ldcg(qrow + i) * scale;
   }
   named_bar(1, NWC * 32);
-  float m_run[G], l_run[G], o[G][DPL];
+  float m_run[HPW], l_run[HPW], o[HPW][DPL];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+  for (int h = 0; h < HPW; ++h) {
     m_run[h] = -INFINITY;
     l_run[h] = 0.f;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
   }
-  const int pg = c.pos / A.page_tokens;
-  const int pos_page = A.page_table[(size_t)c.seq * A.max_pages + pg];
+  const float2* q2 = reinterpret_cast<const float2*>(c.s_q) + (size_t)hg * HPW * W2;
   for (int j = 0; j < te - tb; ++j) {
     const int slot = c.sidx % A.ns;
-    if ((j % NWC) == warp) {
+    if ((j % TS) == tslot) {
       const int t = tb + j;
       const int nt = min(kTile, n - t * kTile);
       const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), (c.sidx / A.ns) & 1, 20);
       __half* kt = reinterpret_cast<__half*>(c.ring + (size_t)slot * A.stage_bytes);
       __half* vt = kt + kTile * HD;
       const int jp = c.pos - t * kTile;  // the new position inside this tile, if any
-      if (jp >= 0 && jp < kTile && pos_page >= 0) {
-        const size_t off = (((size_t)pos_page * A.n_kv + kvh) * A.page_tokens + (c.pos % A.page_tokens)) * HD;
+      if (jp >= 0 && jp < kTile && c.pos_page >= 0) {
+        // both warps of the slot write the same bytes; each reads its own
+        const size_t off = (((size_t)c.pos_page * A.n_kv + kvh) * A.page_tokens + (c.pos % A.page_tokens)) * HD;
         for (int i = lane; i < HD / 2; i += 32) {
           reinterpret_cast<__half2*>(kt + jp * HD)[i] = __ldcg(reinterpret_cast<const __half2*>(k_pool + off) + i);
           reinterpret_cast<__half2*>(vt + jp * HD)[i] = __ldcg(reinterpret_cast<const __half2*>(v_pool + off) + i);
@@ -435,26 +618,25 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
         __syncwarp();
       }
       if (ok) {
-        float sc[G];
+        float sc[HPW];
         {
-          float2 acc[G];
+          float2 acc[HPW];
 #pragma unroll
-          for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+          for (int h = 0; h < HPW; ++h) acc[h] = make_float2(0.f, 0.f);
           const __half2* krow = reinterpret_cast<const __half2*>(kt + lane * HD);
-          const float2* q2 = reinterpret_cast<const float2*>(c.s_q);
 #pragma unroll 4
           for (int w2 = 0; w2 < W2; ++w2) {
             const int wi = (w2 + lane) & (W2 - 1);
             const float2 kf = __half22float2(krow[wi]);
 #pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h]);
+            for (int h = 0; h < HPW; ++h) acc[h] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h]);
           }
 #pragma unroll
-          for (int h = 0; h < G; ++h) sc[h] = lane < nt ? acc[h].x + acc[h].y : -INFINITY;
+          for (int h = 0; h < HPW; ++h) sc[h] = lane < nt ? acc[h].x + acc[h].y : -INFINITY;
         }
-        float p[G];
+        float p[HPW];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
+        for (int h = 0; h < HPW; ++h) {
           const float m_new = fmaxf(m_run[h], warp_max_f(sc[h]));
           p[h] = lane < nt ? expf(sc[h] - m_new) : 0.f;
           const float al = expf(m_run[h] - m_new);
@@ -466,10 +648,20 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
         const __half* vl = vt + lane * DPL;
         for (int jj = 0; jj < nt; ++jj) {
           float vf[DPL];
+          if (DPL == 4) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(vl + jj * HD);
+            const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+            const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+            vf[0] = v01.x;
+            vf[1] = v01.y;
+            vf[2 % DPL] = v23.x;
+            vf[3 % DPL] = v23.y;
+          } else {
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) vf[e] = __half2float(vl[jj * HD + e]);
+            for (int e = 0; e < DPL; ++e) vf[e] = __half2float(vl[jj * HD + e]);
+          }
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
+          for (int h = 0; h < HPW; ++h) {
             const float pj = __shfl_sync(0xffffffffu, p[h], jj);
 #pragma unroll
             for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pj, vf[e], o[h][e]);
@@ -484,59 +676,79 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
     if (lane == 0) mbar_arrive(smem_u32(&c.sh->empty[slot]));
     ++c.sidx;
   }
-  // merge the warps of this CTA
+  // merge the TS warps of each head group
   if (lane == 0) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      c.s_wm[warp * G + h] = m_run[h];
-      c.s_wl[warp * G + h] = l_run[h];
+    for (int h = 0; h < HPW; ++h) {
+      c.s_wm[warp * HPW + h] = m_run[h];
+      c.s_wl[warp * HPW + h] = l_run[h];
     }
   }
 #pragma unroll
-  for (int h = 0; h < G; ++h)
+  for (int h = 0; h < HPW; ++h)
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) c.s_wo[(warp * G + h) * HD + lane * DPL + e] = o[h][e];
+    for (int e = 0; e < DPL; ++e) c.s_wo[(warp * HPW + h) * HD + lane * DPL + e] = o[h][e];
   named_bar(1, NWC * 32);
   if (has_task) {
     const size_t slot = (size_t)kvh * A.S + sp;
     for (int idx = tid; idx < G * HD; idx += NWC * 32) {
-      const int h = idx / HD;
+      const int h = idx / HD, hh = h % HPW, w0 = (h / HPW) * TS;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NWC; ++w) M = fmaxf(M, c.s_wm[w * G + h]);
+      for (int t = 0; t < TS; ++t) M = fmaxf(M, c.s_wm[(w0 + t) * HPW + hh]);
       float acc = 0.f, L = 0.f;
 #pragma unroll
-      for (int w = 0; w < NWC; ++w) {
-        const float ew = c.s_wl[w * G + h] > 0.f ? expf(c.s_wm[w * G + h] - M) : 0.f;
-        acc = fmaf(ew, c.s_wo[(w * G) * HD + idx], acc);
-        L = fmaf(ew, c.s_wl[w * G + h], L);
+      for (int t = 0; t < TS; ++t) {
+        const int wi = (w0 + t) * HPW + hh;
+        const float ew = c.s_wl[wi] > 0.f ? expf(c.s_wm[wi] - M) : 0.f;
+        acc = fmaf(ew, c.s_wo[wi * HD + (idx % HD)], acc);
+        L = fmaf(ew, c.s_wl[wi], L);
       }
       A.part_o[slot * G * HD + idx] = acc;
       if ((idx % HD) == 0) reinterpret_cast<float2*>(A.part_ml)[slot * G + h] = make_float2(M, L);
     }
-    __threadfence();
   }
   named_bar(1, NWC * 32);
-  if (tid == 0) c.sh->last = has_task ? (atomicAdd(&A.att_counters[kvh], 1) == A.S - 1) : 0;
+  // thread 0 publishes the CTA's partials (release, after the CTA barrier)
+  // and, on the last arrival, acquires everyone else's
+  if (tid == 0) {
+    int prev = 0;
+    if (has_task)
+      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev) : "l"(A.att_counters + kvh) : "memory");
+    c.sh->last = has_task && prev == A.S - 1;
+  }
   named_bar(1, NWC * 32);
   if (c.sh->last) {
-    __threadfence();
-    // merge the S splits of this KV head, in split order
+    // merge the S splits of this KV head in split order (running max form),
+    // loads issued in blocks of kMB so they are in flight together
+    constexpr int kMB = 20;
     const size_t slot0 = (size_t)kvh * A.S;
     const float2* ml = reinterpret_cast<const float2*>(A.part_ml);
     for (int idx = tid; idx < G * HD; idx += NWC * 32) {
       const int h = idx / HD;
-      float M = -INFINITY;
-      for (int s = 0; s < A.S; ++s) M = fmaxf(M, __ldcg(&ml[(slot0 + s) * G + h]).x);
-      float num = 0.f, den = 0.f;
-      for (int s = 0; s < A.S; ++s) {
-        const float2 v = __ldcg(&ml[(slot0 + s) * G + h]);
-        if (v.y == 0.f) continue;
-        const float ew = expf(v.x - M);
-        den = fmaf(v.y, ew, den);
-        num = fmaf(__ldcg(&A.part_o[(slot0 + s) * G * HD + idx]), ew, num);
+      const float* po = A.part_o + slot0 * G * HD + idx;
+      float M = -INFINITY, Ls = 0.f, acc = 0.f;
+      for (int s0 = 0; s0 < A.S; s0 += kMB) {
+        float2 mv[kMB];
+        float pv[kMB];
+#pragma unroll
+        for (int k = 0; k < kMB; ++k) {
+          const int sk = s0 + k;
+          mv[k] = sk < A.S ? __ldcg(&ml[(slot0 + sk) * G + h]) : make_float2(-INFINITY, 0.f);
+          pv[k] = sk < A.S ? __ldcg(po + (size_t)sk * G * HD) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kMB; ++k) {
+          if (mv[k].y > 0.f) {  // empty split: nothing to add
+            const float Mn = fmaxf(M, mv[k].x);
+            const float ea = expf(M - Mn), eb = expf(mv[k].x - Mn);
+            acc = acc * ea + pv[k] * eb;
+            Ls = Ls * ea + mv[k].y * eb;
+            M = Mn;
+          }
+        }
       }
-      A.o[(size_t)kvh * G * HD + idx] = num / den;
+      A.o[(size_t)kvh * G * HD + idx] = acc / Ls;
     }
     if (tid == 0) A.att_counters[kvh] = 0;
   }
@@ -568,6 +780,10 @@ __global__ void __launch_bounds__(NTHR, 1) step_kernel(const StepArgs A) {
   c.epoch = 0;
   c.pos = A.sp->pos[0];
   c.seq = A.sp->seq[0];
+  {
+    const int lp = c.pos >= 0 ? c.pos / A.page_tokens : -1;
+    c.pos_page = (lp >= 0 && lp < A.max_pages) ? A.page_table[(size_t)c.seq * A.max_pages + lp] : -1;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -582,24 +798,7 @@ __global__ void __launch_bounds__(NTHR, 1) step_kernel(const StepArgs A) {
 
   if (warp == NWC) {
     // ---------------- producer: every phase's stages, in consumer order
-    if (lane == 0) {
-      int issued = 0;
-      for (int l = 0; l < A.n_layers && !aborted(A); ++l) {
-        const StepLayer& L = A.layers[l];
-        produce_gemv<WT, RSA>(c, L.qkv, 2, issued);
-        produce_attention<HD>(c, L.k_pool, L.v_pool, issued);
-        produce_gemv<WT, RSA>(c, L.o, 1, issued);
-        produce_gemv<WT, RSA>(c, L.gu, 2, issued);
-        produce_gemv<WT, RSB>(c, L.down, 1, issued);
-      }
-      if (!aborted(A) && A.head_rows) produce_gemv<WT, RSA>(c, A.head, 1, issued);
-      // never leave with copies in flight
-      for (int s = max(0, c.sidx - A.ns); s < c.sidx; ++s) {
-        const uint32_t bar = smem_u32(&c.sh->full[s % A.ns]);
-        const uint64_t t0 = global_ns();
-        while (!mbar_try_wait(bar, (s / A.ns) & 1) && global_ns() - t0 < kWaitNs) __nanosleep(100);
-      }
-    }
+    if (lane == 0) produce<WT, HD, RSA, RSB>(c);
   } else {
     // ---------------- consumers
     // embedding row -> x (rows split like the residual epilogues)

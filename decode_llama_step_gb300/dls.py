@@ -81,6 +81,7 @@ _SIGS = {
     "dls_debug_gemm": (ctypes.c_int, [vp, i32, i32, i32, vp, vp]),
     "dls_debug_launches_per_step": (i32, [vp]),
     "dls_debug_profile_step": (ctypes.c_int, [vp, i32, i32, i32, i32, vp, vp, vp]),
+    "dls_debug_step_trace": (ctypes.c_int, [vp, vp, i32, vp]),
 }
 
 
@@ -350,6 +351,13 @@ class Model:
         self._c(self.lib.dls_debug_profile_step(self.handle, seq, int(token), int(pos), max_kernels, ms.ctypes.data,
                                                 kinds.ctypes.data, ctypes.byref(n)))
         return ms[: n.value].copy(), kinds[: n.value].copy()
+
+    def step_trace(self, max_entries: int = 1 << 22) -> np.ndarray:
+        """Per-CTA phase timestamps of the last profiled persistent step: [phase, cta, 4] (ns)."""
+        out = np.zeros(max_entries, dtype=np.uint64)
+        n = ctypes.c_int32(0)
+        self._c(self.lib.dls_debug_step_trace(self.handle, out.ctypes.data, max_entries, ctypes.byref(n)))
+        return out[: n.value]
 
     def launches_per_step(self) -> int:
         return int(self.lib.dls_debug_launches_per_step(self.handle))

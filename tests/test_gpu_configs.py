@@ -1,0 +1,321 @@
+"""GPU parity at the workloads' full sizes, through the C ABI.
+
+The five model shapes and their workloads (the 1B, 8B, fork and 70B shapes;
+the tiny one is covered in test_gpu_tiny.py) run here in the launch
+configuration the benchmark times.  Where the fp64 oracle cannot follow the
+whole model in seconds, it checks a sample it can compute on its own from the
+same seeded inputs: the first layers of the model at full width and full
+context.  Weights are drawn per (shape, layer, tensor), so a model cut to its
+first n layers holds exactly the first n layers of the full model, and the
+GPU's residual stream after those layers in the full model must match the
+oracle's.  Properties that hold at any size cover the rest: the KV fork
+copies bytes exactly, a forked branch decodes exactly like an independent
+prefill, and streamed layers compute what resident layers compute.
+
+Decode inputs come from the oracle: either seeded token ids, or the oracle's
+own greedy token at every step (teacher forcing), so that no input of the
+oracle ever comes from the GPU.  Tolerances: max|gpu - oracle| <= 2e-3 *
+max|oracle| for residuals and logits, identical greedy tokens wherever the
+oracle's top-2 gap exceeds 1e-2, bit-exact fork copies.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import OracleModel, ops
+
+from parity import assert_close, check_greedy
+
+pytestmark = pytest.mark.gpu
+
+GB = 1 << 30
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def cut(cfg, n_layers):
+    """The first n_layers of a shape (same weights for those layers)."""
+    return dataclasses.replace(cfg, n_layers=n_layers)
+
+
+def gpu_model(cfg, w, **kw):
+    from decode_llama_step_gb300 import dls
+    torch = _torch()
+    stream = torch.cuda.Stream()
+    return dls.Model(cfg, w, stream=stream, **kw), stream
+
+
+def captured(m, stream, cfg, fn):
+    """Run fn() with the per-layer capture armed; residuals [n_layers, hidden]."""
+    torch = _torch()
+    cap = torch.empty(cfg.n_layers, cfg.hidden, device="cuda")
+    m.debug_capture(cap)
+    fn()
+    stream.synchronize()
+    return cap.cpu().numpy().astype(np.float64)
+
+
+def host(t, stream):
+    """A device tensor as fp64 numpy, after the model's stream has finished."""
+    stream.synchronize()
+    return t.cpu().numpy().astype(np.float64)
+
+
+def release(*models):
+    torch = _torch()
+    for m in models:
+        if m is not None:
+            m.close()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def test_1b_prefill_512_then_128_greedy_steps(gpu_lib):
+    """Llama-3.2-1B shape (16 layers, tied embeddings, Q8_0): prefill of 512
+    seeded tokens, then 128 greedy decode steps, every layer and every
+    step's logits against the full fp64 oracle."""
+    torch = _torch()
+    cfg = synth.get_config("1b")
+    P, D = cfg.workload["prompt"], cfg.workload["decode"]
+    w = synth.model_weights(cfg)
+    m, stream = gpu_model(cfg, w, max_seqs=1, max_ctx=P + D + 8)
+    orc = OracleModel(cfg, w, cache_bytes=16 * GB)
+    try:
+        prompt = synth.prompt_tokens(cfg, P, seed=1)
+        seq = m.seq_create()
+        logits = torch.empty(cfg.vocab, device="cuda")
+        got_layers = captured(m, stream, cfg, lambda: m.prefill(seq, prompt, logits))
+        oseq = orc.new_seq(capacity=P + D)
+        ref_layers = []
+        ref = orc.prefill(oseq, prompt, capture=ref_layers)
+        for l in range(cfg.n_layers):
+            assert_close(got_layers[l], ref_layers[l], f"prefill layer {l}")
+        got = host(logits, stream)
+        assert_close(got, ref, "prefill logits")
+        tok = check_greedy(got, ref, "prefill")
+        worst = 0.0
+        for i in range(D):
+            pos = P + i
+            m.decode_step(seq, tok, pos, logits)
+            ref = orc.decode_step(oseq, tok, pos)
+            got = host(logits, stream)
+            worst = max(worst, assert_close(got, ref, f"decode step {i}"))
+            tok = check_greedy(got, ref, f"decode step {i}")  # the oracle's token feeds both sides
+        assert m.seq_length(seq) == P + D
+    finally:
+        release(m)
+
+
+@pytest.fixture(scope="module")
+def w8b():
+    cfg = synth.get_config("8b")
+    return cfg, synth.model_weights(cfg)
+
+
+@pytest.mark.parametrize("ctx", [2048, 8192])
+def test_8b_decode_at_context(gpu_lib, w8b, ctx):
+    """Llama-3.1-8B shape, Q8_0, batch-1 decode at KV context 2048 and 8192
+    (the KV filled by prefill of seeded tokens).  The full 32-layer model's
+    residual stream after layers 0 and 1 is checked against the oracle for
+    the last prompt token and each decode step; the model cut to 2 layers
+    (same kernels and launch shapes, full width and vocabulary) is checked
+    end to end, logits included."""
+    torch = _torch()
+    cfg, w = w8b
+    D = 4
+    prompt = synth.prompt_tokens(cfg, ctx, seed=1)
+    toks = synth.prompt_tokens(cfg, D, seed=5)          # seeded decode inputs
+    c2 = cut(cfg, 2)
+    w2 = dict(w, layers=w["layers"][:2])
+    orc = OracleModel(c2, w2, cache_bytes=12 * GB)
+    oseq = orc.new_seq(capacity=ctx + D)
+    ref_pre_layers = []
+    ref_pre = orc.prefill(oseq, prompt, capture=ref_pre_layers)
+    ref_layers, ref_logits = [], []
+    for i in range(D):
+        cap = []
+        ref_logits.append(orc.decode_step(oseq, int(toks[i]), ctx + i, capture=cap))
+        ref_layers.append(cap)
+
+    # the full model: layers 0 and 1 of its residual stream
+    m, stream = gpu_model(cfg, w, max_seqs=1, max_ctx=ctx + D + 8)
+    try:
+        seq = m.seq_create()
+        got = captured(m, stream, cfg, lambda: m.prefill(seq, prompt))
+        for l in range(2):
+            assert_close(got[l], ref_pre_layers[l], f"32-layer model, prefill, layer {l}")
+        for i in range(D):
+            got = captured(m, stream, cfg, lambda: m.decode_step(seq, int(toks[i]), ctx + i))
+            for l in range(2):
+                assert_close(got[l], ref_layers[i][l], f"32-layer model, decode step {i}, layer {l}")
+        # graph-replayed steps (the benchmark's path) continue from the same cache
+        lg = torch.empty(cfg.vocab, device="cuda")
+        m.decode_step(seq, 7, ctx + D, lg)
+        assert np.all(np.isfinite(host(lg, stream)))
+    finally:
+        release(m)
+
+    # the model cut to 2 layers: every output
+    m, stream = gpu_model(c2, w2, max_seqs=1, max_ctx=ctx + D + 8)
+    try:
+        seq = m.seq_create()
+        lg = torch.empty(cfg.vocab, device="cuda")
+        got = captured(m, stream, c2, lambda: m.prefill(seq, prompt, lg))
+        for l in range(2):
+            assert_close(got[l], ref_pre_layers[l], f"2-layer model, prefill, layer {l}")
+        assert_close(host(lg, stream), ref_pre, "2-layer model, prefill logits")
+        kv = torch.empty(ctx, cfg.kv_dim, dtype=torch.float16, device="cuda")
+        vv = torch.empty_like(kv)
+        for l in range(2):
+            m.debug_read_kv(seq, l, kv, vv)
+            assert_close(host(kv, stream), oseq.keys(l)[:ctx].reshape(ctx, -1), f"K cache layer {l}")
+            assert_close(host(vv, stream), oseq.values(l)[:ctx].reshape(ctx, -1), f"V cache layer {l}")
+        for i in range(D):
+            m.decode_step(seq, int(toks[i]), ctx + i, lg)
+            g = host(lg, stream)
+            assert_close(g, ref_logits[i], f"2-layer model, decode step {i} logits")
+            check_greedy(g, ref_logits[i], f"2-layer model, decode step {i}")
+    finally:
+        release(m)
+
+
+def test_fork_8b_q4_0_prefix_4096_eight_branches(gpu_lib):
+    """8B shape, Q4_0: one prefill of a 4096-token seeded prefix, a KV fork
+    into 8 branch slots, then batch-8 greedy decode of 128 tokens from each
+    branch's own seeded start token.  Full model: the fork copies every
+    layer's K/V bit for bit, and the forked branches decode exactly like 8
+    independent prefills of the prefix.  Model cut to 2 layers: the branches'
+    batch-8 logits against the oracle's forked branches (teacher-forced)."""
+    torch = _torch()
+    cfg = synth.get_config("fork8b")
+    P, B, D = cfg.workload["prefix"], cfg.workload["branches"], cfg.workload["decode"]
+    w = synth.model_weights(cfg)
+    prefix = synth.prompt_tokens(cfg, P, seed=1)
+    start = [100 + b for b in range(B)]
+    m, stream = gpu_model(cfg, w, max_seqs=2 * B + 1, max_ctx=P + D + 8, max_batch=B)
+    try:
+        src = m.seq_create()
+        m.prefill(src, prefix)
+        dsts = [m.seq_create() for _ in range(B)]
+        m.kv_fork(src, dsts)
+        ks = torch.empty(P, cfg.kv_dim, dtype=torch.float16, device="cuda")
+        vs, kd, vd = torch.empty_like(ks), torch.empty_like(ks), torch.empty_like(ks)
+        for l in range(cfg.n_layers):
+            m.debug_read_kv(src, l, ks, vs)
+            for d in dsts:
+                assert m.seq_length(d) == P
+                m.debug_read_kv(d, l, kd, vd)
+                stream.synchronize()
+                assert torch.equal(kd.view(torch.int16), ks.view(torch.int16)), f"K layer {l}"
+                assert torch.equal(vd.view(torch.int16), vs.view(torch.int16)), f"V layer {l}"
+        last_f = torch.empty(B, cfg.vocab, device="cuda")
+        toks_f = m.generate(dsts, start, D, last_f)
+        indep = []
+        for _ in range(B):
+            s = m.seq_create()
+            m.prefill(s, prefix)
+            indep.append(s)
+        last_i = torch.empty_like(last_f)
+        toks_i = m.generate(indep, start, D, last_i)
+        stream.synchronize()
+        assert np.array_equal(toks_f, toks_i)
+        assert torch.equal(last_f, last_i)
+        for s in dsts + indep:
+            assert m.seq_length(s) == P + D
+    finally:
+        release(m)
+
+    c2 = cut(cfg, 2)
+    w2 = dict(w, layers=w["layers"][:2])
+    del w
+    Do = 3
+    orc = OracleModel(c2, w2, cache_bytes=12 * GB)
+    oseq = orc.new_seq(capacity=P + Do)
+    orc.prefill(oseq, prefix)
+    branches = [oseq.fork() for _ in range(B)]
+    m, stream = gpu_model(c2, w2, max_seqs=B + 1, max_ctx=P + Do + 8, max_batch=B)
+    try:
+        src = m.seq_create()
+        m.prefill(src, prefix)
+        dsts = [m.seq_create() for _ in range(B)]
+        m.kv_fork(src, dsts)
+        toks = list(start)
+        out = torch.empty(B, cfg.vocab, device="cuda")
+        for i in range(Do):
+            m.decode_batch(dsts, toks, [P + i] * B, out)
+            got = host(out, stream)
+            for b in range(B):
+                ref = orc.decode_step(branches[b], toks[b], P + i)
+                assert_close(got[b], ref, f"branch {b} step {i}")
+                toks[b] = check_greedy(got[b], ref, f"branch {b} step {i}")
+    finally:
+        release(m)
+
+
+def test_70b_q4_0_resident_and_streamed(gpu_lib):
+    """70B shape, Q4_0, batch-1 decode at context 4096.  Full 80-layer model:
+    a 24 GB device budget keeps the first layers resident and streams the
+    rest through the two staging buffers; its greedy tokens and logits equal
+    the fully resident model's.  Model cut to 1 layer (full width, 64/8 heads,
+    FFN 28672): resident and streamed runs against the oracle."""
+    torch = _torch()
+    cfg = synth.get_config("70b")
+    ctx = cfg.workload["ctx"]
+    D = 4
+    prompt = synth.prompt_tokens(cfg, ctx, seed=1)
+
+    c1 = cut(cfg, 1)
+    w1 = synth.model_weights(c1)
+    orc = OracleModel(c1, w1, cache_bytes=16 * GB)
+    oseq = orc.new_seq(capacity=ctx + D)
+    ref_pre = orc.prefill(oseq, prompt)
+    toks = [int(np.argmax(ref_pre))]
+    ref_logits = []
+    for i in range(D):
+        ref_logits.append(orc.decode_step(oseq, toks[-1], ctx + i))
+        toks.append(ops.greedy(ref_logits[-1]))
+    del orc
+    m, stream = gpu_model(c1, w1, max_seqs=1, max_ctx=ctx + D + 8)
+    try:
+        for n_res in (1, 0):
+            m.set_resident_layers(n_res)
+            assert m.resident_layers() == n_res
+            seq = m.seq_create()
+            lg = torch.empty(cfg.vocab, device="cuda")
+            m.prefill(seq, prompt, lg)
+            assert_close(host(lg, stream), ref_pre, f"resident={n_res} prefill logits")
+            for i in range(D):
+                m.decode_step(seq, toks[i], ctx + i, lg)
+                g = host(lg, stream)
+                assert_close(g, ref_logits[i], f"resident={n_res} decode step {i}")
+                check_greedy(g, ref_logits[i], f"resident={n_res} decode step {i}")
+            m.seq_free(seq)
+    finally:
+        release(m)
+    del w1
+
+    w = synth.model_weights(cfg)
+    runs = {}
+    for label, budget in (("resident", 0), ("budget", cfg.workload["budget_bytes"])):
+        m, stream = gpu_model(cfg, w, max_seqs=1, max_ctx=ctx + D + 8, device_budget_bytes=budget)
+        try:
+            if budget:
+                assert 0 < m.resident_layers() < cfg.n_layers
+                assert m.device_bytes() <= budget
+            seq = m.seq_create()
+            lg = torch.empty(cfg.vocab, device="cuda")
+            m.prefill(seq, prompt, lg)
+            t0 = int(np.argmax(host(lg, stream)))
+            last = torch.empty(1, cfg.vocab, device="cuda")
+            gen = m.generate([seq], [t0], D, last)
+            runs[label] = (t0, np.asarray(gen)[:, 0].copy(), host(last, stream)[0])
+        finally:
+            release(m)
+    assert runs["resident"][0] == runs["budget"][0]
+    assert np.array_equal(runs["resident"][1], runs["budget"][1])
+    assert_close(runs["budget"][2], runs["resident"][2], "streamed vs resident logits", tol=1e-4)

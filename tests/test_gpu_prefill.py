@@ -3,10 +3,11 @@ the GEMM on every matrix (one to three 128-token tiles, ragged tails), the
 per-layer residual of the last prompt token, the fp16 K/V it writes, the
 logits, a prefill that continues a sequence, and chunk-size independence.
 
-The GEMM rounds each dequantised weight d*q and each activation to fp16 once
-and accumulates the exact products in fp32.  Against an fp64 product of the
-same fp16-rounded operands it must agree to fp32 accumulation error; against
-the exact fp64 product it must meet the layer tolerance (2e-3 of L-inf).
+The GEMM feeds each dequantised weight d*q and each activation to the
+tensor cores as two fp16 planes (hi = fp16(v), lo = fp16(v - hi)) and sums
+w_hi x_hi + w_hi x_lo + w_lo x_hi in fp32, so it must track the exact fp64
+product to about 1e-5; the layers must meet the layer tolerance (2e-3 of
+L-inf).
 """
 import os
 
@@ -85,10 +86,13 @@ def test_gemm_every_matrix(setup, T):
             W = quant.matrix(w[name], cfg.vocab, cfg.hidden, cfg.wtype)
         else:
             W = quant.matrix(w["layers"][1][name], rows, cols, cfg.wtype)
-        ref16 = _f16(x) @ _f16(W).T
-        e16 = rel_err(got, ref16)
-        assert e16 <= 2e-5, f"{name} T={T}: vs fp16-operand product {e16:.3e}"
-        assert_close(got, x.astype(np.float64) @ W.T, f"gemm {name} T={T}")
+        # activations and dequantised weights enter the tensor cores as
+        # hi + lo fp16 planes (about 22 bits each): the result tracks the
+        # exact product, far inside what single fp16 operands give (~3e-4)
+        exact = x.astype(np.float64) @ W.T
+        e = rel_err(got, exact)
+        assert e <= 1e-5, f"{name} T={T}: vs the exact product {e:.3e}"
+        assert rel_err(_f16(x) @ _f16(W).T, exact) > 10 * e or e < 1e-6
 
 
 def _read_kv(m, cfg, seq, n, layer):
