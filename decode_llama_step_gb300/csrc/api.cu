@@ -934,9 +934,10 @@ int apply_resident(dls_model* m, int n) {
 // scratch once.  Without a plan the step runs as separate kernels.
 int setup_persistent(dls_model* m) {
   m->use_step = false;
-  // opt-in (DLS_STEP_KERNEL=1) until it is faster than the separate kernels
+  // the default for batch-1 steps of a resident model; DLS_STEP_KERNEL=0
+  // runs them as separate kernels instead
   const char* e = getenv("DLS_STEP_KERNEL");
-  if (!e || atoi(e) == 0) return DLS_OK;
+  if (e && atoi(e) == 0) return DLS_OK;
   if (m->resident < m->L) return DLS_OK;
   if (!m->step.fn) m->step = step_plan(m->wtype, m->H, m->q_rows, m->F, m->nh, m->nkv, m->hd, m->num_sms);
   if (!m->step.fn) return DLS_OK;
@@ -949,7 +950,7 @@ int setup_persistent(dls_model* m) {
     TRY(dev_alloc_t(m, (size_t)m->step.grid, &m->step_am, "step_argmax"));
     TRY(dev_alloc_t(m, (size_t)2, &m->step_bar, "step_barrier"));
     TRY(dev_alloc_t(m, (size_t)(5 * m->L + 8), &m->step_trace, "step_trace"));
-    TRY(dev_alloc_t(m, (size_t)(5 * m->L + 8) * m->step.grid * 4, &m->step_ctrace, "step_cta_trace"));
+    TRY(dev_alloc_t(m, (size_t)(5 * m->L + 8) * m->step.grid * 8, &m->step_ctrace, "step_cta_trace"));
     CK(cudaMemsetAsync(m->step_att_cnt, 0, m->nkv * sizeof(int), m->stream));
   }
   std::vector<StepLayer> hl(m->L);
@@ -1523,7 +1524,7 @@ int dls_debug_step_trace(dls_model* m, uint64_t* out, int32_t max_entries, int32
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
   if (!out || !n_entries || max_entries < 0) return fail(m, DLS_ERR_ARG, "output arrays");
   if (!m->use_step || !m->step_ctrace) return fail(m, DLS_ERR_STATE, "no persistent step kernel in use");
-  const size_t n = (size_t)(5 * m->L + 8) * m->step.grid * 4;
+  const size_t n = (size_t)(5 * m->L + 8) * m->step.grid * 8;
   if ((size_t)max_entries < n) return fail(m, DLS_ERR_ARG, "max_entries=%d < %zu", max_entries, n);
   TRY(sync_stream(m, m->stream));
   CK(cudaMemcpy(out, m->step_ctrace, n * sizeof(uint64_t), cudaMemcpyDeviceToHost));

@@ -117,7 +117,12 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
     const int mc = warp < nchunk ? min(MC, (nchunk - warp + nwc - 1) / nwc) : 0;
     constexpr int V4 = G::XV / 2;  // float4 per lane per chunk
     float4 raw[MC][V4];
+    float4 gg[PRO == PRO_RMSNORM ? MC : 1][V4];
     bool valid[MC];
+    // branch-free: all of the lane's float4 loads (x and gains) go out
+    // together; a slice past the matrix reads element 0 and is zeroed
+    // (cols % 4 == 0 is checked at launch: a float4 is all in or all out)
+    bool in4[MC][V4];
 #pragma unroll
     for (int k = 0; k < MC; ++k) {
       const int c = warp + k * nwc;
@@ -126,20 +131,17 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
 #pragma unroll
       for (int m4 = 0; m4 < V4; ++m4) {
         const int i0 = col0 + 4 * m4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (valid[k]) {
-          if (i0 + 3 < cols && (cols & 3) == 0) {
-            v = *reinterpret_cast<const float4*>(a.x + i0);
-          } else {
-            if (i0 < cols) v.x = a.x[i0];
-            if (i0 + 1 < cols) v.y = a.x[i0 + 1];
-            if (i0 + 2 < cols) v.z = a.x[i0 + 2];
-            if (i0 + 3 < cols) v.w = a.x[i0 + 3];
-          }
-        }
-        raw[k][m4] = v;
+        in4[k][m4] = valid[k] && i0 < cols;
+        const int j0 = in4[k][m4] ? i0 : 0;
+        raw[k][m4] = *reinterpret_cast<const float4*>(a.x + j0);
+        if (PRO == PRO_RMSNORM) gg[PRO == PRO_RMSNORM ? k : 0][m4] = *reinterpret_cast<const float4*>(a.g + j0);
       }
     }
+#pragma unroll
+    for (int k = 0; k < MC; ++k)
+#pragma unroll
+      for (int m4 = 0; m4 < V4; ++m4)
+        if (!in4[k][m4]) raw[k][m4] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (PRO == PRO_RMSNORM) {
       float ss = 0.f;
 #pragma unroll
@@ -156,27 +158,13 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) gemv_kernel(const Ge
       for (int i = 0; i < nwc; ++i) t += sh.red[i];  // fixed order, same in every thread
       const float rs = 1.0f / sqrtf(t / (float)cols + a.eps);
 #pragma unroll
-      for (int k = 0; k < MC; ++k) {
-        const int c = warp + k * nwc;
-        const int col0 = WT == 8 ? c * 512 + lane * 16 : (c * 32 + lane) * 32;
+      for (int k = 0; k < MC; ++k)
 #pragma unroll
         for (int m4 = 0; m4 < V4; ++m4) {
-          const int i0 = col0 + 4 * m4;
-          float4 gg = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (valid[k]) {
-            if (i0 + 3 < cols && (cols & 3) == 0) {
-              gg = *reinterpret_cast<const float4*>(a.g + i0);
-            } else {
-              if (i0 < cols) gg.x = a.g[i0];
-              if (i0 + 1 < cols) gg.y = a.g[i0 + 1];
-              if (i0 + 2 < cols) gg.z = a.g[i0 + 2];
-              if (i0 + 3 < cols) gg.w = a.g[i0 + 3];
-            }
-          }
-          raw[k][m4] = make_float4(raw[k][m4].x * rs * gg.x, raw[k][m4].y * rs * gg.y, raw[k][m4].z * rs * gg.z,
-                                   raw[k][m4].w * rs * gg.w);
+          const float4 g = gg[PRO == PRO_RMSNORM ? k : 0][m4];
+          raw[k][m4] = make_float4(raw[k][m4].x * rs * g.x, raw[k][m4].y * rs * g.y, raw[k][m4].z * rs * g.z,
+                                   raw[k][m4].w * rs * g.w);
         }
-      }
     }
     XQ<WT> xq[MC];
 #pragma unroll
@@ -404,7 +392,7 @@ cudaError_t gemv_setup_attributes() {
 cudaError_t launch_gemv(int wtype, int pro, int epi, const GemvArgs& a, const GemvLaunch& l, cudaStream_t s,
                         bool pdl) {
   KernelFn f = pick(wtype, pro, epi, l.rs, l.mc);
-  if (!f || l.ns > 16 || l.nwc > kMaxConsumers || a.w.ds % 8) return cudaErrorInvalidValue;
+  if (!f || l.ns > 16 || l.nwc > kMaxConsumers || a.w.ds % 8 || a.w.cols % 4) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(l.grid);
   cfg.blockDim = dim3(l.threads);

@@ -140,7 +140,7 @@ struct StepArgs {
   int S;                    // attention splits per KV head (one per CTA)
   unsigned long long* trace;  // optional: CTA 0 writes the global timer after each phase
   unsigned long long* ctrace; // optional: per phase and CTA {consumer arrival, release, producer first issue,
-                              // producer last issue}: [phase][grid][4]
+                              // producer last issue, prologue done, stages done, epilogue done, -}: [phase][grid][8]
   int ns;                   // ring stages
   uint32_t stage_bytes;     // ring slot size
 };

@@ -38,6 +38,13 @@ constexpr int kRB = 64;              // rows per epilogue block
 constexpr int kTile = 32;            // attention tokens per ring stage
 constexpr int kMaxStages = 16;
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kTr = 8;               // per-CTA trace slots per phase
+
+// Consumer-side timestamp of this CTA in the current phase (profiling only):
+// slot 4 = prologue done, 5 = last stage consumed, 6 = epilogue done.
+__device__ __forceinline__ void ctmark(const StepArgs& A, unsigned epoch, int slot) {
+  if (A.ctrace && threadIdx.x == 0) A.ctrace[((size_t)epoch * gridDim.x + blockIdx.x) * kTr + slot] = global_ns();
+}
 
 struct Sh {
   uint64_t full[kMaxStages];
@@ -94,7 +101,7 @@ __device__ __forceinline__ void grid_sync(Ctx& c) {
   named_bar(1, NWC * 32);
   if (A.trace && blockIdx.x == 0 && threadIdx.x == 0) A.trace[c.epoch + 1] = global_ns();  // phase end
   if (threadIdx.x == 0) {
-    if (A.ctrace) A.ctrace[((size_t)c.epoch * gridDim.x + blockIdx.x) * 4 + 0] = global_ns();
+    if (A.ctrace) A.ctrace[((size_t)c.epoch * gridDim.x + blockIdx.x) * kTr + 0] = global_ns();
     const unsigned target = (++c.epoch) * gridDim.x;
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(A.bar) : "memory");
     uint64_t t0 = 0;
@@ -113,7 +120,7 @@ __device__ __forceinline__ void grid_sync(Ctx& c) {
       }
       if (i >= 64) __nanosleep(32);
     }
-    if (A.ctrace) A.ctrace[((size_t)(c.epoch - 1) * gridDim.x + blockIdx.x) * 4 + 1] = global_ns();
+    if (A.ctrace) A.ctrace[((size_t)(c.epoch - 1) * gridDim.x + blockIdx.x) * kTr + 1] = global_ns();
   }
   named_bar(1, NWC * 32);
 }
@@ -289,7 +296,7 @@ __device__ void produce(Ctx& c) {
     if (!next_chunk<WT, HD, RSA, RSB>(c, R, rc, ch)) break;
     const int phase = 1 + 5 * rc.l + (rc.l < A.n_layers ? rc.ph : 0);
     if (A.ctrace) {
-      unsigned long long* t = A.ctrace + ((size_t)phase * gridDim.x + blockIdx.x) * 4;
+      unsigned long long* t = A.ctrace + ((size_t)phase * gridDim.x + blockIdx.x) * kTr;
       const unsigned long long now = global_ns();
       if (phase != last_phase) t[2] = now;
       t[3] = now;
@@ -354,31 +361,11 @@ __device__ __forceinline__ void load_x(Ctx& c, const MatDev& w, const float* x, 
   const int mc = warp < nchunk ? min(MC, (nchunk - warp + NWC - 1) / NWC) : 0;
   float4 raw[MC][V4];
   float4 gg[PRO == PRO_RMSNORM ? MC : 1][V4];
-  if (PRO == PRO_RMSNORM) {
-    // the gains are weights: their loads go out together with x's
-#pragma unroll
-    for (int k = 0; k < MC; ++k) {
-      const int ch = warp + k * NWC;
-      const int col0 = WT == 8 ? ch * 512 + lane * 16 : (ch * 32 + lane) * 32;
-      const bool vk = k < mc && col0 < kpad;
-#pragma unroll
-      for (int m4 = 0; m4 < V4; ++m4) {
-        const int i0 = col0 + 4 * m4;
-        float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (vk) {
-          if (i0 + 3 < cols && (cols & 3) == 0) {
-            g = *reinterpret_cast<const float4*>(gain + i0);
-          } else {
-            if (i0 < cols) g.x = gain[i0];
-            if (i0 + 1 < cols) g.y = gain[i0 + 1];
-            if (i0 + 2 < cols) g.z = gain[i0 + 2];
-            if (i0 + 3 < cols) g.w = gain[i0 + 3];
-          }
-        }
-        gg[PRO == PRO_RMSNORM ? k : 0][m4] = g;
-      }
-    }
-  }
+  // branch-free: every float4 of the lane's slices is loaded at once (a
+  // slice past the matrix reads element 0 and is zeroed afterwards), so the
+  // loads of all chunks, x and gains, are in flight together.  cols % 4 == 0
+  // (checked when the kernel is planned): a float4 is all in or all out.
+  bool in4[MC][V4];
 #pragma unroll
   for (int k = 0; k < MC; ++k) {
     const int ch = warp + k * NWC;
@@ -387,20 +374,17 @@ __device__ __forceinline__ void load_x(Ctx& c, const MatDev& w, const float* x, 
 #pragma unroll
     for (int m4 = 0; m4 < V4; ++m4) {
       const int i0 = col0 + 4 * m4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (valid[k]) {
-        if (i0 + 3 < cols && (cols & 3) == 0) {
-          v = __ldcg(reinterpret_cast<const float4*>(x + i0));
-        } else {
-          if (i0 < cols) v.x = __ldcg(x + i0);
-          if (i0 + 1 < cols) v.y = __ldcg(x + i0 + 1);
-          if (i0 + 2 < cols) v.z = __ldcg(x + i0 + 2);
-          if (i0 + 3 < cols) v.w = __ldcg(x + i0 + 3);
-        }
-      }
-      raw[k][m4] = v;
+      in4[k][m4] = valid[k] && i0 < cols;
+      const int j0 = in4[k][m4] ? i0 : 0;
+      raw[k][m4] = __ldcg(reinterpret_cast<const float4*>(x + j0));
+      if (PRO == PRO_RMSNORM) gg[PRO == PRO_RMSNORM ? k : 0][m4] = *reinterpret_cast<const float4*>(gain + j0);
     }
   }
+#pragma unroll
+  for (int k = 0; k < MC; ++k)
+#pragma unroll
+    for (int m4 = 0; m4 < V4; ++m4)
+      if (!in4[k][m4]) raw[k][m4] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (PRO == PRO_RMSNORM) {
     float ss = 0.f;
 #pragma unroll
@@ -445,6 +429,7 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
   XQ<WT> xq[MC];
   bool valid[MC];
   load_x<WT, PRO, MC>(c, w, x, gain, xq, valid);
+  ctmark(A, c.epoch, 4);
   int r0, r1;
   row_split(w.rows, unit, r0, r1);
   const int nrows = max(r1 - r0, 0);
@@ -454,6 +439,16 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
   const int nchunk = (kpad + Gm::CH - 1) / Gm::CH;
   const int nwa = min(NWC, nchunk);
   constexpr int spb = kRB / RS;  // stages per epilogue block
+  // residual rows of the first two epilogue blocks, read before the stages
+  // arrive (no other CTA writes this CTA's rows during the phase)
+  float res_pre[2] = {0.f, 0.f};
+  if (EPI == EPI_RESID && tid < kRB) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const int r = r0 + b * kRB + tid;
+      if (r < r1) res_pre[b] = __ldcg(e.y + r);
+    }
+  }
   // RoPE factors of this thread's pair in the first two epilogue blocks,
   // loaded before the stages arrive (the position is fixed for the step)
   float2 cs_pre[2] = {make_float2(1.f, 0.f), make_float2(1.f, 0.f)};
@@ -499,6 +494,7 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
 
     if ((s + 1) % spb == 0 || s == nst - 1) {
       named_bar(1, NWC * 32);
+      if (s == nst - 1) ctmark(A, c.epoch, 5);
       const int b0 = r0 + (s / spb) * kRB;
       const int bn = min(kRB, r1 - b0);
       if (EPI == EPI_QKV || EPI == EPI_SWIGLU) {
@@ -547,13 +543,19 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
         for (int lr = tid; lr < bn; lr += NWC * 32) {
           float v = 0.f;
           for (int ww = 0; ww < nwa; ++ww) v += c.s_part[ww * kRB + lr];
-          if (EPI == EPI_RESID) e.y[b0 + lr] = __ldcg(e.y + b0 + lr) + v;
-          else e.y[b0 + lr] = v;
+          if (EPI == EPI_RESID) {
+            const int blk = s / spb;
+            const float old = (lr == tid && blk < 2) ? (blk == 0 ? res_pre[0] : res_pre[1]) : __ldcg(e.y + b0 + lr);
+            e.y[b0 + lr] = old + v;
+          } else {
+            e.y[b0 + lr] = v;
+          }
         }
       }
       named_bar(1, NWC * 32);
     }
   }
+  ctmark(A, c.epoch, 6);
 }
 
 __device__ __forceinline__ float warp_max_f(float v) {
@@ -590,6 +592,7 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
     for (int i = tid; i < G * HD; i += NWC * 32) c.s_q[i] = __ldcg(qrow + i) * scale;
   }
   named_bar(1, NWC * 32);
+  ctmark(A, c.epoch, 4);
   float m_run[HPW], l_run[HPW], o[HPW][DPL];
 #pragma unroll
   for (int h = 0; h < HPW; ++h) {
@@ -677,6 +680,7 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
     ++c.sidx;
   }
   // merge the TS warps of each head group
+  ctmark(A, c.epoch, 5);
   if (lane == 0) {
 #pragma unroll
     for (int h = 0; h < HPW; ++h) {
@@ -719,39 +723,61 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
   }
   named_bar(1, NWC * 32);
   if (c.sh->last) {
-    // merge the S splits of this KV head in split order (running max form),
-    // loads issued in blocks of kMB so they are in flight together
-    constexpr int kMB = 20;
+    // merge the S splits of this KV head in split order: every thread's
+    // partial loads go out first, one warp per head turns the (m, l) pairs
+    // into split weights exp(m_s - M) / sum_s l_s exp(m_s - M), then each
+    // output is the weighted sum of its S partials
+    constexpr int kOut = (G * HD + NWC * 32 - 1) / (NWC * 32);  // outputs per thread
+    constexpr int kMB = kOut <= 2 ? 20 : 1;                      // splits loaded up front
     const size_t slot0 = (size_t)kvh * A.S;
     const float2* ml = reinterpret_cast<const float2*>(A.part_ml);
-    for (int idx = tid; idx < G * HD; idx += NWC * 32) {
-      const int h = idx / HD;
-      const float* po = A.part_o + slot0 * G * HD + idx;
-      float M = -INFINITY, Ls = 0.f, acc = 0.f;
-      for (int s0 = 0; s0 < A.S; s0 += kMB) {
-        float2 mv[kMB];
-        float pv[kMB];
+    float* s_w = c.s_wo;  // [G][S] (G * S <= NWC * G * HD)
+    const bool one_round = A.S <= kMB;
+    float pv[kOut][kMB];
 #pragma unroll
-        for (int k = 0; k < kMB; ++k) {
-          const int sk = s0 + k;
-          mv[k] = sk < A.S ? __ldcg(&ml[(slot0 + sk) * G + h]) : make_float2(-INFINITY, 0.f);
-          pv[k] = sk < A.S ? __ldcg(po + (size_t)sk * G * HD) : 0.f;
-        }
+    for (int oi = 0; oi < kOut; ++oi) {
+      const int idx = tid + oi * NWC * 32;
 #pragma unroll
-        for (int k = 0; k < kMB; ++k) {
-          if (mv[k].y > 0.f) {  // empty split: nothing to add
-            const float Mn = fmaxf(M, mv[k].x);
-            const float ea = expf(M - Mn), eb = expf(mv[k].x - Mn);
-            acc = acc * ea + pv[k] * eb;
-            Ls = Ls * ea + mv[k].y * eb;
-            M = Mn;
-          }
-        }
+      for (int k = 0; k < kMB; ++k)
+        pv[oi][k] = (one_round && k < A.S && idx < G * HD) ? __ldcg(A.part_o + (slot0 + k) * G * HD + idx) : 0.f;
+    }
+    for (int h = warp; h < G; h += NWC) {
+      float M = -INFINITY;
+      for (int s2 = lane; s2 < A.S; s2 += 32) M = fmaxf(M, __ldcg(&ml[(slot0 + s2) * G + h]).x);
+      M = warp_max_f(M);
+      float den = 0.f;
+      for (int s2 = lane; s2 < A.S; s2 += 32) {
+        const float2 v = __ldcg(&ml[(slot0 + s2) * G + h]);
+        const float ew = v.y > 0.f ? expf(v.x - M) : 0.f;  // empty split: weight 0
+        s_w[h * A.S + s2] = ew;
+        den = fmaf(v.y, ew, den);
       }
-      A.o[(size_t)kvh * G * HD + idx] = acc / Ls;
+      den = warp_sum(den);
+      const float inv = 1.0f / den;
+      __syncwarp();
+      for (int s2 = lane; s2 < A.S; s2 += 32) s_w[h * A.S + s2] *= inv;
+    }
+    named_bar(1, NWC * 32);
+#pragma unroll
+    for (int oi = 0; oi < kOut; ++oi) {
+      const int idx = tid + oi * NWC * 32;
+      if (idx >= G * HD) continue;
+      const float* wv = s_w + (idx / HD) * A.S;
+      float acc = 0.f;
+      if (one_round) {
+#pragma unroll
+        for (int k = 0; k < kMB; ++k)
+          if (k < A.S) acc = fmaf(wv[k], pv[oi][k], acc);
+      } else {
+        const float* po = A.part_o + slot0 * G * HD + idx;
+#pragma unroll 8
+        for (int s2 = 0; s2 < A.S; ++s2) acc = fmaf(wv[s2], __ldcg(po + (size_t)s2 * G * HD), acc);
+      }
+      A.o[(size_t)kvh * G * HD + idx] = acc;
     }
     if (tid == 0) A.att_counters[kvh] = 0;
   }
+  ctmark(A, c.epoch, 6);
 }
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
@@ -759,7 +785,7 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 }
 
 template <int WT, int HD, int G, int RSA, int MCA, int RSB, int MCB>
-__global__ void __launch_bounds__(NTHR, 1) step_kernel(const StepArgs A) {
+__global__ void __maxnreg__(224) step_kernel(const StepArgs A) {
   extern __shared__ __align__(128) uint8_t smem[];
   Ctx c;
   c.A = &A;
@@ -920,17 +946,18 @@ struct Variant {
 // The shapes with a persistent-kernel instantiation (others use the
 // multi-kernel step).
 const Variant kVariants[] = {
-    {8, 128, 4, 4, 1, 1, 4, &step_fn<8, 128, 4, 4, 1, 1, 4>},  // 8B-shape Q8_0
-    {4, 128, 4, 8, 1, 2, 2, &step_fn<4, 128, 4, 8, 1, 2, 2>},  // 8B-shape Q4_0
-    {8, 64, 4, 8, 1, 2, 2, &step_fn<8, 64, 4, 8, 1, 2, 2>},    // 1B-shape Q8_0
+    {8, 128, 4, 8, 1, 2, 4, &step_fn<8, 128, 4, 8, 1, 2, 4>},  // 8B-shape Q8_0
+    {4, 128, 4, 8, 1, 4, 2, &step_fn<4, 128, 4, 8, 1, 4, 2>},  // 8B-shape Q4_0
+    {8, 64, 4, 8, 1, 4, 2, &step_fn<8, 64, 4, 8, 1, 4, 2>},    // 1B-shape Q8_0
     {8, 64, 2, 8, 1, 8, 1, &step_fn<8, 64, 2, 8, 1, 8, 1>},    // tiny Q8_0
     {4, 64, 2, 8, 1, 8, 1, &step_fn<4, 64, 2, 8, 1, 8, 1>},    // tiny Q4_0
-    {4, 128, 8, 4, 1, 1, 4, &step_fn<4, 128, 8, 4, 1, 1, 4>},  // 70B-shape Q4_0
+    {4, 128, 8, 8, 1, 2, 4, &step_fn<4, 128, 8, 8, 1, 2, 4>},  // 70B-shape Q4_0
 };
 
+// rows per ring stage: as many whole rows as fit 32 KB of codes, at most 8
 int pow2_rows(int row_bytes) {
   int rs = 1;
-  while (rs < 8 && (rs * 2) * row_bytes <= 16384) rs *= 2;
+  while (rs < 8 && (rs * 2) * row_bytes <= 32768) rs *= 2;
   return rs;
 }
 
@@ -940,6 +967,7 @@ StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, i
   StepPlan p{};
   p.fn = nullptr;
   if (q_rows != H) return p;  // O projection must share the hidden-size geometry
+  if (H % 4 || F % 4) return p;  // activation slices are read as whole float4
   const int G = n_heads / n_kv;
   const int nb_h = (H + 31) / 32, nb_f = (F + 31) / 32;
   const int rb_h = wtype == 8 ? nb_h * 32 : nb_h * 16, rb_f = wtype == 8 ? nb_f * 32 : nb_f * 16;

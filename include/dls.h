@@ -290,12 +290,13 @@ int dls_debug_gemm(dls_model* m, int32_t layer, int32_t tensor, int32_t n_tokens
 int dls_debug_profile_step(dls_model* m, int32_t seq, int32_t token, int32_t pos, int32_t max_kernels,
                            float* kernel_ms, int32_t* kernel_kind, int32_t* n_kernels);
 /* Per-CTA phase timestamps (global timer, ns) of the last profiled step of
- * the persistent step kernel: [phase][cta][4] = {consumer arrival at the
+ * the persistent step kernel: [phase][cta][8] = {consumer arrival at the
  * grid barrier that ends the phase, its release, producer's first issue of
- * the phase's copies, producer's last issue}; phase 0 is the embedding,
+ * the phase's copies, producer's last issue, consumers' prologue done, last
+ * stage consumed, epilogue done, unused}; phase 0 is the embedding,
  * 1 + 5 l + k layer l's k-th phase (QKV, attention, O, gate/up, down), then
  * the LM head.  Entries not written hold stale values.  Copies
- * (5 n_layers + 8) * grid * 4 values to host `out`; DLS_ERR_STATE when the
+ * (5 n_layers + 8) * grid * 8 values to host `out`; DLS_ERR_STATE when the
  * step does not run as the persistent kernel.  Profiling only. */
 int dls_debug_step_trace(dls_model* m, uint64_t* out, int32_t max_entries, int32_t* n_entries);
 /* Kernel launches issued by the last decode / generate step (all of this

@@ -36,6 +36,7 @@ def setup(request, gpu_lib):
     os.environ["DLS_STEP_KERNEL"] = step_kernel
     try:
         m = dls.Model(cfg, w, max_seqs=6, max_ctx=160, max_batch=4, page_tokens=32, stream=stream)
+        m.step_kernel = step_kernel
     finally:
         if old is None:
             del os.environ["DLS_STEP_KERNEL"]
@@ -162,8 +163,7 @@ def test_persistent_step_matches_separate_kernels(setup, monkeypatch):
     torch = _torch()
     from decode_llama_step_gb300 import dls
     cfg, w, m, orc, stream = setup
-    import os
-    other = "1" if os.environ.get("DLS_STEP_KERNEL") == "0" else "0"
+    other = "0" if m.step_kernel == "1" else "1"   # the other decode path
     monkeypatch.setenv("DLS_STEP_KERNEL", other)
     m2 = dls.Model(cfg, w, max_seqs=2, max_ctx=160, page_tokens=32, stream=stream)
     monkeypatch.delenv("DLS_STEP_KERNEL")
