@@ -175,6 +175,13 @@ def run_fork(args):
         dsts = [m.seq_create() for _ in range(B)]
         m.kv_fork(src, dsts)
         t_dec = _events(torch, stream, lambda: m.generate(dsts, start, D))
+        # per-kind device time of one batched step (kernels timed one by one)
+        kms, kk = m.profile_batch(dsts, start, [m.seq_length(d) for d in dsts])
+        per_kind = {}
+        for d_ms, k in zip(kms, kk):
+            e = per_kind.setdefault(KIND_NAMES.get(int(k), str(int(k))), {"launches_per_step": 0, "ms_per_step": 0.0})
+            e["launches_per_step"] += 1
+            e["ms_per_step"] = round(e["ms_per_step"] + float(d_ms), 4)
         for d in dsts:
             m.seq_free(d)
         m.seq_free(src)
@@ -198,7 +205,7 @@ def run_fork(args):
                                "decode_ms": round(1000 * t_dec, 2), "decode_tok_s": round(B * D / t_dec, 1),
                                "fork_path_s": round(fork_path, 4), "independent_prefills_path_s": round(indep_path, 4),
                                "speedup_vs_independent": round(indep_path / fork_path, 3)},
-                      "clocks": clk.summary()})
+                      "kernels": per_kind, "clocks": clk.summary()})
 
 
 def h2d_peak(torch, chunk=256 << 20, inflight=4, reps=10):

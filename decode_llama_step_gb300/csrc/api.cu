@@ -1520,6 +1520,49 @@ int dls_debug_profile_step(dls_model* m, int32_t seq, int32_t token, int32_t pos
   return DLS_OK;
 }
 
+int dls_debug_profile_batch(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* tokens, const int32_t* pos,
+                            int32_t max_kernels, float* kernel_ms, int32_t* kernel_kind, int32_t* n_kernels) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (!kernel_ms || !kernel_kind || !n_kernels || max_kernels < 1) return fail(m, DLS_ERR_ARG, "output arrays");
+  if (n < 2 || n > m->max_batch || !seqs || !tokens || !pos)
+    return fail(m, DLS_ERR_ARG, "n=%d max_batch=%d (batches of 2 or more rows)", n, m->max_batch);
+  for (int i = 0; i < n; ++i) {
+    TRY(check_seq(m, seqs[i]));
+    for (int j = 0; j < i; ++j)
+      if (seqs[j] == seqs[i]) return fail(m, DLS_ERR_ARG, "seq=%d repeated", seqs[i]);
+    if (tokens[i] < 0 || tokens[i] >= m->V) return fail(m, DLS_ERR_ARG, "token[%d]=%d", i, tokens[i]);
+    if (pos[i] != m->seqs[seqs[i]].len)
+      return fail(m, DLS_ERR_STATE, "seq=%d pos=%d length=%d", seqs[i], pos[i], m->seqs[seqs[i]].len);
+    if (pos[i] >= m->max_ctx) return fail(m, DLS_ERR_CAPACITY, "seq=%d pos=%d", seqs[i], pos[i]);
+  }
+  int need = 0;
+  for (int i = 0; i < n; ++i)
+    need += std::max(0, pages_needed(m, pos[i] + 1) - (int)m->seqs[seqs[i]].pages.size());
+  if (need > (int)m->free_pages.size()) return fail(m, DLS_ERR_CAPACITY, "need_pages=%d free=%zu", need, m->free_pages.size());
+  for (int i = 0; i < n; ++i) TRY(ensure_pages(m, seqs[i], pos[i] + 1));
+  TRY(set_params(m, n, seqs, tokens, pos, true));
+  // hold the GPU so the whole step is queued before it starts
+  CK(launch_delay(2000000, m->stream));
+  m->prof_kinds.clear();
+  m->profiling = true;
+  TRY(prof_mark(m, 0));
+  const int r = enqueue_step(m, n, true, false, nullptr);
+  m->profiling = false;
+  TRY(r);
+  TRY(sync_stream(m, m->stream));
+  const int nk = (int)m->prof_kinds.size() - 1;
+  if (nk > max_kernels) return fail(m, DLS_ERR_ARG, "max_kernels=%d < %d launches", max_kernels, nk);
+  for (int i = 0; i < nk; ++i) {
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, m->prof_events[i], m->prof_events[i + 1]));
+    kernel_ms[i] = ms;
+    kernel_kind[i] = m->prof_kinds[i + 1];
+  }
+  *n_kernels = nk;
+  for (int i = 0; i < n; ++i) m->seqs[seqs[i]].len += 1;
+  return DLS_OK;
+}
+
 int dls_debug_step_trace(dls_model* m, uint64_t* out, int32_t max_entries, int32_t* n_entries) {
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
   if (!out || !n_entries || max_entries < 0) return fail(m, DLS_ERR_ARG, "output arrays");

@@ -63,10 +63,20 @@ struct Ctx {
   float* s_wl;     // [NWC][G]
   float* s_wo;     // [NWC][G*HD]
   int sidx;        // ring stages consumed / produced so far
+  int slot;        // sidx % ns
+  uint32_t par;    // (sidx / ns) & 1: the phase parity of the current slot's use
   unsigned epoch;  // grid barriers passed (thread 0)
   int pos, seq;
   int pos_page;    // page holding position pos, -1 if none
 };
+
+__device__ __forceinline__ void advance(Ctx& c, int ns) {
+  ++c.sidx;
+  if (++c.slot == ns) {
+    c.slot = 0;
+    c.par ^= 1u;
+  }
+}
 
 __device__ __forceinline__ bool aborted(const StepArgs& A) { return *(volatile int*)A.abort != 0; }
 
@@ -162,17 +172,22 @@ struct PCur {
   const uint8_t* d;
   uint32_t rb, db;
   int rs, row, row_end;
-  // attention phase
-  int tb;
+  // attention phase: tiles [tb, te) of this CTA's task
+  int tb, te;
   const __half* kp;
   const __half* vp;
 };
 
+// One ring stage's copies: codes at 0 and scales at off_b (RS rows of a
+// GEMV), or K at 0 and V at off_b of a 32-token tile, plus K2 and V2 of the
+// next tile at 2 and 3 tile sizes (attention: two tiles per stage).
 struct Chunk {
   const uint8_t* a;
   const uint8_t* b;
-  uint32_t na, nb;   // bytes of each range (both 0: an empty stage)
-  uint32_t off_b;    // stage offset of the second range
+  const uint8_t* a2;
+  const uint8_t* b2;
+  uint32_t na, nb, n2;  // bytes (all 0: an empty stage)
+  uint32_t off_b;
   bool bad_page;
 };
 
@@ -213,9 +228,9 @@ __device__ void begin_phase(const Ctx& c, const Rows& R, PCur& u) {
   switch (u.ph) {
     case 0: gemv_phase<WT>(u, L.qkv, R.qkv0, R.qkv1, RSA); break;
     case 1: {
-      int kvh, te;
-      attn_task(A, c.pos + 1, kvh, u.tb, te);
-      u.n = max(0, te - u.tb);
+      int kvh;
+      attn_task(A, c.pos + 1, kvh, u.tb, u.te);
+      u.n = max(0, (u.te - u.tb + 1) / 2);  // two tiles per stage
       const size_t head_off = (size_t)kvh * A.page_tokens * HD;
       u.kp = L.k_pool + head_off;
       u.vp = L.v_pool + head_off;
@@ -245,19 +260,32 @@ __device__ bool next_chunk(const Ctx& c, const Rows& R, PCur& u, Chunk& ch) {
     begin_phase<WT, HD, RSA, RSB>(c, R, u);
   }
   ch.bad_page = false;
+  ch.n2 = 0;
   if (u.l < A.n_layers && u.ph == 1) {
-    const int t = u.tb + u.i;
+    // tiles 2i and 2i + 1 of the task: K | V | K2 | V2
+    ch.na = ch.nb = 0;
+    ch.off_b = kTile * HD * 2;
+    const int t = u.tb + 2 * u.i;
     // positions before pos are final; pos itself is written by this step
     const int n_old = max(0, min(kTile, c.pos - t * kTile));
     const int page = A.page_table[(size_t)c.seq * A.max_pages + (t * kTile) / A.page_tokens];
-    ch.na = ch.nb = 0;
-    ch.off_b = kTile * HD * 2;
     ch.bad_page = page < 0;
     if (n_old > 0 && page >= 0) {
       const size_t base = ((size_t)page * A.n_kv * A.page_tokens + (t * kTile) % A.page_tokens) * HD;
       ch.a = reinterpret_cast<const uint8_t*>(u.kp + base);
       ch.b = reinterpret_cast<const uint8_t*>(u.vp + base);
       ch.na = ch.nb = (uint32_t)n_old * HD * 2;
+    }
+    if (t + 1 < u.te) {
+      const int n_old2 = max(0, min(kTile, c.pos - (t + 1) * kTile));
+      const int page2 = A.page_table[(size_t)c.seq * A.max_pages + ((t + 1) * kTile) / A.page_tokens];
+      ch.bad_page |= page2 < 0;
+      if (n_old2 > 0 && page2 >= 0) {
+        const size_t base = ((size_t)page2 * A.n_kv * A.page_tokens + ((t + 1) * kTile) % A.page_tokens) * HD;
+        ch.a2 = reinterpret_cast<const uint8_t*>(u.kp + base);
+        ch.b2 = reinterpret_cast<const uint8_t*>(u.vp + base);
+        ch.n2 = (uint32_t)n_old2 * HD * 2;
+      }
     }
   } else {
     const int n = min(u.rs, u.row_end - u.row);
@@ -302,10 +330,10 @@ __device__ void produce(Ctx& c) {
       t[3] = now;
       last_phase = phase;
     }
-    const int slot = c.sidx % A.ns;
+    const int slot = c.slot;
     if (c.sidx >= A.ns) {
       const uint32_t bar = smem_u32(&c.sh->empty[slot]);
-      const uint32_t parity = ((c.sidx / A.ns) - 1) & 1;
+      const uint32_t parity = c.par ^ 1u;  // the slot's previous use
       if (!mbar_try_wait(bar, parity)) {
         const uint64_t t0 = global_ns();
         bool ok = true;
@@ -330,14 +358,19 @@ __device__ void produce(Ctx& c) {
     const uint32_t bar = smem_u32(&c.sh->full[slot]);
     uint8_t* dst = c.ring + (size_t)slot * A.stage_bytes;
     if (ch.bad_page) atomicOr(&A.sp->status, kBadPage);
-    if (ch.na + ch.nb == 0) {
+    const uint32_t total = ch.na + ch.nb + 2 * ch.n2;
+    if (total == 0) {
       mbar_arrive(bar);
     } else {
-      mbar_expect_tx(bar, ch.na + ch.nb);
-      bulk_g2s(smem_u32(dst), ch.a, ch.na, bar);
+      mbar_expect_tx(bar, total);
+      if (ch.na) bulk_g2s(smem_u32(dst), ch.a, ch.na, bar);
       if (ch.nb) bulk_g2s(smem_u32(dst + ch.off_b), ch.b, ch.nb, bar);
+      if (ch.n2) {
+        bulk_g2s(smem_u32(dst + 2 * kTile * HD * 2), ch.a2, ch.n2, bar);
+        bulk_g2s(smem_u32(dst + 3 * kTile * HD * 2), ch.b2, ch.n2, bar);
+      }
     }
-    ++c.sidx;
+    advance(c, A.ns);
   }
   // never leave with copies in flight
   for (int s = max(0, c.sidx - A.ns); s < c.sidx; ++s) {
@@ -460,8 +493,8 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
     }
   }
   for (int s = 0; s < nst; ++s) {
-    const int slot = c.sidx % A.ns;
-    const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), (c.sidx / A.ns) & 1, 20);
+    const int slot = c.slot;
+    const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), c.par, 20);
     const int rows_s = min(RS, nrows - s * RS);
     const uint32_t st = smem_u32(c.ring) + (uint32_t)slot * A.stage_bytes;
     float acc[RS];
@@ -486,7 +519,7 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&c.sh->empty[slot]));
-    ++c.sidx;
+    advance(c, A.ns);
     const float t = butterfly<RS>(acc, lane);
     const int rr = RS == 1 ? 0 : (lane >> (5 - (RS == 2 ? 1 : RS == 4 ? 2 : 3)));
     const int lrow = s * RS + rr - (s / spb) * kRB;
@@ -564,23 +597,25 @@ __device__ __forceinline__ float warp_max_f(float v) {
   return v;
 }
 
-// One CTA's attention task: split sp of KV head kvh, tiles tb .. te-1 (one
-// ring stage each).  The consumer warps form TS tile slots x HG head groups:
-// warp w scores the tiles j with j % TS == w % TS for the HPW query heads of
-// group w / TS, so every warp has work when the task holds TS tiles or more.
-// Position pos (written by this step's QKV phase) is copied from global
-// into its tile before scoring.  The TS warps of a head group merge in
-// shared memory into one (m, l, o) partial per CTA; the last CTA of a KV
-// head merges the S partials in split order with all loads in flight.
+// One CTA's attention task: split sp of KV head kvh, tiles tb .. te-1, two
+// consecutive 32-token tiles per ring stage.  The eight consumer warps are
+// (stage parity) x (tile of the stage) x (head group): warp w works on the
+// stages j with j % 2 == w >> 2, on tile (w >> 1) & 1 of each, for the HPW
+// query heads of group w & 1.  Position pos (written by this step's QKV
+// phase) is copied from global into its tile before scoring.  The four
+// warps of a head group merge in shared memory into one (m, l, o) partial
+// per CTA; the last CTA of a KV head merges the S partials in split order
+// with all loads in flight.
 template <int HD, int G>
 __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_pool) {
-  constexpr int HG = G >= 2 ? 2 : 1;  // head groups
-  constexpr int TS = NWC / HG;        // tile slots
+  static_assert(G >= 2 && NWC == 8, "two head groups over eight warps");
+  constexpr int HG = 2;               // head groups
   constexpr int HPW = G / HG;         // heads per warp
+  constexpr int WPG = NWC / HG;       // warps per head group
   constexpr int DPL = HD / 32, W2 = HD / 2;
   const StepArgs& A = *c.A;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tslot = warp % TS, hg = warp / TS;
+  const int hg = warp & 1, tis = (warp >> 1) & 1, par = warp >> 2;
   const int n = c.pos + 1;
   int kvh, tb, te;
   attn_task(A, n, kvh, tb, te);
@@ -602,17 +637,18 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
     for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
   }
   const float2* q2 = reinterpret_cast<const float2*>(c.s_q) + (size_t)hg * HPW * W2;
-  for (int j = 0; j < te - tb; ++j) {
-    const int slot = c.sidx % A.ns;
-    if ((j % TS) == tslot) {
-      const int t = tb + j;
+  const int nst = max(0, (te - tb + 1) / 2);
+  for (int j = 0; j < nst; ++j) {
+    const int slot = c.slot;
+    const int t = tb + 2 * j + tis;
+    if ((j & 1) == par && t < te) {
       const int nt = min(kTile, n - t * kTile);
-      const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), (c.sidx / A.ns) & 1, 20);
-      __half* kt = reinterpret_cast<__half*>(c.ring + (size_t)slot * A.stage_bytes);
+      const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), c.par, 20);
+      __half* kt = reinterpret_cast<__half*>(c.ring + (size_t)slot * A.stage_bytes) + 2 * tis * kTile * HD;
       __half* vt = kt + kTile * HD;
       const int jp = c.pos - t * kTile;  // the new position inside this tile, if any
       if (jp >= 0 && jp < kTile && c.pos_page >= 0) {
-        // both warps of the slot write the same bytes; each reads its own
+        // the two head-group warps of this tile write the same bytes; each reads its own
         const size_t off = (((size_t)c.pos_page * A.n_kv + kvh) * A.page_tokens + (c.pos % A.page_tokens)) * HD;
         for (int i = lane; i < HD / 2; i += 32) {
           reinterpret_cast<__half2*>(kt + jp * HD)[i] = __ldcg(reinterpret_cast<const __half2*>(k_pool + off) + i);
@@ -677,7 +713,7 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
       __syncwarp();
     }
     if (lane == 0) mbar_arrive(smem_u32(&c.sh->empty[slot]));
-    ++c.sidx;
+    advance(c, A.ns);
   }
   // merge the TS warps of each head group
   ctmark(A, c.epoch, 5);
@@ -696,14 +732,14 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
   if (has_task) {
     const size_t slot = (size_t)kvh * A.S + sp;
     for (int idx = tid; idx < G * HD; idx += NWC * 32) {
-      const int h = idx / HD, hh = h % HPW, w0 = (h / HPW) * TS;
+      const int h = idx / HD, hh = h % HPW, g0 = h / HPW;  // warps g0, g0 + 2, g0 + 4, g0 + 6 hold head h
       float M = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < TS; ++t) M = fmaxf(M, c.s_wm[(w0 + t) * HPW + hh]);
+      for (int t = 0; t < WPG; ++t) M = fmaxf(M, c.s_wm[(g0 + HG * t) * HPW + hh]);
       float acc = 0.f, L = 0.f;
 #pragma unroll
-      for (int t = 0; t < TS; ++t) {
-        const int wi = (w0 + t) * HPW + hh;
+      for (int t = 0; t < WPG; ++t) {
+        const int wi = (g0 + HG * t) * HPW + hh;
         const float ew = c.s_wl[wi] > 0.f ? expf(c.s_wm[wi] - M) : 0.f;
         acc = fmaf(ew, c.s_wo[wi * HD + (idx % HD)], acc);
         L = fmaf(ew, c.s_wl[wi], L);
@@ -803,6 +839,8 @@ __global__ void __maxnreg__(224) step_kernel(const StepArgs A) {
   off += NWC * G * HD * 4;
   c.ring = smem + ((off + 127) & ~(size_t)127);
   c.sidx = 0;
+  c.slot = 0;
+  c.par = 0;
   c.epoch = 0;
   c.pos = A.sp->pos[0];
   c.seq = A.sp->seq[0];
@@ -983,7 +1021,7 @@ StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, i
   if (!p.fn) return p;
   const int ds_h = (nb_h + 7) & ~7, ds_f = (nb_f + 7) & ~7;
   size_t stage = std::max((size_t)rsa * (rb_h + ds_h * 2), (size_t)rsb * (rb_f + ds_f * 2));
-  stage = std::max(stage, (size_t)2 * kTile * hd * 2);
+  stage = std::max(stage, (size_t)4 * kTile * hd * 2);  // two K/V tiles
   stage = (stage + 127) & ~(size_t)127;
   size_t head = ((sizeof(Sh) + 127) & ~(size_t)127) + NWC * kRB * 4 + G * hd * 4 + 2 * NWC * G * 4 + NWC * G * hd * 4;
   head = (head + 127) & ~(size_t)127;

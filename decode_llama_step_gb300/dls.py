@@ -82,6 +82,7 @@ _SIGS = {
     "dls_debug_launches_per_step": (i32, [vp]),
     "dls_debug_profile_step": (ctypes.c_int, [vp, i32, i32, i32, i32, vp, vp, vp]),
     "dls_debug_step_trace": (ctypes.c_int, [vp, vp, i32, vp]),
+    "dls_debug_profile_batch": (ctypes.c_int, [vp, i32, vp, vp, vp, i32, vp, vp, vp]),
 }
 
 
@@ -351,6 +352,19 @@ class Model:
         self._c(self.lib.dls_debug_profile_step(self.handle, seq, int(token), int(pos), max_kernels, ms.ctypes.data,
                                                 kinds.ctypes.data, ctypes.byref(n)))
         return ms[: n.value].copy(), kinds[: n.value].copy()
+
+    def profile_batch(self, seqs, tokens, pos, max_kernels: int = 8192):
+        """(durations_ms, kinds) of every kernel of one batched decode step."""
+        n = len(seqs)
+        sa = np.ascontiguousarray(seqs, dtype=np.int32)
+        ta = np.ascontiguousarray(tokens, dtype=np.int32)
+        pa = np.ascontiguousarray(pos, dtype=np.int32)
+        ms = np.zeros(max_kernels, dtype=np.float32)
+        kinds = np.zeros(max_kernels, dtype=np.int32)
+        cnt = i32()
+        self._c(self.lib.dls_debug_profile_batch(self.handle, n, sa.ctypes.data, ta.ctypes.data, pa.ctypes.data,
+                                                 max_kernels, ms.ctypes.data, kinds.ctypes.data, ctypes.byref(cnt)))
+        return ms[: cnt.value].copy(), kinds[: cnt.value].copy()
 
     def step_trace(self, max_entries: int = 1 << 22) -> np.ndarray:
         """Per-CTA phase timestamps of the last profiled persistent step: [phase, cta, 4] (ns)."""

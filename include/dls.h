@@ -289,6 +289,11 @@ int dls_debug_gemm(dls_model* m, int32_t layer, int32_t tensor, int32_t n_tokens
  * gate/up GEMV, 6 down GEMV, 7 LM head GEMV) and the count to *n_kernels. */
 int dls_debug_profile_step(dls_model* m, int32_t seq, int32_t token, int32_t pos, int32_t max_kernels,
                            float* kernel_ms, int32_t* kernel_kind, int32_t* n_kernels);
+/* dls_debug_profile_step for a batch of n >= 2 rows (the arguments of
+ * dls_decode_batch): every kernel of one batched step timed alone; each
+ * row's sequence grows by one.  Profiling only. */
+int dls_debug_profile_batch(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* tokens, const int32_t* pos,
+                            int32_t max_kernels, float* kernel_ms, int32_t* kernel_kind, int32_t* n_kernels);
 /* Per-CTA phase timestamps (global timer, ns) of the last profiled step of
  * the persistent step kernel: [phase][cta][8] = {consumer arrival at the
  * grid barrier that ends the phase, its release, producer's first issue of
