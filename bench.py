@@ -103,6 +103,24 @@ def _events(torch, stream, fn):
     return e0.elapsed_time(e1) / 1000.0
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time: every rank's replica must finish (barrier +
+    max-over-ranks timing; decode runs as independent replicas, one per GPU,
+    with no data-path collective)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, steps_per_rank, ms):
+    """Whole-job tokens/s: every rank decodes steps_per_rank tokens of its own
+    replica in ms milliseconds (the max over ranks)."""
+    return world * steps_per_rank / (ms / 1000.0)
+
+
 def base_line(metric, value, unit, steps, warmup, ms, workload, extra):
     line = {"metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": 1, "steps": steps,
             "warmup": warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -457,13 +475,9 @@ def main():
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), dist, "cuda")
     ms_per_step = ms / args.steps
-    value = world * args.steps / (ms / 1000.0)
+    value = replica_throughput(world, args.steps, ms)
     tok = int(toks[-1, 0])
     launches = m.launches_per_step()
 

@@ -735,6 +735,20 @@ int enqueue_persistent(dls_model* m, bool head, bool argmax) {
   a.ctrace = m->profiling ? m->step_ctrace : nullptr;
   a.ns = m->step.ns;
   a.stage_bytes = m->step.stage_bytes;
+  {
+    // L2 hints during the attention and O phases: skip the gate/up bytes the
+    // ring will already hold (~96 KB per CTA), then hint the next ~384 KB
+    // (152 CTAs x 384 KB = 58 MB, well inside the L2).  Measured on the 8B
+    // Q8_0 model at ctx 2048: 529 tok/s with the hints, 518 without.
+    const int nb = (m->H + 31) / 32;
+    const int row = (m->wtype == 8 ? nb * 32 : nb * 16) + ((nb + 7) & ~7) * 2;
+    const char* e1 = getenv("DLS_STEP_PF_KB");
+    const char* e2 = getenv("DLS_STEP_PF_SKIP_KB");
+    const long kb = e1 ? std::max(0L, atol(e1)) : 384;
+    const long skip = e2 ? std::max(0L, atol(e2)) : 96;
+    a.pf_rows = (int)(kb * 1024 / row);
+    a.pf_skip = (int)(skip * 1024 / row);
+  }
   CK(cudaMemsetAsync(m->step_bar, 0, 2 * sizeof(unsigned), m->stream));
   LK(K_STEP, launch_step(m->step, a, m->stream));
   return DLS_OK;

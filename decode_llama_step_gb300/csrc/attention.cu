@@ -12,6 +12,9 @@
 // finish combines the S partials in split order (deterministic) and resets
 // the arrival counter to zero for the next launch.
 #include <math.h>
+#include <stdlib.h>
+
+#include <algorithm>
 
 #include <mutex>
 
@@ -282,7 +285,9 @@ void attn_workspace_carve(void* ws, int rows, int n_heads, int n_kv, int head_di
 int attn_default_splits(int rows, int n_kv, int num_sms, int max_len) {
   const int tiles = (max_len + TILE - 1) / TILE;
   int s = (tiles + 3) / 4;  // about one tile per slot
-  const int cap = (4 * num_sms + rows * n_kv - 1) / (rows * n_kv);
+  const char* ew = getenv("DLS_ATTN_WAVES");
+  const int waves = ew ? std::max(1, std::min(64, atoi(ew))) : 4;
+  const int cap = (waves * num_sms + rows * n_kv - 1) / (rows * n_kv);
   if (s > cap) s = cap;
   if (s > kMaxSplits) s = kMaxSplits;  // merge weights live in shared memory
   if (s < 1) s = 1;

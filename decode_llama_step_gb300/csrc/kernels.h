@@ -143,6 +143,7 @@ struct StepArgs {
                               // producer last issue, prologue done, stages done, epilogue done, -}: [phase][grid][8]
   int ns;                   // ring stages
   uint32_t stage_bytes;     // ring slot size
+  int pf_skip, pf_rows;     // gate/up rows [pf_skip, pf_skip + pf_rows) of each CTA hinted into L2 during attention/O
 };
 
 struct StepPlan {

@@ -33,7 +33,7 @@ namespace dls {
 namespace {
 
 constexpr int NWC = 8;               // consumer warps
-constexpr int NTHR = 32 * (NWC + 1);
+constexpr int NTHR = 32 * (NWC + 2);  // consumers, the producer warp, the L2-hint warp
 constexpr int kRB = 64;              // rows per epilogue block
 constexpr int kTile = 32;            // attention tokens per ring stage
 constexpr int kMaxStages = 16;
@@ -51,6 +51,7 @@ struct Sh {
   uint64_t empty[kMaxStages];
   float red[32];
   int last;
+  unsigned epoch_pub;  // grid barriers the consumers have passed
 };
 
 struct Ctx {
@@ -131,6 +132,7 @@ __device__ __forceinline__ void grid_sync(Ctx& c) {
       if (i >= 64) __nanosleep(32);
     }
     if (A.ctrace) A.ctrace[((size_t)(c.epoch - 1) * gridDim.x + blockIdx.x) * kTr + 1] = global_ns();
+    *(volatile unsigned*)&c.sh->epoch_pub = c.epoch;
   }
   named_bar(1, NWC * 32);
 }
@@ -146,6 +148,40 @@ __device__ __forceinline__ void row_split(int rows, int unit, int& r0, int& r1) 
 template <int WT>
 __device__ __forceinline__ size_t row_bytes_of(const MatDev& w) {
   return WT == 8 ? (size_t)w.nb * 32 : (size_t)w.nb * 16;
+}
+
+// While the consumers sit in the latency-bound attention and O phases, HBM
+// would idle once the ring is full.  A warp of its own follows the
+// consumers' phase counter and, when layer l's
+// attention phase begins, hint this CTA's gate/up rows [pf_skip, pf_skip +
+// pf_rows) of layer l (codes and scales) into L2, so the gate/up phase's
+// stage copies find them there.  Bounded: gives up on an abort or after the
+// wait limit.
+template <int WT>
+__device__ void hint_lanes(const Ctx& c) {
+  const StepArgs& A = *c.A;
+  const int lane = threadIdx.x & 31;
+  int r0, r1;
+  row_split(A.layers[0].gu.rows, 2, r0, r1);
+  const int lo = min(r1, r0 + A.pf_skip), hi = min(r1, r0 + A.pf_skip + A.pf_rows);
+  if (lo >= hi) return;
+  const volatile unsigned* ep = &c.sh->epoch_pub;
+  const uint64_t t0 = global_ns();
+  for (int l = 0; l < A.n_layers; ++l) {
+    const unsigned target = 2u + 5u * (unsigned)l;  // barriers passed when layer l's attention starts
+    for (uint32_t i = 0; *ep < target; ++i) {
+      __nanosleep(256);
+      if ((i & 63) == 63 && (aborted(A) || global_ns() - t0 > kWaitNs)) return;
+    }
+    const MatDev& w = A.layers[l].gu;
+    const size_t rb = row_bytes_of<WT>(w), db = (size_t)w.ds * 2;
+    const uint8_t* q = w.qs + (size_t)lo * rb;
+    const size_t nq = (size_t)(hi - lo) * rb;
+    for (size_t off = (size_t)lane * 128; off < nq; off += 32 * 128) prefetch_line_l2(q + off);
+    const uint8_t* d = reinterpret_cast<const uint8_t*>(w.d) + (size_t)lo * db;
+    const size_t nd = (size_t)(hi - lo) * db;
+    for (size_t off = (size_t)lane * 128; off < nd; off += 32 * 128) prefetch_line_l2(d + off);
+  }
 }
 
 // ------------------------------------------------------------------ producer
@@ -821,7 +857,7 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 }
 
 template <int WT, int HD, int G, int RSA, int MCA, int RSB, int MCB>
-__global__ void __maxnreg__(224) step_kernel(const StepArgs A) {
+__global__ void __maxnreg__(200) step_kernel(const StepArgs A) {
   extern __shared__ __align__(128) uint8_t smem[];
   Ctx c;
   c.A = &A;
@@ -855,6 +891,7 @@ __global__ void __maxnreg__(224) step_kernel(const StepArgs A) {
       mbar_init(smem_u32(&c.sh->full[s]), 1);
       mbar_init(smem_u32(&c.sh->empty[s]), NWC);
     }
+    c.sh->epoch_pub = 0;
     mbar_fence_init();
     if (A.trace && blockIdx.x == 0) A.trace[0] = global_ns();
   }
@@ -863,6 +900,9 @@ __global__ void __maxnreg__(224) step_kernel(const StepArgs A) {
   if (warp == NWC) {
     // ---------------- producer: every phase's stages, in consumer order
     if (lane == 0) produce<WT, HD, RSA, RSB>(c);
+  } else if (warp == NWC + 1) {
+    // ---------------- L2 hints for the gate/up rows
+    if (A.pf_rows) hint_lanes<WT>(c);
   } else {
     // ---------------- consumers
     // embedding row -> x (rows split like the residual epilogues)
