@@ -37,7 +37,13 @@ METRIC = "decode tok/s, 8B-shape Q8_0 batch 1; achieved HBM GB/s as % of peak"
 # of the dominant kernel, keyed by the sha256 prefix of the source file it
 # was captured on (a changed kernel has no traffic figure until it is
 # captured again); the captures are summarised under profiles/.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # step.cu: 4-layer 8B Q8_0 model, ctx 2051, one step-kernel launch:
+    # dram read 1,520,923,648 + write 5,118,464 B against 1,520,440,320
+    # algorithmic bytes; the traffic grows with the layers, so a full launch
+    # is scaled by the same ratio (the capture is summarised under profiles/)
+    "0e8b0c8230dc6604": {"ratio": 1526042112 / 1520440320},
+}
 
 KIND_NAMES = {1: "embed", 2: "gemv_qkv", 3: "attention", 4: "gemv_o", 5: "gemv_gate_up", 6: "gemv_down",
               7: "gemv_head", 8: "argmax", 9: "advance"}
@@ -513,7 +519,8 @@ def main():
                 "bytes_per_launch": round(gemv_bytes_total / max(gemv_launches, 1)),
                 "avg_launch_us": round(1000.0 * gemv_ms_total / max(gemv_launches, 1), 2)}
     src_sha = hashlib.sha256(open(os.path.join(ROOT, "decode_llama_step_gb300", "csrc", src), "rb").read()).hexdigest()[:16]
-    traffic = NCU_TRAFFIC.get(src_sha)
+    nt = NCU_TRAFFIC.get(src_sha)
+    traffic = round(nt["ratio"] * kern["bytes_per_launch"]) if nt else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, **kern,
                 "peak_source": f"{peak_src} (MEMORY copy, hbm_gbs)"}
