@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <chrono>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/dls.h"
@@ -113,6 +114,7 @@ struct dls_model {
   size_t page_elems = 0, kv_layer_elems = 0;
   int n_pages = 0;
   std::vector<int> free_pages;
+  std::vector<int> page_ref;  // sequences holding each page (a shared fork makes it > 1)
   std::vector<Seq> seqs;
   int32_t* pt_dev = nullptr;
   std::vector<int32_t> pt_host;
@@ -822,6 +824,7 @@ int ensure_pages(dls_model* m, int seq, int len) {
   for (int i = 0; i < need; ++i) {
     const int p = m->free_pages.back();
     m->free_pages.pop_back();
+    m->page_ref[p] = 1;
     s.pages.push_back(p);
     m->pt_host[(size_t)seq * m->max_pages + first + i] = p;
   }
@@ -833,7 +836,8 @@ int ensure_pages(dls_model* m, int seq, int len) {
 
 int release_pages(dls_model* m, int seq) {
   Seq& s = m->seqs[seq];
-  for (int p : s.pages) m->free_pages.push_back(p);
+  for (int p : s.pages)
+    if (--m->page_ref[p] == 0) m->free_pages.push_back(p);  // shared pages stay with their other holders
   const int n = (int)s.pages.size();
   s.pages.clear();
   s.len = 0;
@@ -843,6 +847,18 @@ int release_pages(dls_model* m, int seq) {
                        n * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
   }
   return DLS_OK;
+}
+
+// Pages that releasing all of `seqs` would return to the pool (pages shared
+// with sequences outside the set stay allocated).
+size_t reclaimable_pages(const dls_model* m, const int32_t* seqs, int n) {
+  std::unordered_map<int, int> held;
+  for (int i = 0; i < n; ++i)
+    for (int p : m->seqs[seqs[i]].pages) ++held[p];
+  size_t r = 0;
+  for (const auto& kv : held)
+    if (kv.second == m->page_ref[kv.first]) ++r;
+  return r;
 }
 
 int check_seq(dls_model* m, int seq) {
@@ -1279,6 +1295,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   dev_free(m, temp);
   m->free_pages.clear();
   for (int i = m->n_pages - 1; i >= 0; --i) m->free_pages.push_back(i);
+  m->page_ref.assign(m->n_pages, 0);
   m->seqs.assign(m->max_seqs, Seq());
   TRYC(setup_persistent(m));
   *out = m;
@@ -1440,9 +1457,8 @@ int dls_kv_fork(dls_model* m, int32_t src, const int32_t* dsts, int32_t n_dst) {
   }
   const int len = m->seqs[src].len;
   const int np = pages_needed(m, len);
-  // capacity: the destinations' own pages come back to the pool first
-  size_t avail = m->free_pages.size();
-  for (int i = 0; i < n_dst; ++i) avail += m->seqs[dsts[i]].pages.size();
+  // capacity: the destinations' pages that only they hold come back first
+  const size_t avail = m->free_pages.size() + reclaimable_pages(m, dsts, n_dst);
   if ((size_t)np * n_dst > avail)
     return fail(m, DLS_ERR_CAPACITY, "src=%d length=%d pages_per_branch=%d branches=%d free_pages=%zu", src, len, np,
                 n_dst, avail);
@@ -1462,6 +1478,59 @@ int dls_kv_fork(dls_model* m, int32_t src, const int32_t* dsts, int32_t n_dst) {
   }
   for (int i = 0; i < n_dst; ++i) m->seqs[dsts[i]].len = len;
   return DLS_OK;
+}
+
+int dls_kv_fork_shared(dls_model* m, int32_t src, const int32_t* dsts, int32_t n_dst) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  TRY(check_seq(m, src));
+  if (n_dst < 1 || !dsts) return fail(m, DLS_ERR_ARG, "n_dst=%d", n_dst);
+  for (int i = 0; i < n_dst; ++i) {
+    TRY(check_seq(m, dsts[i]));
+    if (dsts[i] == src) return fail(m, DLS_ERR_ARG, "dst=%d equals src", dsts[i]);
+    for (int j = 0; j < i; ++j)
+      if (dsts[j] == dsts[i]) return fail(m, DLS_ERR_ARG, "dst=%d repeated", dsts[i]);
+  }
+  const int len = m->seqs[src].len;
+  const int n_full = len / m->pt;        // pages no position at or after len falls in: shared as they are
+  const int tail = len % m->pt ? 1 : 0;  // the page the next position falls in: each branch gets its own copy
+  const size_t avail = m->free_pages.size() + reclaimable_pages(m, dsts, n_dst);
+  if ((size_t)tail * n_dst > avail)
+    return fail(m, DLS_ERR_CAPACITY, "src=%d length=%d branches=%d free_pages=%zu", src, len, n_dst, avail);
+  std::vector<int2> pairs;
+  for (int i = 0; i < n_dst; ++i) {
+    const int d = dsts[i];
+    TRY(release_pages(m, d));
+    Seq& sd = m->seqs[d];
+    const Seq& ss = m->seqs[src];
+    for (int k = 0; k < n_full; ++k) {
+      const int p = ss.pages[k];
+      ++m->page_ref[p];
+      sd.pages.push_back(p);
+      m->pt_host[(size_t)d * m->max_pages + k] = p;
+    }
+    if (n_full) {
+      // pageable source: staged before the call returns
+      CK(cudaMemcpyAsync(m->pt_dev + (size_t)d * m->max_pages, &m->pt_host[(size_t)d * m->max_pages],
+                         n_full * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+    }
+    if (tail) {
+      TRY(ensure_pages(m, d, len));  // one fresh page after the shared ones
+      pairs.push_back(make_int2(ss.pages[n_full], sd.pages[n_full]));
+    }
+  }
+  if (!pairs.empty()) {
+    CK(cudaMemcpyAsync(m->pairs_dev, pairs.data(), pairs.size() * sizeof(int2), cudaMemcpyHostToDevice, m->stream));
+    CK(launch_kv_copy(m->k_pool, m->v_pool, m->kv_layer_elems, m->L, m->page_elems, m->pairs_dev, (int)pairs.size(),
+                      m->stream));
+    TRY(sync_stream(m, m->stream));  // pairs is a pageable host vector
+  }
+  for (int i = 0; i < n_dst; ++i) m->seqs[dsts[i]].len = len;
+  return DLS_OK;
+}
+
+int32_t dls_kv_free_pages(const dls_model* m) {
+  if (!m) return DLS_ERR_ARG;
+  return (int32_t)m->free_pages.size();
 }
 
 int dls_set_resident_layers(dls_model* m, int32_t n) {

@@ -67,6 +67,8 @@ _SIGS = {
     "dls_generate": (ctypes.c_int, [vp, i32, vp, vp, i32, vp, vp]),
     "dls_argmax": (ctypes.c_int, [vp, vp, i32, vp]),
     "dls_kv_fork": (ctypes.c_int, [vp, i32, vp, i32]),
+    "dls_kv_fork_shared": (ctypes.c_int, [vp, i32, vp, i32]),
+    "dls_kv_free_pages": (i32, [vp]),
     "dls_check_context_budget": (ctypes.c_int, [i32, i32, i32, i32]),
     "dls_set_resident_layers": (ctypes.c_int, [vp, i32]),
     "dls_resident_layers": (i32, [vp]),
@@ -307,9 +309,15 @@ class Model:
         self._c(self.lib.dls_argmax(self.handle, _ptr(logits), n_rows, _ptr(res)))
         return res
 
-    def kv_fork(self, src_seq: int, dst_seqs):
+    def kv_fork(self, src_seq: int, dst_seqs, shared: bool = False):
+        """Fork src's KV into each destination: a page copy, or (shared=True)
+        shared prefix pages plus a private copy of the partly filled page."""
         d = np.ascontiguousarray(dst_seqs, dtype=np.int32)
-        self._c(self.lib.dls_kv_fork(self.handle, src_seq, d.ctypes.data, d.size))
+        fn = self.lib.dls_kv_fork_shared if shared else self.lib.dls_kv_fork
+        self._c(fn(self.handle, src_seq, d.ctypes.data, d.size))
+
+    def kv_free_pages(self) -> int:
+        return int(self.lib.dls_kv_free_pages(self.handle))
 
     # --- residency
     def set_resident_layers(self, n: int):

@@ -198,6 +198,21 @@ int dls_argmax(dls_model* m, const float* logits, int32_t n_rows, int32_t* out);
  * dropped.  DLS_ERR_CAPACITY if the KV pool cannot hold the copies. */
 int dls_kv_fork(dls_model* m, int32_t src_seq, const int32_t* dst_seqs, int32_t n_dst);
 
+/* KV fork by reference (the shared-prefix form of the fork: the SwarmKV
+ * page, section 3, notes that paged KV sharing is the same idea as its
+ * snapshot copy).  Each destination's page table takes the pages of
+ * `src_seq` that hold only positions below length(src) as they are (a page
+ * count per page keeps them allocated until every holder is freed); the page
+ * the next position falls in, when partly filled, is copied into a fresh
+ * page per destination, so appends never touch a shared page.  Destinations
+ * read exactly the source's K/V bytes and get length(src).  Same argument
+ * rules as dls_kv_fork; DLS_ERR_CAPACITY if the pool cannot hold one fresh
+ * page per destination. */
+int dls_kv_fork_shared(dls_model* m, int32_t src_seq, const int32_t* dst_seqs, int32_t n_dst);
+
+/* Free pages in the KV pool (pages held by no sequence). */
+int32_t dls_kv_free_pages(const dls_model* m);
+
 /* Context-budget check done before any allocation (SwarmKV page, section 4,
  * step 0): DLS_OK if prefix_tokens + max_branch_tokens + headroom <= n_ctx,
  * else DLS_ERR_CAPACITY with the numbers in dls_last_error(NULL). */

@@ -227,6 +227,18 @@ def test_fork_8b_q4_0_prefix_4096_eight_branches(gpu_lib):
         assert torch.equal(last_f, last_i)
         for s in dsts + indep:
             assert m.seq_length(s) == P + D
+        # the shared-prefix fork (pages by reference) decodes the same tokens
+        for s in dsts:
+            m.seq_free(s)
+        shared = [m.seq_create() for _ in range(B)]
+        free_before = m.kv_free_pages()
+        m.kv_fork(src, shared, shared=True)
+        assert m.kv_free_pages() == free_before                # 4096 = 64 full pages: nothing copied
+        last_s = torch.empty_like(last_f)
+        toks_s = m.generate(shared, start, D, last_s)
+        stream.synchronize()
+        assert np.array_equal(toks_s, toks_f)
+        assert torch.equal(last_s, last_f)
     finally:
         release(m)
 

@@ -304,6 +304,66 @@ def test_kv_fork_bit_exact_and_continues(setup):
             m.seq_free(s)
 
 
+def test_kv_fork_shared_pages(setup):
+    """The shared-prefix fork: branches hold the source's full pages by
+    reference and a private copy of the partly filled page; they read the
+    source's K/V bytes exactly, decode exactly like a copied branch, never
+    disturb each other or the source, and outlive it; every page comes back
+    to the pool when all holders are freed."""
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    free0 = m.kv_free_pages()
+    n = 45                                        # one full 32-token page + 13 positions of the next
+    prefix = synth.prompt_tokens(cfg, n, seed=7)
+    src, a, b, cpy = (m.seq_create() for _ in range(4))
+    live = [src, a, b, cpy]
+    try:
+        m.prefill(src, prefix)
+        held = free0 - m.kv_free_pages()
+        assert held == 2
+        m.kv_fork(src, [a, b], shared=True)
+        assert free0 - m.kv_free_pages() == held + 2          # one fresh page per branch
+        m.kv_fork(src, [cpy])                                  # the copy form, for comparison
+        kvd = cfg.n_kv_heads * cfg.head_dim
+
+        def kv(seq, l):
+            k = torch.empty(n, kvd, dtype=torch.float16, device="cuda")
+            v = torch.empty_like(k)
+            m.debug_read_kv(seq, l, k, v)
+            stream.synchronize()
+            return k.view(torch.int16).clone(), v.view(torch.int16).clone()
+
+        src_kv = [kv(src, l) for l in range(cfg.n_layers)]
+        for d in (a, b):
+            assert m.seq_length(d) == n
+            for l in range(cfg.n_layers):
+                kd, vd = kv(d, l)
+                assert torch.equal(kd, src_kv[l][0]) and torch.equal(vd, src_kv[l][1])
+        la, lb, lc = (torch.empty(cfg.vocab, device="cuda") for _ in range(3))
+        m.decode_step(a, 11, n, la)
+        m.decode_step(cpy, 11, n, lc)
+        m.decode_step(b, 500, n, lb)                           # a different token into b's own page
+        stream.synchronize()
+        assert torch.equal(la, lc)
+        for l in range(cfg.n_layers):                          # the source is untouched
+            ks, vs = kv(src, l)
+            assert torch.equal(ks, src_kv[l][0]) and torch.equal(vs, src_kv[l][1])
+        m.seq_free(src)                                        # the branches keep the shared page
+        live.remove(src)
+        m.decode_step(a, 12, n + 1, la)
+        m.decode_step(cpy, 12, n + 1, lc)
+        stream.synchronize()
+        assert torch.equal(la, lc)
+        ref = orc.new_seq()
+        orc.prefill(ref, prefix)
+        orc.decode_step(ref, 11, n)
+        assert_close(la.cpu().numpy(), orc.decode_step(ref, 12, n + 1), "branch after a shared fork")
+    finally:
+        for q in live:
+            m.seq_free(q)
+    assert m.kv_free_pages() == free0
+
+
 def test_streamed_layers_match_resident(setup):
     torch = _torch()
     cfg, w, m, orc, stream = setup
