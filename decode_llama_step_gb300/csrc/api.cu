@@ -1149,6 +1149,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   CKC(cudaEventCreateWithFlags(&m->ev_start, cudaEventDisableTiming));
   CKC(gemv_setup_attributes());
   CKC(tgemm_setup_attributes());
+  CKC(sgemm_setup_attributes());
   CKC(prefill_setup_attributes());
   CKC(fattn_setup_attributes());
 

@@ -478,6 +478,7 @@ TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split) {
 }
 
 cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, cudaStream_t s) {
+  if (a.T <= 8 && p.bn == 16) return launch_sgemm(wtype, epi, a, p.split, s);
   const MatDev& w = a.w;
   const int kpad = w.nb * 32;
   const int nk = (kpad + GBK - 1) / GBK;

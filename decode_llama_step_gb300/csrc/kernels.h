@@ -185,6 +185,10 @@ struct TgPlan {
 TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split);
 cudaError_t tgemm_setup_attributes();  // smem limits; fails if tensor maps cannot be made
 cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, cudaStream_t s);
+// the small-batch form (T <= 8): raw codes as exact fp16 operands, block
+// scales applied per 32-column block from tensor memory (gemm_small.cu)
+cudaError_t sgemm_setup_attributes();
+cudaError_t launch_sgemm(int wtype, int epi, const PgArgs& a, int split, cudaStream_t s);
 cudaError_t prefill_setup_attributes();
 cudaError_t launch_embed_rows(const MatDev& emb, int wtype, const int32_t* tokens, int T, int vocab, float* x, int ldx,
                               int32_t* status, cudaStream_t s);
