@@ -44,7 +44,7 @@ namespace {
 
 constexpr int SBM = 128, SBK = 64;     // weight rows per CTA, K per step
 constexpr int STHREADS = 320;
-constexpr int kSR = 4;                 // tensor-memory regions (K steps in flight between MMA and epilogue)
+constexpr int kSR = 8;                 // tensor-memory regions (K steps in flight between MMA and epilogue)
 constexpr int kSSplitMax = 16;
 constexpr uint64_t kWaitNsS = 2000000000ull;
 constexpr int kSATile = SBM * SBK * 2;  // 16 KB fp16 A operand
@@ -54,8 +54,8 @@ struct SCfg {
   static constexpr int kCodes = WT == 8 ? SBM * 64 : SBM * 32;
   static constexpr int kB = 2048;                          // 16 rows (8 hi + 8 lo) x 128 bytes
   static constexpr int kStage = kB + kCodes + SBM * 16;     // B | codes | scales (8 per row)
-  static constexpr int NR = WT == 8 ? 4 : 6;
-  static constexpr int NA = 3;
+  static constexpr int NR = WT == 8 ? 3 : 4;
+  static constexpr int NA = 4;
   static constexpr int kScOff = NA * kSATile + NR * kStage;  // float2 scales [kSR][SBM]
   static constexpr int kBarOff = kScOff + kSR * SBM * 8;
   static constexpr int kSmem = kBarOff + 512 + 1024;
