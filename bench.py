@@ -64,10 +64,13 @@ def parse():
                    help="bracket the timed decode region with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     p.add_argument("--layers", type=int, default=0,
                    help="keep only the first N layers (small cases for ncu captures; not a bench result)")
-    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream"], default="decode",
+    p.add_argument("--skip-threshold", type=float, default=0.98,
+                   help="layer skip workload: skip layers whose calibrated cosine exceeds this")
+    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip"], default="decode",
                    help="decode (default, the headline line); the others are secondary measurements: "
                         "prefill (prompt of --ctx tokens), fork (shared prefix -> 8 branches), "
-                        "stream (70B Q4_0 resident vs a 24 GB device budget)")
+                        "stream (70B Q4_0 resident vs a 24 GB device budget), "
+                        "skip (decode with the layers whose calibrated cosine exceeds --skip-threshold skipped)")
     return p.parse_args()
 
 
@@ -243,6 +246,46 @@ def run_fork(args):
                                                 "fork_path_s": round(shared_path, 4),
                                                 "speedup_vs_independent": round(indep_path / shared_path, 3)}},
                       "kernels": per_kind, "clocks": clk.summary()})
+
+
+def run_skip(args):
+    """Decode with layer skip (the engine page's calibration): after a --ctx
+    prefill, one decode step measures every layer's output/input cosine;
+    the layers above the threshold are skipped and greedy decode is timed
+    with and without the skips."""
+    import torch
+    import synth
+    from decode_llama_step_gb300 import dls
+    cfg = load_config(args.config, args.layers)
+    D, W = args.steps, max(args.warmup, 1)
+    w = synth.model_weights(cfg)
+    stream = torch.cuda.Stream()
+    m = dls.Model(cfg, w, max_seqs=1, max_ctx=args.ctx + 2 * (D + W) + 8, stream=stream)
+    del w
+    seq = m.seq_create()
+    prompt = synth.prompt_tokens(cfg, args.ctx, seed=1)
+    lg = torch.empty(cfg.vocab, device="cuda")
+    m.prefill(seq, prompt, lg)
+    tok = int(torch.argmax(lg).item())
+    cos = m.layer_cosines(seq, tok, args.ctx)
+    mask = cos > args.skip_threshold
+    tok = int(m.generate([seq], [tok], W)[-1, 0])
+    t_full = _events(torch, stream, lambda: m.generate([seq], [tok], D))
+    m.set_layer_skip(mask)
+    tok = int(m.generate([seq], [tok], W)[-1, 0])
+    with ClockSampler(0) as clk:
+        t_skip = _events(torch, stream, lambda: m.generate([seq], [tok], D))
+    m.close()
+    return base_line(f"decode tok/s with layer skip (calibrated cosine > {args.skip_threshold}), "
+                     f"{cfg.name}-shape {'Q8_0' if cfg.wtype == 8 else 'Q4_0'} batch 1",
+                     D / t_skip, "tok/s", D, W, 1000 * t_skip / D,
+                     f"{cfg.name} batch-1 greedy decode after a {args.ctx}-token prefill, layers skipped by calibration",
+                     {"skip": {"threshold": args.skip_threshold, "n_skipped": int(mask.sum()),
+                               "skipped_layers": [int(i) for i in np.nonzero(mask)[0]],
+                               "cosines": [round(float(c), 5) for c in cos],
+                               "tok_s_all_layers": round(D / t_full, 2), "tok_s_with_skip": round(D / t_skip, 2),
+                               "speedup": round(t_full / t_skip, 3)},
+                      "clocks": clk.summary()})
 
 
 def h2d_peak(torch, chunk=256 << 20, inflight=4, reps=10):
@@ -436,7 +479,7 @@ def main():
     if args.workload != "decode":
         if int(os.environ.get("RANK", "0")) != 0:
             return 0
-        fn = {"prefill": run_prefill, "fork": run_fork, "stream": run_stream}[args.workload]
+        fn = {"prefill": run_prefill, "fork": run_fork, "stream": run_stream, "skip": run_skip}[args.workload]
         print(json.dumps(fn(args)), flush=True)
         return 0
 

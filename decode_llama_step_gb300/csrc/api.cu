@@ -115,6 +115,8 @@ struct dls_model {
   int n_pages = 0;
   std::vector<int> free_pages;
   std::vector<int> page_ref;  // sequences holding each page (a shared fork makes it > 1)
+  std::vector<uint8_t> skip_host;  // layers skipped by decode steps (dls_set_layer_skip)
+  uint8_t* skip_dev = nullptr;     // the same flags for the step kernel
   std::vector<Seq> seqs;
   int32_t* pt_dev = nullptr;
   std::vector<int32_t> pt_host;
@@ -399,6 +401,11 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
   for (int l = 0; l < m->L; ++l) {
     LayerPtrs P;
     TRY(layer_begin(m, l, &P));
+    if (m->skip_host[l]) {  // skipped: the residual passes through (a streamed layer's copy still runs)
+      if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * m->H, x, m->H * sizeof(float), cudaMemcpyDeviceToDevice, s));
+      TRY(layer_end(m, l));
+      continue;
+    }
     KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
               m->nkv, m->hd, m->pt, m->max_pages};
     // (1) RMSNorm -> QKV GEMV -> RoPE -> fp16 K/V append
@@ -609,6 +616,11 @@ int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
   for (int l = 0; l < m->L; ++l) {
     LayerPtrs P;
     TRY(layer_begin(m, l, &P));
+    if (m->skip_host[l]) {  // skipped: the residuals pass through
+      if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * H, x, H * sizeof(float), cudaMemcpyDeviceToDevice, s));
+      TRY(layer_end(m, l));
+      continue;
+    }
     KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
               m->nkv, m->hd, m->pt, m->max_pages};
     // (1) RMSNorm -> fp16 -> QKV GEMM -> RoPE + fp16 K/V append per row
@@ -735,6 +747,7 @@ int enqueue_persistent(dls_model* m, bool head, bool argmax) {
   a.S = m->step.splits;
   a.trace = m->profiling ? m->step_trace : nullptr;
   a.ctrace = m->profiling ? m->step_ctrace : nullptr;
+  a.skip = m->skip_dev;
   a.ns = m->step.ns;
   a.stage_bytes = m->step.stage_bytes;
   {
@@ -1297,6 +1310,10 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   m->free_pages.clear();
   for (int i = m->n_pages - 1; i >= 0; --i) m->free_pages.push_back(i);
   m->page_ref.assign(m->n_pages, 0);
+  m->skip_host.assign(m->L, 0);
+  TRYC(dev_alloc_t(m, (size_t)m->L, &m->skip_dev, "layer_skip"));
+  CKC(cudaMemsetAsync(m->skip_dev, 0, m->L, m->stream));
+  TRYC(sync_stream(m, m->stream));
   m->seqs.assign(m->max_seqs, Seq());
   TRYC(setup_persistent(m));
   *out = m;
@@ -1529,6 +1546,49 @@ int dls_kv_fork_shared(dls_model* m, int32_t src, const int32_t* dsts, int32_t n
   return DLS_OK;
 }
 
+int dls_set_layer_skip(dls_model* m, const uint8_t* skip, int32_t n_layers) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (skip && n_layers != m->L) return fail(m, DLS_ERR_ARG, "n_layers=%d model has %d", n_layers, m->L);
+  for (int l = 0; l < m->L; ++l) m->skip_host[l] = skip && skip[l] ? 1 : 0;
+  CK(cudaMemcpyAsync(m->skip_dev, m->skip_host.data(), m->L, cudaMemcpyHostToDevice, m->stream));
+  TRY(sync_stream(m, m->stream));  // pageable source
+  drop_graphs(m);                   // captured separate-kernel steps hold the old mask
+  return DLS_OK;
+}
+
+int dls_layer_cosines(dls_model* m, int32_t seq, int32_t token, int32_t pos, float* cos_out) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (!cos_out) return fail(m, DLS_ERR_ARG, "cos_out=NULL");
+  // one decode step with the residual after every layer captured, the
+  // embedding row beside it, then cos(input, output) per layer on the device
+  float* buf = nullptr;
+  TRY(dev_alloc_t(m, (size_t)(m->L + 1) * m->H + m->L, &buf, "layer_cosines"));
+  float* emb = buf;
+  float* cap = buf + m->H;
+  float* cosd = buf + (size_t)(m->L + 1) * m->H;
+  int r = (seq < 0 || seq >= m->max_seqs || !m->seqs[seq].live || token < 0 || token >= m->V)
+              ? fail(m, DLS_ERR_ARG, "seq=%d token=%d", seq, token)
+              : set_params(m, 1, &seq, &token, &pos, false);
+  if (r == DLS_OK) {
+    cudaError_t e = launch_embed(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp, 0, emb, m->V, m->stream, false);
+    if (e != cudaSuccess) r = fail(m, DLS_ERR_CUDA, "embed cuda=%s", cudaGetErrorString(e));
+  }
+  if (r == DLS_OK) {
+    m->capture = cap;
+    r = dls_decode_step(m, seq, token, pos, nullptr);
+    m->capture = nullptr;
+  }
+  if (r == DLS_OK) {
+    cudaError_t e = launch_layer_cosines(emb, cap, m->L, m->H, cosd, m->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(cos_out, cosd, m->L * sizeof(float), cudaMemcpyDeviceToHost, m->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+    if (e != cudaSuccess) r = fail(m, DLS_ERR_CUDA, "layer_cosines cuda=%s", cudaGetErrorString(e));
+  }
+  const int rs = sync_stream(m, m->stream);
+  dev_free(m, buf);
+  return r != DLS_OK ? r : rs;
+}
+
 int32_t dls_kv_free_pages(const dls_model* m) {
   if (!m) return DLS_ERR_ARG;
   return (int32_t)m->free_pages.size();
@@ -1578,7 +1638,9 @@ int dls_debug_profile_step(dls_model* m, int32_t seq, int32_t token, int32_t pos
   TRY(sync_stream(m, m->stream));
   if (m->use_step) {
     // one persistent launch: per-phase durations from its timestamps
-    const int nph = 5 * m->L + 2;  // embed, 5 per layer, head
+    int active = 0;  // layers the step computed
+    for (int l = 0; l < m->L; ++l) active += m->skip_host[l] ? 0 : 1;
+    const int nph = 5 * active + 2;  // embed, 5 per computed layer, head
     std::vector<unsigned long long> ts(nph + 1);
     CK(cudaMemcpy(ts.data(), m->step_trace, ts.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
     const int kinds[5] = {K_QKV, K_ATTN, K_O, K_GATE_UP, K_DOWN};

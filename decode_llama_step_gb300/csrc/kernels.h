@@ -83,6 +83,9 @@ cudaError_t launch_attention(const AttnArgs& a, int rows, cudaStream_t s, bool p
 
 // ---- small kernels --------------------------------------------------------------
 
+// cos(input, output) of every layer's residual: emb [H] (layer 0's input),
+// cap [L][H] (the residual after each layer) -> out [L]
+cudaError_t launch_layer_cosines(const float* emb, const float* cap, int L, int H, float* out, cudaStream_t s);
 cudaError_t launch_embed(const MatDev& emb, int wtype, StepParams* sp, int brow, float* x, int vocab,
                          cudaStream_t s, bool pdl);
 // greedy pick per row over [rows][vocab]; part/counters: scratch of
@@ -144,6 +147,7 @@ struct StepArgs {
   int ns;                   // ring stages
   uint32_t stage_bytes;     // ring slot size
   int pf_skip, pf_rows;     // gate/up rows [pf_skip, pf_skip + pf_rows) of each CTA hinted into L2 during attention/O
+  const uint8_t* skip;      // [n_layers]: layers this step does not compute (their residual passes through)
 };
 
 struct StepPlan {

@@ -272,6 +272,47 @@ int grid_for(long long n, int threads) {
 
 }  // namespace
 
+// cos(x_in, x_out) of every layer: block l reduces the dot product and
+// the two squared norms of (layer l's input, its output), the input of
+// layer 0 being the embedding row and of layer l > 0 layer l-1's output
+__global__ void layer_cosines_kernel(const float* emb, const float* cap, int H, float* out) {
+  const int l = blockIdx.x;
+  const float* xi = l == 0 ? emb : cap + (size_t)(l - 1) * H;
+  const float* xo = cap + (size_t)l * H;
+  float d = 0.f, a = 0.f, b = 0.f;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    const float p = xi[i], q = xo[i];
+    d = fmaf(p, q, d);
+    a = fmaf(p, p, a);
+    b = fmaf(q, q, b);
+  }
+  __shared__ float red[3][32];
+  d = warp_sum(d);
+  a = warp_sum(a);
+  b = warp_sum(b);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red[0][w] = d;
+    red[1][w] = a;
+    red[2][w] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float dd = 0.f, aa = 0.f, bb = 0.f;
+    for (int k = 0; k < (int)(blockDim.x >> 5); ++k) {
+      dd += red[0][k];
+      aa += red[1][k];
+      bb += red[2][k];
+    }
+    out[l] = (aa > 0.f && bb > 0.f) ? dd / (sqrtf(aa) * sqrtf(bb)) : 0.f;
+  }
+}
+
+cudaError_t launch_layer_cosines(const float* emb, const float* cap, int L, int H, float* out, cudaStream_t s) {
+  layer_cosines_kernel<<<L, 256, 0, s>>>(emb, cap, H, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_embed(const MatDev& emb, int wtype, StepParams* sp, int brow, float* x, int vocab,
                          cudaStream_t s, bool pdl) {
   MatDev e = emb;

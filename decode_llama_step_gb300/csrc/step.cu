@@ -167,8 +167,10 @@ __device__ void hint_lanes(const Ctx& c) {
   if (lo >= hi) return;
   const volatile unsigned* ep = &c.sh->epoch_pub;
   const uint64_t t0 = global_ns();
+  unsigned done = 0;  // computed layers before l
   for (int l = 0; l < A.n_layers; ++l) {
-    const unsigned target = 2u + 5u * (unsigned)l;  // barriers passed when layer l's attention starts
+    if (A.skip && A.skip[l]) continue;
+    const unsigned target = 2u + 5u * done++;  // barriers passed when layer l's attention starts
     for (uint32_t i = 0; *ep < target; ++i) {
       __nanosleep(256);
       if ((i & 63) == 63 && (aborted(A) || global_ns() - t0 > kWaitNs)) return;
@@ -258,6 +260,10 @@ __device__ void begin_phase(const Ctx& c, const Rows& R, PCur& u) {
   if (u.l >= A.n_layers) {
     gemv_phase<WT>(u, A.head, R.hd0, R.hd1, RSA);
     if (!A.head_rows) u.n = 0;
+    return;
+  }
+  if (A.skip && A.skip[u.l]) {  // a skipped layer streams nothing
+    u.n = 0;
     return;
   }
   const StepLayer& L = A.layers[u.l];
@@ -930,6 +936,7 @@ __global__ void __maxnreg__(200) step_kernel(const StepArgs A) {
     }
     grid_sync(c);
     for (int l = 0; l < A.n_layers; ++l) {
+      if (A.skip && A.skip[l]) continue;  // the residual passes through; every CTA reads the same flags
       const StepLayer& L = A.layers[l];
       EpiArgs e{};
       e.y = A.q;

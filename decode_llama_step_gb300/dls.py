@@ -69,6 +69,8 @@ _SIGS = {
     "dls_kv_fork": (ctypes.c_int, [vp, i32, vp, i32]),
     "dls_kv_fork_shared": (ctypes.c_int, [vp, i32, vp, i32]),
     "dls_kv_free_pages": (i32, [vp]),
+    "dls_set_layer_skip": (ctypes.c_int, [vp, vp, i32]),
+    "dls_layer_cosines": (ctypes.c_int, [vp, i32, i32, i32, vp]),
     "dls_check_context_budget": (ctypes.c_int, [i32, i32, i32, i32]),
     "dls_set_resident_layers": (ctypes.c_int, [vp, i32]),
     "dls_resident_layers": (i32, [vp]),
@@ -318,6 +320,21 @@ class Model:
 
     def kv_free_pages(self) -> int:
         return int(self.lib.dls_kv_free_pages(self.handle))
+
+    # --- layer skip
+    def set_layer_skip(self, skip=None):
+        """Layers decode steps skip (a boolean per layer), or None for none."""
+        if skip is None:
+            self._c(self.lib.dls_set_layer_skip(self.handle, None, 0))
+            return
+        a = np.ascontiguousarray(np.asarray(skip, dtype=bool).astype(np.uint8))
+        self._c(self.lib.dls_set_layer_skip(self.handle, a.ctypes.data, a.size))
+
+    def layer_cosines(self, seq: int, token: int, pos: int) -> np.ndarray:
+        """One decode step; cosine of each layer's output with its input."""
+        out = np.zeros(self.cfg.n_layers, dtype=np.float32)
+        self._c(self.lib.dls_layer_cosines(self.handle, seq, int(token), int(pos), out.ctypes.data))
+        return out
 
     # --- residency
     def set_resident_layers(self, n: int):

@@ -213,6 +213,25 @@ int dls_kv_fork_shared(dls_model* m, int32_t src_seq, const int32_t* dst_seqs, i
 /* Free pages in the KV pool (pages held by no sequence). */
 int32_t dls_kv_free_pages(const dls_model* m);
 
+/* ---- layer skip (the engine page, sections 2.5, 3.5, 4.5) ---------------------- */
+
+/* Layers that decode steps skip from now on: skip[l] != 0 makes layer l's
+ * output its input (the layer's projections, attention and cache append are
+ * not run).  Host uint8 [n_layers] with n_layers equal to the model's, or
+ * NULL to compute every layer.  Prefill is unaffected.  A layer skipped at
+ * some positions has no cache entries there; compute it again only on
+ * sequences started after the change.  Graph-captured steps are dropped and
+ * captured again. */
+int dls_set_layer_skip(dls_model* m, const uint8_t* skip, int32_t n_layers);
+
+/* The calibration the engine page describes: one decode step of `token` at
+ * `pos` of `seq` (exactly as dls_decode_step, the sequence grows by one),
+ * and for every layer l the cosine similarity of its output with its input
+ * (the previous layer's output; the embedding row for layer 0) written to
+ * host cos_out [n_layers].  Layers above a threshold (0.98 on the page) are
+ * the ones to pass to dls_set_layer_skip. */
+int dls_layer_cosines(dls_model* m, int32_t seq, int32_t token, int32_t pos, float* cos_out);
+
 /* Context-budget check done before any allocation (SwarmKV page, section 4,
  * step 0): DLS_OK if prefix_tokens + max_branch_tokens + headroom <= n_ctx,
  * else DLS_ERR_CAPACITY with the numbers in dls_last_error(NULL). */

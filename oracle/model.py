@@ -47,7 +47,8 @@ class OracleSeq:
 
     @property
     def length(self) -> int:
-        return self.lens[-1] if self.n_layers else 0
+        # positions appended by any layer (a skipped layer appends none)
+        return max(self.lens) if self.n_layers else 0
 
     def _reserve(self, layer: int, n: int):
         cap = self.k[layer].shape[0]
@@ -207,16 +208,35 @@ class OracleModel:
         xn = ops.rmsnorm(x, self.norm_gain(None, "output_norm"), self.cfg.rms_eps)
         return self.matmul(None, "output", xn, rows=rows)
 
-    def decode_step(self, seq: OracleSeq, token: int, pos: int, capture: list | None = None) -> np.ndarray:
-        """Logits [vocab] for `token` at position `pos` (= the cache length)."""
+    def decode_step(self, seq: OracleSeq, token: int, pos: int, capture: list | None = None,
+                    skip=()) -> np.ndarray:
+        """Logits [vocab] for `token` at position `pos` (= the cache length).
+
+        ``skip``: layers not computed at this step (the engine page, sections
+        2.5 / 3.5 / 4.5: a skipped layer's output is the previous layer's
+        output); they append nothing to their cache.
+        """
         if pos != seq.length:
             raise ValueError(f"pos {pos} != sequence length {seq.length}")
         x = self.embed(int(token))
         for l in range(self.cfg.n_layers):
-            x = self.layer_forward(l, x, pos, seq)
+            if l not in skip:
+                x = self.layer_forward(l, x, pos, seq)
             if capture is not None:
                 capture.append(x.copy())
         return self.final_logits(x)
+
+    def layer_cosines(self, seq: OracleSeq, token: int, pos: int) -> np.ndarray:
+        """One decode step of `token` at `pos`; for every layer, the cosine
+        similarity of its output with its input (the previous layer's output,
+        the embedding row for layer 0): the calibration the engine page
+        describes for layer skipping (sections 3.5 and 4.5: layers whose
+        output is more than 0.98 similar to the previous one are skipped)."""
+        x0 = self.embed(int(token))
+        cap = []
+        self.decode_step(seq, token, pos, capture=cap)
+        ins = [x0] + cap[:-1]
+        return np.array([ops.cosine(a, b) for a, b in zip(ins, cap)])
 
     def prefill(self, seq: OracleSeq, tokens, capture: list | None = None) -> np.ndarray:
         """All prompt tokens through every layer at once; last token's logits."""
@@ -229,11 +249,11 @@ class OracleModel:
                 capture.append(X[-1].copy())
         return self.final_logits(X[-1])
 
-    def greedy_decode(self, seq: OracleSeq, token: int, n_steps: int):
+    def greedy_decode(self, seq: OracleSeq, token: int, n_steps: int, skip=()):
         """n_steps greedy steps from `token` at the sequence end; (tokens, logits)."""
         toks, logits = [], []
         for _ in range(n_steps):
-            lg = self.decode_step(seq, token, seq.length)
+            lg = self.decode_step(seq, token, seq.length, skip=skip)
             logits.append(lg)
             token = ops.greedy(lg)
             toks.append(token)

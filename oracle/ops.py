@@ -121,3 +121,11 @@ def top2_gap(logits: np.ndarray) -> float:
     """Difference between the largest and second-largest logit."""
     part = np.partition(np.asarray(logits, dtype=np.float64), -2)
     return float(part[-1] - part[-2])
+
+
+def cosine(a: np.ndarray, b: np.ndarray) -> float:
+    """Cosine similarity a.b / (|a| |b|) of two vectors (0 if either is zero)."""
+    a = np.asarray(a, dtype=np.float64).ravel()
+    b = np.asarray(b, dtype=np.float64).ravel()
+    na, nb = np.sqrt(a @ a), np.sqrt(b @ b)
+    return float(a @ b / (na * nb)) if na > 0 and nb > 0 else 0.0

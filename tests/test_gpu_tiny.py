@@ -364,6 +364,45 @@ def test_kv_fork_shared_pages(setup):
     assert m.kv_free_pages() == free0
 
 
+@pytest.mark.parametrize("skipped", [0, 1])
+def test_layer_skip_calibration_and_decode(setup, skipped):
+    """Layer skip (engine page, sections 2.5, 3.5, 4.5): the per-layer cosine
+    calibration matches the oracle's, and decode steps with a layer skipped
+    match the oracle with the same layer skipped, one step at a time and
+    through greedy generation."""
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    prompt = synth.prompt_tokens(cfg, 20, seed=21)
+    seq = m.seq_create()
+    try:
+        m.prefill(seq, prompt)
+        oseq = orc.new_seq()
+        orc.prefill(oseq, prompt)
+        cos = m.layer_cosines(seq, 17, 20)
+        ocos = orc.layer_cosines(oseq, 17, 20)
+        np.testing.assert_allclose(cos, ocos, atol=2e-4)
+        mask = [l == skipped for l in range(cfg.n_layers)]
+        m.set_layer_skip(mask)
+        lg = torch.empty(cfg.vocab, device="cuda")
+        tok = 5
+        for i in range(4):
+            m.decode_step(seq, tok, 21 + i, lg)
+            stream.synchronize()
+            ref = orc.decode_step(oseq, tok, 21 + i, skip={skipped})
+            got = lg.cpu().numpy()
+            assert_close(got, ref, f"skip {skipped} step {i}")
+            tok = check_greedy(got, ref, f"skip {skipped} step {i}")
+        toks = m.generate([seq], [tok], 6)[:, 0]
+        otoks, ologits = orc.greedy_decode(oseq, tok, 6, skip={skipped})
+        for i in range(6):
+            if ops.top2_gap(ologits[i]) <= 1e-2:
+                break
+            assert toks[i] == otoks[i], f"skip {skipped} generate step {i}"
+    finally:
+        m.set_layer_skip(None)
+        m.seq_free(seq)
+
+
 def test_streamed_layers_match_resident(setup):
     torch = _torch()
     cfg, w, m, orc, stream = setup

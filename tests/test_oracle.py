@@ -416,3 +416,59 @@ def test_selected_logit_rows_match_full_head():
     full = m.final_logits(x)
     rows = [0, 5, 47]
     np.testing.assert_allclose(m.final_logits(x, rows=rows), full[rows], rtol=1e-14)
+
+
+# ---------------------------------------------------------------- layer skip (engine page, sections 2.5, 3.5, 4.5)
+
+def test_cosine_closed_forms():
+    v = np.array([3.0, -4.0, 12.0])
+    w = np.array([4.0, 3.0, 0.0])                    # orthogonal to v
+    assert ops.cosine(v, v) == pytest.approx(1.0, abs=1e-15)
+    assert ops.cosine(v, -v) == pytest.approx(-1.0, abs=1e-15)
+    assert ops.cosine(v, w) == pytest.approx(0.0, abs=1e-15)
+    assert ops.cosine(2.0 * v, 3.0 * (v + w)) == pytest.approx(169.0 / (13.0 * np.sqrt(194.0)), rel=1e-14)
+    assert ops.cosine(v, np.zeros(3)) == 0.0
+
+
+def test_skipping_every_layer_leaves_the_embedding_and_no_cache():
+    cfg, w = _micro_weights()
+    m = OracleModel(cfg, w)
+    s = m.new_seq()
+    lg = m.decode_step(s, 7, 0, skip=set(range(cfg.n_layers)))
+    np.testing.assert_array_equal(lg, m.final_logits(m.embed(7)))
+    assert s.lens == [0] * cfg.n_layers and s.length == 0
+
+
+def test_skipping_an_identity_layer_changes_nothing():
+    # a layer with zero output projections adds nothing to the residual:
+    # skipping it is exact, and its cosine (output vs input) is exactly 1
+    cfg, w = _micro_weights()
+    w["layers"][1]["wo"] = np.zeros_like(w["layers"][1]["wo"])
+    w["layers"][1]["w_down"] = np.zeros_like(w["layers"][1]["w_down"])
+    m = OracleModel(cfg, w)
+    toks = synth.prompt_tokens(cfg, 5)
+    a, b, c = m.new_seq(), m.new_seq(), m.new_seq()
+    for i, t in enumerate(toks):
+        la = m.decode_step(a, int(t), i)
+        lb = m.decode_step(b, int(t), i, skip={1})
+    np.testing.assert_array_equal(la, lb)
+    assert b.lens == [5, 0]                              # the skipped layer appended nothing
+    m.prefill(c, toks[:4])
+    cos = m.layer_cosines(c, int(toks[4]), 4)
+    assert cos[1] == pytest.approx(1.0, abs=1e-15)
+    assert -1.0 <= cos[0] < 1.0
+
+
+def test_layer_cosines_follow_the_captured_residuals():
+    cfg, w = _micro_weights()
+    m = OracleModel(cfg, w)
+    s1, s2 = m.new_seq(), m.new_seq()
+    cos = m.layer_cosines(s1, 9, 0)
+    cap = []
+    m.decode_step(s2, 9, 0, capture=cap)
+    x0 = m.embed(9)
+    # layer l: angle between what entered and what left
+    for l, (xin, xout) in enumerate(zip([x0] + cap[:-1], cap)):
+        num = sum(float(p) * float(q) for p, q in zip(xin, xout))
+        den = np.sqrt(sum(float(p) ** 2 for p in xin)) * np.sqrt(sum(float(q) ** 2 for q in xout))
+        assert cos[l] == pytest.approx(num / den, rel=1e-12)
