@@ -28,6 +28,11 @@ prefill yields; the last token's are the ones decoding continues from).
 
 The fork (SwarmKV page, sections 3-4) copies the source sequence's cache; a
 branch then continues at positions prefix_len, prefix_len + 1, ...
+
+Layer skip and self-speculative decoding (the engine page, sections 2.5,
+3.5, 4.5 and 5.3): a decode step may skip layers (their output is their
+input); the speculative loop drafts with skipped layers and keeps only the
+tokens the full model would pick.
 """
 from __future__ import annotations
 
@@ -44,11 +49,11 @@ class OracleSeq:
         self.k = [np.zeros((capacity, n_kv_heads, head_dim)) for _ in range(n_layers)]
         self.v = [np.zeros((capacity, n_kv_heads, head_dim)) for _ in range(n_layers)]
         self.lens = [0] * n_layers
+        self.n = 0   # positions consumed; a layer skipped at a step appends nothing there
 
     @property
     def length(self) -> int:
-        # positions appended by any layer (a skipped layer appends none)
-        return max(self.lens) if self.n_layers else 0
+        return self.n
 
     def _reserve(self, layer: int, n: int):
         cap = self.k[layer].shape[0]
@@ -68,6 +73,14 @@ class OracleSeq:
         self.k[layer][pos0:pos0 + T] = ops.round_f16(k)
         self.v[layer][pos0:pos0 + T] = ops.round_f16(v)
         self.lens[layer] = pos0 + T
+        self.n = max(self.n, pos0 + T)
+
+    def truncate(self, n: int):
+        """Forget positions >= n in every layer (the sequence continues at n)."""
+        if not 0 <= n <= self.n:
+            raise ValueError(f"truncate to {n} of a sequence of length {self.n}")
+        self.lens = [min(v, n) for v in self.lens]
+        self.n = n
 
     def keys(self, layer: int) -> np.ndarray:
         return self.k[layer][: self.lens[layer]]
@@ -81,6 +94,7 @@ class OracleSeq:
         c.k = [a.copy() for a in self.k]
         c.v = [a.copy() for a in self.v]
         c.lens = list(self.lens)
+        c.n = self.n
         return c
 
     def set_layer(self, layer: int, k: np.ndarray, v: np.ndarray):
@@ -90,6 +104,7 @@ class OracleSeq:
         self.k[layer][:n] = k
         self.v[layer][:n] = v
         self.lens[layer] = n
+        self.n = max(self.n, n)
 
 
 class OracleModel:
@@ -224,6 +239,7 @@ class OracleModel:
                 x = self.layer_forward(l, x, pos, seq)
             if capture is not None:
                 capture.append(x.copy())
+        seq.n = pos + 1
         return self.final_logits(x)
 
     def layer_cosines(self, seq: OracleSeq, token: int, pos: int) -> np.ndarray:
@@ -238,8 +254,11 @@ class OracleModel:
         ins = [x0] + cap[:-1]
         return np.array([ops.cosine(a, b) for a, b in zip(ins, cap)])
 
-    def prefill(self, seq: OracleSeq, tokens, capture: list | None = None) -> np.ndarray:
-        """All prompt tokens through every layer at once; last token's logits."""
+    def prefill(self, seq: OracleSeq, tokens, capture: list | None = None,
+                all_logits: bool = False) -> np.ndarray:
+        """All prompt tokens through every layer at once, at positions
+        length .. length+T-1; the last token's logits, or every token's
+        ([T, vocab]) with all_logits."""
         toks = np.asarray(tokens)
         pos0 = seq.length
         X = self.embed(toks)
@@ -247,7 +266,8 @@ class OracleModel:
             X = self.layer_forward(l, X, pos0, seq)
             if capture is not None:
                 capture.append(X[-1].copy())
-        return self.final_logits(X[-1])
+        seq.n = pos0 + len(toks)
+        return self.final_logits(X) if all_logits else self.final_logits(X[-1])
 
     def greedy_decode(self, seq: OracleSeq, token: int, n_steps: int, skip=()):
         """n_steps greedy steps from `token` at the sequence end; (tokens, logits)."""
@@ -258,3 +278,47 @@ class OracleModel:
             token = ops.greedy(lg)
             toks.append(token)
         return toks, logits
+
+    def speculative_decode(self, seq: OracleSeq, token: int, n_tokens: int, draft_skip, k: int):
+        """Greedy self-speculative decoding (the engine page, sections 3.5 and
+        5.3: a cheap draft proposes tokens, the full model checks them in one
+        pass).  The draft is this model with the layers in ``draft_skip``
+        skipped.  Each round, with the current token t at position P:
+
+          1. the draft decodes r = min(k, tokens still wanted - 1) greedy
+             tokens d_1..d_r from t (its layers fill the cache at P..P+r-1);
+          2. the sequence is cut back to P and the full model runs
+             [t, d_1, .., d_r] at positions P..P+r at once (a prefill that
+             keeps every row's logits), giving greedy tokens v_0..v_r;
+          3. the longest prefix with d_i == v_{i-1} is accepted (n tokens);
+             the round emits d_1..d_n and v_n, and the sequence keeps
+             positions up to P+n (t, d_1..d_n), continuing with v_n.
+
+        Returns (tokens [n_tokens], stats {rounds, drafted, accepted}).  The
+        tokens are the full model's greedy continuation: a draft token is
+        kept only where the full model picks it too.
+        """
+        out = []
+        stats = {"rounds": 0, "drafted": 0, "accepted": 0}
+        cur = int(token)
+        skip = set(draft_skip)
+        while len(out) < n_tokens:
+            P = seq.length
+            r = min(k, n_tokens - len(out) - 1)
+            drafts = []
+            t = cur
+            for i in range(r):
+                t = ops.greedy(self.decode_step(seq, t, P + i, skip=skip))
+                drafts.append(t)
+            seq.truncate(P)
+            v = [ops.greedy(lg) for lg in self.prefill(seq, [cur] + drafts, all_logits=True)]
+            n = 0
+            while n < r and drafts[n] == v[n]:
+                n += 1
+            out += drafts[:n] + [v[n]]
+            seq.truncate(P + n + 1)
+            cur = v[n]
+            stats["rounds"] += 1
+            stats["drafted"] += r
+            stats["accepted"] += n
+        return out, stats

@@ -385,8 +385,7 @@ def test_fork_equals_independent_prefill_and_position_matters():
     # restarting RoPE at 0 on the fork must change the result
     m2 = OracleModel(cfg, w)
     s3 = base.fork()
-    for l in range(cfg.n_layers):
-        s3.lens[l] = 0
+    s3.truncate(0)
     lg_pos0 = m2.decode_step(s3, 3, 0)
     assert np.max(np.abs(lg_pos0 - lg_fork)) > 1e-3
 
@@ -436,7 +435,8 @@ def test_skipping_every_layer_leaves_the_embedding_and_no_cache():
     s = m.new_seq()
     lg = m.decode_step(s, 7, 0, skip=set(range(cfg.n_layers)))
     np.testing.assert_array_equal(lg, m.final_logits(m.embed(7)))
-    assert s.lens == [0] * cfg.n_layers and s.length == 0
+    # no layer wrote the cache, but the step consumed position 0
+    assert s.lens == [0] * cfg.n_layers and s.length == 1
 
 
 def test_skipping_an_identity_layer_changes_nothing():
@@ -472,3 +472,98 @@ def test_layer_cosines_follow_the_captured_residuals():
         num = sum(float(p) * float(q) for p, q in zip(xin, xout))
         den = np.sqrt(sum(float(p) ** 2 for p in xin)) * np.sqrt(sum(float(q) ** 2 for q in xout))
         assert cos[l] == pytest.approx(num / den, rel=1e-12)
+
+
+# ---------------------------------------------------------------- self-speculative decoding (engine page, sections 3.5, 5.3)
+
+DEEP = ModelConfig("deep", 4, 64, 4, 2, 16, 96, 48, 10000.0, 8, 0.05)
+
+
+def test_prefill_rows_match_sequential_decode_logits():
+    cfg, w = _micro_weights()
+    m = OracleModel(cfg, w)
+    toks = synth.prompt_tokens(cfg, 6)
+    s1, s2 = m.new_seq(), m.new_seq()
+    m.prefill(s1, toks[:2])
+    m.prefill(s2, toks[:2])
+    rows = m.prefill(s1, toks[2:], all_logits=True)
+    assert rows.shape == (4, cfg.vocab) and s1.length == 6
+    for i, t in enumerate(toks[2:]):
+        np.testing.assert_allclose(rows[i], m.decode_step(s2, int(t), 2 + i), rtol=1e-12, atol=1e-13)
+
+
+def test_truncate_then_decode_is_as_if_the_tail_never_ran():
+    cfg, w = _micro_weights()
+    m = OracleModel(cfg, w)
+    toks = synth.prompt_tokens(cfg, 9)
+    a, b = m.new_seq(), m.new_seq()
+    m.prefill(a, toks[:5])
+    m.prefill(b, toks[:5])
+    for i in range(5, 9):
+        m.decode_step(a, int(toks[i]), i)
+    a.truncate(5)
+    assert a.length == 5 and a.lens == [5, 5]
+    np.testing.assert_array_equal(m.decode_step(a, 11, 5), m.decode_step(b, 11, 5))
+    with pytest.raises(ValueError):
+        a.truncate(7)
+
+
+def _spec_setup(wtype=8, n_prompt=5):
+    cfg, w = _micro_weights(DEEP, wtype)
+    m = OracleModel(cfg, w)
+    prompt = synth.prompt_tokens(cfg, n_prompt, seed=3)
+    s = m.new_seq()
+    first = ops.greedy(m.prefill(s, prompt))
+    return cfg, m, prompt, s, first
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 5])
+@pytest.mark.parametrize("skip", [(), (3,), (1, 2), (0, 1, 2, 3)])
+def test_speculative_tokens_are_the_full_greedy_tokens(k, skip):
+    cfg, m, prompt, s, first = _spec_setup()
+    ref = s.fork()
+    n = 12
+    want, _ = m.greedy_decode(ref, first, n)
+    got, st = m.speculative_decode(s, first, n, skip, k)
+    assert got == want
+    assert s.length == ref.length == len(prompt) + n
+    assert st["rounds"] + st["accepted"] == n and st["accepted"] <= st["drafted"]
+    for l in range(cfg.n_layers):
+        np.testing.assert_allclose(s.keys(l), ref.keys(l), rtol=1e-3, atol=1e-6)
+        np.testing.assert_allclose(s.values(l), ref.values(l), rtol=1e-3, atol=1e-6)
+
+
+@pytest.mark.parametrize("k", [1, 3, 4])
+def test_speculative_with_the_full_model_as_draft_accepts_every_token(k):
+    cfg, m, prompt, s, first = _spec_setup()
+    n = 11
+    _, st = m.speculative_decode(s, first, n, (), k)
+    assert st["accepted"] == st["drafted"]
+    assert st["rounds"] == -(-n // (k + 1))
+
+
+@pytest.mark.parametrize("skip,k", [((3,), 3), ((1, 2), 2), ((0, 1, 2, 3), 3)])
+def test_speculative_acceptance_matches_brute_force(skip, k):
+    # rebuild every round from scratch: the cache holds the prompt and the
+    # tokens emitted so far; the draft's greedy run is compared with the full
+    # model's greedy tokens, and the common prefix is what a round accepts
+    cfg, m, prompt, s, first = _spec_setup()
+    n = 12
+    full, _ = m.greedy_decode(s.fork(), first, n)
+    _, st = m.speculative_decode(s, first, n, skip, k)
+    emitted = [first] + full
+    e = rounds = accepted = drafted = 0
+    while e < n:
+        r = min(k, n - e - 1)
+        seq = m.new_seq()
+        m.prefill(seq, list(prompt) + emitted[:e])
+        drafts, _ = m.greedy_decode(seq, emitted[e], r, skip=set(skip))
+        a = 0
+        while a < r and drafts[a] == full[e + a]:
+            a += 1
+        e += a + 1
+        rounds += 1
+        accepted += a
+        drafted += r
+    assert st == {"rounds": rounds, "drafted": drafted, "accepted": accepted}
+    assert accepted < drafted       # this draft is wrong somewhere, so rejection is exercised
