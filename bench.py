@@ -66,11 +66,15 @@ def parse():
                    help="keep only the first N layers (small cases for ncu captures; not a bench result)")
     p.add_argument("--skip-threshold", type=float, default=0.98,
                    help="layer skip workload: skip layers whose calibrated cosine exceeds this")
-    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip"], default="decode",
+    p.add_argument("--draft-k", default="1,3,7",
+                   help="speculative workload: draft lengths to time (comma-separated)")
+    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip", "spec"], default="decode",
                    help="decode (default, the headline line); the others are secondary measurements: "
                         "prefill (prompt of --ctx tokens), fork (shared prefix -> 8 branches), "
                         "stream (70B Q4_0 resident vs a 24 GB device budget), "
-                        "skip (decode with the layers whose calibrated cosine exceeds --skip-threshold skipped)")
+                        "skip (decode with the layers whose calibrated cosine exceeds --skip-threshold skipped), "
+                        "spec (self-speculative greedy decoding vs plain greedy decoding; --config 70b: the 24 GB "
+                        "budget with the resident layers as the draft)")
     return p.parse_args()
 
 
@@ -288,6 +292,81 @@ def run_skip(args):
                       "clocks": clk.summary()})
 
 
+def run_spec(args):
+    """Self-speculative greedy decoding against plain greedy decoding from the
+    same state (a copy of one prefilled sequence for every run).  --config
+    70b: 70B Q4_0 under the 24 GB device budget, and the draft is the
+    resident layers (the streamed ones are skipped, so draft steps copy
+    nothing in); other configs: all layers resident, and the draft skips the
+    layers whose calibrated cosine exceeds --skip-threshold."""
+    import torch
+    import synth
+    from decode_llama_step_gb300 import dls
+    cfg = load_config(args.config, args.layers)
+    streamed = cfg.name == "70b"
+    ctx = (args.ctx if args.ctx != 2048 else cfg.workload["ctx"]) if streamed else args.ctx
+    D = args.steps
+    ks = [int(k) for k in args.draft_k.split(",") if k.strip()]
+    w = synth.model_weights(cfg)
+    stream = torch.cuda.Stream()
+    budget = cfg.workload["budget_bytes"] if streamed else 0
+    m = dls.Model(cfg, w, max_seqs=2, max_ctx=ctx + D + 64, stream=stream, device_budget_bytes=budget)
+    del w
+    base, work = m.seq_create(), m.seq_create()
+    prompt = synth.prompt_tokens(cfg, ctx, seed=1)
+    lg = torch.empty(cfg.vocab, device="cuda")
+    m.prefill(base, prompt, lg)
+    tok = int(torch.argmax(lg).item())
+    if streamed:
+        res = m.resident_layers()
+        mask = np.array([l >= res for l in range(cfg.n_layers)])
+        draft = f"the {res} resident layers ({cfg.n_layers - res} streamed layers skipped)"
+    else:
+        m.kv_fork(base, [work])
+        cos = m.layer_cosines(work, tok, ctx)
+        mask = cos > args.skip_threshold
+        draft = f"{cfg.n_layers - int(mask.sum())} layers (cosine > {args.skip_threshold} skipped: " \
+                f"{[int(i) for i in np.nonzero(mask)[0]]})"
+    m.kv_fork(base, [work])
+    m.generate([work], [tok], max(args.warmup, 1))
+    m.kv_fork(base, [work])
+    with ClockSampler(0) as clk:
+        t_plain = _events(torch, stream, lambda: m.generate([work], [tok], D))
+    m.kv_fork(base, [work])
+    ref = m.generate([work], [tok], D)[:, 0]
+    runs = {}
+    best = None
+    for k in ks:
+        m.kv_fork(base, [work])
+        m.generate_speculative(work, tok, min(D, 8), mask, k)   # warm-up: graphs, pages
+        m.kv_fork(base, [work])
+        out = {}
+
+        def go():
+            out["r"] = m.generate_speculative(work, tok, D, mask, k)
+        t = _events(torch, stream, go)
+        toks, st = out["r"]
+        same = int(np.argmax(np.concatenate([toks != ref, [True]])))
+        runs[f"k={k}"] = {"tok_s": round(D / t, 3), "ms_per_token": round(1000 * t / D, 3),
+                          "speedup": round(t_plain / t, 3), "rounds": st["rounds"], "drafted": st["drafted"],
+                          "accepted": st["accepted"],
+                          "acceptance": round(st["accepted"] / max(st["drafted"], 1), 4),
+                          "tokens_per_round": round(D / st["rounds"], 3),
+                          "tokens_equal_to_plain_greedy": same}
+        if best is None or D / t > best[1]:
+            best = (k, D / t, t)
+    m.close()
+    k, v, t = best
+    return base_line(f"self-speculative greedy decode tok/s, {cfg.name}-shape "
+                     f"{'Q8_0' if cfg.wtype == 8 else 'Q4_0'} batch 1"
+                     + (", 24 GB device budget (layer streaming)" if streamed else ""),
+                     v, "tok/s", D, args.warmup, 1000 * t / D,
+                     f"{cfg.name} greedy decode of {D} tokens after a {ctx}-token prompt; draft = {draft}; "
+                     f"best draft length k={k}",
+                     {"speculative": {"plain_tok_s": round(D / t_plain, 3), "runs": runs, "draft": draft},
+                      "clocks": clk.summary()})
+
+
 def h2d_peak(torch, chunk=256 << 20, inflight=4, reps=10):
     """Best pinned host -> device copy rate: 256 MB chunks, several in flight."""
     host = torch.empty(chunk * inflight, dtype=torch.uint8, pin_memory=True)
@@ -479,7 +558,8 @@ def main():
     if args.workload != "decode":
         if int(os.environ.get("RANK", "0")) != 0:
             return 0
-        fn = {"prefill": run_prefill, "fork": run_fork, "stream": run_stream, "skip": run_skip}[args.workload]
+        fn = {"prefill": run_prefill, "fork": run_fork, "stream": run_stream, "skip": run_skip,
+              "spec": run_spec}[args.workload]
         print(json.dumps(fn(args)), flush=True)
         return 0
 

@@ -77,7 +77,7 @@ struct Seq {
 
 struct GraphEntry {
   int rows;
-  bool head, argmax;
+  bool head, argmax, drafting;
   cudaGraphExec_t exec;
 };
 
@@ -117,6 +117,10 @@ struct dls_model {
   std::vector<int> page_ref;  // sequences holding each page (a shared fork makes it > 1)
   std::vector<uint8_t> skip_host;  // layers skipped by decode steps (dls_set_layer_skip)
   uint8_t* skip_dev = nullptr;     // the same flags for the step kernel
+  std::vector<uint8_t> draft_host; // layers the speculative draft skips (dls_generate_speculative)
+  uint8_t* draft_dev = nullptr;
+  bool drafting = false;           // decode steps run the draft (its mask instead of skip_host)
+  bool pass_streams = false;       // the current pass over the layers copies streamed layers in
   std::vector<Seq> seqs;
   int32_t* pt_dev = nullptr;
   std::vector<int32_t> pt_host;
@@ -361,10 +365,16 @@ int enqueue_copy_layer(dls_model* m, int l) {
   return DLS_OK;
 }
 
+// Layers the decode steps skip right now: the draft's mask while drafting.
+const uint8_t* step_skip(const dls_model* m) { return m->drafting ? m->draft_host.data() : m->skip_host.data(); }
+
 // Start a pass over the layers: with streamed layers, the copy stream joins
-// the compute stream here and fills both buffers with the first two.
-int stream_begin(dls_model* m) {
-  if (m->resident >= m->L) return DLS_OK;
+// the compute stream here and fills both buffers with the first two.  A pass
+// that skips every streamed layer (`skip`, or NULL for none) copies nothing.
+int stream_begin(dls_model* m, const uint8_t* skip) {
+  m->pass_streams = false;
+  for (int l = m->resident; l < m->L; ++l) m->pass_streams |= !(skip && skip[l]);
+  if (!m->pass_streams) return DLS_OK;
   CK(cudaEventRecord(m->ev_start, m->stream));
   CK(cudaStreamWaitEvent(m->copy_stream, m->ev_start, 0));
   // both buffers are free at the start of a pass
@@ -378,6 +388,10 @@ int stream_begin(dls_model* m) {
 int layer_begin(dls_model* m, int l, LayerPtrs* P) {
   const bool streamed = l >= m->resident;
   const int buf = (l - m->resident) & 1;
+  if (streamed && !m->pass_streams) {  // a skipped layer of a pass that copies nothing: no weights
+    *P = LayerPtrs{};
+    return DLS_OK;
+  }
   if (streamed) CK(cudaStreamWaitEvent(m->stream, m->ev_filled[buf], 0));
   *P = layer_ptrs(m, streamed ? m->stage[buf] : m->layer_dev[l]);
   return DLS_OK;
@@ -385,7 +399,7 @@ int layer_begin(dls_model* m, int l, LayerPtrs* P) {
 
 // Layer l's last kernel is enqueued: release its buffer, refill it with l + 2.
 int layer_end(dls_model* m, int l) {
-  if (l < m->resident) return DLS_OK;
+  if (l < m->resident || !m->pass_streams) return DLS_OK;
   CK(cudaEventRecord(m->ev_free[(l - m->resident) & 1], m->stream));
   if (l + 2 < m->L) TRY(enqueue_copy_layer(m, l + 2));
   return DLS_OK;
@@ -397,11 +411,12 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
   float* x = m->x + (size_t)b * m->H;
   float* logits = m->logits + (size_t)b * m->V;
   LK(K_EMBED, launch_embed(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp, b, x, m->V, s, pdl));
-  TRY(stream_begin(m));
+  const uint8_t* skip = step_skip(m);
+  TRY(stream_begin(m, skip));
   for (int l = 0; l < m->L; ++l) {
     LayerPtrs P;
     TRY(layer_begin(m, l, &P));
-    if (m->skip_host[l]) {  // skipped: the residual passes through (a streamed layer's copy still runs)
+    if (skip[l]) {  // skipped: the residual passes through (a streamed layer's copy still runs if any streamed layer does)
       if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * m->H, x, m->H * sizeof(float), cudaMemcpyDeviceToDevice, s));
       TRY(layer_end(m, l));
       continue;
@@ -508,13 +523,18 @@ int run_tgemm(dls_model* m, int kind, int epi, PgArgs g) {
 // projections run as tensor-core GEMMs over the T tokens (fp16 operands,
 // fp32 accumulation), attention as a causal flash pass over the paged cache
 // (which already holds positions < pos0 and receives the chunk's K/V here).
-int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos0, bool head, float* capture) {
+// Token ids come from host `tokens`, or are already in pf_tok when it is
+// NULL.  head: HEAD_NONE, HEAD_LAST (the last row's logits into logits row
+// 0) or HEAD_ALL (every row's logits into logits rows 0..T-1, and their
+// greedy picks into next_tok[0..T-1]).  Layer skip masks do not apply.
+enum { HEAD_NONE = 0, HEAD_LAST = 1, HEAD_ALL = 2 };
+int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos0, int head, float* capture) {
   cudaStream_t s = m->stream;
   const int H = m->H, qkv_ld = m->q_rows + 2 * m->kv_rows;
-  CK(cudaMemcpyAsync(m->pf_tok, tokens, (size_t)T * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+  if (tokens) CK(cudaMemcpyAsync(m->pf_tok, tokens, (size_t)T * sizeof(int32_t), cudaMemcpyHostToDevice, s));
   LK(K_EMBED, launch_embed_rows(mat_at(m->emb_block, m->emb_off), m->wtype, m->pf_tok, T, m->V, m->pf_x, H,
                                 &m->sp->status, s));
-  TRY(stream_begin(m));
+  TRY(stream_begin(m, nullptr));
   for (int l = 0; l < m->L; ++l) {
     LayerPtrs P;
     TRY(layer_begin(m, l, &P));
@@ -588,7 +608,21 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
                          cudaMemcpyDeviceToDevice, s));
     TRY(layer_end(m, l));
   }
-  if (head) {
+  if (head == HEAD_ALL) {
+    LK(K_HEAD, launch_rmsnorm_rows(m->pf_x, T, H, H, m->out_norm, m->eps, m->pf_a, m->pf_a_lo, H, s));
+    PgArgs gh{};
+    gh.w = head_mat(m);
+    gh.x = m->pf_a;
+    gh.xlo = m->pf_a_lo;
+    gh.kx = H;
+    gh.T = T;
+    gh.y = m->logits;
+    gh.ldy = m->V;
+    gh.status = &m->sp->status;
+    TRY(run_tgemm(m, K_HEAD, EPI_STORE, gh));
+    LK(K_ARGMAX, launch_argmax(m->logits, m->V, T, m->next_tok, m->argmax_part, m->argmax_cnt,
+                               argmax_blocks(T, m->num_sms), s, false));
+  } else if (head == HEAD_LAST) {
     GemvArgs gh{};
     gh.w = head_mat(m);
     gh.unit = 1;
@@ -612,11 +646,12 @@ int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
   float* x = m->x;  // [n][H]
   LK(K_EMBED, launch_embed_rows(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp->token, n, m->V, x, H,
                                 &m->sp->status, s));
-  TRY(stream_begin(m));
+  const uint8_t* skip = step_skip(m);
+  TRY(stream_begin(m, skip));
   for (int l = 0; l < m->L; ++l) {
     LayerPtrs P;
     TRY(layer_begin(m, l, &P));
-    if (m->skip_host[l]) {  // skipped: the residuals pass through
+    if (skip[l]) {  // skipped: the residuals pass through
       if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * H, x, H * sizeof(float), cudaMemcpyDeviceToDevice, s));
       TRY(layer_end(m, l));
       continue;
@@ -747,7 +782,7 @@ int enqueue_persistent(dls_model* m, bool head, bool argmax) {
   a.S = m->step.splits;
   a.trace = m->profiling ? m->step_trace : nullptr;
   a.ctrace = m->profiling ? m->step_ctrace : nullptr;
-  a.skip = m->skip_dev;
+  a.skip = m->drafting ? m->draft_dev : m->skip_dev;
   a.ns = m->step.ns;
   a.stage_bytes = m->step.stage_bytes;
   {
@@ -798,7 +833,7 @@ int run_step(dls_model* m, int rows, bool head, bool argmax) {
   const bool persistent = m->use_step && rows == 1;
   if (persistent && !m->step_graph_ok) return enqueue_step(m, rows, head, argmax, nullptr);
   for (auto& g : m->graphs)
-    if (g.rows == rows && g.head == head && g.argmax == argmax) {
+    if (g.rows == rows && g.head == head && g.argmax == argmax && g.drafting == m->drafting) {
       CK(cudaGraphLaunch(g.exec, m->stream));
       return DLS_OK;
     }
@@ -817,7 +852,7 @@ int run_step(dls_model* m, int rows, bool head, bool argmax) {
   }
   if (r != DLS_OK) return r;
   if (e != cudaSuccess) return fail(m, DLS_ERR_CUDA, "capture cuda=%s", cudaGetErrorString(e));
-  m->graphs.push_back({rows, head, argmax, exec});
+  m->graphs.push_back({rows, head, argmax, m->drafting, exec});
   CK(cudaGraphLaunch(exec, m->stream));
   return DLS_OK;
 }
@@ -1219,8 +1254,9 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   TRYC(dev_alloc_t(m, (size_t)B * m->q_rows, &m->q, "q"));
   TRYC(dev_alloc_t(m, (size_t)B * m->q_rows, &m->o, "o"));
   TRYC(dev_alloc_t(m, (size_t)B * 2 * m->F, &m->gu, "gate_up"));
-  TRYC(dev_alloc_t(m, (size_t)B * m->V, &m->logits, "logits"));
-  TRYC(dev_alloc_t(m, (size_t)kMaxBatch, &m->next_tok, "next_token"));
+  // logits rows: a batch, or the rows of one dls_verify pass
+  TRYC(dev_alloc_t(m, (size_t)std::max(B, DLS_MAX_VERIFY) * m->V, &m->logits, "logits"));
+  TRYC(dev_alloc_t(m, (size_t)std::max(kMaxBatch, DLS_MAX_VERIFY), &m->next_tok, "next_token"));
   TRYC(dev_alloc_t(m, (size_t)4096, &m->argmax_buf, "argmax"));
   TRYC(dev_alloc_t(m, (size_t)4096 + 2 * m->num_sms, &m->argmax_part, "argmax_partials"));
   TRYC(dev_alloc_t(m, (size_t)4096, &m->argmax_cnt, "argmax_counters"));
@@ -1235,7 +1271,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   if (const char* e = getenv("DLS_PREFILL_CHUNK")) m->pf_cap = std::max(1, std::min(m->max_ctx, atoi(e)));
   m->pf_ldh = (m->F + 31) & ~31;
   // token-major scratch shared by prefill chunks and batched decode rows
-  const size_t pf_rows = (size_t)std::max(m->pf_cap, B);
+  const size_t pf_rows = (size_t)std::max(std::max(m->pf_cap, B), DLS_MAX_VERIFY);
   TRYC(dev_alloc_t(m, pf_rows * m->H, &m->pf_x, "prefill_x"));
   TRYC(dev_alloc_t(m, 2 * pf_rows * std::max(m->H, m->q_rows), &m->pf_a, "prefill_a16"));
   m->pf_a_lo = m->pf_a + pf_rows * std::max(m->H, m->q_rows);
@@ -1243,7 +1279,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   TRYC(dev_alloc_t(m, pf_rows * m->q_rows, &m->pf_q, "prefill_q"));
   TRYC(dev_alloc_t(m, 2 * pf_rows * m->pf_ldh, &m->pf_h, "prefill_h16"));
   m->pf_h_lo = m->pf_h + pf_rows * m->pf_ldh;
-  TRYC(dev_alloc_t(m, (size_t)m->pf_cap, &m->pf_tok, "prefill_tokens"));
+  TRYC(dev_alloc_t(m, pf_rows, &m->pf_tok, "prefill_tokens"));
   if (B > 1) {
     m->attn_splits_b = attn_default_splits(B, m->nkv, m->num_sms, m->max_ctx);
     const size_t wsb = attn_workspace_bytes(B, m->nh, m->nkv, m->hd, m->attn_splits_b);
@@ -1254,7 +1290,8 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   }
   {
     // split-K partials for batches of up to 16 rows: [split][16][rows]
-    const int max_rows = std::max(std::max(m->q_rows + 2 * m->kv_rows, 2 * m->F), m->H);
+    // (the LM head of a batch or of a dls_verify pass included)
+    const int max_rows = std::max(std::max(std::max(m->q_rows + 2 * m->kv_rows, 2 * m->F), m->H), m->V);
     m->tg_part_elems = (size_t)kTgMaxSplit * 16 * max_rows;
     TRYC(dev_alloc_t(m, m->tg_part_elems, &m->tg_part, "gemm_split_partials"));
     TRYC(dev_alloc_t(m, (size_t)kTgCounters, &m->tg_cnt, "gemm_split_counters"));
@@ -1313,6 +1350,9 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   m->skip_host.assign(m->L, 0);
   TRYC(dev_alloc_t(m, (size_t)m->L, &m->skip_dev, "layer_skip"));
   CKC(cudaMemsetAsync(m->skip_dev, 0, m->L, m->stream));
+  m->draft_host.assign(m->L, 0);
+  TRYC(dev_alloc_t(m, (size_t)m->L, &m->draft_dev, "draft_skip"));
+  CKC(cudaMemsetAsync(m->draft_dev, 0, m->L, m->stream));
   TRYC(sync_stream(m, m->stream));
   m->seqs.assign(m->max_seqs, Seq());
   TRYC(setup_persistent(m));
@@ -1366,7 +1406,8 @@ int dls_prefill(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, flo
   for (int c0 = 0; c0 < n; c0 += m->pf_cap) {
     const int T = std::min(m->pf_cap, n - c0);
     const bool last = c0 + T == n;
-    TRY(enqueue_prefill(m, seq, tokens + c0, T, pos0 + c0, last && logits_out != nullptr, last ? cap : nullptr));
+    TRY(enqueue_prefill(m, seq, tokens + c0, T, pos0 + c0, last && logits_out ? HEAD_LAST : HEAD_NONE,
+                        last ? cap : nullptr));
   }
   TRY(copy_out(m, logits_out, m->logits, (size_t)m->V * sizeof(float)));
   TRY(sync_stream(m, m->stream));
@@ -1451,6 +1492,158 @@ int dls_generate(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* to
   TRY(sync_stream(m, m->stream));
   TRY(check_status(m));
   for (int i = 0; i < n; ++i) m->seqs[seqs[i]].len += n_steps;
+  return DLS_OK;
+}
+
+// Cut `seq` back to `len` positions: pages past them return to the pool
+// (a shared page stays with its other holders), and the page position len
+// falls in, when partly kept and shared, is replaced by a private copy so
+// that later appends never write into a page another sequence reads.
+int truncate_seq(dls_model* m, int seq, int len) {
+  Seq& s = m->seqs[seq];
+  if (len < 0 || len > s.len) return fail(m, DLS_ERR_ARG, "seq=%d truncate to %d of length %d", seq, len, s.len);
+  const int keep = std::min(pages_needed(m, len), (int)s.pages.size());
+  const bool cow = len % m->pt && keep > 0 && m->page_ref[s.pages[keep - 1]] > 1;
+  if (cow) {
+    size_t avail = m->free_pages.size();
+    for (size_t k = keep; k < s.pages.size(); ++k) avail += m->page_ref[s.pages[k]] == 1 ? 1 : 0;
+    if (avail < 1) return fail(m, DLS_ERR_CAPACITY, "seq=%d truncate needs a page for its shared tail", seq);
+  }
+  const int n_drop = (int)s.pages.size() - keep;
+  for (int k = keep; k < (int)s.pages.size(); ++k) {
+    const int p = s.pages[k];
+    if (--m->page_ref[p] == 0) m->free_pages.push_back(p);
+    m->pt_host[(size_t)seq * m->max_pages + k] = -1;
+  }
+  s.pages.resize(keep);
+  if (n_drop > 0)  // pageable source: staged before the call returns
+    CK(cudaMemcpyAsync(m->pt_dev + (size_t)seq * m->max_pages + keep, &m->pt_host[(size_t)seq * m->max_pages + keep],
+                       n_drop * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+  if (cow) {
+    const int old = s.pages[keep - 1];
+    const int fresh = m->free_pages.back();
+    m->free_pages.pop_back();
+    m->page_ref[fresh] = 1;
+    --m->page_ref[old];
+    s.pages[keep - 1] = fresh;
+    m->pt_host[(size_t)seq * m->max_pages + keep - 1] = fresh;
+    const int2 pair = make_int2(old, fresh);
+    CK(cudaMemcpyAsync(m->pairs_dev, &pair, sizeof(int2), cudaMemcpyHostToDevice, m->stream));
+    CK(launch_kv_copy(m->k_pool, m->v_pool, m->kv_layer_elems, m->L, m->page_elems, m->pairs_dev, 1, m->stream));
+    CK(cudaMemcpyAsync(m->pt_dev + (size_t)seq * m->max_pages + keep - 1,
+                       &m->pt_host[(size_t)seq * m->max_pages + keep - 1], sizeof(int32_t), cudaMemcpyHostToDevice,
+                       m->stream));
+    TRY(sync_stream(m, m->stream));  // `pair` lives on this stack frame
+  }
+  s.len = len;
+  return DLS_OK;
+}
+
+int dls_seq_truncate(dls_model* m, int32_t seq, int32_t len) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  TRY(check_seq(m, seq));
+  return truncate_seq(m, seq, len);
+}
+
+int dls_verify(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out, int32_t* argmax_out) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  TRY(check_seq(m, seq));
+  if (n < 1 || n > DLS_MAX_VERIFY || !tokens) return fail(m, DLS_ERR_ARG, "n=%d (1..%d) tokens=%p", n, DLS_MAX_VERIFY,
+                                                          (const void*)tokens);
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= m->V) return fail(m, DLS_ERR_ARG, "token[%d]=%d vocab=%d", i, tokens[i], m->V);
+  Seq& s = m->seqs[seq];
+  if ((long long)s.len + n > m->max_ctx)
+    return fail(m, DLS_ERR_CAPACITY, "seq=%d length=%d n=%d max_ctx=%d", seq, s.len, n, m->max_ctx);
+  TRY(ensure_pages(m, seq, s.len + n));
+  const int32_t pos0 = s.len;
+  TRY(set_params(m, 1, &seq, &tokens[0], &pos0, true));
+  TRY(enqueue_prefill(m, seq, tokens, n, pos0, HEAD_ALL, nullptr));
+  TRY(copy_out(m, logits_out, m->logits, (size_t)n * m->V * sizeof(float)));
+  if (argmax_out) CK(cudaMemcpyAsync(argmax_out, m->next_tok, n * sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
+  TRY(sync_stream(m, m->stream));
+  TRY(check_status(m));
+  s.len += n;
+  return DLS_OK;
+}
+
+// Self-speculative greedy decoding: per round, r draft steps (decode steps
+// with the draft's layers skipped, tokens fed back on the device), the
+// sequence cut back, one dls_verify-style pass of the current token and the
+// r drafts through every layer, and the longest agreeing prefix kept.  One
+// host round trip per round (the drafts and the full model's picks).
+int dls_generate_speculative(dls_model* m, int32_t seq, int32_t token, int32_t n_tokens, const uint8_t* draft_skip,
+                             int32_t draft_k, int32_t* tokens_out, int32_t* stats) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  TRY(check_seq(m, seq));
+  if (token < 0 || token >= m->V) return fail(m, DLS_ERR_ARG, "token=%d vocab=%d", token, m->V);
+  if (n_tokens < 1 || !tokens_out || !draft_skip || draft_k < 0 || draft_k >= DLS_MAX_VERIFY)
+    return fail(m, DLS_ERR_ARG, "n_tokens=%d draft_k=%d (0..%d) draft_skip=%p", n_tokens, draft_k, DLS_MAX_VERIFY - 1,
+                (const void*)draft_skip);
+  Seq& s = m->seqs[seq];
+  const int P0 = s.len;
+  if ((long long)P0 + n_tokens > m->max_ctx)
+    return fail(m, DLS_ERR_CAPACITY, "seq=%d length=%d n_tokens=%d max_ctx=%d", seq, P0, n_tokens, m->max_ctx);
+  const int need = std::max(0, pages_needed(m, P0 + n_tokens) - (int)s.pages.size());
+  if (need > (int)m->free_pages.size()) return fail(m, DLS_ERR_CAPACITY, "need_pages=%d free=%zu", need, m->free_pages.size());
+  bool same = true;
+  for (int l = 0; l < m->L; ++l) same &= (m->draft_host[l] != 0) == (draft_skip[l] != 0);
+  if (!same) {
+    for (int l = 0; l < m->L; ++l) m->draft_host[l] = draft_skip[l] ? 1 : 0;
+    CK(cudaMemcpyAsync(m->draft_dev, m->draft_host.data(), m->L, cudaMemcpyHostToDevice, m->stream));
+    TRY(sync_stream(m, m->stream));  // pageable source
+    drop_graphs(m);                   // captured draft steps hold the old mask
+  }
+  if (m->tokens_cap < (size_t)DLS_MAX_VERIFY) {
+    int32_t* t = nullptr;
+    TRY(dev_alloc_t(m, (size_t)1024, &t, "generated_tokens"));
+    dev_free(m, m->tokens_dev);
+    m->tokens_dev = t;
+    m->tokens_cap = 1024;
+    drop_graphs(m);  // graphs bake the output pointer in
+  }
+  int rounds = 0, drafted = 0, accepted = 0, done = 0, cur = token;
+  int32_t host[2 * DLS_MAX_VERIFY];
+  while (done < n_tokens) {
+    const int P = s.len;
+    const int r = std::min(draft_k, n_tokens - done - 1);
+    TRY(ensure_pages(m, seq, P + r + 1));
+    TRY(set_params(m, 1, &seq, &cur, &P, true));
+    if (r > 0) {
+      m->drafting = true;
+      int rc = DLS_OK;
+      for (int t = 0; t < r && rc == DLS_OK; ++t) rc = run_step(m, 1, false, true);
+      m->drafting = false;
+      TRY(rc);
+      // the verify pass reads [cur, d_1 .. d_r]: cur from the host, the drafts where the steps left them
+      CK(cudaMemcpyAsync(m->pf_tok + 1, m->tokens_dev, r * sizeof(int32_t), cudaMemcpyDeviceToDevice, m->stream));
+    }
+    CK(cudaMemcpyAsync(m->pf_tok, &cur, sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+    TRY(enqueue_prefill(m, seq, nullptr, r + 1, P, HEAD_ALL, nullptr));
+    // read back after the whole round is enqueued (pageable destinations block the host)
+    if (r > 0)
+      CK(cudaMemcpyAsync(host + DLS_MAX_VERIFY, m->tokens_dev, r * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                         m->stream));
+    CK(cudaMemcpyAsync(host, m->next_tok, (r + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
+    TRY(sync_stream(m, m->stream));
+    TRY(check_status(m));
+    int n = 0;
+    while (n < r && host[DLS_MAX_VERIFY + n] == host[n]) ++n;
+    for (int i = 0; i < n; ++i) tokens_out[done + i] = host[DLS_MAX_VERIFY + i];
+    tokens_out[done + n] = host[n];
+    done += n + 1;
+    cur = host[n];
+    s.len = P + r + 1;  // the verify pass filled positions P .. P+r
+    TRY(truncate_seq(m, seq, P + n + 1));
+    ++rounds;
+    drafted += r;
+    accepted += n;
+  }
+  if (stats) {
+    stats[0] = rounds;
+    stats[1] = drafted;
+    stats[2] = accepted;
+  }
   return DLS_OK;
 }
 

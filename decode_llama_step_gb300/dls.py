@@ -71,6 +71,9 @@ _SIGS = {
     "dls_kv_free_pages": (i32, [vp]),
     "dls_set_layer_skip": (ctypes.c_int, [vp, vp, i32]),
     "dls_layer_cosines": (ctypes.c_int, [vp, i32, i32, i32, vp]),
+    "dls_seq_truncate": (ctypes.c_int, [vp, i32, i32]),
+    "dls_verify": (ctypes.c_int, [vp, i32, vp, i32, vp, vp]),
+    "dls_generate_speculative": (ctypes.c_int, [vp, i32, i32, i32, vp, i32, vp, vp]),
     "dls_check_context_budget": (ctypes.c_int, [i32, i32, i32, i32]),
     "dls_set_resident_layers": (ctypes.c_int, [vp, i32]),
     "dls_resident_layers": (i32, [vp]),
@@ -335,6 +338,27 @@ class Model:
         out = np.zeros(self.cfg.n_layers, dtype=np.float32)
         self._c(self.lib.dls_layer_cosines(self.handle, seq, int(token), int(pos), out.ctypes.data))
         return out
+
+    def seq_truncate(self, seq: int, length: int):
+        self._c(self.lib.dls_seq_truncate(self.handle, seq, int(length)))
+
+    def verify(self, seq: int, tokens, logits_out=None) -> np.ndarray:
+        """Score tokens at the sequence end in one pass; each position's greedy pick."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        out = np.empty(t.size, dtype=np.int32)
+        self._c(self.lib.dls_verify(self.handle, seq, t.ctypes.data, t.size, _ptr(logits_out), out.ctypes.data))
+        return out
+
+    def generate_speculative(self, seq: int, token: int, n_tokens: int, draft_skip, draft_k: int = 3):
+        """Greedy self-speculative generation; (tokens [n_tokens], stats dict)."""
+        mask = np.ascontiguousarray(np.asarray(draft_skip, dtype=bool).astype(np.uint8))
+        if mask.size != self.cfg.n_layers:
+            raise ValueError(f"draft_skip has {mask.size} entries, the model {self.cfg.n_layers} layers")
+        out = np.empty(int(n_tokens), dtype=np.int32)
+        st = np.zeros(3, dtype=np.int32)
+        self._c(self.lib.dls_generate_speculative(self.handle, seq, int(token), int(n_tokens), mask.ctypes.data,
+                                                  int(draft_k), out.ctypes.data, st.ctypes.data))
+        return out, {"rounds": int(st[0]), "drafted": int(st[1]), "accepted": int(st[2])}
 
     # --- residency
     def set_resident_layers(self, n: int):

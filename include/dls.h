@@ -56,6 +56,8 @@ extern "C" {
 
 #define DLS_ABI_VERSION 1
 #define DLS_MAX_BATCH 8
+/* Most positions one dls_verify pass scores (and 1 + the longest draft). */
+#define DLS_MAX_VERIFY 16
 
 typedef struct dls_model dls_model;
 
@@ -155,8 +157,9 @@ int32_t dls_seq_length(const dls_model* m, int32_t seq);
  * token once).  The tokens go through in chunks of up to 1024 (the
  * environment variable DLS_PREFILL_CHUNK, read at model creation, sets
  * another size): each projection of a chunk is one tensor-core GEMM with
- * fp16 operands (weights dequantised to fp16(d*q), activations rounded to
- * fp16) and fp32 accumulation; attention is causal over the cache.  The
+ * split fp16 operands (weights d*q and activations each as an fp16 value
+ * plus the fp16 of its rounding residual, three products per K step) and
+ * fp32 accumulation; attention is causal over the cache.  The
  * chunking changes a token's results at most by the fp32 summation order of
  * the GEMM tiling (chunks of up to 16 tokens split K across CTAs).  logits_out (host or device fp32
  * [vocab], or NULL) receives the logits of the last token.  DLS_ERR_CAPACITY
@@ -231,6 +234,42 @@ int dls_set_layer_skip(dls_model* m, const uint8_t* skip, int32_t n_layers);
  * host cos_out [n_layers].  Layers above a threshold (0.98 on the page) are
  * the ones to pass to dls_set_layer_skip. */
 int dls_layer_cosines(dls_model* m, int32_t seq, int32_t token, int32_t pos, float* cos_out);
+
+/* ---- self-speculative decoding (the engine page, sections 3.5 and 5.3) ------- */
+
+/* Cut `seq` back to its first `len` positions (0 <= len <= length, else
+ * DLS_ERR_ARG); decoding continues at position len.  Pages past them return
+ * to the pool (pages shared by a dls_kv_fork_shared stay with their other
+ * holders); when the page that position len falls in is shared, it is first
+ * replaced by a private copy (DLS_ERR_CAPACITY, nothing changed, if the pool
+ * has no page for it). */
+int dls_seq_truncate(dls_model* m, int32_t seq, int32_t len);
+
+/* Score n tokens at once (1 <= n <= DLS_MAX_VERIFY): tokens (host int32
+ * [n]) go through every layer at positions length..length+n-1 as one
+ * dls_prefill chunk (the cache receives their K/V, the sequence grows by n),
+ * and every position's logits are kept: logits_out (host or device fp32
+ * [n][vocab], or NULL) and their greedy picks argmax_out (host int32 [n],
+ * lowest index on ties, or NULL).  Row i is the model's prediction after
+ * tokens[0..i].  The layer skip mask does not apply. */
+int dls_verify(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, float* logits_out, int32_t* argmax_out);
+
+/* Greedy self-speculative generation of n_tokens tokens from `token` at the
+ * end of `seq` (the same tokens_out as dls_generate with one sequence, and
+ * the sequence grows by n_tokens).  The draft is this model with the layers
+ * draft_skip[l] != 0 skipped (host uint8 [n_layers]; e.g. the streamed
+ * layers, or those dls_layer_cosines finds above a threshold).  Each round:
+ * r = min(draft_k, tokens still wanted - 1) draft decode steps from the
+ * current token t at position P; the sequence cut back to P; one dls_verify
+ * pass of [t, d_1..d_r] through every layer; the longest prefix of drafts the
+ * full model also picks is accepted, and the round emits those drafts plus
+ * the full model's next pick (so the output is the full model's greedy
+ * continuation).  0 <= draft_k < DLS_MAX_VERIFY.  stats (host int32 [3], or
+ * NULL) receives rounds, drafted and accepted token counts.  Draft steps
+ * skip streamed layers' copies when the draft skips every streamed layer.
+ * The mask of dls_set_layer_skip is not used by this call. */
+int dls_generate_speculative(dls_model* m, int32_t seq, int32_t token, int32_t n_tokens, const uint8_t* draft_skip,
+                             int32_t draft_k, int32_t* tokens_out, int32_t* stats);
 
 /* Context-budget check done before any allocation (SwarmKV page, section 4,
  * step 0): DLS_OK if prefix_tokens + max_branch_tokens + headroom <= n_ctx,

@@ -294,12 +294,14 @@ class OracleModel:
              the round emits d_1..d_n and v_n, and the sequence keeps
              positions up to P+n (t, d_1..d_n), continuing with v_n.
 
-        Returns (tokens [n_tokens], stats {rounds, drafted, accepted}).  The
-        tokens are the full model's greedy continuation: a draft token is
-        kept only where the full model picks it too.
+        Returns (tokens [n_tokens], stats {rounds, drafted, accepted,
+        min_gap}).  The tokens are the full model's greedy continuation: a
+        draft token is kept only where the full model picks it too.  min_gap
+        is the smallest top-2 logit gap of any greedy pick made (draft or
+        full), i.e. how far the run is from a tie.
         """
         out = []
-        stats = {"rounds": 0, "drafted": 0, "accepted": 0}
+        stats = {"rounds": 0, "drafted": 0, "accepted": 0, "min_gap": np.inf}
         cur = int(token)
         skip = set(draft_skip)
         while len(out) < n_tokens:
@@ -308,10 +310,14 @@ class OracleModel:
             drafts = []
             t = cur
             for i in range(r):
-                t = ops.greedy(self.decode_step(seq, t, P + i, skip=skip))
+                lg = self.decode_step(seq, t, P + i, skip=skip)
+                stats["min_gap"] = min(stats["min_gap"], ops.top2_gap(lg))
+                t = ops.greedy(lg)
                 drafts.append(t)
             seq.truncate(P)
-            v = [ops.greedy(lg) for lg in self.prefill(seq, [cur] + drafts, all_logits=True)]
+            rows = self.prefill(seq, [cur] + drafts, all_logits=True)
+            stats["min_gap"] = min([stats["min_gap"]] + [ops.top2_gap(lg) for lg in rows])
+            v = [ops.greedy(lg) for lg in rows]
             n = 0
             while n < r and drafts[n] == v[n]:
                 n += 1

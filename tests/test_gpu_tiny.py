@@ -403,6 +403,175 @@ def test_layer_skip_calibration_and_decode(setup, skipped):
         m.seq_free(seq)
 
 
+def test_verify_scores_every_position(setup):
+    """dls_verify: n tokens through every layer at once, every row's logits
+    and greedy pick against the oracle's all-row prefill."""
+    torch = _torch()
+    cfg, w, m, orc, stream = setup
+    prompt = synth.prompt_tokens(cfg, 30, seed=31)
+    seq = m.seq_create()
+    try:
+        m.prefill(seq, prompt[:25])
+        oseq = orc.new_seq()
+        orc.prefill(oseq, prompt[:25])
+        lg = torch.empty(5, cfg.vocab, device="cuda")
+        picks = m.verify(seq, prompt[25:], lg)
+        stream.synchronize()
+        ref = orc.prefill(oseq, prompt[25:], all_logits=True)
+        got = lg.cpu().numpy()
+        for i in range(5):
+            assert_close(got[i], ref[i], f"verify row {i}")
+            check_greedy(got[i], ref[i], f"verify row {i}")
+            assert picks[i] == int(np.argmax(got[i]))
+        assert m.seq_length(seq) == 30
+        # the cache it filled serves the next decode step
+        m.decode_step(seq, 7, 30, lg[0])
+        stream.synchronize()
+        assert_close(lg[0].cpu().numpy(), orc.decode_step(oseq, 7, 30), "decode after verify")
+    finally:
+        m.seq_free(seq)
+
+
+def test_seq_truncate(setup):
+    """Truncation: decoding after a cut equals decoding a sequence that never
+    went further; cutting back into a page shared by a fork gives the
+    sequence a private copy and leaves the other holder's K/V untouched."""
+    torch = _torch()
+    from decode_llama_step_gb300 import dls
+    cfg, w, m, orc, stream = setup
+    free0 = m.kv_free_pages()
+    prompt = synth.prompt_tokens(cfg, 70, seed=41)
+    a, b, c = (m.seq_create() for _ in range(3))
+    try:
+        m.prefill(a, prompt[:40])
+        m.prefill(b, prompt[:40])
+        m.prefill(a, prompt[40:70])                  # a: 70 positions = 3 pages of 32
+        assert free0 - m.kv_free_pages() == 3 + 2
+        m.seq_truncate(a, 40)
+        assert m.seq_length(a) == 40 and free0 - m.kv_free_pages() == 2 + 2
+        la, lb = torch.empty(cfg.vocab, device="cuda"), torch.empty(cfg.vocab, device="cuda")
+        m.decode_step(a, 9, 40, la)
+        m.decode_step(b, 9, 40, lb)
+        stream.synchronize()
+        assert torch.equal(la, lb)
+        with pytest.raises(dls.DlsError) as e:
+            m.seq_truncate(a, 42)
+        assert e.value.code == dls.DLS_ERR_ARG
+        # shared pages: c holds a's first page (positions 0..31) by reference
+        m.kv_fork(a, [c], shared=True)
+        kvd = cfg.n_kv_heads * cfg.head_dim
+
+        def kv(seq, n):
+            k = torch.empty(n, kvd, dtype=torch.float16, device="cuda")
+            v = torch.empty_like(k)
+            m.debug_read_kv(seq, 1, k, v)
+            stream.synchronize()
+            return k.clone(), v.clone()
+
+        before = kv(a, 41)
+        used = free0 - m.kv_free_pages()
+        m.seq_truncate(c, 20)                         # into the shared page: c gets its own copy
+        assert free0 - m.kv_free_pages() == used + 1 - 1   # c's private tail page freed, one copy taken
+        assert torch.equal(kv(c, 20)[0], before[0][:20])
+        m.decode_step(c, 3, 20)                       # writes position 20 of c's copy only
+        after = kv(a, 41)
+        assert torch.equal(after[0], before[0]) and torch.equal(after[1], before[1])
+        oc = orc.new_seq()
+        orc.prefill(oc, prompt[:20])
+        orc.decode_step(oc, 3, 20)
+        m.decode_step(c, 4, 21, lb)
+        stream.synchronize()
+        assert_close(lb.cpu().numpy(), orc.decode_step(oc, 4, 21), "decode after a copy-on-write cut")
+    finally:
+        for q in (a, b, c):
+            m.seq_free(q)
+    assert m.kv_free_pages() == free0
+
+
+def _oracle_seq(orc, prompt):
+    s = orc.new_seq()
+    orc.prefill(s, prompt)
+    return s
+
+
+def _check_speculative(cfg, m, orc, seq, prompt, tok, n, mask, k, what):
+    """Speculative generation through the library against the oracle: the
+    tokens are the oracle's full greedy run up to its first near-tie, and
+    when no greedy pick of the oracle's speculative run (draft or full) is
+    near a tie, the rounds and acceptance counts are the oracle's too."""
+    toks, st = m.generate_speculative(seq, tok, n, mask, k)
+    assert st["rounds"] + st["accepted"] == n and st["accepted"] <= st["drafted"], f"{what}: {st}"
+    otoks, ologits = orc.greedy_decode(_oracle_seq(orc, prompt), tok, n)
+    for i in range(n):
+        if ops.top2_gap(ologits[i]) <= 1e-2:
+            break  # beyond here the runs may legitimately diverge
+        assert toks[i] == otoks[i], f"{what}: step {i}"
+    skip = {l for l in range(cfg.n_layers) if mask[l]}
+    stoks, ost = orc.speculative_decode(_oracle_seq(orc, prompt), tok, n, skip, k)
+    assert stoks == otoks
+    if ost["min_gap"] > 1e-3:
+        assert list(toks) == otoks, f"{what}: tokens"
+        assert (st["rounds"], st["drafted"], st["accepted"]) == \
+            (ost["rounds"], ost["drafted"], ost["accepted"]), f"{what}: {st} vs {ost}"
+    return toks, st
+
+
+@pytest.mark.parametrize("k", [1, 3])
+@pytest.mark.parametrize("draft", ["skip-last", "skip-first", "skip-all", "full"])
+def test_speculative_decode_matches_oracle(setup, draft, k):
+    """Self-speculative greedy decoding (engine page, sections 3.5 and 5.3):
+    the tokens, the rounds and the acceptance counts equal the oracle's, the
+    tokens are the full model's greedy run (the library's own plain greedy
+    generation too), and the sequence ends where plain generation would."""
+    cfg, w, m, orc, stream = setup
+    L = cfg.n_layers
+    mask = {"skip-last": [l == L - 1 for l in range(L)], "skip-first": [l == 0 for l in range(L)],
+            "skip-all": [True] * L, "full": [False] * L}[draft]
+    prompt = synth.prompt_tokens(cfg, 24, seed=51)
+    seq, ref = m.seq_create(), m.seq_create()
+    try:
+        m.prefill(seq, prompt)
+        m.prefill(ref, prompt)
+        tok = int(np.argmax(orc.prefill(orc.new_seq(), prompt)))
+        n = 13
+        toks, st = _check_speculative(cfg, m, orc, seq, prompt, tok, n, mask, k, f"{draft} k={k}")
+        if draft == "full":
+            assert st["accepted"] == st["drafted"]
+        assert m.seq_length(seq) == 24 + n
+        plain = m.generate([ref], [tok], n)[:, 0]
+        _, ologits = orc.greedy_decode(_oracle_seq(orc, prompt), tok, n)
+        for i in range(n):
+            if ops.top2_gap(ologits[i]) <= 1e-2:
+                break
+            assert toks[i] == plain[i], f"step {i}"
+        # one token: a round with no draft
+        one, st1 = m.generate_speculative(seq, int(toks[-1]), 1, mask, k)
+        assert st1 == {"rounds": 1, "drafted": 0, "accepted": 0}
+        assert m.seq_length(seq) == 24 + n + 1
+    finally:
+        m.seq_free(seq)
+        m.seq_free(ref)
+
+
+def test_speculative_decode_with_streamed_layers(setup):
+    """The pages' configuration: resident layers draft, the streamed rest
+    only joins the verify pass (draft steps copy nothing in)."""
+    cfg, w, m, orc, stream = setup
+    L = cfg.n_layers
+    prompt = synth.prompt_tokens(cfg, 24, seed=52)
+    m.set_resident_layers(1)
+    seq = m.seq_create()
+    try:
+        m.prefill(seq, prompt)
+        tok = int(np.argmax(orc.prefill(orc.new_seq(), prompt)))
+        mask = [l >= 1 for l in range(L)]
+        _check_speculative(cfg, m, orc, seq, prompt, tok, 11, mask, 3, "streamed")
+        assert m.seq_length(seq) == 24 + 11
+    finally:
+        m.seq_free(seq)
+        m.set_resident_layers(L)
+
+
 def test_streamed_layers_match_resident(setup):
     torch = _torch()
     cfg, w, m, orc, stream = setup

@@ -565,5 +565,5 @@ def test_speculative_acceptance_matches_brute_force(skip, k):
         rounds += 1
         accepted += a
         drafted += r
-    assert st == {"rounds": rounds, "drafted": drafted, "accepted": accepted}
+    assert (st["rounds"], st["drafted"], st["accepted"]) == (rounds, drafted, accepted)
     assert accepted < drafted       # this draft is wrong somewhere, so rejection is exercised
