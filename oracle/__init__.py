@@ -14,7 +14,9 @@ definition states:
 * ``ops``    - RMSNorm, RoPE, causal GQA attention with softmax, SiLU/SwiGLU,
                fp16 rounding of the KV cache.
 * ``model``  - embedding, the per-layer decode step, final norm, LM head,
-               greedy pick, prefill, and the KV fork.
+               greedy pick, prefill, the KV fork, layer skip and
+               self-speculative decoding.
+* ``kquant`` - Q4_K / Q6_K super-block dequantisation and the dequant-GEMV.
 
 Sources (by page and section): the pure C + CUDA inference engine page (rskf.cn),
 section 1 (the engine implements RoPE, GQA, SwiGLU, RMSNorm and a KV cache for
@@ -33,5 +35,5 @@ T tokens equals T decode steps; a fork equals an independent prefill) and by
 wiring cases with closed forms; there is no external worked example, so the
 full-model composition beyond those is "parity unpinned".
 """
-from . import quant, ops, model  # noqa: F401
+from . import quant, ops, model, kquant  # noqa: F401
 from .model import OracleModel, OracleSeq  # noqa: F401

@@ -1,0 +1,145 @@
+"""Pins for the K-quant oracle (Q4_K, Q6_K super-blocks and the dequant-GEMV).
+
+Blocks are assembled here field by field from the layout the oracle's
+docstring states, by writers that run the opposite way to its readers
+(packing values into bytes rather than unpacking them), so that a swapped
+field, a wrong shift or nibble, or a misplaced index fails.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import kquant as kq
+
+
+def _f16le(v: float) -> list:
+    b = int(np.array([v], dtype=np.float16).view(np.uint16)[0])
+    return [b & 0xFF, b >> 8]
+
+
+def _pack_q4_k(d, dmin, sc, m, q):
+    """One Q4_K super-block from d, dmin, eight (sc, m) pairs and 256 codes."""
+    blk = np.zeros(144, dtype=np.uint8)
+    blk[0:2] = _f16le(d)
+    blk[2:4] = _f16le(dmin)
+    s12 = [0] * 12
+    for s in range(8):
+        if s < 4:
+            s12[s] |= sc[s]
+            s12[s + 4] |= m[s]
+        else:
+            s12[s + 4] = (sc[s] & 15) | ((m[s] & 15) << 4)
+            s12[s - 4] |= (sc[s] >> 4) << 6
+            s12[s] |= (m[s] >> 4) << 6
+    blk[4:16] = s12
+    for i in range(256):
+        g, r = divmod(i, 64)
+        byte = 16 + 32 * g + (r % 32)
+        blk[byte] |= q[i] if r < 32 else q[i] << 4
+    return blk
+
+
+def _pack_q6_k(d, scales, code):
+    """One Q6_K super-block from d, sixteen int8 scales and 256 codes 0..63."""
+    blk = np.zeros(210, dtype=np.uint8)
+    for i in range(256):
+        h, o = divmod(i, 128)
+        g, l = divmod(o, 32)
+        low, high = code[i] & 15, code[i] >> 4
+        at = 64 * h + l + (32 if g % 2 else 0)
+        blk[at] |= low if g < 2 else low << 4
+        blk[128 + 32 * h + l] |= high << (2 * g)
+    blk[192:208] = np.array(scales, dtype=np.int8).view(np.uint8)
+    blk[208:210] = _f16le(d)
+    return blk
+
+
+def test_q4_k_uniform_block_closed_form():
+    for q, a, b in [(0, 0, 0), (15, 63, 0), (7, 1, 63), (15, 63, 63), (3, 40, 17)]:
+        blk = _pack_q4_k(0.5, 0.25, [a] * 8, [b] * 8, [q] * 256)
+        w = kq.dequant_q4_k(blk, 1)[0]
+        assert np.all(w == 0.5 * a * q - 0.25 * b), (q, a, b)
+
+
+def test_q4_k_every_nibble_lands_on_its_weight():
+    # one code of 1 at a time, unit scales, no minimums: exactly one weight is d
+    for i in range(256):
+        q = [0] * 256
+        q[i] = 1
+        w = kq.dequant_q4_k(_pack_q4_k(1.0, 0.0, [1] * 8, [0] * 8, q), 1)[0]
+        assert w[i] == 1.0 and np.count_nonzero(w) == 1, i
+    # and the byte written for weight 64g + 32 + l is the high nibble of byte 32g + l
+    q = [0] * 256
+    q[64 + 32 + 5] = 9
+    blk = _pack_q4_k(1.0, 0.0, [1] * 8, [0] * 8, q)
+    assert blk[16 + 32 + 5] == 9 << 4
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_q4_k_six_bit_scales_and_minimums(seed):
+    rng = np.random.default_rng(seed)
+    sc = [int(v) for v in rng.integers(0, 64, 8)]
+    m = [int(v) for v in rng.integers(0, 64, 8)]
+    sc[5], m[6] = 63, 48                        # top bits set in the split fields
+    blk = _pack_q4_k(1.0, 1.0, sc, m, [1] * 256)
+    got_sc, got_m = kq.q4_k_scales_mins(blk[None, 4:16])
+    assert list(got_sc[0]) == sc and list(got_m[0]) == m
+    w = kq.dequant_q4_k(blk, 1)[0]
+    for s in range(8):
+        assert np.all(w[32 * s: 32 * s + 32] == sc[s] - m[s]), s
+
+
+def test_q6_k_uniform_block_closed_form():
+    for c, a in [(32, 5), (0, 1), (63, -128), (40, 127), (31, -3)]:
+        blk = _pack_q6_k(0.125, [a] * 16, [c] * 256)
+        w = kq.dequant_q6_k(blk, 1)[0]
+        assert np.all(w == 0.125 * a * (c - 32)), (c, a)
+
+
+def test_q6_k_every_code_lands_on_its_weight():
+    # background code 32 (weight 0); one weight at a time gets 33 (low bits)
+    # or 48 (high bits only): exactly that weight is nonzero
+    for bump in (1, 16, 31):
+        for i in range(256):
+            code = [32] * 256
+            code[i] = 32 + bump
+            w = kq.dequant_q6_k(_pack_q6_k(1.0, [1] * 16, code), 1)[0]
+            assert w[i] == float(bump) and np.count_nonzero(w) == 1, (bump, i)
+
+
+def test_q6_k_scale_k_covers_weights_16k_to_16k_plus_15():
+    scales = [int(v) for v in np.random.default_rng(3).integers(-128, 128, 16)]
+    w = kq.dequant_q6_k(_pack_q6_k(2.0, scales, [33] * 256), 1)[0]
+    for i in range(256):
+        assert w[i] == 2.0 * scales[i // 16], i
+
+
+def test_fp16_scales_are_little_endian():
+    blk = _pack_q6_k(1.0, [1] * 16, [33] * 256)
+    blk[208], blk[209] = 0x00, 0xC0            # 0xC000 = -2.0
+    assert np.all(kq.dequant_q6_k(blk, 1)[0] == -2.0)
+    blk = _pack_q4_k(1.0, 0.0, [1] * 8, [0] * 8, [1] * 256)
+    blk[0], blk[1] = 0x00, 0x38                # 0x3800 = 0.5
+    assert np.all(kq.dequant_q4_k(blk, 1)[0] == 0.5)
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q6_k"])
+def test_gemv_exact_against_fractions(fmt):
+    rows, cols = 3, 512
+    b = synth.kquant_matrix(synth.stream_key("kq-pin", fmt), rows, cols, fmt)
+    x = synth.normal(synth.stream_key("kq-pin-x", fmt), cols, 1.0)
+    y = kq.gemv(b, rows, cols, fmt, x, chunk_rows=2)
+    w = kq.matrix_rows(b, cols, fmt, 0, rows)
+    for r in range(rows):
+        exact = sum(Fraction(float(w[r, c])) * Fraction(float(x[c])) for c in range(cols))
+        assert abs(Fraction(float(y[r])) - exact) <= abs(exact) * Fraction(1, 10 ** 12) + Fraction(1, 10 ** 15)
+    # rows come out in order: row r of the matrix is super-blocks r*cols/256 ..
+    one = kq.dequant_blocks(b[(cols // 256) * 144 if fmt == "q4_k" else (cols // 256) * 210:], cols // 256, fmt)
+    assert np.array_equal(one.reshape(-1), w[1])
+
+
+def test_rejects_ragged_columns():
+    with pytest.raises(ValueError):
+        kq.matrix_rows(np.zeros(144, dtype=np.uint8), 300, "q4_k", 0, 1)
