@@ -68,13 +68,15 @@ def parse():
                    help="layer skip workload: skip layers whose calibrated cosine exceeds this")
     p.add_argument("--draft-k", default="1,3,7",
                    help="speculative workload: draft lengths to time (comma-separated)")
-    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip", "spec"], default="decode",
+    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip", "spec", "kquant"],
+                   default="decode",
                    help="decode (default, the headline line); the others are secondary measurements: "
                         "prefill (prompt of --ctx tokens), fork (shared prefix -> 8 branches), "
                         "stream (70B Q4_0 resident vs a 24 GB device budget), "
                         "skip (decode with the layers whose calibrated cosine exceeds --skip-threshold skipped), "
                         "spec (self-speculative greedy decoding vs plain greedy decoding; --config 70b: the 24 GB "
-                        "budget with the resident layers as the draft)")
+                        "budget with the resident layers as the draft), "
+                        "kquant (Q4_K / Q6_K dequant-GEMV on the 70B projection shapes)")
     return p.parse_args()
 
 
@@ -367,6 +369,71 @@ def run_spec(args):
                       "clocks": clk.summary()})
 
 
+KQ_SHAPES_70B = {"wq/wo": (8192, 8192), "wk/wv": (1024, 8192), "w_gate/w_up": (28672, 8192),
+                 "w_down": (8192, 28672)}
+# Q4_K_M's usual type per 70B matrix (the attention value and FFN down
+# projections kept at 6 bits, the rest at 4)
+KQ_Q4_K_M = {"wq": "q4_k", "wk": "q4_k", "wv": "q6_k", "wo": "q4_k", "w_gate": "q4_k", "w_up": "q4_k",
+             "w_down": "q6_k"}
+
+
+def run_kquant(args):
+    """K-quant dequant-GEMV bandwidth on the 70B projection shapes: each
+    (format, shape) timed over --steps launches that cycle through enough
+    copies of the matrix to exceed the L2 several times (every launch reads
+    its weights from HBM)."""
+    import torch
+    import synth
+    from decode_llama_step_gb300 import dls
+    peak, src = peaks()
+    stream = torch.cuda.Stream()
+    L2 = 129 * 2 ** 20
+    res = {}
+    with ClockSampler(0) as clk:
+        for fmt in ("q4_k", "q6_k"):
+            for name, (rows, cols) in KQ_SHAPES_70B.items():
+                blocks = torch.from_numpy(synth.kquant_matrix(synth.stream_key("bench-kq", fmt, name), rows, cols,
+                                                              fmt)).cuda()
+                nbytes = dls.kquant_packed_bytes(fmt, rows, cols)
+                copies = max(2, -(-4 * L2 // nbytes))
+                packed = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(copies)]
+                for p_ in packed:
+                    dls.kquant_pack(fmt, blocks, rows, cols, p_, stream=stream)
+                del blocks
+                x = torch.randn(cols, device="cuda")
+                y = torch.empty(rows, device="cuda")
+                status = torch.zeros(1, dtype=torch.int32, device="cuda")
+                for i in range(max(args.warmup, 3)):
+                    dls.kquant_gemv(fmt, packed[i % copies], rows, cols, x, y, status, stream)
+                n = max(args.steps, copies)
+
+                def go():
+                    for i in range(n):
+                        dls.kquant_gemv(fmt, packed[i % copies], rows, cols, x, y, status, stream)
+                t = _events(torch, stream, go) / n
+                assert int(status.item()) == 0
+                alg = dls.kquant_packed_bytes(fmt, rows, cols) + 4 * (rows + cols)
+                res[f"{fmt} {name} {rows}x{cols}"] = {"us": round(1e6 * t, 2), "bytes": alg,
+                                                      "gbs": round(alg / t / 1e9, 1),
+                                                      "frac": round(alg / t / 1e9 / peak, 4)}
+                del packed
+    layer_us = sum(res[f"{KQ_Q4_K_M[m]} {k} {KQ_SHAPES_70B[k][0]}x{KQ_SHAPES_70B[k][1]}"]["us"]
+                   for k in KQ_SHAPES_70B for m in k.split("/"))
+    layer_bytes = sum(res[f"{KQ_Q4_K_M[m]} {k} {KQ_SHAPES_70B[k][0]}x{KQ_SHAPES_70B[k][1]}"]["bytes"]
+                      for k in KQ_SHAPES_70B for m in k.split("/"))
+    top = res["q4_k w_gate/w_up 28672x8192"]
+    return base_line("Q4_K dequant-GEMV GB/s, 70B gate/up shape (28672 x 8192)", top["gbs"], "GB/s", args.steps,
+                     args.warmup, top["us"] / 1000.0, "70B projection shapes, Q4_K and Q6_K, batch 1, inputs > L2",
+                     {"roofline": {"bound": "hbm", "achieved": top["gbs"], "peak": peak, "unit": "GB/s",
+                                   "frac": top["frac"], "traffic": None, "peak_source": src},
+                      "kquant": res,
+                      "q4_k_m_layer": {"matrices": KQ_Q4_K_M, "gemv_us_sum": round(layer_us, 1),
+                                       "bytes": layer_bytes,
+                                       "gbs": round(layer_bytes / (layer_us * 1e-6) / 1e9, 1),
+                                       "how": "sum of the seven matrices' measured GEMV times"},
+                      "clocks": clk.summary()})
+
+
 def h2d_peak(torch, chunk=256 << 20, inflight=4, reps=10):
     """Best pinned host -> device copy rate: 256 MB chunks, several in flight."""
     host = torch.empty(chunk * inflight, dtype=torch.uint8, pin_memory=True)
@@ -559,7 +626,7 @@ def main():
         if int(os.environ.get("RANK", "0")) != 0:
             return 0
         fn = {"prefill": run_prefill, "fork": run_fork, "stream": run_stream, "skip": run_skip,
-              "spec": run_spec}[args.workload]
+              "spec": run_spec, "kquant": run_kquant}[args.workload]
         print(json.dumps(fn(args)), flush=True)
         return 0
 

@@ -192,6 +192,30 @@ cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, c
 // the small-batch form (T <= 8): raw codes as exact fp16 operands, block
 // scales applied per 32-column block from tensor memory (gemm_small.cu)
 cudaError_t sgemm_setup_attributes();
+
+// ---- K-quant dequant-GEMV (Q4_K, Q6_K; kquant.cu) ------------------------------
+enum KqFormat { KQ_Q4_K = 12, KQ_Q6_K = 14 };  // the GGUF type ids
+
+struct KqArgs {
+  const uint8_t* w;   // packed super-blocks (Q4_K 144 bytes, Q6_K 208 bytes each), row-major
+  const __half* d6;   // Q6_K: super-block scales [rows][nsb rounded up to 8]; unused for Q4_K
+  int rows, cols;     // cols a multiple of 256
+  const float* x;     // [cols], 16-byte aligned
+  float* y;           // [rows]
+  int* status;        // kTimeout is or-ed in when a bounded wait runs out (may be NULL)
+};
+
+struct KqLaunch {
+  int grid, threads, smem;
+  int nwc, rs, ns, mc;  // consumer warps, rows per ring stage, stages, units per lane
+};
+
+size_t kq_packed_bytes(int fmt, int rows, int cols);
+const __half* kq_d6(const void* packed, int rows, int cols);
+cudaError_t launch_kq_pack(int fmt, const void* blocks, int rows, int cols, void* packed, cudaStream_t s);
+KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms);  // grid 0: unsupported shape
+cudaError_t kq_setup_attributes();
+cudaError_t launch_kq_gemv(int fmt, const KqArgs& a, const KqLaunch& l, cudaStream_t s);
 cudaError_t launch_sgemm(int wtype, int epi, const PgArgs& a, int split, cudaStream_t s);
 cudaError_t prefill_setup_attributes();
 cudaError_t launch_embed_rows(const MatDev& emb, int wtype, const int32_t* tokens, int T, int vocab, float* x, int ldx,

@@ -1,0 +1,522 @@
+// Batch-1 dequant-GEMV y = W x for K-quant weights (Q4_K, Q6_K): the
+// projection of a decode step on the GGUF K-quant files the engine page runs
+// its 70B model from (section 1: Q4_K_M and Q6_K among its formats).
+//
+// Device layout ("packed"), 16-byte aligned throughout so that whole rows
+// move with 1-D bulk async copies:
+//  * Q4_K: the GGUF super-block as it is, 144 bytes = 16 bytes of scales
+//    (d, dmin, twelve bytes of 6-bit sub-block scales and minimums) + 128
+//    bytes of 4-bit codes; a row is cols/256 consecutive super-blocks.
+//  * Q6_K: the first 208 bytes of each GGUF super-block (low code bits, high
+//    code bits, sixteen int8 scales) row-major, then a separate fp16 array of
+//    the super-block scales d, [rows][nsb rounded up to 8].
+//
+// Same HBM-bound scheme as the Q8_0 / Q4_0 GEMV: one CTA per SM (two where
+// registers allow) owns a contiguous row range; a producer warp streams its
+// rows through a shared-memory ring with cp.async.bulk and mbarriers; each
+// consumer lane owns a fixed slice of the columns ("unit"), holds that slice
+// of x as int16 with one scale in registers, and takes exact int32 dot
+// products of codes and activations (dp2a) per row.
+//  * Q4_K unit: 16 code bytes = 32 weights, the low nibbles of sub-block 2g
+//    and the high nibbles of sub-block 2g+1; eight units per super-block.
+//    y += xs * (d * (sc_a I_a + sc_b I_b) - dmin * (m_a S_a + m_b S_b)), with
+//    I the integer code-activation dots and S the sums of the int16 slice.
+//  * Q6_K unit: 48 code bytes = 64 weights in four groups of 16, each group
+//    with its int8 scale; y += xs * d * sum_g sc_g (I_g - 32 S_g).
+#include <stdlib.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/dls.h"
+#include "gemv_core.cuh"
+#include "kernels.h"
+
+namespace dls {
+
+namespace {
+
+constexpr int kMaxWarps = 8;   // consumer warps: cols up to 32768 at most 4 (Q4_K) or 2 (Q6_K) units per lane
+constexpr int kRB = 64;              // rows per reduction block
+constexpr int kStageBytes = 16384;   // target code bytes per ring stage
+constexpr int kRing = 64 * 1024;
+
+struct KqShared {
+  uint64_t full[16];
+  uint64_t empty[16];
+  int abort;
+};
+
+template <int FMT>
+struct KqGeo {
+  static constexpr int UPB = FMT == KQ_Q4_K ? 8 : 4;        // units per super-block
+  static constexpr int NP = FMT == KQ_Q4_K ? 16 : 32;       // int16 pairs per unit
+  static constexpr int NG = FMT == KQ_Q4_K ? 2 : 4;         // scale groups per unit
+  static constexpr int SB = FMT == KQ_Q4_K ? 144 : 208;     // packed super-block bytes
+  static constexpr int MCMAX = FMT == KQ_Q4_K ? 4 : 2;      // units per lane (registers)
+};
+
+template <int FMT>
+struct KqX {
+  uint32_t p[KqGeo<FMT>::NP];   // int16 pairs: element 2e in the low half of p[e]
+  int sum[KqGeo<FMT>::NG];      // per scale group: sum of the int16 values
+  float s;                      // x_i ~= s * X_i
+};
+
+// Byte i (0..15) of a 16-byte vector.
+__device__ __forceinline__ uint32_t byte_of(const uint4& v, int i) {
+  const uint32_t w = i < 4 ? v.x : i < 8 ? v.y : i < 12 ? v.z : v.w;
+  return (w >> (8 * (i & 3))) & 0xFFu;
+}
+
+// The element offsets (within the row) of one unit's groups of 16.
+template <int FMT>
+__device__ __forceinline__ int group_col(int unit, int g) {
+  if (FMT == KQ_Q4_K) {
+    const int sb = unit >> 3, v = unit & 7, gg = v >> 1, l0 = (v & 1) * 16;
+    return sb * 256 + 64 * gg + 32 * g + l0;        // g = 0: low nibbles, g = 1: high nibbles
+  } else {
+    const int sb = unit >> 2, v = unit & 3, h = v >> 1, l0 = (v & 1) * 16;
+    return sb * 256 + 128 * h + 32 * g + l0;
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ void load_unit_x(const float* x, int unit, bool valid, KqX<FMT>& xq) {
+  constexpr int NG = KqGeo<FMT>::NG;
+  float v[NG * 16];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const int c0 = valid ? group_col<FMT>(unit, g) : 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float4 f = *reinterpret_cast<const float4*>(x + c0 + 4 * j);
+      if (!valid) f = make_float4(0.f, 0.f, 0.f, 0.f);
+      v[g * 16 + 4 * j] = f.x;
+      v[g * 16 + 4 * j + 1] = f.y;
+      v[g * 16 + 4 * j + 2] = f.z;
+      v[g * 16 + 4 * j + 3] = f.w;
+    }
+  }
+  float mx = 0.f;
+#pragma unroll
+  for (int i = 0; i < NG * 16; ++i) mx = fmaxf(mx, fabsf(v[i]));
+  const float s = mx > 0.f ? mx / 32767.0f : 1.0f;
+  const float inv = 1.0f / s;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int a = __float2int_rn(v[g * 16 + 2 * e] * inv), b = __float2int_rn(v[g * 16 + 2 * e + 1] * inv);
+      sum += a + b;
+      xq.p[g * 8 + e] = (uint32_t)(a & 0xFFFF) | ((uint32_t)b << 16);
+    }
+    xq.sum[g] = sum;
+  }
+  xq.s = s;
+}
+
+// 16 unsigned code bytes (one per element, 4 words) against 8 int16 pairs.
+__device__ __forceinline__ int dot16(const uint32_t (&c)[4], const uint32_t* p) {
+  int s0 = 0, s1 = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    s0 = dp2a_lo(p[2 * k], c[k], s0);
+    s1 = dp2a_hi(p[2 * k + 1], c[k], s1);
+  }
+  return s0 + s1;
+}
+
+// One Q4_K unit of one row: codes at qa (16 bytes), super-block scales at ma.
+__device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, int lane, const KqX<KQ_Q4_K>& xq) {
+  const uint4 q = lds128(qa);
+  const uint4 m = lds128(ma);
+  const float d = __half2float(__ushort_as_half((unsigned short)(m.x & 0xFFFF)));
+  const float dmin = __half2float(__ushort_as_half((unsigned short)(m.x >> 16)));
+  const uint4 sb = make_uint4(m.y, m.z, m.w, 0u);   // the twelve scale bytes
+  const int g = (lane & 7) >> 1;                     // this lane's 64-weight group
+  float sc[2], mn[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int s = 2 * g + h;
+    uint32_t a, b;
+    if (s < 4) {
+      a = byte_of(sb, s) & 63u;
+      b = byte_of(sb, s + 4) & 63u;
+    } else {
+      const uint32_t hi = byte_of(sb, s + 4);
+      a = (hi & 15u) | ((byte_of(sb, s - 4) >> 6) << 4);
+      b = (hi >> 4) | ((byte_of(sb, s) >> 6) << 4);
+    }
+    sc[h] = (float)a;
+    mn[h] = (float)b;
+  }
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    lo[k] = w[k] & 0x0F0F0F0Fu;
+    hi[k] = (w[k] >> 4) & 0x0F0F0F0Fu;
+  }
+  const float ia = (float)dot16(lo, xq.p), ib = (float)dot16(hi, xq.p + 8);
+  return xq.s * (d * fmaf(sc[0], ia, sc[1] * ib) - dmin * fmaf(mn[0], (float)xq.sum[0], mn[1] * (float)xq.sum[1]));
+}
+
+// One Q6_K unit of one row: ql halves at aa / ba, qh at ha, scales at sa.
+__device__ __forceinline__ float unit_q6_k(uint32_t aa, uint32_t ba, uint32_t ha, uint32_t sa, float d, int lane,
+                                           const KqX<KQ_Q6_K>& xq) {
+  const uint4 A = lds128(aa), B = lds128(ba), Q = lds128(ha), S = lds128(sa);
+  const uint32_t a[4] = {A.x, A.y, A.z, A.w}, b[4] = {B.x, B.y, B.z, B.w}, qh[4] = {Q.x, Q.y, Q.z, Q.w};
+  const int base = 8 * ((lane & 3) >> 1) + (lane & 1);   // scale of group 0 (8h + l0/16)
+  float acc = 0.f;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint32_t c[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t src = (g & 1) ? b[k] : a[k];
+      const uint32_t low = (g < 2 ? src : src >> 4) & 0x0F0F0F0Fu;
+      const uint32_t high = (qh[k] >> (2 * g)) & 0x03030303u;
+      c[k] = low | (high << 4);
+    }
+    const int ig = dot16(c, xq.p + 8 * g) - 32 * xq.sum[g];
+    const float scg = (float)(int)(int8_t)byte_of(S, base + 2 * g);
+    acc = fmaf(scg, (float)ig, acc);
+  }
+  return xq.s * d * acc;
+}
+
+template <int FMT, int RS, int MC>
+__global__ void __launch_bounds__(32 * (kMaxWarps + 1)) kq_gemv_kernel(const KqArgs a, const KqLaunch L) {
+  using G = KqGeo<FMT>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  KqShared& sh = *reinterpret_cast<KqShared*>(smem_raw);
+  float* s_part = reinterpret_cast<float*>(smem_raw + sizeof(KqShared));   // [nwc][kRB]
+  uint8_t* ring = smem_raw + ((sizeof(KqShared) + L.nwc * kRB * 4 + 127) & ~127);
+  const int nsb = a.cols / 256;
+  const int nsb_pad = (nsb + 7) & ~7;
+  const int nwc = L.nwc, NS = L.ns;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t row_bytes = (uint32_t)nsb * G::SB;
+  const uint32_t drow_bytes = FMT == KQ_Q6_K ? (uint32_t)nsb_pad * 2 : 0;
+  const uint32_t stage_q = RS * row_bytes;
+  const uint32_t stage_bytes = stage_q + RS * drow_bytes;
+  const int r0 = (int)((long long)a.rows * blockIdx.x / gridDim.x);
+  const int r1 = (int)((long long)a.rows * (blockIdx.x + 1) / gridDim.x);
+  const int nrows = max(r1 - r0, 0);
+  const int nst = (nrows + RS - 1) / RS;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&sh.full[s]), 1);
+      mbar_init(smem_u32(&sh.empty[s]), nwc);
+    }
+    sh.abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == nwc) {
+    // ---------------- producer: this CTA's rows through the ring
+    if (lane == 0) {
+      int issued = 0;
+      for (int s = 0; s < nst; ++s) {
+        const int slot = s % NS;
+        if (s >= NS && !mbar_wait(smem_u32(&sh.empty[slot]), ((s / NS) - 1) & 1)) {
+          if (a.status) atomicOr(a.status, kTimeout);
+          sh.abort = 1;
+          break;
+        }
+        const int rows_s = min(RS, nrows - s * RS);
+        const int row = r0 + s * RS;
+        uint8_t* dst = ring + (size_t)slot * stage_bytes;
+        const uint32_t qb = rows_s * row_bytes, db = rows_s * drow_bytes;
+        const uint32_t bar = smem_u32(&sh.full[slot]);
+        mbar_expect_tx(bar, qb + db);
+        bulk_g2s(smem_u32(dst), a.w + (size_t)row * row_bytes, qb, bar);
+        if (FMT == KQ_Q6_K)
+          bulk_g2s(smem_u32(dst + stage_q), reinterpret_cast<const uint8_t*>(a.d6) + (size_t)row * drow_bytes, db, bar);
+        ++issued;
+      }
+      // never leave with copies in flight
+      for (int s = max(0, issued - NS); s < issued; ++s) mbar_wait(smem_u32(&sh.full[s % NS]), (s / NS) & 1);
+    }
+  } else {
+    // ---------------- consumers
+    const int nunits = nsb * G::UPB;
+    KqX<FMT> xq[MC];
+    bool valid[MC];
+    int ubase[MC];
+#pragma unroll
+    for (int k = 0; k < MC; ++k) {
+      const int unit = (warp + k * nwc) * 32 + lane;
+      valid[k] = unit < nunits;
+      ubase[k] = valid[k] ? unit : 0;
+      load_unit_x<FMT>(a.x, ubase[k], valid[k], xq[k]);
+    }
+    const int stages_per_block = kRB / RS;
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % NS;
+      if (!sh.abort && !mbar_wait(smem_u32(&sh.full[slot]), (s / NS) & 1)) {
+        if (a.status) atomicOr(a.status, kTimeout);
+        sh.abort = 1;
+      }
+      const int rows_s = min(RS, nrows - s * RS);
+      const uint32_t st = smem_u32(ring) + (uint32_t)slot * stage_bytes;
+      float acc[RS];
+#pragma unroll
+      for (int rr = 0; rr < RS; ++rr) acc[rr] = 0.f;
+      if (!sh.abort) {
+#pragma unroll
+        for (int k = 0; k < MC; ++k) {
+          const int unit = ubase[k];
+#pragma unroll
+          for (int rr = 0; rr < RS; ++rr) {
+            const uint32_t rowa = st + rr * row_bytes;
+            float t;
+            if constexpr (FMT == KQ_Q4_K) {
+              const int sb = unit >> 3, v = unit & 7;
+              const uint32_t blk = rowa + (uint32_t)sb * 144;
+              t = unit_q4_k(blk + 16 + 32 * (v >> 1) + 16 * (v & 1), blk, lane, xq[k]);
+            } else {
+              const int sb = unit >> 2, v = unit & 3, h = v >> 1, l0 = (v & 1) * 16;
+              const uint32_t blk = rowa + (uint32_t)sb * 208;
+              const float d = lds_half_as_float(st + stage_q + rr * drow_bytes + sb * 2);
+              t = unit_q6_k(blk + 64 * h + l0, blk + 64 * h + 32 + l0, blk + 128 + 32 * h + l0, blk + 192, d, lane,
+                            xq[k]);
+            }
+            acc[rr] = valid[k] ? acc[rr] + t : acc[rr];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.empty[slot]));
+      const float t = butterfly<RS>(acc, lane);
+      const int rr = RS == 1 ? 0 : (lane >> (5 - (RS == 2 ? 1 : RS == 4 ? 2 : 3)));
+      const int lrow = s * RS + rr - (s / stages_per_block) * kRB;
+      if ((lane & ((32 / RS) - 1)) == 0 && rr < rows_s) s_part[warp * kRB + lrow] = t;
+      if ((s + 1) % stages_per_block == 0 || s == nst - 1) {
+        named_bar(1, nwc * 32);
+        const int b0 = r0 + (s / stages_per_block) * kRB;
+        const int bn = min(kRB, r1 - b0);
+        for (int lr = tid; lr < bn; lr += nwc * 32) {
+          float v = 0.f;
+          for (int ww = 0; ww < nwc; ++ww) v += s_part[ww * kRB + lr];   // fixed order
+          a.y[b0 + lr] = v;
+        }
+        named_bar(1, nwc * 32);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+using KqFn = void (*)(const KqArgs, const KqLaunch);
+
+template <int FMT, int MC>
+KqFn kq_pick_rs(int rs) {
+  switch (rs) {
+    case 1: return &kq_gemv_kernel<FMT, 1, MC>;
+    case 2: return &kq_gemv_kernel<FMT, 2, MC>;
+    case 4: return &kq_gemv_kernel<FMT, 4, MC>;
+    case 8: return &kq_gemv_kernel<FMT, 8, MC>;
+  }
+  return nullptr;
+}
+
+KqFn kq_pick(int fmt, int rs, int mc) {
+  if (fmt == KQ_Q4_K) {
+    if (mc <= 1) return kq_pick_rs<KQ_Q4_K, 1>(rs);
+    if (mc <= 2) return kq_pick_rs<KQ_Q4_K, 2>(rs);
+    if (mc <= 4) return kq_pick_rs<KQ_Q4_K, 4>(rs);
+  } else if (fmt == KQ_Q6_K) {
+    if (mc <= 1) return kq_pick_rs<KQ_Q6_K, 1>(rs);
+    if (mc <= 2) return kq_pick_rs<KQ_Q6_K, 2>(rs);
+  }
+  return nullptr;
+}
+
+// Q6_K GGUF super-blocks (210 bytes, not 16-byte aligned) -> the packed
+// layout: one thread per 32-bit word of the 208-byte part, one per d.
+__global__ void kq_pack_q6_k_kernel(const uint8_t* src, int rows, int nsb, uint8_t* dst, __half* d6) {
+  const int nsb_pad = (nsb + 7) & ~7;
+  const long long words = (long long)rows * nsb * 52;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < words;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long blk = i / 52;
+    const int w = (int)(i % 52);
+    const uint8_t* s = src + blk * 210 + 4 * w;
+    const uint32_t v = (uint32_t)s[0] | ((uint32_t)s[1] << 8) | ((uint32_t)s[2] << 16) | ((uint32_t)s[3] << 24);
+    reinterpret_cast<uint32_t*>(dst)[i] = v;
+    if (w == 0) {
+      const long long r = blk / nsb, sb = blk % nsb;
+      const uint8_t* dp = src + blk * 210 + 208;
+      d6[r * nsb_pad + sb] = __ushort_as_half((unsigned short)(dp[0] | (dp[1] << 8)));
+    }
+  }
+}
+
+}  // namespace
+
+size_t kq_packed_bytes(int fmt, int rows, int cols) {
+  const size_t nsb = (size_t)cols / 256, nsb_pad = (nsb + 7) & ~(size_t)7;
+  if (fmt == KQ_Q4_K) return (size_t)rows * nsb * 144;
+  const size_t main = ((size_t)rows * nsb * 208 + 255) & ~(size_t)255;
+  return main + (size_t)rows * nsb_pad * 2;
+}
+
+const __half* kq_d6(const void* packed, int rows, int cols) {
+  const size_t nsb = (size_t)cols / 256;
+  const size_t main = ((size_t)rows * nsb * 208 + 255) & ~(size_t)255;
+  return reinterpret_cast<const __half*>(static_cast<const uint8_t*>(packed) + main);
+}
+
+cudaError_t launch_kq_pack(int fmt, const void* blocks, int rows, int cols, void* packed, cudaStream_t s) {
+  if (fmt == KQ_Q4_K)
+    return cudaMemcpyAsync(packed, blocks, kq_packed_bytes(fmt, rows, cols), cudaMemcpyDeviceToDevice, s);
+  const int nsb = cols / 256;
+  uint8_t* dst = static_cast<uint8_t*>(packed);
+  __half* d6 = const_cast<__half*>(kq_d6(packed, rows, cols));
+  const size_t nsb_pad = ((size_t)nsb + 7) & ~(size_t)7;
+  cudaError_t e = cudaMemsetAsync(d6, 0, (size_t)rows * nsb_pad * 2, s);
+  if (e != cudaSuccess) return e;
+  const long long words = (long long)rows * nsb * 52;
+  const int grid = (int)std::min<long long>((words + 255) / 256, 65535);
+  kq_pack_q6_k_kernel<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(blocks), rows, nsb, dst, d6);
+  return cudaGetLastError();
+}
+
+KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms) {
+  KqLaunch l{};
+  if ((fmt != KQ_Q4_K && fmt != KQ_Q6_K) || cols % 256 || cols <= 0 || rows <= 0) return l;
+  const int nsb = cols / 256;
+  const int upb = fmt == KQ_Q4_K ? 8 : 4, mcmax = fmt == KQ_Q4_K ? 4 : 2;
+  const int nchunk = (nsb * upb + 31) / 32;
+  int nwc = 0;
+  for (int d = 1; d <= 8; ++d)
+    if (nchunk % d == 0 && nchunk / d <= mcmax) nwc = d;
+  if (!nwc) nwc = std::min(kMaxWarps, (nchunk + mcmax - 1) / mcmax);
+  const int mc = (nchunk + nwc - 1) / nwc;
+  if (mc > mcmax) return l;
+  const int row_bytes = nsb * (fmt == KQ_Q4_K ? 144 : 208);
+  const int drow = fmt == KQ_Q6_K ? ((nsb + 7) & ~7) * 2 : 0;
+  int rs = 1;
+  while (rs < 8 && (rs * 2) * row_bytes <= kStageBytes) rs *= 2;
+  const int stage = rs * (row_bytes + drow);
+  const int ns = std::max(2, std::min(16, kRing / stage));
+  l.nwc = nwc;
+  l.mc = mc;
+  l.rs = rs;
+  l.ns = ns;
+  l.threads = 32 * (nwc + 1);
+  l.smem = (int)((sizeof(KqShared) + nwc * kRB * 4 + 127) & ~127) + ns * stage;
+  if (l.smem > 200 * 1024) return KqLaunch{};
+  int occ = 1;
+  KqFn f = kq_pick(fmt, rs, mc);
+  if (!f) return KqLaunch{};
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, l.threads, l.smem) != cudaSuccess) {
+    cudaGetLastError();
+    occ = 1;
+  }
+  occ = std::max(1, std::min(2, occ));
+  l.grid = std::max(1, std::min(num_sms * occ, rows));
+  return l;
+}
+
+cudaError_t kq_setup_attributes() {
+  for (int fmt : {(int)KQ_Q4_K, (int)KQ_Q6_K})
+    for (int rs : {1, 2, 4, 8})
+      for (int mc : {1, 2, 4}) {
+        KqFn f = kq_pick(fmt, rs, mc);
+        if (!f) continue;
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+      }
+  return cudaSuccess;
+}
+
+cudaError_t launch_kq_gemv(int fmt, const KqArgs& a, const KqLaunch& l, cudaStream_t s) {
+  KqFn f = kq_pick(fmt, l.rs, l.mc);
+  if (!f || l.grid < 1 || l.ns > 16 || l.nwc < 1 || l.nwc > kMaxWarps || a.cols % 256 || !a.w || !a.x || !a.y ||
+      (fmt == KQ_Q6_K && !a.d6))
+    return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.w) | reinterpret_cast<uintptr_t>(a.d6) | reinterpret_cast<uintptr_t>(a.x)) & 15)
+    return cudaErrorInvalidValue;
+  f<<<l.grid, l.threads, l.smem, s>>>(a, l);
+  return cudaGetLastError();
+}
+
+}  // namespace dls
+
+// ---- C ABI ------------------------------------------------------------------------
+
+namespace {
+
+bool kq_type_ok(int32_t type) { return type == DLS_Q4_K || type == DLS_Q6_K; }
+
+std::mutex g_kq_mu;
+std::map<std::tuple<int, int, int, int>, dls::KqLaunch> g_kq_plans;  // (device, type, rows, cols)
+bool g_kq_attr[64] = {};
+
+// The launch plan of one shape on the current device (cached), with the
+// kernels' shared-memory limit raised once per device.
+int kq_launch_for(int32_t type, int32_t rows, int32_t cols, dls::KqLaunch* out) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
+    return dls::report_error(DLS_ERR_CUDA, "kquant: no current device");
+  std::lock_guard<std::mutex> g(g_kq_mu);
+  if (dev >= 0 && dev < 64 && !g_kq_attr[dev]) {
+    if (dls::kq_setup_attributes() != cudaSuccess) return dls::report_error(DLS_ERR_CUDA, "kquant: attributes");
+    g_kq_attr[dev] = true;
+  }
+  const auto key = std::make_tuple(dev, (int)type, (int)rows, (int)cols);
+  auto it = g_kq_plans.find(key);
+  if (it == g_kq_plans.end()) it = g_kq_plans.emplace(key, dls::kq_plan(type, rows, cols, sms)).first;
+  if (it->second.grid < 1)
+    return dls::report_error(DLS_ERR_ARG, "kquant: unsupported shape type=%d rows=%d cols=%d", type, rows, cols);
+  *out = it->second;
+  return DLS_OK;
+}
+
+}  // namespace
+
+extern "C" uint64_t dls_kquant_packed_bytes(int32_t type, int32_t rows, int32_t cols) {
+  if (!kq_type_ok(type) || rows < 1 || cols < 256 || cols % 256) return 0;
+  return dls::kq_packed_bytes(type, rows, cols);
+}
+
+extern "C" int dls_kquant_pack(int32_t type, const void* blocks, int32_t rows, int32_t cols, void* packed,
+                               void* cuda_stream) {
+  if (!kq_type_ok(type) || rows < 1 || cols < 256 || cols % 256 || !blocks || !packed)
+    return dls::report_error(DLS_ERR_ARG, "kquant pack: type=%d rows=%d cols=%d", type, rows, cols);
+  if (reinterpret_cast<uintptr_t>(packed) & 255)
+    return dls::report_error(DLS_ERR_ARG, "kquant pack: the packed buffer must be 256-byte aligned");
+  const cudaError_t e = dls::launch_kq_pack(type, blocks, rows, cols, packed, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return dls::report_error(DLS_ERR_CUDA, "kquant pack: cuda=%s", cudaGetErrorString(e));
+  return DLS_OK;
+}
+
+extern "C" int dls_kquant_gemv(int32_t type, const void* packed, int32_t rows, int32_t cols, const float* x,
+                               float* y, int32_t* status, void* cuda_stream) {
+  if (!kq_type_ok(type) || rows < 1 || cols < 256 || cols % 256 || !packed || !x || !y)
+    return dls::report_error(DLS_ERR_ARG, "kquant gemv: type=%d rows=%d cols=%d", type, rows, cols);
+  if ((reinterpret_cast<uintptr_t>(packed) & 255) || (reinterpret_cast<uintptr_t>(x) & 15))
+    return dls::report_error(DLS_ERR_ARG, "kquant gemv: packed must be 256-byte and x 16-byte aligned");
+  dls::KqLaunch l;
+  const int r = kq_launch_for(type, rows, cols, &l);
+  if (r != DLS_OK) return r;
+  dls::KqArgs a{};
+  a.w = static_cast<const uint8_t*>(packed);
+  a.d6 = type == DLS_Q6_K ? dls::kq_d6(packed, rows, cols) : nullptr;
+  a.rows = rows;
+  a.cols = cols;
+  a.x = x;
+  a.y = y;
+  a.status = status;
+  const cudaError_t e = dls::launch_kq_gemv(type, a, l, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return dls::report_error(DLS_ERR_CUDA, "kquant gemv: cuda=%s", cudaGetErrorString(e));
+  return DLS_OK;
+}

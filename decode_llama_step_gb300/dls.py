@@ -81,6 +81,9 @@ _SIGS = {
     "dls_attention_decode": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, sz, i32, i32, i32, i32, i32, i32, i32, vp]),
     "dls_attention_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
     "dls_attention_decode_noalloc": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]),
+    "dls_kquant_packed_bytes": (ctypes.c_uint64, [i32, i32, i32]),
+    "dls_kquant_pack": (ctypes.c_int, [i32, vp, i32, i32, vp, vp]),
+    "dls_kquant_gemv": (ctypes.c_int, [i32, vp, i32, i32, vp, vp, vp, vp]),
     "dls_debug_capture": (ctypes.c_int, [vp, vp]),
     "dls_debug_read_kv": (ctypes.c_int, [vp, i32, i32, vp, vp]),
     "dls_debug_dequant": (ctypes.c_int, [vp, i32, i32, vp]),
@@ -173,6 +176,26 @@ def attention_decode_noalloc(q, k_pages, v_pages, page_table, lengths, o, n_batc
     _check(load().dls_attention_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
                                                _ptr(lengths), _ptr(o), n_batch, n_heads, n_kv_heads, head_dim,
                                                page_tokens, max_pages, n_splits, _stream_handle(stream)))
+
+
+DLS_Q4_K = 12
+DLS_Q6_K = 14
+KQUANT_TYPES = {"q4_k": DLS_Q4_K, "q6_k": DLS_Q6_K}
+
+
+def kquant_packed_bytes(fmt: str, rows: int, cols: int) -> int:
+    return int(load().dls_kquant_packed_bytes(KQUANT_TYPES[fmt], rows, cols))
+
+
+def kquant_pack(fmt: str, blocks, rows: int, cols: int, packed, stream=None):
+    """GGUF K-quant super-blocks (device) -> the GEMV's device layout."""
+    _check(load().dls_kquant_pack(KQUANT_TYPES[fmt], _ptr(blocks), rows, cols, _ptr(packed), _stream_handle(stream)))
+
+
+def kquant_gemv(fmt: str, packed, rows: int, cols: int, x, y, status=None, stream=None):
+    """y = W x on a packed K-quant matrix (device buffers)."""
+    _check(load().dls_kquant_gemv(KQUANT_TYPES[fmt], _ptr(packed), rows, cols, _ptr(x), _ptr(y), _ptr(status),
+                                  _stream_handle(stream)))
 
 
 def _stream_handle(stream):

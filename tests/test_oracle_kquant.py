@@ -143,3 +143,38 @@ def test_gemv_exact_against_fractions(fmt):
 def test_rejects_ragged_columns():
     with pytest.raises(ValueError):
         kq.matrix_rows(np.zeros(144, dtype=np.uint8), 300, "q4_k", 0, 1)
+
+
+# Plausible mistakes, planted in a copy of the oracle on the CPU: each must
+# make at least one of the pins above fail.
+_MUTANTS = [
+    ("((b[:, s] >> 6) << 4)", "((b[:, s - 4] >> 6) << 4)"),                       # minimum's top bits from the wrong byte
+    ("qs[:, 32 * g: 32 * g + 32] >> 4", "qs[:, 32 * g: 32 * g + 32] & 0x0F"),     # high nibble read as low
+    (">> (2 * g)) & 3", ">> (2 * (g ^ 1))) & 3"),                                 # Q6_K high bits of the wrong group
+    ("np.arange(QK) // 16]", "np.arange(QK) // 16 ^ 1]"),                         # neighbouring Q6_K scale
+    ("low = src & 0x0F if g < 2 else src >> 4", "low = src & 0x0F if g % 2 == 0 else src >> 4"),
+    ("- dmin[:, None] * m[:, sub]", "+ dmin[:, None] * m[:, sub]"),               # minimum's sign
+]
+
+
+@pytest.mark.parametrize("old,new", _MUTANTS)
+def test_pins_catch_planted_mistakes(old, new, monkeypatch):
+    import importlib.util
+    import sys
+    src = open(kq.__file__).read()
+    assert src.count(old) == 1, old
+    spec = importlib.util.spec_from_loader("kquant_mutant", loader=None)
+    mutant = importlib.util.module_from_spec(spec)
+    exec(compile(src.replace(old, new), "kquant_mutant", "exec"), mutant.__dict__)
+    monkeypatch.setitem(sys.modules, "kquant_mutant", mutant)
+    monkeypatch.setattr(sys.modules[__name__], "kq", mutant)
+    pins = [test_q4_k_uniform_block_closed_form, test_q4_k_every_nibble_lands_on_its_weight,
+            lambda: test_q4_k_six_bit_scales_and_minimums(0), test_q6_k_uniform_block_closed_form,
+            test_q6_k_every_code_lands_on_its_weight, test_q6_k_scale_k_covers_weights_16k_to_16k_plus_15]
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1
