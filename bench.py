@@ -66,6 +66,8 @@ def parse():
                    help="keep only the first N layers (small cases for ncu captures; not a bench result)")
     p.add_argument("--skip-threshold", type=float, default=0.98,
                    help="layer skip workload: skip layers whose calibrated cosine exceeds this")
+    p.add_argument("--kq-only", default="",
+                   help="kquant workload: only this format and shape, e.g. q4_k:28672x8192 (small ncu captures)")
     p.add_argument("--draft-k", default="1,3,7",
                    help="speculative workload: draft lengths to time (comma-separated)")
     p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip", "spec", "kquant"],
@@ -392,6 +394,8 @@ def run_kquant(args):
     with ClockSampler(0) as clk:
         for fmt in ("q4_k", "q6_k"):
             for name, (rows, cols) in KQ_SHAPES_70B.items():
+                if args.kq_only and args.kq_only != f"{fmt}:{rows}x{cols}":
+                    continue
                 blocks = torch.from_numpy(synth.kquant_matrix(synth.stream_key("bench-kq", fmt, name), rows, cols,
                                                               fmt)).cuda()
                 nbytes = dls.kquant_packed_bytes(fmt, rows, cols)
@@ -417,6 +421,10 @@ def run_kquant(args):
                                                       "gbs": round(alg / t / 1e9, 1),
                                                       "frac": round(alg / t / 1e9 / peak, 4)}
                 del packed
+    if args.kq_only:
+        (key, r), = res.items()
+        return base_line(f"{key} dequant-GEMV GB/s", r["gbs"], "GB/s", args.steps, args.warmup, r["us"] / 1000.0,
+                         f"one K-quant GEMV shape ({key}), batch 1, inputs > L2", {"kquant": res})
     layer_us = sum(res[f"{KQ_Q4_K_M[m]} {k} {KQ_SHAPES_70B[k][0]}x{KQ_SHAPES_70B[k][1]}"]["us"]
                    for k in KQ_SHAPES_70B for m in k.split("/"))
     layer_bytes = sum(res[f"{KQ_Q4_K_M[m]} {k} {KQ_SHAPES_70B[k][0]}x{KQ_SHAPES_70B[k][1]}"]["bytes"]

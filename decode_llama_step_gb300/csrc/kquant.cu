@@ -38,7 +38,15 @@ namespace dls {
 
 namespace {
 
-constexpr int kMaxWarps = 8;   // consumer warps: cols up to 32768 at most 4 (Q4_K) or 2 (Q6_K) units per lane
+// Consumer warps per CTA: as many as one unit per lane needs (a warp per 32
+// units of a row) while registers allow, else fewer warps with 2-4 units per
+// lane.  Cols up to 32768 fit.
+constexpr int kMaxWarps = 31;
+constexpr int kMaxWarpsMC = 8;
+template <int FMT, int MC>
+struct KqBounds {
+  static constexpr int threads = MC > 1 ? 32 * (kMaxWarpsMC + 1) : FMT == KQ_Q4_K ? 1024 : 512;
+};
 constexpr int kRB = 64;              // rows per reduction block
 constexpr int kStageBytes = 16384;   // target code bytes per ring stage
 constexpr int kRing = 64 * 1024;
@@ -130,30 +138,39 @@ __device__ __forceinline__ int dot16(const uint32_t (&c)[4], const uint32_t* p) 
   return s0 + s1;
 }
 
-// One Q4_K unit of one row: codes at qa (16 bytes), super-block scales at ma.
-__device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, int lane, const KqX<KQ_Q4_K>& xq) {
+// Per-lane byte selectors for the Q4_K scale bytes of the lane's two
+// sub-blocks s = 2g, 2g+1 (g = (lane & 7) >> 1, fixed for the kernel).
+// Scale bytes 0-7 are words y, z of the super-block's first 16 bytes (after
+// d, dmin), bytes 8-11 word w.
+//   g < 2:  [sc_a, sc_b, m_a, m_b] = low 6 bits of bytes (s, s, s+4, s+4)
+//   g >= 2: low 4 bits from the nibbles of bytes s+4 (word w), top 2 bits
+//           from the top of bytes s-4 (sc) and s (m)
+struct Q4kSel {
+  uint32_t s1, s2;
+  bool split;
+};
+
+__device__ __forceinline__ Q4kSel q4k_sel(int lane) {
+  const int g = (lane & 7) >> 1, a = 2 * g;
+  Q4kSel q;
+  q.split = g >= 2;
+  q.s1 = q.split ? (uint32_t)((a - 4) | (a - 3) << 4 | a << 8 | (a + 1) << 12)
+                 : (uint32_t)(a | (a + 1) << 4 | (a + 4) << 8 | (a + 5) << 12);
+  q.s2 = (uint32_t)((a - 4) & 7) * 0x0101u | (uint32_t)((a - 3) & 7) * 0x1010u;
+  return q;
+}
+
+// One Q4_K unit of one row: codes at qa (16 bytes), super-block head at ma.
+__device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, const Q4kSel& sel, const KqX<KQ_Q4_K>& xq) {
   const uint4 q = lds128(qa);
   const uint4 m = lds128(ma);
   const float d = __half2float(__ushort_as_half((unsigned short)(m.x & 0xFFFF)));
   const float dmin = __half2float(__ushort_as_half((unsigned short)(m.x >> 16)));
-  const uint4 sb = make_uint4(m.y, m.z, m.w, 0u);   // the twelve scale bytes
-  const int g = (lane & 7) >> 1;                     // this lane's 64-weight group
-  float sc[2], mn[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int s = 2 * g + h;
-    uint32_t a, b;
-    if (s < 4) {
-      a = byte_of(sb, s) & 63u;
-      b = byte_of(sb, s + 4) & 63u;
-    } else {
-      const uint32_t hi = byte_of(sb, s + 4);
-      a = (hi & 15u) | ((byte_of(sb, s - 4) >> 6) << 4);
-      b = (hi >> 4) | ((byte_of(sb, s) >> 6) << 4);
-    }
-    sc[h] = (float)a;
-    mn[h] = (float)b;
-  }
+  // [sc_a, sc_b, m_a, m_b], one per byte
+  const uint32_t t1 = __byte_perm(m.y, m.z, sel.s1);
+  const uint32_t t2 = __byte_perm(m.w, 0u, sel.s2);
+  const uint32_t v = sel.split ? ((t2 & 0x00000F0Fu) | ((t2 >> 4) & 0x0F0F0000u) | (((t1 >> 6) & 0x03030303u) << 4))
+                               : (t1 & 0x3F3F3F3Fu);
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
   uint32_t lo[4], hi[4];
 #pragma unroll
@@ -161,8 +178,11 @@ __device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, int lane, c
     lo[k] = w[k] & 0x0F0F0F0Fu;
     hi[k] = (w[k] >> 4) & 0x0F0F0F0Fu;
   }
-  const float ia = (float)dot16(lo, xq.p), ib = (float)dot16(hi, xq.p + 8);
-  return xq.s * (d * fmaf(sc[0], ia, sc[1] * ib) - dmin * fmaf(mn[0], (float)xq.sum[0], mn[1] * (float)xq.sum[1]));
+  const int ia = dot16(lo, xq.p), ib = dot16(hi, xq.p + 8);
+  // exact in int32: |sc * I| <= 63 * 16 * 15 * 32767, |m * S| <= 63 * 16 * 32767
+  const int isc = (int)(v & 0xFFu) * ia + (int)((v >> 8) & 0xFFu) * ib;
+  const int imn = (int)((v >> 16) & 0xFFu) * xq.sum[0] + (int)(v >> 24) * xq.sum[1];
+  return xq.s * fmaf(d, (float)isc, -dmin * (float)imn);
 }
 
 // One Q6_K unit of one row: ql halves at aa / ba, qh at ha, scales at sa.
@@ -190,7 +210,7 @@ __device__ __forceinline__ float unit_q6_k(uint32_t aa, uint32_t ba, uint32_t ha
 }
 
 template <int FMT, int RS, int MC>
-__global__ void __launch_bounds__(32 * (kMaxWarps + 1)) kq_gemv_kernel(const KqArgs a, const KqLaunch L) {
+__global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC>::threads) kq_gemv_kernel(const KqArgs a, const KqLaunch L) {
   using G = KqGeo<FMT>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   KqShared& sh = *reinterpret_cast<KqShared*>(smem_raw);
@@ -257,6 +277,7 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 1)) kq_gemv_kernel(const KqA
       ubase[k] = valid[k] ? unit : 0;
       load_unit_x<FMT>(a.x, ubase[k], valid[k], xq[k]);
     }
+    const Q4kSel qsel = q4k_sel(lane);
     const int stages_per_block = kRB / RS;
     for (int s = 0; s < nst; ++s) {
       const int slot = s % NS;
@@ -280,7 +301,7 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 1)) kq_gemv_kernel(const KqA
             if constexpr (FMT == KQ_Q4_K) {
               const int sb = unit >> 3, v = unit & 7;
               const uint32_t blk = rowa + (uint32_t)sb * 144;
-              t = unit_q4_k(blk + 16 + 32 * (v >> 1) + 16 * (v & 1), blk, lane, xq[k]);
+              t = unit_q4_k(blk + 16 + 32 * (v >> 1) + 16 * (v & 1), blk, qsel, xq[k]);
             } else {
               const int sb = unit >> 2, v = unit & 3, h = v >> 1, l0 = (v & 1) * 16;
               const uint32_t blk = rowa + (uint32_t)sb * 208;
@@ -394,35 +415,54 @@ KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms) {
   if ((fmt != KQ_Q4_K && fmt != KQ_Q6_K) || cols % 256 || cols <= 0 || rows <= 0) return l;
   const int nsb = cols / 256;
   const int upb = fmt == KQ_Q4_K ? 8 : 4, mcmax = fmt == KQ_Q4_K ? 4 : 2;
+  const int max1 = (fmt == KQ_Q4_K ? 1024 : 512) / 32 - 1;  // consumer warps at one unit per lane
   const int nchunk = (nsb * upb + 31) / 32;
-  int nwc = 0;
-  for (int d = 1; d <= 8; ++d)
-    if (nchunk % d == 0 && nchunk / d <= mcmax) nwc = d;
-  if (!nwc) nwc = std::min(kMaxWarps, (nchunk + mcmax - 1) / mcmax);
-  const int mc = (nchunk + nwc - 1) / nwc;
+  int nwc = 0, mc = 0;
+  if (nchunk <= max1) {
+    nwc = nchunk;
+    mc = 1;
+  } else {
+    for (int d = 1; d <= kMaxWarpsMC; ++d)
+      if (nchunk % d == 0 && nchunk / d <= mcmax) nwc = d;
+    if (!nwc) nwc = std::min(kMaxWarpsMC, (nchunk + mcmax - 1) / mcmax);
+    mc = (nchunk + nwc - 1) / nwc;
+  }
   if (mc > mcmax) return l;
   const int row_bytes = nsb * (fmt == KQ_Q4_K ? 144 : 208);
   const int drow = fmt == KQ_Q6_K ? ((nsb + 7) & ~7) * 2 : 0;
   int rs = 1;
   while (rs < 8 && (rs * 2) * row_bytes <= kStageBytes) rs *= 2;
   const int stage = rs * (row_bytes + drow);
-  const int ns = std::max(2, std::min(16, kRing / stage));
+  KqFn f = kq_pick(fmt, rs, mc);
+  if (!f) return l;
+  const int threads = 32 * (nwc + 1);
+  const int head = (int)((sizeof(KqShared) + nwc * kRB * 4 + 127) & ~127);
+  // two CTAs per SM with a 64 KB ring, or up to four with ~40 KB rings when
+  // registers allow (more warps to hide the shared-memory and dp2a latency)
+  int best_occ = 0, best_ns = 0;
+  for (int ring : {kRing, 40 * 1024}) {
+    const int ns = std::max(2, std::min(16, ring / stage));
+    const int smem = head + ns * stage;
+    if (smem > 200 * 1024) continue;
+    int occ = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, threads, smem) != cudaSuccess) {
+      cudaGetLastError();
+      occ = 1;
+    }
+    occ = std::max(1, std::min(ring == kRing ? 2 : 4, occ));
+    if (occ > best_occ) {
+      best_occ = occ;
+      best_ns = ns;
+    }
+  }
+  if (!best_occ) return l;
   l.nwc = nwc;
   l.mc = mc;
   l.rs = rs;
-  l.ns = ns;
-  l.threads = 32 * (nwc + 1);
-  l.smem = (int)((sizeof(KqShared) + nwc * kRB * 4 + 127) & ~127) + ns * stage;
-  if (l.smem > 200 * 1024) return KqLaunch{};
-  int occ = 1;
-  KqFn f = kq_pick(fmt, rs, mc);
-  if (!f) return KqLaunch{};
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, l.threads, l.smem) != cudaSuccess) {
-    cudaGetLastError();
-    occ = 1;
-  }
-  occ = std::max(1, std::min(2, occ));
-  l.grid = std::max(1, std::min(num_sms * occ, rows));
+  l.ns = best_ns;
+  l.threads = threads;
+  l.smem = head + best_ns * stage;
+  l.grid = std::max(1, std::min(num_sms * best_occ, rows));
   return l;
 }
 
