@@ -8,7 +8,9 @@
 
 #include <algorithm>
 #include <chrono>
+#include <map>
 #include <string>
+#include <tuple>
 #include <unordered_map>
 #include <vector>
 
@@ -28,6 +30,7 @@ constexpr int kPrefillChunk = 2048;
 // split-K limits of the tensor-core GEMM at batch sizes <= 16
 constexpr int kTgMaxSplit = 16;
 constexpr int kTgCounters = 4096;
+constexpr int kRgMaxRows = 4;  // batched steps of up to this many rows use the multi-row GEMV
 
 struct MatOff {
   size_t qs = 0, d = 0;
@@ -120,6 +123,8 @@ struct dls_model {
   std::vector<uint8_t> draft_host; // layers the speculative draft skips (dls_generate_speculative)
   uint8_t* draft_dev = nullptr;
   bool drafting = false;           // decode steps run the draft (its mask instead of skip_host)
+  bool verifying = false;          // a speculative verify pass: every layer runs
+  std::vector<uint8_t> no_skip;    // all zero
   bool pass_streams = false;       // the current pass over the layers copies streamed layers in
   std::vector<Seq> seqs;
   int32_t* pt_dev = nullptr;
@@ -152,6 +157,9 @@ struct dls_model {
   float *part_o_b = nullptr, *part_ml_b = nullptr;
   int* counters_b = nullptr;
   int attn_splits_b = 1;
+  bool batch_tc = false;  // every batched step through the small-batch tensor-core GEMM
+  bool batch_rg = false;  // every batched step through the multi-row GEMV
+  std::map<std::tuple<int, int, int>, RgLaunch> rg_plans;  // (matrix kind, rows, T) -> multi-row GEMV plan
   // tensor-core GEMM split-K workspace: partial sums and per-tile counters
   float* tg_part = nullptr;
   int* tg_cnt = nullptr;
@@ -366,7 +374,9 @@ int enqueue_copy_layer(dls_model* m, int l) {
 }
 
 // Layers the decode steps skip right now: the draft's mask while drafting.
-const uint8_t* step_skip(const dls_model* m) { return m->drafting ? m->draft_host.data() : m->skip_host.data(); }
+const uint8_t* step_skip(const dls_model* m) {
+  return m->verifying ? m->no_skip.data() : m->drafting ? m->draft_host.data() : m->skip_host.data();
+}
 
 // Start a pass over the layers: with streamed layers, the copy stream joins
 // the compute stream here and fills both buffers with the first two.  A pass
@@ -518,6 +528,25 @@ int run_tgemm(dls_model* m, int kind, int epi, PgArgs g) {
   return DLS_OK;
 }
 
+// One multi-row GEMV over `a.T` activation rows (plan cached per matrix kind).
+int run_rgemv(dls_model* m, int kind, int pro, int epi, RgArgs a) {
+  const auto key = std::make_tuple(kind * 4 + epi, a.w.rows, a.T);
+  auto it = m->rg_plans.find(key);
+  if (it == m->rg_plans.end())
+    it = m->rg_plans.emplace(key, rgemv_plan(m->wtype, pro, epi, a.w.rows, a.w.nb, a.T, m->num_sms, a.unit)).first;
+  const RgLaunch& l = it->second;
+  if (l.grid < 1) return fail(m, DLS_ERR_ARG, "no multi-row GEMV plan rows=%d T=%d", a.w.rows, a.T);
+  if (l.split > 1) {
+    if ((size_t)l.split * a.T * a.w.rows > m->tg_part_elems || l.grid > kTgCounters)
+      return fail(m, DLS_ERR_CAPACITY, "multi-row GEMV split workspace rows=%d T=%d split=%d", a.w.rows, a.T, l.split);
+    a.part = m->tg_part;
+    a.counters = m->tg_cnt;
+  }
+  a.status = &m->sp->status;
+  LK(kind, launch_rgemv(m->wtype, pro, epi, a, l, m->stream));
+  return DLS_OK;
+}
+
 // ---- prefill ---------------------------------------------------------------------
 // T prompt tokens at positions pos0 .. pos0+T-1 of `seq`, all at once: the
 // projections run as tensor-core GEMMs over the T tokens (fp16 operands,
@@ -640,7 +669,112 @@ int enqueue_prefill(dls_model* m, int seq, const int32_t* tokens, int T, int pos
 // position sp->pos[b]) in one pass over the weights: each projection is one
 // tensor-core GEMM over the n rows (fp16 operands, fp32 accumulation), so a
 // weight byte is read once per step for the whole batch.
+int enqueue_batch_tc(dls_model* m, int n, bool head, bool argmax, float* capture);
+
+// Batched step through the multi-row CUDA-core GEMV: fp32 activations end to
+// end, RMSNorm fused into the projections that follow it.
 int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
+  if (m->batch_tc || (n > kRgMaxRows && !m->batch_rg)) return enqueue_batch_tc(m, n, head, argmax, capture);
+  cudaStream_t s = m->stream;
+  const int H = m->H, qkv_ld = m->q_rows + 2 * m->kv_rows;
+  float* x = m->x;  // [n][H]
+  LK(K_EMBED, launch_embed_rows(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp->token, n, m->V, x, H,
+                                &m->sp->status, s));
+  const uint8_t* skip = step_skip(m);
+  TRY(stream_begin(m, skip));
+  for (int l = 0; l < m->L; ++l) {
+    LayerPtrs P;
+    TRY(layer_begin(m, l, &P));
+    if (skip[l]) {
+      if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * H, x, H * sizeof(float), cudaMemcpyDeviceToDevice, s));
+      TRY(layer_end(m, l));
+      continue;
+    }
+    KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
+              m->nkv, m->hd, m->pt, m->max_pages};
+    // (1) RMSNorm -> QKV -> RoPE + fp16 K/V append per row
+    RgArgs g{};
+    g.w = P.qkv;
+    g.unit = 2;
+    g.x = x;
+    g.ldx = H;
+    g.T = n;
+    g.g = P.attn_norm;
+    g.eps = m->eps;
+    g.y = m->pf_qkv;
+    g.ldy = qkv_ld;
+    TRY(run_rgemv(m, K_QKV, PRO_RMSNORM, EPI_STORE, g));
+    LK(K_QKV, launch_rope_kv_batch(m->pf_qkv, n, qkv_ld, m->q_rows, m->kv_rows, kv, m->sp->seq, m->sp->pos, m->rope,
+                                   m->rope_len, m->pf_q, &m->sp->status, s));
+    // (2) split-K attention, one row per (sequence, position)
+    AttnArgs a{};
+    a.q = m->pf_q;
+    a.o = m->o;
+    a.k_pool = kv.k_pool;
+    a.v_pool = kv.v_pool;
+    a.page_table = m->pt_dev;
+    a.max_pages = m->max_pages;
+    a.pt_row = m->sp->seq;
+    a.len = m->sp->pos;
+    a.len_add = 1;
+    a.n_heads = m->nh;
+    a.n_kv = m->nkv;
+    a.head_dim = m->hd;
+    a.page_tokens = m->pt;
+    a.n_splits = m->attn_splits_b;
+    a.row0 = 0;
+    a.part_o = m->part_o_b;
+    a.part_ml = m->part_ml_b;
+    a.counters = m->counters_b;
+    a.status = &m->sp->status;
+    a.max_len = m->max_ctx;
+    LK(K_ATTN, launch_attention(a, n, s, false));
+    // (3) O projection + residual
+    RgArgs go = g;
+    go.w = P.o;
+    go.unit = 1;
+    go.x = m->o;
+    go.ldx = m->q_rows;
+    go.g = nullptr;
+    go.y = x;
+    go.ldy = H;
+    TRY(run_rgemv(m, K_O, PRO_COPY, EPI_RESID, go));
+    // (4) RMSNorm -> gate/up -> SwiGLU: h [n][F]
+    RgArgs gg = g;
+    gg.w = P.gu;
+    gg.g = P.ffn_norm;
+    gg.y = m->gu;
+    gg.ldy = m->F;
+    TRY(run_rgemv(m, K_GATE_UP, PRO_RMSNORM, EPI_SWIGLU, gg));
+    // (5) down + residual
+    RgArgs gd = go;
+    gd.w = P.down;
+    gd.x = m->gu;
+    gd.ldx = m->F;
+    TRY(run_rgemv(m, K_DOWN, PRO_COPY, EPI_RESID, gd));
+    if (capture) CK(cudaMemcpyAsync(capture + (size_t)l * H, x, H * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    TRY(layer_end(m, l));
+  }
+  if (head || argmax) {
+    RgArgs gh{};
+    gh.w = head_mat(m);
+    gh.unit = 1;
+    gh.x = x;
+    gh.ldx = H;
+    gh.T = n;
+    gh.g = m->out_norm;
+    gh.eps = m->eps;
+    gh.y = m->logits;
+    gh.ldy = m->V;
+    TRY(run_rgemv(m, K_HEAD, PRO_RMSNORM, EPI_STORE, gh));
+  }
+  if (argmax)
+    LK(K_ARGMAX, launch_argmax(m->logits, m->V, n, m->next_tok, m->argmax_part, m->argmax_cnt,
+                               argmax_blocks(n, m->num_sms), s, false));
+  return DLS_OK;
+}
+
+int enqueue_batch_tc(dls_model* m, int n, bool head, bool argmax, float* capture) {
   cudaStream_t s = m->stream;
   const int H = m->H, qkv_ld = m->q_rows + 2 * m->kv_rows;
   float* x = m->x;  // [n][H]
@@ -1198,6 +1332,15 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   CKC(gemv_setup_attributes());
   CKC(tgemm_setup_attributes());
   CKC(sgemm_setup_attributes());
+  CKC(rgemv_setup_attributes());
+  // batched steps: the multi-row CUDA-core GEMV for 2-4 rows, the
+  // small-batch tensor-core GEMM for 5-8 (measured on the 8B Q8_0 model at
+  // ctx 2048, per step: 3.5 vs 5.5 ms at 2 rows, 4.6 vs 5.9 at 4, 7.4 vs 6.5
+  // at 8); DLS_BATCH_GEMM=tc or =rg selects one for every batch size
+  if (const char* e = getenv("DLS_BATCH_GEMM")) {
+    m->batch_tc = strcmp(e, "tc") == 0;
+    m->batch_rg = strcmp(e, "rg") == 0;
+  }
   CKC(prefill_setup_attributes());
   CKC(fattn_setup_attributes());
 
@@ -1250,10 +1393,13 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   CKC(cudaMemsetAsync(m->k_pool, 0, (size_t)m->L * m->kv_layer_elems * sizeof(__half), m->stream));
   CKC(cudaMemsetAsync(m->v_pool, 0, (size_t)m->L * m->kv_layer_elems * sizeof(__half), m->stream));
   TRYC(dev_alloc_t(m, (size_t)m->max_seqs * m->max_pages, &m->pt_dev, "page_table"));
-  TRYC(dev_alloc_t(m, (size_t)B * m->H, &m->x, "x"));
-  TRYC(dev_alloc_t(m, (size_t)B * m->q_rows, &m->q, "q"));
-  TRYC(dev_alloc_t(m, (size_t)B * m->q_rows, &m->o, "o"));
-  TRYC(dev_alloc_t(m, (size_t)B * 2 * m->F, &m->gu, "gate_up"));
+  // per-row scratch for batched steps: a user batch, or the rows of one
+  // speculative verify pass (up to kMaxBatch)
+  const int BR = std::max(B, kMaxBatch);
+  TRYC(dev_alloc_t(m, (size_t)BR * m->H, &m->x, "x"));
+  TRYC(dev_alloc_t(m, (size_t)BR * m->q_rows, &m->q, "q"));
+  TRYC(dev_alloc_t(m, (size_t)BR * m->q_rows, &m->o, "o"));
+  TRYC(dev_alloc_t(m, (size_t)BR * 2 * m->F, &m->gu, "gate_up"));
   // logits rows: a batch, or the rows of one dls_verify pass
   TRYC(dev_alloc_t(m, (size_t)std::max(B, DLS_MAX_VERIFY) * m->V, &m->logits, "logits"));
   TRYC(dev_alloc_t(m, (size_t)std::max(kMaxBatch, DLS_MAX_VERIFY), &m->next_tok, "next_token"));
@@ -1280,13 +1426,13 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   TRYC(dev_alloc_t(m, 2 * pf_rows * m->pf_ldh, &m->pf_h, "prefill_h16"));
   m->pf_h_lo = m->pf_h + pf_rows * m->pf_ldh;
   TRYC(dev_alloc_t(m, pf_rows, &m->pf_tok, "prefill_tokens"));
-  if (B > 1) {
-    m->attn_splits_b = attn_default_splits(B, m->nkv, m->num_sms, m->max_ctx);
-    const size_t wsb = attn_workspace_bytes(B, m->nh, m->nkv, m->hd, m->attn_splits_b);
+  {
+    m->attn_splits_b = attn_default_splits(BR, m->nkv, m->num_sms, m->max_ctx);
+    const size_t wsb = attn_workspace_bytes(BR, m->nh, m->nkv, m->hd, m->attn_splits_b);
     TRYC(dev_alloc(m, wsb, &m->attn_ws_b, "attention_scratch_batch"));
-    attn_workspace_carve(m->attn_ws_b, B, m->nh, m->nkv, m->hd, m->attn_splits_b, &m->part_o_b, &m->part_ml_b,
+    attn_workspace_carve(m->attn_ws_b, BR, m->nh, m->nkv, m->hd, m->attn_splits_b, &m->part_o_b, &m->part_ml_b,
                          &m->counters_b);
-    CKC(cudaMemsetAsync(m->counters_b, 0, (size_t)B * m->nkv * sizeof(int), m->stream));
+    CKC(cudaMemsetAsync(m->counters_b, 0, (size_t)BR * m->nkv * sizeof(int), m->stream));
   }
   {
     // split-K partials for batches of up to 16 rows: [split][16][rows]
@@ -1351,6 +1497,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   TRYC(dev_alloc_t(m, (size_t)m->L, &m->skip_dev, "layer_skip"));
   CKC(cudaMemsetAsync(m->skip_dev, 0, m->L, m->stream));
   m->draft_host.assign(m->L, 0);
+  m->no_skip.assign(m->L, 0);
   TRYC(dev_alloc_t(m, (size_t)m->L, &m->draft_dev, "draft_skip"));
   CKC(cudaMemsetAsync(m->draft_dev, 0, m->L, m->stream));
   TRYC(sync_stream(m, m->stream));
@@ -1618,8 +1765,25 @@ int dls_generate_speculative(dls_model* m, int32_t seq, int32_t token, int32_t n
       // the verify pass reads [cur, d_1 .. d_r]: cur from the host, the drafts where the steps left them
       CK(cudaMemcpyAsync(m->pf_tok + 1, m->tokens_dev, r * sizeof(int32_t), cudaMemcpyDeviceToDevice, m->stream));
     }
-    CK(cudaMemcpyAsync(m->pf_tok, &cur, sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
-    TRY(enqueue_prefill(m, seq, nullptr, r + 1, P, HEAD_ALL, nullptr));
+    if (r > 0 && r + 1 <= kMaxBatch) {
+      // rows t = 0..r at positions P + t of this one sequence through the
+      // batched step (each row attends to the positions up to its own)
+      int32_t vs[kMaxBatch], vt[kMaxBatch], vp[kMaxBatch];
+      for (int t = 0; t <= r; ++t) {
+        vs[t] = seq;
+        vt[t] = cur;
+        vp[t] = P + t;
+      }
+      TRY(set_params(m, r + 1, vs, vt, vp, false));
+      CK(cudaMemcpyAsync(m->sp->token + 1, m->tokens_dev, r * sizeof(int32_t), cudaMemcpyDeviceToDevice, m->stream));
+      m->verifying = true;
+      const int rc = enqueue_batch(m, r + 1, true, true, nullptr);
+      m->verifying = false;
+      TRY(rc);
+    } else {
+      CK(cudaMemcpyAsync(m->pf_tok, &cur, sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+      TRY(enqueue_prefill(m, seq, nullptr, r + 1, P, HEAD_ALL, nullptr));
+    }
     // read back after the whole round is enqueued (pageable destinations block the host)
     if (r > 0)
       CK(cudaMemcpyAsync(host + DLS_MAX_VERIFY, m->tokens_dev, r * sizeof(int32_t), cudaMemcpyDeviceToHost,

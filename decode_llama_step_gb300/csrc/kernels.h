@@ -193,6 +193,32 @@ cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, c
 // scales applied per 32-column block from tensor memory (gemm_small.cu)
 cudaError_t sgemm_setup_attributes();
 
+// ---- multi-row dequant-GEMV (2..8 activation rows; gemv_rows.cu) ---------------
+struct RgArgs {
+  MatDev w;
+  int unit;              // rows are split across CTAs in multiples of this (2 for SwiGLU pairs)
+  const float* x;        // activations [T][ldx] fp32
+  int ldx;
+  int T;                 // activation rows, 1..8
+  const float* g;        // RMSNorm gain [cols] (PRO_RMSNORM)
+  float eps;
+  float* y;              // STORE: y[t*ldy + r]; RESID: +=; SWIGLU: y[t*ldy + r/2] = silu(gate) * up
+  int ldy;
+  int32_t* status;       // kTimeout when a bounded wait ran out
+  float* part;           // split-K partials [split][T][rows] (split > 1)
+  int* counters;         // one per row range (grid.x), zero between launches (split > 1)
+};
+
+struct RgLaunch {
+  int grid, threads, smem;
+  int nt, rs, mc, ns, split;  // rows padded to nt, weight rows per stage, chunks per lane, stages, K splits
+  int stage;                  // ring stage stride in bytes
+};
+
+RgLaunch rgemv_plan(int wtype, int pro, int epi, int rows, int nb, int T, int num_sms, int unit);  // grid 0: unsupported
+cudaError_t rgemv_setup_attributes();
+cudaError_t launch_rgemv(int wtype, int pro, int epi, const RgArgs& a, const RgLaunch& l, cudaStream_t s);
+
 // ---- K-quant dequant-GEMV (Q4_K, Q6_K; kquant.cu) ------------------------------
 enum KqFormat { KQ_Q4_K = 12, KQ_Q6_K = 14 };  // the GGUF type ids
 

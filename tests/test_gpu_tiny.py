@@ -230,6 +230,54 @@ def test_decode_batch_equals_single_steps(setup):
             m.seq_free(s)
 
 
+@pytest.mark.parametrize("mode", ["rg", "tc"])
+@pytest.mark.parametrize("cfg", [TINY, TINY_Q4], ids=["q8_0", "q4_0"])
+def test_batch_paths_match_oracle(gpu_lib, mode, cfg):
+    """Both batched-step paths (the multi-row CUDA-core GEMV and the
+    small-batch tensor-core GEMM, DLS_BATCH_GEMM, read at model creation) at
+    every batch size 2..8 against the oracle, rows at different lengths."""
+    import os
+    torch = _torch()
+    from decode_llama_step_gb300 import dls
+    w = synth.model_weights(cfg)
+    stream = torch.cuda.Stream()
+    old = os.environ.get("DLS_BATCH_GEMM")
+    os.environ["DLS_BATCH_GEMM"] = mode
+    try:
+        m = dls.Model(cfg, w, max_seqs=8, max_ctx=96, max_batch=8, page_tokens=32, stream=stream)
+    finally:
+        if old is None:
+            del os.environ["DLS_BATCH_GEMM"]
+        else:
+            os.environ["DLS_BATCH_GEMM"] = old
+    orc = OracleModel(cfg, w)
+    try:
+        prompts = [synth.prompt_tokens(cfg, 4 + 5 * i, seed=60 + i) for i in range(8)]
+        refs = []
+        for p in prompts:
+            o = orc.new_seq()
+            orc.prefill(o, p)
+            refs.append(o)
+        for n in (2, 3, 4, 5, 8):
+            seqs = [m.seq_create() for _ in range(n)]
+            try:
+                for s, p in zip(seqs, prompts):
+                    m.prefill(s, p)
+                toks = [(37 * i + n) % cfg.vocab for i in range(n)]
+                pos = [m.seq_length(s) for s in seqs]
+                out = torch.empty(n, cfg.vocab, device="cuda")
+                m.decode_batch(seqs, toks, pos, out)
+                stream.synchronize()
+                for i in range(n):
+                    ref = orc.decode_step(refs[i].fork(), toks[i], pos[i])
+                    assert_close(out[i].cpu().numpy(), ref, f"{mode} n={n} row {i}")
+            finally:
+                for s in seqs:
+                    m.seq_free(s)
+    finally:
+        m.close()
+
+
 def test_generate_batch_matches_oracle(setup):
     # three sequences of different lengths decode together on the tensor-core
     # path; every step's token is the oracle's greedy token while the
