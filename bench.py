@@ -39,10 +39,10 @@ METRIC = "decode tok/s, 8B-shape Q8_0 batch 1; achieved HBM GB/s as % of peak"
 # captured again); the captures are summarised under profiles/.
 NCU_TRAFFIC = {
     # step.cu: 4-layer 8B Q8_0 model, ctx 2051, one step-kernel launch:
-    # dram read 1,520,923,648 + write 5,118,464 B against 1,520,440,320
+    # dram read 1,521,000,448 + write 5,145,344 B against 1,520,440,320
     # algorithmic bytes; the traffic grows with the layers, so a full launch
     # is scaled by the same ratio (the capture is summarised under profiles/)
-    "0e8b0c8230dc6604": {"ratio": 1526042112 / 1520440320},
+    "37032cc45be1d22a": {"ratio": 1526145792 / 1520440320},
 }
 
 KIND_NAMES = {1: "embed", 2: "gemv_qkv", 3: "attention", 4: "gemv_o", 5: "gemv_gate_up", 6: "gemv_down",
@@ -70,7 +70,7 @@ def parse():
                    help="kquant workload: only this format and shape, e.g. q4_k:28672x8192 (small ncu captures)")
     p.add_argument("--draft-k", default="1,3,7",
                    help="speculative workload: draft lengths to time (comma-separated)")
-    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip", "spec", "kquant"],
+    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip", "spec", "kquant", "batch"],
                    default="decode",
                    help="decode (default, the headline line); the others are secondary measurements: "
                         "prefill (prompt of --ctx tokens), fork (shared prefix -> 8 branches), "
@@ -78,7 +78,8 @@ def parse():
                         "skip (decode with the layers whose calibrated cosine exceeds --skip-threshold skipped), "
                         "spec (self-speculative greedy decoding vs plain greedy decoding; --config 70b: the 24 GB "
                         "budget with the resident layers as the draft), "
-                        "kquant (Q4_K / Q6_K dequant-GEMV on the 70B projection shapes)")
+                        "kquant (Q4_K / Q6_K dequant-GEMV on the 70B projection shapes), "
+                        "batch (batched decode of 2, 4 and 8 sequences at ctx --ctx: tok/s and per-kernel times)")
     return p.parse_args()
 
 
@@ -442,6 +443,48 @@ def run_kquant(args):
                       "clocks": clk.summary()})
 
 
+def run_batch(args):
+    """Batched decode of 2, 4 and 8 sequences (copies of one --ctx prompt's
+    cache): greedy tok/s over --steps graph-replayed steps per batch size,
+    and one step's kernels timed one by one.  DLS_BATCH_GEMM (tc or rg)
+    forces one projection path for every batch size."""
+    import torch
+    import synth
+    from decode_llama_step_gb300 import dls
+    cfg = load_config(args.config, args.layers)
+    D, W = args.steps, max(args.warmup, 1)
+    w = synth.model_weights(cfg)
+    stream = torch.cuda.Stream()
+    m = dls.Model(cfg, w, max_seqs=9, max_ctx=args.ctx + D + W + 8, max_batch=8, page_tokens=64, stream=stream)
+    del w
+    base = m.seq_create()
+    m.prefill(base, synth.prompt_tokens(cfg, args.ctx, seed=1))
+    res = {}
+    with ClockSampler(0) as clk:
+        for n in (2, 4, 8):
+            seqs = [m.seq_create() for _ in range(n)]
+            m.kv_fork(base, seqs)
+            toks = [100 + i for i in range(n)]
+            m.generate(seqs, toks, W)
+            t = _events(torch, stream, lambda: m.generate(seqs, toks, D))
+            kms, kk = m.profile_batch(seqs, toks, [m.seq_length(s) for s in seqs])
+            per_kind = {}
+            for d_ms, k in zip(kms, kk):
+                name = KIND_NAMES.get(int(k), str(int(k)))
+                per_kind[name] = round(per_kind.get(name, 0.0) + float(d_ms), 4)
+            res[f"batch{n}"] = {"tok_s": round(n * D / t, 1), "ms_per_step": round(1000 * t / D, 3),
+                                "kernels_ms": per_kind, "kernels_total_ms": round(sum(per_kind.values()), 3)}
+            for s_ in seqs:
+                m.seq_free(s_)
+    m.close()
+    b = res["batch8"]
+    path = os.environ.get("DLS_BATCH_GEMM", "default (rows <= 4: multi-row GEMV; 5-8: tensor-core GEMM)")
+    return base_line(f"batched decode tok/s, {cfg.name}-shape {'Q8_0' if cfg.wtype == 8 else 'Q4_0'}, batch 8",
+                     b["tok_s"], "tok/s", D, W, b["ms_per_step"],
+                     f"{cfg.name} batched greedy decode of copies of a {args.ctx}-token cache, batch 2/4/8",
+                     {"batch": res, "projection_path": path, "clocks": clk.summary()})
+
+
 def h2d_peak(torch, chunk=256 << 20, inflight=4, reps=10):
     """Best pinned host -> device copy rate: 256 MB chunks, several in flight."""
     host = torch.empty(chunk * inflight, dtype=torch.uint8, pin_memory=True)
@@ -634,7 +677,7 @@ def main():
         if int(os.environ.get("RANK", "0")) != 0:
             return 0
         fn = {"prefill": run_prefill, "fork": run_fork, "stream": run_stream, "skip": run_skip,
-              "spec": run_spec, "kquant": run_kquant}[args.workload]
+              "spec": run_spec, "kquant": run_kquant, "batch": run_batch}[args.workload]
         print(json.dumps(fn(args)), flush=True)
         return 0
 

@@ -46,12 +46,15 @@ __device__ __forceinline__ void ctmark(const StepArgs& A, unsigned epoch, int sl
   if (A.ctrace && threadIdx.x == 0) A.ctrace[((size_t)epoch * gridDim.x + blockIdx.x) * kTr + slot] = global_ns();
 }
 
+constexpr int kMaxSkipLayers = 256;  // layer-skip flags kept in shared memory
+
 struct Sh {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   float red[32];
   int last;
   unsigned epoch_pub;  // grid barriers the consumers have passed
+  uint8_t skip[kMaxSkipLayers];  // the step's layer-skip flags (copied once from global memory)
 };
 
 struct Ctx {
@@ -169,7 +172,7 @@ __device__ void hint_lanes(const Ctx& c) {
   const uint64_t t0 = global_ns();
   unsigned done = 0;  // computed layers before l
   for (int l = 0; l < A.n_layers; ++l) {
-    if (A.skip && A.skip[l]) continue;
+    if (c.sh->skip[l]) continue;
     const unsigned target = 2u + 5u * done++;  // barriers passed when layer l's attention starts
     for (uint32_t i = 0; *ep < target; ++i) {
       __nanosleep(256);
@@ -262,7 +265,7 @@ __device__ void begin_phase(const Ctx& c, const Rows& R, PCur& u) {
     if (!A.head_rows) u.n = 0;
     return;
   }
-  if (A.skip && A.skip[u.l]) {  // a skipped layer streams nothing
+  if (c.sh->skip[u.l]) {  // a skipped layer streams nothing
     u.n = 0;
     return;
   }
@@ -901,6 +904,7 @@ __global__ void __maxnreg__(200) step_kernel(const StepArgs A) {
     mbar_fence_init();
     if (A.trace && blockIdx.x == 0) A.trace[0] = global_ns();
   }
+  for (int l = tid; l < kMaxSkipLayers; l += blockDim.x) c.sh->skip[l] = (A.skip && l < A.n_layers) ? A.skip[l] : 0;
   __syncthreads();
 
   if (warp == NWC) {
@@ -936,7 +940,7 @@ __global__ void __maxnreg__(200) step_kernel(const StepArgs A) {
     }
     grid_sync(c);
     for (int l = 0; l < A.n_layers; ++l) {
-      if (A.skip && A.skip[l]) continue;  // the residual passes through; every CTA reads the same flags
+      if (c.sh->skip[l]) continue;  // the residual passes through; every CTA reads the same flags
       const StepLayer& L = A.layers[l];
       EpiArgs e{};
       e.y = A.q;
@@ -1103,7 +1107,7 @@ StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, i
 }
 
 cudaError_t launch_step(const StepPlan& p, const StepArgs& a, cudaStream_t s) {
-  if (!p.fn) return cudaErrorInvalidValue;
+  if (!p.fn || a.n_layers > kMaxSkipLayers) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.threads);
