@@ -564,7 +564,7 @@ def _check_speculative(cfg, m, orc, seq, prompt, tok, n, mask, k, what):
     return toks, st
 
 
-@pytest.mark.parametrize("k", [1, 3])
+@pytest.mark.parametrize("k", [1, 3, 9])  # 9: a verify pass of 10 positions (the prefill-chunk form)
 @pytest.mark.parametrize("draft", ["skip-last", "skip-first", "skip-all", "full"])
 def test_speculative_decode_matches_oracle(setup, draft, k):
     """Self-speculative greedy decoding (engine page, sections 3.5 and 5.3):
