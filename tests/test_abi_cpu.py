@@ -105,3 +105,30 @@ def test_attention_op_rejects_bad_shapes(lib):
     assert rc == dls.DLS_ERR_ARG
     rc = lib.dls_attention_decode(None, 1, 1, 1, 1, 1, 1, 1 << 20, 1, 4, 2, 64, 64, 4, 1, None)
     assert rc == dls.DLS_ERR_ARG
+
+
+def test_null_model_calls_of_the_later_entry_points(lib):
+    assert lib.dls_seq_truncate(None, 0, 0) == dls.DLS_ERR_ARG
+    assert lib.dls_verify(None, 0, None, 1, None, None) == dls.DLS_ERR_ARG
+    assert lib.dls_generate_speculative(None, 0, 1, 4, None, 3, None, None) == dls.DLS_ERR_ARG
+    assert lib.dls_set_layer_skip(None, None, 0) == dls.DLS_ERR_ARG
+    assert lib.dls_layer_cosines(None, 0, 1, 0, None) == dls.DLS_ERR_ARG
+
+
+def test_kquant_layout_sizes_and_argument_checks(lib):
+    # Q4_K: the GGUF super-blocks as they are (144 bytes per 256 weights)
+    assert lib.dls_kquant_packed_bytes(dls.DLS_Q4_K, 3, 512) == 3 * 2 * 144
+    # Q6_K: 208 bytes per super-block, 256-byte aligned, then fp16 scales
+    # with each row padded to 8 super-blocks
+    rows, nsb = 5, 17
+    main = (rows * nsb * 208 + 255) // 256 * 256
+    assert lib.dls_kquant_packed_bytes(dls.DLS_Q6_K, rows, nsb * 256) == main + rows * 24 * 2
+    for bad in [(dls.DLS_Q4_K, 3, 300), (dls.DLS_Q4_K, 0, 256), (13, 4, 256), (dls.DLS_Q6_K, 4, 0)]:
+        assert lib.dls_kquant_packed_bytes(*bad) == 0
+    # rejected before any CUDA call
+    assert lib.dls_kquant_gemv(13, 256, 4, 256, 256, 256, None, None) == dls.DLS_ERR_ARG
+    assert lib.dls_kquant_gemv(dls.DLS_Q4_K, None, 4, 256, 256, 256, None, None) == dls.DLS_ERR_ARG
+    assert lib.dls_kquant_gemv(dls.DLS_Q4_K, 256, 4, 300, 256, 256, None, None) == dls.DLS_ERR_ARG
+    assert lib.dls_kquant_gemv(dls.DLS_Q4_K, 256 + 16, 4, 256, 256, 256, None, None) == dls.DLS_ERR_ARG
+    assert lib.dls_kquant_pack(dls.DLS_Q6_K, None, 4, 256, 256, None) == dls.DLS_ERR_ARG
+    assert "kquant" in lib.dls_last_error(None).decode()
