@@ -1716,9 +1716,11 @@ int dls_verify(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, floa
 
 // Self-speculative greedy decoding: per round, r draft steps (decode steps
 // with the draft's layers skipped, tokens fed back on the device), the
-// sequence cut back, one dls_verify-style pass of the current token and the
-// r drafts through every layer, and the longest agreeing prefix kept.  One
-// host round trip per round (the drafts and the full model's picks).
+// sequence cut back, one pass of the current token and the r drafts through
+// every layer (a batched step over the one sequence for up to kMaxBatch
+// positions, else a prefill chunk keeping every row's logits), and the
+// longest agreeing prefix kept.  One host round trip per round (the drafts
+// and the full model's picks).
 int dls_generate_speculative(dls_model* m, int32_t seq, int32_t token, int32_t n_tokens, const uint8_t* draft_skip,
                              int32_t draft_k, int32_t* tokens_out, int32_t* stats) {
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
@@ -1762,8 +1764,6 @@ int dls_generate_speculative(dls_model* m, int32_t seq, int32_t token, int32_t n
       for (int t = 0; t < r && rc == DLS_OK; ++t) rc = run_step(m, 1, false, true);
       m->drafting = false;
       TRY(rc);
-      // the verify pass reads [cur, d_1 .. d_r]: cur from the host, the drafts where the steps left them
-      CK(cudaMemcpyAsync(m->pf_tok + 1, m->tokens_dev, r * sizeof(int32_t), cudaMemcpyDeviceToDevice, m->stream));
     }
     if (r > 0 && r + 1 <= kMaxBatch) {
       // rows t = 0..r at positions P + t of this one sequence through the
@@ -1781,6 +1781,9 @@ int dls_generate_speculative(dls_model* m, int32_t seq, int32_t token, int32_t n
       m->verifying = false;
       TRY(rc);
     } else {
+      // the prefill chunk reads [cur, d_1 .. d_r]: cur from the host, the drafts where the steps left them
+      if (r > 0)
+        CK(cudaMemcpyAsync(m->pf_tok + 1, m->tokens_dev, r * sizeof(int32_t), cudaMemcpyDeviceToDevice, m->stream));
       CK(cudaMemcpyAsync(m->pf_tok, &cur, sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
       TRY(enqueue_prefill(m, seq, nullptr, r + 1, P, HEAD_ALL, nullptr));
     }

@@ -260,11 +260,12 @@ int dls_verify(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, floa
  * draft_skip[l] != 0 skipped (host uint8 [n_layers]; e.g. the streamed
  * layers, or those dls_layer_cosines finds above a threshold).  Each round:
  * r = min(draft_k, tokens still wanted - 1) draft decode steps from the
- * current token t at position P; the sequence cut back to P; one dls_verify
- * pass of [t, d_1..d_r] through every layer; the longest prefix of drafts the
- * full model also picks is accepted, and the round emits those drafts plus
- * the full model's next pick (so the output is the full model's greedy
- * continuation).  0 <= draft_k < DLS_MAX_VERIFY.  stats (host int32 [3], or
+ * current token t at position P; the sequence cut back to P; one pass of
+ * [t, d_1..d_r] at positions P..P+r through every layer (a batched decode
+ * step over the one sequence when r + 1 <= 8, else a dls_verify prefill
+ * chunk); the longest prefix of drafts the full model also picks is
+ * accepted, and the round emits those drafts plus the full model's next pick
+ * (so the output is the full model's greedy continuation).  0 <= draft_k < DLS_MAX_VERIFY.  stats (host int32 [3], or
  * NULL) receives rounds, drafted and accepted token counts.  Draft steps
  * skip streamed layers' copies when the draft skips every streamed layer.
  * The mask of dls_set_layer_skip is not used by this call. */

@@ -30,7 +30,8 @@ length).  The pages give no formulas; the readings taken where they are
 silent are listed in each function's docstring.
 
 Parity status: every op is pinned by tests against closed forms, invariants
-or brute force.  The composed model is pinned by self-consistency (prefill of
+or brute force (the K-quant formats by blocks written field by field from the
+stated layout, and by planted mistakes that the pins must catch).  The composed model is pinned by self-consistency (prefill of
 T tokens equals T decode steps; a fork equals an independent prefill) and by
 wiring cases with closed forms; there is no external worked example, so the
 full-model composition beyond those is "parity unpinned".
