@@ -1,4 +1,4 @@
-"""Q4_K and Q6_K block dequantisation and the dequant-GEMV, fp64.
+"""Q4_K, Q5_K and Q6_K block dequantisation and the dequant-GEMV, fp64.
 
 TEST INFRASTRUCTURE (see the package docstring): only the tests, the smoke
 check and the benchmark's CPU leg use it.
@@ -24,6 +24,12 @@ Q4_K, 144 bytes:
                in its high nibble
   weight_i = d * sc_s * q_i - dmin * m_s       (s = i // 32)
 
+Q5_K, 176 bytes: Q4_K's first 16 bytes (d, dmin, the twelve scale bytes),
+  then 32 bytes qh of fifth code bits, then Q4_K's 128 bytes of low 4 bits.
+  Weight 64g + l takes bit 2g of qh[l] as its fifth bit, weight 64g + 32 + l
+  bit 2g + 1 (g = 0..3, l = 0..31); q = low | fifth << 4 (0..31) and
+  weight_i = d * sc_s * q_i - dmin * m_s as for Q4_K.
+
 Q6_K, 210 bytes:
   bytes 0-127   ql: low 4 bits of the codes
   bytes 128-191 qh: high 2 bits of the codes
@@ -40,7 +46,7 @@ from __future__ import annotations
 import numpy as np
 
 QK = 256
-BLOCK_BYTES = {"q4_k": 144, "q6_k": 210}
+BLOCK_BYTES = {"q4_k": 144, "q5_k": 176, "q6_k": 210}
 
 
 def _f16(lo: np.ndarray, hi: np.ndarray) -> np.ndarray:
@@ -77,6 +83,22 @@ def dequant_q4_k(blocks: np.ndarray, n_blocks: int) -> np.ndarray:
     return d[:, None] * sc[:, sub] * q - dmin[:, None] * m[:, sub]
 
 
+def dequant_q5_k(blocks: np.ndarray, n_blocks: int) -> np.ndarray:
+    """n_blocks Q5_K super-blocks -> float64 [n_blocks, 256]."""
+    b = np.asarray(blocks, dtype=np.uint8)[: n_blocks * 176].reshape(n_blocks, 176)
+    d = _f16(b[:, 0], b[:, 1])
+    dmin = _f16(b[:, 2], b[:, 3])
+    sc, m = q4_k_scales_mins(b[:, 4:16])
+    qh = b[:, 16:48].astype(np.int64)
+    qs = b[:, 48:].astype(np.int64)
+    q = np.empty((n_blocks, QK), dtype=np.int64)
+    for g in range(4):
+        q[:, 64 * g: 64 * g + 32] = (qs[:, 32 * g: 32 * g + 32] & 0x0F) | (((qh >> (2 * g)) & 1) << 4)
+        q[:, 64 * g + 32: 64 * g + 64] = (qs[:, 32 * g: 32 * g + 32] >> 4) | (((qh >> (2 * g + 1)) & 1) << 4)
+    sub = np.arange(QK) // 32
+    return d[:, None] * sc[:, sub] * q - dmin[:, None] * m[:, sub]
+
+
 def q6_k_codes(ql: np.ndarray, qh: np.ndarray) -> np.ndarray:
     """ql [n, 128] and qh [n, 64] -> the 6-bit codes [n, 256] (0..63)."""
     ql = ql.astype(np.int64)
@@ -103,6 +125,8 @@ def dequant_q6_k(blocks: np.ndarray, n_blocks: int) -> np.ndarray:
 def dequant_blocks(blocks: np.ndarray, n_blocks: int, fmt: str) -> np.ndarray:
     if fmt == "q4_k":
         return dequant_q4_k(blocks, n_blocks)
+    if fmt == "q5_k":
+        return dequant_q5_k(blocks, n_blocks)
     if fmt == "q6_k":
         return dequant_q6_k(blocks, n_blocks)
     raise ValueError(f"unknown K-quant format {fmt}")

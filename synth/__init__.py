@@ -165,24 +165,25 @@ def prompt_tokens(cfg: ModelConfig, n: int, seed: int = 1) -> np.ndarray:
 # --------------------------------------------------------------------------
 # K-quant super-blocks (Q4_K: 144 bytes, Q6_K: 210 bytes per 256 weights)
 
-KQUANT_BLOCK_BYTES = {"q4_k": 144, "q6_k": 210}
+KQUANT_BLOCK_BYTES = {"q4_k": 144, "q5_k": 176, "q6_k": 210}
 
 
 def kquant_matrix(key: int, rows: int, cols: int, fmt: str) -> np.ndarray:
     """[rows x cols] matrix of seeded K-quant super-blocks (uint8, flat,
     row-major, cols / 256 per row).  Every code and sub-block scale byte is
     uniform over its range; the fp16 super-block scales are drawn in
-    [0.5, 1.5) x 2^-12 (Q4_K d and dmin) or x 2^-14 (Q6_K d), which keeps
-    weights within about +-0.25, the spread of a trained model's."""
+    [0.5, 1.5) x 2^-12 (Q4_K d and dmin), x 2^-13 (Q5_K) or x 2^-14 (Q6_K
+    d), which keeps weights within about +-0.25, the spread of a trained
+    model's."""
     if cols % 256:
         raise ValueError(f"cols={cols} is not a multiple of 256")
     bb = KQUANT_BLOCK_BYTES[fmt]
     nblk = rows * (cols // 256)
     raw = tokens(key, nblk * bb, 256).astype(np.uint8).reshape(nblk, bb)
     u = tokens(key ^ 0x5BD1E995, 2 * nblk, 256).astype(np.float64).reshape(nblk, 2)
-    if fmt == "q4_k":
+    if fmt in ("q4_k", "q5_k"):
         for j, at in enumerate((0, 2)):
-            d = ((0.5 + u[:, j] / 256.0) * 2.0 ** -12).astype(np.float16).view(np.uint16)
+            d = ((0.5 + u[:, j] / 256.0) * 2.0 ** (-12 if fmt == "q4_k" else -13)).astype(np.float16).view(np.uint16)
             raw[:, at] = d & 0xFF
             raw[:, at + 1] = d >> 8
     else:

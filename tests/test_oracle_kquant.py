@@ -41,6 +41,20 @@ def _pack_q4_k(d, dmin, sc, m, q):
     return blk
 
 
+def _pack_q5_k(d, dmin, sc, m, q):
+    """One Q5_K super-block from d, dmin, eight (sc, m) pairs and 256 codes 0..31."""
+    low = [v & 15 for v in q]
+    q4 = _pack_q4_k(d, dmin, sc, m, low)
+    blk = np.zeros(176, dtype=np.uint8)
+    blk[0:16] = q4[0:16]
+    blk[48:176] = q4[16:144]
+    for i in range(256):
+        g, r = divmod(i, 64)
+        bit = 2 * g + (1 if r >= 32 else 0)
+        blk[16 + (r % 32)] |= (q[i] >> 4) << bit
+    return blk
+
+
 def _pack_q6_k(d, scales, code):
     """One Q6_K super-block from d, sixteen int8 scales and 256 codes 0..63."""
     blk = np.zeros(210, dtype=np.uint8)
@@ -91,6 +105,37 @@ def test_q4_k_six_bit_scales_and_minimums(seed):
         assert np.all(w[32 * s: 32 * s + 32] == sc[s] - m[s]), s
 
 
+def test_q5_k_uniform_block_closed_form():
+    for q, a, b in [(0, 0, 0), (31, 63, 0), (16, 1, 63), (31, 63, 63), (17, 40, 17)]:
+        blk = _pack_q5_k(0.5, 0.25, [a] * 8, [b] * 8, [q] * 256)
+        w = kq.dequant_q5_k(blk, 1)[0]
+        assert np.all(w == 0.5 * a * q - 0.25 * b), (q, a, b)
+
+
+def test_q5_k_every_code_lands_on_its_weight():
+    # 1 (low bits only) and 16 (fifth bit only) at one weight at a time
+    for v in (1, 16):
+        for i in range(256):
+            q = [0] * 256
+            q[i] = v
+            w = kq.dequant_q5_k(_pack_q5_k(1.0, 0.0, [1] * 8, [0] * 8, q), 1)[0]
+            assert w[i] == float(v) and np.count_nonzero(w) == 1, (v, i)
+    # the fifth bit of weight 64g + 32 + l is bit 2g + 1 of qh byte l
+    q = [0] * 256
+    q[128 + 32 + 7] = 16
+    assert _pack_q5_k(1.0, 0.0, [1] * 8, [0] * 8, q)[16 + 7] == 1 << 5
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_q5_k_scales_and_minimums_as_q4_k(seed):
+    rng = np.random.default_rng(10 + seed)
+    sc = [int(v) for v in rng.integers(0, 64, 8)]
+    m = [int(v) for v in rng.integers(0, 64, 8)]
+    w = kq.dequant_q5_k(_pack_q5_k(1.0, 1.0, sc, m, [17] * 256), 1)[0]
+    for s_ in range(8):
+        assert np.all(w[32 * s_: 32 * s_ + 32] == 17 * sc[s_] - m[s_]), s_
+
+
 def test_q6_k_uniform_block_closed_form():
     for c, a in [(32, 5), (0, 1), (63, -128), (40, 127), (31, -3)]:
         blk = _pack_q6_k(0.125, [a] * 16, [c] * 256)
@@ -125,7 +170,7 @@ def test_fp16_scales_are_little_endian():
     assert np.all(kq.dequant_q4_k(blk, 1)[0] == 0.5)
 
 
-@pytest.mark.parametrize("fmt", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("fmt", ["q4_k", "q5_k", "q6_k"])
 def test_gemv_exact_against_fractions(fmt):
     rows, cols = 3, 512
     b = synth.kquant_matrix(synth.stream_key("kq-pin", fmt), rows, cols, fmt)
@@ -136,7 +181,7 @@ def test_gemv_exact_against_fractions(fmt):
         exact = sum(Fraction(float(w[r, c])) * Fraction(float(x[c])) for c in range(cols))
         assert abs(Fraction(float(y[r])) - exact) <= abs(exact) * Fraction(1, 10 ** 12) + Fraction(1, 10 ** 15)
     # rows come out in order: row r of the matrix is super-blocks r*cols/256 ..
-    one = kq.dequant_blocks(b[(cols // 256) * 144 if fmt == "q4_k" else (cols // 256) * 210:], cols // 256, fmt)
+    one = kq.dequant_blocks(b[(cols // 256) * kq.BLOCK_BYTES[fmt]:], cols // 256, fmt)
     assert np.array_equal(one.reshape(-1), w[1])
 
 
@@ -149,11 +194,13 @@ def test_rejects_ragged_columns():
 # make at least one of the pins above fail.
 _MUTANTS = [
     ("((b[:, s] >> 6) << 4)", "((b[:, s - 4] >> 6) << 4)"),                       # minimum's top bits from the wrong byte
-    ("qs[:, 32 * g: 32 * g + 32] >> 4", "qs[:, 32 * g: 32 * g + 32] & 0x0F"),     # high nibble read as low
+    ("= qs[:, 32 * g: 32 * g + 32] >> 4", "= qs[:, 32 * g: 32 * g + 32] & 0x0F"),  # high nibble read as low
     (">> (2 * g)) & 3", ">> (2 * (g ^ 1))) & 3"),                                 # Q6_K high bits of the wrong group
     ("np.arange(QK) // 16]", "np.arange(QK) // 16 ^ 1]"),                         # neighbouring Q6_K scale
     ("low = src & 0x0F if g < 2 else src >> 4", "low = src & 0x0F if g % 2 == 0 else src >> 4"),
-    ("- dmin[:, None] * m[:, sub]", "+ dmin[:, None] * m[:, sub]"),               # minimum's sign
+    ("- dmin[:, None] * m[:, sub]\n\n\ndef dequant_q5_k", "+ dmin[:, None] * m[:, sub]\n\n\ndef dequant_q5_k"),  # minimum's sign
+    ("(((qh >> (2 * g)) & 1) << 4)", "(((qh >> (2 * g + 1)) & 1) << 4)"),        # Q5_K fifth bit of the wrong weight
+    ("qh = b[:, 16:48]", "qh = b[:, 48:80]"),                                      # Q5_K field offsets
 ]
 
 
@@ -170,7 +217,9 @@ def test_pins_catch_planted_mistakes(old, new, monkeypatch):
     monkeypatch.setattr(sys.modules[__name__], "kq", mutant)
     pins = [test_q4_k_uniform_block_closed_form, test_q4_k_every_nibble_lands_on_its_weight,
             lambda: test_q4_k_six_bit_scales_and_minimums(0), test_q6_k_uniform_block_closed_form,
-            test_q6_k_every_code_lands_on_its_weight, test_q6_k_scale_k_covers_weights_16k_to_16k_plus_15]
+            test_q6_k_every_code_lands_on_its_weight, test_q6_k_scale_k_covers_weights_16k_to_16k_plus_15,
+            test_q5_k_uniform_block_closed_form, test_q5_k_every_code_lands_on_its_weight,
+            lambda: test_q5_k_scales_and_minimums_as_q4_k(0)]
     failed = 0
     for pin in pins:
         try:
