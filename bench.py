@@ -393,7 +393,7 @@ def run_kquant(args):
     L2 = 129 * 2 ** 20
     res = {}
     with ClockSampler(0) as clk:
-        for fmt in ("q4_k", "q6_k"):
+        for fmt in ("q4_k", "q5_k", "q6_k"):
             for name, (rows, cols) in KQ_SHAPES_70B.items():
                 if args.kq_only and args.kq_only != f"{fmt}:{rows}x{cols}":
                     continue

@@ -220,10 +220,10 @@ cudaError_t rgemv_setup_attributes();
 cudaError_t launch_rgemv(int wtype, int pro, int epi, const RgArgs& a, const RgLaunch& l, cudaStream_t s);
 
 // ---- K-quant dequant-GEMV (Q4_K, Q6_K; kquant.cu) ------------------------------
-enum KqFormat { KQ_Q4_K = 12, KQ_Q6_K = 14 };  // the GGUF type ids
+enum KqFormat { KQ_Q4_K = 12, KQ_Q5_K = 13, KQ_Q6_K = 14 };  // the GGUF type ids
 
 struct KqArgs {
-  const uint8_t* w;   // packed super-blocks (Q4_K 144 bytes, Q6_K 208 bytes each), row-major
+  const uint8_t* w;   // packed super-blocks (Q4_K 144, Q5_K 176, Q6_K 208 bytes each), row-major
   const __half* d6;   // Q6_K: super-block scales [rows][nsb rounded up to 8]; unused for Q4_K
   int rows, cols;     // cols a multiple of 256
   const float* x;     // [cols], 16-byte aligned

@@ -45,7 +45,7 @@ constexpr int kMaxWarps = 31;
 constexpr int kMaxWarpsMC = 8;
 template <int FMT, int MC>
 struct KqBounds {
-  static constexpr int threads = MC > 1 ? 32 * (kMaxWarpsMC + 1) : FMT == KQ_Q4_K ? 1024 : 512;
+  static constexpr int threads = MC > 1 ? 32 * (kMaxWarpsMC + 1) : FMT != KQ_Q6_K ? 1024 : 512;
 };
 constexpr int kRB = 64;              // rows per reduction block
 constexpr int kStageBytes = 16384;   // target code bytes per ring stage
@@ -59,11 +59,12 @@ struct KqShared {
 
 template <int FMT>
 struct KqGeo {
-  static constexpr int UPB = FMT == KQ_Q4_K ? 8 : 4;        // units per super-block
-  static constexpr int NP = FMT == KQ_Q4_K ? 16 : 32;       // int16 pairs per unit
-  static constexpr int NG = FMT == KQ_Q4_K ? 2 : 4;         // scale groups per unit
-  static constexpr int SB = FMT == KQ_Q4_K ? 144 : 208;     // packed super-block bytes
-  static constexpr int MCMAX = FMT == KQ_Q4_K ? 4 : 2;      // units per lane (registers)
+  static constexpr bool K4 = FMT != KQ_Q6_K;               // Q4_K and Q5_K share the unit geometry
+  static constexpr int UPB = K4 ? 8 : 4;                    // units per super-block
+  static constexpr int NP = K4 ? 16 : 32;                   // int16 pairs per unit
+  static constexpr int NG = K4 ? 2 : 4;                     // scale groups per unit
+  static constexpr int SB = FMT == KQ_Q4_K ? 144 : FMT == KQ_Q5_K ? 176 : 208;  // packed super-block bytes
+  static constexpr int MCMAX = K4 ? 4 : 2;                  // units per lane (registers)
 };
 
 template <int FMT>
@@ -82,7 +83,7 @@ __device__ __forceinline__ uint32_t byte_of(const uint4& v, int i) {
 // The element offsets (within the row) of one unit's groups of 16.
 template <int FMT>
 __device__ __forceinline__ int group_col(int unit, int g) {
-  if (FMT == KQ_Q4_K) {
+  if (FMT != KQ_Q6_K) {
     const int sb = unit >> 3, v = unit & 7, gg = v >> 1, l0 = (v & 1) * 16;
     return sb * 256 + 64 * gg + 32 * g + l0;        // g = 0: low nibbles, g = 1: high nibbles
   } else {
@@ -161,7 +162,11 @@ __device__ __forceinline__ Q4kSel q4k_sel(int lane) {
 }
 
 // One Q4_K unit of one row: codes at qa (16 bytes), super-block head at ma.
-__device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, const Q4kSel& sel, const KqX<KQ_Q4_K>& xq) {
+// Q5_K (FIFTH): the fifth code bits at ha, bit 2g of byte l for the low
+// nibbles' weights and bit 2g + 1 for the high nibbles'.
+template <bool FIFTH, int FMT>
+__device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, uint32_t ha, int g, const Q4kSel& sel,
+                                           const KqX<FMT>& xq) {
   const uint4 q = lds128(qa);
   const uint4 m = lds128(ma);
   const float d = __half2float(__ushort_as_half((unsigned short)(m.x & 0xFFFF)));
@@ -178,8 +183,18 @@ __device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, const Q4kSe
     lo[k] = w[k] & 0x0F0F0F0Fu;
     hi[k] = (w[k] >> 4) & 0x0F0F0F0Fu;
   }
+  if constexpr (FIFTH) {
+    const uint4 h = lds128(ha);
+    const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      lo[k] |= ((hw[k] >> (2 * g)) & 0x01010101u) << 4;
+      hi[k] |= ((hw[k] >> (2 * g + 1)) & 0x01010101u) << 4;
+    }
+  }
   const int ia = dot16(lo, xq.p), ib = dot16(hi, xq.p + 8);
-  // exact in int32: |sc * I| <= 63 * 16 * 15 * 32767, |m * S| <= 63 * 16 * 32767
+  // exact in int32: |sc * I| <= 63 * 16 * 31 * 32767 (twice that < 2^31),
+  // |m * S| <= 63 * 16 * 32767
   const int isc = (int)(v & 0xFFu) * ia + (int)((v >> 8) & 0xFFu) * ib;
   const int imn = (int)((v >> 16) & 0xFFu) * xq.sum[0] + (int)(v >> 24) * xq.sum[1];
   return xq.s * fmaf(d, (float)isc, -dmin * (float)imn);
@@ -301,7 +316,12 @@ __global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC>::threads) kq_gemv_k
             if constexpr (FMT == KQ_Q4_K) {
               const int sb = unit >> 3, v = unit & 7;
               const uint32_t blk = rowa + (uint32_t)sb * 144;
-              t = unit_q4_k(blk + 16 + 32 * (v >> 1) + 16 * (v & 1), blk, qsel, xq[k]);
+              t = unit_q4_k<false>(blk + 16 + 32 * (v >> 1) + 16 * (v & 1), blk, 0u, 0, qsel, xq[k]);
+            } else if constexpr (FMT == KQ_Q5_K) {
+              const int sb = unit >> 3, v = unit & 7;
+              const uint32_t blk = rowa + (uint32_t)sb * 176;
+              t = unit_q4_k<true>(blk + 48 + 32 * (v >> 1) + 16 * (v & 1), blk, blk + 16 + 16 * (v & 1), v >> 1, qsel,
+                                  xq[k]);
             } else {
               const int sb = unit >> 2, v = unit & 3, h = v >> 1, l0 = (v & 1) * 16;
               const uint32_t blk = rowa + (uint32_t)sb * 208;
@@ -353,6 +373,10 @@ KqFn kq_pick(int fmt, int rs, int mc) {
     if (mc <= 1) return kq_pick_rs<KQ_Q4_K, 1>(rs);
     if (mc <= 2) return kq_pick_rs<KQ_Q4_K, 2>(rs);
     if (mc <= 4) return kq_pick_rs<KQ_Q4_K, 4>(rs);
+  } else if (fmt == KQ_Q5_K) {
+    if (mc <= 1) return kq_pick_rs<KQ_Q5_K, 1>(rs);
+    if (mc <= 2) return kq_pick_rs<KQ_Q5_K, 2>(rs);
+    if (mc <= 4) return kq_pick_rs<KQ_Q5_K, 4>(rs);
   } else if (fmt == KQ_Q6_K) {
     if (mc <= 1) return kq_pick_rs<KQ_Q6_K, 1>(rs);
     if (mc <= 2) return kq_pick_rs<KQ_Q6_K, 2>(rs);
@@ -385,6 +409,7 @@ __global__ void kq_pack_q6_k_kernel(const uint8_t* src, int rows, int nsb, uint8
 size_t kq_packed_bytes(int fmt, int rows, int cols) {
   const size_t nsb = (size_t)cols / 256, nsb_pad = (nsb + 7) & ~(size_t)7;
   if (fmt == KQ_Q4_K) return (size_t)rows * nsb * 144;
+  if (fmt == KQ_Q5_K) return (size_t)rows * nsb * 176;
   const size_t main = ((size_t)rows * nsb * 208 + 255) & ~(size_t)255;
   return main + (size_t)rows * nsb_pad * 2;
 }
@@ -396,7 +421,7 @@ const __half* kq_d6(const void* packed, int rows, int cols) {
 }
 
 cudaError_t launch_kq_pack(int fmt, const void* blocks, int rows, int cols, void* packed, cudaStream_t s) {
-  if (fmt == KQ_Q4_K)
+  if (fmt == KQ_Q4_K || fmt == KQ_Q5_K)
     return cudaMemcpyAsync(packed, blocks, kq_packed_bytes(fmt, rows, cols), cudaMemcpyDeviceToDevice, s);
   const int nsb = cols / 256;
   uint8_t* dst = static_cast<uint8_t*>(packed);
@@ -412,10 +437,11 @@ cudaError_t launch_kq_pack(int fmt, const void* blocks, int rows, int cols, void
 
 KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms) {
   KqLaunch l{};
-  if ((fmt != KQ_Q4_K && fmt != KQ_Q6_K) || cols % 256 || cols <= 0 || rows <= 0) return l;
+  if ((fmt != KQ_Q4_K && fmt != KQ_Q5_K && fmt != KQ_Q6_K) || cols % 256 || cols <= 0 || rows <= 0) return l;
   const int nsb = cols / 256;
-  const int upb = fmt == KQ_Q4_K ? 8 : 4, mcmax = fmt == KQ_Q4_K ? 4 : 2;
-  const int max1 = (fmt == KQ_Q4_K ? 1024 : 512) / 32 - 1;  // consumer warps at one unit per lane
+  const bool k4 = fmt != KQ_Q6_K;
+  const int upb = k4 ? 8 : 4, mcmax = k4 ? 4 : 2;
+  const int max1 = (k4 ? 1024 : 512) / 32 - 1;  // consumer warps at one unit per lane
   const int nchunk = (nsb * upb + 31) / 32;
   int nwc = 0, mc = 0;
   if (nchunk <= max1) {
@@ -428,7 +454,7 @@ KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms) {
     mc = (nchunk + nwc - 1) / nwc;
   }
   if (mc > mcmax) return l;
-  const int row_bytes = nsb * (fmt == KQ_Q4_K ? 144 : 208);
+  const int row_bytes = nsb * (fmt == KQ_Q4_K ? 144 : fmt == KQ_Q5_K ? 176 : 208);
   const int drow = fmt == KQ_Q6_K ? ((nsb + 7) & ~7) * 2 : 0;
   int rs = 1;
   while (rs < 8 && (rs * 2) * row_bytes <= kStageBytes) rs *= 2;
@@ -467,7 +493,7 @@ KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms) {
 }
 
 cudaError_t kq_setup_attributes() {
-  for (int fmt : {(int)KQ_Q4_K, (int)KQ_Q6_K})
+  for (int fmt : {(int)KQ_Q4_K, (int)KQ_Q5_K, (int)KQ_Q6_K})
     for (int rs : {1, 2, 4, 8})
       for (int mc : {1, 2, 4}) {
         KqFn f = kq_pick(fmt, rs, mc);
@@ -495,7 +521,7 @@ cudaError_t launch_kq_gemv(int fmt, const KqArgs& a, const KqLaunch& l, cudaStre
 
 namespace {
 
-bool kq_type_ok(int32_t type) { return type == DLS_Q4_K || type == DLS_Q6_K; }
+bool kq_type_ok(int32_t type) { return type == DLS_Q4_K || type == DLS_Q5_K || type == DLS_Q6_K; }
 
 std::mutex g_kq_mu;
 std::map<std::tuple<int, int, int, int>, dls::KqLaunch> g_kq_plans;  // (device, type, rows, cols)

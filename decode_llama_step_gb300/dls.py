@@ -179,8 +179,9 @@ def attention_decode_noalloc(q, k_pages, v_pages, page_table, lengths, o, n_batc
 
 
 DLS_Q4_K = 12
+DLS_Q5_K = 13
 DLS_Q6_K = 14
-KQUANT_TYPES = {"q4_k": DLS_Q4_K, "q6_k": DLS_Q6_K}
+KQUANT_TYPES = {"q4_k": DLS_Q4_K, "q5_k": DLS_Q5_K, "q6_k": DLS_Q6_K}
 
 
 def kquant_packed_bytes(fmt: str, rows: int, cols: int) -> int:

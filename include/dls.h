@@ -334,16 +334,19 @@ int dls_attention_decode_noalloc(const float* q, const void* k_pages, const void
                                  int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t page_tokens,
                                  int32_t max_pages, int32_t n_splits, void* cuda_stream);
 
-/* ---- K-quant dequant-GEMV (the engine page, section 1: Q4_K_M and Q6_K) -------- */
+/* ---- K-quant dequant-GEMV (the engine page, section 1: Q4_K_M, Q5_K, Q6_K) ----- */
 
 /* GGUF K-quant types: 256 weights per super-block; Q4_K 144 bytes (fp16 d,
  * fp16 dmin, twelve bytes of 6-bit sub-block scales and minimums, 128 bytes
- * of 4-bit codes; weight = d*sc*q - dmin*m per sub-block of 32), Q6_K 210
+ * of 4-bit codes; weight = d*sc*q - dmin*m per sub-block of 32), Q5_K 176
+ * bytes (Q4_K's first 16, then 32 bytes holding a fifth code bit per weight,
+ * then the 128 bytes of low 4 bits; the same weight formula), Q6_K 210
  * bytes (128 bytes of low code bits, 64 of high bits, sixteen int8 scales,
  * fp16 d; weight = d*scale*(code - 32) per group of 16).  A [rows][cols]
  * matrix is row-major with cols/256 super-blocks per row (cols a multiple of
  * 256). */
 #define DLS_Q4_K 12
+#define DLS_Q5_K 13
 #define DLS_Q6_K 14
 
 /* Bytes of the device layout dls_kquant_gemv reads (0 for a bad type or
@@ -352,14 +355,14 @@ uint64_t dls_kquant_packed_bytes(int32_t type, int32_t rows, int32_t cols);
 
 /* Lay out `blocks` (device, GGUF super-blocks as above) for the GEMV into
  * `packed` (device, 256-byte aligned, dls_kquant_packed_bytes bytes, owned by
- * the caller): Q4_K as it is; Q6_K with the fp16 scales moved to a separate
+ * the caller): Q4_K and Q5_K as they are; Q6_K with the fp16 scales moved to a separate
  * array so that every row is 16-byte aligned.  Enqueued on cuda_stream. */
 int dls_kquant_pack(int32_t type, const void* blocks, int32_t rows, int32_t cols, void* packed, void* cuda_stream);
 
 /* y = W x, the decode step's projection on a K-quant matrix: x device fp32
  * [cols] (16-byte aligned), y device fp32 [rows], packed from
  * dls_kquant_pack.  Each weight row streams through shared memory once;
- * activations are held as int16 slices with one scale per 32 (Q4_K) or 64
+ * activations are held as int16 slices with one scale per 32 (Q4_K, Q5_K) or 64
  * (Q6_K) columns, so the code-activation products are exact int32 and the
  * result is within 2^-16 of each slice's largest activation of the exact
  * product.  status (device int32, or NULL) gets bit 8 or-ed in when a

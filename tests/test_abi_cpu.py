@@ -118,15 +118,16 @@ def test_null_model_calls_of_the_later_entry_points(lib):
 def test_kquant_layout_sizes_and_argument_checks(lib):
     # Q4_K: the GGUF super-blocks as they are (144 bytes per 256 weights)
     assert lib.dls_kquant_packed_bytes(dls.DLS_Q4_K, 3, 512) == 3 * 2 * 144
+    assert lib.dls_kquant_packed_bytes(dls.DLS_Q5_K, 3, 512) == 3 * 2 * 176
     # Q6_K: 208 bytes per super-block, 256-byte aligned, then fp16 scales
     # with each row padded to 8 super-blocks
     rows, nsb = 5, 17
     main = (rows * nsb * 208 + 255) // 256 * 256
     assert lib.dls_kquant_packed_bytes(dls.DLS_Q6_K, rows, nsb * 256) == main + rows * 24 * 2
-    for bad in [(dls.DLS_Q4_K, 3, 300), (dls.DLS_Q4_K, 0, 256), (13, 4, 256), (dls.DLS_Q6_K, 4, 0)]:
+    for bad in [(dls.DLS_Q4_K, 3, 300), (dls.DLS_Q4_K, 0, 256), (15, 4, 256), (dls.DLS_Q6_K, 4, 0)]:
         assert lib.dls_kquant_packed_bytes(*bad) == 0
     # rejected before any CUDA call
-    assert lib.dls_kquant_gemv(13, 256, 4, 256, 256, 256, None, None) == dls.DLS_ERR_ARG
+    assert lib.dls_kquant_gemv(15, 256, 4, 256, 256, 256, None, None) == dls.DLS_ERR_ARG
     assert lib.dls_kquant_gemv(dls.DLS_Q4_K, None, 4, 256, 256, 256, None, None) == dls.DLS_ERR_ARG
     assert lib.dls_kquant_gemv(dls.DLS_Q4_K, 256, 4, 300, 256, 256, None, None) == dls.DLS_ERR_ARG
     assert lib.dls_kquant_gemv(dls.DLS_Q4_K, 256 + 16, 4, 256, 256, 256, None, None) == dls.DLS_ERR_ARG

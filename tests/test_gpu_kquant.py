@@ -1,4 +1,4 @@
-"""GPU parity of the K-quant dequant-GEMV (Q4_K, Q6_K) against the oracle,
+"""GPU parity of the K-quant dequant-GEMV (Q4_K, Q5_K, Q6_K) against the oracle,
 through the C ABI: the device layout byte for byte, y = W x on small and
 ragged shapes in full, and on the 70B projection shapes on sampled rows."""
 import numpy as np
@@ -41,7 +41,7 @@ def _bound(w, x):
     return 0.5 * step * np.abs(w).sum(axis=-1) * 1.001 + 2e-6 * np.abs(w * x).sum(axis=-1) + 1e-6
 
 
-@pytest.mark.parametrize("fmt", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("fmt", ["q4_k", "q5_k", "q6_k"])
 @pytest.mark.parametrize("rows,cols", [(1, 256), (37, 512), (300, 2048), (129, 4352), (1000, 8192),
                                        (5, 28672)])
 def test_kquant_gemv_matches_oracle(fmt, rows, cols):
@@ -52,13 +52,13 @@ def test_kquant_gemv_matches_oracle(fmt, rows, cols):
     assert np.all(err <= _bound(w, x.astype(np.float64))), f"max err {err.max():.3e}"
 
 
-@pytest.mark.parametrize("fmt", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("fmt", ["q4_k", "q5_k", "q6_k"])
 def test_kquant_packed_layout_bytes(fmt):
     rows, cols = 9, 4352                             # 17 super-blocks: the Q6_K scale rows are padded
     blocks, _, packed, _ = _setup(fmt, rows, cols)
     nsb = cols // 256
     raw = blocks.reshape(rows * nsb, kq.BLOCK_BYTES[fmt])
-    if fmt == "q4_k":
+    if fmt in ("q4_k", "q5_k"):
         assert np.array_equal(packed, blocks)
         return
     main = packed[: rows * nsb * 208].reshape(rows * nsb, 208)
@@ -70,7 +70,7 @@ def test_kquant_packed_layout_bytes(fmt):
     assert not d[:, nsb:, :].any()
 
 
-@pytest.mark.parametrize("fmt", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("fmt", ["q4_k", "q5_k", "q6_k"])
 @pytest.mark.parametrize("rows,cols", [(8192, 8192), (28672, 8192), (8192, 28672)])
 def test_kquant_gemv_70b_shapes_sampled_rows(fmt, rows, cols):
     blocks, x, _, y = _setup(fmt, rows, cols, seed=1)
