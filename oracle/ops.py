@@ -81,6 +81,47 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
     return o
 
 
+def attention_partial(q: np.ndarray, k: np.ndarray, v: np.ndarray):
+    """The softmax statistics of one query position over a subset of its keys
+    (the form in which attention over a shared prefix and over each branch's
+    own positions are computed apart and then merged: cascade attention for
+    the branches of a fork, which read one prefix).
+
+    q: [n_heads, hd]; k, v: [n, n_kv_heads, hd] (n may be 0).  Returns
+    (o, m, l): per head the running maximum m of the scaled scores, the sum
+    l of exp(score - m) and the unnormalised o = sum exp(score - m) v; an
+    empty key set gives m = -inf, l = 0, o = 0.
+    """
+    nh, hd = q.shape
+    nkv = k.shape[1]
+    g = nh // nkv
+    o = np.zeros((nh, hd), dtype=np.float64)
+    m = np.full(nh, -np.inf)
+    l = np.zeros(nh)
+    if k.shape[0] == 0:
+        return o, m, l
+    for h in range(nh):
+        kv = h // g
+        s = k[:, kv, :] @ q[h] / np.sqrt(hd)
+        m[h] = np.max(s)
+        e = np.exp(s - m[h])
+        l[h] = np.sum(e)
+        o[h] = e @ v[:, kv, :]
+    return o, m, l
+
+
+def merge_partials(parts) -> np.ndarray:
+    """Attention output from the statistics of disjoint key subsets that
+    together cover the key range: rescale every part to the common maximum
+    and divide the summed outputs by the summed weights."""
+    ms = np.stack([p[1] for p in parts])                 # [parts, n_heads]
+    mx = np.max(ms, axis=0)
+    scale = np.where(np.isfinite(ms), np.exp(ms - mx[None, :]), 0.0)
+    o = sum(sc[:, None] * p[0] for sc, p in zip(scale, parts))
+    l = sum(sc * p[2] for sc, p in zip(scale, parts))
+    return o / l[:, None]
+
+
 def causal_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos0: int = 0) -> np.ndarray:
     """Attention of T query positions q_pos0 .. q_pos0+T-1 over keys 0..n-1.
 

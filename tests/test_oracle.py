@@ -567,3 +567,50 @@ def test_speculative_acceptance_matches_brute_force(skip, k):
         drafted += r
     assert (st["rounds"], st["drafted"], st["accepted"]) == (rounds, drafted, accepted)
     assert accepted < drafted       # this draft is wrong somewhere, so rejection is exercised
+
+
+# ---------------------------------------------------------------- split softmax (cascade attention over a shared prefix)
+
+@pytest.mark.parametrize("cuts", [[], [0], [5], [1, 2, 9], [11], [3, 3, 7]])
+def test_merged_partials_equal_attention_over_all_keys(cuts):
+    rng = np.random.default_rng(len(cuts) + sum(cuts))
+    nh, nkv, hd, n = 4, 2, 16, 11
+    q = rng.normal(size=(nh, hd))
+    k = rng.normal(size=(n, nkv, hd)) * 2.0
+    v = rng.normal(size=(n, nkv, hd))
+    bounds = [0] + list(cuts) + [n]
+    parts = [ops.attention_partial(q, k[a:b], v[a:b]) for a, b in zip(bounds[:-1], bounds[1:])]
+    np.testing.assert_allclose(ops.merge_partials(parts), ops.attention(q, k, v), rtol=1e-12, atol=1e-14)
+    # the order of the parts does not matter
+    np.testing.assert_allclose(ops.merge_partials(parts[::-1]), ops.attention(q, k, v), rtol=1e-12, atol=1e-14)
+
+
+def test_partial_of_one_key_and_of_none():
+    q = np.array([[1.0, 0.0], [0.0, 2.0]])
+    k = np.array([[[3.0, 4.0]]])
+    v = np.array([[[5.0, -6.0]]])
+    o, m, l = ops.attention_partial(q, k, v)
+    # one key: the score itself is the maximum, its weight exp(0) = 1
+    assert list(m) == pytest.approx([3.0 / np.sqrt(2.0), 8.0 / np.sqrt(2.0)], rel=1e-15)
+    assert list(l) == [1.0, 1.0]
+    np.testing.assert_array_equal(o, [[5.0, -6.0], [5.0, -6.0]])
+    o0, m0, l0 = ops.attention_partial(q, k[:0], v[:0])
+    assert np.all(m0 == -np.inf) and np.all(l0 == 0) and np.all(o0 == 0)
+
+
+def test_prefix_and_branch_parts_rebuild_a_forked_decode_step():
+    # a fork's branch attends over the shared prefix and its own positions:
+    # the two parts merged give the oracle's decode-step attention
+    cfg, w = _micro_weights()
+    m = OracleModel(cfg, w)
+    toks = synth.prompt_tokens(cfg, 9)
+    base = m.new_seq()
+    m.prefill(base, toks[:6])
+    br = base.fork()
+    for i, t in enumerate(toks[6:]):
+        m.decode_step(br, int(t), 6 + i)
+    q = synth.normal(77, cfg.n_heads * cfg.head_dim).reshape(cfg.n_heads, cfg.head_dim)
+    k, v = br.keys(1), br.values(1)
+    whole = ops.attention(q, k, v)
+    merged = ops.merge_partials([ops.attention_partial(q, k[:6], v[:6]), ops.attention_partial(q, k[6:], v[6:])])
+    np.testing.assert_allclose(merged, whole, rtol=1e-12, atol=1e-14)
