@@ -184,6 +184,61 @@ def test_8b_decode_at_context(gpu_lib, w8b, ctx):
         release(m)
 
 
+def test_8b_layer_skip_and_speculative_at_full_size(gpu_lib, w8b):
+    """The 8B Q8_0 model at ctx 2048, as the skip and spec workloads run it:
+    the calibration's cosines are finite and in [-1, 1]; self-speculative
+    greedy generation (the calibrated layers as the draft's skips, draft
+    lengths 1, 3 and 9, so both verify forms) gives the library's own plain
+    greedy tokens up to the first step whose top-2 logit gap is within 1e-3
+    (a property that holds at any size; the tiny tests pin both to the
+    oracle); with every layer skipped, a decode step's logits are the LM
+    head of the embedding row (checked against the oracle on sampled vocab
+    rows)."""
+    torch = _torch()
+    cfg, w = w8b
+    P, N = 2048, 24
+    prompt = synth.prompt_tokens(cfg, P, seed=1)
+    m, stream = gpu_model(cfg, w, max_seqs=3, max_ctx=P + N + 32)
+    try:
+        base, a, b = m.seq_create(), m.seq_create(), m.seq_create()
+        lg = torch.empty(cfg.vocab, device="cuda")
+        m.prefill(base, prompt, lg)
+        tok = int(torch.argmax(lg).item())
+        m.kv_fork(base, [a])
+        cos = m.layer_cosines(a, tok, P)
+        assert np.all(np.isfinite(cos)) and np.all(np.abs(cos) <= 1.0 + 1e-5)
+        mask = cos > 0.98
+        # plain greedy with per-step logits (gaps)
+        m.kv_fork(base, [a])
+        plain, gaps, t = [], [], tok
+        for i in range(N):
+            m.decode_step(a, t, P + i, lg)
+            g = host(lg, stream)
+            top = np.sort(g)[-2:]
+            gaps.append(top[1] - top[0])
+            t = int(np.argmax(g))
+            plain.append(t)
+        agree = next((i for i in range(N) if gaps[i] <= 1e-3), N)
+        for k in (1, 3, 9):
+            m.kv_fork(base, [b])
+            toks, st = m.generate_speculative(b, tok, N, mask, k)
+            assert st["rounds"] + st["accepted"] == N
+            assert list(toks[:agree]) == plain[:agree], f"k={k}"
+            assert m.seq_length(b) == P + N
+        # every layer skipped: embedding -> final norm -> LM head
+        m.kv_fork(base, [a])
+        m.set_layer_skip([True] * cfg.n_layers)
+        m.decode_step(a, tok, P, lg)
+        got = host(lg, stream)
+        m.set_layer_skip(None)
+        orc = OracleModel(cfg, w, cache_bytes=0)
+        rows = np.unique(np.concatenate([[int(np.argmax(got))], np.random.default_rng(3).integers(0, cfg.vocab, 64)]))
+        ref = orc.final_logits(orc.embed(tok), rows=rows)
+        assert_close(got[rows], ref, "all layers skipped: LM head of the embedding")
+    finally:
+        release(m)
+
+
 def test_fork_8b_q4_0_prefix_4096_eight_branches(gpu_lib):
     """8B shape, Q4_0: one prefill of a 4096-token seeded prefix, a KV fork
     into 8 branch slots, then batch-8 greedy decode of 128 tokens from each
