@@ -289,6 +289,7 @@ def test_silu_closed_forms():
                                [1.5 * math.log(3.0)], rtol=1e-15)
 
 
+@pytest.mark.filterwarnings("ignore:overflow encountered in cast")  # values past the fp16 range, on purpose
 def test_round_f16_nearest_even():
     # 1 + 2^-11 is halfway between 1 and 1 + 2^-10 -> ties to even (1.0);
     # 1 + 3*2^-11 -> 1 + 2^-9 (even mantissa)

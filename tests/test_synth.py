@@ -1,5 +1,6 @@
 """The seeded input generator: determinism, distribution, formats.  CPU only."""
 import numpy as np
+import pytest
 
 import synth
 from synth.configs import CONFIGS
@@ -29,6 +30,7 @@ def test_quant_matrix_matches_quantize_of_normals():
         np.testing.assert_array_equal(synth.quant_matrix(key, rows, cols, 0.02, wt), synth.quantize(x, wt))
 
 
+@pytest.mark.filterwarnings("ignore:overflow encountered in cast")  # values past the fp16 range, on purpose
 def test_f16_conversion_matches_numpy():
     v = np.concatenate([synth.normal(3, 20000, 1.0), synth.normal(4, 20000, 1e-5),
                         synth.normal(5, 2000, 3e4), [0.0, -0.0, 65504.0, 65519.99, 2 ** -25, 3 * 2 ** -26]])
