@@ -52,3 +52,35 @@ def test_prefill_flops_closed_form():
     att = 2 * 2 * 32 * 128 * pairs                             # QK^T and PV, 2 flops per multiply-add
     want = 32 * (2 * layer_params * T + att) + 2 * 128256 * 4096
     assert bench.prefill_flops(cfg, T) == want
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the reference arm (the oracle on the host cores) on the tiny shape: one
+    # JSON line with the keys the driver reads, the steps and warmup it ran
+    import json
+    import subprocess
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                          "--steps", "3", "--warmup", "1", "--ctx", "64"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "impl"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 1
+    assert d["value"] > 0 and d["unit"] == "tok/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert abs(d["ms_per_step"] - 1000.0 / d["value"]) <= 0.01 * d["ms_per_step"]
+
+
+def test_reference_arm_runs_on_rank_0_only():
+    import subprocess
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                          "--steps", "2", "--warmup", "0", "--ctx", "64", "--gpus", "2"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert not [l for l in out.stdout.splitlines() if l.startswith("{")]
