@@ -38,7 +38,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import ops, quant
+from . import kquant, ops, quant
 
 
 class OracleSeq:
@@ -113,6 +113,11 @@ class OracleModel:
     ``cfg`` needs: n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn,
     vocab, rope_theta, rms_eps, wtype, tied.  Dequantised matrices are cached
     up to ``cache_bytes``; larger models dequantise rows in chunks per call.
+
+    Every matrix is in the format ``cfg.wtype`` (8: Q8_0, 4: Q4_0) unless
+    ``weights["formats"]`` maps its (layer, name) to another: "q4_k", "q5_k"
+    or "q6_k" (a K-quant file mixes these per matrix, Q4_K_M for instance;
+    layer None for tok_embd and output).
     """
 
     def __init__(self, cfg, weights: dict, cache_bytes: int = 2 << 30, chunk_rows: int = 8192):
@@ -141,13 +146,24 @@ class OracleModel:
             raise ValueError(f"layer {layer} weights were not generated")
         return lw[name]
 
+    def _rows(self, layer, name, r0: int, r1: int) -> np.ndarray:
+        """Rows [r0, r1) of one matrix, dequantised from its own format."""
+        cols = self.shapes[name][1]
+        if name == "output" and layer is None and self.w.get("output") is None:
+            name = "tok_embd"
+        fmt = self.w.get("formats", {}).get((layer, name), self.cfg.wtype)
+        blocks = self._blocks(layer, name)
+        if fmt in (8, 4):
+            return quant.matrix_rows(blocks, cols, fmt, r0, r1)
+        return kquant.matrix_rows(blocks, cols, fmt, r0, r1)
+
     def matrix(self, layer, name) -> np.ndarray:
         """Dequantised fp64 [rows, cols] of one matrix (cached when it fits)."""
         key = (layer, name)
         if key in self._cache:
             return self._cache[key]
         rows, cols = self.shapes[name]
-        m = quant.matrix(self._blocks(layer, name), rows, cols, self.cfg.wtype)
+        m = self._rows(layer, name, 0, rows)
         if self._cached + m.nbytes <= self.cache_bytes:
             self._cache[key] = m
             self._cached += m.nbytes
@@ -158,19 +174,17 @@ class OracleModel:
         nrows, cols = self.shapes[name]
         key = (layer, name)
         if rows is not None:
-            blocks = self._blocks(layer, name)
             out = []
             for r in np.asarray(rows).ravel():
-                w = quant.matrix_rows(blocks, cols, self.cfg.wtype, int(r), int(r) + 1)
+                w = self._rows(layer, name, int(r), int(r) + 1)
                 out.append(x @ w[0])
             return np.stack(out, axis=-1)
         if key in self._cache or nrows * cols * 8 <= self.cache_bytes - self._cached:
             return x @ self.matrix(layer, name).T
-        blocks = self._blocks(layer, name)
         parts = []
         for r0 in range(0, nrows, self.chunk_rows):
             r1 = min(nrows, r0 + self.chunk_rows)
-            w = quant.matrix_rows(blocks, cols, self.cfg.wtype, r0, r1)
+            w = self._rows(layer, name, r0, r1)
             parts.append(x @ w.T)
         return np.concatenate(parts, axis=-1)
 
@@ -186,10 +200,8 @@ class OracleModel:
 
     def embed(self, tokens) -> np.ndarray:
         """Dequantised embedding rows: [T, hidden] (or [hidden] for one id)."""
-        cfg = self.cfg
         toks = np.atleast_1d(np.asarray(tokens))
-        rows = [quant.matrix_rows(self.w["tok_embd"], cfg.hidden, cfg.wtype, int(t), int(t) + 1)[0]
-                for t in toks]
+        rows = [self._rows(None, "tok_embd", int(t), int(t) + 1)[0] for t in toks]
         x = np.stack(rows)
         return x if np.ndim(tokens) else x[0]
 

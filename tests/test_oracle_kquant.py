@@ -227,3 +227,77 @@ def test_pins_catch_planted_mistakes(old, new, monkeypatch):
         except AssertionError:
             failed += 1
     assert failed >= 1
+
+
+# ---------------------------------------------------------------- K-quant matrices inside the model
+
+def _q4_0_and_q4_k(rng, rows, cols):
+    """The same weights as Q4_0 blocks and as Q4_K super-blocks: every Q4_0
+    block of a 256-column run shares one scale d, so the Q4_K form with
+    d, dmin = d, every sub-block scale 1 and minimum 8 gives d * (q - 8)
+    exactly, weight for weight."""
+    nsb = cols // 256
+    q = rng.integers(0, 16, size=(rows, cols))
+    d = (rng.uniform(0.5, 1.5, size=(rows, nsb)) * 2.0 ** -6).astype(np.float16).astype(np.float64)
+    q40 = np.zeros((rows, cols // 32, 18), dtype=np.uint8)
+    q4k = np.zeros((rows, nsb, 144), dtype=np.uint8)
+    for r in range(rows):
+        for b in range(cols // 32):
+            q40[r, b, 0:2] = _f16le(d[r, b // 8])
+            for j in range(16):
+                q40[r, b, 2 + j] = q[r, 32 * b + j] | (q[r, 32 * b + 16 + j] << 4)
+        for s_ in range(nsb):
+            q4k[r, s_] = _pack_q4_k(d[r, s_], d[r, s_], [1] * 8, [8] * 8, list(q[r, 256 * s_: 256 * s_ + 256]))
+    return q40.reshape(-1), q4k.reshape(-1)
+
+
+def test_a_q4_k_model_equals_the_q4_0_model_with_the_same_weights():
+    from oracle.model import OracleModel
+    from synth.configs import ModelConfig
+    cfg = ModelConfig("kqmix", 2, 256, 4, 2, 64, 512, 48, 10000.0, 4, 0.05)
+    rng = np.random.default_rng(5)
+    shapes = synth.matrix_shapes(cfg)
+    w40 = synth.model_weights(cfg)
+    wk = dict(w40, layers=[dict(lw) for lw in w40["layers"]], formats={})
+    for l in range(cfg.n_layers):
+        for name in synth.LAYER_MATRICES:
+            rows, cols = shapes[name]
+            a, b = _q4_0_and_q4_k(rng, rows, cols)
+            w40["layers"][l][name] = a
+            wk["layers"][l][name] = b
+            wk["formats"][(l, name)] = "q4_k"
+    m40, mk = OracleModel(cfg, w40), OracleModel(cfg, wk)
+    for l in range(cfg.n_layers):
+        for name in synth.LAYER_MATRICES:
+            assert np.array_equal(m40.matrix(l, name), mk.matrix(l, name)), (l, name)
+    # the same weights give the same model (up to the BLAS summation order,
+    # which may follow the arrays' placement in memory)
+    toks = synth.prompt_tokens(cfg, 5, seed=2)
+    s40, sk = m40.new_seq(), mk.new_seq()
+    np.testing.assert_allclose(m40.prefill(s40, toks), mk.prefill(sk, toks), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(m40.decode_step(s40, 7, 5), mk.decode_step(sk, 7, 5), rtol=1e-12, atol=1e-13)
+
+
+def test_a_mixed_k_quant_model_prefill_equals_sequential_decode():
+    # Q4_K_M-style mix: value and down projections Q6_K, the rest Q4_K / Q5_K
+    from oracle.model import OracleModel
+    from synth.configs import ModelConfig
+    cfg = ModelConfig("kqmix2", 2, 256, 4, 2, 64, 512, 48, 10000.0, 4, 0.05)
+    shapes = synth.matrix_shapes(cfg)
+    w = synth.model_weights(cfg)
+    w["formats"] = {}
+    for l in range(cfg.n_layers):
+        for name in synth.LAYER_MATRICES:
+            rows, cols = shapes[name]
+            fmt = "q6_k" if name in ("wv", "w_down") else ("q5_k" if l == 1 and name == "wq" else "q4_k")
+            w["layers"][l][name] = synth.kquant_matrix(synth.stream_key("kqmix2", l, name), rows, cols, fmt)
+            w["formats"][(l, name)] = fmt
+    m = OracleModel(cfg, w)
+    toks = synth.prompt_tokens(cfg, 6, seed=4)
+    s1, s2 = m.new_seq(), m.new_seq()
+    lg1 = m.prefill(s1, toks)
+    for i, t in enumerate(toks):
+        lg2 = m.decode_step(s2, int(t), i)
+    np.testing.assert_allclose(lg1, lg2, rtol=1e-12, atol=1e-13)
+    # and the matrices really are read in their own formats
+    assert np.array_equal(m.matrix(0, "wv"), kq.matrix_rows(w["layers"][0]["wv"], 256, "q6_k", 0, shapes["wv"][0]))
