@@ -11,8 +11,12 @@ weights (8.2 GB per token) are larger than L2, so no flush is needed between
 steps.
 
 Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on the
-same workload instead (bounded sample).  Under torchrun each rank runs an
-independent replica (decode does not shard); rank 0 prints.
+same workload instead (one layer of the step per sample).  Under torchrun
+each rank runs an independent replica (decode does not shard); rank 0
+prints.  ``--workload`` selects the secondary measurements: prefill, fork
+(shared-prefix fan-out), stream (70B with a device budget), skip (layer
+skip), spec (self-speculative decoding), kquant (K-quant GEMV bandwidth),
+batch (batched decode of 2/4/8 sequences).
 """
 from __future__ import annotations
 
