@@ -158,6 +158,26 @@ def model_weights(cfg: ModelConfig, layers=None) -> dict:
     return w
 
 
+def with_random_gains(w: dict, cfg: ModelConfig, sigma: float = 0.2, tag: str = "gains") -> dict:
+    """A copy of the weights `w` whose RMSNorm gains are seeded draws instead
+    of ones: every layer's attn_norm and ffn_norm and the output_norm, each
+    element N(1, sigma), stored fp32.  The matrices are shared with `w`."""
+    H = cfg.hidden
+    out = dict(w)
+    out["output_norm"] = (1.0 + normal(stream_key(cfg.name, tag, "output_norm"), H, sigma)).astype(np.float32)
+    layers = []
+    for l, lw in enumerate(w["layers"]):
+        if lw is None:
+            layers.append(None)
+            continue
+        lw = dict(lw)
+        for name in ("attn_norm", "ffn_norm"):
+            lw[name] = (1.0 + normal(stream_key(cfg.name, tag, l, name), H, sigma)).astype(np.float32)
+        layers.append(lw)
+    out["layers"] = layers
+    return out
+
+
 def prompt_tokens(cfg: ModelConfig, n: int, seed: int = 1) -> np.ndarray:
     return tokens(stream_key(cfg.name, "prompt", seed), n, cfg.vocab)
 

@@ -50,3 +50,21 @@ def test_config_parameter_counts():
     assert CONFIGS["8b"].layer_params() == 218_103_808
     assert CONFIGS["70b"].layer_params() == 855_638_016
     assert CONFIGS["1b"].layer_params() == 60_817_408
+
+
+def test_random_gains_are_seeded_and_leave_matrices_shared():
+    cfg = CONFIGS["tiny"]
+    w = synth.model_weights(cfg)
+    g1 = synth.with_random_gains(w, cfg)
+    g2 = synth.with_random_gains(w, cfg)
+    for l in range(cfg.n_layers):
+        a, f = g1["layers"][l]["attn_norm"], g1["layers"][l]["ffn_norm"]
+        assert a.dtype == np.float32 and a.shape == (cfg.hidden,)
+        np.testing.assert_array_equal(a, g2["layers"][l]["attn_norm"])
+        assert not np.array_equal(a, f)                       # distinct per norm
+        assert np.all(w["layers"][l]["attn_norm"] == 1.0)     # the source is untouched
+        assert g1["layers"][l]["wq"] is w["layers"][l]["wq"]
+    assert not np.array_equal(g1["layers"][0]["attn_norm"], g1["layers"][1]["attn_norm"])
+    allg = np.concatenate([g1["output_norm"]] + [g1["layers"][l][n] for l in range(cfg.n_layers)
+                                                 for n in ("attn_norm", "ffn_norm")])
+    assert abs(allg.mean() - 1.0) < 0.03 and abs(allg.std() - 0.2) < 0.03
