@@ -101,6 +101,7 @@ struct dls_model {
   dls_allocator alloc{};
   bool have_alloc = false;
   uint64_t used = 0, budget = 0;
+  uint64_t credit = 0;  // bytes an in-progress layout change will free (counted as gone by the ledger)
   std::vector<std::pair<void*, size_t>> allocs;
   // weights
   std::vector<uint8_t*> layer_dev, layer_host;
@@ -170,7 +171,7 @@ struct dls_model {
   float* capture = nullptr;
   int launches_per_step = 0;
   int launch_count = 0;
-  // persistent decode-step kernel (all layers resident, one row, no capture)
+  // persistent decode-step kernel (all layers resident, one row)
   StepPlan step{};
   bool use_step = false;
   bool step_graph_ok = true;  // false: the cooperative launch could not be captured; run it eagerly
@@ -234,7 +235,8 @@ int fail(dls_model* m, int code, const char* fmt, ...) {
 
 int dev_alloc(dls_model* m, size_t bytes, void** out, const char* what) {
   bytes = a256(bytes ? bytes : 256);
-  if (m->budget && (bytes > m->budget || m->used > m->budget - bytes))
+  const uint64_t used = m->used > m->credit ? m->used - m->credit : 0;
+  if (m->budget && (bytes > m->budget || used > m->budget - bytes))
     return fail(m, DLS_ERR_BUDGET, "what=%s bytes=%zu used=%llu budget=%llu", what, bytes,
                 (unsigned long long)m->used, (unsigned long long)m->budget);
   void* p = nullptr;
@@ -291,6 +293,7 @@ int check_status(dls_model* m) {
     const int32_t zero = 0;
     CK(cudaMemcpyAsync(&m->sp->status, &zero, sizeof zero, cudaMemcpyHostToDevice, m->stream));
     TRY(sync_stream(m, m->stream));
+    if (st & kTimeout) return fail(m, DLS_ERR_TIMEOUT, "device_status=0x%x (8=a bounded device wait ran out)", st);
     return fail(m, DLS_ERR_STATE, "device_status=0x%x (1=page 2=token 4=position)", st);
   }
   return DLS_OK;
@@ -876,7 +879,7 @@ int enqueue_batch_tc(dls_model* m, int n, bool head, bool argmax, float* capture
   return DLS_OK;
 }
 
-int enqueue_persistent(dls_model* m, bool head, bool argmax) {
+int enqueue_persistent(dls_model* m, bool head, bool argmax, float* capture) {
   StepArgs a{};
   a.layers = m->step_layers;
   a.n_layers = m->L;
@@ -917,6 +920,7 @@ int enqueue_persistent(dls_model* m, bool head, bool argmax) {
   a.trace = m->profiling ? m->step_trace : nullptr;
   a.ctrace = m->profiling ? m->step_ctrace : nullptr;
   a.skip = m->drafting ? m->draft_dev : m->skip_dev;
+  a.capture = capture;
   a.ns = m->step.ns;
   a.stage_bytes = m->step.stage_bytes;
   {
@@ -940,8 +944,8 @@ int enqueue_persistent(dls_model* m, bool head, bool argmax) {
 
 int enqueue_step(dls_model* m, int rows, bool head, bool argmax, float* capture) {
   m->launch_count = 0;
-  if (m->use_step && rows == 1 && !capture) {
-    TRY(enqueue_persistent(m, head, argmax));
+  if (m->use_step && rows == 1) {
+    TRY(enqueue_persistent(m, head, argmax, capture));
     m->launches_per_step = m->launch_count;
     return DLS_OK;
   }
@@ -1102,44 +1106,146 @@ int auto_resident(const dls_model* m, uint64_t other_bytes) {
 
 int setup_persistent(dls_model* m);
 
+int step_scratch(dls_model* m, std::vector<void*>* made);
+
+// Change the resident count to n, all or nothing (the LayerStreamer page's
+// ledger: reserve, commit on success, roll back on failure).  Everything the
+// new layout needs -- pinned host copies of the layers to evict, the two
+// staging buffers, device copies of the layers to load, the persistent
+// kernel's scratch -- is allocated first; if any allocation fails, what this
+// call allocated is released and the model is unchanged.  Only then are
+// layers copied and the old buffers freed.  While it allocates, the ledger
+// credits the bytes the commit will free, so the budget is checked against
+// the final layout (the device briefly holds both).
 int apply_resident(dls_model* m, int n) {
-  // evict layers [n, L): keep a pinned host copy, then free the device copy
-  for (int l = n; l < m->L; ++l) {
-    if (!m->layer_dev[l]) continue;
-    if (!m->layer_host[l]) {
-      void* h = nullptr;
-      CK(cudaHostAlloc(&h, m->lay.bytes, cudaHostAllocDefault));
-      m->layer_host[l] = static_cast<uint8_t*>(h);
-      CK(cudaMemcpyAsync(h, m->layer_dev[l], m->lay.bytes, cudaMemcpyDeviceToHost, m->stream));
-      TRY(sync_stream(m, m->stream));
+  std::vector<int> evict, load;
+  for (int l = n; l < m->L; ++l)
+    if (m->layer_dev[l]) evict.push_back(l);
+  for (int l = 0; l < n; ++l)
+    if (!m->layer_dev[l]) load.push_back(l);
+  const bool need_stage = n < m->L && !m->stage[0];
+  const bool drop_stage = n >= m->L && m->stage[0];
+  std::vector<int> new_host;   // layers whose pinned host copy this call made
+  std::vector<void*> new_dev;  // device buffers this call allocated
+  auto rollback = [&](int r) {
+    m->credit = 0;
+    cudaStreamSynchronize(m->stream);  // no copy into a buffer about to be released is left in flight
+    for (void* p : new_dev) dev_free(m, p);
+    for (int l : new_host) {
+      cudaFreeHost(m->layer_host[l]);
+      m->layer_host[l] = nullptr;
     }
+    return r;
+  };
+  // 1. pinned host copies of the layers to evict
+  for (int l : evict) {
+    if (m->layer_host[l]) continue;
+    void* h = nullptr;
+    if (cudaHostAlloc(&h, m->lay.bytes, cudaHostAllocDefault) != cudaSuccess || !h) {
+      cudaGetLastError();
+      return rollback(fail(m, DLS_ERR_CUDA, "what=pinned_layer_copy layer=%d bytes=%zu allocation failed", l,
+                           m->lay.bytes));
+    }
+    m->layer_host[l] = static_cast<uint8_t*>(h);
+    new_host.push_back(l);
+    if (cudaMemcpyAsync(h, m->layer_dev[l], m->lay.bytes, cudaMemcpyDeviceToHost, m->stream) != cudaSuccess)
+      return rollback(fail(m, DLS_ERR_CUDA, "layer=%d copy to host failed", l));
+  }
+  // 2. device memory of the new layout
+  m->credit = (uint64_t)evict.size() * a256(m->lay.bytes) + (drop_stage ? staging_bytes(m) : 0);
+  uint8_t* stage_new[2] = {nullptr, nullptr};
+  if (need_stage) {
+    for (auto& st : stage_new) {
+      void* p = nullptr;
+      const int r = dev_alloc(m, m->lay.bytes, &p, "stream_buffer");
+      if (r != DLS_OK) return rollback(r);
+      new_dev.push_back(p);
+      st = static_cast<uint8_t*>(p);
+    }
+  }
+  std::vector<uint8_t*> load_ptr;
+  for (int l : load) {
+    void* p = nullptr;
+    const int r = dev_alloc(m, m->lay.bytes, &p, "layer");
+    if (r != DLS_OK) return rollback(r);
+    (void)l;
+    new_dev.push_back(p);
+    load_ptr.push_back(static_cast<uint8_t*>(p));
+  }
+  if (n >= m->L) {
+    const int r = step_scratch(m, &new_dev);
+    if (r != DLS_OK) return rollback(r);
+  }
+  m->credit = 0;
+  {
+    const int r = sync_stream(m, m->stream);  // the host copies have landed
+    if (r != DLS_OK) return rollback(r);
+  }
+  // 3. commit
+  for (size_t i = 0; i < load.size(); ++i) {
+    m->layer_dev[load[i]] = load_ptr[i];
+    CK(cudaMemcpyAsync(load_ptr[i], m->layer_host[load[i]], m->lay.bytes, cudaMemcpyHostToDevice, m->stream));
+  }
+  for (int l : evict) {
     dev_free(m, m->layer_dev[l]);
     m->layer_dev[l] = nullptr;
   }
-  if (n >= m->L) {
+  if (drop_stage) {
     for (auto& st : m->stage) {
       dev_free(m, st);
       st = nullptr;
     }
   }
-  if (n < m->L && !m->stage[0]) {
-    for (auto& st : m->stage) {
-      void* p = nullptr;
-      TRY(dev_alloc(m, m->lay.bytes, &p, "stream_buffer"));
-      st = static_cast<uint8_t*>(p);
-    }
-  }
-  for (int l = 0; l < n; ++l) {
-    if (m->layer_dev[l]) continue;
-    void* p = nullptr;
-    TRY(dev_alloc(m, m->lay.bytes, &p, "layer"));
-    m->layer_dev[l] = static_cast<uint8_t*>(p);
-    CK(cudaMemcpyAsync(p, m->layer_host[l], m->lay.bytes, cudaMemcpyHostToDevice, m->stream));
+  if (need_stage) {
+    m->stage[0] = stage_new[0];
+    m->stage[1] = stage_new[1];
   }
   TRY(sync_stream(m, m->stream));
   m->resident = n;
   drop_graphs(m);
   return setup_persistent(m);
+}
+
+// Scratch of the persistent step kernel for the model's plan, allocated once;
+// `made` (may be NULL) collects what this call allocated.
+int step_scratch(dls_model* m, std::vector<void*>* made) {
+  const char* e = getenv("DLS_STEP_KERNEL");
+  if (e && atoi(e) == 0) return DLS_OK;
+  if (!m->step.fn) m->step = step_plan(m->wtype, m->H, m->q_rows, m->F, m->nh, m->nkv, m->hd, m->num_sms);
+  if (!m->step.fn || m->step_layers) return DLS_OK;
+  const int g = m->nh / m->nkv, S = m->step.splits;
+  std::vector<void*> got;
+  auto one = [&](size_t bytes, const char* what, void** out) {
+    const int r = dev_alloc(m, bytes, out, what);
+    if (r == DLS_OK) got.push_back(*out);
+    return r;
+  };
+  void* p[8] = {};
+  int r = one((size_t)m->L * sizeof(StepLayer), "step_layers", &p[0]);
+  if (r == DLS_OK) r = one((size_t)m->nkv * S * g * m->hd * sizeof(float), "step_attention_partials", &p[1]);
+  if (r == DLS_OK) r = one((size_t)m->nkv * S * g * 2 * sizeof(float), "step_attention_ml", &p[2]);
+  if (r == DLS_OK) r = one((size_t)m->nkv * sizeof(int), "step_attention_counters", &p[3]);
+  if (r == DLS_OK) r = one((size_t)m->step.grid * sizeof(int2), "step_argmax", &p[4]);
+  if (r == DLS_OK) r = one(2 * sizeof(unsigned), "step_barrier", &p[5]);
+  if (r == DLS_OK) r = one((size_t)(5 * m->L + 8) * sizeof(unsigned long long), "step_trace", &p[6]);
+  if (r == DLS_OK)
+    r = one((size_t)(5 * m->L + 8) * m->step.grid * 8 * sizeof(unsigned long long), "step_cta_trace", &p[7]);
+  if (r == DLS_OK && cudaMemsetAsync(p[3], 0, m->nkv * sizeof(int), m->stream) != cudaSuccess)
+    r = fail(m, DLS_ERR_CUDA, "clearing the step counters failed");
+  if (r != DLS_OK) {
+    for (void* q : got) dev_free(m, q);
+    return r;
+  }
+  m->step_layers = static_cast<StepLayer*>(p[0]);
+  m->step_part_o = static_cast<float*>(p[1]);
+  m->step_part_ml = static_cast<float*>(p[2]);
+  m->step_att_cnt = static_cast<int*>(p[3]);
+  m->step_am = static_cast<int2*>(p[4]);
+  m->step_bar = static_cast<unsigned*>(p[5]);
+  m->step_trace = static_cast<unsigned long long*>(p[6]);
+  m->step_ctrace = static_cast<unsigned long long*>(p[7]);
+  if (made) made->insert(made->end(), got.begin(), got.end());
+  return DLS_OK;
 }
 
 // Plan the persistent step kernel when every layer is resident; allocate its
@@ -1151,20 +1257,8 @@ int setup_persistent(dls_model* m) {
   const char* e = getenv("DLS_STEP_KERNEL");
   if (e && atoi(e) == 0) return DLS_OK;
   if (m->resident < m->L) return DLS_OK;
-  if (!m->step.fn) m->step = step_plan(m->wtype, m->H, m->q_rows, m->F, m->nh, m->nkv, m->hd, m->num_sms);
+  TRY(step_scratch(m, nullptr));
   if (!m->step.fn) return DLS_OK;
-  const int g = m->nh / m->nkv, S = m->step.splits;
-  if (!m->step_layers) {
-    TRY(dev_alloc_t(m, (size_t)m->L, &m->step_layers, "step_layers"));
-    TRY(dev_alloc_t(m, (size_t)m->nkv * S * g * m->hd, &m->step_part_o, "step_attention_partials"));
-    TRY(dev_alloc_t(m, (size_t)m->nkv * S * g * 2, &m->step_part_ml, "step_attention_ml"));
-    TRY(dev_alloc_t(m, (size_t)m->nkv, &m->step_att_cnt, "step_attention_counters"));
-    TRY(dev_alloc_t(m, (size_t)m->step.grid, &m->step_am, "step_argmax"));
-    TRY(dev_alloc_t(m, (size_t)2, &m->step_bar, "step_barrier"));
-    TRY(dev_alloc_t(m, (size_t)(5 * m->L + 8), &m->step_trace, "step_trace"));
-    TRY(dev_alloc_t(m, (size_t)(5 * m->L + 8) * m->step.grid * 8, &m->step_ctrace, "step_cta_trace"));
-    CK(cudaMemsetAsync(m->step_att_cnt, 0, m->nkv * sizeof(int), m->stream));
-  }
   std::vector<StepLayer> hl(m->L);
   for (int l = 0; l < m->L; ++l) {
     const LayerPtrs P = layer_ptrs(m, m->layer_dev[l]);
@@ -1218,6 +1312,7 @@ int validate_desc(const dls_model_desc* d) {
   if (pt != 32 && pt != 64 && pt != 128 && pt != 256) return fail(m, DLS_ERR_ARG, "page_tokens=%d", d->page_tokens);
   if (d->max_seqs < 1 || d->max_ctx < 1) return fail(m, DLS_ERR_ARG, "max_seqs=%d max_ctx=%d", d->max_seqs, d->max_ctx);
   if (d->max_batch < 0 || d->max_batch > DLS_MAX_BATCH) return fail(m, DLS_ERR_ARG, "max_batch=%d", d->max_batch);
+  if (d->kv_pool_pages < 0) return fail(m, DLS_ERR_ARG, "kv_pool_pages=%d", d->kv_pool_pages);
   if (!(d->rope_theta > 0.f) || !(d->rms_eps >= 0.f))
     return fail(m, DLS_ERR_ARG, "rope_theta=%g rms_eps=%g", d->rope_theta, d->rms_eps);
   if (!d->tok_embd || !d->output_norm || !d->layers || (!d->tied_embeddings && !d->output))
@@ -1370,7 +1465,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
 
   // fixed allocations (everything but the layers)
   const int B = m->max_batch;
-  m->n_pages = m->max_seqs * m->max_pages;
+  m->n_pages = d.kv_pool_pages > 0 ? d.kv_pool_pages : m->max_seqs * m->max_pages;
   m->page_elems = (size_t)m->nkv * m->pt * m->hd;
   m->kv_layer_elems = (size_t)m->n_pages * m->page_elems;
   m->rope_len = m->max_ctx;
@@ -2085,6 +2180,15 @@ int dls_debug_capture(dls_model* m, float* per_layer_out) {
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
   m->capture = per_layer_out;
   return DLS_OK;
+}
+
+int dls_debug_bounded_wait(dls_model* m, int64_t limit_ns) {
+  if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
+  if (limit_ns < 1000 || limit_ns > 10000000000LL)
+    return fail(m, DLS_ERR_ARG, "limit_ns=%lld (1e3..1e10)", (long long)limit_ns);
+  CK(launch_unarrived_wait((unsigned long long)limit_ns, &m->sp->status, m->stream));
+  TRY(sync_stream(m, m->stream));
+  return check_status(m);
 }
 
 int dls_debug_read_kv(dls_model* m, int32_t seq, int32_t layer, void* k_out, void* v_out) {

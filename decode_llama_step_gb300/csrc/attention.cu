@@ -301,14 +301,23 @@ int attn_smem(int hd, int g) {
   return ts * 2 * TILE * hd * 2;
 }
 
+// The dynamic shared memory limit is a per-device function attribute: raise
+// it once on every device the kernel runs on (flags per device id, under a
+// lock, since calls may come from several host threads).
+constexpr int kMaxDevices = 256;
+std::mutex g_attr_mu;
+
 template <int HD, int G>
 AttnFn attn_fn() {
-  static bool done = false;  // raise the dynamic shared memory limit once
-  if (!done) {
+  static bool done[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  if (!done[dev]) {
     if (cudaFuncSetAttribute(attn_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              attn_smem(HD, G)) != cudaSuccess)
       return nullptr;
-    done = true;
+    done[dev] = true;
   }
   return attn_kernel<HD, G>;
 }
@@ -348,30 +357,20 @@ cudaError_t launch_attention(const AttnArgs& a, int rows, cudaStream_t s, bool p
 
 // ---- standalone C-ABI op ---------------------------------------------------------
 
-extern "C" size_t dls_attention_workspace_bytes(int32_t n_batch, int32_t n_heads, int32_t n_kv_heads,
-                                                int32_t head_dim, int32_t n_splits) {
-  if (n_batch < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || n_splits < 1) return 0;
-  return dls::attn_workspace_bytes(n_batch, n_heads, n_kv_heads, head_dim, n_splits);
+namespace {
+
+bool bad_shape(int32_t n_batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t page_tokens,
+               int32_t max_pages, int32_t n_splits) {
+  return n_splits > dls::kMaxSplits || n_batch < 1 || n_kv_heads < 1 || n_heads < 1 || n_heads % n_kv_heads ||
+         n_heads / n_kv_heads > dls::kMaxG || (head_dim != 32 && head_dim != 64 && head_dim != 128) ||
+         page_tokens < 32 || page_tokens % 32 || max_pages < 1;
 }
 
-extern "C" int dls_attention_decode(const float* q, const void* k_pages, const void* v_pages,
-                                    const int32_t* page_table, const int32_t* lengths, float* o, void* workspace,
-                                    size_t workspace_bytes, int32_t n_batch, int32_t n_heads, int32_t n_kv_heads,
-                                    int32_t head_dim, int32_t page_tokens, int32_t max_pages, int32_t n_splits,
-                                    void* cuda_stream) {
-  if (!q || !k_pages || !v_pages || !page_table || !lengths || !o || !workspace) return DLS_ERR_ARG;
-  if (n_splits > 128) return DLS_ERR_ARG;
-  if (n_batch < 1 || n_kv_heads < 1 || n_heads < 1 || n_heads % n_kv_heads || n_heads / n_kv_heads > dls::kMaxG ||
-      (head_dim != 32 && head_dim != 64 && head_dim != 128) || page_tokens < 32 || page_tokens % 32 ||
-      max_pages < 1)
-    return DLS_ERR_ARG;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
-    return DLS_ERR_CUDA;
-  const int max_len = page_tokens * max_pages;
-  if (n_splits <= 0) n_splits = dls::attn_default_splits(n_batch, n_kv_heads, sms, max_len);
-  if (workspace_bytes < dls::attn_workspace_bytes(n_batch, n_heads, n_kv_heads, head_dim, n_splits))
-    return DLS_ERR_ARG;
+// Launch arguments shared by both entry points (scratch carved from `ws`).
+dls::AttnArgs standalone_args(const float* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                              const int32_t* lengths, float* o, int32_t n_heads, int32_t n_kv_heads,
+                              int32_t head_dim, int32_t page_tokens, int32_t max_pages, int32_t n_splits,
+                              int32_t* status, void* ws, int32_t n_batch) {
   dls::AttnArgs a = {};
   a.q = q;
   a.o = o;
@@ -388,12 +387,63 @@ extern "C" int dls_attention_decode(const float* q, const void* k_pages, const v
   a.page_tokens = page_tokens;
   a.n_splits = n_splits;
   a.row0 = 0;
-  a.status = nullptr;
-  a.max_len = max_len;
-  dls::attn_workspace_carve(workspace, n_batch, n_heads, n_kv_heads, head_dim, n_splits, &a.part_o, &a.part_ml,
+  a.status = status;
+  a.max_len = page_tokens * max_pages;
+  dls::attn_workspace_carve(ws, n_batch, n_heads, n_kv_heads, head_dim, n_splits, &a.part_o, &a.part_ml,
                             &a.counters);
-  cudaError_t e = dls::launch_attention(a, n_batch, static_cast<cudaStream_t>(cuda_stream), false);
-  return e == cudaSuccess ? DLS_OK : DLS_ERR_CUDA;
+  return a;
+}
+
+}  // namespace
+
+extern "C" size_t dls_attention_workspace_bytes(int32_t n_batch, int32_t n_heads, int32_t n_kv_heads,
+                                                int32_t head_dim, int32_t n_splits) {
+  if (n_batch < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || n_splits < 1) return 0;
+  return dls::attn_workspace_bytes(n_batch, n_heads, n_kv_heads, head_dim, n_splits);
+}
+
+extern "C" int dls_attention_decode(const float* q, const void* k_pages, const void* v_pages,
+                                    const int32_t* page_table, const int32_t* lengths, float* o, void* workspace,
+                                    size_t workspace_bytes, int32_t n_batch, int32_t n_heads, int32_t n_kv_heads,
+                                    int32_t head_dim, int32_t page_tokens, int32_t max_pages, int32_t n_splits,
+                                    int32_t* status, void* cuda_stream) {
+  if (!q || !k_pages || !v_pages || !page_table || !lengths || !o || !workspace)
+    return dls::report_error(DLS_ERR_ARG, "attention: NULL pointer argument");
+  if (bad_shape(n_batch, n_heads, n_kv_heads, head_dim, page_tokens, max_pages, n_splits))
+    return dls::report_error(DLS_ERR_ARG, "attention: bad shape n_batch=%d n_heads=%d n_kv_heads=%d head_dim=%d "
+                             "page_tokens=%d max_pages=%d n_splits=%d", n_batch, n_heads, n_kv_heads, head_dim,
+                             page_tokens, max_pages, n_splits);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
+    return dls::report_error(DLS_ERR_CUDA, "attention: no current device");
+  if (n_splits <= 0) n_splits = dls::attn_default_splits(n_batch, n_kv_heads, sms, page_tokens * max_pages);
+  const size_t need = dls::attn_workspace_bytes(n_batch, n_heads, n_kv_heads, head_dim, n_splits);
+  if (workspace_bytes < need)
+    return dls::report_error(DLS_ERR_ARG, "attention: workspace_bytes=%zu < %zu needed for n_splits=%d",
+                             workspace_bytes, need, n_splits);
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess)
+    return dls::report_error(DLS_ERR_CUDA, "attention: clearing the status word failed");
+  const dls::AttnArgs a = standalone_args(q, k_pages, v_pages, page_table, lengths, o, n_heads, n_kv_heads, head_dim,
+                                          page_tokens, max_pages, n_splits, status, workspace, n_batch);
+  if (dls::launch_attention(a, n_batch, st, false) != cudaSuccess)
+    return dls::report_error(DLS_ERR_CUDA, "attention: launch failed");
+  return DLS_OK;
+}
+
+extern "C" int dls_attention_status(const int32_t* status, void* cuda_stream) {
+  if (!status) return dls::report_error(DLS_ERR_ARG, "attention status: NULL status word");
+  int32_t v = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaMemcpyAsync(&v, status, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return dls::report_error(DLS_ERR_CUDA, "attention status: reading the status word failed");
+  if (v & dls::kTimeout)
+    return dls::report_error(DLS_ERR_TIMEOUT, "attention: a bounded wait ran out device_status=0x%x", v);
+  if (v)
+    return dls::report_error(DLS_ERR_STATE, "attention: device_status=0x%x (1=missing page 4=length outside "
+                             "1..page_tokens*max_pages)", v);
+  return DLS_OK;
 }
 
 // ---- allocation-free variant -------------------------------------------------------
@@ -413,13 +463,13 @@ namespace {
 static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[DLS_ATTENTION_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[256] = {};  // device address of the scratch, per device id
+void* g_noalloc_ptr[dls::kMaxDevices] = {};  // device address of the scratch, per device id
 
 // Device address of the scratch on the current device, looked up once per
 // device (host code sees only a host-side stand-in under the symbol's name).
 int noalloc_scratch(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return DLS_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= dls::kMaxDevices) return DLS_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
@@ -436,25 +486,28 @@ extern "C" int dls_attention_decode_noalloc(const float* q, const void* k_pages,
                                             const int32_t* page_table, const int32_t* lengths, float* o,
                                             int32_t n_batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                             int32_t page_tokens, int32_t max_pages, int32_t n_splits,
-                                            void* cuda_stream) {
+                                            int32_t* status, void* cuda_stream) {
   if (!q || !k_pages || !v_pages || !page_table || !lengths || !o)
     return dls::report_error(DLS_ERR_ARG, "noalloc attention: NULL pointer argument");
-  if (n_splits > 128 || n_batch < 1 || n_kv_heads < 1 || n_heads < 1 || n_heads % n_kv_heads ||
-      n_heads / n_kv_heads > dls::kMaxG || (head_dim != 32 && head_dim != 64 && head_dim != 128) ||
-      page_tokens < 32 || page_tokens % 32 || max_pages < 1)
+  if (bad_shape(n_batch, n_heads, n_kv_heads, head_dim, page_tokens, max_pages, n_splits))
     return dls::report_error(DLS_ERR_ARG, "noalloc attention: bad shape n_batch=%d n_heads=%d n_kv_heads=%d "
                              "head_dim=%d page_tokens=%d max_pages=%d n_splits=%d", n_batch, n_heads, n_kv_heads,
                              head_dim, page_tokens, max_pages, n_splits);
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
     return dls::report_error(DLS_ERR_CUDA, "noalloc attention: no current device");
-  const int max_len = page_tokens * max_pages;
-  if (n_splits <= 0) n_splits = dls::attn_default_splits(n_batch, n_kv_heads, sms, max_len);
+  const size_t cap = DLS_ATTENTION_NOALLOC_SCRATCH_BYTES;
+  if (n_splits <= 0) {
+    // the usual choice, cut down to the largest split count whose partials
+    // fit the array (any count gives the same result up to fp32 rounding)
+    n_splits = dls::attn_default_splits(n_batch, n_kv_heads, sms, page_tokens * max_pages);
+    while (n_splits > 1 && dls::attn_workspace_bytes(n_batch, n_heads, n_kv_heads, head_dim, n_splits) > cap)
+      --n_splits;
+  }
   const size_t need = dls::attn_workspace_bytes(n_batch, n_heads, n_kv_heads, head_dim, n_splits);
-  if (need > DLS_ATTENTION_NOALLOC_SCRATCH_BYTES)
-    return dls::report_error(DLS_ERR_CAPACITY, "noalloc attention: needs %zu bytes of scratch, the built-in "
-                             "array holds %zu (fewer rows or splits fit)", need,
-                             (size_t)DLS_ATTENTION_NOALLOC_SCRATCH_BYTES);
+  if (need > cap)
+    return dls::report_error(DLS_ERR_CAPACITY, "noalloc attention: needs %zu bytes of scratch for n_splits=%d, the "
+                             "built-in array holds %zu (fewer rows or splits fit)", need, n_splits, cap);
   void* ws = nullptr;
   if (noalloc_scratch(&ws) != DLS_OK)
     return dls::report_error(DLS_ERR_CUDA, "noalloc attention: cudaGetSymbolAddress failed");
@@ -463,26 +516,10 @@ extern "C" int dls_attention_decode_noalloc(const float* q, const void* k_pages,
   const size_t counter_bytes = ((size_t)n_batch * n_kv_heads * sizeof(int) + 255) & ~(size_t)255;
   if (cudaMemsetAsync(ws, 0, counter_bytes, st) != cudaSuccess)
     return dls::report_error(DLS_ERR_CUDA, "noalloc attention: clearing the counters failed");
-  dls::AttnArgs a = {};
-  a.q = q;
-  a.o = o;
-  a.k_pool = static_cast<const __half*>(k_pages);
-  a.v_pool = static_cast<const __half*>(v_pages);
-  a.page_table = page_table;
-  a.max_pages = max_pages;
-  a.pt_row = nullptr;
-  a.len = lengths;
-  a.len_add = 0;
-  a.n_heads = n_heads;
-  a.n_kv = n_kv_heads;
-  a.head_dim = head_dim;
-  a.page_tokens = page_tokens;
-  a.n_splits = n_splits;
-  a.row0 = 0;
-  a.status = nullptr;
-  a.max_len = max_len;
-  dls::attn_workspace_carve(ws, n_batch, n_heads, n_kv_heads, head_dim, n_splits, &a.part_o, &a.part_ml,
-                            &a.counters);
+  if (status && cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess)
+    return dls::report_error(DLS_ERR_CUDA, "noalloc attention: clearing the status word failed");
+  const dls::AttnArgs a = standalone_args(q, k_pages, v_pages, page_table, lengths, o, n_heads, n_kv_heads, head_dim,
+                                          page_tokens, max_pages, n_splits, status, ws, n_batch);
   if (dls::launch_attention(a, n_batch, st, false) != cudaSuccess)
     return dls::report_error(DLS_ERR_CUDA, "noalloc attention: launch failed");
   return DLS_OK;

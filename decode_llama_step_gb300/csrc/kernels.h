@@ -104,6 +104,8 @@ cudaError_t launch_dequant(const MatDev& m, int wtype, float* out, cudaStream_t 
 // copy whole KV pages: pairs[i] = (src_page, dst_page), for every layer
 cudaError_t launch_kv_copy(__half* k_pool, __half* v_pool, size_t layer_stride_elems, int n_layers,
                            size_t page_elems, const int2* pairs, int n_pairs, cudaStream_t s);
+// a bounded mbarrier wait that is never satisfied: kTimeout into *status after limit_ns
+cudaError_t launch_unarrived_wait(unsigned long long limit_ns, int32_t* status, cudaStream_t s);
 // spin (bounded by the global timer) for `ns` nanoseconds on the stream
 cudaError_t launch_delay(long long ns, cudaStream_t s);
 cudaError_t launch_kv_gather(const __half* pool, const int32_t* pages, int len, int n_kv, int page_tokens,
@@ -148,6 +150,7 @@ struct StepArgs {
   uint32_t stage_bytes;     // ring slot size
   int pf_skip, pf_rows;     // gate/up rows [pf_skip, pf_skip + pf_rows) of each CTA hinted into L2 during attention/O
   const uint8_t* skip;      // [n_layers]: layers this step does not compute (their residual passes through)
+  float* capture;           // optional [n_layers][H]: the residual stream after every layer
 };
 
 struct StepPlan {

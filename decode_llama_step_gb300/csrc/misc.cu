@@ -373,6 +373,22 @@ cudaError_t launch_kv_copy(__half* k_pool, __half* v_pool, size_t layer_stride_e
   return cudaGetLastError();
 }
 
+// One thread waits, with the library's bounded mbarrier wait, on a barrier
+// that nothing arrives at; when the limit runs out it records kTimeout in
+// the status word, exactly as a kernel whose copy never landed would.
+__global__ void unarrived_wait_kernel(unsigned long long limit_ns, int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  mbar_fence_init();
+  if (!mbar_wait(smem_u32(&bar), 0, 1000, limit_ns)) atomicOr(status, kTimeout);
+}
+
+cudaError_t launch_unarrived_wait(unsigned long long limit_ns, int32_t* status, cudaStream_t s) {
+  unarrived_wait_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_delay(long long ns, cudaStream_t s) {
   delay_kernel<<<1, 1, 0, s>>>(ns);
   return cudaGetLastError();

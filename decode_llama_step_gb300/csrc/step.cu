@@ -497,6 +497,9 @@ struct EpiArgs {
   // EPI_QKV
   __half* k_pool;
   __half* v_pool;
+  // EPI_RESID: optional copy of the updated rows (the residual stream
+  // after a layer, for the per-layer capture)
+  float* cap;
 };
 
 template <int WT, int PRO, int EPI, int RS, int MC>
@@ -625,6 +628,7 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
             const int blk = s / spb;
             const float old = (lr == tid && blk < 2) ? (blk == 0 ? res_pre[0] : res_pre[1]) : __ldcg(e.y + b0 + lr);
             e.y[b0 + lr] = old + v;
+            if (e.cap) e.cap[b0 + lr] = old + v;
           } else {
             e.y[b0 + lr] = v;
           }
@@ -940,7 +944,16 @@ __global__ void __maxnreg__(200) step_kernel(const StepArgs A) {
     }
     grid_sync(c);
     for (int l = 0; l < A.n_layers; ++l) {
-      if (c.sh->skip[l]) continue;  // the residual passes through; every CTA reads the same flags
+      if (c.sh->skip[l]) {  // the residual passes through; every CTA reads the same flags
+        if (A.capture) {
+          // this CTA's rows of x, which no CTA writes before the next layer's
+          // O phase (two grid barriers later)
+          int r0, r1;
+          row_split(A.H, 1, r0, r1);
+          for (int r = r0 + tid; r < r1; r += NWC * 32) A.capture[(size_t)l * A.H + r] = __ldcg(A.x + r);
+        }
+        continue;
+      }
       const StepLayer& L = A.layers[l];
       EpiArgs e{};
       e.y = A.q;
@@ -957,6 +970,7 @@ __global__ void __maxnreg__(200) step_kernel(const StepArgs A) {
       consume_gemv<WT, PRO_RMSNORM, EPI_SWIGLU, RSA, MCA>(c, L.gu, 2, A.x, L.ffn_norm, e);
       grid_sync(c);
       e.y = A.x;
+      e.cap = A.capture ? A.capture + (size_t)l * A.H : nullptr;
       consume_gemv<WT, PRO_COPY, EPI_RESID, RSB, MCB>(c, L.down, 1, A.h, nullptr, e);
       grid_sync(c);
     }

@@ -46,7 +46,8 @@ class dls_model_desc(ctypes.Structure):
                 ("ffn", i32), ("vocab", i32), ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
                 ("tied_embeddings", i32), ("wtype", i32), ("page_tokens", i32), ("max_seqs", i32),
                 ("max_ctx", i32), ("max_batch", i32), ("device_budget_bytes", u64), ("tok_embd", vp),
-                ("output", vp), ("output_norm", vp), ("layers", ctypes.POINTER(dls_layer_desc))]
+                ("output", vp), ("output_norm", vp), ("layers", ctypes.POINTER(dls_layer_desc)),
+                ("kv_pool_pages", i32)]
 
 
 _SIGS = {
@@ -78,14 +79,16 @@ _SIGS = {
     "dls_set_resident_layers": (ctypes.c_int, [vp, i32]),
     "dls_resident_layers": (i32, [vp]),
     "dls_layer_bytes": (u64, [vp]),
-    "dls_attention_decode": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, sz, i32, i32, i32, i32, i32, i32, i32, vp]),
+    "dls_attention_decode": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, sz, i32, i32, i32, i32, i32, i32, i32, vp, vp]),
+    "dls_attention_status": (ctypes.c_int, [vp, vp]),
     "dls_attention_workspace_bytes": (sz, [i32, i32, i32, i32, i32]),
-    "dls_attention_decode_noalloc": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]),
+    "dls_attention_decode_noalloc": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]),
     "dls_kquant_packed_bytes": (ctypes.c_uint64, [i32, i32, i32]),
     "dls_kquant_pack": (ctypes.c_int, [i32, vp, i32, i32, vp, vp]),
     "dls_kquant_gemv": (ctypes.c_int, [i32, vp, i32, i32, vp, vp, vp, vp]),
     "dls_debug_capture": (ctypes.c_int, [vp, vp]),
     "dls_debug_read_kv": (ctypes.c_int, [vp, i32, i32, vp, vp]),
+    "dls_debug_bounded_wait": (ctypes.c_int, [vp, ctypes.c_int64]),
     "dls_debug_dequant": (ctypes.c_int, [vp, i32, i32, vp]),
     "dls_debug_gemv": (ctypes.c_int, [vp, i32, i32, vp, vp]),
     "dls_debug_gemm": (ctypes.c_int, [vp, i32, i32, i32, vp, vp]),
@@ -160,22 +163,33 @@ def attention_workspace_bytes(n_batch, n_heads, n_kv_heads, head_dim, n_splits) 
 
 
 def attention_decode(q, k_pages, v_pages, page_table, lengths, o, workspace, workspace_bytes, n_batch, n_heads,
-                     n_kv_heads, head_dim, page_tokens, max_pages, n_splits=0, stream=None):
+                     n_kv_heads, head_dim, page_tokens, max_pages, n_splits=0, status=None, stream=None):
+    """Split-K GQA decode attention over a paged fp16 cache (device buffers).
+    ``status``: optional device int32[1] the kernel reports into; read it
+    with attention_status()."""
     _check(load().dls_attention_decode(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(lengths),
                                        _ptr(o), _ptr(workspace), workspace_bytes, n_batch, n_heads, n_kv_heads,
-                                       head_dim, page_tokens, max_pages, n_splits, _stream_handle(stream)))
+                                       head_dim, page_tokens, max_pages, n_splits, _ptr(status),
+                                       _stream_handle(stream)))
+
+
+def attention_status(status, stream=None):
+    """Wait for the stream and raise DlsError (DLS_ERR_STATE or
+    DLS_ERR_TIMEOUT) if the attention kernel flagged its status word."""
+    _check(load().dls_attention_status(_ptr(status), _stream_handle(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20  # DLS_ATTENTION_NOALLOC_SCRATCH_BYTES
 
 
 def attention_decode_noalloc(q, k_pages, v_pages, page_table, lengths, o, n_batch, n_heads, n_kv_heads, head_dim,
-                             page_tokens, max_pages, n_splits=0, stream=None):
+                             page_tokens, max_pages, n_splits=0, status=None, stream=None):
     """dls_attention_decode without a workspace: for callers that may not
     allocate device memory; the scratch is a fixed array in the library."""
     _check(load().dls_attention_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
                                                _ptr(lengths), _ptr(o), n_batch, n_heads, n_kv_heads, head_dim,
-                                               page_tokens, max_pages, n_splits, _stream_handle(stream)))
+                                               page_tokens, max_pages, n_splits, _ptr(status),
+                                               _stream_handle(stream)))
 
 
 DLS_Q4_K = 12
@@ -207,17 +221,29 @@ def _stream_handle(stream):
     return stream.cuda_stream
 
 
-class _TorchAllocator:
-    """Device memory from PyTorch's caching allocator."""
+class TorchAllocator:
+    """Device memory from PyTorch's caching allocator, through the library's
+    allocator callbacks.  ``live`` maps the pointers it handed out to their
+    sizes.  ``fail_at`` = k makes the k-th allocation call from now on return
+    NULL (the library then reports DLS_ERR_CUDA and rolls the call back);
+    ``calls`` counts allocation calls."""
 
-    def __init__(self, device: int):
+    def __init__(self, device: int, fail_at=None):
         import torch
 
         self.torch = torch
         self.device = device
         self.live = {}
+        self.calls = 0
+        self.fail_at = fail_at
 
         def _alloc(ctx, nbytes, stream):
+            self.calls += 1
+            if self.fail_at is not None:
+                self.fail_at -= 1
+                if self.fail_at == 0:
+                    self.fail_at = None
+                    return None
             try:
                 p = torch.cuda.caching_allocator_alloc(int(nbytes), self.device, int(stream or 0))
                 self.live[p] = nbytes
@@ -246,7 +272,7 @@ class Model:
     """
 
     def __init__(self, cfg, weights, *, max_seqs=1, max_ctx=1024, max_batch=1, page_tokens=64,
-                 device_budget_bytes=0, stream=None, torch_allocator=True):
+                 device_budget_bytes=0, stream=None, torch_allocator=True, allocator=None, kv_pool_pages=0):
         self.lib = load()
         self.cfg = cfg
         self.stream = stream
@@ -272,12 +298,16 @@ class Model:
                            page_tokens, max_seqs, max_ctx, max_batch, int(device_budget_bytes),
                            host(weights["tok_embd"], np.uint8), None if out is None else host(out, np.uint8),
                            host(weights["output_norm"], np.float32), layers)
+        d.kv_pool_pages = int(kv_pool_pages)
         self._alloc = None
         alloc_ptr = None
-        if torch_allocator:
+        if allocator is not None:
+            self._alloc = allocator
+            alloc_ptr = ctypes.pointer(allocator.struct)
+        elif torch_allocator:
             import torch
 
-            self._alloc = _TorchAllocator(torch.cuda.current_device())
+            self._alloc = TorchAllocator(torch.cuda.current_device())
             alloc_ptr = ctypes.pointer(self._alloc.struct)
         h = vp()
         _check(self.lib.dls_model_create(ctypes.byref(d), alloc_ptr, _stream_handle(stream), ctypes.byref(h)))
@@ -403,6 +433,10 @@ class Model:
     # --- hooks
     def debug_capture(self, per_layer_out):
         self._c(self.lib.dls_debug_capture(self.handle, _ptr(per_layer_out)))
+
+    def debug_bounded_wait(self, limit_ns: int):
+        """A bounded device wait that nothing satisfies (raises DLS_ERR_TIMEOUT)."""
+        self._c(self.lib.dls_debug_bounded_wait(self.handle, int(limit_ns)))
 
     def debug_read_kv(self, seq: int, layer: int, k_out, v_out):
         self._c(self.lib.dls_debug_read_kv(self.handle, seq, layer, _ptr(k_out), _ptr(v_out)))

@@ -118,6 +118,10 @@ typedef struct dls_model_desc {
   const void* output;      /* host blocks [vocab x hidden], or NULL when tied */
   const float* output_norm;/* host fp32 [hidden] */
   const dls_layer_desc* layers; /* host array [n_layers] */
+  int32_t kv_pool_pages;   /* KV pages shared by all sequences; 0 = max_seqs * ceil(max_ctx / page_tokens),
+                              which lets every sequence reach max_ctx on private pages.  A smaller pool
+                              oversubscribes: a call that needs a page when none is free fails with
+                              DLS_ERR_CAPACITY and changes nothing. */
 } dls_model_desc;
 
 /* ---- model ------------------------------------------------------------- */
@@ -292,24 +296,42 @@ uint64_t dls_layer_bytes(const dls_model* m);
 /* ---- standalone op ----------------------------------------------------------- */
 
 /* Split-K (flash-decoding) GQA attention of one query position over an fp16
- * paged KV cache, for `n_batch` independent rows.  All pointers device:
+ * paged KV cache, for `n_batch` independent rows (the engine page, section
+ * 4.4: causal softmax with the mask inside the kernel; section 1: GQA over a
+ * KV cache).  All pointers device:
  *   q         fp32 [n_batch][n_heads][head_dim] (already rotated)
  *   k_pages,  fp16 pools [n_pages][n_kv_heads][page_tokens][head_dim]
  *   v_pages
  *   page_table int32 [n_batch][max_pages]: logical page -> physical page
- *   lengths   int32 [n_batch]: keys 0..lengths[b]-1 are attended (>= 1)
+ *   lengths   int32 [n_batch]: keys 0..lengths[b]-1 are attended
+ *             (1 <= lengths[b] <= page_tokens * max_pages)
  *   o         fp32 [n_batch][n_heads][head_dim]
  *   workspace scratch of dls_attention_workspace_bytes(...) bytes; its
  *             counter words must be zero before the first call (the call
  *             leaves them zero again).
- * `n_splits` = how many CTAs share one (row, kv head); 0 = choose.  Returns
- * DLS_ERR_ARG on a bad shape.  cuda_stream orders the work. */
+ *   status    int32 [1] or NULL.  The call zeroes it on cuda_stream; the
+ *             kernel ORs in 1 when a page-table entry it needs is negative,
+ *             4 when a length is outside 1..page_tokens*max_pages (the
+ *             kernel then clamps it) and 8 when a bounded wait ran out.  Read
+ *             it with dls_attention_status once the work is done.
+ * `n_splits` = how many CTAs share one (row, kv head), 1..128; 0 = choose.
+ * Returns DLS_ERR_ARG on a bad shape or a workspace too small for the split
+ * count; the work is enqueued on cuda_stream (the outputs are valid once it
+ * completes). */
 int dls_attention_decode(const float* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
                          const int32_t* lengths, float* o, void* workspace, size_t workspace_bytes,
                          int32_t n_batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
-                         int32_t page_tokens, int32_t max_pages, int32_t n_splits, void* cuda_stream);
+                         int32_t page_tokens, int32_t max_pages, int32_t n_splits, int32_t* status,
+                         void* cuda_stream);
 size_t dls_attention_workspace_bytes(int32_t n_batch, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                      int32_t n_splits);
+
+/* Wait for cuda_stream, read the status word of a standalone attention call
+ * and turn it into a status code: DLS_OK (0), DLS_ERR_TIMEOUT (bit 8: a
+ * bounded wait ran out), DLS_ERR_STATE (bits 1 or 4: a missing page or a bad
+ * length; the output is not meaningful), with the flags in
+ * dls_last_error(NULL). */
+int dls_attention_status(const int32_t* status, void* cuda_stream);
 
 /* Allocation-free dls_attention_decode.  The pages have no counterpart of
  * this call: it serves callers that may not allocate device memory at all
@@ -325,14 +347,16 @@ size_t dls_attention_workspace_bytes(int32_t n_batch, int32_t n_heads, int32_t n
  *  - Every call shares the one array; the call zeroes the arrival counters
  *    it needs on `cuda_stream`, but calls that overlap on the GPU (other
  *    streams, concurrent threads) race on the scratch and must not be issued.
- *  - DLS_ERR_CAPACITY if the shape needs more scratch than the array holds
- *    (dls_attention_workspace_bytes tells the need), DLS_ERR_ARG on a bad
+ *  - n_splits = 0 takes the usual split count, lowered until the partials
+ *    fit the array.  DLS_ERR_CAPACITY if the shape needs more scratch than
+ *    the array holds even so, or for an explicit n_splits
+ *    (dls_attention_workspace_bytes tells the need); DLS_ERR_ARG on a bad
  *    shape; the message is in dls_last_error(NULL). */
 #define DLS_ATTENTION_NOALLOC_SCRATCH_BYTES (4u << 20)
 int dls_attention_decode_noalloc(const float* q, const void* k_pages, const void* v_pages,
                                  const int32_t* page_table, const int32_t* lengths, float* o, int32_t n_batch,
                                  int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t page_tokens,
-                                 int32_t max_pages, int32_t n_splits, void* cuda_stream);
+                                 int32_t max_pages, int32_t n_splits, int32_t* status, void* cuda_stream);
 
 /* ---- K-quant dequant-GEMV (the engine page, section 1: Q4_K_M, Q5_K, Q6_K) ----- */
 
@@ -377,8 +401,17 @@ int dls_kquant_gemv(int32_t type, const void* packed, int32_t rows, int32_t cols
 /* Arm a capture of the residual stream after every layer for the next
  * decode call (batch row 0) or prefill call (its last prompt token):
  * per_layer_out device fp32 [n_layers][hidden].  NULL disarms.  A captured
- * decode call runs without CUDA-graph replay. */
+ * decode call runs the same kernels as an uncaptured one (the persistent
+ * step kernel for batch-1 steps of a resident model, which then also writes
+ * each layer's residual), launched without CUDA-graph replay. */
 int dls_debug_capture(dls_model* m, float* per_layer_out);
+/* Run, on the model's stream, the library's bounded mbarrier wait against
+ * a barrier that nothing arrives at, with a limit of limit_ns (1e3..1e10;
+ * the kernels' own limit is 2 s).  The wait gives up, records the timeout
+ * in the model's device status word, and the call returns DLS_ERR_TIMEOUT
+ * like any call whose kernel saw a wait run out; the model stays usable.
+ * DLS_ERR_ARG for a limit out of range.  Synchronises the stream. */
+int dls_debug_bounded_wait(dls_model* m, int64_t limit_ns);
 /* Copy positions [0, length) of one layer's K and V of `seq` into device
  * fp16 [length][n_kv_heads][head_dim] buffers. */
 int dls_debug_read_kv(dls_model* m, int32_t seq, int32_t layer, void* k_out, void* v_out);

@@ -101,10 +101,16 @@ def test_null_model_calls_fail_cleanly(lib):
 
 def test_attention_op_rejects_bad_shapes(lib):
     assert lib.dls_attention_workspace_bytes(1, 5, 2, 64, 4) == 0
-    rc = lib.dls_attention_decode(1, 1, 1, 1, 1, 1, 1, 1 << 20, 1, 4, 2, 96, 64, 4, 1, None)
+    rc = lib.dls_attention_decode(1, 1, 1, 1, 1, 1, 1, 1 << 20, 1, 4, 2, 96, 64, 4, 1, None, None)
     assert rc == dls.DLS_ERR_ARG
-    rc = lib.dls_attention_decode(None, 1, 1, 1, 1, 1, 1, 1 << 20, 1, 4, 2, 64, 64, 4, 1, None)
+    rc = lib.dls_attention_decode(None, 1, 1, 1, 1, 1, 1, 1 << 20, 1, 4, 2, 64, 64, 4, 1, None, None)
     assert rc == dls.DLS_ERR_ARG
+    rc = lib.dls_attention_decode(1, 1, 1, 1, 1, 1, 1, 1 << 20, 1, 4, 2, 64, 64, 4, 129, None, None)
+    assert rc == dls.DLS_ERR_ARG
+    assert "attention" in lib.dls_last_error(None).decode()
+    rc = lib.dls_attention_decode_noalloc(1, 1, 1, 1, 1, 1, 1, 4, 2, 64, 16, 4, 1, None, None)
+    assert rc == dls.DLS_ERR_ARG       # page_tokens below 32
+    assert lib.dls_attention_status(None, None) == dls.DLS_ERR_ARG
 
 
 def test_null_model_calls_of_the_later_entry_points(lib):

@@ -184,6 +184,61 @@ def test_8b_decode_at_context(gpu_lib, w8b, ctx):
         release(m)
 
 
+def teacher_forced_layers(cfg, w, m, stream, seq, steps, layers, what):
+    """The layer-sliced check: for each decode step (token, position, the
+    GPU's captured residual after every layer) and each layer in `layers`,
+    the oracle runs that layer alone from the GPU's input to it (the
+    embedding row for layer 0) and the GPU's K/V cache of the positions
+    before the step, and its output and the K/V it appends at the step's
+    position are compared with the GPU's.  One oracle per layer holds that
+    layer's dequantised matrices for all steps."""
+    torch = _torch()
+    n = m.seq_length(seq)
+    kv = torch.empty(n, cfg.kv_dim, dtype=torch.float16, device="cuda")
+    vv = torch.empty_like(kv)
+    shape = (n, cfg.n_kv_heads, cfg.head_dim)
+    for l in layers:
+        m.debug_read_kv(seq, l, kv, vv)
+        K = host(kv, stream).reshape(shape)
+        V = host(vv, stream).reshape(shape)
+        orc = OracleModel(cfg, w, cache_bytes=4 * GB)
+        for i, (tok, pos, got) in enumerate(steps):
+            x_in = orc.embed(tok) if l == 0 else got[l - 1]
+            oseq = orc.new_seq(capacity=pos + 1)
+            oseq.set_layer(l, K[:pos], V[:pos])
+            out = orc.layer_forward(l, x_in, pos, oseq)
+            assert_close(got[l], out, f"{what}, step {i}, layer {l}")
+            assert_close(K[pos], oseq.keys(l)[pos], f"{what}, step {i}, layer {l}, K appended")
+            assert_close(V[pos], oseq.values(l)[pos], f"{what}, step {i}, layer {l}, V appended")
+        del orc
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("ctx", [2048, 8192])
+def test_8b_every_layer_teacher_forced(gpu_lib, w8b, ctx):
+    """All 32 layers of the full 8B Q8_0 model, for two decode steps at KV
+    context 2048 and 8192 on the benchmark's path (the persistent step
+    kernel, which writes each layer's residual when the capture is armed):
+    every layer's output and appended K/V against the oracle run from the
+    GPU's input to that layer and the GPU's cache (layer-sliced; the
+    independent full-model check is the 2-layer one above)."""
+    cfg, w = w8b
+    D = 2
+    prompt = synth.prompt_tokens(cfg, ctx, seed=1)
+    toks = [int(t) for t in synth.prompt_tokens(cfg, D, seed=6)]
+    m, stream = gpu_model(cfg, w, max_seqs=1, max_ctx=ctx + D + 8)
+    try:
+        seq = m.seq_create()
+        m.prefill(seq, prompt)
+        steps = []
+        for i in range(D):
+            got = captured(m, stream, cfg, lambda: m.decode_step(seq, toks[i], ctx + i))
+            steps.append((toks[i], ctx + i, got))
+        teacher_forced_layers(cfg, w, m, stream, seq, steps, range(cfg.n_layers), f"8B ctx {ctx}")
+    finally:
+        release(m)
+
+
 def test_8b_layer_skip_and_speculative_at_full_size(gpu_lib, w8b):
     """The 8B Q8_0 model at ctx 2048, as the skip and spec workloads run it:
     the calibration's cosines are finite and in [-1, 1]; self-speculative
@@ -381,6 +436,15 @@ def test_70b_q4_0_resident_and_streamed(gpu_lib):
             last = torch.empty(1, cfg.vocab, device="cuda")
             gen = m.generate([seq], [t0], D, last)
             runs[label] = (t0, np.asarray(gen)[:, 0].copy(), host(last, stream)[0])
+            if budget:
+                # one more step with the capture armed; sampled resident and
+                # streamed layers, layer-sliced against the oracle
+                n_res = m.resident_layers()
+                tok, pos = int(np.asarray(gen)[-1, 0]), ctx + D
+                got = captured(m, stream, cfg, lambda: m.decode_step(seq, tok, pos))
+                sample = sorted({0, n_res - 1, n_res, (n_res + cfg.n_layers) // 2, cfg.n_layers - 1})
+                teacher_forced_layers(cfg, w, m, stream, seq, [(tok, pos, got)], sample,
+                                      f"70B, 24 GB budget ({n_res} resident)")
         finally:
             release(m)
     assert runs["resident"][0] == runs["budget"][0]

@@ -127,10 +127,10 @@ def test_decode_across_page_boundaries(setup):
 
 
 def test_graph_replay_matches_eager(setup):
-    # decode without capture replays a captured graph (the persistent step
-    # kernel where the shape has one); with capture armed the step runs as
-    # separate kernels, eagerly.  Same math, different split of attention:
-    # equal to fp32 rounding.
+    # decode without capture replays a captured graph; with capture armed
+    # the same kernels (the persistent step kernel where the shape has one)
+    # launch eagerly and also write the per-layer residuals, which must not
+    # change the logits.
     torch = _torch()
     cfg, w, m, orc, stream = setup
     prompt = synth.prompt_tokens(cfg, 9, seed=3)
@@ -681,12 +681,15 @@ def test_attention_op_against_oracle(gpu_lib):
         tk, tv = torch.from_numpy(kp).cuda(), torch.from_numpy(vp).cuda()
         tt, tl = torch.from_numpy(table).cuda(), torch.from_numpy(lengths).cuda()
         tq = torch.from_numpy(q).cuda()
+        status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
         for splits in (1, 3, 7, 0):
-            ns = splits or 16
-            wsb = dls.attention_workspace_bytes(nb, nh, nkv, hd, ns)
+            # splits = 0: the call chooses; a workspace sized for the most
+            # splits (128) serves any choice
+            wsb = dls.attention_workspace_bytes(nb, nh, nkv, hd, splits or 128)
             ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
             o = torch.empty(nb, nh, hd, device="cuda")
-            dls.attention_decode(tq, tk, tv, tt, tl, o, ws, wsb, nb, nh, nkv, hd, pt, maxp, ns)
+            dls.attention_decode(tq, tk, tv, tt, tl, o, ws, wsb, nb, nh, nkv, hd, pt, maxp, splits, status=status)
+            dls.attention_status(status)
             got = o.cpu().numpy()
             for b in range(nb):
                 n = lengths[b]
@@ -698,3 +701,43 @@ def test_attention_op_against_oracle(gpu_lib):
                 assert_close(got[b], ref, f"attn nh={nh} nkv={nkv} hd={hd} n={n} splits={splits}", tol=1e-5)
             # the call leaves its arrival counters at zero for the next call
             assert int(ws[: nb * nkv * 4].view(torch.int32).abs().sum()) == 0
+
+
+def test_attention_op_reports_bad_pages_and_lengths(gpu_lib):
+    # a negative page-table entry and a length outside 1..page_tokens*max_pages
+    # are reported through the status word (the kernel skips the missing
+    # page and clamps the length; nothing is read out of bounds)
+    torch = _torch()
+    from decode_llama_step_gb300 import dls
+    rng = np.random.default_rng(4)
+    nb, nh, nkv, hd, pt, maxp = 2, 4, 2, 64, 32, 4
+    kp = torch.from_numpy(rng.standard_normal((nb * maxp, nkv, pt, hd)).astype(np.float16)).cuda()
+    vp = torch.from_numpy(rng.standard_normal((nb * maxp, nkv, pt, hd)).astype(np.float16)).cuda()
+    q = torch.from_numpy(rng.standard_normal((nb, nh, hd)).astype(np.float32)).cuda()
+    o = torch.empty(nb, nh, hd, device="cuda")
+    wsb = dls.attention_workspace_bytes(nb, nh, nkv, hd, 2)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    good = np.arange(nb * maxp, dtype=np.int32).reshape(nb, maxp)
+    cases = [(good, [100, 128], None),
+             (np.where(good == 5, -1, good), [100, 128], dls.DLS_ERR_STATE),   # row 1's page 1 missing
+             (good, [0, 128], dls.DLS_ERR_STATE),                              # empty row
+             (good, [100, 129], dls.DLS_ERR_STATE)]                            # past the table
+    for table, lens, want in cases:
+        tt = torch.from_numpy(np.ascontiguousarray(table, dtype=np.int32)).cuda()
+        tl = torch.from_numpy(np.array(lens, dtype=np.int32)).cuda()
+        dls.attention_decode(q, kp, vp, tt, tl, o, ws, wsb, nb, nh, nkv, hd, pt, maxp, 2, status=status)
+        if want is None:
+            dls.attention_status(status)
+        else:
+            with pytest.raises(dls.DlsError) as e:
+                dls.attention_status(status)
+            assert e.value.code == want
+        for fn in ("noalloc",):
+            dls.attention_decode_noalloc(q, kp, vp, tt, tl, o, nb, nh, nkv, hd, pt, maxp, 2, status=status)
+            if want is None:
+                dls.attention_status(status)
+            else:
+                with pytest.raises(dls.DlsError) as e:
+                    dls.attention_status(status)
+                assert e.value.code == want, fn
