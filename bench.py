@@ -74,7 +74,8 @@ def parse():
                    help="kquant workload: only this format and shape, e.g. q4_k:28672x8192 (small ncu captures)")
     p.add_argument("--draft-k", default="1,3,7",
                    help="speculative workload: draft lengths to time (comma-separated)")
-    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip", "spec", "kquant", "batch"],
+    p.add_argument("--workload", choices=["decode", "prefill", "fork", "stream", "skip", "spec", "kquant", "batch",
+                                          "h2d"],
                    default="decode",
                    help="decode (default, the headline line); the others are secondary measurements: "
                         "prefill (prompt of --ctx tokens), fork (shared prefix -> 8 branches), "
@@ -146,7 +147,10 @@ def replica_throughput(world, steps_per_rank, ms):
 def base_line(metric, value, unit, steps, warmup, ms, workload, extra):
     line = {"metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": 1, "steps": steps,
             "warmup": warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": {"workload": workload}}
+            "vs_baseline": None, "dtype": "int32+f32", "data": "synthetic", "config": {"workload": workload},
+            "arith": "decode GEMVs: Q8_0/Q4_0 codes x int16-quantised activation slices, exact int32 dot products, "
+                     "fp32 scaling and accumulation; tensor-core GEMMs: fp16 operand planes, fp32 accumulation; "
+                     "fp16 KV cache"}
     line.update(extra)
     return line
 
@@ -175,14 +179,20 @@ def run_prefill(args):
     t = sum(times) / len(times)
     fl = prefill_flops(cfg, args.ctx)
     peak, src = peaks("bf16_tflops")
+    peak_s, _ = peaks("bf16_tflops_sustained")
     m.close()
+    extra = {"tensor": {"flops_per_prefill": fl, "achieved_tflops": round(fl / t / 1e12, 1),
+                        "peak_tflops": peak, "frac": round(fl / t / 1e12 / peak, 4),
+                        "frac_of_sustained": round(fl / t / 1e12 / peak_s, 4),
+                        "peak_source": f"{src} bf16_tflops (fp16 operands run at the bf16 rate)"},
+             "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        tps, desc, cores = cpu_oracle_prefill_sample(cfg, args.ctx)
+        extra["cpu_baseline"] = {"value": round(tps, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                 "sample": desc}
     return base_line(f"prefill tok/s, {cfg.name}-shape {'Q8_0' if cfg.wtype == 8 else 'Q4_0'}", args.ctx / t,
                      "tok/s", args.steps, args.warmup, 1000 * t,
-                     f"{cfg.name} prefill of a {args.ctx}-token prompt (seeded ids) on an empty sequence",
-                     {"tensor": {"flops_per_prefill": fl, "achieved_tflops": round(fl / t / 1e12, 1),
-                                 "peak_tflops": peak, "frac": round(fl / t / 1e12 / peak, 4),
-                                 "peak_source": f"{src} bf16_tflops (fp16 operands run at the bf16 rate)"},
-                      "clocks": clk.summary()})
+                     f"{cfg.name} prefill of a {args.ctx}-token prompt (seeded ids) on an empty sequence", extra)
 
 
 def run_fork(args):
@@ -490,19 +500,53 @@ def run_batch(args):
 
 
 def h2d_peak(torch, chunk=256 << 20, inflight=4, reps=10):
-    """Best pinned host -> device copy rate: 256 MB chunks, several in flight."""
+    """Best pinned host -> device copy rate over several methods: 256 MB
+    chunks, four in flight, issued on one, two or four streams (copy
+    engines), and the library's SM-driven copy kernel (CTAs reading the
+    pinned buffer over the host link) at several CTA counts.  Returns
+    (best GB/s, {method: GB/s})."""
+    from decode_llama_step_gb300 import dls
     host = torch.empty(chunk * inflight, dtype=torch.uint8, pin_memory=True)
+    host.fill_(1)
     dev = torch.empty(chunk * inflight, dtype=torch.uint8, device="cuda")
-    s = torch.cuda.Stream()
-    best = 0.0
-    for _ in range(reps):
-        def go():
-            with torch.cuda.stream(s):
+    main = torch.cuda.Stream()
+    rates = {}
+    for ns in (1, 2, 4):
+        streams = [torch.cuda.Stream() for _ in range(ns)]
+        best = 0.0
+        for _ in range(reps):
+            def go():
+                ev = torch.cuda.Event()
+                ev.record(main)
                 for i in range(inflight):
-                    dev[i * chunk:(i + 1) * chunk].copy_(host[i * chunk:(i + 1) * chunk], non_blocking=True)
-        t = _events(torch, s, go)
-        best = max(best, chunk * inflight / t / 1e9)
-    return best
+                    st = streams[i % ns]
+                    st.wait_event(ev)
+                    with torch.cuda.stream(st):
+                        dev[i * chunk:(i + 1) * chunk].copy_(host[i * chunk:(i + 1) * chunk], non_blocking=True)
+                for st in streams:
+                    e2 = torch.cuda.Event()
+                    e2.record(st)
+                    main.wait_event(e2)
+            t = _events(torch, main, go)
+            best = max(best, chunk * inflight / t / 1e9)
+        rates[f"copy_engines_{ns}_streams"] = round(best, 1)
+    for ctas in (16, 32, 64, 152):
+        best = 0.0
+        for _ in range(reps):
+            t = _events(torch, main, lambda: dls.h2d_copy_sm(dev, host, chunk * inflight, ctas, main))
+            best = max(best, chunk * inflight / t / 1e9)
+        rates[f"sm_kernel_{ctas}_ctas"] = round(best, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(dev[:4096].cpu(), host[:4096])
+    return max(rates.values()), rates
+
+
+def run_h2d(args):
+    """Host -> device bandwidth only: the methods h2d_peak compares."""
+    import torch
+    peak, rates = h2d_peak(torch)
+    return base_line("pinned host -> device copy GB/s (best method)", peak, "GB/s", 10, 1, 0.0,
+                     "4 x 256 MB pinned host buffers to device memory", {"h2d_rates_gbs": rates})
 
 
 def run_stream(args):
@@ -517,11 +561,20 @@ def run_stream(args):
     D = min(args.steps, cfg.workload["decode"])
     w = synth.model_weights(cfg)
     stream = torch.cuda.Stream()
-    peak_h2d = h2d_peak(torch)
+    peak_h2d, h2d_rates = h2d_peak(torch)
     prompt = synth.prompt_tokens(cfg, ctx, seed=1)
     out = {}
-    for label, budget in (("resident", 0), ("budget_24GB", cfg.workload["budget_bytes"])):
-        m = dls.Model(cfg, w, max_seqs=1, max_ctx=ctx + D + 16, stream=stream, device_budget_bytes=budget)
+    sm_best = max((k for k in h2d_rates if k.startswith("sm_kernel")), key=lambda k: h2d_rates[k])
+    sm_ctas = int(sm_best.split("_")[2])
+    runs = [("resident", 0, None), ("budget_24GB", cfg.workload["budget_bytes"], None),
+            ("budget_24GB_sm_copy", cfg.workload["budget_bytes"], f"sm:{sm_ctas}")]
+    for label, budget, copy_mode in runs:
+        if copy_mode:
+            os.environ["DLS_STREAM_COPY"] = copy_mode      # read when the model is created
+        try:
+            m = dls.Model(cfg, w, max_seqs=1, max_ctx=ctx + D + 16, stream=stream, device_budget_bytes=budget)
+        finally:
+            os.environ.pop("DLS_STREAM_COPY", None)
         s = m.seq_create()
         t_pre = _events(torch, stream, lambda: m.prefill(s, prompt))
         m.generate([s], [1], 2)
@@ -533,14 +586,15 @@ def run_stream(args):
                       "prefill_s": round(t_pre, 2), "h2d_bytes_per_token": streamed_bytes,
                       "h2d_gbs": round(streamed_bytes / (t / D) / 1e9, 1) if streamed_bytes else None,
                       "h2d_frac_of_peak": round(streamed_bytes / (t / D) / 1e9 / peak_h2d, 4) if streamed_bytes else None,
-                      "clocks": clk.summary()}
+                      "clocks": clk.summary(), "copy": copy_mode or "copy engines (cudaMemcpyAsync)"}
         m.close()
     del w
-    b = out["budget_24GB"]
+    b = max((out["budget_24GB"], out["budget_24GB_sm_copy"]), key=lambda r: r["decode_tok_s"])
     return base_line("70B-shape Q4_0 decode tok/s with a 24 GB device budget (layer streaming)", b["decode_tok_s"],
                      "tok/s", D, 2, b["ms_per_token"], f"70b Q4_0, KV ctx {ctx}, {D} greedy tokens",
-                     {"stream": out, "h2d_peak_gbs": round(peak_h2d, 1),
-                      "h2d_peak_how": "pinned cudaMemcpyAsync, 4 x 256 MB in flight, best of 10"})
+                     {"stream": out, "h2d_peak_gbs": round(peak_h2d, 1), "h2d_rates_gbs": h2d_rates,
+                      "h2d_peak_how": "best of: pinned cudaMemcpyAsync of 4 x 256 MB on 1, 2 or 4 streams; the "
+                                      "SM-driven copy kernel at 16-152 CTAs; best of 10 each"})
 
 
 def gemv_bytes(rows, cols, wtype):
@@ -653,6 +707,30 @@ def cpu_oracle_sample(cfg, ctx, n_layer_samples=2):
     return 1.0 / per_tok, t_layers * len(layers) + t_head, desc, cores
 
 
+def cpu_oracle_prefill_sample(cfg, T):
+    """Time the fp64 oracle's prefill on a bounded sample: layer 0 of the
+    model over the whole T-token prompt plus the last token's LM head,
+    scaled to the whole model.  Returns (tok/s, description, cores)."""
+    import synth
+    from oracle import OracleModel
+
+    w = synth.model_weights(cfg, layers=[0])
+    orc = OracleModel(cfg, w, cache_bytes=0)
+    seq = orc.new_seq(capacity=T + 1)
+    X = orc.embed(synth.prompt_tokens(cfg, T, seed=1))
+    t0 = time.perf_counter()
+    X = orc.layer_forward(0, X, 0, seq)
+    t_layer = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    orc.final_logits(X[-1])
+    t_head = time.perf_counter() - t1
+    per_prefill = t_layer * cfg.n_layers + t_head
+    cores = len(os.sched_getaffinity(0))
+    desc = (f"fp64 oracle prefill of layer 0 of {cfg.n_layers} over the {T}-token prompt plus the LM head, scaled "
+            f"to {cfg.n_layers} layers ({t_layer:.2f} s/layer, head {t_head:.2f} s)")
+    return T / per_prefill, desc, cores
+
+
 def run_reference(args):
     """The reference arm: the fp64 oracle on the host cores, on the headline
     workload.  Each step is a bounded sample of a decode step: one layer of
@@ -697,6 +775,9 @@ def run_reference(args):
             f"{cfg.n_layers} layers")
     line = {"metric": METRIC, "impl": "reference", "value": round(tps, 6), "unit": "tok/s", "n_gpus": args.gpus,
             "steps": K, "warmup": W, "ms_per_step": round(1000.0 * per_tok, 3), "higher_is_better": True,
+            "step_kind": f"one timed step = one layer of the {cfg.n_layers}-layer decode step (a bounded sample); "
+                         f"ms_per_step and value are the per-token figures scaled from the samples",
+            "ms_per_sample": round(1000.0 * t_layer, 3), "ms_lm_head": round(1000.0 * t_head, 3),
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{cfg.name} Q8_0 batch-1 greedy decode, KV ctx {ctx}", "ctx": ctx, "batch": 1},
             "cpu_baseline": {"value": round(tps, 6), "unit": "tok/s", "cores": cores, "kind": "oracle",
@@ -714,7 +795,7 @@ def main():
         if int(os.environ.get("RANK", "0")) != 0:
             return 0
         fn = {"prefill": run_prefill, "fork": run_fork, "stream": run_stream, "skip": run_skip,
-              "spec": run_spec, "kquant": run_kquant, "batch": run_batch}[args.workload]
+              "spec": run_spec, "kquant": run_kquant, "batch": run_batch, "h2d": run_h2d}[args.workload]
         print(json.dumps(fn(args)), flush=True)
         return 0
 
@@ -836,7 +917,9 @@ def main():
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "int32+f32", "data": "synthetic",
+            "arith": "Q8_0 codes x int16-quantised activation slices (16 per lane), exact int32 dot products, fp32 "
+                     "scaling and accumulation; fp16 KV cache, fp32 attention",
             "config": {"workload": f"{cfg.name}-shape {'Q8_0' if cfg.wtype == 8 else 'Q4_0'} batch-1 greedy decode, "
                                    f"{cfg.n_layers} layers, KV ctx {ctx0}..{ctx0 + args.steps}",
                        "ctx": args.ctx, "batch": 1, "weights": "seeded N(0,0.02), quantised Q8_0",

@@ -187,6 +187,9 @@ struct dls_model {
   // programmatic dependent launch between the step's kernels; off by default
   // (measured slower on this path), DLS_PDL=1 turns it on
   bool pdl = false;
+  // streamed layers: copy-engine cudaMemcpyAsync (0), or the SM-driven copy
+  // kernel with this many CTAs on the copy stream (DLS_STREAM_COPY=sm:<ctas>)
+  int stream_sm_ctas = 0;
   std::vector<cudaEvent_t> prof_events;
   std::vector<int> prof_kinds;
   std::string err;
@@ -371,7 +374,15 @@ int prof_mark(dls_model* m, int kind) {
 int enqueue_copy_layer(dls_model* m, int l) {
   const int buf = (l - m->resident) & 1;
   CK(cudaStreamWaitEvent(m->copy_stream, m->ev_free[buf], 0));
-  CK(cudaMemcpyAsync(m->stage[buf], m->layer_host[l], m->lay.bytes, cudaMemcpyHostToDevice, m->copy_stream));
+  void* src_dev = nullptr;
+  if (m->stream_sm_ctas > 0 && m->lay.bytes % 16 == 0 &&
+      cudaHostGetDevicePointer(&src_dev, m->layer_host[l], 0) == cudaSuccess && src_dev) {
+    // the pinned copy is mapped: SM-driven copy over the host link
+    CK(launch_h2d_sm(m->stage[buf], src_dev, m->lay.bytes, m->stream_sm_ctas, m->copy_stream));
+  } else {
+    cudaGetLastError();
+    CK(cudaMemcpyAsync(m->stage[buf], m->layer_host[l], m->lay.bytes, cudaMemcpyHostToDevice, m->copy_stream));
+  }
   CK(cudaEventRecord(m->ev_filled[buf], m->copy_stream));
   return DLS_OK;
 }
@@ -1350,6 +1361,26 @@ int32_t dls_resident_layers(const dls_model* m) { return m ? m->resident : -1; }
 uint64_t dls_layer_bytes(const dls_model* m) { return m ? m->lay.bytes : 0; }
 int32_t dls_debug_launches_per_step(const dls_model* m) { return m ? m->launches_per_step : -1; }
 
+int dls_h2d_copy_sm(void* dst, const void* src_host, size_t bytes, int32_t ctas, void* cuda_stream) {
+  if (!dst || !src_host || ctas < 1 || ctas > 4096)
+    return fail(nullptr, DLS_ERR_ARG, "h2d_copy_sm dst=%p src=%p ctas=%d", dst, src_host, ctas);
+  if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src_host) | bytes) & 15)
+    return fail(nullptr, DLS_ERR_ARG, "h2d_copy_sm: pointers and bytes must be 16-byte multiples (bytes=%zu)", bytes);
+  // the kernel dereferences src on the device: only pinned (page-locked,
+  // mapped) host memory and device memory of this GPU are accepted
+  cudaPointerAttributes as, ad;
+  if (cudaPointerGetAttributes(&as, src_host) != cudaSuccess || cudaPointerGetAttributes(&ad, dst) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(nullptr, DLS_ERR_ARG, "h2d_copy_sm: pointer attributes unavailable");
+  }
+  if (as.type != cudaMemoryTypeHost || !as.devicePointer || ad.type != cudaMemoryTypeDevice)
+    return fail(nullptr, DLS_ERR_ARG, "h2d_copy_sm: src must be pinned host memory, dst device memory "
+                "(types %d, %d)", (int)as.type, (int)ad.type);
+  const cudaError_t e = launch_h2d_sm(dst, as.devicePointer, bytes, ctas, static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return fail(nullptr, DLS_ERR_CUDA, "h2d_copy_sm cuda=%s", cudaGetErrorString(e));
+  return DLS_OK;
+}
+
 int dls_check_context_budget(int32_t prefix_tokens, int32_t max_branch_tokens, int32_t headroom, int32_t n_ctx) {
   dls_model* m = nullptr;
   if (prefix_tokens < 0 || max_branch_tokens < 0 || headroom < 0 || n_ctx < 0)
@@ -1392,6 +1423,8 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
     m->have_alloc = true;
   }
   if (const char* e = getenv("DLS_PDL")) m->pdl = atoi(e) != 0;
+  if (const char* e = getenv("DLS_STREAM_COPY"))
+    if (strncmp(e, "sm:", 3) == 0) m->stream_sm_ctas = std::max(0, std::min(4096, atoi(e + 3)));
   auto bail = [&](int r) {
     std::string e = m->err;
     destroy(m);

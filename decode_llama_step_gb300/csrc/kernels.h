@@ -104,6 +104,8 @@ cudaError_t launch_dequant(const MatDev& m, int wtype, float* out, cudaStream_t 
 // copy whole KV pages: pairs[i] = (src_page, dst_page), for every layer
 cudaError_t launch_kv_copy(__half* k_pool, __half* v_pool, size_t layer_stride_elems, int n_layers,
                            size_t page_elems, const int2* pairs, int n_pairs, cudaStream_t s);
+// host -> device copy by the SMs reading pinned (mapped) host memory; 16-byte aligned, bytes % 16 == 0
+cudaError_t launch_h2d_sm(void* dst, const void* src, size_t bytes, int ctas, cudaStream_t s);
 // a bounded mbarrier wait that is never satisfied: kTimeout into *status after limit_ns
 cudaError_t launch_unarrived_wait(unsigned long long limit_ns, int32_t* status, cudaStream_t s);
 // spin (bounded by the global timer) for `ns` nanoseconds on the stream

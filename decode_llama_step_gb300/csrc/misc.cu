@@ -389,6 +389,31 @@ cudaError_t launch_unarrived_wait(unsigned long long limit_ns, int32_t* status, 
   return cudaGetLastError();
 }
 
+// Host -> device copy driven by the SMs: every thread reads 16-byte words of
+// pinned host memory straight over the host link (four loads in flight per
+// thread before the stores) and writes them to device memory.  Both
+// pointers 16-byte aligned, bytes a multiple of 16 (checked by the caller).
+__global__ void __launch_bounds__(512) h2d_sm_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
+                                                     size_t n16) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = __ldcs(src + i), b = __ldcs(src + i + stride), c = __ldcs(src + i + 2 * stride),
+                d = __ldcs(src + i + 3 * stride);
+    __stcg(dst + i, a);
+    __stcg(dst + i + stride, b);
+    __stcg(dst + i + 2 * stride, c);
+    __stcg(dst + i + 3 * stride, d);
+  }
+  for (; i < n16; i += stride) __stcg(dst + i, __ldcs(src + i));
+}
+
+cudaError_t launch_h2d_sm(void* dst, const void* src, size_t bytes, int ctas, cudaStream_t s) {
+  if (bytes == 0) return cudaSuccess;
+  h2d_sm_kernel<<<ctas, 512, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), bytes / 16);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_delay(long long ns, cudaStream_t s) {
   delay_kernel<<<1, 1, 0, s>>>(ns);
   return cudaGetLastError();

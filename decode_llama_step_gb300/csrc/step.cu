@@ -24,6 +24,7 @@
 // sets a global abort flag that ends all other waits, and a status bit the
 // host reads.  The producer never leaves with copies in flight.
 #include <math.h>
+#include <stdlib.h>
 
 #include "gemv_core.cuh"
 #include "kernels.h"
@@ -41,7 +42,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kTr = 8;               // per-CTA trace slots per phase
 
 // Consumer-side timestamp of this CTA in the current phase (profiling only):
-// slot 4 = prologue done, 5 = last stage consumed, 6 = epilogue done.
+// slot 4 = prologue done, 5 = last stage consumed, 6 = epilogue done, 7 =
+// first stage's data ready (thread 0's warp).
 __device__ __forceinline__ void ctmark(const StepArgs& A, unsigned epoch, int slot) {
   if (A.ctrace && threadIdx.x == 0) A.ctrace[((size_t)epoch * gridDim.x + blockIdx.x) * kTr + slot] = global_ns();
 }
@@ -66,6 +68,7 @@ struct Ctx {
   float* s_wm;     // [NWC][G]
   float* s_wl;     // [NWC][G]
   float* s_wo;     // [NWC][G*HD]
+  __half* s_kvpos; // [2][HD]: K and V of position pos (attention), loaded with q
   int sidx;        // ring stages consumed / produced so far
   int slot;        // sidx % ns
   uint32_t par;    // (sidx / ns) & 1: the phase parity of the current slot's use
@@ -543,6 +546,7 @@ __device__ void consume_gemv(Ctx& c, const MatDev& w, int unit, const float* x, 
   for (int s = 0; s < nst; ++s) {
     const int slot = c.slot;
     const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), c.par, 20);
+    if (s == 0) ctmark(A, c.epoch, 7);
     const int rows_s = min(RS, nrows - s * RS);
     const uint32_t st = smem_u32(c.ring) + (uint32_t)slot * A.stage_bytes;
     float acc[RS];
@@ -671,9 +675,22 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
   const bool has_task = (int)blockIdx.x < A.n_kv * A.S;
   const int sp = blockIdx.x % A.S;
   const float scale = 1.0f / sqrtf((float)HD);
+  // the tile holding position pos (written by this step's QKV phase, so not
+  // in the ring): its K and V rows are loaded here, beside q, rather than
+  // after the stage arrives, which keeps that L2 round trip off the
+  // critical path of the CTA that holds the newest tile
+  const int pos_tile = c.pos / kTile;
+  const bool has_pos = has_task && pos_tile >= tb && pos_tile < te && c.pos_page >= 0;
   if (has_task) {
     const float* qrow = A.q + (size_t)kvh * G * HD;
     for (int i = tid; i < G * HD; i += NWC * 32) c.s_q[i] = __ldcg(qrow + i) * scale;
+    if (has_pos) {
+      const size_t off = (((size_t)c.pos_page * A.n_kv + kvh) * A.page_tokens + (c.pos % A.page_tokens)) * HD;
+      for (int i = tid; i < HD / 2; i += NWC * 32) {
+        reinterpret_cast<__half2*>(c.s_kvpos)[i] = __ldcg(reinterpret_cast<const __half2*>(k_pool + off) + i);
+        reinterpret_cast<__half2*>(c.s_kvpos + HD)[i] = __ldcg(reinterpret_cast<const __half2*>(v_pool + off) + i);
+      }
+    }
   }
   named_bar(1, NWC * 32);
   ctmark(A, c.epoch, 4);
@@ -693,34 +710,38 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
     if ((j & 1) == par && t < te) {
       const int nt = min(kTile, n - t * kTile);
       const bool ok = wait_bar(A, smem_u32(&c.sh->full[slot]), c.par, 20);
+      if (j == 0) ctmark(A, c.epoch, 7);
       __half* kt = reinterpret_cast<__half*>(c.ring + (size_t)slot * A.stage_bytes) + 2 * tis * kTile * HD;
       __half* vt = kt + kTile * HD;
       const int jp = c.pos - t * kTile;  // the new position inside this tile, if any
-      if (jp >= 0 && jp < kTile && c.pos_page >= 0) {
-        // the two head-group warps of this tile write the same bytes; each reads its own
-        const size_t off = (((size_t)c.pos_page * A.n_kv + kvh) * A.page_tokens + (c.pos % A.page_tokens)) * HD;
+      if (has_pos && t == pos_tile) {
+        // the two head-group warps of this tile write the same bytes
         for (int i = lane; i < HD / 2; i += 32) {
-          reinterpret_cast<__half2*>(kt + jp * HD)[i] = __ldcg(reinterpret_cast<const __half2*>(k_pool + off) + i);
-          reinterpret_cast<__half2*>(vt + jp * HD)[i] = __ldcg(reinterpret_cast<const __half2*>(v_pool + off) + i);
+          reinterpret_cast<__half2*>(kt + jp * HD)[i] = reinterpret_cast<const __half2*>(c.s_kvpos)[i];
+          reinterpret_cast<__half2*>(vt + jp * HD)[i] = reinterpret_cast<const __half2*>(c.s_kvpos + HD)[i];
         }
         __syncwarp();
       }
       if (ok) {
         float sc[HPW];
         {
-          float2 acc[HPW];
+          // two accumulator chains per head halve the dependent FMA chain
+          float2 acc[HPW][2];
 #pragma unroll
-          for (int h = 0; h < HPW; ++h) acc[h] = make_float2(0.f, 0.f);
+          for (int h = 0; h < HPW; ++h) acc[h][0] = acc[h][1] = make_float2(0.f, 0.f);
           const __half2* krow = reinterpret_cast<const __half2*>(kt + lane * HD);
-#pragma unroll 4
+#pragma unroll 8
           for (int w2 = 0; w2 < W2; ++w2) {
             const int wi = (w2 + lane) & (W2 - 1);
             const float2 kf = __half22float2(krow[wi]);
 #pragma unroll
-            for (int h = 0; h < HPW; ++h) acc[h] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h]);
+            for (int h = 0; h < HPW; ++h) acc[h][w2 & 1] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h][w2 & 1]);
           }
 #pragma unroll
-          for (int h = 0; h < HPW; ++h) sc[h] = lane < nt ? acc[h].x + acc[h].y : -INFINITY;
+          for (int h = 0; h < HPW; ++h) {
+            const float2 a = __fadd2_rn(acc[h][0], acc[h][1]);
+            sc[h] = lane < nt ? a.x + a.y : -INFINITY;
+          }
         }
         float p[HPW];
 #pragma unroll
@@ -733,11 +754,17 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
 #pragma unroll
           for (int e = 0; e < DPL; ++e) o[h][e] *= al;
         }
+        // o += P V over the tile's tokens, fully unrolled and branch-free so
+        // the V loads and the p broadcasts of all 32 tokens are in flight
+        // together; rows past nt hold stale bytes and are zeroed (their p
+        // is 0 too)
         const __half* vl = vt + lane * DPL;
-        for (int jj = 0; jj < nt; ++jj) {
+#pragma unroll
+        for (int jj = 0; jj < kTile; ++jj) {
           float vf[DPL];
           if (DPL == 4) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(vl + jj * HD);
+            uint2 raw = *reinterpret_cast<const uint2*>(vl + jj * HD);
+            if (jj >= nt) raw = make_uint2(0u, 0u);
             const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
             const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
             vf[0] = v01.x;
@@ -746,7 +773,7 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
             vf[3 % DPL] = v23.y;
           } else {
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) vf[e] = __half2float(vl[jj * HD + e]);
+            for (int e = 0; e < DPL; ++e) vf[e] = jj < nt ? __half2float(vl[jj * HD + e]) : 0.f;
           }
 #pragma unroll
           for (int h = 0; h < HPW; ++h) {
@@ -756,9 +783,10 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
           }
         }
       }
-      // generic writes into the slot above must be ordered before the next
-      // bulk copy into it
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      // the generic writes of the new position's row into the slot must be
+      // ordered before the next bulk copy into it (a slot that was only read
+      // needs no proxy fence: the empty-barrier arrival orders the reads)
+      if (has_pos && t == pos_tile) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
     }
     if (lane == 0) mbar_arrive(smem_u32(&c.sh->empty[slot]));
@@ -827,20 +855,28 @@ __device__ void consume_attention(Ctx& c, const __half* k_pool, const __half* v_
         pv[oi][k] = (one_round && k < A.S && idx < G * HD) ? __ldcg(A.part_o + (slot0 + k) * G * HD + idx) : 0.f;
     }
     for (int h = warp; h < G; h += NWC) {
+      // each lane holds up to kMl splits' (m, l) pairs: one round of loads
+      constexpr int kMl = 4;
+      float2 v[kMl];
       float M = -INFINITY;
-      for (int s2 = lane; s2 < A.S; s2 += 32) M = fmaxf(M, __ldcg(&ml[(slot0 + s2) * G + h]).x);
+#pragma unroll
+      for (int k = 0; k < kMl; ++k) {
+        const int s2 = lane + 32 * k;
+        v[k] = s2 < A.S ? __ldcg(&ml[(slot0 + s2) * G + h]) : make_float2(-INFINITY, 0.f);
+        M = fmaxf(M, v[k].x);
+      }
       M = warp_max_f(M);
-      float den = 0.f;
-      for (int s2 = lane; s2 < A.S; s2 += 32) {
-        const float2 v = __ldcg(&ml[(slot0 + s2) * G + h]);
-        const float ew = v.y > 0.f ? expf(v.x - M) : 0.f;  // empty split: weight 0
-        s_w[h * A.S + s2] = ew;
-        den = fmaf(v.y, ew, den);
+      float den = 0.f, ew[kMl];
+#pragma unroll
+      for (int k = 0; k < kMl; ++k) {
+        ew[k] = v[k].y > 0.f ? expf(v[k].x - M) : 0.f;  // empty split: weight 0
+        den = fmaf(v[k].y, ew[k], den);
       }
       den = warp_sum(den);
       const float inv = 1.0f / den;
-      __syncwarp();
-      for (int s2 = lane; s2 < A.S; s2 += 32) s_w[h * A.S + s2] *= inv;
+#pragma unroll
+      for (int k = 0; k < kMl; ++k)
+        if (lane + 32 * k < A.S) s_w[h * A.S + lane + 32 * k] = ew[k] * inv;
     }
     named_bar(1, NWC * 32);
 #pragma unroll
@@ -886,6 +922,8 @@ __global__ void __maxnreg__(200) step_kernel(const StepArgs A) {
   off += NWC * G * 4;
   c.s_wo = reinterpret_cast<float*>(smem + off);
   off += NWC * G * HD * 4;
+  c.s_kvpos = reinterpret_cast<__half*>(smem + off);
+  off += 2 * HD * 2;
   c.ring = smem + ((off + 127) & ~(size_t)127);
   c.sidx = 0;
   c.slot = 0;
@@ -1088,11 +1126,13 @@ StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, i
   size_t stage = std::max((size_t)rsa * (rb_h + ds_h * 2), (size_t)rsb * (rb_f + ds_f * 2));
   stage = std::max(stage, (size_t)4 * kTile * hd * 2);  // two K/V tiles
   stage = (stage + 127) & ~(size_t)127;
-  size_t head = ((sizeof(Sh) + 127) & ~(size_t)127) + NWC * kRB * 4 + G * hd * 4 + 2 * NWC * G * 4 + NWC * G * hd * 4;
+  size_t head = ((sizeof(Sh) + 127) & ~(size_t)127) + NWC * kRB * 4 + G * hd * 4 + 2 * NWC * G * 4 + NWC * G * hd * 4 +
+                2 * hd * 2;
   head = (head + 127) & ~(size_t)127;
   const size_t budget = 220 * 1024;
   int ns = (int)((budget - head) / stage);
   ns = std::min(ns, kMaxStages);
+  if (const char* e = getenv("DLS_STEP_STAGES")) ns = std::min(ns, std::max(2, atoi(e)));  // tuning knob
   if (ns < 2) {
     p.fn = nullptr;
     return p;
@@ -1102,7 +1142,7 @@ StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, i
   p.smem = (int)(head + ns * stage);
   p.grid = num_sms;
   p.threads = NTHR;
-  p.splits = num_sms / n_kv;
+  p.splits = std::min(num_sms / n_kv, 128);  // the merge holds up to 4 x 32 splits' (m, l) pairs per warp
   if (p.splits < 1) {
     p.fn = nullptr;
     return p;

@@ -76,6 +76,7 @@ _SIGS = {
     "dls_verify": (ctypes.c_int, [vp, i32, vp, i32, vp, vp]),
     "dls_generate_speculative": (ctypes.c_int, [vp, i32, i32, i32, vp, i32, vp, vp]),
     "dls_check_context_budget": (ctypes.c_int, [i32, i32, i32, i32]),
+    "dls_h2d_copy_sm": (ctypes.c_int, [vp, vp, sz, i32, vp]),
     "dls_set_resident_layers": (ctypes.c_int, [vp, i32]),
     "dls_resident_layers": (i32, [vp]),
     "dls_layer_bytes": (u64, [vp]),
@@ -152,6 +153,11 @@ def _check(rc: int, model_handle=None):
 
 def status_name(code: int) -> str:
     return load().dls_status_name(code).decode()
+
+
+def h2d_copy_sm(dst, src_host, nbytes: int, ctas: int = 64, stream=None):
+    """Copy pinned host memory to the device with an SM-driven kernel."""
+    _check(load().dls_h2d_copy_sm(_ptr(dst), _ptr(src_host), int(nbytes), int(ctas), _stream_handle(stream)))
 
 
 def check_context_budget(prefix_tokens: int, max_branch_tokens: int, headroom: int, n_ctx: int) -> None:

@@ -158,7 +158,7 @@ int32_t dls_seq_length(const dls_model* m, int32_t seq);
 /* Run n prompt tokens (host int32 [n], each in [0, vocab)) through every
  * layer at positions length..length+n-1 of `seq`, filling its KV cache
  * (SwarmKV, section 2: prefill computes and stores the K/V of every prompt
- * token once).  The tokens go through in chunks of up to 1024 (the
+ * token once).  The tokens go through in chunks of up to 2048 (the
  * environment variable DLS_PREFILL_CHUNK, read at model creation, sets
  * another size): each projection of a chunk is one tensor-core GEMM with
  * split fp16 operands (weights d*q and activations each as an fp16 value
@@ -179,10 +179,15 @@ int dls_decode_step(dls_model* m, int32_t seq, int32_t token, int32_t pos, float
 /* n decode steps in one pass over the weights (1 <= n <= max_batch): row i
  * is token tokens[i] of sequence seqs[i] at position pos[i] (host arrays;
  * distinct sequences).  logits_out: host or device fp32 [n][vocab] or NULL.
- * With n >= 2 every projection is one tensor-core GEMM over the n rows
- * (fp16 operands as in dls_prefill, fp32 accumulation), so each weight byte
- * is read once per step for the whole batch (SwarmKV, section 4: the
- * branches of a fork decode together); n = 1 is dls_decode_step. */
+ * With n >= 2 each projection is one pass over the weights for all n rows,
+ * so each weight byte is read once per step for the whole batch (SwarmKV,
+ * section 4: the branches of a fork decode together): for n = 2..4 a
+ * multi-row CUDA-core dequant-GEMV (exact int32 code x int16-slice
+ * products, fp32 scaling), for n = 5..8 a tensor-core GEMM with the raw
+ * codes as exact fp16 operands and the activations as hi + lo fp16 planes,
+ * fp32 accumulation (the environment variable DLS_BATCH_GEMM=rg or tc,
+ * read at model creation, forces one of the two); n = 1 is
+ * dls_decode_step. */
 int dls_decode_batch(dls_model* m, int32_t n, const int32_t* seqs, const int32_t* tokens, const int32_t* pos,
                      float* logits_out);
 
@@ -292,6 +297,16 @@ int32_t dls_resident_layers(const dls_model* m);
 /* Bytes of one layer's weights as the kernels read them (the per-layer H2D
  * transfer of a streamed layer). */
 uint64_t dls_layer_bytes(const dls_model* m);
+
+/* Host -> device copy performed by `ctas` CTAs of 512 threads that read the
+ * pinned host buffer directly over the host link (on a Grace host, NVLink-C2C)
+ * instead of through the copy engines that cudaMemcpyAsync uses (the engine
+ * page, sections 3.3 and 4.2: streamed layers are bound by the host link, so
+ * the faster path matters).  src_host: pinned host memory (cudaHostAlloc or
+ * registered); dst: device memory; both 16-byte aligned, bytes a multiple of
+ * 16.  Enqueued on cuda_stream.  DLS_ERR_ARG for any other pointer kind
+ * (checked with cudaPointerGetAttributes before anything is launched). */
+int dls_h2d_copy_sm(void* dst, const void* src_host, size_t bytes, int32_t ctas, void* cuda_stream);
 
 /* ---- standalone op ----------------------------------------------------------- */
 
@@ -443,7 +458,7 @@ int dls_debug_profile_batch(dls_model* m, int32_t n, const int32_t* seqs, const 
  * the persistent step kernel: [phase][cta][8] = {consumer arrival at the
  * grid barrier that ends the phase, its release, producer's first issue of
  * the phase's copies, producer's last issue, consumers' prologue done, last
- * stage consumed, epilogue done, unused}; phase 0 is the embedding,
+ * stage consumed, epilogue done, first stage's data ready}; phase 0 is the embedding,
  * 1 + 5 l + k layer l's k-th phase (QKV, attention, O, gate/up, down), then
  * the LM head.  Entries not written hold stale values.  Copies
  * (5 n_layers + 8) * grid * 8 values to host `out`; DLS_ERR_STATE when the
