@@ -235,10 +235,24 @@ def run_fork(args):
             e["ms_per_step"] = round(e["ms_per_step"] + float(d_ms), 4)
         for d in dsts:
             m.seq_free(d)
-        # the shared-prefix form of the fork: full pages by reference
+        # the shared-prefix form of the fork: full pages by reference, and
+        # the batched steps' attention over the prefix runs once for all
+        # branches (cascade attention)
+        dsts = [m.seq_create() for _ in range(B)]
+        m.kv_fork(src, dsts, shared=True)
+        m.generate(dsts, start, 2)  # capture the cascade graph outside the timing
+        for d in dsts:
+            m.seq_free(d)
         dsts = [m.seq_create() for _ in range(B)]
         t_fork_sh = _events(torch, stream, lambda: m.kv_fork(src, dsts, shared=True))
         t_dec_sh = _events(torch, stream, lambda: m.generate(dsts, start, D))
+        kms, kk = m.profile_batch(dsts, start, [m.seq_length(d) for d in dsts])
+        per_kind_sh = {}
+        for d_ms, k in zip(kms, kk):
+            e = per_kind_sh.setdefault(KIND_NAMES.get(int(k), str(int(k))), {"launches_per_step": 0,
+                                                                              "ms_per_step": 0.0})
+            e["launches_per_step"] += 1
+            e["ms_per_step"] = round(e["ms_per_step"] + float(d_ms), 4)
         for d in dsts:
             m.seq_free(d)
         m.seq_free(src)
@@ -267,7 +281,8 @@ def run_fork(args):
                                                 "decode_ms": round(1000 * t_dec_sh, 2),
                                                 "decode_tok_s": round(B * D / t_dec_sh, 1),
                                                 "fork_path_s": round(shared_path, 4),
-                                                "speedup_vs_independent": round(indep_path / shared_path, 3)}},
+                                                "speedup_vs_independent": round(indep_path / shared_path, 3),
+                                                "kernels": per_kind_sh}},
                       "kernels": per_kind, "clocks": clk.summary()})
 
 

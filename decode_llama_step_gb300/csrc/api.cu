@@ -81,7 +81,9 @@ struct Seq {
 struct GraphEntry {
   int rows;
   bool head, argmax, drafting;
+  int casc;  // suffix split count of a cascade step (0: no shared prefix)
   cudaGraphExec_t exec;
+  int launches;  // kernels in the graph
 };
 
 }  // namespace
@@ -158,6 +160,13 @@ struct dls_model {
   float *part_o_b = nullptr, *part_ml_b = nullptr;
   int* counters_b = nullptr;
   int attn_splits_b = 1;
+  // cascade attention for batched steps whose rows share leading KV pages
+  // (DLS_CASCADE=0 turns it off): prefix partials, their split count, and
+  // this step's shared length (0 = none) and suffix split count
+  float *casc_o = nullptr, *casc_ml = nullptr;
+  int casc_splits = 0;
+  bool cascade = true;
+  int casc_len = 0, casc_suffix_splits = 0;
   bool batch_tc = false;  // every batched step through the small-batch tensor-core GEMM
   bool batch_rg = false;  // every batched step through the multi-row GEMV
   std::map<std::tuple<int, int, int>, RgLaunch> rg_plans;  // (matrix kind, rows, T) -> multi-row GEMV plan
@@ -687,6 +696,63 @@ int enqueue_batch_tc(dls_model* m, int n, bool head, bool argmax, float* capture
 
 // Batched step through the multi-row CUDA-core GEMV: fp32 activations end to
 // end, RMSNorm fused into the projections that follow it.
+// Split-K attention of a batched step, one row per (sequence, position); q
+// in pf_q, o to m->o.  With a shared prefix (m->casc_len > 0) the cascade
+// kernel first covers the prefix once for all rows, and the per-row launch
+// covers the rest and merges both parts.
+int enqueue_batch_attention(dls_model* m, const KvView& kv, int n) {
+  cudaStream_t s = m->stream;
+  AttnArgs a{};
+  a.q = m->pf_q;
+  a.o = m->o;
+  a.k_pool = kv.k_pool;
+  a.v_pool = kv.v_pool;
+  a.page_table = m->pt_dev;
+  a.max_pages = m->max_pages;
+  a.pt_row = m->sp->seq;
+  a.len = m->sp->pos;
+  a.len_add = 1;
+  a.n_heads = m->nh;
+  a.n_kv = m->nkv;
+  a.head_dim = m->hd;
+  a.page_tokens = m->pt;
+  a.n_splits = m->attn_splits_b;
+  a.row0 = 0;
+  a.part_o = m->part_o_b;
+  a.part_ml = m->part_ml_b;
+  a.counters = m->counters_b;
+  a.status = &m->sp->status;
+  a.max_len = m->max_ctx;
+  if (m->casc_len > 0) {
+    CascArgs c{};
+    c.q = m->pf_q;
+    c.k_pool = kv.k_pool;
+    c.v_pool = kv.v_pool;
+    c.page_table = m->pt_dev;
+    c.max_pages = m->max_pages;
+    c.pt_row = m->sp->seq;
+    c.shared_len = &m->sp->shared_len;
+    c.rows = n;
+    c.n_heads = m->nh;
+    c.n_kv = m->nkv;
+    c.head_dim = m->hd;
+    c.page_tokens = m->pt;
+    c.n_splits = m->casc_splits;
+    c.part_o = m->casc_o;
+    c.part_ml = m->casc_ml;
+    c.status = &m->sp->status;
+    c.max_len = m->max_ctx;
+    LK(K_ATTN, launch_cascade_prefix(c, s));
+    a.start_len = &m->sp->shared_len;
+    a.pre_o = m->casc_o;
+    a.pre_ml = m->casc_ml;
+    a.pre_splits = m->casc_splits;
+    a.n_splits = m->casc_suffix_splits;
+  }
+  LK(K_ATTN, launch_attention(a, n, s, false));
+  return DLS_OK;
+}
+
 int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
   if (m->batch_tc || (n > kRgMaxRows && !m->batch_rg)) return enqueue_batch_tc(m, n, head, argmax, capture);
   cudaStream_t s = m->stream;
@@ -721,28 +787,7 @@ int enqueue_batch(dls_model* m, int n, bool head, bool argmax, float* capture) {
     LK(K_QKV, launch_rope_kv_batch(m->pf_qkv, n, qkv_ld, m->q_rows, m->kv_rows, kv, m->sp->seq, m->sp->pos, m->rope,
                                    m->rope_len, m->pf_q, &m->sp->status, s));
     // (2) split-K attention, one row per (sequence, position)
-    AttnArgs a{};
-    a.q = m->pf_q;
-    a.o = m->o;
-    a.k_pool = kv.k_pool;
-    a.v_pool = kv.v_pool;
-    a.page_table = m->pt_dev;
-    a.max_pages = m->max_pages;
-    a.pt_row = m->sp->seq;
-    a.len = m->sp->pos;
-    a.len_add = 1;
-    a.n_heads = m->nh;
-    a.n_kv = m->nkv;
-    a.head_dim = m->hd;
-    a.page_tokens = m->pt;
-    a.n_splits = m->attn_splits_b;
-    a.row0 = 0;
-    a.part_o = m->part_o_b;
-    a.part_ml = m->part_ml_b;
-    a.counters = m->counters_b;
-    a.status = &m->sp->status;
-    a.max_len = m->max_ctx;
-    LK(K_ATTN, launch_attention(a, n, s, false));
+    TRY(enqueue_batch_attention(m, kv, n));
     // (3) O projection + residual
     RgArgs go = g;
     go.w = P.o;
@@ -821,28 +866,7 @@ int enqueue_batch_tc(dls_model* m, int n, bool head, bool argmax, float* capture
     LK(K_QKV, launch_rope_kv_batch(m->pf_qkv, n, qkv_ld, m->q_rows, m->kv_rows, kv, m->sp->seq, m->sp->pos, m->rope,
                                    m->rope_len, m->pf_q, &m->sp->status, s));
     // (2) split-K attention, one row per sequence
-    AttnArgs a{};
-    a.q = m->pf_q;
-    a.o = m->o;
-    a.k_pool = kv.k_pool;
-    a.v_pool = kv.v_pool;
-    a.page_table = m->pt_dev;
-    a.max_pages = m->max_pages;
-    a.pt_row = m->sp->seq;
-    a.len = m->sp->pos;
-    a.len_add = 1;
-    a.n_heads = m->nh;
-    a.n_kv = m->nkv;
-    a.head_dim = m->hd;
-    a.page_tokens = m->pt;
-    a.n_splits = m->attn_splits_b;
-    a.row0 = 0;
-    a.part_o = m->part_o_b;
-    a.part_ml = m->part_ml_b;
-    a.counters = m->counters_b;
-    a.status = &m->sp->status;
-    a.max_len = m->max_ctx;
-    LK(K_ATTN, launch_attention(a, n, s, false));
+    TRY(enqueue_batch_attention(m, kv, n));
     // (3) O GEMM + residual
     LK(K_O, launch_to_f16_rows(m->o, n, m->q_rows, m->q_rows, m->pf_a, m->pf_a_lo, m->q_rows, s));
     PgArgs go = g;
@@ -982,8 +1006,10 @@ int run_step(dls_model* m, int rows, bool head, bool argmax) {
   const bool persistent = m->use_step && rows == 1;
   if (persistent && !m->step_graph_ok) return enqueue_step(m, rows, head, argmax, nullptr);
   for (auto& g : m->graphs)
-    if (g.rows == rows && g.head == head && g.argmax == argmax && g.drafting == m->drafting) {
+    if (g.rows == rows && g.head == head && g.argmax == argmax && g.drafting == m->drafting &&
+        g.casc == (rows >= 2 ? m->casc_suffix_splits : 0)) {
       CK(cudaGraphLaunch(g.exec, m->stream));
+      m->launches_per_step = g.launches;
       return DLS_OK;
     }
   cudaGraph_t graph = nullptr;
@@ -1001,7 +1027,8 @@ int run_step(dls_model* m, int rows, bool head, bool argmax) {
   }
   if (r != DLS_OK) return r;
   if (e != cudaSuccess) return fail(m, DLS_ERR_CUDA, "capture cuda=%s", cudaGetErrorString(e));
-  m->graphs.push_back({rows, head, argmax, m->drafting, exec});
+  m->graphs.push_back({rows, head, argmax, m->drafting, rows >= 2 ? m->casc_suffix_splits : 0, exec,
+                       m->launches_per_step});
   CK(cudaGraphLaunch(exec, m->stream));
   return DLS_OK;
 }
@@ -1063,6 +1090,29 @@ int check_seq(dls_model* m, int seq) {
   return DLS_OK;
 }
 
+// Positions [0, len) that every row of a batched step reads from the same
+// physical KV pages (a shared fork, or rows of one sequence): whole leading
+// pages common to all rows, no further than the shortest row's length,
+// rounded down to whole 32-token tiles.  0 below four tiles (not worth the
+// extra launch) or with the cascade off.
+int shared_prefix_len(const dls_model* m, int n, const int32_t* seqs, const int32_t* pos) {
+  if (n < 2 || !m->cascade || !m->casc_o) return 0;
+  int minpos = pos[0];
+  for (int i = 1; i < n; ++i) minpos = std::min(minpos, pos[i]);
+  const std::vector<int>& p0 = m->seqs[seqs[0]].pages;
+  int k = 0;
+  for (; k < (int)p0.size(); ++k) {
+    bool same = true;
+    for (int i = 1; i < n && same; ++i) {
+      const std::vector<int>& pi = m->seqs[seqs[i]].pages;
+      same = k < (int)pi.size() && pi[k] == p0[k];
+    }
+    if (!same) break;
+  }
+  const int len = std::min(k * m->pt, minpos) / 32 * 32;
+  return len >= 128 ? len : 0;
+}
+
 int set_params(dls_model* m, int n, const int32_t* seqs, const int32_t* tokens, const int32_t* pos, bool reset) {
   StepParams h{};
   h.n = n;
@@ -1070,6 +1120,14 @@ int set_params(dls_model* m, int n, const int32_t* seqs, const int32_t* tokens, 
     h.seq[i] = seqs[i];
     h.token[i] = tokens[i];
     h.pos[i] = pos[i];
+  }
+  h.shared_len = shared_prefix_len(m, n, seqs, pos);
+  m->casc_len = h.shared_len;
+  m->casc_suffix_splits = 0;
+  if (m->casc_len > 0) {
+    // the per-row launch only covers the keys after the shared prefix
+    const int s = attn_default_splits(n, m->nkv, m->num_sms, m->max_ctx - m->casc_len);
+    m->casc_suffix_splits = std::max(1, std::min(std::min(s, m->attn_splits_b), 128 - m->casc_splits));
   }
   CK(launch_set_params(m->sp, h, reset, m->stream));
   return DLS_OK;
@@ -1561,6 +1619,15 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
     attn_workspace_carve(m->attn_ws_b, BR, m->nh, m->nkv, m->hd, m->attn_splits_b, &m->part_o_b, &m->part_ml_b,
                          &m->counters_b);
     CKC(cudaMemsetAsync(m->counters_b, 0, (size_t)BR * m->nkv * sizeof(int), m->stream));
+  }
+  if (const char* e = getenv("DLS_CASCADE")) m->cascade = atoi(e) != 0;
+  if (BR >= 2 && cascade_supported(m->nh, m->nkv, m->hd)) {
+    // prefix partials of cascade attention: [rows][n_kv][splits][group][head_dim]
+    m->casc_splits = std::max(1, std::min(2 * m->num_sms / m->nkv, 64));  // two CTAs per SM
+    const size_t slots = (size_t)std::min(BR, kMaxBatch) * m->nkv * m->casc_splits;
+    const int g = m->nh / m->nkv;
+    TRYC(dev_alloc_t(m, slots * g * m->hd, &m->casc_o, "cascade_partials"));
+    TRYC(dev_alloc_t(m, slots * g * 2, &m->casc_ml, "cascade_ml"));
   }
   {
     // split-K partials for batches of up to 16 rows: [split][16][rows]

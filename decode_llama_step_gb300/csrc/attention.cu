@@ -37,6 +37,73 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// One warp's online-softmax update over one 32-token tile staged in shared
+// memory (K rows at kt, V rows at vt, head_dim halves each), for HPW query
+// heads whose pre-scaled q lies at q2 (float2 words, HD/2 per head).  Scores
+// take one lane per token (the head dimension walked from a lane-dependent
+// start, so the 32 lanes hit 32 different banks) in two accumulator chains;
+// P V gives each lane HD/32 output dimensions, unrolled over the tile with
+// rows past nt zeroed (their p is 0 as well).
+template <int HD, int HPW>
+__device__ __forceinline__ void tile_update(const __half* kt, const __half* vt, const float2* q2, int nt, int lane,
+                                            float (&m_run)[HPW], float (&l_run)[HPW], float (&o)[HPW][HD / 32]) {
+  constexpr int DPL = HD / 32, W2 = HD / 2;
+  float sc[HPW];
+  {
+    float2 acc[HPW][2];
+#pragma unroll
+    for (int h = 0; h < HPW; ++h) acc[h][0] = acc[h][1] = make_float2(0.f, 0.f);
+    const __half2* krow = reinterpret_cast<const __half2*>(kt + lane * HD);
+#pragma unroll 8
+    for (int w2 = 0; w2 < W2; ++w2) {
+      const int wi = (w2 + lane) & (W2 - 1);
+      const float2 kf = __half22float2(krow[wi]);
+#pragma unroll
+      for (int h = 0; h < HPW; ++h) acc[h][w2 & 1] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h][w2 & 1]);
+    }
+#pragma unroll
+    for (int h = 0; h < HPW; ++h) {
+      const float2 a = __fadd2_rn(acc[h][0], acc[h][1]);
+      sc[h] = lane < nt ? a.x + a.y : -INFINITY;
+    }
+  }
+  float p[HPW];
+#pragma unroll
+  for (int h = 0; h < HPW; ++h) {
+    const float m_new = fmaxf(m_run[h], warp_max(sc[h]));
+    p[h] = lane < nt ? expf(sc[h] - m_new) : 0.f;
+    const float al = expf(m_run[h] - m_new);  // 0 on the warp's first tile
+    l_run[h] = l_run[h] * al + warp_sum(p[h]);
+    m_run[h] = m_new;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[h][e] *= al;
+  }
+  const __half* vl = vt + lane * DPL;
+#pragma unroll
+  for (int j = 0; j < TILE; ++j) {
+    float vf[DPL];
+    if (DPL == 4) {
+      uint2 raw = *reinterpret_cast<const uint2*>(vl + j * HD);
+      if (j >= nt) raw = make_uint2(0u, 0u);
+      const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+      const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+      vf[0] = v01.x;
+      vf[1] = v01.y;
+      vf[2 % DPL] = v23.x;
+      vf[3 % DPL] = v23.y;
+    } else {
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) vf[e] = j < nt ? __half2float(vl[j * HD + e]) : 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < HPW; ++h) {
+      const float pj = __shfl_sync(0xffffffffu, p[h], j);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pj, vf[e], o[h][e]);
+    }
+  }
+}
+
 // CTA (kv head, split sp) covers a contiguous run of 32-token tiles of one
 // sequence.  Its 8 warps form TS tile slots x HG head groups: warp w works
 // on tiles slot, slot + TS, ... (slot = w % TS) for the query heads of group
@@ -83,8 +150,12 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   const int ptrow = a.pt_row ? a.pt_row[b] : b;
   const int32_t* ptab = a.page_table + (size_t)ptrow * a.max_pages;
   const int n_tiles = (n + TILE - 1) / TILE;
-  const int per = (n_tiles + S - 1) / S;
-  const int tb = sp * per, te = min(n_tiles, tb + per);
+  // with a shared prefix computed by the cascade kernel, this launch covers
+  // only the tiles from the prefix's end on
+  int t0 = 0;
+  if (a.start_len) t0 = min(max(*a.start_len, 0), n) / TILE;
+  const int per = (n_tiles - t0 + S - 1) / S;
+  const int tb = t0 + sp * per, te = min(n_tiles, tb + per);
 
   // the first warp of a slot copies tile i (K then V) into the slot's stage
   __half* st = s_stage + (size_t)slot * STAGE;
@@ -127,58 +198,7 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   for (int i = tb + slot; i < te; i += TS, ++use) {
     const int nt = min(TILE, n - i * TILE);
     if (!mbar_wait(bar, use & 1)) failed = true;
-    // ---- scores, lane = token
-    float sc[HPW];
-    {
-      float2 acc[HPW];
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) acc[h] = make_float2(0.f, 0.f);
-      const __half2* krow = reinterpret_cast<const __half2*>(st + lane * HD);
-#pragma unroll 4
-      for (int w2 = 0; w2 < W2; ++w2) {
-        const int wi = (w2 + lane) & (W2 - 1);
-        const float2 kf = __half22float2(krow[wi]);
-#pragma unroll
-        for (int h = 0; h < HPW; ++h) acc[h] = __ffma2_rn(kf, q2[h * W2 + wi], acc[h]);
-      }
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) sc[h] = lane < nt ? acc[h].x + acc[h].y : -INFINITY;
-    }
-    // ---- online softmax (per head, in registers)
-    float p[HPW];
-#pragma unroll
-    for (int h = 0; h < HPW; ++h) {
-      const float m_new = fmaxf(m_run[h], warp_max(sc[h]));
-      p[h] = lane < nt ? expf(sc[h] - m_new) : 0.f;
-      const float al = expf(m_run[h] - m_new);  // 0 on the warp's first tile
-      l_run[h] = l_run[h] * al + warp_sum(p[h]);
-      m_run[h] = m_new;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) o[h][e] *= al;
-    }
-    // ---- o += P V, lane = DPL dims
-    const __half* vt = st + TILE * HD + lane * DPL;
-    for (int j = 0; j < nt; ++j) {
-      float vf[DPL];
-      if (DPL == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(vt + j * HD);
-        const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-        const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-        vf[0] = v01.x;
-        vf[1] = v01.y;
-        vf[2 % DPL] = v23.x;
-        vf[3 % DPL] = v23.y;
-      } else {
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) vf[e] = __half2float(vt[j * HD + e]);
-      }
-#pragma unroll
-      for (int h = 0; h < HPW; ++h) {
-        const float pj = __shfl_sync(0xffffffffu, p[h], j);
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pj, vf[e], o[h][e]);
-      }
-    }
+    tile_update<HD, HPW>(st, st + TILE * HD, q2, nt, lane, m_run, l_run, o);
     // both warps of the slot are done with the stage before it is refilled
     if (HG > 1) named_bar(1 + slot, 32 * HG);
     else __syncwarp();
@@ -229,32 +249,242 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  // ---- last CTA of this (row, kv head): merge the S splits, all loads in flight
+  // ---- last CTA of this (row, kv head): merge the S splits (and the P
+  // splits of the shared prefix from the cascade kernel, after them in split
+  // order), all loads in flight
+  const int P = a.pre_splits;
+  const size_t pslot0 = ((size_t)brel * a.n_kv + kvh) * (size_t)P;
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+  const float2* pml = reinterpret_cast<const float2*>(a.pre_ml);
   for (int h = warp; h < G; h += NW) {
+    // every lane's (at most four) splits in one round of loads
+    float2 v[kMaxSplits / 32];
     float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(&ml[(slot0 + s) * G + h]).x);
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) {
+      const int s = lane + 32 * k;
+      v[k] = s < S ? __ldcg(&ml[(slot0 + s) * G + h])
+           : s < S + P ? __ldcg(&pml[(pslot0 + s - S) * G + h]) : make_float2(-INFINITY, 0.f);
+      M = fmaxf(M, v[k].x);
+    }
     M = warp_max(M);
-    float den = 0.f;
-    for (int s = lane; s < S; s += 32) {
-      const float2 v = __ldcg(&ml[(slot0 + s) * G + h]);
-      const float e = v.y > 0.f ? expf(v.x - M) : 0.f;  // empty split: weight 0
-      s_w[h][s] = e;
-      den = fmaf(v.y, e, den);
+    float den = 0.f, e[kMaxSplits / 32];
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) {
+      e[k] = v[k].y > 0.f ? expf(v[k].x - M) : 0.f;  // empty split: weight 0
+      den = fmaf(v[k].y, e[k], den);
     }
     den = warp_sum(den);
-    for (int s = lane; s < S; s += 32) s_w[h][s] /= den;
+    const float inv = 1.0f / den;
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k)
+      if (lane + 32 * k < S + P) s_w[h][lane + 32 * k] = e[k] * inv;
   }
   __syncthreads();
   for (int idx = tid; idx < G * HD; idx += NT) {
     const int h = idx / HD;
     const float* po = a.part_o + slot0 * G * HD + idx;
+    const float* pp = a.pre_o + pslot0 * G * HD + idx;
     float acc = 0.f;
-#pragma unroll 16
-    for (int s = 0; s < S; ++s) acc = fmaf(s_w[h][s], __ldcg(po + (size_t)s * G * HD), acc);
+    // sixteen partials' loads in flight per round
+    for (int s0 = 0; s0 < S + P; s0 += 16) {
+      float pv[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int s = s0 + k;
+        pv[k] = s < S ? __ldcg(po + (size_t)s * G * HD) : s < S + P ? __ldcg(pp + (size_t)(s - S) * G * HD) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (s0 + k < S + P) acc = fmaf(s_w[h][s0 + k], pv[k], acc);
+    }
     a.o[((size_t)brel * a.n_heads + (size_t)kvh * G) * HD + idx] = acc;
   }
   if (tid == 0) a.counters[(size_t)brel * a.n_kv + kvh] = 0;
+}
+
+// The per-tile update of the cascade kernel.  Eight warps (one per batch
+// row) read every tile, so the tile's K is first transposed in shared
+// memory into kt2[i][token] = (K[token][2i], K[token][2i+1]): a lane (one
+// token) then reads one 4-byte word per dimension pair without bank
+// conflicts while every lane reads the same q pair (a broadcast), instead of
+// each lane walking q at its own offset.  Softmax and P V as tile_update.
+template <int HD, int HPW>
+__device__ __forceinline__ void tile_update_kt(const __half2* kt2, const __half* vt, const float2* q2, int lane,
+                                               float (&m_run)[HPW], float (&l_run)[HPW], float (&o)[HPW][HD / 32]) {
+  constexpr int DPL = HD / 32, W2 = HD / 2;
+  float sc[HPW];
+  {
+    float2 acc[HPW][2];
+#pragma unroll
+    for (int h = 0; h < HPW; ++h) acc[h][0] = acc[h][1] = make_float2(0.f, 0.f);
+#pragma unroll 8
+    for (int i = 0; i < W2; ++i) {
+      const float2 kf = __half22float2(kt2[i * TILE + lane]);
+#pragma unroll
+      for (int h = 0; h < HPW; ++h) acc[h][i & 1] = __ffma2_rn(kf, q2[h * W2 + i], acc[h][i & 1]);
+    }
+#pragma unroll
+    for (int h = 0; h < HPW; ++h) {
+      const float2 a = __fadd2_rn(acc[h][0], acc[h][1]);
+      sc[h] = a.x + a.y;
+    }
+  }
+  float p[HPW];
+#pragma unroll
+  for (int h = 0; h < HPW; ++h) {
+    const float m_new = fmaxf(m_run[h], warp_max(sc[h]));
+    p[h] = expf(sc[h] - m_new);
+    const float al = expf(m_run[h] - m_new);
+    l_run[h] = l_run[h] * al + warp_sum(p[h]);
+    m_run[h] = m_new;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[h][e] *= al;
+  }
+  const __half* vl = vt + lane * DPL;
+#pragma unroll
+  for (int j = 0; j < TILE; ++j) {
+    float vf[DPL];
+    if (DPL == 4) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(vl + j * HD);
+      const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+      const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+      vf[0] = v01.x;
+      vf[1] = v01.y;
+      vf[2 % DPL] = v23.x;
+      vf[3 % DPL] = v23.y;
+    } else {
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) vf[e] = __half2float(vl[j * HD + e]);
+    }
+#pragma unroll
+    for (int h = 0; h < HPW; ++h) {
+      const float pj = __shfl_sync(0xffffffffu, p[h], j);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pj, vf[e], o[h][e]);
+    }
+  }
+}
+
+// ---- cascade attention: the shared prefix, once for every batch row --------------
+
+constexpr int kCascStages = 4;
+
+// Grid (n_kv * S): CTA (kv head, split sp) covers a contiguous run of the
+// prefix's 32-token tiles.  Warp NW (the producer) streams the tiles -- K
+// then V, one bulk copy each, from the pages of batch row 0, which every row
+// shares -- through a ring of kCascStages stages; consumer warp r < rows
+// applies each tile to row r's G query heads (the same per-tile update as the
+// per-row kernel) and writes one (m, l, o) partial per head.  The prefix
+// bytes are read once per step instead of once per row.
+template <int HD, int G>
+__global__ void __launch_bounds__(NT + 32) cascade_prefix_kernel(const CascArgs a) {
+  constexpr int DPL = HD / 32;
+  constexpr int STAGE = 2 * TILE * HD;  // halves: K then V
+  extern __shared__ __align__(128) uint8_t s_dyn[];
+  __half* s_stage = reinterpret_cast<__half*>(s_dyn);
+  __half2* s_kt2 = reinterpret_cast<__half2*>(s_dyn + (size_t)kCascStages * STAGE * 2);  // [HD/2][TILE]
+  float* s_q = reinterpret_cast<float*>(s_dyn + (size_t)kCascStages * STAGE * 2 + (size_t)HD / 2 * TILE * 4);
+  __shared__ __align__(8) uint64_t s_full[kCascStages], s_empty[kCascStages];
+  const int S = a.n_splits;
+  const int kvh = blockIdx.x / S, sp = blockIdx.x - kvh * S;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rows = a.rows;
+  if (tid == 0) {
+    for (int i = 0; i < kCascStages; ++i) {
+      mbar_init(smem_u32(&s_full[i]), 1);
+      mbar_init(smem_u32(&s_empty[i]), rows);
+    }
+    mbar_fence_init();
+  }
+  int n = *a.shared_len;
+  if (n < 0 || n > a.max_len || n % TILE) {
+    if (a.status && tid == 0) atomicOr(a.status, kBadPos);
+    n = 0;
+  }
+  const int n_tiles = n / TILE;
+  const int per = (n_tiles + S - 1) / S;
+  const int tb = min(n_tiles, sp * per), te = min(n_tiles, tb + per);
+  const int pt = a.page_tokens;
+  const float scale = 1.0f / sqrtf((float)HD);
+  for (int i = tid; i < rows * G * HD; i += NT + 32) {
+    const int r = i / (G * HD), j = i - r * (G * HD);
+    s_q[i] = a.q[(size_t)r * a.n_heads * HD + (size_t)kvh * G * HD + j] * scale;
+  }
+  __syncthreads();
+
+  if (warp == NW) {  // producer
+    if (lane == 0) {
+      const int ptrow = a.pt_row ? a.pt_row[0] : 0;
+      const int32_t* ptab = a.page_table + (size_t)ptrow * a.max_pages;
+      int k = 0;
+      for (int i = tb; i < te; ++i, ++k) {
+        const int st = k % kCascStages;
+        const uint32_t full = smem_u32(&s_full[st]);
+        if (k >= kCascStages && !mbar_wait(smem_u32(&s_empty[st]), ((k / kCascStages) - 1) & 1)) {
+          if (a.status) atomicOr(a.status, kTimeout);
+          break;
+        }
+        const int t = i * TILE;
+        const int page = ptab[t / pt];
+        if (page < 0) {
+          if (a.status) atomicOr(a.status, kBadPage);
+          mbar_arrive(full);  // the phase completes with nothing copied
+          continue;
+        }
+        const size_t base = (((size_t)page * a.n_kv + kvh) * pt + (t % pt)) * HD;
+        const uint32_t bytes = TILE * HD * 2;
+        __half* dst = s_stage + (size_t)st * STAGE;
+        mbar_expect_tx(full, 2 * bytes);
+        bulk_g2s(smem_u32(dst), a.k_pool + base, bytes, full);
+        bulk_g2s(smem_u32(dst + TILE * HD), a.v_pool + base, bytes, full);
+      }
+      // never leave with copies in flight
+      for (int j = max(0, k - kCascStages); j < k; ++j) mbar_wait(smem_u32(&s_full[j % kCascStages]), (j / kCascStages) & 1);
+    }
+    return;
+  }
+  if (warp >= rows) return;
+
+  float m_run[G], l_run[G], o[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
+  }
+  const float2* q2 = reinterpret_cast<const float2*>(s_q + (size_t)warp * G * HD);
+  bool failed = false;
+  const int ctid = tid;  // consumer threads: 0 .. rows * 32 - 1
+  for (int i = tb, k = 0; i < te; ++i, ++k) {
+    const int st = k % kCascStages;
+    // every consumer waits (bounded) even after a failure, so the named
+    // barriers below always see all of them
+    if (!mbar_wait(smem_u32(&s_full[st]), (k / kCascStages) & 1)) failed = true;
+    const __half* kt = s_stage + (size_t)st * STAGE;
+    named_bar(1, rows * 32);  // every warp is done with the previous tile's transpose
+    // transpose: word i of token t -> kt2[i][t]; lanes walk the words from a
+    // token-dependent start so reads and writes both spread over the banks
+    const uint32_t* kw = reinterpret_cast<const uint32_t*>(kt);
+    uint32_t* tw = reinterpret_cast<uint32_t*>(s_kt2);
+    for (int e = ctid; e < TILE * (HD / 2); e += rows * 32) {
+      const int t = e % TILE, i = ((e / TILE) + t) % (HD / 2);
+      tw[i * TILE + t] = kw[t * (HD / 2) + i];
+    }
+    named_bar(1, rows * 32);
+    tile_update_kt<HD, G>(s_kt2, kt + TILE * HD, q2, lane, m_run, l_run, o);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s_empty[st]));
+  }
+  if (failed && a.status && lane == 0) atomicOr(a.status, kTimeout);
+  const size_t slot = ((size_t)warp * a.n_kv + kvh) * S + sp;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) a.part_o[(slot * G + h) * HD + lane * DPL + e] = o[h][e];
+    if (lane == 0) reinterpret_cast<float2*>(a.part_ml)[slot * G + h] = make_float2(m_run[h], l_run[h]);
+  }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -334,8 +564,42 @@ AttnFn attn_fn_g(int g) {
   return nullptr;
 }
 
+using CascFn = void (*)(const CascArgs);
+
+size_t casc_smem(int hd, int g, int rows) {
+  return (size_t)kCascStages * 2 * TILE * hd * 2 + (size_t)hd / 2 * TILE * 4 + (size_t)rows * g * hd * 4;
+}
+
+template <int HD, int G>
+CascFn casc_fn() {
+  static bool done[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(cascade_prefix_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)casc_smem(HD, G, kMaxBatch)) != cudaSuccess)
+      return nullptr;
+    done[dev] = true;
+  }
+  return cascade_prefix_kernel<HD, G>;
+}
+
+template <int HD>
+CascFn casc_fn_g(int g) {
+  switch (g) {
+    case 1: return casc_fn<HD, 1>();
+    case 2: return casc_fn<HD, 2>();
+    case 4: return casc_fn<HD, 4>();
+    case 8: return casc_fn<HD, 8>();
+  }
+  return nullptr;
+}
+
 cudaError_t launch_attention(const AttnArgs& a, int rows, cudaStream_t s, bool pdl) {
   if (a.n_splits > kMaxSplits || a.n_splits < 1 || a.n_kv < 1 || a.n_heads % a.n_kv) return cudaErrorInvalidValue;
+  if (a.pre_splits < 0 || a.n_splits + a.pre_splits > kMaxSplits || (a.pre_splits && (!a.pre_o || !a.pre_ml)))
+    return cudaErrorInvalidValue;
   const int g = a.n_heads / a.n_kv;
   AttnFn f = a.head_dim == 32 ? attn_fn_g<32>(g) : a.head_dim == 64 ? attn_fn_g<64>(g)
            : a.head_dim == 128 ? attn_fn_g<128>(g) : nullptr;
@@ -351,6 +615,22 @@ cudaError_t launch_attention(const AttnArgs& a, int rows, cudaStream_t s, bool p
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, f, a);
+}
+
+bool cascade_supported(int n_heads, int n_kv, int head_dim) {
+  if (n_kv < 1 || n_heads % n_kv) return false;
+  const int g = n_heads / n_kv;
+  return (g == 1 || g == 2 || g == 4 || g == 8) && (head_dim == 32 || head_dim == 64 || head_dim == 128);
+}
+
+cudaError_t launch_cascade_prefix(const CascArgs& a, cudaStream_t s) {
+  if (a.rows < 1 || a.rows > kMaxBatch || a.n_splits < 1 || !cascade_supported(a.n_heads, a.n_kv, a.head_dim))
+    return cudaErrorInvalidValue;
+  const int g = a.n_heads / a.n_kv;
+  CascFn f = a.head_dim == 32 ? casc_fn_g<32>(g) : a.head_dim == 64 ? casc_fn_g<64>(g) : casc_fn_g<128>(g);
+  if (!f) return cudaErrorInvalidValue;
+  f<<<a.n_kv * a.n_splits, NT + 32, casc_smem(a.head_dim, g, a.rows), s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace dls

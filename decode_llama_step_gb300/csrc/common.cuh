@@ -20,6 +20,8 @@ struct StepParams {
   int32_t seq[kMaxBatch];
   int32_t step;                // generation step counter (argmax output slot)
   int32_t status;              // nonzero: a kernel saw an invalid index (bit flags)
+  int32_t shared_len;          // batched steps: leading positions every row holds in the same KV pages (a
+                               // multiple of 32; their attention runs once for all rows), 0 = none
 };
 
 enum StatusBits : int32_t {

@@ -73,7 +73,38 @@ struct AttnArgs {
   int* counters;             // [rows][n_kv], zero between launches
   int32_t* status;           // optional status word (may be NULL)
   int max_len;               // upper bound on keys (guards page-table reads)
+  // cascade (shared-prefix) attention: keys [0, *start_len) were covered by
+  // launch_cascade_prefix, whose P = pre_splits partials per (row, kv head)
+  // join this launch's merge (start_len NULL / pre_splits 0: no prefix part)
+  const int32_t* start_len;  // device, a multiple of 32
+  const float* pre_o;        // [rows][n_kv][P][G][head_dim]
+  const float* pre_ml;       // [rows][n_kv][P][G] (m, l) pairs
+  int pre_splits;
 };
+
+// The shared-prefix half of cascade attention: the keys [0, *shared_len) that
+// every batch row holds in the same KV pages (a shared fork), read once per
+// KV head for all rows.  CTA (kv head, split) streams its run of 32-token
+// tiles through shared memory; warp r applies each tile to batch row r's G
+// query heads.  Writes one (m, l, o) partial per (row, kv head, split).
+struct CascArgs {
+  const float* q;             // [rows][n_heads*head_dim]
+  const __half* k_pool;
+  const __half* v_pool;
+  const int32_t* page_table;
+  int max_pages;
+  const int32_t* pt_row;      // page-table row of batch row 0 (the prefix pages are every row's)
+  const int32_t* shared_len;  // device: shared prefix length, a multiple of 32 (0: nothing to do)
+  int rows;                   // 1..8
+  int n_heads, n_kv, head_dim, page_tokens;
+  int n_splits;               // splits per KV head
+  float* part_o;              // [rows][n_kv][n_splits][G][head_dim]
+  float* part_ml;             // [rows][n_kv][n_splits][G]
+  int32_t* status;
+  int max_len;
+};
+cudaError_t launch_cascade_prefix(const CascArgs& a, cudaStream_t s);
+bool cascade_supported(int n_heads, int n_kv, int head_dim);
 
 size_t attn_workspace_bytes(int rows, int n_heads, int n_kv, int head_dim, int n_splits);
 void attn_workspace_carve(void* ws, int rows, int n_heads, int n_kv, int head_dim, int n_splits, float** part_o,

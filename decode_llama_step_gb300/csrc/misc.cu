@@ -174,6 +174,7 @@ __global__ void set_params_kernel(StepParams* sp, const StepParams h, int reset_
   }
   if (b == 0) {
     sp->n = h.n;
+    sp->shared_len = h.shared_len;
     if (reset_step) {
       sp->step = 0;
       sp->status = 0;
