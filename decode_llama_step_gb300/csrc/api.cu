@@ -196,6 +196,19 @@ struct dls_model {
   // programmatic dependent launch between the step's kernels; off by default
   // (measured slower on this path), DLS_PDL=1 turns it on
   bool pdl = false;
+  // per-matrix weight types ("mixed" model: some matrix in a K-quant format):
+  // matrices wq wk wv wo w_gate w_up w_down stored one by one in the layer
+  // block, K-quant ones packed (mkq: offset), the others in the wtype's
+  // layout (mleg); run through the mixed-format path
+  bool mixed = false;
+  int mtype[7] = {0, 0, 0, 0, 0, 0, 0};
+  size_t mkq[7] = {0, 0, 0, 0, 0, 0, 0};
+  MatOff mleg[7];
+  int emb_type = 0, out_type = 0;
+  size_t out_bytes = 0;
+  std::map<std::tuple<int, int, int>, KqLaunch> kq_plans;      // (type, rows, cols)
+  std::map<std::pair<int, int>, GemvLaunch> mix_gemv_plans;   // (rows, blocks per row)
+  float* mix_buf = nullptr;  // normalised activations [H] | projection output [max(H, q_rows)]
   // streamed layers: copy-engine cudaMemcpyAsync (0), or the SM-driven copy
   // kernel with this many CTAs on the copy stream (DLS_STREAM_COPY=sm:<ctas>)
   int stream_sm_ctas = 0;
@@ -334,6 +347,7 @@ int copy_out(dls_model* m, void* dst, const void* src, size_t bytes) {
 struct LayerPtrs {
   const float *attn_norm, *ffn_norm;
   MatDev qkv, o, gu, down;
+  const uint8_t* base;  // the layer block (mixed-format matrices are found from it)
 };
 
 LayerPtrs layer_ptrs(const dls_model* m, const uint8_t* base) {
@@ -344,6 +358,7 @@ LayerPtrs layer_ptrs(const dls_model* m, const uint8_t* base) {
   p.o = mat_at(base, m->lay.o);
   p.gu = mat_at(base, m->lay.gu);
   p.down = mat_at(base, m->lay.down);
+  p.base = base;
   return p;
 }
 
@@ -534,6 +549,158 @@ int enqueue_row(dls_model* m, int b, bool head, bool argmax, float* capture) {
   if (argmax)
     LK(K_ARGMAX, launch_argmax(logits, m->V, 1, m->next_tok + b, m->argmax_part, m->argmax_cnt,
                                argmax_blocks(1, m->num_sms), s, pdl));
+  return DLS_OK;
+}
+
+// ---- the mixed-format path (models with K-quant matrices) ------------------------
+
+// Shape of layer matrix i (wq, wk, wv, wo, w_gate, w_up, w_down).
+void mix_shape(const dls_model* m, int i, int* rows, int* cols) {
+  const int r[7] = {m->q_rows, m->kv_rows, m->kv_rows, m->H, m->F, m->F, m->H};
+  const int c[7] = {m->H, m->H, m->H, m->q_rows, m->H, m->H, m->F};
+  *rows = r[i];
+  *cols = c[i];
+}
+
+size_t kq_host_bytes(int type, int rows, int cols) {
+  return (size_t)rows * (cols / 256) * (type == DLS_Q4_K ? 144 : type == DLS_Q5_K ? 176 : 210);
+}
+
+// y = W x for one matrix: a K-quant matrix (packed at w) through the K-quant
+// GEMV, a Q8_0 / Q4_0 matrix (md) through the decode GEMV with a plain
+// prologue and epilogue.
+int mix_gemv(dls_model* m, int type, const uint8_t* w, const MatDev& md, int rows, int cols, const float* x,
+             float* y, int kind) {
+  if (type) {
+    const auto key = std::make_tuple(type, rows, cols);
+    auto it = m->kq_plans.find(key);
+    if (it == m->kq_plans.end()) it = m->kq_plans.emplace(key, kq_plan(type, rows, cols, m->num_sms)).first;
+    if (it->second.grid < 1) return fail(m, DLS_ERR_ARG, "no K-quant GEMV for type=%d rows=%d cols=%d", type, rows, cols);
+    KqArgs a{};
+    a.w = w;
+    a.d6 = type == DLS_Q6_K ? kq_d6(w, rows, cols) : nullptr;
+    a.rows = rows;
+    a.cols = cols;
+    a.x = x;
+    a.y = y;
+    a.status = &m->sp->status;
+    LK(kind, launch_kq_gemv(type, a, it->second, m->stream));
+    return DLS_OK;
+  }
+  const auto key = std::make_pair(md.rows, md.nb);
+  auto it = m->mix_gemv_plans.find(key);
+  if (it == m->mix_gemv_plans.end())
+    it = m->mix_gemv_plans.emplace(key, gemv_plan(m->wtype, PRO_COPY, EPI_STORE, md.rows, md.nb, m->num_sms, 1)).first;
+  GemvArgs g{};
+  g.w = md;
+  g.unit = 1;
+  g.x = x;
+  g.y = y;
+  LK(kind, launch_gemv(m->wtype, PRO_COPY, EPI_STORE, g, it->second, m->stream, false));
+  return DLS_OK;
+}
+
+int mix_layer_gemv(dls_model* m, const uint8_t* base, int i, const float* x, float* y, int kind) {
+  int rows, cols;
+  mix_shape(m, i, &rows, &cols);
+  const MatDev md = m->mtype[i] ? MatDev{} : mat_at(base, m->mleg[i]);
+  return mix_gemv(m, m->mtype[i], base + m->mkq[i], md, rows, cols, x, y, kind);
+}
+
+// The decode step of `n` batch rows (values in m->sp) on a mixed-format
+// model: per layer, each row in turn runs RMSNorm, the Q, K and V GEMVs, the
+// RoPE + K/V append, split-K attention, the O GEMV + residual, RMSNorm,
+// the gate and up GEMVs, SwiGLU and the down GEMV + residual.  Rows of one
+// sequence at consecutive positions (a prefill chunk) see the keys the
+// earlier rows appended.  head_row >= 0: the LM head for that row only,
+// into logits row 0; head_row == -1 with `head`: every row's logits.
+int enqueue_mixed(dls_model* m, int n, bool head, int head_row, bool argmax, float* capture, int cap_row) {
+  cudaStream_t s = m->stream;
+  const int H = m->H, qkv_ld = m->q_rows + 2 * m->kv_rows;
+  float* xn = m->mix_buf;
+  float* tmp = m->mix_buf + H;
+  float* gbuf = m->gu;  // [F] gate | [F] up | [F] h (m->gu holds 2 F per batch row, 16 rows or more)
+  float* ubuf = m->gu + m->F;
+  float* hbuf = m->gu + 2 * (size_t)m->F;
+  for (int r = 0; r < n; ++r) {
+    float* x = m->x + (size_t)r * H;
+    if (m->emb_type)
+      LK(K_EMBED, launch_kq_dequant_rows(m->emb_type, m->emb_block, m->V, H, 0, m->sp->token + r, 1, x, H,
+                                         &m->sp->status, s));
+    else
+      LK(K_EMBED, launch_embed(mat_at(m->emb_block, m->emb_off), m->wtype, m->sp, r, x, m->V, s, false));
+  }
+  const uint8_t* skip = step_skip(m);
+  TRY(stream_begin(m, skip));
+  for (int l = 0; l < m->L; ++l) {
+    LayerPtrs P;
+    TRY(layer_begin(m, l, &P));
+    for (int r = 0; r < n; ++r) {
+      float* x = m->x + (size_t)r * H;
+      if (skip[l]) {
+        if (capture && r == cap_row)
+          CK(cudaMemcpyAsync(capture + (size_t)l * H, x, H * sizeof(float), cudaMemcpyDeviceToDevice, s));
+        continue;
+      }
+      KvView kv{m->k_pool + (size_t)l * m->kv_layer_elems, m->v_pool + (size_t)l * m->kv_layer_elems, m->pt_dev,
+                m->nkv, m->hd, m->pt, m->max_pages};
+      float* qkv = m->pf_qkv + (size_t)r * qkv_ld;
+      float* q = m->pf_q + (size_t)r * m->q_rows;
+      LK(K_QKV, launch_rmsnorm_vec(x, H, P.attn_norm, m->eps, xn, s));
+      TRY(mix_layer_gemv(m, P.base, 0, xn, qkv, K_QKV));
+      TRY(mix_layer_gemv(m, P.base, 1, xn, qkv + m->q_rows, K_QKV));
+      TRY(mix_layer_gemv(m, P.base, 2, xn, qkv + m->q_rows + m->kv_rows, K_QKV));
+      LK(K_QKV, launch_rope_kv_batch(qkv, 1, qkv_ld, m->q_rows, m->kv_rows, kv, m->sp->seq + r, m->sp->pos + r,
+                                     m->rope, m->rope_len, q, &m->sp->status, s));
+      AttnArgs a{};
+      a.q = q;
+      a.o = m->o;
+      a.k_pool = kv.k_pool;
+      a.v_pool = kv.v_pool;
+      a.page_table = m->pt_dev;
+      a.max_pages = m->max_pages;
+      a.pt_row = m->sp->seq;
+      a.len = m->sp->pos;
+      a.len_add = 1;
+      a.n_heads = m->nh;
+      a.n_kv = m->nkv;
+      a.head_dim = m->hd;
+      a.page_tokens = m->pt;
+      a.n_splits = m->attn_splits;
+      a.row0 = r;
+      a.part_o = m->part_o;
+      a.part_ml = m->part_ml;
+      a.counters = m->counters;
+      a.status = &m->sp->status;
+      a.max_len = m->max_ctx;
+      LK(K_ATTN, launch_attention(a, 1, s, false));
+      TRY(mix_layer_gemv(m, P.base, 3, m->o, tmp, K_O));
+      LK(K_O, launch_add_vec(x, tmp, H, s));
+      LK(K_GATE_UP, launch_rmsnorm_vec(x, H, P.ffn_norm, m->eps, xn, s));
+      TRY(mix_layer_gemv(m, P.base, 4, xn, gbuf, K_GATE_UP));
+      TRY(mix_layer_gemv(m, P.base, 5, xn, ubuf, K_GATE_UP));
+      LK(K_GATE_UP, launch_swiglu_vec(gbuf, ubuf, hbuf, m->F, s));
+      TRY(mix_layer_gemv(m, P.base, 6, hbuf, tmp, K_DOWN));
+      LK(K_DOWN, launch_add_vec(x, tmp, H, s));
+      if (capture && r == cap_row)
+        CK(cudaMemcpyAsync(capture + (size_t)l * H, x, H * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    }
+    TRY(layer_end(m, l));
+  }
+  if (head || argmax) {
+    const int htype = m->tied ? m->emb_type : m->out_type;
+    const uint8_t* hblk = m->tied ? m->emb_block : m->out_block;
+    const MatDev md = htype ? MatDev{} : head_mat(m);
+    for (int r = 0; r < n; ++r) {
+      if (head_row >= 0 && r != head_row) continue;
+      float* logits = m->logits + (size_t)(head_row >= 0 ? 0 : r) * m->V;
+      LK(K_HEAD, launch_rmsnorm_vec(m->x + (size_t)r * H, H, m->out_norm, m->eps, xn, s));
+      TRY(mix_gemv(m, htype, hblk, md, m->V, H, xn, logits, K_HEAD));
+    }
+  }
+  if (argmax)
+    LK(K_ARGMAX, launch_argmax(m->logits, m->V, n, m->next_tok, m->argmax_part, m->argmax_cnt,
+                               argmax_blocks(n, m->num_sms), s, false));
   return DLS_OK;
 }
 
@@ -979,6 +1146,12 @@ int enqueue_persistent(dls_model* m, bool head, bool argmax, float* capture) {
 
 int enqueue_step(dls_model* m, int rows, bool head, bool argmax, float* capture) {
   m->launch_count = 0;
+  if (m->mixed) {
+    TRY(enqueue_mixed(m, rows, head, -1, argmax, capture, 0));
+    if (argmax) LK(K_ADVANCE, launch_advance(m->sp, m->next_tok, m->tokens_dev, rows, m->stream, false));
+    m->launches_per_step = m->launch_count;
+    return DLS_OK;
+  }
   if (m->use_step && rows == 1) {
     TRY(enqueue_persistent(m, head, argmax, capture));
     m->launches_per_step = m->launch_count;
@@ -1096,7 +1269,7 @@ int check_seq(dls_model* m, int seq) {
 // rounded down to whole 32-token tiles.  0 below four tiles (not worth the
 // extra launch) or with the cascade off.
 int shared_prefix_len(const dls_model* m, int n, const int32_t* seqs, const int32_t* pos) {
-  if (n < 2 || !m->cascade || !m->casc_o) return 0;
+  if (n < 2 || !m->cascade || !m->casc_o || m->mixed) return 0;
   int minpos = pos[0];
   for (int i = 1; i < n; ++i) minpos = std::min(minpos, pos[i]);
   const std::vector<int>& p0 = m->seqs[seqs[0]].pages;
@@ -1147,9 +1320,27 @@ int upload_matrix(dls_model* m, const void* host_blocks, int rows, int cols, uin
   return DLS_OK;
 }
 
+// host GGUF K-quant super-blocks -> the packed device layout at dst
+int upload_kq(dls_model* m, const void* host_blocks, int type, int rows, int cols, uint8_t* dst, uint8_t* temp) {
+  CK(cudaMemcpyAsync(temp, host_blocks, kq_host_bytes(type, rows, cols), cudaMemcpyHostToDevice, m->stream));
+  CK(launch_kq_pack(type, temp, rows, cols, dst, m->stream));
+  // the next upload reuses temp: the pack must have read it
+  return sync_stream(m, m->stream);
+}
+
 int upload_layer(dls_model* m, const dls_layer_desc& ld, uint8_t* dst, uint8_t* temp) {
   CK(cudaMemcpyAsync(dst + m->lay.attn_norm, ld.attn_norm, m->H * sizeof(float), cudaMemcpyHostToDevice, m->stream));
   CK(cudaMemcpyAsync(dst + m->lay.ffn_norm, ld.ffn_norm, m->H * sizeof(float), cudaMemcpyHostToDevice, m->stream));
+  if (m->mixed) {
+    const void* src[7] = {ld.wq, ld.wk, ld.wv, ld.wo, ld.w_gate, ld.w_up, ld.w_down};
+    for (int i = 0; i < 7; ++i) {
+      int rows, cols;
+      mix_shape(m, i, &rows, &cols);
+      if (m->mtype[i]) TRY(upload_kq(m, src[i], m->mtype[i], rows, cols, dst + m->mkq[i], temp));
+      else TRY(upload_matrix(m, src[i], rows, cols, dst, m->mleg[i], 0, temp));
+    }
+    return DLS_OK;
+  }
   TRY(upload_matrix(m, ld.wq, m->q_rows, m->H, dst, m->lay.qkv, 0, temp));
   TRY(upload_matrix(m, ld.wk, m->kv_rows, m->H, dst, m->lay.qkv, m->q_rows, temp));
   TRY(upload_matrix(m, ld.wv, m->kv_rows, m->H, dst, m->lay.qkv, m->q_rows + m->kv_rows, temp));
@@ -1280,6 +1471,7 @@ int apply_resident(dls_model* m, int n) {
 int step_scratch(dls_model* m, std::vector<void*>* made) {
   const char* e = getenv("DLS_STEP_KERNEL");
   if (e && atoi(e) == 0) return DLS_OK;
+  if (m->mixed) return DLS_OK;
   if (!m->step.fn) m->step = step_plan(m->wtype, m->H, m->q_rows, m->F, m->nh, m->nkv, m->hd, m->num_sms);
   if (!m->step.fn || m->step_layers) return DLS_OK;
   const int g = m->nh / m->nkv, S = m->step.splits;
@@ -1325,7 +1517,7 @@ int setup_persistent(dls_model* m) {
   // runs them as separate kernels instead
   const char* e = getenv("DLS_STEP_KERNEL");
   if (e && atoi(e) == 0) return DLS_OK;
-  if (m->resident < m->L) return DLS_OK;
+  if (m->resident < m->L || m->mixed) return DLS_OK;
   TRY(step_scratch(m, nullptr));
   if (!m->step.fn) return DLS_OK;
   std::vector<StepLayer> hl(m->L);
@@ -1386,10 +1578,26 @@ int validate_desc(const dls_model_desc* d) {
     return fail(m, DLS_ERR_ARG, "rope_theta=%g rms_eps=%g", d->rope_theta, d->rms_eps);
   if (!d->tok_embd || !d->output_norm || !d->layers || (!d->tied_embeddings && !d->output))
     return fail(m, DLS_ERR_ARG, "missing tensor pointer");
+  auto kq = [](int t) { return t == DLS_Q4_K || t == DLS_Q5_K || t == DLS_Q6_K; };
+  const int in_cols[7] = {d->hidden, d->hidden, d->hidden, d->n_heads * d->head_dim, d->hidden, d->hidden, d->ffn};
   for (int l = 0; l < d->n_layers; ++l) {
     const dls_layer_desc& L = d->layers[l];
     if (!L.attn_norm || !L.ffn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.w_gate || !L.w_up || !L.w_down)
       return fail(m, DLS_ERR_ARG, "layer=%d missing tensor pointer", l);
+    for (int i = 0; i < 7; ++i) {
+      const int t = L.types[i];
+      if (t != 0 && !kq(t)) return fail(m, DLS_ERR_ARG, "layer=%d matrix=%d type=%d (0 or a K-quant type)", l, i, t);
+      if (t != d->layers[0].types[i])
+        return fail(m, DLS_ERR_ARG, "layer=%d matrix=%d type=%d differs from layer 0 (%d)", l, i, t,
+                    d->layers[0].types[i]);
+      if (kq(t) && (in_cols[i] % 256 || in_cols[i] > 32768))
+        return fail(m, DLS_ERR_ARG, "matrix=%d input width %d: a K-quant matrix needs a multiple of 256 up to 32768",
+                    i, in_cols[i]);
+    }
+  }
+  for (int t : {d->tok_embd_type, d->output_type}) {
+    if (t != 0 && !kq(t)) return fail(m, DLS_ERR_ARG, "embedding/output type=%d", t);
+    if (kq(t) && d->hidden % 256) return fail(m, DLS_ERR_ARG, "K-quant embedding/output needs hidden %% 256 == 0");
   }
   return DLS_OK;
 }
@@ -1530,22 +1738,45 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   CKC(prefill_setup_attributes());
   CKC(fattn_setup_attributes());
 
+  // per-matrix types (validated: every layer gives the same)
+  for (int i = 0; i < 7; ++i) m->mtype[i] = d.layers[0].types[i];
+  m->emb_type = d.tok_embd_type;
+  m->out_type = m->tied ? 0 : d.output_type;
+  m->mixed = m->emb_type || m->out_type;
+  for (int i = 0; i < 7; ++i) m->mixed |= m->mtype[i] != 0;
+  if (m->mixed) CKC(kq_setup_attributes());
+
   // layouts
   size_t cur = 0;
   m->lay.attn_norm = cur;
   cur = a256(cur + m->H * sizeof(float));
   m->lay.ffn_norm = cur;
   cur = a256(cur + m->H * sizeof(float));
-  m->lay.qkv = mat_off(cur, m->q_rows + 2 * m->kv_rows, m->H, m->wtype);
-  m->lay.o = mat_off(cur, m->H, m->q_rows, m->wtype);
-  m->lay.gu = mat_off(cur, 2 * m->F, m->H, m->wtype);
-  m->lay.down = mat_off(cur, m->H, m->F, m->wtype);
+  if (!m->mixed) {
+    m->lay.qkv = mat_off(cur, m->q_rows + 2 * m->kv_rows, m->H, m->wtype);
+    m->lay.o = mat_off(cur, m->H, m->q_rows, m->wtype);
+    m->lay.gu = mat_off(cur, 2 * m->F, m->H, m->wtype);
+    m->lay.down = mat_off(cur, m->H, m->F, m->wtype);
+  } else {
+    // the seven matrices one after another, each in its own format
+    for (int i = 0; i < 7; ++i) {
+      int rows, cols;
+      mix_shape(m, i, &rows, &cols);
+      if (m->mtype[i]) {
+        m->mkq[i] = cur;
+        cur = a256(cur + kq_packed_bytes(m->mtype[i], rows, cols));
+      } else {
+        m->mleg[i] = mat_off(cur, rows, cols, m->wtype);
+      }
+    }
+  }
   m->lay.bytes = cur;
   cur = 0;
   m->emb_off = mat_off(cur, m->V, m->H, m->wtype);
-  m->emb_bytes = cur;
+  m->emb_bytes = m->emb_type ? kq_packed_bytes(m->emb_type, m->V, m->H) : cur;
   cur = 0;
   m->out_off = mat_off(cur, m->V, m->H, m->wtype);
+  m->out_bytes = m->out_type ? kq_packed_bytes(m->out_type, m->V, m->H) : cur;
 
   m->plan_qkv = gemv_plan(m->wtype, PRO_RMSNORM, EPI_QKV, m->lay.qkv.rows, m->lay.qkv.nb, m->num_sms, 2);
   m->plan_o = gemv_plan(m->wtype, PRO_COPY, EPI_RESID, m->lay.o.rows, m->lay.o.nb, m->num_sms, 1);
@@ -1564,13 +1795,27 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   size_t temp_bytes = (size_t)m->V * m->emb_off.nb * bsz;
   temp_bytes = std::max(temp_bytes, (size_t)2 * m->F * ((m->H + 31) / 32) * bsz);
   temp_bytes = std::max(temp_bytes, (size_t)m->H * ((m->F + 31) / 32) * bsz);
+  for (int i = 0; i < 7; ++i)
+    if (m->mtype[i]) {
+      int rows, cols;
+      mix_shape(m, i, &rows, &cols);
+      temp_bytes = std::max(temp_bytes, kq_host_bytes(m->mtype[i], rows, cols));
+    }
+  for (int t : {m->emb_type, m->out_type})
+    if (t) temp_bytes = std::max(temp_bytes, kq_host_bytes(t, m->V, m->H));
   void* p = nullptr;
   TRYC(dev_alloc(m, m->emb_bytes, &p, "tok_embd"));
   m->emb_block = static_cast<uint8_t*>(p);
+  // padding (the scale rows' round-up to 8 blocks, alignment gaps) stays zero:
+  // the tensor-core GEMMs read whole 64-column tiles, and a zero-filled code
+  // times a stale scale could be 0 * inf
+  CKC(cudaMemsetAsync(m->emb_block, 0, m->emb_bytes, m->stream));
   if (!m->tied) {
-    TRYC(dev_alloc(m, m->emb_bytes, &p, "output"));
+    TRYC(dev_alloc(m, m->out_bytes, &p, "output"));
     m->out_block = static_cast<uint8_t*>(p);
+    CKC(cudaMemsetAsync(m->out_block, 0, m->out_bytes, m->stream));
   }
+  if (m->mixed) TRYC(dev_alloc_t(m, (size_t)m->H + std::max(m->H, m->q_rows), &m->mix_buf, "mixed_path_vectors"));
   TRYC(dev_alloc_t(m, m->H, &m->out_norm, "output_norm"));
   TRYC(dev_alloc_t(m, (size_t)m->L * m->kv_layer_elems, &m->k_pool, "k_cache"));
   TRYC(dev_alloc_t(m, (size_t)m->L * m->kv_layer_elems, &m->v_pool, "v_cache"));
@@ -1664,10 +1909,15 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   // upload: norms, embeddings, layers (streamed layers go through buffer 0
   // and then to pinned host memory)
   CKC(cudaMemcpyAsync(m->out_norm, d.output_norm, m->H * sizeof(float), cudaMemcpyHostToDevice, m->stream));
-  TRYC(upload_matrix(m, d.tok_embd, m->V, m->H, m->emb_block, m->emb_off, 0, static_cast<uint8_t*>(temp)));
-  if (!m->tied) TRYC(upload_matrix(m, d.output, m->V, m->H, m->out_block, m->out_off, 0, static_cast<uint8_t*>(temp)));
+  if (m->emb_type) TRYC(upload_kq(m, d.tok_embd, m->emb_type, m->V, m->H, m->emb_block, static_cast<uint8_t*>(temp)));
+  else TRYC(upload_matrix(m, d.tok_embd, m->V, m->H, m->emb_block, m->emb_off, 0, static_cast<uint8_t*>(temp)));
+  if (!m->tied) {
+    if (m->out_type) TRYC(upload_kq(m, d.output, m->out_type, m->V, m->H, m->out_block, static_cast<uint8_t*>(temp)));
+    else TRYC(upload_matrix(m, d.output, m->V, m->H, m->out_block, m->out_off, 0, static_cast<uint8_t*>(temp)));
+  }
   for (int l = 0; l < m->L; ++l) {
     uint8_t* dst = l < nres ? m->layer_dev[l] : m->stage[0];
+    CKC(cudaMemsetAsync(dst, 0, m->lay.bytes, m->stream));  // padding stays zero (as for the embedding)
     TRYC(upload_layer(m, d.layers[l], dst, static_cast<uint8_t*>(temp)));
     if (l >= nres) {
       void* h = nullptr;
@@ -1745,11 +1995,30 @@ int dls_prefill(dls_model* m, int32_t seq, const int32_t* tokens, int32_t n, flo
   TRY(set_params(m, 1, &seq, &tokens[0], &pos0, true));  // clears the device status word
   float* cap = m->capture;
   m->capture = nullptr;
-  for (int c0 = 0; c0 < n; c0 += m->pf_cap) {
-    const int T = std::min(m->pf_cap, n - c0);
-    const bool last = c0 + T == n;
-    TRY(enqueue_prefill(m, seq, tokens + c0, T, pos0 + c0, last && logits_out ? HEAD_LAST : HEAD_NONE,
-                        last ? cap : nullptr));
+  if (m->mixed) {
+    // a mixed-format model: up to 8 prompt tokens per pass over the layers,
+    // each token through the decode-step kernels (a streamed layer is copied
+    // once per pass)
+    for (int c0 = 0; c0 < n; c0 += kMaxBatch) {
+      const int T = std::min(kMaxBatch, n - c0);
+      int32_t seqs[kMaxBatch], poss[kMaxBatch];
+      for (int t = 0; t < T; ++t) {
+        seqs[t] = seq;
+        poss[t] = pos0 + c0 + t;
+      }
+      if (c0 > 0) TRY(set_params(m, T, seqs, tokens + c0, poss, false));
+      else TRY(set_params(m, T, seqs, tokens + c0, poss, true));
+      m->launch_count = 0;
+      const bool last = c0 + T == n;
+      TRY(enqueue_mixed(m, T, last && logits_out, last ? T - 1 : -1, false, last ? cap : nullptr, T - 1));
+    }
+  } else {
+    for (int c0 = 0; c0 < n; c0 += m->pf_cap) {
+      const int T = std::min(m->pf_cap, n - c0);
+      const bool last = c0 + T == n;
+      TRY(enqueue_prefill(m, seq, tokens + c0, T, pos0 + c0, last && logits_out ? HEAD_LAST : HEAD_NONE,
+                          last ? cap : nullptr));
+    }
   }
   TRY(copy_out(m, logits_out, m->logits, (size_t)m->V * sizeof(float)));
   TRY(sync_stream(m, m->stream));
@@ -2332,9 +2601,46 @@ static int find_matrix(dls_model* m, int32_t layer, int32_t tensor, MatDev* out)
   return DLS_OK;
 }
 
+// A mixed-format model's matrix `tensor` (ids of dls_debug_dequant): its
+// type, K-quant data, Q8_0 / Q4_0 view, and shape.
+int find_matrix_mixed(dls_model* m, int32_t layer, int32_t tensor, int* type, const uint8_t** w, MatDev* md,
+                      int* rows, int* cols) {
+  *rows = m->V;
+  *cols = m->H;
+  if (tensor == 7 || (tensor == 8 && m->tied)) {
+    *type = m->emb_type;
+    *w = m->emb_block;
+    *md = mat_at(m->emb_block, m->emb_off);
+    return DLS_OK;
+  }
+  if (tensor == 8) {
+    *type = m->out_type;
+    *w = m->out_block;
+    *md = mat_at(m->out_block, m->out_off);
+    return DLS_OK;
+  }
+  if (tensor < 0 || tensor > 8 || layer < 0 || layer >= m->L) return fail(m, DLS_ERR_ARG, "layer=%d tensor=%d", layer, tensor);
+  const uint8_t* base = m->layer_dev[layer];
+  if (!base) return fail(m, DLS_ERR_STATE, "layer=%d is not resident", layer);
+  mix_shape(m, tensor, rows, cols);
+  *type = m->mtype[tensor];
+  *w = base + m->mkq[tensor];
+  *md = m->mtype[tensor] ? MatDev{} : mat_at(base, m->mleg[tensor]);
+  return DLS_OK;
+}
+
 int dls_debug_dequant(dls_model* m, int32_t layer, int32_t tensor, float* out) {
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
   if (!out) return fail(m, DLS_ERR_ARG, "out=NULL");
+  if (m->mixed) {
+    int type, rows, cols;
+    const uint8_t* w;
+    MatDev md;
+    TRY(find_matrix_mixed(m, layer, tensor, &type, &w, &md, &rows, &cols));
+    if (type) CK(launch_kq_dequant_rows(type, w, rows, cols, 0, nullptr, rows, out, cols, nullptr, m->stream));
+    else CK(launch_dequant(md, m->wtype, out, m->stream));
+    return DLS_OK;
+  }
   MatDev md;
   TRY(find_matrix(m, layer, tensor, &md));
   CK(launch_dequant(md, m->wtype, out, m->stream));
@@ -2344,6 +2650,13 @@ int dls_debug_dequant(dls_model* m, int32_t layer, int32_t tensor, float* out) {
 int dls_debug_gemv(dls_model* m, int32_t layer, int32_t tensor, const float* x, float* y) {
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
   if (!x || !y) return fail(m, DLS_ERR_ARG, "x/y NULL");
+  if (m->mixed) {
+    int type, rows, cols;
+    const uint8_t* w;
+    MatDev md;
+    TRY(find_matrix_mixed(m, layer, tensor, &type, &w, &md, &rows, &cols));
+    return mix_gemv(m, type, w, md, rows, cols, x, y, K_HEAD);
+  }
   MatDev md;
   TRY(find_matrix(m, layer, tensor, &md));
   GemvArgs g{};
@@ -2369,6 +2682,7 @@ int dls_debug_gemv(dls_model* m, int32_t layer, int32_t tensor, const float* x, 
 int dls_debug_gemm(dls_model* m, int32_t layer, int32_t tensor, int32_t n_tokens, const float* x, float* y) {
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
   if (!x || !y || n_tokens < 1) return fail(m, DLS_ERR_ARG, "x/y NULL or n_tokens=%d", n_tokens);
+  if (m->mixed) return fail(m, DLS_ERR_STATE, "a mixed-format model has no tensor-core GEMM");
   MatDev md;
   TRY(find_matrix(m, layer, tensor, &md));
   const bool pair = md.rstep == 2;  // gate or up: run the interleaved matrix, keep every other column

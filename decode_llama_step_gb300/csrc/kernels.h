@@ -276,6 +276,13 @@ size_t kq_packed_bytes(int fmt, int rows, int cols);
 const __half* kq_d6(const void* packed, int rows, int cols);
 cudaError_t launch_kq_pack(int fmt, const void* blocks, int rows, int cols, void* packed, cudaStream_t s);
 KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms);  // grid 0: unsupported shape
+// rows row0 .. row0+n-1 (idx NULL) or idx[0..n) of a packed K-quant matrix -> fp32 out [n][ldo]
+cudaError_t launch_kq_dequant_rows(int fmt, const void* packed, int rows, int cols, int row0, const int32_t* idx,
+                                   int n, float* out, int ldo, int32_t* status, cudaStream_t s);
+// single-vector helpers of the mixed-format decode path
+cudaError_t launch_rmsnorm_vec(const float* x, int H, const float* g, float eps, float* out, cudaStream_t s);
+cudaError_t launch_add_vec(float* x, const float* y, int n, cudaStream_t s);
+cudaError_t launch_swiglu_vec(const float* gate, const float* up, float* h, int n, cudaStream_t s);
 cudaError_t kq_setup_attributes();
 cudaError_t launch_kq_gemv(int fmt, const KqArgs& a, const KqLaunch& l, cudaStream_t s);
 cudaError_t launch_sgemm(int wtype, int epi, const PgArgs& a, int split, cudaStream_t s);

@@ -420,6 +420,72 @@ const __half* kq_d6(const void* packed, int rows, int cols) {
   return reinterpret_cast<const __half*>(static_cast<const uint8_t*>(packed) + main);
 }
 
+// ---- dequantisation of single weights (embedding rows, test hooks) ---------------
+
+// Weight (row, col) of a packed K-quant matrix, from the fields of its
+// super-block (the layouts in the header comment), computed in fp64 and
+// rounded once to fp32.
+__device__ double kq_weight(int fmt, const uint8_t* w, const __half* d6, int nsb, int row, int col) {
+  const int sbi = col >> 8, i = col & 255;
+  if (fmt == KQ_Q6_K) {
+    const uint8_t* b = w + ((size_t)row * nsb + sbi) * 208;
+    const int h = i >> 7, o = i & 127, g = o >> 5, l = o & 31;
+    const uint32_t qlb = b[64 * h + 32 * (g & 1) + l];
+    const int low = g < 2 ? (int)(qlb & 15u) : (int)(qlb >> 4);
+    const int high = (b[128 + 32 * h + l] >> (2 * g)) & 3;
+    const int sc = (int)(int8_t)b[192 + (i >> 4)];
+    const double d = (double)__half2float(d6[(size_t)row * ((nsb + 7) & ~7) + sbi]);
+    return d * (double)(sc * ((low | (high << 4)) - 32));
+  }
+  const int sbb = fmt == KQ_Q4_K ? 144 : 176;
+  const uint8_t* b = w + ((size_t)row * nsb + sbi) * sbb;
+  const double d = (double)__half2float(__ushort_as_half((uint16_t)(b[0] | (b[1] << 8))));
+  const double dmin = (double)__half2float(__ushort_as_half((uint16_t)(b[2] | (b[3] << 8))));
+  const uint8_t* sb = b + 4;
+  const int s = i >> 5;
+  int sc, m;
+  if (s < 4) {
+    sc = sb[s] & 63;
+    m = sb[s + 4] & 63;
+  } else {
+    sc = (sb[s + 4] & 15) | ((sb[s - 4] >> 6) << 4);
+    m = (sb[s + 4] >> 4) | ((sb[s] >> 6) << 4);
+  }
+  const int g = i >> 6, l = i & 31, hi = (i >> 5) & 1;
+  const uint8_t* qs = b + (fmt == KQ_Q4_K ? 16 : 48);
+  int q = hi ? (qs[32 * g + l] >> 4) : (qs[32 * g + l] & 15);
+  if (fmt == KQ_Q5_K) q |= ((b[16 + l] >> (2 * g + hi)) & 1) << 4;
+  return d * (double)(sc * q) - dmin * (double)m;
+}
+
+// out[i][c] = weight(row_i, c): rows row0.. (idx NULL) or idx[i] (clamped to
+// [0, rows), a bad index flagged in *status)
+__global__ void kq_dequant_rows_kernel(int fmt, const uint8_t* w, const __half* d6, int rows, int cols, int row0,
+                                       const int32_t* idx, int n, float* out, int ldo, int32_t* status) {
+  const int nsb = cols / 256;
+  const size_t total = (size_t)n * cols;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const int i = (int)(e / cols), c = (int)(e % cols);
+    int r = idx ? idx[i] : row0 + i;
+    if (r < 0 || r >= rows) {
+      if (status && c == 0) atomicOr(status, kBadToken);
+      r = 0;
+    }
+    out[(size_t)i * ldo + c] = (float)kq_weight(fmt, w, d6, nsb, r, c);
+  }
+}
+
+cudaError_t launch_kq_dequant_rows(int fmt, const void* packed, int rows, int cols, int row0, const int32_t* idx,
+                                   int n, float* out, int ldo, int32_t* status, cudaStream_t s) {
+  if ((fmt != KQ_Q4_K && fmt != KQ_Q5_K && fmt != KQ_Q6_K) || cols % 256 || n < 1) return cudaErrorInvalidValue;
+  const size_t total = (size_t)n * cols;
+  const int grid = (int)std::min<size_t>((total + 255) / 256, 4096);
+  kq_dequant_rows_kernel<<<grid, 256, 0, s>>>(fmt, static_cast<const uint8_t*>(packed),
+                                              fmt == KQ_Q6_K ? kq_d6(packed, rows, cols) : nullptr, rows, cols, row0,
+                                              idx, n, out, ldo, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_kq_pack(int fmt, const void* blocks, int rows, int cols, void* packed, cudaStream_t s) {
   if (fmt == KQ_Q4_K || fmt == KQ_Q5_K)
     return cudaMemcpyAsync(packed, blocks, kq_packed_bytes(fmt, rows, cols), cudaMemcpyDeviceToDevice, s);

@@ -3,6 +3,8 @@
 // fork copy and test-only gathers.
 #include <math.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace dls {
@@ -387,6 +389,46 @@ __global__ void unarrived_wait_kernel(unsigned long long limit_ns, int32_t* stat
 
 cudaError_t launch_unarrived_wait(unsigned long long limit_ns, int32_t* status, cudaStream_t s) {
   unarrived_wait_kernel<<<1, 32, 0, s>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+// ---- single-vector helpers (the mixed-format decode path) ------------------------
+
+// out = x / sqrt(mean(x^2) + eps) * g, one CTA, fixed-order reduction
+__global__ void rmsnorm_vec_kernel(const float* x, int H, const float* g, float eps, float* out) {
+  __shared__ float red[32];
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+  const float rs = 1.0f / sqrtf(t / (float)H + eps);
+  for (int i = threadIdx.x; i < H; i += blockDim.x) out[i] = x[i] * rs * g[i];
+}
+
+__global__ void add_vec_kernel(float* x, const float* y, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) x[i] += y[i];
+}
+
+__global__ void swiglu_vec_kernel(const float* gate, const float* up, float* h, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    h[i] = silu(gate[i]) * up[i];
+}
+
+cudaError_t launch_rmsnorm_vec(const float* x, int H, const float* g, float eps, float* out, cudaStream_t s) {
+  rmsnorm_vec_kernel<<<1, 1024, 0, s>>>(x, H, g, eps, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add_vec(float* x, const float* y, int n, cudaStream_t s) {
+  add_vec_kernel<<<std::min((n + 255) / 256, 1024), 256, 0, s>>>(x, y, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_vec(const float* gate, const float* up, float* h, int n, cudaStream_t s) {
+  swiglu_vec_kernel<<<std::min((n + 255) / 256, 1024), 256, 0, s>>>(gate, up, h, n);
   return cudaGetLastError();
 }
 

@@ -38,7 +38,8 @@ class dls_allocator(ctypes.Structure):
 
 
 class dls_layer_desc(ctypes.Structure):
-    _fields_ = [(n, vp) for n in ("attn_norm", "ffn_norm", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")]
+    _fields_ = [(n, vp) for n in ("attn_norm", "ffn_norm", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")] + \
+               [("types", i32 * 7)]
 
 
 class dls_model_desc(ctypes.Structure):
@@ -47,7 +48,7 @@ class dls_model_desc(ctypes.Structure):
                 ("tied_embeddings", i32), ("wtype", i32), ("page_tokens", i32), ("max_seqs", i32),
                 ("max_ctx", i32), ("max_batch", i32), ("device_budget_bytes", u64), ("tok_embd", vp),
                 ("output", vp), ("output_norm", vp), ("layers", ctypes.POINTER(dls_layer_desc)),
-                ("kv_pool_pages", i32)]
+                ("kv_pool_pages", i32), ("tok_embd_type", i32), ("output_type", i32)]
 
 
 _SIGS = {
@@ -290,14 +291,18 @@ class Model:
             keep.append(a)
             return a.ctypes.data
 
+        # per-matrix weight types (weights["formats"]: (layer, name) -> "q4_k" / "q5_k" / "q6_k"; others
+        # are the config's Q8_0 / Q4_0)
+        fmts = weights.get("formats", {})
+        names = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
         layers = (dls_layer_desc * L)()
         for l in range(L):
             lw = weights["layers"][l]
             if lw is None:
                 raise ValueError(f"layer {l} weights missing")
+            types = (i32 * 7)(*(KQUANT_TYPES.get(fmts.get((l, n)), 0) for n in names))
             layers[l] = dls_layer_desc(host(lw["attn_norm"], np.float32), host(lw["ffn_norm"], np.float32),
-                                       *(host(lw[n], np.uint8) for n in ("wq", "wk", "wv", "wo", "w_gate",
-                                                                         "w_up", "w_down")))
+                                       *(host(lw[n], np.uint8) for n in names), types)
         out = weights.get("output")
         d = dls_model_desc(L, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn, cfg.vocab,
                            float(cfg.rope_theta), float(cfg.rms_eps), int(bool(cfg.tied)), int(cfg.wtype),
@@ -305,6 +310,8 @@ class Model:
                            host(weights["tok_embd"], np.uint8), None if out is None else host(out, np.uint8),
                            host(weights["output_norm"], np.float32), layers)
         d.kv_pool_pages = int(kv_pool_pages)
+        d.tok_embd_type = KQUANT_TYPES.get(fmts.get((None, "tok_embd")), 0)
+        d.output_type = KQUANT_TYPES.get(fmts.get((None, "output")), 0)
         self._alloc = None
         alloc_ptr = None
         if allocator is not None:

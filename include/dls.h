@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define DLS_ABI_VERSION 1
+#define DLS_ABI_VERSION 2
 #define DLS_MAX_BATCH 8
 /* Most positions one dls_verify pass scores (and 1 + the longest draft). */
 #define DLS_MAX_VERIFY 16
@@ -78,6 +78,11 @@ typedef enum dls_status {
  * A matrix [rows x in] is row-major with ceil(in/32) blocks per row; columns
  * past `in` in the last block must be zero weights. */
 typedef enum dls_wtype { DLS_Q4_0 = 4, DLS_Q8_0 = 8 } dls_wtype;
+/* GGUF K-quant types (layouts under "K-quant dequant-GEMV" below); allowed
+ * per matrix (dls_layer_desc.types, tok_embd_type, output_type). */
+#define DLS_Q4_K 12
+#define DLS_Q5_K 13
+#define DLS_Q6_K 14
 
 /* Device memory source.  alloc returns device memory of at least `bytes`
  * (256-byte aligned) or NULL; free releases it.  `stream` is the model's
@@ -101,6 +106,16 @@ typedef struct dls_layer_desc {
   const void* w_gate;     /* blocks [ffn x hidden] */
   const void* w_up;       /* blocks [ffn x hidden] */
   const void* w_down;     /* blocks [hidden x ffn] (ffn padded to 32 with zero weights) */
+  /* Weight type of wq, wk, wv, wo, w_gate, w_up, w_down in that order: 0 =
+   * the model's wtype, or DLS_Q4_K / DLS_Q5_K / DLS_Q6_K for GGUF K-quant
+   * super-blocks (the matrix's input width a multiple of 256).  Every layer
+   * must give the same types.  A model with any K-quant matrix ("mixed")
+   * runs its decode steps, batched steps and prefill through per-matrix
+   * dequant-GEMVs with separate RMSNorm, RoPE/KV-append, attention, SwiGLU
+   * and residual kernels, one row at a time (prefill: up to 8 tokens per
+   * pass over the layers); the persistent step kernel and the tensor-core
+   * paths serve Q8_0 / Q4_0 models. */
+  int32_t types[7];
 } dls_layer_desc;
 
 typedef struct dls_model_desc {
@@ -122,6 +137,8 @@ typedef struct dls_model_desc {
                               which lets every sequence reach max_ctx on private pages.  A smaller pool
                               oversubscribes: a call that needs a page when none is free fails with
                               DLS_ERR_CAPACITY and changes nothing. */
+  int32_t tok_embd_type;   /* 0 = wtype, or a K-quant type (hidden a multiple of 256) */
+  int32_t output_type;     /* the LM head's type likewise (ignored when tied) */
 } dls_model_desc;
 
 /* ---- model ------------------------------------------------------------- */
@@ -384,9 +401,6 @@ int dls_attention_decode_noalloc(const float* q, const void* k_pages, const void
  * fp16 d; weight = d*scale*(code - 32) per group of 16).  A [rows][cols]
  * matrix is row-major with cols/256 super-blocks per row (cols a multiple of
  * 256). */
-#define DLS_Q4_K 12
-#define DLS_Q5_K 13
-#define DLS_Q6_K 14
 
 /* Bytes of the device layout dls_kquant_gemv reads (0 for a bad type or
  * shape). */

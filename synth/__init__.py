@@ -59,6 +59,8 @@ def _load():
             lib.synth_tokens.restype = None
             lib.synth_quant_matrix.argtypes = [u64, i64, i64, dbl, ctypes.c_int, vp]
             lib.synth_quant_matrix.restype = ctypes.c_int
+            lib.synth_quant_matrix_k.argtypes = [u64, i64, i64, dbl, ctypes.c_int, vp]
+            lib.synth_quant_matrix_k.restype = ctypes.c_int
             lib.synth_quantize.argtypes = [vp, i64, ctypes.c_int, vp]
             lib.synth_quantize.restype = ctypes.c_int
             lib.synth_f64_to_f16.argtypes = [dbl]
@@ -94,6 +96,20 @@ def quant_matrix(key: int, rows: int, cols: int, sigma: float, wtype: int) -> np
     rc = _load().synth_quant_matrix(key, rows, cols, sigma, wtype, out.ctypes.data)
     if rc != 0:
         raise ValueError(f"bad wtype {wtype}")
+    return out
+
+
+KQUANT_KIND = {"q4_k": 12, "q5_k": 13, "q6_k": 14}
+
+
+def quant_matrix_k(key: int, rows: int, cols: int, sigma: float, fmt: str) -> np.ndarray:
+    """[rows x cols] N(0, sigma) matrix (the same draws as quant_matrix with
+    this key) quantised to K-quant super-blocks (uint8, flat)."""
+    if cols % 256:
+        raise ValueError(f"cols={cols} is not a multiple of 256")
+    out = np.empty(rows * (cols // 256) * KQUANT_BLOCK_BYTES[fmt], dtype=np.uint8)
+    if _load().synth_quant_matrix_k(key, rows, cols, sigma, KQUANT_KIND[fmt], out.ctypes.data) != 0:
+        raise ValueError(f"bad K-quant format {fmt}")
     return out
 
 
@@ -176,6 +192,48 @@ def with_random_gains(w: dict, cfg: ModelConfig, sigma: float = 0.2, tag: str = 
         layers.append(lw)
     out["layers"] = layers
     return out
+
+
+# A Q4_K_M-style mix (the engine page, section 1: 70B as Q4_K_M): the value
+# and down projections and the LM head in Q6_K, every other matrix in Q4_K.
+Q4_K_M = {"wq": "q4_k", "wk": "q4_k", "wv": "q6_k", "wo": "q4_k", "w_gate": "q4_k", "w_up": "q4_k",
+          "w_down": "q6_k", "tok_embd": "q4_k", "output": "q6_k"}
+
+
+def model_weights_k(cfg: ModelConfig, formats: dict, layers=None) -> dict:
+    """model_weights with matrices in per-matrix formats: `formats` maps a
+    matrix name (the seven layer matrices, "tok_embd", "output") to "q4_k",
+    "q5_k", "q6_k", or is missing it (the config's Q8_0 / Q4_0).  Every layer
+    uses the same formats.  The result carries weights["formats"], keyed
+    (layer, name) (layer None for tok_embd and output), which the oracle
+    reads; the normals are those of model_weights."""
+    H, V = cfg.hidden, cfg.vocab
+    fm = {}
+
+    def mat(key, rows, cols, name, layer):
+        f = formats.get(name)
+        if f is None:
+            return quant_matrix(key, rows, cols, cfg.sigma, cfg.wtype)
+        fm[(layer, name)] = f
+        return quant_matrix_k(key, rows, cols, cfg.sigma, f)
+
+    w = {"config": cfg, "output_norm": np.ones(H, dtype=np.float32),
+         "tok_embd": mat(stream_key(cfg.name, "tok_embd"), V, H, "tok_embd", None)}
+    w["output"] = None if cfg.tied else mat(stream_key(cfg.name, "output"), V, H, "output", None)
+    sel = range(cfg.n_layers) if layers is None else layers
+    shapes = matrix_shapes(cfg)
+    out_layers = []
+    for l in range(cfg.n_layers):
+        if l not in sel:
+            out_layers.append(None)
+            continue
+        lw = {name: mat(stream_key(cfg.name, l, name), rows, cols, name, l) for name, (rows, cols) in shapes.items()}
+        lw["attn_norm"] = np.ones(H, dtype=np.float32)
+        lw["ffn_norm"] = np.ones(H, dtype=np.float32)
+        out_layers.append(lw)
+    w["layers"] = out_layers
+    w["formats"] = fm
+    return w
 
 
 def prompt_tokens(cfg: ModelConfig, n: int, seed: int = 1) -> np.ndarray:

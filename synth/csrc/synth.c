@@ -147,6 +147,102 @@ static void quant_block_q4_0(const double* x, uint8_t* out) {
   for (int j = 0; j < 16; ++j) out[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
 }
 
+/*
+ * K-quant super-blocks (256 weights; the GGUF layouts the engine page's Q4_K_M
+ * and Q6_K files use), for drawing synthetic K-quant matrices.  Quantiser
+ * (our reading; any valid blocks serve as inputs, since both consumers read
+ * the bytes): per 32-weight sub-block (Q4_K, Q5_K) the range [min(lo, 0),
+ * hi] is split into 15 (31) steps, the step sizes and the offsets -min are
+ * coded as 6-bit multiples of the super-block's d and dmin (their maxima over
+ * 63, stored fp16); per 16-weight group (Q6_K) the step is amax / 31, coded
+ * as an int8 multiple of d (the largest step over 127, stored fp16).  Codes
+ * are round-half-away of (x + offset) / step, clamped to the code range.
+ *   Q4_K 144 bytes: d, dmin, 12 scale bytes, 128 bytes of nibbles (byte
+ *     32g + l: weight 64g + l low, 64g + 32 + l high).
+ *   Q5_K 176 bytes: d, dmin, 12 scale bytes, 32 bytes qh (bit 2g / 2g + 1 of
+ *     qh[l]: fifth bit of weight 64g + l / 64g + 32 + l), 128 bytes of nibbles.
+ *   Q6_K 210 bytes: 128 bytes ql, 64 bytes qh, 16 int8 scales, fp16 d.
+ */
+static void pack_scales_k(const int* sc, const int* m, uint8_t* b) {
+  for (int s = 0; s < 4; ++s) {
+    b[s] = (uint8_t)((sc[s] & 63) | ((sc[s + 4] >> 4) << 6));
+    b[s + 4] = (uint8_t)((m[s] & 63) | ((m[s + 4] >> 4) << 6));
+    b[s + 8] = (uint8_t)((sc[s + 4] & 15) | ((m[s + 4] & 15) << 4));
+  }
+}
+
+static void quant_super_k45(const double* x, int qmax, uint8_t* out) {
+  double step[8], off[8], dmax = 0.0, omax = 0.0;
+  for (int s = 0; s < 8; ++s) {
+    double lo = 0.0, hi = -INFINITY;
+    for (int i = 0; i < 32; ++i) {
+      lo = fmin(lo, x[32 * s + i]);
+      hi = fmax(hi, x[32 * s + i]);
+    }
+    step[s] = (hi - lo) / qmax;
+    off[s] = -lo;
+    dmax = fmax(dmax, step[s]);
+    omax = fmax(omax, off[s]);
+  }
+  const uint16_t dh = f64_to_f16_bits(dmax / 63.0), mh = f64_to_f16_bits(omax / 63.0);
+  const double d = f16_bits_to_f64(dh), dmin = f16_bits_to_f64(mh);
+  int sc[8], m[8];
+  for (int s = 0; s < 8; ++s) {
+    double a = d > 0.0 ? round_half_away(step[s] / d) : 0.0;
+    double b = dmin > 0.0 ? round_half_away(off[s] / dmin) : 0.0;
+    sc[s] = (int)fmin(fmax(a, 0.0), 63.0);
+    m[s] = (int)fmin(fmax(b, 0.0), 63.0);
+  }
+  memcpy(out, &dh, 2);
+  memcpy(out + 2, &mh, 2);
+  pack_scales_k(sc, m, out + 4);
+  uint8_t* qh = qmax == 31 ? out + 16 : NULL;
+  uint8_t* qs = out + (qmax == 31 ? 48 : 16);
+  if (qh) memset(qh, 0, 32);
+  for (int i = 0; i < 256; ++i) {
+    const int s = i / 32;
+    const double w = d * sc[s];
+    double q = w > 0.0 ? round_half_away((x[i] + dmin * m[s]) / w) : 0.0;
+    q = fmin(fmax(q, 0.0), (double)qmax);
+    const int qi = (int)q, g = i / 64, l = i % 32, high = (i / 32) & 1;
+    uint8_t* byte = &qs[32 * g + l];
+    if (high) *byte = (uint8_t)((*byte & 0x0F) | ((qi & 15) << 4));
+    else *byte = (uint8_t)((*byte & 0xF0) | (qi & 15));
+    if (qh && (qi >> 4)) qh[l] |= (uint8_t)(1u << (2 * g + high));
+  }
+}
+
+static void quant_super_q6_k(const double* x, uint8_t* out) {
+  double step[16], dmax = 0.0;
+  for (int k = 0; k < 16; ++k) {
+    double amax = 0.0;
+    for (int i = 0; i < 16; ++i) amax = fmax(amax, fabs(x[16 * k + i]));
+    step[k] = amax / 31.0;
+    dmax = fmax(dmax, step[k]);
+  }
+  const uint16_t dh = f64_to_f16_bits(dmax / 127.0);
+  const double d = f16_bits_to_f64(dh);
+  uint8_t* ql = out;
+  uint8_t* qh = out + 128;
+  int8_t* scales = (int8_t*)(out + 192);
+  memset(out, 0, 192);
+  for (int k = 0; k < 16; ++k) {
+    const double a = d > 0.0 ? round_half_away(step[k] / d) : 0.0;
+    scales[k] = (int8_t)(int)fmin(fmax(a, 0.0), 127.0);
+  }
+  for (int i = 0; i < 256; ++i) {
+    const double w = d * scales[i / 16];
+    double q = w > 0.0 ? round_half_away(x[i] / w) : 0.0;
+    q = fmin(fmax(q, -32.0), 31.0);
+    const int code = (int)q + 32, h = i / 128, o = i % 128, g = o / 32, l = o % 32;
+    uint8_t* lb = &ql[64 * h + 32 * (g % 2) + l];
+    if (g < 2) *lb = (uint8_t)((*lb & 0xF0) | (code & 15));
+    else *lb = (uint8_t)((*lb & 0x0F) | ((code & 15) << 4));
+    qh[32 * h + l] |= (uint8_t)(((code >> 4) & 3) << (2 * g));
+  }
+  memcpy(out + 208, &dh, 2);
+}
+
 /* ---- exported API ------------------------------------------------------- */
 
 /* n normals * sigma, elements [start, start+n) of stream key */
@@ -191,6 +287,35 @@ int synth_quant_matrix(uint64_t key, int64_t rows, int64_t cols, double sigma, i
       uint8_t* o = out + (r * nb + b) * bsz;
       if (wtype == 8) quant_block_q8_0(x, o);
       else quant_block_q4_0(x, o);
+    }
+  }
+  return 0;
+}
+
+/*
+ * K-quant matrix [rows x cols] (cols a multiple of 256) of sigma*N(0,1),
+ * element (r, c) = element r*cols + c of stream key, as the normals of
+ * synth_quant_matrix.  kind 12 = Q4_K (144-byte super-blocks), 13 = Q5_K
+ * (176), 14 = Q6_K (210).  Returns 0, or -1 on a bad kind or shape.
+ */
+int synth_quant_matrix_k(uint64_t key, int64_t rows, int64_t cols, double sigma, int kind, uint8_t* out) {
+  if ((kind != 12 && kind != 13 && kind != 14) || cols % 256) return -1;
+  const int64_t nsb = cols / 256;
+  const int64_t bsz = kind == 12 ? 144 : kind == 13 ? 176 : 210;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    double x[256];
+    for (int64_t b = 0; b < nsb; ++b) {
+      const uint64_t base = (uint64_t)(r * cols + b * 256);  /* even: cols is a multiple of 256 */
+      for (int i = 0; i < 256; i += 2) {
+        double z0, z1;
+        normal_pair(key, (base + (uint64_t)i) >> 1, &z0, &z1);
+        x[i] = sigma * z0;
+        x[i + 1] = sigma * z1;
+      }
+      uint8_t* o = out + (r * nsb + b) * bsz;
+      if (kind == 14) quant_super_q6_k(x, o);
+      else quant_super_k45(x, kind == 12 ? 15 : 31, o);
     }
   }
   return 0;

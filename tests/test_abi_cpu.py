@@ -36,7 +36,7 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_abi_version_and_status_names(lib):
-    assert lib.dls_abi_version() == 1
+    assert lib.dls_abi_version() == 2
     assert dls.status_name(0) == "OK"
     assert dls.status_name(-2) == "BUDGET"
     assert dls.status_name(-6) == "STATE"

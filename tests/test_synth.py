@@ -68,3 +68,31 @@ def test_random_gains_are_seeded_and_leave_matrices_shared():
     allg = np.concatenate([g1["output_norm"]] + [g1["layers"][l][n] for l in range(cfg.n_layers)
                                                  for n in ("attn_norm", "ffn_norm")])
     assert abs(allg.mean() - 1.0) < 0.03 and abs(allg.std() - 0.2) < 0.03
+
+
+def test_k_quant_matrices_round_trip_and_share_the_normals():
+    # the K-quant generator quantises the very normals of the Q8_0 generator
+    # (same key, same element order); the oracle's reader turns its blocks
+    # back into weights within each format's step
+    from oracle import kquant
+    key = synth.stream_key("kq-roundtrip")
+    rows, cols = 6, 768
+    x = synth.normal(key, rows * cols, 0.02).reshape(rows, cols)
+    for fmt, bound in (("q4_k", 0.08), ("q5_k", 0.04), ("q6_k", 0.02)):
+        b = synth.quant_matrix_k(key, rows, cols, 0.02, fmt)
+        assert b.size == rows * (cols // 256) * synth.KQUANT_BLOCK_BYTES[fmt]
+        w = kquant.matrix_rows(b, cols, fmt, 0, rows)
+        assert np.max(np.abs(w - x)) <= bound * np.max(np.abs(x)), fmt
+        assert abs(w.std() - x.std()) < 0.05 * x.std()
+    with pytest.raises(ValueError):
+        synth.quant_matrix_k(key, 2, 300, 0.02, "q4_k")
+
+
+def test_q4_k_m_model_weights_carry_their_formats():
+    cfg = CONFIGS["tiny"]
+    import dataclasses
+    cfgk = dataclasses.replace(cfg, ffn=768)
+    w = synth.model_weights_k(cfgk, synth.Q4_K_M)
+    assert w["formats"][(0, "wv")] == "q6_k" and w["formats"][(1, "wq")] == "q4_k"
+    assert w["formats"][(None, "output")] == "q6_k" and w["formats"][(None, "tok_embd")] == "q4_k"
+    assert w["layers"][0]["w_down"].size == cfgk.hidden * (768 // 256) * 210
