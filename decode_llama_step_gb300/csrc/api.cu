@@ -169,6 +169,7 @@ struct dls_model {
   int casc_len = 0, casc_suffix_splits = 0;
   bool batch_tc = false;  // every batched step through the small-batch tensor-core GEMM
   bool batch_rg = false;  // every batched step through the multi-row GEMV
+  bool pf_planes = true;  // prompt chunks through the split-plane GEMM (false: the exact-code one)
   std::map<std::tuple<int, int, int>, RgLaunch> rg_plans;  // (matrix kind, rows, T) -> multi-row GEMV plan
   // tensor-core GEMM split-K workspace: partial sums and per-tile counters
   float* tg_part = nullptr;
@@ -708,6 +709,10 @@ int enqueue_mixed(dls_model* m, int n, bool head, int head_row, bool argmax, flo
 
 int run_tgemm(dls_model* m, int kind, int epi, PgArgs g) {
   const TgPlan p = tgemm_plan(g.w.rows, g.w.nb * 32, g.T, m->num_sms, kTgMaxSplit);
+  if (p.bn == 128 && !m->pf_planes) {  // a prompt chunk
+    LK(kind, launch_cgemm(m->wtype, epi, g, m->stream));
+    return DLS_OK;
+  }
   if (p.split > 1) {
     if ((size_t)p.split * g.T * g.w.rows > m->tg_part_elems || (size_t)((g.w.rows + 127) / 128) > (size_t)kTgCounters)
       return fail(m, DLS_ERR_CAPACITY, "gemm split workspace rows=%d T=%d split=%d", g.w.rows, g.T, p.split);
@@ -1725,6 +1730,10 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   CKC(cudaEventCreateWithFlags(&m->ev_start, cudaEventDisableTiming));
   CKC(gemv_setup_attributes());
   CKC(tgemm_setup_attributes());
+  CKC(cgemm_setup_attributes());
+  // prompt chunks: the split-plane GEMM (default, faster as measured) or the
+  // exact-code GEMM (DLS_PREFILL_GEMM=codes)
+  if (const char* e = getenv("DLS_PREFILL_GEMM")) m->pf_planes = strcmp(e, "codes") != 0;
   CKC(sgemm_setup_attributes());
   CKC(rgemv_setup_attributes());
   // batched steps: the multi-row CUDA-core GEMV for 2-4 rows, the

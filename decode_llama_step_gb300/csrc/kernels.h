@@ -224,6 +224,10 @@ struct TgPlan {
 };
 TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split);
 cudaError_t tgemm_setup_attributes();  // smem limits; fails if tensor maps cannot be made
+// the prompt-chunk GEMM with the codes as exact MMA operands and the block
+// scales applied per 32 columns by the epilogue (gemm_codes.cu): 128 x 128 tiles, no split
+cudaError_t cgemm_setup_attributes();
+cudaError_t launch_cgemm(int wtype, int epi, const PgArgs& a, cudaStream_t s);
 cudaError_t launch_tgemm(int wtype, int epi, const PgArgs& a, const TgPlan& p, cudaStream_t s);
 // the small-batch form (T <= 8): raw codes as exact fp16 operands, block
 // scales applied per 32-column block from tensor memory (gemm_small.cu)

@@ -191,3 +191,43 @@ def test_chunk_size_does_not_change_results(gpu_lib):
     for (k, v), (k0, v0) in zip(kv, outs[0][1]):
         assert_close(k.float().cpu().numpy(), k0.float().cpu().numpy(), "K, chunks of 7", tol=1e-3)
         assert_close(v.float().cpu().numpy(), v0.float().cpu().numpy(), "V, chunks of 7", tol=1e-3)
+
+
+@pytest.mark.parametrize("cfg,pt", [(TINY, 32), (RAGGED, 32), (RAGGED_Q4, 32)], ids=["tiny", "ragged", "raggedq4"])
+def test_exact_code_gemm_prefill(gpu_lib, cfg, pt, monkeypatch):
+    """The prompt-chunk GEMM with the codes as exact MMA operands and the
+    block scales applied per 32 columns after the MMA (DLS_PREFILL_GEMM=codes,
+    read at model creation): every projection of a 300-token chunk against
+    the exact product, then a prefill's residuals and logits against the
+    oracle."""
+    torch = _torch()
+    monkeypatch.setenv("DLS_PREFILL_GEMM", "codes")
+    w = synth.model_weights(cfg)
+    m, stream = _make(cfg, w, chunk=120, page_tokens=pt, max_ctx=320)
+    monkeypatch.delenv("DLS_PREFILL_GEMM")
+    orc = OracleModel(cfg, w)
+    try:
+        shapes = synth.matrix_shapes(cfg)
+        shapes["output"] = (cfg.vocab, cfg.hidden)
+        T = 300
+        for name, (rows, cols) in shapes.items():
+            x = synth.normal(synth.stream_key("gemm-x", name, T), T * cols, 1.0).astype(np.float32).reshape(T, cols)
+            y = torch.empty(T, rows, device="cuda")
+            m.debug_gemm(1, name, torch.from_numpy(x).cuda(), y)
+            W = quant.matrix(w[name] if name == "output" else w["layers"][1][name], rows, cols, cfg.wtype)
+            assert rel_err(y.cpu().numpy(), x.astype(np.float64) @ W.T) <= 1e-5, name
+        prompt = synth.prompt_tokens(cfg, 250, seed=6)
+        seq = m.seq_create()
+        lg = torch.empty(cfg.vocab, device="cuda")
+        cap = torch.empty(cfg.n_layers, cfg.hidden, device="cuda")
+        m.debug_capture(cap)
+        m.prefill(seq, prompt, lg)
+        stream.synchronize()
+        oseq = orc.new_seq(capacity=260)
+        ocap = []
+        ref = orc.prefill(oseq, prompt, capture=ocap)
+        for l in range(cfg.n_layers):
+            assert_close(cap[l].cpu().numpy(), ocap[l], f"codes GEMM prefill layer {l}")
+        assert_close(lg.cpu().numpy(), ref, "codes GEMM prefill logits")
+    finally:
+        m.close()
