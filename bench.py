@@ -935,6 +935,7 @@ def main():
     peak, peak_src = peaks()
     achieved = gemv_bytes_total / (gemv_ms_total / 1000.0) / 1e9 if gemv_ms_total else 0.0
     persistent = launches == 1
+    step_used, step_why = m.step_kernel_in_use()
     if persistent:
         # one cooperative launch per token: the step kernel is the whole
         # step; its duration is the span of its phase timestamps
@@ -987,6 +988,7 @@ def main():
             "hbm": {"algorithmic_bytes_per_step": step_b, "achieved_gbs": round(whole, 1),
                     "frac_of_peak": round(whole / peak, 4), "peak_gbs": peak},
             "roofline": roofline,
+            "decode_path": "persistent step kernel" if step_used else f"separate kernels ({step_why})",
             "kernels": per_kind,
             "e2e": {"value": round(e2e_val, 3), "unit": "tok/s", "h2d_bytes_per_step": 8,
                     "d2h_bytes_per_step": cfg.vocab * 4,

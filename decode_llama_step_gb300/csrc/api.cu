@@ -2542,6 +2542,21 @@ int dls_debug_profile_batch(dls_model* m, int32_t n, const int32_t* seqs, const 
   return DLS_OK;
 }
 
+int32_t dls_step_kernel_in_use(const dls_model* m, const char** why) {
+  if (why) *why = nullptr;
+  if (!m) return 0;
+  if (m->use_step) return 1;
+  if (why) {
+    const char* e = getenv("DLS_STEP_KERNEL");
+    if (e && atoi(e) == 0) *why = "disabled";
+    else if (m->mixed) *why = "mixed weight formats";
+    else if (m->resident < m->L) *why = "not all layers resident";
+    else if (!m->step.fn) *why = m->step.why ? m->step.why : "not planned";
+    else *why = "not set up";
+  }
+  return 0;
+}
+
 int dls_debug_step_trace(dls_model* m, uint64_t* out, int32_t max_entries, int32_t* n_entries) {
   if (!m) return fail(m, DLS_ERR_ARG, "model=NULL");
   if (!out || !n_entries || max_entries < 0) return fail(m, DLS_ERR_ARG, "output arrays");

@@ -190,6 +190,7 @@ struct StepPlan {
   const void* fn;  // NULL: no persistent kernel for this shape
   int grid, threads, smem, ns, splits;
   uint32_t stage_bytes;
+  const char* why;  // when fn is NULL: the reason
 };
 
 StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, int hd, int num_sms);

@@ -905,8 +905,11 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
+// At most 168 registers a thread: the 10 warps spread 3-3-2-2 over the
+// SM's four schedulers, and three warps x 32 threads x 168 registers fill
+// one scheduler's 16K-entry register file (at 200 the CTA does not launch).
 template <int WT, int HD, int G, int RSA, int MCA, int RSB, int MCB>
-__global__ void __maxnreg__(200) step_kernel(const StepArgs A) {
+__global__ void __maxnreg__(168) step_kernel(const StepArgs A) {
   extern __shared__ __align__(128) uint8_t smem[];
   Ctx c;
   c.A = &A;
@@ -1107,7 +1110,9 @@ int pow2_rows(int row_bytes) {
 StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, int hd, int num_sms) {
   StepPlan p{};
   p.fn = nullptr;
+  p.why = "the O projection's input width differs from the hidden size";
   if (q_rows != H) return p;  // O projection must share the hidden-size geometry
+  p.why = "hidden or FFN size not a multiple of 4";
   if (H % 4 || F % 4) return p;  // activation slices are read as whole float4
   const int G = n_heads / n_kv;
   const int nb_h = (H + 31) / 32, nb_f = (F + 31) / 32;
@@ -1121,6 +1126,7 @@ StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, i
       p.fn = v.fn();
       break;
     }
+  p.why = "no instantiation for this shape";
   if (!p.fn) return p;
   const int ds_h = (nb_h + 7) & ~7, ds_f = (nb_f + 7) & ~7;
   size_t stage = std::max((size_t)rsa * (rb_h + ds_h * 2), (size_t)rsb * (rb_f + ds_f * 2));
@@ -1134,6 +1140,7 @@ StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, i
   ns = std::min(ns, kMaxStages);
   if (const char* e = getenv("DLS_STEP_STAGES")) ns = std::min(ns, std::max(2, atoi(e)));  // tuning knob
   if (ns < 2) {
+    p.why = "fewer than two ring stages fit in shared memory";
     p.fn = nullptr;
     return p;
   }
@@ -1142,19 +1149,23 @@ StepPlan step_plan(int wtype, int H, int q_rows, int F, int n_heads, int n_kv, i
   p.smem = (int)(head + ns * stage);
   p.grid = num_sms;
   p.threads = NTHR;
+  p.why = nullptr;
   p.splits = std::min(num_sms / n_kv, 128);  // the merge holds up to 4 x 32 splits' (m, l) pairs per warp
   if (p.splits < 1) {
+    p.why = "more KV heads than SMs";
     p.fn = nullptr;
     return p;
   }
   if (cudaFuncSetAttribute(p.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem) != cudaSuccess) {
     cudaGetLastError();
+    p.why = "the shared-memory size was refused";
     p.fn = nullptr;
     return p;
   }
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p.fn, p.threads, p.smem) != cudaSuccess || occ < 1) {
     cudaGetLastError();
+    p.why = "one CTA per SM does not fit (registers or shared memory)";
     p.fn = nullptr;
   }
   return p;

@@ -97,6 +97,7 @@ _SIGS = {
     "dls_debug_launches_per_step": (i32, [vp]),
     "dls_debug_profile_step": (ctypes.c_int, [vp, i32, i32, i32, i32, vp, vp, vp]),
     "dls_debug_step_trace": (ctypes.c_int, [vp, vp, i32, vp]),
+    "dls_step_kernel_in_use": (i32, [vp, vp]),
     "dls_debug_profile_batch": (ctypes.c_int, [vp, i32, vp, vp, vp, i32, vp, vp, vp]),
 }
 
@@ -495,6 +496,13 @@ class Model:
 
     def launches_per_step(self) -> int:
         return int(self.lib.dls_debug_launches_per_step(self.handle))
+
+    def step_kernel_in_use(self):
+        """(True, None) when batch-1 steps run as the persistent step kernel,
+        else (False, reason)."""
+        why = ctypes.c_char_p()
+        used = bool(self.lib.dls_step_kernel_in_use(self.handle, ctypes.byref(why)))
+        return used, (why.value.decode() if why.value else None)
 
     def last_error(self) -> str:
         return self.lib.dls_last_error(self.handle).decode(errors="replace")

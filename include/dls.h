@@ -482,6 +482,14 @@ int dls_debug_step_trace(dls_model* m, uint64_t* out, int32_t max_entries, int32
  * library's kernels, per step). */
 int32_t dls_debug_launches_per_step(const dls_model* m);
 
+/* Whether batch-1 steps run as the one persistent step kernel (1) or as
+ * separate kernels (0).  When 0 and the persistent kernel was wanted,
+ * *why (may be NULL) receives the reason as a static string ("disabled",
+ * "not all layers resident", "mixed weight formats", or the planner's
+ * reason: no instantiation for the shape, shared memory or registers do
+ * not fit one CTA per SM, ...); NULL when in use. */
+int32_t dls_step_kernel_in_use(const dls_model* m, const char** why);
+
 /* ---- errors -------------------------------------------------------------------- */
 
 const char* dls_last_error(const dls_model* m);

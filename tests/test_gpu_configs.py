@@ -228,6 +228,8 @@ def test_8b_every_layer_teacher_forced(gpu_lib, w8b, ctx):
     toks = [int(t) for t in synth.prompt_tokens(cfg, D, seed=6)]
     m, stream = gpu_model(cfg, w, max_seqs=1, max_ctx=ctx + D + 8)
     try:
+        used, why = m.step_kernel_in_use()
+        assert used, why
         seq = m.seq_create()
         m.prefill(seq, prompt)
         steps = []
@@ -462,4 +464,8 @@ def test_70b_q4_0_resident_and_streamed(gpu_lib):
             release(m)
     assert runs["resident"][0] == runs["budget"][0]
     assert np.array_equal(runs["resident"][1], runs["budget"][1])
-    assert_close(runs["budget"][2], runs["resident"][2], "streamed vs resident logits", tol=1e-4)
+    # the fully resident model decodes through the persistent step kernel,
+    # the budgeted one through the separate kernels (its layers stream):
+    # the same arithmetic in other fp32 reduction orders, over 80 layers;
+    # each path is held to the oracle's 2e-3 above and layer by layer
+    assert_close(runs["budget"][2], runs["resident"][2], "streamed vs resident logits", tol=1e-3)

@@ -52,6 +52,9 @@ def _single_row(cfg, w, orc, env, n_prompt=20, n_decode=6, resident=None):
     try:
         if resident is not None:
             m.set_resident_layers(resident)
+        elif env.get("DLS_STEP_KERNEL") == "1":
+            used, why = m.step_kernel_in_use()
+            assert used, why
         prompt = synth.prompt_tokens(cfg, n_prompt, seed=21)
         seq = m.seq_create()
         lg = torch.empty(cfg.vocab, device="cuda")

@@ -37,6 +37,8 @@ def setup(request, gpu_lib):
     try:
         m = dls.Model(cfg, w, max_seqs=6, max_ctx=160, max_batch=4, page_tokens=32, stream=stream)
         m.step_kernel = step_kernel
+        used, why = m.step_kernel_in_use()
+        assert used == (step_kernel == "1"), why
     finally:
         if old is None:
             del os.environ["DLS_STEP_KERNEL"]
