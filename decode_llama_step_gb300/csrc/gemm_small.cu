@@ -54,8 +54,8 @@ struct SCfg {
   static constexpr int kCodes = WT == 8 ? SBM * 64 : SBM * 32;
   static constexpr int kB = 2048;                          // 16 rows (8 hi + 8 lo) x 128 bytes
   static constexpr int kStage = kB + kCodes + SBM * 16;     // B | codes | scales (8 per row)
-  static constexpr int NR = WT == 8 ? 3 : 4;
-  static constexpr int NA = 4;
+  static constexpr int NR = WT == 8 ? 5 : 8;  // ring stages: the bytes in flight set the pace
+  static constexpr int NA = 2;                // A tiles: converts run at most two steps ahead of the MMA
   static constexpr int kScOff = NA * kSATile + NR * kStage;  // float2 scales [kSR][SBM]
   static constexpr int kBarOff = kScOff + kSR * SBM * 8;
   static constexpr int kSmem = kBarOff + 512 + 1024;
@@ -211,14 +211,38 @@ __global__ void __launch_bounds__(STHREADS) sgemm_kernel(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem;
+  // Programmatic dependent launch: the next kernel in the stream may start
+  // its prologue now (it waits for this grid's completion before it reads
+  // what this one writes); this one's weights stream before its own wait.
+  griddep_launch();
 
   if (warp == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer: the first stages' codes and scales go
+    // out before the wait on the previous kernel (they do not depend on it),
+    // the activations after it
     if (lane == 0) {
       int issued = 0;
-      for (int i = 0; i < nk; ++i) {
+      const int pre = nk < C::NR ? nk : C::NR;
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t st = rbase + i * C::kStage;
+        const uint32_t bar = smem_u32(&sh.rfull[i]);
+        const int kt = kt0 + i;
+        mbar_expect_tx(bar, C::kStage);
+        tma_load_2d(st + C::kB, &tm_q, kt * (WT == 8 ? 64 : 32), m0, bar);
+        tma_load_2d(st + C::kB + C::kCodes, &tm_d, (kt * 2) & ~7, m0, bar);
+      }
+      griddep_wait();
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t st = rbase + i * C::kStage;
+        const uint32_t bar = smem_u32(&sh.rfull[i]);
+        const int kt = kt0 + i;
+        tma_load_2d(st, &tm_xh, kt * SBK, 0, bar);
+        tma_load_2d(st + 1024, &tm_xl, kt * SBK, 0, bar);
+        issued = i + 1;
+      }
+      for (int i = pre; i < nk; ++i) {
         const int s = i % C::NR;
-        if (i >= C::NR && !swait(smem_u32(&sh.rempty[s]), ((i / C::NR) - 1) & 1, &sh.abort)) break;
+        if (!swait(smem_u32(&sh.rempty[s]), ((i / C::NR) - 1) & 1, &sh.abort)) break;
         const uint32_t st = rbase + s * C::kStage;
         const uint32_t bar = smem_u32(&sh.rfull[s]);
         const int kt = kt0 + i;
@@ -277,7 +301,10 @@ __global__ void __launch_bounds__(STHREADS) sgemm_kernel(const __grid_constant__
       }
     }
   } else {
-    // ---------------- epilogue: thread = weight row (its TMEM lane)
+    // ---------------- epilogue: thread = weight row (its TMEM lane); it
+    // reads and writes what neighbouring kernels touch, so only after the
+    // previous kernel has completed
+    griddep_wait();
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int m = m0 + row;
@@ -405,9 +432,17 @@ cudaError_t launch_sgemm(int wtype, int epi, const PgArgs& a, int split, cudaStr
       !make_tmap_2d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w.d, (uint64_t)w.ds, (uint64_t)w.rows, (uint64_t)w.ds * 2, 8,
                     SBM, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  dim3 grid(1, (w.rows + SBM - 1) / SBM, split);
-  f<<<grid, STHREADS, smem, s>>>(th, tl, tq, td, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, (w.rows + SBM - 1) / SBM, split);
+  cfg.blockDim = dim3(STHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, f, th, tl, tq, td, a);
 }
 
 }  // namespace dls

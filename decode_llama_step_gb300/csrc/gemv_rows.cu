@@ -147,6 +147,11 @@ __global__ void __launch_bounds__(32 * (kRW + 1), 2) rgemv_kernel(const RgArgs a
     mbar_fence_init();
   }
   __syncthreads();
+  // Programmatic dependent launch: the next kernel may start its prologue
+  // (it waits for this grid's completion before reading its outputs); the
+  // weight stream below does not depend on the previous kernel, the
+  // consumers wait for it before reading the activations.
+  griddep_launch();
 
   if (warp == kRW) {
     // ---------------- producer
@@ -185,6 +190,7 @@ __global__ void __launch_bounds__(32 * (kRW + 1), 2) rgemv_kernel(const RgArgs a
     }
   } else {
     // ---------------- consumers
+    griddep_wait();
     float rs[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) rs[t] = 1.0f;
@@ -452,8 +458,17 @@ cudaError_t launch_rgemv(int wtype, int pro, int epi, const RgArgs& a, const RgL
     return cudaErrorInvalidValue;
   if (l.split > 1 && (!a.part || !a.counters)) return cudaErrorInvalidValue;
   if (epi == EPI_SWIGLU && (a.unit % 2 || a.w.rows % 2)) return cudaErrorInvalidValue;
-  f<<<dim3(l.grid, l.split), l.threads, l.smem, s>>>(a, l);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(l.grid, l.split);
+  cfg.blockDim = dim3(l.threads);
+  cfg.dynamicSmemBytes = l.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see the kernel's griddep calls
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, f, a, l);
 }
 
 }  // namespace dls
