@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "libdls.so")
-SOURCES = ["api.cu", "gemv.cu", "attention.cu", "misc.cu", "step.cu", "prefill.cu", "gemm.cu", "gemm_small.cu", "fattn.cu", "kquant.cu", "gemv_rows.cu", "gemm_codes.cu"]
+SOURCES = ["api.cu", "gemv.cu", "attention.cu", "misc.cu", "step.cu", "prefill.cu", "gemm.cu", "gemm_small.cu", "fattn.cu", "kquant.cu", "gemv_rows.cu", "gemm_codes.cu", "casc_tc.cu"]
 HEADERS = ["common.cuh", "kernels.h", "gemv_core.cuh", "tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

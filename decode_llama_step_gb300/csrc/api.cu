@@ -165,6 +165,7 @@ struct dls_model {
   // this step's shared length (0 = none) and suffix split count
   float *casc_o = nullptr, *casc_ml = nullptr;
   int casc_splits = 0;
+  bool casc_tc = false;  // the shared-prefix pass runs on the tensor cores (casc_tc.cu)
   bool cascade = true;
   int casc_len = 0, casc_suffix_splits = 0;
   bool batch_tc = false;  // every batched step through the small-batch tensor-core GEMM
@@ -914,7 +915,8 @@ int enqueue_batch_attention(dls_model* m, const KvView& kv, int n) {
     c.part_ml = m->casc_ml;
     c.status = &m->sp->status;
     c.max_len = m->max_ctx;
-    LK(K_ATTN, launch_cascade_prefix(c, s));
+    c.pool_rows = m->n_pages * m->nkv * m->pt;
+    LK(K_ATTN, m->casc_tc ? launch_cascade_prefix_tc(c, s) : launch_cascade_prefix(c, s));
     a.start_len = &m->sp->shared_len;
     a.pre_o = m->casc_o;
     a.pre_ml = m->casc_ml;
@@ -1876,8 +1878,14 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   }
   if (const char* e = getenv("DLS_CASCADE")) m->cascade = atoi(e) != 0;
   if (BR >= 2 && cascade_supported(m->nh, m->nkv, m->hd)) {
+    // the shared-prefix pass: on the tensor cores where the shape allows
+    // (DLS_CASCADE_TC=0 keeps the CUDA-core kernel), one CTA per SM; the
+    // CUDA-core kernel runs two CTAs per SM
+    m->casc_tc = cascade_tc_supported(m->nh, m->nkv, m->hd, m->pt);
+    if (const char* e = getenv("DLS_CASCADE_TC")) m->casc_tc = m->casc_tc && atoi(e) != 0;
+    if (m->casc_tc) CKC(cascade_tc_setup_attributes());
     // prefix partials of cascade attention: [rows][n_kv][splits][group][head_dim]
-    m->casc_splits = std::max(1, std::min(2 * m->num_sms / m->nkv, 64));  // two CTAs per SM
+    m->casc_splits = std::max(1, std::min((m->casc_tc ? 1 : 2) * m->num_sms / m->nkv, 64));
     const size_t slots = (size_t)std::min(BR, kMaxBatch) * m->nkv * m->casc_splits;
     const int g = m->nh / m->nkv;
     TRYC(dev_alloc_t(m, slots * g * m->hd, &m->casc_o, "cascade_partials"));

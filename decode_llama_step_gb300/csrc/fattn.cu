@@ -65,22 +65,6 @@ __device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, int* abort_
   }
 }
 
-// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle:
-// each K row holds 64 MN elements (128 bytes), 8-row groups along K are
-// `sbo` bytes apart and 64-element blocks along MN `lbo` bytes apart.
-__device__ __forceinline__ uint64_t umma_desc_mn128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// kind::f16 instruction descriptor with B MN-major (bit 16)
-__host__ __device__ constexpr uint32_t umma_idesc_f16_bmn(int M, int N) { return umma_idesc_f16(M, N) | (1u << 16); }
-
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);

@@ -102,9 +102,15 @@ struct CascArgs {
   float* part_ml;             // [rows][n_kv][n_splits][G]
   int32_t* status;
   int max_len;
+  int pool_rows;              // rows of head_dim in one layer's K (or V) pool (the tensor-core kernel's maps)
 };
 cudaError_t launch_cascade_prefix(const CascArgs& a, cudaStream_t s);
 bool cascade_supported(int n_heads, int n_kv, int head_dim);
+// The same pass on the tensor cores (casc_tc.cu): head_dim 64 or 128, any
+// group size up to 8, pages a multiple or a divisor of 64 tokens.
+bool cascade_tc_supported(int n_heads, int n_kv, int head_dim, int page_tokens);
+cudaError_t cascade_tc_setup_attributes();
+cudaError_t launch_cascade_prefix_tc(const CascArgs& a, cudaStream_t s);
 
 size_t attn_workspace_bytes(int rows, int n_heads, int n_kv, int head_dim, int n_splits);
 void attn_workspace_carve(void* ws, int rows, int n_heads, int n_kv, int head_dim, int n_splits, float** part_o,

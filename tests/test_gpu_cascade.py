@@ -14,36 +14,48 @@ import pytest
 
 import synth
 from oracle import OracleModel, ops
+from synth.configs import ModelConfig
 
 from parity import assert_close, check_greedy
 
 pytestmark = pytest.mark.gpu
 
 TINY = synth.get_config("tiny")
+# a group of 8 query heads per KV head: 8 branches fill 64 rows of the
+# tensor-core kernel's tile; head_dim 64 and 128
+G8 = ModelConfig("g8", 2, 512, 8, 1, 64, 1024, 1024, 10000.0, 8, 0.02)
+G8H128 = ModelConfig("g8h128", 1, 1024, 8, 1, 128, 1024, 1024, 10000.0, 8, 0.02)
 
 
-def _model(cascade: bool, max_batch=8):
+def _model(cfg, w, cascade: bool, tc: str, max_batch=8):
     import torch
     from decode_llama_step_gb300 import dls
-    old = os.environ.get("DLS_CASCADE")
-    os.environ["DLS_CASCADE"] = "1" if cascade else "0"
+    env = {"DLS_CASCADE": "1" if cascade else "0", "DLS_CASCADE_TC": tc}
+    old = {k: os.environ.get(k) for k in env}
+    os.environ.update(env)
     try:
         stream = torch.cuda.Stream()
-        w = synth.model_weights(TINY)
-        return dls.Model(TINY, w, max_seqs=2 * max_batch + 2, max_ctx=320, max_batch=max_batch, page_tokens=32,
-                         stream=stream), stream, w
+        return dls.Model(cfg, w, max_seqs=2 * max_batch + 2, max_ctx=320, max_batch=max_batch, page_tokens=32,
+                         stream=stream), stream
     finally:
-        if old is None:
-            del os.environ["DLS_CASCADE"]
-        else:
-            os.environ["DLS_CASCADE"] = old
+        for k, v in old.items():
+            if v is None:
+                del os.environ[k]
+            else:
+                os.environ[k] = v
 
 
-@pytest.fixture(scope="module")
-def models(gpu_lib):
-    on, s_on, w = _model(True)
-    off, s_off, _ = _model(False)
-    yield on, s_on, off, s_off, OracleModel(TINY, w)
+@pytest.fixture(scope="module", params=[(TINY, "1"), (TINY, "0"), (G8, "1"), (G8H128, "1")],
+                ids=["tiny-tensor-cores", "tiny-cuda-cores", "g8-tensor-cores", "g8-hd128-tensor-cores"])
+def models(request, gpu_lib):
+    """The shared-prefix pass on the tensor cores (casc_tc.cu) or on the
+    CUDA cores (DLS_CASCADE_TC=0), beside the same model without cascade
+    attention."""
+    cfg, tc = request.param
+    w = synth.model_weights(cfg)
+    on, s_on = _model(cfg, w, True, tc)
+    off, s_off = _model(cfg, w, False, tc)
+    yield cfg, on, s_on, off, s_off, OracleModel(cfg, w)
     on.close()
     off.close()
 
@@ -54,8 +66,8 @@ def test_cascade_batch_matches_oracle_and_plain_attention(models, prefix, branch
     it (150, 200: the partly filled page is copied per branch); branches
     continue from their own tokens; three teacher-forced batched steps."""
     import torch
-    on, s_on, off, s_off, orc = models
-    prompt = synth.prompt_tokens(TINY, prefix, seed=prefix)
+    cfg, on, s_on, off, s_off, orc = models
+    prompt = synth.prompt_tokens(cfg, prefix, seed=prefix)
     oseq = orc.new_seq(capacity=prefix + 8)
     orc.prefill(oseq, prompt)
     obr = [oseq.fork() for _ in range(branches)]
@@ -66,16 +78,16 @@ def test_cascade_batch_matches_oracle_and_plain_attention(models, prefix, branch
         dst = [m.seq_create() for _ in range(branches)]
         m.kv_fork(src, dst, shared=True)
         runs.append((m, stream, src, dst))
-    toks = [int(t) for t in synth.prompt_tokens(TINY, branches, seed=7)]
+    toks = [int(t) for t in synth.prompt_tokens(cfg, branches, seed=7)]
     try:
         for i in range(3):
             outs = []
             for m, stream, src, dst in runs:
-                out = torch.empty(branches, TINY.vocab, device="cuda")
+                out = torch.empty(branches, cfg.vocab, device="cuda")
                 m.decode_batch(dst, toks, [prefix + i] * branches, out)
                 stream.synchronize()
                 outs.append(out.cpu().numpy())
-            assert on.launches_per_step() == off.launches_per_step() + TINY.n_layers   # the cascade kernel ran
+            assert on.launches_per_step() == off.launches_per_step() + cfg.n_layers   # the cascade kernel ran
             for b in range(branches):
                 ref = orc.decode_step(obr[b], toks[b], prefix + i)
                 assert_close(outs[0][b], ref, f"cascade prefix {prefix} branch {b} step {i}")
@@ -92,16 +104,16 @@ def test_cascade_generate_and_mixed_batches(models):
     agrees with the plain attention path; a batch whose rows share nothing
     runs without the cascade kernel."""
     import torch
-    on, s_on, off, s_off, orc = models
+    cfg, on, s_on, off, s_off, orc = models
     prefix, B, D = 160, 6, 12
-    prompt = synth.prompt_tokens(TINY, prefix, seed=3)
+    prompt = synth.prompt_tokens(cfg, prefix, seed=3)
     res = []
     for m, stream in ((on, s_on), (off, s_off)):
         src = m.seq_create()
         m.prefill(src, prompt)
         dst = [m.seq_create() for _ in range(B)]
         m.kv_fork(src, dst, shared=True)
-        last = torch.empty(B, TINY.vocab, device="cuda")
+        last = torch.empty(B, cfg.vocab, device="cuda")
         toks = m.generate(dst, list(range(20, 20 + B)), D, last)
         stream.synchronize()
         res.append((toks, last.cpu().numpy()))
@@ -113,7 +125,7 @@ def test_cascade_generate_and_mixed_batches(models):
     seqs = []
     for r in range(3):
         s = on.seq_create()
-        on.prefill(s, synth.prompt_tokens(TINY, 140 + r, seed=30 + r))
+        on.prefill(s, synth.prompt_tokens(cfg, 140 + r, seed=30 + r))
         seqs.append(s)
     on.decode_batch(seqs, [1, 2, 3], [140, 141, 142])
     s_on.synchronize()
@@ -122,7 +134,7 @@ def test_cascade_generate_and_mixed_batches(models):
     on.kv_fork(seqs[0], [a, b], shared=True)
     on.decode_batch([a, b], [4, 5], [141, 141])
     s_on.synchronize()
-    assert on.launches_per_step() == base + TINY.n_layers
+    assert on.launches_per_step() == base + cfg.n_layers
     for q in seqs + [a, b]:
         on.seq_free(q)
 
