@@ -151,6 +151,7 @@ struct dls_model {
   size_t pairs_cap = 0;
   // prefill scratch for chunks of up to pf_cap tokens (tensor-core path)
   int pf_cap = 0, pf_ldh = 0;
+  int pf_bn = 0;  // prompt-chunk GEMM tile width: 0 choose, 128 or 256 (DLS_PREFILL_BN)
   float *pf_x = nullptr, *pf_qkv = nullptr, *pf_q = nullptr;
   __half *pf_a = nullptr, *pf_h = nullptr;        // fp16 GEMM operands (hi planes)
   __half *pf_a_lo = nullptr, *pf_h_lo = nullptr;  // their lo planes (fp16 of the rounding residual)
@@ -709,8 +710,8 @@ int enqueue_mixed(dls_model* m, int n, bool head, int head_row, bool argmax, flo
 // ---- tensor-core GEMM -----------------------------------------------------------
 
 int run_tgemm(dls_model* m, int kind, int epi, PgArgs g) {
-  const TgPlan p = tgemm_plan(g.w.rows, g.w.nb * 32, g.T, m->num_sms, kTgMaxSplit);
-  if (p.bn == 128 && !m->pf_planes) {  // a prompt chunk
+  const TgPlan p = tgemm_plan(g.w.rows, g.w.nb * 32, g.T, m->num_sms, kTgMaxSplit, m->pf_bn);
+  if (p.bn >= 128 && !m->pf_planes) {  // a prompt chunk
     LK(kind, launch_cgemm(m->wtype, epi, g, m->stream));
     return DLS_OK;
   }
@@ -1736,6 +1737,7 @@ int dls_model_create(const dls_model_desc* desc, const dls_allocator* allocator,
   // prompt chunks: the split-plane GEMM (default, faster as measured) or the
   // exact-code GEMM (DLS_PREFILL_GEMM=codes)
   if (const char* e = getenv("DLS_PREFILL_GEMM")) m->pf_planes = strcmp(e, "codes") != 0;
+  if (const char* e = getenv("DLS_PREFILL_BN")) m->pf_bn = atoi(e) == 128 ? 128 : atoi(e) == 256 ? 256 : 0;
   CKC(sgemm_setup_attributes());
   CKC(rgemv_setup_attributes());
   // batched steps: the multi-row CUDA-core GEMV for 2-4 rows, the
@@ -2736,7 +2738,7 @@ int dls_debug_gemm(dls_model* m, int32_t layer, int32_t tensor, int32_t n_tokens
     g.y = pair ? static_cast<float*>(yt) : y;
     g.ldy = w.rows;
     g.status = &m->sp->status;
-    const TgPlan p = tgemm_plan(w.rows, kx, n_tokens, m->num_sms, kTgMaxSplit);
+    const TgPlan p = tgemm_plan(w.rows, kx, n_tokens, m->num_sms, kTgMaxSplit, m->pf_bn);
     if (p.split > 1) {
       if ((size_t)p.split * n_tokens * w.rows > m->tg_part_elems) e = cudaErrorInvalidValue;
       g.part = m->tg_part;

@@ -27,6 +27,7 @@
 #include <cuda.h>
 
 #include <mutex>
+#include <stdlib.h>
 
 #include "kernels.h"
 #include "tc.cuh"
@@ -50,8 +51,10 @@ struct GCfg {
   static constexpr int kStage = 2 * kB + kCodes + kScaleBox;  // bytes the TMA lands per stage: x hi | x lo | codes | scales
   // small batches: two CTAs per SM (<= 113 KB each), one streaming while
   // the other starts up or finishes
-  static constexpr int NR = BN >= 128 ? 3 : (WT == 8 ? 3 : 4);
-  static constexpr int NA = BN >= 128 ? 3 : 2;                // fp16 weight tiles (hi and lo planes)
+  // prompt chunks: 128-token tiles with three stages, or 256-token tiles
+  // (each dequantised weight tile feeds twice the tokens) with two
+  static constexpr int NR = BN >= 256 ? 2 : BN >= 128 ? 3 : (WT == 8 ? 3 : 4);
+  static constexpr int NA = BN >= 256 ? 2 : BN >= 128 ? 3 : 2;  // fp16 weight tiles (hi and lo planes)
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
   static constexpr int kBarOff = NA * 2 * kATile + NR * kStage;
   static constexpr int kSmem = kBarOff + 256 + 1024;
@@ -430,6 +433,7 @@ TgFn tg_select(int wtype, int epi, int bn, int* smem) {
   switch (bn) {
     case 16: return tg_pick<16>(wtype, epi, smem);
     case 128: return tg_pick<128>(wtype, epi, smem);
+    case 256: return tg_pick<256>(wtype, epi, smem);
   }
   return nullptr;
 }
@@ -439,7 +443,7 @@ TgFn tg_select(int wtype, int epi, int bn, int* smem) {
 cudaError_t tgemm_setup_attributes() {
   for (int wt : {8, 4})
     for (int e : {EPI_STORE, EPI_RESID, EPI_SWIGLU})
-      for (int bn : {16, 128}) {
+      for (int bn : {16, 128, 256}) {
         int smem = 0;
         TgFn f = tg_select(wt, e, bn, &smem);
         cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -448,7 +452,7 @@ cudaError_t tgemm_setup_attributes() {
   return encode_fn() ? cudaSuccess : cudaErrorNotSupported;
 }
 
-TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split) {
+TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split, int chunk_bn) {
   TgPlan p{};
   const int mt = (rows + GBM - 1) / GBM;
   const int nk = (kpad + GBK - 1) / GBK;
@@ -469,9 +473,11 @@ TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split) {
       }
     }
   } else {
-    // prompt chunk: 128-token tiles (two activation planes and two weight
-    // planes leave no room for wider ones)
-    p.bn = 128;
+    // prompt chunk: 256-token tiles when they still give every SM a tile
+    // (half the dequantising work per token of 128-token tiles), else 128;
+    // chunk_bn 128 or 256 fixes the width (0: choose)
+    const int t256 = mt * ((T + 255) / 256);
+    p.bn = chunk_bn == 128 ? 128 : chunk_bn == 256 ? 256 : (T >= 256 && t256 >= num_sms) ? 256 : 128;
     p.split = 1;
   }
   return p;

@@ -229,7 +229,7 @@ struct PgArgs {
 struct TgPlan {
   int bn, split;
 };
-TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split);
+TgPlan tgemm_plan(int rows, int kpad, int T, int num_sms, int max_split, int chunk_bn = 0);
 cudaError_t tgemm_setup_attributes();  // smem limits; fails if tensor maps cannot be made
 // the prompt-chunk GEMM with the codes as exact MMA operands and the block
 // scales applied per 32 columns by the epilogue (gemm_codes.cu): 128 x 128 tiles, no split

@@ -95,6 +95,30 @@ def test_gemm_every_matrix(setup, T):
         assert rel_err(_f16(x) @ _f16(W).T, exact) > 10 * e or e < 1e-6
 
 
+@pytest.mark.parametrize("T", [256, 300, 520])
+def test_gemm_256_token_tiles(gpu_lib, T, monkeypatch):
+    """Prompt chunks on 256-token tiles (DLS_PREFILL_BN=256; large matrices
+    choose them by themselves): every matrix of the ragged shapes, token
+    counts on and off a tile boundary, against the exact product."""
+    torch = _torch()
+    monkeypatch.setenv("DLS_PREFILL_BN", "256")
+    for cfg in (RAGGED, RAGGED_Q4):
+        w = synth.model_weights(cfg)
+        m, stream = _make(cfg, w, max_ctx=600)
+        try:
+            shapes = synth.matrix_shapes(cfg)
+            for name, (rows, cols) in shapes.items():
+                x = synth.normal(synth.stream_key("gemm256-x", name, T), T * cols, 1.0).astype(np.float32)
+                x = x.reshape(T, cols)
+                y = torch.empty(T, rows, device="cuda")
+                m.debug_gemm(1, name, torch.from_numpy(x).cuda(), y)
+                W = quant.matrix(w["layers"][1][name], rows, cols, cfg.wtype)
+                e = rel_err(y.cpu().numpy(), x.astype(np.float64) @ W.T)
+                assert e <= 1e-5, f"{cfg.name} {name} T={T}: vs the exact product {e:.3e}"
+        finally:
+            m.close()
+
+
 def _read_kv(m, cfg, seq, n, layer):
     torch = _torch()
     kvd = cfg.n_kv_heads * cfg.head_dim
