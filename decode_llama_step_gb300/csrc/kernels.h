@@ -281,6 +281,7 @@ struct KqArgs {
 struct KqLaunch {
   int grid, threads, smem;
   int nwc, rs, ns, mc;  // consumer warps, rows per ring stage, stages, units per lane
+  int wide;             // Q4_K / Q5_K: 64-weight units (else 32)
 };
 
 size_t kq_packed_bytes(int fmt, int rows, int cols);

@@ -17,10 +17,17 @@
 // consumer lane owns a fixed slice of the columns ("unit"), holds that slice
 // of x as int16 with one scale in registers, and takes exact int32 dot
 // products of codes and activations (dp2a) per row.
-//  * Q4_K unit: 16 code bytes = 32 weights, the low nibbles of sub-block 2g
-//    and the high nibbles of sub-block 2g+1; eight units per super-block.
+//  * Q4_K unit: the low nibbles of sub-block 2g and the high nibbles of
+//    sub-block 2g+1 (one pair of 6-bit scales and minimums, decoded once per
+//    unit).  Wide units (rows of 16K columns or more): all 32 code bytes of
+//    the pair = 64 weights, four per super-block.  Narrow units (shorter
+//    rows, where more lanes per row keep more warps in flight): 16 code
+//    bytes = 32 weights, eight per super-block.
 //    y += xs * (d * (sc_a I_a + sc_b I_b) - dmin * (m_a S_a + m_b S_b)), with
 //    I the integer code-activation dots and S the sums of the int16 slice.
+//    The high nibbles enter the dot product in place (byte & 0xF0 = 16 x
+//    code) and I_b is the exact quotient by 16 (Q5_K, whose fifth bit sits
+//    above the nibble, shifts them down instead).
 //  * Q6_K unit: 48 code bytes = 64 weights in four groups of 16, each group
 //    with its int8 scale; y += xs * d * sum_g sc_g (I_g - 32 S_g).
 #include <stdlib.h>
@@ -43,9 +50,9 @@ namespace {
 // lane.  Cols up to 32768 fit.
 constexpr int kMaxWarps = 31;
 constexpr int kMaxWarpsMC = 8;
-template <int FMT, int MC>
+template <int FMT, int MC, int W>
 struct KqBounds {
-  static constexpr int threads = MC > 1 ? 32 * (kMaxWarpsMC + 1) : FMT != KQ_Q6_K ? 1024 : 512;
+  static constexpr int threads = MC > 1 ? 32 * (kMaxWarpsMC + 1) : (FMT != KQ_Q6_K && !W) ? 1024 : 512;
 };
 constexpr int kRB = 64;              // rows per reduction block
 constexpr int kStageBytes = 16384;   // target code bytes per ring stage
@@ -57,21 +64,25 @@ struct KqShared {
   int abort;
 };
 
-template <int FMT>
+// W: wide Q4_K / Q5_K units (64 weights) or narrow ones (32); Q6_K units
+// are 64 weights either way.
+template <int FMT, int W>
 struct KqGeo {
   static constexpr bool K4 = FMT != KQ_Q6_K;               // Q4_K and Q5_K share the unit geometry
-  static constexpr int UPB = K4 ? 8 : 4;                    // units per super-block
-  static constexpr int NP = K4 ? 16 : 32;                   // int16 pairs per unit
-  static constexpr int NG = K4 ? 2 : 4;                     // scale groups per unit
+  static constexpr bool WIDE = !K4 || W;
+  static constexpr int UPB = WIDE ? 4 : 8;                  // units per super-block
+  static constexpr int NP = WIDE ? 32 : 16;                 // int16 pairs per unit
+  static constexpr int NGL = NP / 8;                        // groups of 16 weights per unit
+  static constexpr int NG = K4 ? 2 : 4;                     // sums kept: per sub-block (Q4_K) or scale group (Q6_K)
   static constexpr int SB = FMT == KQ_Q4_K ? 144 : FMT == KQ_Q5_K ? 176 : 208;  // packed super-block bytes
-  static constexpr int MCMAX = K4 ? 4 : 2;                  // units per lane (registers)
+  static constexpr int MCMAX = WIDE ? 2 : 4;                // units per lane (registers)
 };
 
-template <int FMT>
+template <int FMT, int W>
 struct KqX {
-  uint32_t p[KqGeo<FMT>::NP];   // int16 pairs: element 2e in the low half of p[e]
-  int sum[KqGeo<FMT>::NG];      // per scale group: sum of the int16 values
-  float s;                      // x_i ~= s * X_i
+  uint32_t p[KqGeo<FMT, W>::NP];  // int16 pairs: element 2e in the low half of p[e]
+  int sum[KqGeo<FMT, W>::NG];     // per sum group: sum of the int16 values
+  float s;                        // x_i ~= s * X_i
 };
 
 // Byte i (0..15) of a 16-byte vector.
@@ -81,24 +92,30 @@ __device__ __forceinline__ uint32_t byte_of(const uint4& v, int i) {
 }
 
 // The element offsets (within the row) of one unit's groups of 16.
-template <int FMT>
+template <int FMT, int W>
 __device__ __forceinline__ int group_col(int unit, int g) {
-  if (FMT != KQ_Q6_K) {
+  if (FMT != KQ_Q6_K && W) {
+    // 64 consecutive columns: the low nibbles' 32 (sub-block 2gg), then the
+    // high nibbles' 32 (sub-block 2gg + 1)
+    const int sb = unit >> 2, gg = unit & 3;
+    return sb * 256 + 64 * gg + 16 * g;
+  } else if (FMT != KQ_Q6_K) {
+    // 16 columns of sub-block 2gg (g = 0, low nibbles) and the same 16 of 2gg + 1 (g = 1)
     const int sb = unit >> 3, v = unit & 7, gg = v >> 1, l0 = (v & 1) * 16;
-    return sb * 256 + 64 * gg + 32 * g + l0;        // g = 0: low nibbles, g = 1: high nibbles
+    return sb * 256 + 64 * gg + 32 * g + l0;
   } else {
     const int sb = unit >> 2, v = unit & 3, h = v >> 1, l0 = (v & 1) * 16;
     return sb * 256 + 128 * h + 32 * g + l0;
   }
 }
 
-template <int FMT>
-__device__ __forceinline__ void load_unit_x(const float* x, int unit, bool valid, KqX<FMT>& xq) {
-  constexpr int NG = KqGeo<FMT>::NG;
-  float v[NG * 16];
+template <int FMT, int W>
+__device__ __forceinline__ void load_unit_x(const float* x, int unit, bool valid, KqX<FMT, W>& xq) {
+  constexpr int NG = KqGeo<FMT, W>::NG, NGL = KqGeo<FMT, W>::NGL;
+  float v[NGL * 16];
 #pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    const int c0 = valid ? group_col<FMT>(unit, g) : 0;
+  for (int g = 0; g < NGL; ++g) {
+    const int c0 = valid ? group_col<FMT, W>(unit, g) : 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float4 f = *reinterpret_cast<const float4*>(x + c0 + 4 * j);
@@ -111,11 +128,13 @@ __device__ __forceinline__ void load_unit_x(const float* x, int unit, bool valid
   }
   float mx = 0.f;
 #pragma unroll
-  for (int i = 0; i < NG * 16; ++i) mx = fmaxf(mx, fabsf(v[i]));
+  for (int i = 0; i < NGL * 16; ++i) mx = fmaxf(mx, fabsf(v[i]));
   const float s = mx > 0.f ? mx / 32767.0f : 1.0f;
   const float inv = 1.0f / s;
 #pragma unroll
-  for (int g = 0; g < NG; ++g) {
+  for (int g = 0; g < NG; ++g) xq.sum[g] = 0;
+#pragma unroll
+  for (int g = 0; g < NGL; ++g) {
     int sum = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -123,7 +142,7 @@ __device__ __forceinline__ void load_unit_x(const float* x, int unit, bool valid
       sum += a + b;
       xq.p[g * 8 + e] = (uint32_t)(a & 0xFFFF) | ((uint32_t)b << 16);
     }
-    xq.sum[g] = sum;
+    xq.sum[g * NG / NGL] += sum;  // wide Q4_K / Q5_K units: two groups per sub-block
   }
   xq.s = s;
 }
@@ -140,7 +159,8 @@ __device__ __forceinline__ int dot16(const uint32_t (&c)[4], const uint32_t* p) 
 }
 
 // Per-lane byte selectors for the Q4_K scale bytes of the lane's two
-// sub-blocks s = 2g, 2g+1 (g = (lane & 7) >> 1, fixed for the kernel).
+// sub-blocks s = 2g, 2g+1 (g = lane & 3 for wide units, (lane & 7) >> 1 for
+// narrow ones; fixed for the kernel).
 // Scale bytes 0-7 are words y, z of the super-block's first 16 bytes (after
 // d, dmin), bytes 8-11 word w.
 //   g < 2:  [sc_a, sc_b, m_a, m_b] = low 6 bits of bytes (s, s, s+4, s+4)
@@ -151,8 +171,8 @@ struct Q4kSel {
   bool split;
 };
 
-__device__ __forceinline__ Q4kSel q4k_sel(int lane) {
-  const int g = (lane & 7) >> 1, a = 2 * g;
+__device__ __forceinline__ Q4kSel q4k_sel(int lane, bool wide) {
+  const int g = wide ? lane & 3 : (lane & 7) >> 1, a = 2 * g;
   Q4kSel q;
   q.split = g >= 2;
   q.s1 = q.split ? (uint32_t)((a - 4) | (a - 3) << 4 | a << 8 | (a + 1) << 12)
@@ -161,21 +181,26 @@ __device__ __forceinline__ Q4kSel q4k_sel(int lane) {
   return q;
 }
 
-// One Q4_K unit of one row: codes at qa (16 bytes), super-block head at ma.
-// Q5_K (FIFTH): the fifth code bits at ha, bit 2g of byte l for the low
-// nibbles' weights and bit 2g + 1 for the high nibbles'.
-template <bool FIFTH, int FMT>
-__device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, uint32_t ha, int g, const Q4kSel& sel,
-                                           const KqX<FMT>& xq) {
-  const uint4 q = lds128(qa);
-  const uint4 m = lds128(ma);
-  const float d = __half2float(__ushort_as_half((unsigned short)(m.x & 0xFFFF)));
-  const float dmin = __half2float(__ushort_as_half((unsigned short)(m.x >> 16)));
-  // [sc_a, sc_b, m_a, m_b], one per byte
+// The scale bytes [sc_a, sc_b, m_a, m_b] of the lane's sub-block pair and
+// the super-block's d and dmin, from its 16-byte head.
+__device__ __forceinline__ uint32_t q4k_scales(const uint4& m, const Q4kSel& sel, float& d, float& dmin) {
+  d = __half2float(__ushort_as_half((unsigned short)(m.x & 0xFFFF)));
+  dmin = __half2float(__ushort_as_half((unsigned short)(m.x >> 16)));
   const uint32_t t1 = __byte_perm(m.y, m.z, sel.s1);
   const uint32_t t2 = __byte_perm(m.w, 0u, sel.s2);
-  const uint32_t v = sel.split ? ((t2 & 0x00000F0Fu) | ((t2 >> 4) & 0x0F0F0000u) | (((t1 >> 6) & 0x03030303u) << 4))
-                               : (t1 & 0x3F3F3F3Fu);
+  return sel.split ? ((t2 & 0x00000F0Fu) | ((t2 >> 4) & 0x0F0F0000u) | (((t1 >> 6) & 0x03030303u) << 4))
+                   : (t1 & 0x3F3F3F3Fu);
+}
+
+// One narrow Q4_K unit of one row: codes at qa (16 bytes), super-block head
+// at ma.  Q5_K (FIFTH): the fifth code bits at ha, bit 2g of byte l for the
+// low nibbles' weights and bit 2g + 1 for the high nibbles'.
+template <bool FIFTH, int FMT>
+__device__ __forceinline__ float unit_q4_k_narrow(uint32_t qa, uint32_t ma, uint32_t ha, int g, const Q4kSel& sel,
+                                                  const KqX<FMT, 0>& xq) {
+  const uint4 q = lds128(qa);
+  float d, dmin;
+  const uint32_t v = q4k_scales(lds128(ma), sel, d, dmin);
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
   uint32_t lo[4], hi[4];
 #pragma unroll
@@ -200,9 +225,52 @@ __device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, uint32_t ha
   return xq.s * fmaf(d, (float)isc, -dmin * (float)imn);
 }
 
+// One wide Q4_K unit of one row: codes at qa (32 bytes), super-block head at
+// ma.  Q5_K (FIFTH): the fifth code bits at ha (32 bytes), bit 2g of byte l
+// for the low nibbles' weights and bit 2g + 1 for the high nibbles'.
+template <bool FIFTH, int FMT>
+__device__ __forceinline__ float unit_q4_k(uint32_t qa, uint32_t ma, uint32_t ha, int g, const Q4kSel& sel,
+                                           const KqX<FMT, 1>& xq) {
+  const uint4 q0 = lds128(qa), q1 = lds128(qa + 16);
+  float d, dmin;
+  const uint32_t v = q4k_scales(lds128(ma), sel, d, dmin);
+  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  uint32_t lo[8], hi[8];
+  int ia, ib;
+  if constexpr (FIFTH) {
+    const uint4 h0 = lds128(ha), h1 = lds128(ha + 16);
+    const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lo[k] = (w[k] & 0x0F0F0F0Fu) | (((hw[k] >> (2 * g)) & 0x01010101u) << 4);
+      hi[k] = ((w[k] >> 4) & 0x0F0F0F0Fu) | (((hw[k] >> (2 * g + 1)) & 0x01010101u) << 4);
+    }
+    ia = dot16(*reinterpret_cast<const uint32_t(*)[4]>(lo), xq.p) +
+         dot16(*reinterpret_cast<const uint32_t(*)[4]>(lo + 4), xq.p + 8);
+    ib = dot16(*reinterpret_cast<const uint32_t(*)[4]>(hi), xq.p + 16) +
+         dot16(*reinterpret_cast<const uint32_t(*)[4]>(hi + 4), xq.p + 24);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lo[k] = w[k] & 0x0F0F0F0Fu;
+      hi[k] = w[k] & 0xF0F0F0F0u;  // 16 x the high nibble
+    }
+    ia = dot16(*reinterpret_cast<const uint32_t(*)[4]>(lo), xq.p) +
+         dot16(*reinterpret_cast<const uint32_t(*)[4]>(lo + 4), xq.p + 8);
+    // |16 I_b| <= 32 x 240 x 32767 < 2^31; a multiple of 16, so the shift is exact
+    ib = (dot16(*reinterpret_cast<const uint32_t(*)[4]>(hi), xq.p + 16) +
+          dot16(*reinterpret_cast<const uint32_t(*)[4]>(hi + 4), xq.p + 24)) >> 4;
+  }
+  // exact in int32: |sc * I| <= 63 * 32 * 31 * 32767 (twice that < 2^31),
+  // |m * S| <= 63 * 32 * 32767
+  const int isc = (int)(v & 0xFFu) * ia + (int)((v >> 8) & 0xFFu) * ib;
+  const int imn = (int)((v >> 16) & 0xFFu) * xq.sum[0] + (int)(v >> 24) * xq.sum[1];
+  return xq.s * fmaf(d, (float)isc, -dmin * (float)imn);
+}
+
 // One Q6_K unit of one row: ql halves at aa / ba, qh at ha, scales at sa.
 __device__ __forceinline__ float unit_q6_k(uint32_t aa, uint32_t ba, uint32_t ha, uint32_t sa, float d, int lane,
-                                           const KqX<KQ_Q6_K>& xq) {
+                                           const KqX<KQ_Q6_K, 1>& xq) {
   const uint4 A = lds128(aa), B = lds128(ba), Q = lds128(ha), S = lds128(sa);
   const uint32_t a[4] = {A.x, A.y, A.z, A.w}, b[4] = {B.x, B.y, B.z, B.w}, qh[4] = {Q.x, Q.y, Q.z, Q.w};
   const int base = 8 * ((lane & 3) >> 1) + (lane & 1);   // scale of group 0 (8h + l0/16)
@@ -224,9 +292,10 @@ __device__ __forceinline__ float unit_q6_k(uint32_t aa, uint32_t ba, uint32_t ha
   return xq.s * d * acc;
 }
 
-template <int FMT, int RS, int MC>
-__global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC>::threads) kq_gemv_kernel(const KqArgs a, const KqLaunch L) {
-  using G = KqGeo<FMT>;
+template <int FMT, int RS, int MC, int W>
+__global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC, W>::threads) kq_gemv_kernel(const KqArgs a,
+                                                                                       const KqLaunch L) {
+  using G = KqGeo<FMT, W>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   KqShared& sh = *reinterpret_cast<KqShared*>(smem_raw);
   float* s_part = reinterpret_cast<float*>(smem_raw + sizeof(KqShared));   // [nwc][kRB]
@@ -282,7 +351,7 @@ __global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC>::threads) kq_gemv_k
   } else {
     // ---------------- consumers
     const int nunits = nsb * G::UPB;
-    KqX<FMT> xq[MC];
+    KqX<FMT, G::WIDE ? 1 : 0> xq[MC];
     bool valid[MC];
     int ubase[MC];
 #pragma unroll
@@ -290,9 +359,9 @@ __global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC>::threads) kq_gemv_k
       const int unit = (warp + k * nwc) * 32 + lane;
       valid[k] = unit < nunits;
       ubase[k] = valid[k] ? unit : 0;
-      load_unit_x<FMT>(a.x, ubase[k], valid[k], xq[k]);
+      load_unit_x<FMT, G::WIDE ? 1 : 0>(a.x, ubase[k], valid[k], xq[k]);
     }
-    const Q4kSel qsel = q4k_sel(lane);
+    const Q4kSel qsel = q4k_sel(lane, G::WIDE);
     const int stages_per_block = kRB / RS;
     for (int s = 0; s < nst; ++s) {
       const int slot = s % NS;
@@ -313,15 +382,17 @@ __global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC>::threads) kq_gemv_k
           for (int rr = 0; rr < RS; ++rr) {
             const uint32_t rowa = st + rr * row_bytes;
             float t;
-            if constexpr (FMT == KQ_Q4_K) {
+            if constexpr (FMT != KQ_Q6_K && G::WIDE) {
+              constexpr bool Q5 = FMT == KQ_Q5_K;
+              const int sb = unit >> 2, gg = unit & 3;
+              const uint32_t blk = rowa + (uint32_t)sb * G::SB;
+              t = unit_q4_k<Q5>(blk + (Q5 ? 48 : 16) + 32 * gg, blk, blk + 16, gg, qsel, xq[k]);
+            } else if constexpr (FMT != KQ_Q6_K) {
+              constexpr bool Q5 = FMT == KQ_Q5_K;
               const int sb = unit >> 3, v = unit & 7;
-              const uint32_t blk = rowa + (uint32_t)sb * 144;
-              t = unit_q4_k<false>(blk + 16 + 32 * (v >> 1) + 16 * (v & 1), blk, 0u, 0, qsel, xq[k]);
-            } else if constexpr (FMT == KQ_Q5_K) {
-              const int sb = unit >> 3, v = unit & 7;
-              const uint32_t blk = rowa + (uint32_t)sb * 176;
-              t = unit_q4_k<true>(blk + 48 + 32 * (v >> 1) + 16 * (v & 1), blk, blk + 16 + 16 * (v & 1), v >> 1, qsel,
-                                  xq[k]);
+              const uint32_t blk = rowa + (uint32_t)sb * G::SB;
+              t = unit_q4_k_narrow<Q5>(blk + (Q5 ? 48 : 16) + 32 * (v >> 1) + 16 * (v & 1), blk, blk + 16 + 16 * (v & 1),
+                                       v >> 1, qsel, xq[k]);
             } else {
               const int sb = unit >> 2, v = unit & 3, h = v >> 1, l0 = (v & 1) * 16;
               const uint32_t blk = rowa + (uint32_t)sb * 208;
@@ -357,30 +428,32 @@ __global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC>::threads) kq_gemv_k
 
 using KqFn = void (*)(const KqArgs, const KqLaunch);
 
-template <int FMT, int MC>
+template <int FMT, int MC, int W>
 KqFn kq_pick_rs(int rs) {
   switch (rs) {
-    case 1: return &kq_gemv_kernel<FMT, 1, MC>;
-    case 2: return &kq_gemv_kernel<FMT, 2, MC>;
-    case 4: return &kq_gemv_kernel<FMT, 4, MC>;
-    case 8: return &kq_gemv_kernel<FMT, 8, MC>;
+    case 1: return &kq_gemv_kernel<FMT, 1, MC, W>;
+    case 2: return &kq_gemv_kernel<FMT, 2, MC, W>;
+    case 4: return &kq_gemv_kernel<FMT, 4, MC, W>;
+    case 8: return &kq_gemv_kernel<FMT, 8, MC, W>;
   }
   return nullptr;
 }
 
-KqFn kq_pick(int fmt, int rs, int mc) {
-  if (fmt == KQ_Q4_K) {
-    if (mc <= 1) return kq_pick_rs<KQ_Q4_K, 1>(rs);
-    if (mc <= 2) return kq_pick_rs<KQ_Q4_K, 2>(rs);
-    if (mc <= 4) return kq_pick_rs<KQ_Q4_K, 4>(rs);
-  } else if (fmt == KQ_Q5_K) {
-    if (mc <= 1) return kq_pick_rs<KQ_Q5_K, 1>(rs);
-    if (mc <= 2) return kq_pick_rs<KQ_Q5_K, 2>(rs);
-    if (mc <= 4) return kq_pick_rs<KQ_Q5_K, 4>(rs);
-  } else if (fmt == KQ_Q6_K) {
-    if (mc <= 1) return kq_pick_rs<KQ_Q6_K, 1>(rs);
-    if (mc <= 2) return kq_pick_rs<KQ_Q6_K, 2>(rs);
+template <int FMT, int W>
+KqFn kq_pick_mc(int rs, int mc) {
+  if (mc <= 1) return kq_pick_rs<FMT, 1, W>(rs);
+  if (mc <= 2) return kq_pick_rs<FMT, 2, W>(rs);
+  if constexpr (!W) {
+    if (mc <= 4) return kq_pick_rs<FMT, 4, W>(rs);
   }
+  return nullptr;
+}
+
+// wide: 64-weight Q4_K / Q5_K units (ignored for Q6_K, whose units always are)
+KqFn kq_pick(int fmt, int rs, int mc, bool wide) {
+  if (fmt == KQ_Q4_K) return wide ? kq_pick_mc<KQ_Q4_K, 1>(rs, mc) : kq_pick_mc<KQ_Q4_K, 0>(rs, mc);
+  if (fmt == KQ_Q5_K) return wide ? kq_pick_mc<KQ_Q5_K, 1>(rs, mc) : kq_pick_mc<KQ_Q5_K, 0>(rs, mc);
+  if (fmt == KQ_Q6_K) return kq_pick_mc<KQ_Q6_K, 1>(rs, mc);
   return nullptr;
 }
 
@@ -505,9 +578,14 @@ KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms) {
   KqLaunch l{};
   if ((fmt != KQ_Q4_K && fmt != KQ_Q5_K && fmt != KQ_Q6_K) || cols % 256 || cols <= 0 || rows <= 0) return l;
   const int nsb = cols / 256;
-  const bool k4 = fmt != KQ_Q6_K;
-  const int upb = k4 ? 8 : 4, mcmax = k4 ? 4 : 2;
-  const int max1 = (k4 ? 1024 : 512) / 32 - 1;  // consumer warps at one unit per lane
+  // wide Q4_K / Q5_K units (fewer instructions per weight) where a row has
+  // 256 of them or more, or where there are 16K rows or more (long streams
+  // per CTA); narrow units otherwise, whose lighter lanes keep more warps in
+  // flight.  Measured on the 70B shapes: 28672 x 8192 wide 4290 GB/s, narrow
+  // 3788; 8192 x 8192 wide 2297, narrow 2608; 8192 x 28672 wide 3282, narrow 3124.
+  const bool k4 = fmt != KQ_Q6_K, wide = !k4 || nsb * 4 >= 256 || rows >= 16384;
+  const int upb = wide ? 4 : 8, mcmax = wide ? 2 : 4;
+  const int max1 = (wide ? 512 : 1024) / 32 - 1;  // consumer warps at one unit per lane
   const int nchunk = (nsb * upb + 31) / 32;
   int nwc = 0, mc = 0;
   if (nchunk <= max1) {
@@ -525,7 +603,7 @@ KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms) {
   int rs = 1;
   while (rs < 8 && (rs * 2) * row_bytes <= kStageBytes) rs *= 2;
   const int stage = rs * (row_bytes + drow);
-  KqFn f = kq_pick(fmt, rs, mc);
+  KqFn f = kq_pick(fmt, rs, mc, wide);
   if (!f) return l;
   const int threads = 32 * (nwc + 1);
   const int head = (int)((sizeof(KqShared) + nwc * kRB * 4 + 127) & ~127);
@@ -550,6 +628,7 @@ KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms) {
   if (!best_occ) return l;
   l.nwc = nwc;
   l.mc = mc;
+  l.wide = wide ? 1 : 0;
   l.rs = rs;
   l.ns = best_ns;
   l.threads = threads;
@@ -561,17 +640,18 @@ KqLaunch kq_plan(int fmt, int rows, int cols, int num_sms) {
 cudaError_t kq_setup_attributes() {
   for (int fmt : {(int)KQ_Q4_K, (int)KQ_Q5_K, (int)KQ_Q6_K})
     for (int rs : {1, 2, 4, 8})
-      for (int mc : {1, 2, 4}) {
-        KqFn f = kq_pick(fmt, rs, mc);
-        if (!f) continue;
-        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-      }
+      for (int mc : {1, 2, 4})
+        for (bool wide : {false, true}) {
+          KqFn f = kq_pick(fmt, rs, mc, wide);
+          if (!f) continue;
+          cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+          if (e != cudaSuccess) return e;
+        }
   return cudaSuccess;
 }
 
 cudaError_t launch_kq_gemv(int fmt, const KqArgs& a, const KqLaunch& l, cudaStream_t s) {
-  KqFn f = kq_pick(fmt, l.rs, l.mc);
+  KqFn f = kq_pick(fmt, l.rs, l.mc, l.wide != 0);
   if (!f || l.grid < 1 || l.ns > 16 || l.nwc < 1 || l.nwc > kMaxWarps || a.cols % 256 || !a.w || !a.x || !a.y ||
       (fmt == KQ_Q6_K && !a.d6))
     return cudaErrorInvalidValue;
