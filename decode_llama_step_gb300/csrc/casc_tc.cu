@@ -9,11 +9,16 @@
 //   S = Q K^T       tcgen05.mma kind::f16, M = 128, N = 64 keys, K = hd, with
 //                   Q as two fp16 planes q_hi = fp16(q), q_lo = fp16(q - q_hi):
 //                   q_hi k + q_lo k carries q to ~22 bits (k is fp16 exactly)
-//   softmax         warps 2-5, thread = row: scale, mask keys past the prefix,
-//                   running max, p = exp(s - max) as the planes p_hi, p_lo
+//   softmax         warps 2-9, two threads per row (each half the tile's
+//                   keys and half the output columns; the pair exchanges its
+//                   maxima through shared memory): scale, mask keys past the
+//                   prefix, running max, p = exp(s - max) as the planes
+//                   p_hi, p_lo
 //   O_t = P V       M = 128, N = hd, K = 64 keys (V an MN-major operand),
 //                   p_hi V + p_lo V
-//   o = o * exp(max_old - max_new) + O_t   in the softmax threads' registers
+//   o = o * exp(max_old - max_new) + O_t   in the softmax threads' registers,
+//                   one tile late: P and O_t have two buffers each, so tile
+//                   j's P V runs while the softmax threads score tile j + 1
 // and the CTA writes one (m, l, o) partial per live row in the layout of the
 // CUDA-core cascade kernel (o unnormalised, relative to m; natural-log
 // units), which the per-row suffix kernel merges.  K/V tiles come from batch
@@ -31,8 +36,9 @@ namespace {
 
 constexpr int CBK = 64;     // keys per tile
 constexpr int CROWS = 128;  // MMA rows
-constexpr int CTHR = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
-constexpr int CNS = 3;      // K/V ring stages
+constexpr int CTHR = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per TMEM lane quarter)
+constexpr int NSW = 8;      // softmax warps
+constexpr int CNS = 2;      // K/V ring stages
 constexpr uint64_t kWaitNsT = 2000000000ull;
 
 template <int HD>
@@ -42,15 +48,16 @@ struct TCfg {
   static constexpr int kKV = CBK * HD * 2;    // one K or V tile
   static constexpr int kP = CROWS * CBK * 2;  // one fp16 plane of P (one swizzle atom wide)
   static constexpr int kKVOff = 2 * kQ;       // stage s: K at + 2 s kKV, V at + (2 s + 1) kKV
-  static constexpr int kPOff = kKVOff + CNS * 2 * kKV;
-  static constexpr int kBarOff = kPOff + 2 * kP;
+  static constexpr int kPOff = kKVOff + CNS * 2 * kKV;  // P buffer b: hi at + 2 b kP, lo at + (2 b + 1) kP
+  static constexpr int kXOff = kPOff + 4 * kP;  // float [3][2 halves][128 rows]: row maxima (by tile parity), l
+  static constexpr int kBarOff = kXOff + 3 * 2 * CROWS * 4;
   static constexpr int kSmem = kBarOff + 256 + 1024;
-  static constexpr int kTmemCols = 256;       // S: columns 0-63, O: 64 .. 64 + hd
+  static constexpr int kTmemCols = 512;       // S: columns 0-63, O buffer b: 64 + b hd .. 64 + (b + 1) hd
   static_assert(kSmem <= 227 * 1024, "one CTA per SM");
 };
 
 struct TBars {
-  uint64_t kv_full[CNS], kv_empty[CNS], q_full, s_full, s_free, p_full, o_full, o_free;
+  uint64_t kv_full[CNS], kv_empty[CNS], q_full, s_full, s_free, p_full, o_full[2], o_free[2];
   uint32_t tmem;
   int abort;
 };
@@ -90,7 +97,7 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   const uint32_t qhi = raw + pad, qlo = qhi + C::kQ;
   const uint32_t kvbase = raw + pad + C::kKVOff;
-  const uint32_t phi = raw + pad + C::kPOff, plo = phi + C::kP;
+  const uint32_t pbase = raw + pad + C::kPOff;
   TBars& sh = *reinterpret_cast<TBars*>(tsm + pad + C::kBarOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.n_splits;
@@ -118,12 +125,14 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
       mbar_init(smem_u32(&sh.kv_full[i]), 1);
       mbar_init(smem_u32(&sh.kv_empty[i]), 1);
     }
-    mbar_init(smem_u32(&sh.q_full), 4);
+    mbar_init(smem_u32(&sh.q_full), NSW);
     mbar_init(smem_u32(&sh.s_full), 1);
-    mbar_init(smem_u32(&sh.s_free), 4);
-    mbar_init(smem_u32(&sh.p_full), 4);
-    mbar_init(smem_u32(&sh.o_full), 1);
-    mbar_init(smem_u32(&sh.o_free), 4);
+    mbar_init(smem_u32(&sh.s_free), NSW);
+    mbar_init(smem_u32(&sh.p_full), NSW);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sh.o_full[b]), 1);
+      mbar_init(smem_u32(&sh.o_free[b]), NSW);
+    }
     sh.abort = 0;
     mbar_fence_init();
     prefetch_tmap(&tm_k);
@@ -172,7 +181,7 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t id_s = umma_idesc_f16(CROWS, CBK);
       constexpr uint32_t id_o = umma_idesc_f16_bmn(CROWS, HD);
-      const uint32_t t_s = tmem, t_o = tmem + CBK;
+      const uint32_t t_s = tmem;
       bool go = twait(smem_u32(&sh.q_full), 0, &sh.abort);
       for (int j = 0; go && j < nt; ++j) {
         const int s = j % CNS;
@@ -189,39 +198,47 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
           umma_f16(t_s, umma_desc_k128(qlo + oq), bk, id_s, 1);
         }
         umma_commit(smem_u32(&sh.s_full));
+        // P V of tile j into O buffer b (from P buffer b), once the softmax
+        // threads have taken that buffer's previous tile (j - 2)
+        const int b = j & 1;
         if (!twait(smem_u32(&sh.p_full), j & 1, &sh.abort)) break;
-        if (j > 0 && !twait(smem_u32(&sh.o_free), (j - 1) & 1, &sh.abort)) break;
+        if (j >= 2 && !twait(smem_u32(&sh.o_free[b]), ((j >> 1) - 1) & 1, &sh.abort)) break;
         tc_fence_after();
+        const uint32_t t_o = tmem + CBK + b * HD, ph = pbase + 2 * b * C::kP, pl = ph + C::kP;
 #pragma unroll
         for (int ks = 0; ks < CBK / 16; ++ks) {
           const uint64_t bv = umma_desc_mn128(vd + ks * 16 * 128, CBK * 128, 1024);
-          umma_f16(t_o, umma_desc_k128(phi + ks * 32), bv, id_o, ks != 0);
-          umma_f16(t_o, umma_desc_k128(plo + ks * 32), bv, id_o, 1);
+          umma_f16(t_o, umma_desc_k128(ph + ks * 32), bv, id_o, ks != 0);
+          umma_f16(t_o, umma_desc_k128(pl + ks * 32), bv, id_o, 1);
         }
-        umma_commit(smem_u32(&sh.o_full));
+        umma_commit(smem_u32(&sh.o_full[b]));
         umma_commit(smem_u32(&sh.kv_empty[s]));
       }
     }
     __syncwarp();
   } else {
-    // ---------------- softmax (thread = MMA row r; TMEM lane r)
-    const int quarter = warp & 3;
+    // ---------------- softmax: warp w handles TMEM lane quarter w & 3 (rows
+    // r = 32 (w & 3) + lane) and half hf = (w - 2) / 4 of the tile's keys and
+    // of the output columns
+    const int quarter = warp & 3, hf = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const bool live = r < R;
     const int rb = live ? r / G : 0, h = r % G;
+    constexpr int KH = CBK / 2, OH = HD / 2;  // keys, output columns per thread
+    float* xch = reinterpret_cast<float*>(tsm + pad + C::kXOff);  // [tile parity | l][half][row]
     // Q -> the two fp16 planes, swizzled (atom at = d / 64, 16-byte chunk
-    // (d % 64) / 8): the 128 softmax threads read the live rows' q as 8-float
+    // (d % 64) / 8): the 256 softmax threads read the live rows' q as 8-float
     // chunks, consecutive threads consecutive chunks (a batch row's G heads
     // are contiguous), every load in flight at once; rows past the live ones
     // are zero
     {
-      constexpr int CPR = HD / 8;                 // chunks per MMA row
-      constexpr int NCH = CROWS * CPR / 128;      // chunks per thread
-      const int st = tid - 64;                    // 0 .. 127
+      constexpr int CPR = HD / 8;                      // chunks per MMA row
+      constexpr int NCH = CROWS * CPR / (32 * NSW);    // chunks per thread
+      const int st = tid - 64;                         // 0 .. 255
       float4 v0[NCH], v1[NCH];
 #pragma unroll
       for (int k = 0; k < NCH; ++k) {
-        const int e = st + k * 128, rr = e / CPR, c = e % CPR;
+        const int e = st + k * 32 * NSW, rr = e / CPR, c = e % CPR;
         v0[k] = v1[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (rr < R) {
           const float* qr = a.q + (size_t)(rr / G) * a.n_heads * HD + ((size_t)kvh * G + rr % G) * HD + 8 * c;
@@ -231,7 +248,7 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
       }
 #pragma unroll
       for (int k = 0; k < NCH; ++k) {
-        const int e = st + k * 128, rr = e / CPR, c = e % CPR;
+        const int e = st + k * 32 * NSW, rr = e / CPR, c = e % CPR;
         uint4 hi, lo;
         split2(v0[k].x, v0[k].y, hi.x, lo.x);
         split2(v0[k].z, v0[k].w, hi.y, lo.y);
@@ -242,72 +259,91 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
         sts128(qlo + off, lo);
       }
       fence_async_smem();
-      // the MMA reads every row, written by any of the four warps
-      named_bar(1, 128);
+      // the MMA reads every row, written by any of the eight warps
+      named_bar(5, 32 * NSW);
       if (lane == 0) mbar_arrive(smem_u32(&sh.q_full));
     }
     const float scale = 1.0f / sqrtf((float)HD);
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    float o[HD];
+    float o[OH];
 #pragma unroll
-    for (int d = 0; d < HD; ++d) o[d] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+    for (int d = 0; d < OH; ++d) o[d] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, alpha_prev = 1.f;  // l_run: this half's keys only
     bool ok = true;
+    // o = o * alpha + (this half of tile jj's P V, in O buffer jj & 1)
+    auto accumulate_o = [&](int jj, float alpha) {
+      const int b = jj & 1;
+      if (ok && !twait(smem_u32(&sh.o_full[b]), (jj >> 1) & 1, &sh.abort)) ok = false;
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int c2 = 0; c2 < OH / 32; ++c2) {  // two 16-column loads in flight per wait
+          uint32_t v[2][16];
+          const uint32_t col = CBK + b * HD + hf * OH + c2 * 32;
+          tmem_ld16(trow + col, v[0]);
+          tmem_ld16(trow + col + 16, v[1]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              o[c2 * 32 + hh * 16 + i] = fmaf(o[c2 * 32 + hh * 16 + i], alpha, __uint_as_float(v[hh][i]));
+        }
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.o_free[b]));
+    };
+    // every iteration runs the pair's exchange barrier, even after a failed
+    // wait (the partner could otherwise wait on it for ever)
     for (int j = 0; j < nt; ++j) {
-      if (!twait(smem_u32(&sh.s_full), j & 1, &sh.abort)) {
-        ok = false;
-        break;
-      }
+      if (ok && !twait(smem_u32(&sh.s_full), j & 1, &sh.abort)) ok = false;
       tc_fence_after();
-      const int kbase = (tb + j) * CBK;
-      // pass 1: the row's max over the scaled scores of keys in the prefix
-      // (two 16-column loads in flight per wait)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c2 = 0; c2 < CBK / 32; ++c2) {
-        uint32_t v[2][16];
-        tmem_ld16(trow + c2 * 32, v[0]);
-        tmem_ld16(trow + c2 * 32 + 16, v[1]);
+      const int kbase = (tb + j) * CBK + hf * KH;  // this half's first key
+      // P buffer j & 1: its previous tile's P V (j - 2) has completed, as
+      // has every MMA issued before this tile's S = Q K^T
+      const uint32_t pbuf = pbase + 2 * (j & 1) * C::kP;
+      uint32_t sv[2][16];
+      if (ok) {
+        tmem_ld16(trow + hf * KH, sv[0]);
+        tmem_ld16(trow + hf * KH + 16, sv[1]);
         tmem_wait_ld();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (kbase + c2 * 32 + hh * 16 + i < n) mx = fmaxf(mx, __uint_as_float(v[hh][i]) * scale);
       }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (ok && kbase + hh * 16 + i < n) mx = fmaxf(mx, __uint_as_float(sv[hh][i]) * scale);
+      // the row's max over both halves
+      float* xm = xch + (j & 1) * 2 * CROWS;
+      xm[hf * CROWS + r] = mx;
+      named_bar(1 + quarter, 64);
+      mx = fmaxf(mx, xm[(hf ^ 1) * CROWS + r]);
       const float m_new = fmaxf(m_run, mx);
-      // pass 2: p = exp(s - m_new) into the two planes, and the row sum
+      // p = exp(s - m_new) into this half's chunks of the two planes, and this half's sum
       float sum = 0.f;
-#pragma unroll 1
-      for (int c2 = 0; c2 < CBK / 32; ++c2) {
-        uint32_t vv[2][16];
-        tmem_ld16(trow + c2 * 32, vv[0]);
-        tmem_ld16(trow + c2 * 32 + 16, vv[1]);
-        tmem_wait_ld();
 #pragma unroll
-        for (int c1 = 0; c1 < 2; ++c1) {
-          const int c = 2 * c2 + c1;
-          const uint32_t* v = vv[c1];
-          float p[16];
+      for (int c1 = 0; c1 < 2; ++c1) {
+        float p[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const bool in = live && kbase + c * 16 + i < n && m_new != -INFINITY;
-            p[i] = in ? expf(__uint_as_float(v[i]) * scale - m_new) : 0.f;
-            sum += p[i];
-          }
-          // keys 16c .. 16c+15 = 16-byte chunks 2c, 2c+1 of the row
+        for (int i = 0; i < 16; ++i) {
+          const bool in = ok && live && kbase + c1 * 16 + i < n && m_new != -INFINITY;
+          p[i] = in ? expf(__uint_as_float(sv[c1][i]) * scale - m_new) : 0.f;
+          sum += p[i];
+        }
+        // keys 16 (2 hf + c1) .. +15 = 16-byte chunks 2 (2 hf + c1) and +1 of the row
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int kc = 2 * c + hh;
-            uint4 hi, lo;
-            split2(p[8 * hh + 0], p[8 * hh + 1], hi.x, lo.x);
-            split2(p[8 * hh + 2], p[8 * hh + 3], hi.y, lo.y);
-            split2(p[8 * hh + 4], p[8 * hh + 5], hi.z, lo.z);
-            split2(p[8 * hh + 6], p[8 * hh + 7], hi.w, lo.w);
-            const uint32_t off = r * 128 + ((kc ^ (r & 7)) << 4);
-            sts128(phi + off, hi);
-            sts128(plo + off, lo);
-          }
+        for (int hh = 0; hh < 2; ++hh) {
+          const int kc = 2 * (2 * hf + c1) + hh;
+          uint4 hi, lo;
+          split2(p[8 * hh + 0], p[8 * hh + 1], hi.x, lo.x);
+          split2(p[8 * hh + 2], p[8 * hh + 3], hi.y, lo.y);
+          split2(p[8 * hh + 4], p[8 * hh + 5], hi.z, lo.z);
+          split2(p[8 * hh + 6], p[8 * hh + 7], hi.w, lo.w);
+          const uint32_t off = r * 128 + ((kc ^ (r & 7)) << 4);
+          sts128(pbuf + off, hi);
+          sts128(pbuf + C::kP + off, lo);
         }
       }
       tc_fence_before();
@@ -320,36 +356,24 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
       const float alpha = m_new == -INFINITY ? 1.f : expf(m_run - m_new);
       l_run = l_run * alpha + sum;
       m_run = m_new;
-      // this tile's P V -> the rescaled running sum
-      if (!twait(smem_u32(&sh.o_full), j & 1, &sh.abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int c2 = 0; c2 < HD / 32; ++c2) {  // two 16-column loads in flight per wait
-        uint32_t v[2][16];
-        tmem_ld16(trow + CBK + c2 * 32, v[0]);
-        tmem_ld16(trow + CBK + c2 * 32 + 16, v[1]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            o[c2 * 32 + hh * 16 + i] = fmaf(o[c2 * 32 + hh * 16 + i], alpha, __uint_as_float(v[hh][i]));
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.o_free));
+      // the previous tile's P V -> the running sum, rescaled by that tile's
+      // alpha (this tile's P V runs meanwhile)
+      if (j > 0) accumulate_o(j - 1, alpha_prev);
+      alpha_prev = alpha;
     }
+    if (nt > 0) accumulate_o(nt - 1, alpha_prev);
+    // the row's l: both halves' sums (the same m)
+    xch[4 * CROWS + hf * CROWS + r] = l_run;
+    named_bar(1 + quarter, 64);
+    l_run += xch[4 * CROWS + (hf ^ 1) * CROWS + r];
     ok = __all_sync(0xffffffffu, ok && !*(volatile int*)&sh.abort);
     if (ok && live) {
       const size_t slot = ((size_t)rb * a.n_kv + kvh) * S + sp;
-      float* po = a.part_o + (slot * G + h) * HD;
+      float* po = a.part_o + (slot * G + h) * HD + hf * OH;
 #pragma unroll
-      for (int c = 0; c < HD / 4; ++c)
+      for (int c = 0; c < OH / 4; ++c)
         *reinterpret_cast<float4*>(po + 4 * c) = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-      reinterpret_cast<float2*>(a.part_ml)[slot * G + h] = make_float2(m_run, l_run);
+      if (hf == 0) reinterpret_cast<float2*>(a.part_ml)[slot * G + h] = make_float2(m_run, l_run);
     }
     if (!ok && a.status && lane == 0) atomicOr(a.status, kTimeout);
   }
