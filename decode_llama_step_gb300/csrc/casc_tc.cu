@@ -9,11 +9,11 @@
 //   S = Q K^T       tcgen05.mma kind::f16, M = 128, N = 64 keys, K = hd, with
 //                   Q as two fp16 planes q_hi = fp16(q), q_lo = fp16(q - q_hi):
 //                   q_hi k + q_lo k carries q to ~22 bits (k is fp16 exactly)
-//   softmax         warps 2-9, two threads per row (each half the tile's
-//                   keys and half the output columns; the pair exchanges its
-//                   maxima through shared memory): scale, mask keys past the
-//                   prefix, running max, p = exp(s - max) as the planes
-//                   p_hi, p_lo
+//   softmax         warps 2-17, four threads per row (each a quarter of the
+//                   tile's keys and of the output columns; a row's threads
+//                   exchange their maxima through shared memory): scale, mask
+//                   keys past the prefix, running max, p = exp(s - max) as the
+//                   planes p_hi, p_lo
 //   O_t = P V       M = 128, N = hd, K = 64 keys (V an MN-major operand),
 //                   p_hi V + p_lo V
 //   o = o * exp(max_old - max_new) + O_t   in the softmax threads' registers,
@@ -36,8 +36,9 @@ namespace {
 
 constexpr int CBK = 64;     // keys per tile
 constexpr int CROWS = 128;  // MMA rows
-constexpr int CTHR = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per TMEM lane quarter)
-constexpr int NSW = 8;      // softmax warps
+constexpr int NSW = 16;     // softmax warps: HPR per TMEM lane quarter
+constexpr int HPR = NSW / 4;  // threads per row
+constexpr int CTHR = 32 * (NSW + 2);  // warp 0 TMA, warp 1 MMA, warps 2 .. NSW+1 softmax
 constexpr int CNS = 2;      // K/V ring stages
 constexpr uint64_t kWaitNsT = 2000000000ull;
 
@@ -49,8 +50,8 @@ struct TCfg {
   static constexpr int kP = CROWS * CBK * 2;  // one fp16 plane of P (one swizzle atom wide)
   static constexpr int kKVOff = 2 * kQ;       // stage s: K at + 2 s kKV, V at + (2 s + 1) kKV
   static constexpr int kPOff = kKVOff + CNS * 2 * kKV;  // P buffer b: hi at + 2 b kP, lo at + (2 b + 1) kP
-  static constexpr int kXOff = kPOff + 4 * kP;  // float [3][2 halves][128 rows]: row maxima (by tile parity), l
-  static constexpr int kBarOff = kXOff + 3 * 2 * CROWS * 4;
+  static constexpr int kXOff = kPOff + 4 * kP;  // float [3][HPR parts][128 rows]: row maxima (by tile parity), l
+  static constexpr int kBarOff = kXOff + 3 * HPR * CROWS * 4;
   static constexpr int kSmem = kBarOff + 256 + 1024;
   static constexpr int kTmemCols = 512;       // S: columns 0-63, O buffer b: 64 + b hd .. 64 + (b + 1) hd
   static_assert(kSmem <= 227 * 1024, "one CTA per SM");
@@ -218,14 +219,15 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
     __syncwarp();
   } else {
     // ---------------- softmax: warp w handles TMEM lane quarter w & 3 (rows
-    // r = 32 (w & 3) + lane) and half hf = (w - 2) / 4 of the tile's keys and
+    // r = 32 (w & 3) + lane) and part hf = (w - 2) / 4 of the tile's keys and
     // of the output columns
     const int quarter = warp & 3, hf = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const bool live = r < R;
     const int rb = live ? r / G : 0, h = r % G;
-    constexpr int KH = CBK / 2, OH = HD / 2;  // keys, output columns per thread
-    float* xch = reinterpret_cast<float*>(tsm + pad + C::kXOff);  // [tile parity | l][half][row]
+    constexpr int KH = CBK / HPR, OH = HD / HPR;  // keys, output columns per thread
+    static_assert(KH % 16 == 0 && OH % 16 == 0, "whole 16-column TMEM loads");
+    float* xch = reinterpret_cast<float*>(tsm + pad + C::kXOff);  // [tile parity | l][part][row]
     // Q -> the two fp16 planes, swizzled (atom at = d / 64, 16-byte chunk
     // (d % 64) / 8): the 256 softmax threads read the live rows' q as 8-float
     // chunks, consecutive threads consecutive chunks (a batch row's G heads
@@ -277,18 +279,14 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int c2 = 0; c2 < OH / 32; ++c2) {  // two 16-column loads in flight per wait
-          uint32_t v[2][16];
-          const uint32_t col = CBK + b * HD + hf * OH + c2 * 32;
-          tmem_ld16(trow + col, v[0]);
-          tmem_ld16(trow + col + 16, v[1]);
-          tmem_wait_ld();
+        uint32_t v[OH / 16][16];  // every load of this part's columns in flight per wait
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
+        for (int c = 0; c < OH / 16; ++c) tmem_ld16(trow + CBK + b * HD + hf * OH + c * 16, v[c]);
+        tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              o[c2 * 32 + hh * 16 + i] = fmaf(o[c2 * 32 + hh * 16 + i], alpha, __uint_as_float(v[hh][i]));
-        }
+        for (int c = 0; c < OH / 16; ++c)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[c * 16 + i] = fmaf(o[c * 16 + i], alpha, __uint_as_float(v[c][i]));
         tc_fence_before();
       }
       __syncwarp();
@@ -303,28 +301,29 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
       // P buffer j & 1: its previous tile's P V (j - 2) has completed, as
       // has every MMA issued before this tile's S = Q K^T
       const uint32_t pbuf = pbase + 2 * (j & 1) * C::kP;
-      uint32_t sv[2][16];
+      uint32_t sv[KH / 16][16];
       if (ok) {
-        tmem_ld16(trow + hf * KH, sv[0]);
-        tmem_ld16(trow + hf * KH + 16, sv[1]);
+#pragma unroll
+        for (int c = 0; c < KH / 16; ++c) tmem_ld16(trow + hf * KH + c * 16, sv[c]);
         tmem_wait_ld();
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
+      for (int hh = 0; hh < KH / 16; ++hh)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           if (ok && kbase + hh * 16 + i < n) mx = fmaxf(mx, __uint_as_float(sv[hh][i]) * scale);
-      // the row's max over both halves
-      float* xm = xch + (j & 1) * 2 * CROWS;
+      // the row's max over all its parts
+      float* xm = xch + (j & 1) * HPR * CROWS;
       xm[hf * CROWS + r] = mx;
-      named_bar(1 + quarter, 64);
-      mx = fmaxf(mx, xm[(hf ^ 1) * CROWS + r]);
+      named_bar(1 + quarter, 32 * HPR);
+#pragma unroll
+      for (int o2 = 1; o2 < HPR; ++o2) mx = fmaxf(mx, xm[((hf + o2) % HPR) * CROWS + r]);
       const float m_new = fmaxf(m_run, mx);
-      // p = exp(s - m_new) into this half's chunks of the two planes, and this half's sum
+      // p = exp(s - m_new) into this part's chunks of the two planes, and this part's sum
       float sum = 0.f;
 #pragma unroll
-      for (int c1 = 0; c1 < 2; ++c1) {
+      for (int c1 = 0; c1 < KH / 16; ++c1) {
         float p[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -332,10 +331,10 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
           p[i] = in ? expf(__uint_as_float(sv[c1][i]) * scale - m_new) : 0.f;
           sum += p[i];
         }
-        // keys 16 (2 hf + c1) .. +15 = 16-byte chunks 2 (2 hf + c1) and +1 of the row
+        // keys 16 (hf KH / 16 + c1) .. +15 = 16-byte chunks 2 (hf KH / 16 + c1) and +1 of the row
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int kc = 2 * (2 * hf + c1) + hh;
+          const int kc = 2 * (hf * (KH / 16) + c1) + hh;
           uint4 hi, lo;
           split2(p[8 * hh + 0], p[8 * hh + 1], hi.x, lo.x);
           split2(p[8 * hh + 2], p[8 * hh + 3], hi.y, lo.y);
@@ -362,10 +361,12 @@ __global__ void __launch_bounds__(CTHR, 1) casc_tc_kernel(const __grid_constant_
       alpha_prev = alpha;
     }
     if (nt > 0) accumulate_o(nt - 1, alpha_prev);
-    // the row's l: both halves' sums (the same m)
-    xch[4 * CROWS + hf * CROWS + r] = l_run;
-    named_bar(1 + quarter, 64);
-    l_run += xch[4 * CROWS + (hf ^ 1) * CROWS + r];
+    // the row's l: all parts' sums (the same m), in part order
+    xch[2 * HPR * CROWS + hf * CROWS + r] = l_run;
+    named_bar(1 + quarter, 32 * HPR);
+    l_run = 0.f;
+#pragma unroll
+    for (int o2 = 0; o2 < HPR; ++o2) l_run += xch[2 * HPR * CROWS + o2 * CROWS + r];
     ok = __all_sync(0xffffffffu, ok && !*(volatile int*)&sh.abort);
     if (ok && live) {
       const size_t slot = ((size_t)rb * a.n_kv + kvh) * S + sp;
