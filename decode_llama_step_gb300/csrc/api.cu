@@ -1306,8 +1306,12 @@ int set_params(dls_model* m, int n, const int32_t* seqs, const int32_t* tokens, 
   m->casc_len = h.shared_len;
   m->casc_suffix_splits = 0;
   if (m->casc_len > 0) {
-    // the per-row launch only covers the keys after the shared prefix
-    const int s = attn_default_splits(n, m->nkv, m->num_sms, m->max_ctx - m->casc_len);
+    // the per-row launch only covers the keys after the shared prefix; up
+    // to 8 tiles of them take one split (its partial never leaves the CTA)
+    int maxpos = pos[0];
+    for (int i = 1; i < n; ++i) maxpos = std::max(maxpos, pos[i]);
+    const int sfx_tiles = (maxpos + 1 - m->casc_len + 31) / 32;
+    const int s = sfx_tiles <= 8 ? 1 : attn_default_splits(n, m->nkv, m->num_sms, m->max_ctx - m->casc_len);
     m->casc_suffix_splits = std::max(1, std::min(std::min(s, m->attn_splits_b), 128 - m->casc_splits));
   }
   CK(launch_set_params(m->sp, h, reset, m->stream));

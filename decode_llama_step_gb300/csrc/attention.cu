@@ -224,6 +224,13 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
     for (int e = 0; e < DPL; ++e) s_wo[warp][h * HD + lane * DPL + e] = o[h][e];
   __syncthreads();
   const size_t slot0 = ((size_t)brel * a.n_kv + kvh) * S;
+  // one split (S == 1): its partial stays in shared memory, after the
+  // per-warp outputs, and this CTA merges it with the prefix partials (if
+  // any) without the global round trip and the arrival counter
+  const bool solo = S == 1;
+  float* s_po = reinterpret_cast<float*>(s_dyn + NW * HPW * HD * 4);          // [G * HD]
+  float2* s_pml = reinterpret_cast<float2*>(s_dyn + NW * HPW * HD * 4 + G * HD * 4);  // [G]
+  static_assert(NW * HPW * HD * 4 + G * HD * 4 + G * 8 <= TS * 2 * TILE * HD * 2, "solo partial must fit the stages");
   for (int idx = tid; idx < G * HD; idx += NT) {
     const int h = idx / HD, hl = h % HPW, g0 = (h / HPW) * TS;  // warps g0 .. g0+TS-1 hold head h
     float M = -INFINITY;
@@ -236,18 +243,27 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
       acc = fmaf(e, s_wo[g0 + t][hl * HD + (idx % HD)], acc);
       L = fmaf(e, s_wl[g0 + t][hl], L);
     }
-    a.part_o[(slot0 + sp) * G * HD + idx] = acc;
-    if ((idx % HD) == 0) reinterpret_cast<float2*>(a.part_ml)[(slot0 + sp) * G + h] = make_float2(M, L);
+    if (solo) {
+      s_po[idx] = acc;
+      if ((idx % HD) == 0) s_pml[h] = make_float2(M, L);
+    } else {
+      a.part_o[(slot0 + sp) * G * HD + idx] = acc;
+      if ((idx % HD) == 0) reinterpret_cast<float2*>(a.part_ml)[(slot0 + sp) * G + h] = make_float2(M, L);
+    }
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&a.counters[(size_t)brel * a.n_kv + kvh], 1);
-    s_last = prev == S - 1;
+  if (solo) {
+    __syncthreads();
+  } else {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const int prev = atomicAdd(&a.counters[(size_t)brel * a.n_kv + kvh], 1);
+      s_last = prev == S - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
 
   // ---- last CTA of this (row, kv head): merge the S splits (and the P
   // splits of the shared prefix from the cascade kernel, after them in split
@@ -263,7 +279,7 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
 #pragma unroll
     for (int k = 0; k < kMaxSplits / 32; ++k) {
       const int s = lane + 32 * k;
-      v[k] = s < S ? __ldcg(&ml[(slot0 + s) * G + h])
+      v[k] = s < S ? (solo ? s_pml[h] : __ldcg(&ml[(slot0 + s) * G + h]))
            : s < S + P ? __ldcg(&pml[(pslot0 + s - S) * G + h]) : make_float2(-INFINITY, 0.f);
       M = fmaxf(M, v[k].x);
     }
@@ -292,7 +308,8 @@ __global__ void __launch_bounds__(NT) attn_kernel(const AttnArgs a) {
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const int s = s0 + k;
-        pv[k] = s < S ? __ldcg(po + (size_t)s * G * HD) : s < S + P ? __ldcg(pp + (size_t)(s - S) * G * HD) : 0.f;
+        pv[k] = s < S ? (solo ? s_po[idx] : __ldcg(po + (size_t)s * G * HD))
+              : s < S + P ? __ldcg(pp + (size_t)(s - S) * G * HD) : 0.f;
       }
 #pragma unroll
       for (int k = 0; k < 16; ++k)
