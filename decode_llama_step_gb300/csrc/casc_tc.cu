@@ -54,7 +54,10 @@ struct TCfg {
   static constexpr int kBarOff = kXOff + 3 * HPR * CROWS * 4;
   static constexpr int kSmem = kBarOff + 256 + 1024;
   static constexpr int kTmemCols = 512;       // S: columns 0-63, O buffer b: 64 + b hd .. 64 + (b + 1) hd
-  static_assert(kSmem <= 227 * 1024, "one CTA per SM");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+  // the CTA allocates all of tensor memory: its shared memory must keep a
+  // second CTA of the kernel off the SM
+  static_assert(2 * kSmem > 227 * 1024, "one CTA per SM");
 };
 
 struct TBars {
