@@ -42,6 +42,14 @@ def test_abi_version_and_status_names(lib):
     assert dls.status_name(-6) == "STATE"
 
 
+def test_step_kernel_query_without_a_model(lib):
+    # no model: not in use, and no reason string is invented
+    why = ctypes.c_char_p(b"unset")
+    assert lib.dls_step_kernel_in_use(None, ctypes.byref(why)) == 0
+    assert why.value is None
+    assert lib.dls_step_kernel_in_use(None, None) == 0
+
+
 def _golden_budget_cases():
     rows = []
     for line in open(os.path.join(ROOT, "tests", "golden", "context_budget.txt")):
