@@ -322,6 +322,11 @@ __global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC, W>::threads) kq_gem
     mbar_fence_init();
   }
   __syncthreads();
+  // Programmatic dependent launch: the next kernel may start now (it waits
+  // for this grid's completion before reading its output); the weight
+  // stream below does not depend on the previous kernel, the consumers wait
+  // for it before reading x.
+  griddep_launch();
 
   if (warp == nwc) {
     // ---------------- producer: this CTA's rows through the ring
@@ -350,6 +355,7 @@ __global__ void __launch_bounds__(KqBounds<FMT, RS * 0 + MC, W>::threads) kq_gem
     }
   } else {
     // ---------------- consumers
+    griddep_wait();
     const int nunits = nsb * G::UPB;
     KqX<FMT, G::WIDE ? 1 : 0> xq[MC];
     bool valid[MC];
@@ -657,8 +663,17 @@ cudaError_t launch_kq_gemv(int fmt, const KqArgs& a, const KqLaunch& l, cudaStre
     return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(a.w) | reinterpret_cast<uintptr_t>(a.d6) | reinterpret_cast<uintptr_t>(a.x)) & 15)
     return cudaErrorInvalidValue;
-  f<<<l.grid, l.threads, l.smem, s>>>(a, l);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(l.grid);
+  cfg.blockDim = dim3(l.threads);
+  cfg.dynamicSmemBytes = l.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see the kernel's griddep calls
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, f, a, l);
 }
 
 }  // namespace dls

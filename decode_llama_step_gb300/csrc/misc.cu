@@ -393,9 +393,15 @@ cudaError_t launch_unarrived_wait(unsigned long long limit_ns, int32_t* status, 
 }
 
 // ---- single-vector helpers (the mixed-format decode path) ------------------------
+//
+// Launched with programmatic dependent launch: each waits for the previous
+// kernel's results before it reads or writes anything, then lets the next
+// kernel (a GEMV that streams its weights meanwhile) start.
 
 // out = x / sqrt(mean(x^2) + eps) * g, one CTA, fixed-order reduction
 __global__ void rmsnorm_vec_kernel(const float* x, int H, const float* g, float eps, float* out) {
+  griddep_wait();
+  griddep_launch();
   __shared__ float red[32];
   float ss = 0.f;
   for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
@@ -409,27 +415,32 @@ __global__ void rmsnorm_vec_kernel(const float* x, int H, const float* g, float 
 }
 
 __global__ void add_vec_kernel(float* x, const float* y, int n) {
+  griddep_wait();
+  griddep_launch();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) x[i] += y[i];
 }
 
 __global__ void swiglu_vec_kernel(const float* gate, const float* up, float* h, int n) {
+  griddep_wait();
+  griddep_launch();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
     h[i] = silu(gate[i]) * up[i];
 }
 
 cudaError_t launch_rmsnorm_vec(const float* x, int H, const float* g, float eps, float* out, cudaStream_t s) {
-  rmsnorm_vec_kernel<<<1, 1024, 0, s>>>(x, H, g, eps, out);
-  return cudaGetLastError();
+  void* args[] = {(void*)&x, &H, (void*)&g, &eps, &out};
+  return launch_ex((const void*)rmsnorm_vec_kernel, dim3(1), dim3(1024), s, true, args);
 }
 
 cudaError_t launch_add_vec(float* x, const float* y, int n, cudaStream_t s) {
-  add_vec_kernel<<<std::min((n + 255) / 256, 1024), 256, 0, s>>>(x, y, n);
-  return cudaGetLastError();
+  void* args[] = {&x, (void*)&y, &n};
+  return launch_ex((const void*)add_vec_kernel, dim3(std::min((n + 255) / 256, 1024)), dim3(256), s, true, args);
 }
 
 cudaError_t launch_swiglu_vec(const float* gate, const float* up, float* h, int n, cudaStream_t s) {
-  swiglu_vec_kernel<<<std::min((n + 255) / 256, 1024), 256, 0, s>>>(gate, up, h, n);
-  return cudaGetLastError();
+  void* args[] = {(void*)&gate, (void*)&up, &h, &n};
+  return launch_ex((const void*)swiglu_vec_kernel, dim3(std::min((n + 255) / 256, 1024)), dim3(256), s, true,
+                   args);
 }
 
 // Host -> device copy driven by the SMs: every thread reads 16-byte words of
